@@ -1,0 +1,174 @@
+"""Pins for oracle.decode: the §3 identities, support recovery, hand case."""
+
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+from oracle import decode as dec
+from oracle import entmax as em
+from oracle import pages as pg
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _case(rng, n_tok=200, d=16, g=2, needles=3):
+    K = rng.normal(size=(n_tok, d))
+    V = rng.normal(size=(n_tok, d))
+    Q = rng.normal(size=(g, d))
+    pos = rng.choice(n_tok, size=needles, replace=False)
+    for i, p in enumerate(pos):
+        u = Q[i % g]
+        K[p] = 3.0 * u / np.linalg.norm(u) * math.sqrt(d) + 0.3 * rng.normal(size=d)
+    return K, V, Q
+
+
+def test_hand_decode_case():
+    c = json.load(open(os.path.join(GOLD, "decode_hand_case.json")))
+    K, V, Q = np.array(c["k"]), np.array(c["v"]), np.array(c["q"])
+    for policy, budget in (("full", 0), ("topk", c["topk_budget_tokens"])):
+        r = dec.decode_group(K, V, Q, c["alpha"], policy, c["page_size"], budget)
+        np.testing.assert_allclose(r["out"][0], [eval(x) for x in c["out"]], atol=1e-15)
+        assert abs(r["tau"][0] - eval(c["tau"])) < 1e-15
+        assert r["delta_exact"][0] == 0.0
+    assert list(r["page_ids"]) == c["topk_page_ids"]
+    assert r["delta"][0] == 0.0  # certified bound: page 1's bound lies below τ̃
+
+
+@pytest.mark.parametrize("alpha", [1.5, 2.0])
+def test_l1_gap_is_twice_dropped_mass_and_2B_delta_bound(alpha):
+    rng = np.random.default_rng(20)
+    beta = 1.0 / (alpha - 1.0)
+    for trial in range(10):
+        K, V, Q = _case(rng)
+        s = K @ Q[0] / math.sqrt(K.shape[1])
+        p_full, _ = em.entmax(s, alpha)
+        keep = rng.random(K.shape[0]) < 0.5
+        keep[np.argmax(s)] = True
+        p_k, _ = em.entmax(s[keep], alpha)
+        pt = np.zeros_like(p_full)
+        pt[keep] = p_k
+        delta = p_full[~keep].sum()
+        assert abs(np.abs(p_full - pt).sum() - 2.0 * delta) < 1e-12
+        o, ot = p_full @ V, pt @ V
+        B = np.linalg.norm(V, axis=1).max()
+        assert np.linalg.norm(o - ot) <= 2.0 * B * delta + 1e-12
+
+
+@pytest.mark.parametrize("alpha", [1.5, 2.0])
+def test_support_recovery_is_exact(alpha):
+    rng = np.random.default_rng(21)
+    P = 8
+    for _ in range(10):
+        K, V, Q = _case(rng, n_tok=203, needles=4)
+        full = dec.decode_group(K, V, Q, alpha, "full", P)
+        s = K @ Q.T / math.sqrt(K.shape[1])
+        supp_pages = set()
+        for h in range(Q.shape[0]):
+            p, _ = em.entmax(s[:, h], alpha)
+            supp_pages |= set(np.nonzero(p > 0)[0] // P)
+        n_pages = -(-K.shape[0] // P)
+        extra = set(rng.choice(n_pages, size=3, replace=False))
+        keep_pages = supp_pages | extra
+        # top-k with a budget covering exactly those pages is not guaranteed to
+        # pick them, so call the kept-set attention directly.
+        keep = np.zeros(K.shape[0], bool)
+        for p in keep_pages:
+            keep[p * P:(p + 1) * P] = True
+        for h in range(Q.shape[0]):
+            p_k, tau_k = em.entmax(s[keep, h], alpha)
+            np.testing.assert_allclose(p_k @ V[keep], full["out"][h], atol=1e-12)
+            assert abs(tau_k - full["tau"][h]) < 1e-12
+
+
+def test_softmax_always_drops_mass():
+    rng = np.random.default_rng(22)
+    K, V, Q = _case(rng)
+    s = K @ Q[0] / math.sqrt(K.shape[1])
+    p, _ = em.softmax(s)
+    for drop in (1, 5, 100):
+        idx = rng.choice(s.size, size=drop, replace=False)
+        assert p[idx].sum() > 0.0
+    # entmax with the same kept set can drop nothing
+    pe, _ = em.entmax(s, 1.5)
+    zero = np.nonzero(pe == 0)[0]
+    assert zero.size > 0 and pe[zero].sum() == 0.0
+
+
+@pytest.mark.parametrize("alpha", [1.5, 2.0])
+def test_topk_certified_delta_bounds_exact(alpha):
+    rng = np.random.default_rng(23)
+    for _ in range(8):
+        K, V, Q = _case(rng, n_tok=256, needles=5, g=4)
+        for budget in (16, 64, 128):
+            r = dec.decode_group(K, V, Q, alpha, "topk", 16, budget)
+            assert np.all(r["delta"] >= r["delta_exact"] - 1e-12)
+            assert np.all(r["delta"] <= 1.0)
+            full = dec.decode_group(K, V, Q, alpha, "full", 16)
+            for h in range(Q.shape[0]):
+                if r["delta"][h] == 0.0:
+                    np.testing.assert_allclose(r["out"][h], full["out"][h], atol=1e-12)
+                B = np.linalg.norm(V, axis=1).max()
+                err = np.linalg.norm(r["out"][h] - full["out"][h])
+                assert err <= 2 * B * r["delta_exact"][h] + 1e-12
+
+
+@pytest.mark.parametrize("alpha", [1.5, 2.0])
+def test_gaussian_policy_consistency(alpha):
+    rng = np.random.default_rng(24)
+    K, V, Q = _case(rng, n_tok=512, d=32, g=4, needles=6)
+    beta = 1.0 / (alpha - 1.0)
+    a1 = alpha - 1.0
+    r0 = None
+    for margin in (0.0, 0.5, 1.0):
+        r = dec.decode_group(K, V, Q, alpha, "gaussian", 16, 0, margin)
+        meta = r["meta"]
+        for h in range(4):
+            F = pg.normaliser(r["tauhat"][h], a1 * r["mu"][h], a1 * r["sigma"][h], meta["n"], beta)
+            assert abs(F - 1.0) < 1e-10
+            kept = pg.normaliser(r["tauhat"][h], a1 * r["mu"][h, r["page_ids"]],
+                                 a1 * r["sigma"][h, r["page_ids"]], meta["n"][r["page_ids"]], beta)
+            assert abs(kept + r["delta"][h] - 1.0) < 1e-10
+        if r0 is not None:
+            assert set(r0) <= set(r["page_ids"])
+        r0 = r["page_ids"]
+    # uncapped Gaussian at a huge margin keeps every page and is exact
+    r = dec.decode_group(K, V, Q, alpha, "gaussian", 16, 0, 1e6)
+    full = dec.decode_group(K, V, Q, alpha, "full", 16)
+    np.testing.assert_allclose(r["out"], full["out"], atol=1e-12)
+    assert np.all(r["delta_exact"] == 0.0)
+
+
+def test_recall_and_empty():
+    rng = np.random.default_rng(25)
+    K, V, Q = _case(rng, n_tok=64)
+    r = dec.decode_group(K, V, Q, 1.5, "full", 16)
+    assert np.all(r["recall"] == 1.0)
+    e = dec.decode_group(K[:0], V[:0], Q, 1.5, "full", 16)
+    assert np.all(e["out"] == 0.0) and e["page_ids"].size == 0
+
+
+@pytest.mark.parametrize("alpha", [1.5, 2.0])
+def test_gaussian_selector_exact_on_constant_pages(alpha):
+    # Pages whose tokens are all equal have σ_p = 0, so the page model is the
+    # exact score distribution and τ̂ is the full-cache τ. At Δ = 0 the selector
+    # must then keep exactly the pages holding support, and decode exactly.
+    rng = np.random.default_rng(26)
+    P, n_pages, d = 8, 40, 16
+    base = rng.normal(size=(n_pages, d)) * 2.0
+    K = np.repeat(base, P, axis=0)
+    V = rng.normal(size=(n_pages * P, d))
+    Q = rng.normal(size=(2, d))
+    r = dec.decode_group(K, V, Q, alpha, "gaussian", P, 0, 0.0)
+    full = dec.decode_group(K, V, Q, alpha, "full", P)
+    s = K @ Q.T / math.sqrt(d)
+    supp = set()
+    for h in range(2):
+        assert abs(r["tauhat"][h] - full["tau"][h]) < 1e-10
+        p, _ = em.entmax(s[:, h], alpha)
+        supp |= set(np.nonzero(p > 0)[0] // P)
+    assert set(r["page_ids"]) == supp
+    np.testing.assert_allclose(r["out"], full["out"], atol=1e-12)
+    np.testing.assert_allclose(r["delta"], 0.0, atol=1e-12)

@@ -1,0 +1,175 @@
+"""Pins for oracle.pages: metadata, bounds, Gaussian model, τ̂ and selection."""
+
+import json
+import math
+import os
+
+import numpy as np
+
+from oracle import entmax as em
+from oracle import pages as pg
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def test_metadata_twopass_welford_chan_agree():
+    rng = np.random.default_rng(10)
+    keys = rng.normal(size=(77, 9)) * 3.0 + 1.5
+    P = 16
+    meta = pg.page_metadata(keys, P)
+    assert list(meta["n"]) == [16, 16, 16, 16, 13]
+    for p in range(5):
+        blk = keys[p * P: (p + 1) * P]
+        # token-by-token (append of one token at a time)
+        n, mean, m2 = 0, np.zeros(9), np.zeros(9)
+        for x in blk:
+            n, mean, m2 = pg.welford_append(n, mean, m2, x)
+        np.testing.assert_allclose(mean, meta["mean"][p], rtol=1e-13, atol=1e-13)
+        np.testing.assert_allclose(m2 / n, meta["var"][p], rtol=1e-12, atol=1e-13)
+        # two halves merged (append of a block to a partly filled page)
+        h = len(blk) // 3
+        a, b = blk[:h], blk[h:]
+        ma, mb = a.mean(0), b.mean(0)
+        n2, mean2, m22 = pg.chan_merge(len(a), ma, ((a - ma) ** 2).sum(0),
+                                       len(b), mb, ((b - mb) ** 2).sum(0))
+        np.testing.assert_allclose(mean2, meta["mean"][p], rtol=1e-13, atol=1e-13)
+        np.testing.assert_allclose(m22 / n2, meta["var"][p], rtol=1e-12, atol=1e-13)
+        # bounding box: every key inside, and each face attained by some key
+        assert np.all(blk >= meta["kmin"][p]) and np.all(blk <= meta["kmax"][p])
+        assert np.all((blk == meta["kmin"][p]).any(0)) and np.all((blk == meta["kmax"][p]).any(0))
+
+
+def test_bbox_is_an_upper_bound_and_tight():
+    rng = np.random.default_rng(11)
+    d, P = 16, 8
+    keys = rng.normal(size=(8 * P + 3, d))
+    meta = pg.page_metadata(keys, P)
+    for _ in range(20):
+        q = rng.normal(size=d)
+        U = pg.bbox_bound(q, meta["kmin"], meta["kmax"])
+        s = keys @ q / math.sqrt(d)
+        for p in range(U.size):
+            assert U[p] >= s[p * P:(p + 1) * P].max() - 1e-12
+        # equivalent split form: positive part of q meets kmax, negative kmin
+        U2 = (meta["kmax"] @ np.maximum(q, 0) + meta["kmin"] @ np.minimum(q, 0)) / math.sqrt(d)
+        np.testing.assert_allclose(U, U2, atol=1e-12)
+    # tight for one-token pages and for pages of identical tokens
+    one = pg.page_metadata(keys[:5], 1)
+    q = rng.normal(size=d)
+    np.testing.assert_allclose(pg.bbox_bound(q, one["kmin"], one["kmax"]),
+                               keys[:5] @ q / math.sqrt(d), atol=1e-12)
+    same = pg.page_metadata(np.repeat(keys[:1], 4, axis=0), 4)
+    np.testing.assert_allclose(pg.bbox_bound(q, same["kmin"], same["kmax"]),
+                               keys[:1] @ q / math.sqrt(d), atol=1e-12)
+
+
+def test_hand_decode_case_bbox_and_topk():
+    c = json.load(open(os.path.join(GOLD, "decode_hand_case.json")))
+    meta = pg.page_metadata(np.array(c["k"]), c["page_size"])
+    U = pg.bbox_bound(np.array(c["q"][0]), meta["kmin"], meta["kmax"])
+    assert abs(U[0] - eval(c["bbox_U_page0"])) < 1e-15
+    assert abs(U[1] - eval(c["bbox_U_page1"])) < 1e-15
+    k = c["topk_budget_tokens"] // c["page_size"]
+    assert list(pg.select_topk(U, k)) == c["topk_page_ids"]
+
+
+def test_topk_matches_stable_sort_with_ties():
+    rng = np.random.default_rng(12)
+    for n in (1, 5, 64, 300):
+        u = np.round(rng.normal(size=n), 1)  # many exact ties
+        for k in (1, 3, n // 2 + 1, n, n + 5):
+            got = pg.select_topk(u, k)
+            order = np.lexsort((np.arange(n), -u))  # by -u, then index
+            want = np.sort(order[:k])
+            assert list(got) == list(want)
+
+
+def _hadamard(n):
+    H = np.array([[1.0]])
+    while H.shape[0] < n:
+        H = np.block([[H, H], [H, -H]])
+    return H
+
+
+def test_gauss_model_is_exact_for_uncorrelated_page():
+    # Columns 1..d of a Hadamard matrix are centred and mutually orthogonal,
+    # so the page's empirical covariance is diagonal; then the model's μ_p and
+    # σ_p² equal the empirical mean and variance of the page's token scores.
+    d, n = 12, 32
+    H = _hadamard(n)[:, 1:d + 1]
+    rng = np.random.default_rng(13)
+    scale = rng.uniform(0.5, 2.0, size=d)
+    keys = rng.normal(size=d) + H * scale
+    meta = pg.page_metadata(keys, n)
+    q = rng.normal(size=d)
+    mu, sig = pg.gauss_page_scores(q, meta["mean"], meta["var"])
+    s = keys @ q / math.sqrt(d)
+    assert abs(mu[0] - s.mean()) < 1e-12
+    assert abs(sig[0] ** 2 - s.var()) < 1e-12
+
+
+def test_partial_moments_match_quadrature():
+    rng = np.random.default_rng(14)
+    for beta in (1.0, 2.0):
+        for _ in range(25):
+            a = rng.normal() * 3.0
+            if a + 12 * 3.0 <= 0.0:
+                continue
+            sg = rng.uniform(0.05, 3.0)
+            # the integrand vanishes below 0 and is smooth above it, so integrate
+            # from the kink at 0 (or a − 12σ if that is larger)
+            x = np.linspace(max(0.0, a - 12 * sg), a + 12 * sg, 100001)
+            dens = np.exp(-0.5 * ((x - a) / sg) ** 2) / (sg * math.sqrt(2 * math.pi))
+            f = np.clip(x, 0, None) ** beta * dens
+            h = x[1] - x[0]  # composite Simpson on an even number of intervals
+            quad = float(h / 3.0 * (f[0] + f[-1] + 4.0 * f[1:-1:2].sum() + 2.0 * f[2:-1:2].sum()))
+            got = float(pg.partial_moment(a, sg, beta))
+            assert abs(got - quad) < 1e-9 * max(1.0, abs(quad)), (beta, a, sg, got, quad)
+        # σ = 0 reduces to the plain power of the positive part
+        assert float(pg.partial_moment(0.7, 0.0, beta)) == 0.7 ** beta
+        assert float(pg.partial_moment(-0.7, 0.0, beta)) == 0.0
+
+
+def test_tauhat_degenerate_equals_exact_entmax_of_means():
+    # With σ_p = 0 every page is a point mass, so F(τ) = Σ_p n_p (m_p − τ)_+^β
+    # is the exact entmax normaliser of the page means repeated n_p times.
+    rng = np.random.default_rng(15)
+    for alpha in (1.5, 2.0):
+        m = rng.normal(size=40)
+        n = rng.integers(1, 33, size=40)
+        th = pg.tauhat(m, np.zeros(40), n, alpha)
+        ref = em.threshold(np.repeat(m, n), alpha)
+        assert abs(th - ref) < 1e-10
+
+
+def test_tauhat_solves_normaliser_and_F_decreasing():
+    rng = np.random.default_rng(16)
+    for alpha in (1.5, 2.0):
+        beta = 1.0 / (alpha - 1.0)
+        m = rng.normal(size=200) * 0.4
+        sg = rng.uniform(0.1, 0.8, size=200)
+        n = np.full(200, 32)
+        th = pg.tauhat(m, sg, n, alpha)
+        assert abs(pg.normaliser(th, m, sg, n, beta) - 1.0) < 1e-10
+        ts = np.linspace(m.max() - 1.0, th + 2.0, 50)
+        F = [pg.normaliser(t, m, sg, n, beta) for t in ts]
+        assert all(F[i] > F[i + 1] for i in range(len(F) - 1))
+        assert th >= m.max() - 1.0
+
+
+def test_gaussian_selection_monotone_in_margin():
+    rng = np.random.default_rng(17)
+    mh = rng.normal(size=(4, 500))
+    thr = rng.normal(size=4) + 1.0
+    prev = None
+    for delta in (0.0, 0.25, 0.5, 1.0, 2.0):
+        sel = set(pg.select_gaussian(mh, thr - delta))
+        if prev is not None:
+            assert prev <= sel
+        prev = sel
+    # equality selects
+    assert list(pg.select_gaussian(np.array([[1.0, 0.5]]), np.array([0.5]))) == [0, 1]
+
+
+def test_est_max_one_token_page_is_mean():
+    assert pg.est_max(np.array([0.3]), np.array([5.0]), np.array([1]))[0] == 0.3
