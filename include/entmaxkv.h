@@ -1,0 +1,210 @@
+/*
+ * entmaxkv.h -- C ABI of libentmaxkv, the GB300 (sm_103a) EntmaxKV decode step.
+ *
+ * The method is "EntmaxKV: Support-Aware Decoding for Entmax Attention"
+ * (gist.science technical summary; arXiv abstract on the mlsanity.com index
+ * page). A decode step scores the pages of a paged KV cache from per-page key
+ * metadata (summary §2A), selects candidate pages (§2B: top-k by a bounding-
+ * box bound, or a Gaussian estimate τ̂ of the entmax threshold with margin Δ),
+ * and runs exact α-entmax attention over the selected pages only (§2C):
+ *
+ *   s_i = q·k_i/√d,  z_i = (α−1)·s_i,  p_i = [z_i − τ]_+^{1/(α−1)},  Σ p_i = 1,
+ *   o = Σ_i p_i v_i.
+ *
+ * Conventions for every call:
+ *   - Pointers marked (device) point to CUDA device memory the CALLER owns
+ *     and keeps alive until the work queued on `stream` has finished. The
+ *     library allocates nothing and keeps no state between calls.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream). All work is queued asynchronously on it; outputs are valid
+ *     once the stream has been synchronised. No call synchronises.
+ *   - Argument errors are found on the host and returned at once; nothing is
+ *     queued then. Errors found by a kernel (a block-table entry out of
+ *     range, an append past the block table, ...) are OR-ed as
+ *     ENTMAXKV_DEV_* bits into the caller's device status word
+ *     (entmaxkv_cache.status, may be NULL). Nothing prints, traps or throws.
+ *   - No kernel spins: kernels never wait on other kernels or on flags; the
+ *     split-K combines use a "last block to finish combines" counter.
+ */
+#ifndef ENTMAXKV_H
+#define ENTMAXKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ENTMAXKV_VERSION 1
+
+/* Return codes of every call. */
+typedef enum {
+  ENTMAXKV_OK = 0,
+  ENTMAXKV_ERR_INVALID_ARG = 1,       /* a NULL, negative or inconsistent argument   */
+  ENTMAXKV_ERR_UNSUPPORTED = 2,       /* a valid but unimplemented shape/dtype/alpha */
+  ENTMAXKV_ERR_WORKSPACE_TOO_SMALL = 3,
+  ENTMAXKV_ERR_CUDA = 4               /* a CUDA launch or memset failed              */
+} entmaxkv_status;
+
+/* Bits a kernel ORs into the device status word. */
+#define ENTMAXKV_DEV_BAD_PAGE_TABLE  0x1u  /* block-table entry outside [0, num_phys_pages): page skipped   */
+#define ENTMAXKV_DEV_CAPACITY        0x2u  /* append past max_pages_per_seq, or Gaussian cap overflow       */
+#define ENTMAXKV_DEV_TAUHAT_NOCONV   0x4u  /* the τ̂ solve stopped at its iteration limit                    */
+#define ENTMAXKV_DEV_CAND_OVERFLOW   0x8u  /* informational: the exact-τ solve used its slow full-scan path */
+#define ENTMAXKV_DEV_TAU_NOCONV      0x10u /* the exact-τ solve stopped at its iteration limit              */
+#define ENTMAXKV_DEV_BAD_SEQ_ID      0x20u /* a seq_ids entry outside [0, max_seqs): that sequence skipped  */
+
+/* KV storage types. */
+#define ENTMAXKV_F32  0
+#define ENTMAXKV_BF16 1
+
+/* Page-selection policies (summary §2B) and the in-run baselines (§4). */
+#define ENTMAXKV_POLICY_FULL     0  /* every page: full-cache α-entmax                      */
+#define ENTMAXKV_POLICY_TOPK     1  /* the k = budget/page_size pages with the largest bound */
+#define ENTMAXKV_POLICY_GAUSSIAN 2  /* pages whose estimated max clears τ̂ − Δ               */
+#define ENTMAXKV_POLICY_SOFTMAX  3  /* full-cache softmax (FlashDecoding-style baseline)     */
+
+/* Decode flags. */
+#define ENTMAXKV_FLAG_DENSE_V 0x1u  /* read every selected V page even where all p_i = 0
+                                       (the dense full-cache entmax baseline); without it a
+                                       page whose scores all sit at or below τ is skipped,
+                                       which is exact since its weights are 0.            */
+
+/*
+ * Cache geometry. Supported: head_dim ∈ {64, 128}; page_size ∈ {16, 32};
+ * 1 ≤ group ≤ 8 (query heads per KV head; query head h reads KV head h/group).
+ */
+typedef struct {
+  int32_t num_kv_heads;       /* Hkv                                           */
+  int32_t group;              /* g = Hq / Hkv                                  */
+  int32_t head_dim;           /* d                                             */
+  int32_t page_size;          /* P tokens per page                             */
+  int32_t max_seqs;           /* rows of the block table / entries of seq_lens */
+  int32_t max_pages_per_seq;  /* row length of the block table                 */
+  int32_t num_phys_pages;     /* pages in the K/V pools                        */
+  int32_t kv_dtype;           /* ENTMAXKV_F32 or ENTMAXKV_BF16                 */
+} entmaxkv_config;
+
+/*
+ * The paged cache: caller-owned device buffers (summary §2A: the cache is
+ * split into pages; each page keeps k_min/k_max and the mean and variance of
+ * its keys). Layouts, row-major:
+ *   k_pool, v_pool [num_phys_pages][num_kv_heads][page_size][head_dim]  kv_dtype
+ *   kmin, kmax     [num_phys_pages][num_kv_heads][head_dim]             kv_dtype
+ *   mean, m2       [num_phys_pages][num_kv_heads][head_dim]             float32
+ *       (m2 = Σ (k − mean)² over the page's valid tokens; var = m2 / n_p)
+ *   block_table    [max_seqs][max_pages_per_seq] int32: logical page → physical page
+ *   seq_lens       [max_seqs] int32 valid tokens per sequence
+ *   status         one uint32 the kernels OR ENTMAXKV_DEV_* bits into (may be NULL)
+ * Metadata of a page covers its valid tokens only and is written by
+ * entmaxkv_append; a partial last page holds n_p = len − P·(pages−1) tokens.
+ */
+typedef struct {
+  void* k_pool;
+  void* v_pool;
+  void* kmin;
+  void* kmax;
+  float* mean;
+  float* m2;
+  const int32_t* block_table;
+  int32_t* seq_lens;
+  uint32_t* status;
+} entmaxkv_cache;
+
+/* Library version (ENTMAXKV_VERSION). */
+int32_t entmaxkv_version(void);
+
+/* Static text for a return code; never NULL. */
+const char* entmaxkv_status_string(int32_t status);
+
+/*
+ * Append n_tokens tokens to each of n_seqs sequences (summary §2A: the page
+ * metadata the scorers read is maintained as keys are written).
+ *   k, v     (device) [n_seqs][num_kv_heads][n_tokens][head_dim], kv_dtype
+ *   seq_ids  (device) [n_seqs] distinct sequence rows, or NULL for 0..n_seqs−1
+ * For sequence b with old length L, token t goes to logical page (L+t)/P,
+ * slot (L+t)%P, through the block table; the caller must have filled the
+ * block-table entries of every page being written. Each touched page's
+ * kmin/kmax (exact element min/max) and mean/m2 (float32; a partly filled
+ * page is merged with the Chan et al. pairwise update) are updated, then
+ * seq_lens[seq] += n_tokens. A page past max_pages_per_seq or a block-table
+ * entry out of range is skipped and flagged on the device status word.
+ * n_tokens == 0 or n_seqs == 0 queues nothing and returns OK.
+ */
+int32_t entmaxkv_append(const entmaxkv_config* cfg, const entmaxkv_cache* cache,
+                        const void* k, const void* v, const int32_t* seq_ids,
+                        int32_t n_seqs, int32_t n_tokens, void* stream);
+
+/*
+ * Bytes of device workspace entmaxkv_decode needs for n_seqs sequences under
+ * `policy` and `budget_tokens`. Returns 0 for invalid arguments.
+ */
+size_t entmaxkv_workspace_bytes(const entmaxkv_config* cfg, int32_t n_seqs,
+                                int32_t policy, int32_t budget_tokens);
+
+/*
+ * One decode step for n_seqs sequences (summary §2A-§2C; δ from §3).
+ *   q          (device) [n_seqs][Hq][head_dim], kv_dtype (Hq = Hkv·group)
+ *   seq_ids    (device) [n_seqs] sequence rows, or NULL for 0..n_seqs−1
+ *   alpha      α > 1 (GAUSSIAN needs α ∈ {1.5, 2}); ignored by SOFTMAX
+ *   policy     ENTMAXKV_POLICY_*
+ *   budget_tokens  TOPK: k = budget_tokens / page_size pages (must be ≥ 1);
+ *                  GAUSSIAN: a cap in tokens (0 = none; on overflow the pages
+ *                  with the largest margin max_h(M̂_p − threshold_h) are kept,
+ *                  ties to the lower index, and ENTMAXKV_DEV_CAPACITY is set);
+ *                  FULL/SOFTMAX: ignored
+ *   margin     Δ in score units (GAUSSIAN)
+ *   flags      ENTMAXKV_FLAG_*
+ *   workspace  (device) ≥ entmaxkv_workspace_bytes(...) bytes, 256-byte
+ *              aligned; contents need no initialisation and are scratch
+ *              afterwards. One workspace must not be shared by decodes that
+ *              may run concurrently.
+ * Outputs (device; any may be NULL except out):
+ *   out        [n_seqs][Hq][head_dim] float32
+ *   page_ids   [n_seqs][Hkv][page_ids_stride] int32: selected logical page
+ *              ids, ascending (FULL/SOFTMAX: every page)
+ *   n_sel      [n_seqs][Hkv] int32 selected pages
+ *   tau        [n_seqs][Hq] float32: the exact α-entmax threshold over the
+ *              kept tokens on the z scale (SOFTMAX: log Σ exp(s_i)); NaN for
+ *              an empty kept set
+ *   delta      [n_seqs][Hq] float32 dropped mass: FULL/SOFTMAX 0; TOPK the
+ *              certified bound min(1, Σ_dropped n_p·[(α−1)U_p − τ]_+^β);
+ *              GAUSSIAN the page model's estimate of the dropped mass
+ * page_ids_stride must be ≥ the most pages the policy can select
+ * (TOPK: k; GAUSSIAN: the cap in pages, or max_pages_per_seq; otherwise
+ * max_pages_per_seq) when page_ids is not NULL.
+ * An empty sequence yields out = 0, tau = NaN, delta = 0, n_sel = 0.
+ */
+int32_t entmaxkv_decode(const entmaxkv_config* cfg, const entmaxkv_cache* cache,
+                        const void* q, const int32_t* seq_ids, int32_t n_seqs,
+                        float alpha, int32_t policy, int32_t budget_tokens,
+                        float margin, uint32_t flags,
+                        void* workspace, size_t workspace_bytes,
+                        float* out, int32_t* page_ids, int32_t page_ids_stride,
+                        int32_t* n_sel, float* tau, float* delta, void* stream);
+
+/*
+ * Where the decode keeps its intermediate results inside the workspace, so
+ * that tests and tools can read the page scores, τ̂ and the selection of the
+ * last decode. Offsets are in bytes from the workspace base; a region the
+ * policy does not use has offset SIZE_MAX. Layouts:
+ *   bbox_u     float [n_seqs][Hq][max_pages_per_seq]   U_p per query head
+ *   bbox_uhat  float [n_seqs][Hkv][max_pages_per_seq]  max over the group
+ *   gauss_ms   float2 [n_seqs][Hq][max_pages_per_seq]  (m_p, ς_p) = (α−1)(μ_p, σ_p)
+ *   tauhat     float [n_seqs][Hq]                      τ̂ on the z scale
+ *   sel_bitmap uint32 [n_seqs][Hkv][ceil(max_pages_per_seq/32)]
+ */
+typedef struct {
+  size_t bbox_u, bbox_uhat, gauss_ms, tauhat, sel_bitmap;
+  size_t total;
+} entmaxkv_workspace_view;
+
+int32_t entmaxkv_workspace_layout(const entmaxkv_config* cfg, int32_t n_seqs,
+                                  int32_t policy, int32_t budget_tokens,
+                                  entmaxkv_workspace_view* view);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* ENTMAXKV_H */

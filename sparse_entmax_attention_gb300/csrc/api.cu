@@ -1,0 +1,300 @@
+// api.cu -- the extern "C" entry points of libentmaxkv: argument checks,
+// workspace layout and the launch chain of one decode step.
+#include <math.h>
+#include <string.h>
+
+#include "common.cuh"
+
+namespace ekv {
+
+constexpr int kSmCount = 152;                 // GB300: grids are sized for its 152 SMs
+constexpr int kTargetBlocks = 4 * kSmCount;   // decode blocks per launch to aim for
+
+struct Layout {
+  size_t zmax, mmax, cnt_a, cnt_b, cand_cnt, kept_mass, dbar, bitmap, ctrl_end;
+  size_t tauhat, tau_ws, nsel_ws, sel_list, bbox_u, bbox_uhat, gauss_ms, cand, z, pmax, partial;
+  size_t total;
+  int splits, cap_pages, words, kpages, gcap;
+};
+
+static size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+static int check_config(const entmaxkv_config* c) {
+  if (!c) return ENTMAXKV_ERR_INVALID_ARG;
+  if (c->num_kv_heads < 1 || c->group < 1 || c->max_seqs < 1 || c->max_pages_per_seq < 1 ||
+      c->num_phys_pages < 1 || c->num_kv_heads > 65535)
+    return ENTMAXKV_ERR_INVALID_ARG;
+  if (c->kv_dtype != ENTMAXKV_F32 && c->kv_dtype != ENTMAXKV_BF16) return ENTMAXKV_ERR_INVALID_ARG;
+  if (c->group > 8) return ENTMAXKV_ERR_UNSUPPORTED;
+  if (c->head_dim != 64 && c->head_dim != 128) return ENTMAXKV_ERR_UNSUPPORTED;
+  if (c->page_size != 16 && c->page_size != 32) return ENTMAXKV_ERR_UNSUPPORTED;
+  if ((long long)c->max_pages_per_seq * c->page_size > 0x7fffffffLL) return ENTMAXKV_ERR_UNSUPPORTED;
+  return ENTMAXKV_OK;
+}
+
+static int check_cache(const entmaxkv_cache* k) {
+  if (!k || !k->k_pool || !k->v_pool || !k->kmin || !k->kmax || !k->mean || !k->m2 ||
+      !k->block_table || !k->seq_lens)
+    return ENTMAXKV_ERR_INVALID_ARG;
+  return ENTMAXKV_OK;
+}
+
+static int compute_layout(const entmaxkv_config* c, int S, int policy, int budget, Layout& L) {
+  int st = check_config(c);
+  if (st) return st;
+  if (S < 1 || S > 65535) return ENTMAXKV_ERR_INVALID_ARG;
+  if (policy < ENTMAXKV_POLICY_FULL || policy > ENTMAXKV_POLICY_SOFTMAX) return ENTMAXKV_ERR_INVALID_ARG;
+  const int Hkv = c->num_kv_heads, G = c->group, Hq = Hkv * G, D = c->head_dim, P = c->page_size;
+  const int maxp = c->max_pages_per_seq;
+  memset(&L, 0, sizeof(L));
+  L.words = (maxp + 31) / 32;
+  L.kpages = 0;
+  L.gcap = 0;
+  int cap = maxp;
+  if (policy == ENTMAXKV_POLICY_TOPK) {
+    if (budget < P) return ENTMAXKV_ERR_INVALID_ARG;
+    L.kpages = budget / P;
+    cap = L.kpages < maxp ? L.kpages : maxp;
+  } else if (policy == ENTMAXKV_POLICY_GAUSSIAN) {
+    if (budget < 0) return ENTMAXKV_ERR_INVALID_ARG;
+    if (budget > 0) {
+      L.gcap = budget / P;
+      if (L.gcap < 1) return ENTMAXKV_ERR_INVALID_ARG;
+      cap = L.gcap < maxp ? L.gcap : maxp;
+    }
+  }
+  L.cap_pages = cap;
+  const long long units = (long long)S * Hkv;
+  long long splits = (cap + 7) / 8;
+  long long tgt = (kTargetBlocks + units - 1) / units;
+  if (splits > tgt) splits = tgt;
+  const bool bitmap = policy == ENTMAXKV_POLICY_TOPK || policy == ENTMAXKV_POLICY_GAUSSIAN;
+  const long long need = (cap + kListCap - 1) / kListCap;
+  if (bitmap && splits < need) splits = need;
+  if (splits < 1) splits = 1;
+  if (splits > 65535) return ENTMAXKV_ERR_UNSUPPORTED;
+  L.splits = (int)splits;
+  const bool entmax = policy != ENTMAXKV_POLICY_SOFTMAX;
+  const size_t nq = (size_t)S * Hq, nk = (size_t)S * Hkv;
+  size_t off = 0;
+  auto take = [&](size_t bytes) { size_t o = off; off = up256(off + bytes); return o; };
+  const size_t none = (size_t)-1;
+  L.zmax = take(nq * 4);
+  L.mmax = take(nq * 4);
+  L.cnt_a = take(nk * 4);
+  L.cnt_b = take(nk * 4);
+  L.cand_cnt = take(nq * 4);
+  L.kept_mass = take(nq * 4);
+  L.dbar = take(nq * 4);
+  L.bitmap = bitmap ? take(nk * L.words * 4) : none;
+  L.ctrl_end = off;
+  L.tauhat = policy == ENTMAXKV_POLICY_GAUSSIAN ? take(nq * 4) : none;
+  L.tau_ws = take(nq * 4);
+  L.nsel_ws = take(nk * 4);
+  L.sel_list = bitmap ? take(nk * (size_t)cap * 4) : none;
+  L.bbox_u = policy == ENTMAXKV_POLICY_TOPK ? take(nq * (size_t)maxp * 4) : none;
+  L.bbox_uhat = policy == ENTMAXKV_POLICY_TOPK ? take(nk * (size_t)maxp * 4) : none;
+  L.gauss_ms = policy == ENTMAXKV_POLICY_GAUSSIAN ? take(nq * (size_t)maxp * 8) : none;
+  L.cand = entmax ? take(nq * (size_t)kCandCap * 4) : none;
+  L.z = entmax ? take(nk * (size_t)cap * P * G * 4) : none;
+  L.pmax = entmax ? take(nk * (size_t)cap * G * 4) : none;
+  L.partial = take(nk * (size_t)L.splits * G * (D + 2) * 4);
+  L.total = off;
+  return ENTMAXKV_OK;
+}
+
+template <typename T>
+static T* at(void* base, size_t off) {
+  return off == (size_t)-1 ? nullptr : reinterpret_cast<T*>(static_cast<char*>(base) + off);
+}
+
+}  // namespace ekv
+
+using namespace ekv;
+
+extern "C" {
+
+int32_t entmaxkv_version(void) { return ENTMAXKV_VERSION; }
+
+const char* entmaxkv_status_string(int32_t s) {
+  switch (s) {
+    case ENTMAXKV_OK: return "ok";
+    case ENTMAXKV_ERR_INVALID_ARG: return "invalid argument";
+    case ENTMAXKV_ERR_UNSUPPORTED: return "unsupported shape, dtype or alpha";
+    case ENTMAXKV_ERR_WORKSPACE_TOO_SMALL: return "workspace too small or misaligned";
+    case ENTMAXKV_ERR_CUDA: return "CUDA launch failed";
+    default: return "unknown status";
+  }
+}
+
+size_t entmaxkv_workspace_bytes(const entmaxkv_config* cfg, int32_t n_seqs, int32_t policy,
+                                int32_t budget_tokens) {
+  Layout L;
+  if (compute_layout(cfg, n_seqs, policy, budget_tokens, L) != ENTMAXKV_OK) return 0;
+  return L.total;
+}
+
+int32_t entmaxkv_workspace_layout(const entmaxkv_config* cfg, int32_t n_seqs, int32_t policy,
+                                  int32_t budget_tokens, entmaxkv_workspace_view* view) {
+  if (!view) return ENTMAXKV_ERR_INVALID_ARG;
+  Layout L;
+  const int st = compute_layout(cfg, n_seqs, policy, budget_tokens, L);
+  if (st) return st;
+  view->bbox_u = L.bbox_u;
+  view->bbox_uhat = L.bbox_uhat;
+  view->gauss_ms = L.gauss_ms;
+  view->tauhat = L.tauhat;
+  view->sel_bitmap = L.bitmap;
+  view->total = L.total;
+  return ENTMAXKV_OK;
+}
+
+int32_t entmaxkv_append(const entmaxkv_config* cfg, const entmaxkv_cache* cache, const void* k,
+                        const void* v, const int32_t* seq_ids, int32_t n_seqs, int32_t n_tokens,
+                        void* stream) {
+  int st = check_config(cfg);
+  if (st) return st;
+  if ((st = check_cache(cache))) return st;
+  if (n_seqs < 0 || n_tokens < 0 || n_seqs > 65535) return ENTMAXKV_ERR_INVALID_ARG;
+  if (n_seqs == 0 || n_tokens == 0) return ENTMAXKV_OK;
+  if (!k || !v) return ENTMAXKV_ERR_INVALID_ARG;
+  if ((long long)n_tokens > (long long)cfg->max_pages_per_seq * cfg->page_size)
+    return ENTMAXKV_ERR_INVALID_ARG;
+  AppendArgs a;
+  a.Hkv = cfg->num_kv_heads;
+  a.D = cfg->head_dim;
+  a.P = cfg->page_size;
+  a.maxp = cfg->max_pages_per_seq;
+  a.nphys = cfg->num_phys_pages;
+  a.max_seqs = cfg->max_seqs;
+  a.n_seqs = n_seqs;
+  a.n_tokens = n_tokens;
+  a.k = k;
+  a.v = v;
+  a.seq_ids = seq_ids;
+  a.k_pool = cache->k_pool;
+  a.v_pool = cache->v_pool;
+  a.kmin = cache->kmin;
+  a.kmax = cache->kmax;
+  a.mean = cache->mean;
+  a.m2 = cache->m2;
+  a.block_table = cache->block_table;
+  a.seq_lens = cache->seq_lens;
+  a.status = cache->status;
+  return launch_append(a, cfg->kv_dtype, (cudaStream_t)stream) == cudaSuccess ? ENTMAXKV_OK
+                                                                             : ENTMAXKV_ERR_CUDA;
+}
+
+int32_t entmaxkv_decode(const entmaxkv_config* cfg, const entmaxkv_cache* cache, const void* q,
+                        const int32_t* seq_ids, int32_t n_seqs, float alpha, int32_t policy,
+                        int32_t budget_tokens, float margin, uint32_t flags, void* workspace,
+                        size_t workspace_bytes, float* out, int32_t* page_ids,
+                        int32_t page_ids_stride, int32_t* n_sel, float* tau, float* delta,
+                        void* stream) {
+  int st = check_config(cfg);
+  if (st) return st;
+  if ((st = check_cache(cache))) return st;
+  if (n_seqs < 0) return ENTMAXKV_ERR_INVALID_ARG;
+  if (n_seqs == 0) return ENTMAXKV_OK;
+  if (!q || !out) return ENTMAXKV_ERR_INVALID_ARG;
+  if (policy != ENTMAXKV_POLICY_SOFTMAX && !(alpha > 1.0f && isfinite(alpha)))
+    return ENTMAXKV_ERR_INVALID_ARG;
+  if (policy == ENTMAXKV_POLICY_GAUSSIAN) {
+    if (!isfinite(margin)) return ENTMAXKV_ERR_INVALID_ARG;
+    if (alpha != 1.5f && alpha != 2.0f) return ENTMAXKV_ERR_UNSUPPORTED;
+  }
+  Layout L;
+  if ((st = compute_layout(cfg, n_seqs, policy, budget_tokens, L))) return st;
+  if (!workspace || ((uintptr_t)workspace & 255u) || workspace_bytes < L.total)
+    return ENTMAXKV_ERR_WORKSPACE_TOO_SMALL;
+  if (page_ids && page_ids_stride < L.cap_pages) return ENTMAXKV_ERR_INVALID_ARG;
+
+  DecodeArgs a;
+  memset(&a, 0, sizeof(a));
+  a.Hkv = cfg->num_kv_heads;
+  a.G = cfg->group;
+  a.Hq = a.Hkv * a.G;
+  a.D = cfg->head_dim;
+  a.P = cfg->page_size;
+  a.maxp = cfg->max_pages_per_seq;
+  a.nphys = cfg->num_phys_pages;
+  a.max_seqs = cfg->max_seqs;
+  a.S = n_seqs;
+  a.words = L.words;
+  a.policy = policy;
+  a.splits = L.splits;
+  a.cap_pages = L.cap_pages;
+  a.kpages = L.kpages;
+  a.gcap = L.gcap;
+  a.flags = flags;
+  const float al = policy == ENTMAXKV_POLICY_SOFTMAX ? 2.0f : alpha;
+  a.alpha = al;
+  a.a1 = al - 1.0f;
+  a.beta = (float)(1.0 / ((double)al - 1.0));
+  a.inv_sqrt_d = (float)(1.0 / sqrt((double)a.D));
+  a.zscale = (float)(((double)al - 1.0) / sqrt((double)a.D));
+  a.margin_z = (float)(((double)al - 1.0) * (double)margin);
+  a.k_pool = cache->k_pool;
+  a.v_pool = cache->v_pool;
+  a.kmin = cache->kmin;
+  a.kmax = cache->kmax;
+  a.mean = cache->mean;
+  a.m2 = cache->m2;
+  a.block_table = cache->block_table;
+  a.seq_lens = cache->seq_lens;
+  a.status = cache->status;
+  a.q = q;
+  a.seq_ids = seq_ids;
+  a.out = out;
+  a.page_ids = page_ids;
+  a.page_ids_stride = page_ids_stride;
+  a.n_sel_out = n_sel;
+  a.tau_out = tau;
+  a.delta_out = delta;
+  a.zmax = at<uint32_t>(workspace, L.zmax);
+  a.mmax = at<uint32_t>(workspace, L.mmax);
+  a.cnt_a = at<int32_t>(workspace, L.cnt_a);
+  a.cnt_b = at<int32_t>(workspace, L.cnt_b);
+  a.cand_cnt = at<int32_t>(workspace, L.cand_cnt);
+  a.kept_mass = at<float>(workspace, L.kept_mass);
+  a.dbar = at<float>(workspace, L.dbar);
+  a.bitmap = at<uint32_t>(workspace, L.bitmap);
+  a.tauhat = at<float>(workspace, L.tauhat);
+  a.tau_ws = at<float>(workspace, L.tau_ws);
+  a.nsel_ws = at<int32_t>(workspace, L.nsel_ws);
+  a.sel_list = at<int32_t>(workspace, L.sel_list);
+  a.bbox_u = at<float>(workspace, L.bbox_u);
+  a.bbox_uhat = at<float>(workspace, L.bbox_uhat);
+  a.gauss_ms = at<float2>(workspace, L.gauss_ms);
+  a.cand = at<float>(workspace, L.cand);
+  a.z = at<float>(workspace, L.z);
+  a.pmax = at<float>(workspace, L.pmax);
+  a.partial = at<float>(workspace, L.partial);
+
+  cudaStream_t s = (cudaStream_t)stream;
+  if (cudaMemsetAsync(workspace, 0, L.ctrl_end, s) != cudaSuccess) return ENTMAXKV_ERR_CUDA;
+  cudaError_t e = cudaSuccess;
+  const int dt = cfg->kv_dtype;
+  switch (policy) {
+    case ENTMAXKV_POLICY_FULL:
+      if ((e = launch_pass_a(a, dt, s)) == cudaSuccess) e = launch_pass_b(a, dt, s);
+      break;
+    case ENTMAXKV_POLICY_TOPK:
+      if ((e = launch_bbox(a, dt, kSmCount, s)) == cudaSuccess && (e = launch_topk(a, 0, s)) == cudaSuccess &&
+          (e = launch_pass_a(a, dt, s)) == cudaSuccess)
+        e = launch_pass_b(a, dt, s);
+      break;
+    case ENTMAXKV_POLICY_GAUSSIAN:
+      if ((e = launch_gauss(a, dt, kSmCount, s)) == cudaSuccess && (e = launch_tauhat(a, s)) == cudaSuccess &&
+          (L.gcap == 0 || (e = launch_topk(a, 1, s)) == cudaSuccess) &&
+          (e = launch_pass_a(a, dt, s)) == cudaSuccess)
+        e = launch_pass_b(a, dt, s);
+      break;
+    default:
+      e = launch_softmax(a, dt, s);
+      break;
+  }
+  return e == cudaSuccess ? ENTMAXKV_OK : ENTMAXKV_ERR_CUDA;
+}
+
+}  // extern "C"

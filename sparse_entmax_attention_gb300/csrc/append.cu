@@ -1,0 +1,142 @@
+// append.cu -- write new tokens into their pages and maintain the per-page
+// key metadata the scorers read.
+//
+// EntmaxKV (gist.science technical summary, §2A "Query-Aware Page Scoring"):
+// each page keeps the coordinate-wise minimum and maximum key and the first
+// and second moments (mean and variance) of its keys. Here kmin/kmax are
+// exact element-wise extrema in the KV dtype; mean and m2 (the sum of squared
+// deviations, var = m2/n_p) are float32. A page that already holds tokens is
+// merged with the new ones by the pairwise update of Chan, Golub & LeVeque:
+//   n = na + nb,  δ = mean_b − mean_a,  mean = mean_a + δ·nb/n,
+//   m2 = m2_a + m2_b + δ²·na·nb/n.
+#include "common.cuh"
+
+namespace ekv {
+
+template <typename T, int N>
+struct alignas(N * sizeof(T)) Vec {
+  T v[N];
+};
+
+// One warp per (sequence, KV head, touched page); lane j covers elements
+// [j·D/32, (j+1)·D/32) of every row.
+template <typename T, int D>
+__global__ void __launch_bounds__(128) append_kernel(AppendArgs a) {
+  constexpr int EPL = D / 32;
+  using V = Vec<T, EPL>;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = blockIdx.z, kvh = blockIdx.y;
+  const int i = blockIdx.x * 4 + warp;
+  const int seq = seq_row(a.seq_ids, b, a.max_seqs, lane == 0 ? a.status : nullptr);
+  if (seq < 0) return;
+  int L = a.seq_lens[seq];
+  if (L < 0) L = 0;
+  const int P = a.P, T_new = a.n_tokens;
+  const int first = L / P, last = (L + T_new - 1) / P;
+  const int lp = first + i;
+  if (lp > last) return;
+  if (lp >= a.maxp) {
+    if (lane == 0) raise_flag(a.status, ENTMAXKV_DEV_CAPACITY);
+    return;
+  }
+  const int ph = phys_page(a.block_table, seq, lp, a.maxp, a.nphys, lane == 0 ? a.status : nullptr);
+  if (ph < 0) return;
+  const int tlo = max(L, lp * P), thi = min(L + T_new, (lp + 1) * P);
+  const int n_old = tlo - lp * P, n_new = thi - tlo;
+
+  const size_t src_row0 = (((size_t)b * a.Hkv + kvh) * T_new + (tlo - L)) * D + lane * EPL;
+  const size_t dst_row0 = (((size_t)ph * a.Hkv + kvh) * P + n_old) * D + lane * EPL;
+  const T* ks = (const T*)a.k + src_row0;
+  const T* vs = (const T*)a.v + src_row0;
+  T* kd = (T*)a.k_pool + dst_row0;
+  T* vd = (T*)a.v_pool + dst_row0;
+
+  float mn[EPL], mx[EPL], sum[EPL];
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) {
+    mn[e] = CUDART_INF_F;
+    mx[e] = -CUDART_INF_F;
+    sum[e] = 0.0f;
+  }
+  for (int t = 0; t < n_new; ++t) {
+    V kv = *reinterpret_cast<const V*>(ks + (size_t)t * D);
+    V vv = *reinterpret_cast<const V*>(vs + (size_t)t * D);
+    *reinterpret_cast<V*>(kd + (size_t)t * D) = kv;
+    *reinterpret_cast<V*>(vd + (size_t)t * D) = vv;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+      float x = to_f(kv.v[e]);
+      mn[e] = fminf(mn[e], x);
+      mx[e] = fmaxf(mx[e], x);
+      sum[e] += x;
+    }
+  }
+  float mean[EPL], m2[EPL];
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) {
+    mean[e] = sum[e] / (float)n_new;
+    m2[e] = 0.0f;
+  }
+  for (int t = 0; t < n_new; ++t) {  // second pass over the (cached) new rows
+    V kv = *reinterpret_cast<const V*>(ks + (size_t)t * D);
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+      float dx = to_f(kv.v[e]) - mean[e];
+      m2[e] = fmaf(dx, dx, m2[e]);
+    }
+  }
+  const size_t meta = ((size_t)ph * a.Hkv + kvh) * D + lane * EPL;
+  V* kminp = reinterpret_cast<V*>((T*)a.kmin + meta);
+  V* kmaxp = reinterpret_cast<V*>((T*)a.kmax + meta);
+  float* meanp = a.mean + meta;
+  float* m2p = a.m2 + meta;
+  if (n_old > 0) {
+    V omin = *kminp, omax = *kmaxp;
+    const float na = (float)n_old, nb = (float)n_new, n = na + nb;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+      mn[e] = fminf(mn[e], to_f(omin.v[e]));
+      mx[e] = fmaxf(mx[e], to_f(omax.v[e]));
+      float om = meanp[e], om2 = m2p[e];
+      float dlt = mean[e] - om;
+      mean[e] = om + dlt * (nb / n);
+      m2[e] = om2 + m2[e] + dlt * dlt * (na * nb / n);
+    }
+  }
+  V vmin, vmax;
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) {
+    vmin.v[e] = (T)mn[e];  // exact: each extremum is one of the stored values
+    vmax.v[e] = (T)mx[e];
+    meanp[e] = mean[e];
+    m2p[e] = m2[e];
+  }
+  *kminp = vmin;
+  *kmaxp = vmax;
+}
+
+__global__ void advance_lens_kernel(AppendArgs a) {
+  int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= a.n_seqs) return;
+  int seq = a.seq_ids ? a.seq_ids[b] : b;
+  if (seq < 0 || seq >= a.max_seqs) return;  // flagged by append_kernel
+  a.seq_lens[seq] += a.n_tokens;
+}
+
+template <typename T, int D>
+static cudaError_t launch_append_t(const AppendArgs& a, cudaStream_t st) {
+  const int pages = (a.n_tokens + a.P - 1) / a.P + 1;  // pages one append can touch
+  dim3 grid((pages + 3) / 4, a.Hkv, a.n_seqs);
+  append_kernel<T, D><<<grid, 128, 0, st>>>(a);
+  advance_lens_kernel<<<(a.n_seqs + 127) / 128, 128, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_append(const AppendArgs& a, int kv_dtype, cudaStream_t st) {
+  if (kv_dtype == ENTMAXKV_BF16)
+    return a.D == 128 ? launch_append_t<__nv_bfloat16, 128>(a, st)
+                      : launch_append_t<__nv_bfloat16, 64>(a, st);
+  return a.D == 128 ? launch_append_t<float, 128>(a, st) : launch_append_t<float, 64>(a, st);
+}
+
+}  // namespace ekv

@@ -1,0 +1,252 @@
+// common.cuh -- shared device helpers and the argument blocks of the
+// libentmaxkv kernels (sm_103a). Internal: not part of the C ABI.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math_constants.h>
+#include <stdint.h>
+
+#include "entmaxkv.h"
+
+namespace ekv {
+
+constexpr int kThreads = 256;       // decode / scoring blocks: 8 warps
+constexpr int kWarps = kThreads / 32;
+constexpr int kCandCap = 16384;     // exact-τ candidates kept per query head
+constexpr int kWarpCand = 1024;     // candidates a solver warp keeps in shared memory
+constexpr int kListCap = 1024;      // selected pages one decode block handles
+constexpr int kTauhatCluster = 8;   // blocks per τ̂ cluster (one cluster per query head)
+
+// Everything a decode kernel needs, passed by value (well under 4 KB).
+struct DecodeArgs {
+  // geometry
+  int Hkv, G, Hq, D, P, maxp, nphys, max_seqs, S, words;
+  int policy, splits, cap_pages, kpages, gcap;
+  uint32_t flags;
+  float alpha, a1, beta, zscale, inv_sqrt_d, margin_z;
+  // cache
+  const void* k_pool;
+  const void* v_pool;
+  const void* kmin;
+  const void* kmax;
+  const float* mean;
+  const float* m2;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  uint32_t* status;
+  // inputs
+  const void* q;
+  const int32_t* seq_ids;
+  // outputs
+  float* out;
+  int32_t* page_ids;
+  int page_ids_stride;
+  int32_t* n_sel_out;
+  float* tau_out;
+  float* delta_out;
+  // workspace: zeroed at the start of every decode
+  uint32_t* zmax;      // [S][Hq]   ordered-encoded max z
+  uint32_t* mmax;      // [S][Hq]   ordered-encoded max m (Gaussian)
+  int32_t* cnt_a;      // [S][Hkv]  blocks of pass A done
+  int32_t* cnt_b;      // [S][Hkv]  blocks of pass B done
+  int32_t* cand_cnt;   // [S][Hq]
+  float* kept_mass;    // [S][Hq]   Gaussian model mass of the kept pages
+  float* dbar;         // [S][Hq]   top-k certified dropped mass
+  uint32_t* bitmap;    // [S][Hkv][words]
+  // workspace: written before it is read in every decode
+  float* tauhat;       // [S][Hq]
+  float* tau_ws;       // [S][Hq]
+  int32_t* nsel_ws;    // [S][Hkv]
+  int32_t* sel_list;   // [S][Hkv][cap_pages]
+  float* bbox_u;       // [S][Hq][maxp]
+  float* bbox_uhat;    // [S][Hkv][maxp]
+  float2* gauss_ms;    // [S][Hq][maxp]
+  float* cand;         // [S][Hq][kCandCap]
+  float* z;            // [S][Hkv][cap_pages][P][G]
+  float* pmax;         // [S][Hkv][cap_pages][G]
+  float* partial;      // [S][Hkv][splits][G][D + 2]
+};
+
+struct AppendArgs {
+  int Hkv, D, P, maxp, nphys, max_seqs, n_seqs, n_tokens;
+  const void* k;
+  const void* v;
+  const int32_t* seq_ids;
+  void* k_pool;
+  void* v_pool;
+  void* kmin;
+  void* kmax;
+  float* mean;
+  float* m2;
+  const int32_t* block_table;
+  int32_t* seq_lens;
+  uint32_t* status;
+};
+
+// ---------------------------------------------------------------------------
+// small helpers
+
+__device__ __forceinline__ void raise_flag(uint32_t* st, uint32_t bit) {
+  if (st) atomicOr(st, bit);
+}
+
+// Order-preserving map float -> uint32 (for atomicMax on floats). 0 is below
+// every encoded value and stands for "no value yet" (−inf).
+__device__ __forceinline__ uint32_t ord_enc(float f) {
+  uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float ord_dec(uint32_t o) {
+  if (o == 0u) return -CUDART_INF_F;
+  uint32_t u = (o & 0x80000000u) ? (o & 0x7fffffffu) : ~o;
+  return __uint_as_float(u);
+}
+
+// bf16 pair in one 32-bit word -> floats (exact).
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T>
+__device__ __forceinline__ T warp_sum(T v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ double warp_min_d(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmin(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// D = A·B + D for one m16n8k16 tile, bf16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// 16-byte load of data no kernel writes while it runs (K/V pages, metadata);
+// it is read once, so it skips L1 allocation.
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+  uint4 r;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];\n"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "l"(p));
+  return r;
+}
+
+// Sequence row of decode slot s, validated (−1 and flagged when invalid).
+__device__ __forceinline__ int seq_row(const int32_t* seq_ids, int s, int max_seqs, uint32_t* st) {
+  int seq = seq_ids ? seq_ids[s] : s;
+  if (seq < 0 || seq >= max_seqs) {
+    raise_flag(st, ENTMAXKV_DEV_BAD_SEQ_ID);
+    return -1;
+  }
+  return seq;
+}
+
+// Valid length of a sequence clamped to its block-table row.
+__device__ __forceinline__ int seq_len_clamped(const int32_t* lens, int seq, int maxp, int P,
+                                               uint32_t* st) {
+  if (seq < 0) return 0;
+  int L = lens[seq];
+  long long cap = (long long)maxp * P;
+  if (L < 0) L = 0;
+  if ((long long)L > cap) {
+    raise_flag(st, ENTMAXKV_DEV_CAPACITY);
+    L = (int)cap;
+  }
+  return L;
+}
+
+// Physical page of logical page lp, or −1 (flagged) when out of range.
+__device__ __forceinline__ int phys_page(const int32_t* bt, int seq, int lp, int maxp, int nphys,
+                                         uint32_t* st) {
+  int ph = bt[(size_t)seq * maxp + lp];
+  if (ph < 0 || ph >= nphys) {
+    raise_flag(st, ENTMAXKV_DEV_BAD_PAGE_TABLE);
+    return -1;
+  }
+  return ph;
+}
+
+// [x]_+^β for the β of the decode (β = 2 and 1 exactly, else powf).
+__device__ __forceinline__ float pos_pow(float x, float beta) {
+  x = fmaxf(x, 0.0f);
+  if (beta == 2.0f) return x * x;
+  if (beta == 1.0f) return x;
+  return x > 0.0f ? powf(x, beta) : 0.0f;
+}
+
+// E[(a + σZ)_+^β] and its derivative in a, Z ~ N(0,1), for β ∈ {1, 2}:
+//   β = 1:  a·Φ(t) + σ·φ(t),          d/da = Φ(t)
+//   β = 2:  (a²+σ²)·Φ(t) + a·σ·φ(t),  d/da = 2(a·Φ(t) + σ·φ(t)),   t = a/σ.
+__device__ __forceinline__ void gauss_moment(float a, float sg, bool beta2, float& g, float& dg) {
+  if (!(sg > 0.0f)) {
+    float ap = fmaxf(a, 0.0f);
+    g = beta2 ? ap * ap : ap;
+    dg = beta2 ? 2.0f * ap : (a > 0.0f ? 1.0f : 0.0f);
+    return;
+  }
+  float t = a / sg;
+  float Phi = normcdff(t);
+  float phi = 0.3989422804014327f * expf(-0.5f * t * t);
+  if (beta2) {
+    g = (a * a + sg * sg) * Phi + a * sg * phi;
+    dg = 2.0f * (a * Phi + sg * phi);
+  } else {
+    g = a * Phi + sg * phi;
+    dg = Phi;
+  }
+}
+
+// Block-wide exclusive scan of one int per thread (blockDim multiple of 32).
+// Returns the sum below this thread; `total` receives the block sum.
+__device__ __forceinline__ int block_exclusive_scan(int v, int* sh, int& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) sh[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < nw ? sh[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    if (lane < nw) sh[lane] = w;
+  }
+  __syncthreads();
+  total = sh[nw - 1];
+  const int before = (warp > 0 ? sh[warp - 1] : 0) + x - v;
+  __syncthreads();
+  return before;
+}
+
+// Launchers (one translation unit each).
+cudaError_t launch_append(const AppendArgs& a, int kv_dtype, cudaStream_t st);
+cudaError_t launch_bbox(const DecodeArgs& a, int kv_dtype, int sms, cudaStream_t st);
+cudaError_t launch_gauss(const DecodeArgs& a, int kv_dtype, int sms, cudaStream_t st);
+cudaError_t launch_tauhat(const DecodeArgs& a, cudaStream_t st);
+cudaError_t launch_topk(const DecodeArgs& a, int mode, cudaStream_t st);
+cudaError_t launch_pass_a(const DecodeArgs& a, int kv_dtype, cudaStream_t st);
+cudaError_t launch_pass_b(const DecodeArgs& a, int kv_dtype, cudaStream_t st);
+cudaError_t launch_softmax(const DecodeArgs& a, int kv_dtype, cudaStream_t st);
+
+}  // namespace ekv

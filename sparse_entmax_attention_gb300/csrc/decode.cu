@@ -1,0 +1,576 @@
+// decode.cu -- sparse α-entmax attention over the selected pages (EntmaxKV,
+// gist.science technical summary §2C), the exact threshold, and the
+// full-cache entmax baseline (§4) as the same kernels over every page.
+//
+// For each (sequence, KV head) the selected pages are split evenly over
+// `splits` blocks ("split-K").
+//   pass A  gathers each selected K page (16-byte loads straight into the
+//           MMA fragment registers), scores it for the g query heads of the
+//           group (bf16: m16n8k16 MMA, tokens × heads, fp32 accumulate; fp32:
+//           CUDA-core dot products) on the z = (α−1)·q·k/√d scale, stores
+//           z and each page's max z, and publishes the block's max z. Every
+//           token that can be in the support has z > max z − 1 (τ ≥ z_max − 1),
+//           so each block also emits its tokens above (its best known max − 1)
+//           as candidates. The last block to finish solves the exact τ of each
+//           query head from the candidates (one warp per head).
+//   pass B  gathers V only for pages with some z above τ (all pages for the
+//           dense baseline), accumulates Σ p_i v_i with p_i = [z_i − τ]_+^β in
+//           fp32, writes a per-block partial, and the last block to finish
+//           sums the partials in split order (deterministic).
+// Exact τ: τ solves Σ_i [z_i − τ]_+^β = 1. Starting from τ = z_max − 1
+// (where the sum is ≥ 1) Newton steps on this convex decreasing function stay
+// below the root; after each step the closed-form root on the current support
+// S = {z > τ} is tried (β = 2: Σ_S (z−t)² = 1, β = 1: Σ_S (z−t) = 1) and
+// accepted once it lies in [τ, min_S z], which makes it the exact root.
+#include "common.cuh"
+#include "page_scores.cuh"
+
+namespace ekv {
+
+constexpr int kTauIters = 64;
+
+__device__ __forceinline__ bool uses_bitmap(int policy) {
+  return policy == ENTMAXKV_POLICY_TOPK || policy == ENTMAXKV_POLICY_GAUSSIAN;
+}
+
+// This block's share [lo, hi) of the n_sel selected pages; for bitmap
+// policies the page ids of that share go to list[0 .. hi−lo).
+__device__ void block_page_range(const DecodeArgs& a, int s, int kvh, int n_pages, int split,
+                                 int* list, int* sh_scan, int& n_sel, int& lo, int& hi) {
+  if (!uses_bitmap(a.policy)) {
+    n_sel = n_pages;
+    lo = (int)(((long long)n_sel * split) / a.splits);
+    hi = (int)(((long long)n_sel * (split + 1)) / a.splits);
+    return;
+  }
+  const uint32_t* bm = a.bitmap + ((size_t)s * a.Hkv + kvh) * a.words;
+  const int W = (n_pages + 31) / 32;
+  const int wpt = (W + kThreads - 1) / kThreads;
+  const int w0 = threadIdx.x * wpt;
+  int cnt = 0;
+  for (int j = 0; j < wpt; ++j)
+    if (w0 + j < W) cnt += __popc(bm[w0 + j]);
+  int total;
+  int r = block_exclusive_scan(cnt, sh_scan, total);
+  n_sel = total;
+  lo = (int)(((long long)n_sel * split) / a.splits);
+  hi = (int)(((long long)n_sel * (split + 1)) / a.splits);
+  for (int j = 0; j < wpt; ++j) {
+    if (w0 + j >= W || r >= hi) break;
+    uint32_t bits = bm[w0 + j];
+    while (bits) {
+      const int b = __ffs(bits) - 1;
+      if (r >= lo && r < hi) list[r - lo] = (w0 + j) * 32 + b;
+      ++r;
+      bits &= bits - 1u;
+    }
+  }
+  __syncthreads();
+}
+
+// ---------------------------------------------------------------------------
+// Exact τ of one query head by one warp.
+
+struct TauSource {
+  const float* wc;   // compacted candidates in shared memory (mode 0)
+  int m;
+  const float* cand; // candidate list in global memory (mode 1)
+  int nc;
+  const float* z;    // all scores of the head (mode 2): z[(rank·P + t)·G + hg]
+  int n_sel, P, G, hg;
+  int mode;
+};
+
+__device__ __forceinline__ int tau_src_count(const TauSource& S) {
+  return S.mode == 0 ? S.m : (S.mode == 1 ? S.nc : S.n_sel * S.P);
+}
+__device__ __forceinline__ float tau_src_get(const TauSource& S, int i) {
+  if (S.mode == 0) return S.wc[i];
+  if (S.mode == 1) return __ldcg(S.cand + i);
+  return __ldcg(S.z + (size_t)i * S.G + S.hg);
+}
+
+__device__ double solve_tau_warp(const TauSource& S, double tau0, float beta, bool& ok) {
+  const int lane = threadIdx.x & 31;
+  const int n = tau_src_count(S);
+  double tau = tau0;
+  ok = false;
+  for (int it = 0; it < kTauIters; ++it) {
+    double k = 0.0, s1 = 0.0, s2 = 0.0, sb = 0.0, sb1 = 0.0, mn = CUDART_INF;
+    for (int i = lane; i < n; i += 32) {
+      const double zv = (double)tau_src_get(S, i);
+      if (zv > tau) {
+        const double y = zv - tau;
+        k += 1.0;
+        s1 += y;
+        s2 += y * y;
+        mn = fmin(mn, y);
+        if (beta != 2.0f && beta != 1.0f) {
+          sb += pow(y, (double)beta);
+          sb1 += pow(y, (double)beta - 1.0);
+        }
+      }
+    }
+    k = warp_sum(k);
+    s1 = warp_sum(s1);
+    s2 = warp_sum(s2);
+    sb = warp_sum(sb);
+    sb1 = warp_sum(sb1);
+    mn = warp_min_d(mn);
+    if (k == 0.0) break;  // cannot happen while τ < z_max
+    double next;
+    if (beta == 2.0f) {
+      // root t = τ + δ of Σ_S (y − δ)² = 1 on the branch δ ≤ min y
+      const double disc = s1 * s1 - k * (s2 - 1.0);
+      if (disc >= 0.0) {
+        const double d = (s1 - sqrt(disc)) / k;
+        if (d >= 0.0 && d <= mn) {
+          tau += d;
+          ok = true;
+          break;
+        }
+      }
+      next = tau + (s2 - 1.0) / (2.0 * s1);
+    } else if (beta == 1.0f) {
+      const double d = (s1 - 1.0) / k;
+      if (d >= 0.0 && d <= mn) {
+        tau += d;
+        ok = true;
+        break;
+      }
+      next = tau + d;
+    } else {
+      next = tau + (sb - 1.0) / ((double)beta * sb1);
+      if (fabs(next - tau) <= 1e-13 * fmax(1.0, fabs(tau))) {
+        tau = next;
+        ok = true;
+        break;
+      }
+    }
+    if (!(next > tau)) {  // no progress left in double precision
+      ok = true;
+      break;
+    }
+    tau = next;
+  }
+  return tau;
+}
+
+// ---------------------------------------------------------------------------
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads) pass_a_kernel(DecodeArgs a) {
+  __shared__ int list[kListCap];
+  __shared__ int sh_scan[32];
+  __shared__ float qs[8][D];
+  __shared__ float wmax[kWarps][8];
+  __shared__ float wkept[kWarps][8];
+  __shared__ float thr_sh[8];
+  __shared__ float th_sh[8];
+  __shared__ int last_sh;
+  __shared__ float wcand[kWarps][kWarpCand];
+  const int split = blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = a.G, P = a.P;
+  const int seq = seq_row(a.seq_ids, s, a.max_seqs, tid == 0 ? a.status : nullptr);
+  const int L = seq_len_clamped(a.seq_lens, seq, a.maxp, P, tid == 0 ? a.status : nullptr);
+  const int n_pages = (L + P - 1) / P;
+  int n_sel, lo, hi;
+  block_page_range(a, s, kvh, n_pages, split, list, sh_scan, n_sel, lo, hi);
+  const bool bitmap = uses_bitmap(a.policy);
+  const size_t skv = (size_t)s * a.Hkv + kvh;
+  if (split == 0 && tid == 0) {
+    a.nsel_ws[skv] = n_sel;
+    if (a.n_sel_out) a.n_sel_out[skv] = n_sel;
+  }
+  for (int i = tid; i < hi - lo; i += kThreads) {
+    const int page = bitmap ? list[i] : lo + i;
+    if (bitmap) a.sel_list[skv * a.cap_pages + lo + i] = page;
+    if (a.page_ids) a.page_ids[skv * a.page_ids_stride + lo + i] = page;
+  }
+  const size_t hq0 = (size_t)s * a.Hq + (size_t)kvh * G;  // first query head of the group
+  if (tid < 8) {
+    wkept[0][tid] = 0.0f;
+    th_sh[tid] = (a.policy == ENTMAXKV_POLICY_GAUSSIAN && tid < G) ? a.tauhat[hq0 + tid] : 0.0f;
+  }
+  uint32_t bq[D / 16][2];
+  if constexpr (sizeof(T) == 2) {
+    load_q_bfrag<D>((const __nv_bfloat16*)a.q + hq0 * D, G, lane, bq);
+  } else {
+    for (int i = tid; i < G * D; i += kThreads) qs[i / D][i % D] = ((const float*)a.q)[hq0 * D + i];
+  }
+  __syncthreads();
+
+  float wm[8], kept[8];
+#pragma unroll
+  for (int h = 0; h < 8; ++h) {
+    wm[h] = -CUDART_INF_F;
+    kept[h] = 0.0f;
+  }
+  const bool beta2 = a.beta == 2.0f;
+  for (int i = warp; i < hi - lo; i += kWarps) {
+    const int rank = lo + i;
+    const int page = bitmap ? list[i] : rank;
+    const int ph = phys_page(a.block_table, seq, page, a.maxp, a.nphys, lane == 0 ? a.status : nullptr);
+    const int nv = min(P, L - page * P);
+    float* zb = a.z + (skv * a.cap_pages + rank) * (size_t)P * G;
+    float* pm = a.pmax + (skv * a.cap_pages + rank) * (size_t)G;
+    if (ph < 0) {  // unreadable page: no scores
+      for (int e = lane; e < P * G; e += 32) zb[e] = -CUDART_INF_F;
+      if (lane < G) pm[lane] = -CUDART_INF_F;
+      continue;
+    }
+    const size_t slab_off = ((size_t)ph * a.Hkv + kvh) * P * D;
+    if constexpr (sizeof(T) == 2) {
+      float zf[2][4];
+      page_scores_bf16<D>((const __nv_bfloat16*)a.k_pool + slab_off, P, nv, bq, a.zscale, lane, zf);
+      const int r = lane >> 2, c = lane & 3, h0 = 2 * c, h1 = h0 + 1;
+      float pm0 = -CUDART_INF_F, pm1 = -CUDART_INF_F;
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+        if (16 * mt >= P) break;
+        const int t0 = 16 * mt + r, t1 = t0 + 8;
+        if (h0 < G) {
+          zb[t0 * G + h0] = zf[mt][0];
+          zb[t1 * G + h0] = zf[mt][2];
+        }
+        if (h1 < G) {
+          zb[t0 * G + h1] = zf[mt][1];
+          zb[t1 * G + h1] = zf[mt][3];
+        }
+        pm0 = fmaxf(pm0, fmaxf(zf[mt][0], zf[mt][2]));
+        pm1 = fmaxf(pm1, fmaxf(zf[mt][1], zf[mt][3]));
+      }
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        pm0 = fmaxf(pm0, __shfl_xor_sync(0xffffffffu, pm0, o));
+        pm1 = fmaxf(pm1, __shfl_xor_sync(0xffffffffu, pm1, o));
+      }
+      if (r == 0) {
+        if (h0 < G) pm[h0] = pm0;
+        if (h1 < G) pm[h1] = pm1;
+      }
+      // lane c keeps the running max of heads 2c, 2c+1 in wm[0], wm[1]
+      wm[0] = fmaxf(wm[0], pm0);
+      wm[1] = fmaxf(wm[1], pm1);
+    } else {
+      float zt[8];
+      page_scores_f32<D>((const float*)a.k_pool + slab_off, nv, qs, G, a.zscale, lane, zt);
+#pragma unroll
+      for (int h = 0; h < 8; ++h) {
+        if (h < G) {
+          if (lane < P) zb[lane * G + h] = zt[h];
+          const float m = warp_max(zt[h]);
+          if (lane == 0) pm[h] = m;
+          wm[h] = fmaxf(wm[h], m);
+        }
+      }
+    }
+    if (a.policy == ENTMAXKV_POLICY_GAUSSIAN && lane < G) {
+      const float2 v = a.gauss_ms[(hq0 + lane) * a.maxp + page];
+      float g, dg;
+      gauss_moment(v.x - th_sh[lane], v.y, beta2, g, dg);
+      kept[0] += (float)nv * g;  // lane h accumulates head h
+    }
+  }
+  // block max z per head → global max; candidate threshold per head
+  if constexpr (sizeof(T) == 2) {
+    const int c = lane & 3;
+    if (lane < 4) {
+      if (2 * c < 8) wmax[warp][2 * c] = wm[0];
+      if (2 * c + 1 < 8) wmax[warp][2 * c + 1] = wm[1];
+    }
+  } else {
+    if (lane == 0)
+      for (int h = 0; h < 8; ++h) wmax[warp][h] = wm[h];
+  }
+  if (lane < 8) wkept[warp][lane] = lane < G ? kept[0] : 0.0f;
+  __syncthreads();
+  if (tid < G) {
+    float m = -CUDART_INF_F, ks = 0.0f;
+    for (int w = 0; w < kWarps; ++w) {
+      m = fmaxf(m, wmax[w][tid]);
+      ks += wkept[w][tid];
+    }
+    float gm = m;
+    if (m > -CUDART_INF_F) {
+      const uint32_t old = atomicMax(&a.zmax[hq0 + tid], ord_enc(m));
+      gm = fmaxf(m, ord_dec(old));
+    }
+    thr_sh[tid] = gm - 1.0f;
+    if (a.policy == ENTMAXKV_POLICY_GAUSSIAN && ks != 0.0f) atomicAdd(&a.kept_mass[hq0 + tid], ks);
+  }
+  __syncthreads();
+  // candidates: tokens above (best known max − 1) of pages whose max clears it
+  for (int i = warp; i < hi - lo; i += kWarps) {
+    const int rank = lo + i;
+    const float* zb = a.z + (skv * a.cap_pages + rank) * (size_t)P * G;
+    const float* pm = a.pmax + (skv * a.cap_pages + rank) * (size_t)G;
+    for (int hg = 0; hg < G; ++hg) {
+      const float thr = thr_sh[hg];
+      if (!(pm[hg] > thr)) continue;
+      for (int t0 = 0; t0 < P; t0 += 32) {
+        const int t = t0 + lane;
+        const float zv = t < P ? zb[t * G + hg] : -CUDART_INF_F;
+        const bool pred = zv > thr;
+        const uint32_t bits = __ballot_sync(0xffffffffu, pred);
+        if (!bits) continue;
+        int base = 0;
+        if (lane == 0) base = atomicAdd(&a.cand_cnt[hq0 + hg], __popc(bits));
+        base = __shfl_sync(0xffffffffu, base, 0);
+        const int idx = base + __popc(bits & ((1u << lane) - 1u));
+        if (pred && idx < kCandCap) a.cand[(hq0 + hg) * kCandCap + idx] = zv;
+      }
+    }
+  }
+  // the last block of this (sequence, KV head) solves τ
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) last_sh = atomicAdd(&a.cnt_a[skv], 1) == a.splits - 1;
+  __syncthreads();
+  if (!last_sh) return;
+  __threadfence();
+  if (warp >= G) return;
+  const int hg = warp;
+  const size_t hs = hq0 + hg;
+  const float zm = ord_dec(__ldcg(&a.zmax[hs]));
+  float tau_f = CUDART_NAN_F;
+  if (zm > -CUDART_INF_F) {
+    const float T0 = zm - 1.0f;
+    TauSource src;
+    src.wc = wcand[warp];
+    src.m = 0;
+    src.cand = a.cand + hs * kCandCap;
+    src.nc = __ldcg(&a.cand_cnt[hs]);
+    src.z = a.z + skv * a.cap_pages * (size_t)P * G;
+    src.n_sel = n_sel;
+    src.P = P;
+    src.G = G;
+    src.hg = hg;
+    if (src.nc <= kCandCap) {
+      int m = 0;
+      for (int i0 = 0; i0 < src.nc; i0 += 32) {
+        const int i = i0 + lane;
+        const float zv = i < src.nc ? __ldcg(src.cand + i) : -CUDART_INF_F;
+        const bool pred = zv > T0;
+        const uint32_t bits = __ballot_sync(0xffffffffu, pred);
+        const int pos = m + __popc(bits & ((1u << lane) - 1u));
+        if (pred && pos < kWarpCand) wcand[warp][pos] = zv;
+        m += __popc(bits);
+      }
+      __syncwarp();
+      if (m <= kWarpCand) {
+        src.mode = 0;
+        src.m = m;
+      } else {
+        src.mode = 1;
+      }
+    } else {
+      src.mode = 2;
+      if (lane == 0) raise_flag(a.status, ENTMAXKV_DEV_CAND_OVERFLOW);
+    }
+    bool ok;
+    const double tau = solve_tau_warp(src, (double)T0, a.beta, ok);
+    if (!ok && lane == 0) raise_flag(a.status, ENTMAXKV_DEV_TAU_NOCONV);
+    tau_f = (float)tau;
+  }
+  if (lane == 0) {
+    a.tau_ws[hs] = tau_f;
+    if (a.tau_out) a.tau_out[hs] = tau_f;
+    if (a.delta_out) {
+      if (a.policy == ENTMAXKV_POLICY_GAUSSIAN)
+        a.delta_out[hs] = L > 0 ? fminf(1.0f, fmaxf(0.0f, 1.0f - __ldcg(&a.kept_mass[hs]))) : 0.0f;
+      else if (a.policy == ENTMAXKV_POLICY_FULL)
+        a.delta_out[hs] = 0.0f;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+
+template <typename T>
+struct VTraits;
+template <>
+struct VTraits<float> {
+  static constexpr int VEC = 4;
+  __device__ static void unpack(const uint4& r, float (&v)[4]) {
+    v[0] = __uint_as_float(r.x);
+    v[1] = __uint_as_float(r.y);
+    v[2] = __uint_as_float(r.z);
+    v[3] = __uint_as_float(r.w);
+  }
+};
+template <>
+struct VTraits<__nv_bfloat16> {
+  static constexpr int VEC = 8;
+  __device__ static void unpack(const uint4& r, float (&v)[8]) {
+    v[0] = bf_lo(r.x); v[1] = bf_hi(r.x);
+    v[2] = bf_lo(r.y); v[3] = bf_hi(r.y);
+    v[4] = bf_lo(r.z); v[5] = bf_hi(r.z);
+    v[6] = bf_lo(r.w); v[7] = bf_hi(r.w);
+  }
+};
+
+template <typename T, int D, int GP>
+__global__ void __launch_bounds__(kThreads) pass_b_kernel(DecodeArgs a) {
+  constexpr int VEC = VTraits<T>::VEC, LPR = D / VEC, TG = 32 / LPR;
+  __shared__ float tau_sh[GP];
+  __shared__ float red[kWarps][GP][D];
+  __shared__ float dsum[kWarps][GP];
+  __shared__ int last_sh;
+  const int split = blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = a.G, P = a.P;
+  const int dc = lane % LPR, tg = lane / LPR;
+  const int seq = seq_row(a.seq_ids, s, a.max_seqs, nullptr);
+  const int L = seq_len_clamped(a.seq_lens, seq, a.maxp, P, nullptr);
+  const int n_pages = (L + P - 1) / P;
+  const bool bitmap = uses_bitmap(a.policy);
+  const size_t skv = (size_t)s * a.Hkv + kvh;
+  const size_t hq0 = (size_t)s * a.Hq + (size_t)kvh * G;
+  const int n_sel = bitmap ? __ldcg(&a.nsel_ws[skv]) : n_pages;
+  const int lo = (int)(((long long)n_sel * split) / a.splits);
+  const int hi = (int)(((long long)n_sel * (split + 1)) / a.splits);
+  if (tid < GP) tau_sh[tid] = tid < G ? __ldcg(&a.tau_ws[hq0 + tid]) : CUDART_INF_F;
+  __syncthreads();
+  float tau[GP];
+#pragma unroll
+  for (int h = 0; h < GP; ++h) tau[h] = tau_sh[h];
+  const bool dense = (a.flags & ENTMAXKV_FLAG_DENSE_V) != 0;
+  float acc[GP][VEC];
+#pragma unroll
+  for (int h = 0; h < GP; ++h)
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) acc[h][j] = 0.0f;
+
+  for (int i = warp; i < hi - lo; i += kWarps) {
+    const int rank = lo + i;
+    const float* pm = a.pmax + (skv * a.cap_pages + rank) * (size_t)G;
+    bool need = dense;
+#pragma unroll
+    for (int h = 0; h < GP; ++h)
+      if (h < G) need = need || (__ldcg(pm + h) > tau[h]);
+    if (!need) continue;
+    const int page = bitmap ? __ldcg(&a.sel_list[skv * a.cap_pages + rank]) : rank;
+    const int ph = phys_page(a.block_table, seq, page, a.maxp, a.nphys, nullptr);
+    if (ph < 0) continue;
+    const int nv = min(P, L - page * P);
+    const T* vs = (const T*)a.v_pool + ((size_t)ph * a.Hkv + kvh) * P * D + dc * VEC;
+    const float* zb = a.z + (skv * a.cap_pages + rank) * (size_t)P * G;
+    for (int t = tg; t < nv; t += TG) {
+      const uint4 raw = ld_stream(vs + (size_t)t * D);
+      float v[VEC];
+      VTraits<T>::unpack(raw, v);
+#pragma unroll
+      for (int h = 0; h < GP; ++h) {
+        if (h < G) {
+          const float p = pos_pow(__ldcg(zb + t * G + h) - tau[h], a.beta);
+#pragma unroll
+          for (int j = 0; j < VEC; ++j) acc[h][j] = fmaf(p, v[j], acc[h][j]);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int o = LPR; o < 32; o <<= 1)
+#pragma unroll
+    for (int h = 0; h < GP; ++h)
+#pragma unroll
+      for (int j = 0; j < VEC; ++j) acc[h][j] += __shfl_xor_sync(0xffffffffu, acc[h][j], o);
+  if (tg == 0) {
+#pragma unroll
+    for (int h = 0; h < GP; ++h)
+#pragma unroll
+      for (int j = 0; j < VEC; ++j) red[warp][h][dc * VEC + j] = acc[h][j];
+  }
+  // top-k: this block's share of the certified dropped mass
+  float dd[GP];
+#pragma unroll
+  for (int h = 0; h < GP; ++h) dd[h] = 0.0f;
+  if (a.policy == ENTMAXKV_POLICY_TOPK) {
+    const uint32_t* bm = a.bitmap + skv * a.words;
+    const int plo = (int)(((long long)n_pages * split) / a.splits);
+    const int phi = (int)(((long long)n_pages * (split + 1)) / a.splits);
+    for (int p = plo + tid; p < phi; p += kThreads) {
+      if ((bm[p >> 5] >> (p & 31)) & 1u) continue;
+      const float np = (float)(p == n_pages - 1 ? L - p * P : P);
+#pragma unroll
+      for (int h = 0; h < GP; ++h)
+        if (h < G) dd[h] += np * pos_pow(a.a1 * a.bbox_u[(hq0 + h) * a.maxp + p] - tau[h], a.beta);
+    }
+#pragma unroll
+    for (int h = 0; h < GP; ++h) {
+      const float w = warp_sum(dd[h]);
+      if (lane == 0) dsum[warp][h] = w;
+    }
+  }
+  __syncthreads();
+  float* part = a.partial + (skv * a.splits + split) * (size_t)G * (D + 2);
+  for (int e = tid; e < G * D; e += kThreads) {
+    const int h = e / D, d = e % D;
+    float sum = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) sum += red[w][h][d];
+    part[h * (D + 2) + d] = sum;
+  }
+  if (a.policy == ENTMAXKV_POLICY_TOPK && tid < G) {
+    float sum = 0.0f;
+    for (int w = 0; w < kWarps; ++w) sum += dsum[w][tid];
+    if (sum != 0.0f) atomicAdd(&a.dbar[hq0 + tid], sum);
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) last_sh = atomicAdd(&a.cnt_b[skv], 1) == a.splits - 1;
+  __syncthreads();
+  if (!last_sh) return;
+  __threadfence();
+  for (int e = tid; e < G * D; e += kThreads) {
+    const int h = e / D, d = e % D;
+    float sum = 0.0f;
+    for (int sp = 0; sp < a.splits; ++sp)
+      sum += __ldcg(a.partial + (skv * a.splits + sp) * (size_t)G * (D + 2) + h * (D + 2) + d);
+    a.out[(hq0 + h) * D + d] = sum;
+  }
+  if (a.policy == ENTMAXKV_POLICY_TOPK && a.delta_out && tid < G)
+    a.delta_out[hq0 + tid] = L > 0 ? fminf(1.0f, __ldcg(&a.dbar[hq0 + tid])) : 0.0f;
+}
+
+// ---------------------------------------------------------------------------
+
+static int pick_gp(int G) { return G <= 1 ? 1 : (G <= 2 ? 2 : (G <= 4 ? 4 : 8)); }
+
+cudaError_t launch_pass_a(const DecodeArgs& a, int kv_dtype, cudaStream_t st) {
+  dim3 grid(a.splits, a.Hkv, a.S);
+  if (kv_dtype == ENTMAXKV_BF16) {
+    if (a.D == 128) pass_a_kernel<__nv_bfloat16, 128><<<grid, kThreads, 0, st>>>(a);
+    else pass_a_kernel<__nv_bfloat16, 64><<<grid, kThreads, 0, st>>>(a);
+  } else {
+    if (a.D == 128) pass_a_kernel<float, 128><<<grid, kThreads, 0, st>>>(a);
+    else pass_a_kernel<float, 64><<<grid, kThreads, 0, st>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+template <typename T, int D>
+static void pass_b_g(const DecodeArgs& a, dim3 grid, cudaStream_t st) {
+  switch (pick_gp(a.G)) {
+    case 1: pass_b_kernel<T, D, 1><<<grid, kThreads, 0, st>>>(a); break;
+    case 2: pass_b_kernel<T, D, 2><<<grid, kThreads, 0, st>>>(a); break;
+    case 4: pass_b_kernel<T, D, 4><<<grid, kThreads, 0, st>>>(a); break;
+    default: pass_b_kernel<T, D, 8><<<grid, kThreads, 0, st>>>(a); break;
+  }
+}
+
+cudaError_t launch_pass_b(const DecodeArgs& a, int kv_dtype, cudaStream_t st) {
+  dim3 grid(a.splits, a.Hkv, a.S);
+  if (kv_dtype == ENTMAXKV_BF16) {
+    if (a.D == 128) pass_b_g<__nv_bfloat16, 128>(a, grid, st);
+    else pass_b_g<__nv_bfloat16, 64>(a, grid, st);
+  } else {
+    if (a.D == 128) pass_b_g<float, 128>(a, grid, st);
+    else pass_b_g<float, 64>(a, grid, st);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace ekv

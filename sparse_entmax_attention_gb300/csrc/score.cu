@@ -1,0 +1,310 @@
+// score.cu -- query-aware page scoring from per-page metadata.
+//
+// EntmaxKV (gist.science technical summary, §2A):
+//  * bounding box: U_p = Σ_d max(q_d·kmin_d, q_d·kmax_d)/√d bounds every
+//    token score of page p. With q⁺ = max(q,0), q⁻ = min(q,0) this is the
+//    contraction U_p = (q⁺·kmax_p + q⁻·kmin_p)/√d, exact term by term.
+//  * Gaussian statistics: token scores of page p modelled as N(μ_p, σ_p²)
+//    with μ_p = q·mean_p/√d and σ_p² = Σ_d q_d²·var_{p,d}/d (diagonal model),
+//    reported on the z scale: m_p = (α−1)μ_p, ς_p = (α−1)σ_p.
+//
+// bf16 metadata: the group's g query heads against 16 pages form a
+// [16 pages × 2d] · [2d × 8 heads] tile: one m16n8k16 bf16 MMA chain per 16
+// pages (products of bf16 values are exact in the fp32 accumulator). The
+// tile's A operand is read straight from global memory with 16-byte loads in
+// a permuted k order; the B operand ([q⁺; q⁻]) is permuted identically, so
+// the contraction is unchanged.
+#include "common.cuh"
+
+namespace ekv {
+
+// B fragment words of query head n (= lane/4) for k-step (s2, u):
+// dims 32·s2 + 8·c + 4·u + {0,1} and {2,3}, c = lane%4.
+__device__ __forceinline__ void load_q_frag_bf16(const __nv_bfloat16* qh, bool valid, int s2,
+                                                 int u, int c, uint32_t& w0, uint32_t& w1) {
+  if (!valid) {
+    w0 = w1 = 0u;
+    return;
+  }
+  const uint2 x = *reinterpret_cast<const uint2*>(qh + 32 * s2 + 8 * c + 4 * u);
+  w0 = x.x;
+  w1 = x.y;
+}
+
+// Split a bf16 pair into its positive and negative parts (exact).
+__device__ __forceinline__ void split_sign(uint32_t w, uint32_t& pos, uint32_t& neg) {
+  uint32_t lo = w & 0xffffu, hi = w >> 16;
+  uint32_t plo = (lo & 0x8000u) ? 0u : lo, nlo = (lo & 0x8000u) ? lo : 0u;
+  uint32_t phi = (hi & 0x8000u) ? 0u : hi, nhi = (hi & 0x8000u) ? hi : 0u;
+  pos = plo | (phi << 16);
+  neg = nlo | (nhi << 16);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads) bbox_bf16_kernel(DecodeArgs a) {
+  constexpr int KS = D / 16;   // k-steps per half of the 2d contraction
+  constexpr int C16 = D / 32;  // 16-byte chunks per row per lane
+  const int kvh = blockIdx.y, s = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = lane >> 2, c = lane & 3;
+  const int seq = seq_row(a.seq_ids, s, a.max_seqs, threadIdx.x == 0 ? a.status : nullptr);
+  if (seq < 0) return;
+  const int L = seq_len_clamped(a.seq_lens, seq, a.maxp, a.P, threadIdx.x == 0 ? a.status : nullptr);
+  const int n_pages = (L + a.P - 1) / a.P;
+  const int tiles = (n_pages + 15) / 16;
+  if ((int)(blockIdx.x * kWarps) >= tiles) return;
+
+  // B operand: [q⁺ ; q⁻] of head n = r.
+  const bool hv = r < a.G;
+  const __nv_bfloat16* qh =
+      (const __nv_bfloat16*)a.q + ((size_t)s * a.Hq + (size_t)kvh * a.G + (hv ? r : 0)) * D;
+  uint32_t bp[KS][2], bn[KS][2];
+#pragma unroll
+  for (int ks = 0; ks < KS; ++ks) {
+    uint32_t w0, w1;
+    load_q_frag_bf16(qh, hv, ks >> 1, ks & 1, c, w0, w1);
+    split_sign(w0, bp[ks][0], bn[ks][0]);
+    split_sign(w1, bp[ks][1], bn[ks][1]);
+  }
+  const size_t ustride = (size_t)a.maxp;
+  float* urow = a.bbox_u + ((size_t)s * a.Hq + (size_t)kvh * a.G) * ustride;
+  float* uhat = a.bbox_uhat + ((size_t)s * a.Hkv + kvh) * ustride;
+  const __nv_bfloat16* kmax = (const __nv_bfloat16*)a.kmax;
+  const __nv_bfloat16* kmin = (const __nv_bfloat16*)a.kmin;
+
+  for (int tile = blockIdx.x * kWarps + warp; tile < tiles; tile += gridDim.x * kWarps) {
+    const int p0 = tile * 16 + r, p1 = p0 + 8;
+    const int ph0 = p0 < n_pages ? phys_page(a.block_table, seq, p0, a.maxp, a.nphys, a.status) : -1;
+    const int ph1 = p1 < n_pages ? phys_page(a.block_table, seq, p1, a.maxp, a.nphys, a.status) : -1;
+    uint4 hx0[C16], hx1[C16], lo0[C16], lo1[C16];
+    const size_t m0 = ((size_t)(ph0 < 0 ? 0 : ph0) * a.Hkv + kvh) * D + 8 * c;
+    const size_t m1 = ((size_t)(ph1 < 0 ? 0 : ph1) * a.Hkv + kvh) * D + 8 * c;
+#pragma unroll
+    for (int j = 0; j < C16; ++j) {
+      const uint4 zz = make_uint4(0u, 0u, 0u, 0u);
+      hx0[j] = ph0 >= 0 ? ld_stream(kmax + m0 + 32 * j) : zz;
+      hx1[j] = ph1 >= 0 ? ld_stream(kmax + m1 + 32 * j) : zz;
+      lo0[j] = ph0 >= 0 ? ld_stream(kmin + m0 + 32 * j) : zz;
+      lo1[j] = ph1 >= 0 ? ld_stream(kmin + m1 + 32 * j) : zz;
+    }
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      const int j = ks >> 1;
+      const bool u = ks & 1;
+      mma_bf16(acc, u ? hx0[j].z : hx0[j].x, u ? hx1[j].z : hx1[j].x, u ? hx0[j].w : hx0[j].y,
+               u ? hx1[j].w : hx1[j].y, bp[ks][0], bp[ks][1]);
+      mma_bf16(acc, u ? lo0[j].z : lo0[j].x, u ? lo1[j].z : lo1[j].x, u ? lo0[j].w : lo0[j].y,
+               u ? lo1[j].w : lo1[j].y, bn[ks][0], bn[ks][1]);
+    }
+    const int h0 = 2 * c, h1 = 2 * c + 1;
+    // an unreadable page gets −inf: no bound mass, never preferred by top-k
+    const float u00 = ph0 >= 0 ? acc[0] * a.inv_sqrt_d : -CUDART_INF_F;
+    const float u01 = ph0 >= 0 ? acc[1] * a.inv_sqrt_d : -CUDART_INF_F;
+    const float u10 = ph1 >= 0 ? acc[2] * a.inv_sqrt_d : -CUDART_INF_F;
+    const float u11 = ph1 >= 0 ? acc[3] * a.inv_sqrt_d : -CUDART_INF_F;
+    if (p0 < n_pages) {
+      if (h0 < a.G) urow[h0 * ustride + p0] = u00;
+      if (h1 < a.G) urow[h1 * ustride + p0] = u01;
+    }
+    if (p1 < n_pages) {
+      if (h0 < a.G) urow[h0 * ustride + p1] = u10;
+      if (h1 < a.G) urow[h1 * ustride + p1] = u11;
+    }
+    float mx0 = fmaxf(h0 < a.G ? u00 : -CUDART_INF_F, h1 < a.G ? u01 : -CUDART_INF_F);
+    float mx1 = fmaxf(h0 < a.G ? u10 : -CUDART_INF_F, h1 < a.G ? u11 : -CUDART_INF_F);
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+    if (c == 0) {
+      if (p0 < n_pages) uhat[p0] = mx0;
+      if (p1 < n_pages) uhat[p1] = mx1;
+    }
+  }
+}
+
+// fp32 metadata: one thread per page, q in shared memory.
+template <int D>
+__global__ void __launch_bounds__(kThreads) bbox_f32_kernel(DecodeArgs a) {
+  __shared__ float qs[8][D];
+  const int kvh = blockIdx.y, s = blockIdx.z;
+  const int seq = seq_row(a.seq_ids, s, a.max_seqs, threadIdx.x == 0 ? a.status : nullptr);
+  if (seq < 0) return;
+  const int L = seq_len_clamped(a.seq_lens, seq, a.maxp, a.P, threadIdx.x == 0 ? a.status : nullptr);
+  const int n_pages = (L + a.P - 1) / a.P;
+  for (int i = threadIdx.x; i < a.G * D; i += blockDim.x)
+    qs[i / D][i % D] = ((const float*)a.q)[((size_t)s * a.Hq + (size_t)kvh * a.G) * D + i];
+  __syncthreads();
+  for (int p = blockIdx.x * blockDim.x + threadIdx.x; p < n_pages; p += gridDim.x * blockDim.x) {
+    const int ph = phys_page(a.block_table, seq, p, a.maxp, a.nphys, a.status);
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (ph >= 0) {
+      const float* lo = (const float*)a.kmin + ((size_t)ph * a.Hkv + kvh) * D;
+      const float* hi = (const float*)a.kmax + ((size_t)ph * a.Hkv + kvh) * D;
+      for (int d = 0; d < D; d += 4) {
+        const float4 l4 = *reinterpret_cast<const float4*>(lo + d);
+        const float4 h4 = *reinterpret_cast<const float4*>(hi + d);
+        const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, hv[4] = {h4.x, h4.y, h4.z, h4.w};
+#pragma unroll
+        for (int h = 0; h < 8; ++h) {
+          if (h < a.G) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float qd = qs[h][d + e];
+              acc[h] += fmaxf(qd * lv[e], qd * hv[e]);
+            }
+          }
+        }
+      }
+    }
+    float mx = -CUDART_INF_F;
+    for (int h = 0; h < a.G; ++h) {
+      const float u = ph >= 0 ? acc[h] * a.inv_sqrt_d : -CUDART_INF_F;
+      a.bbox_u[((size_t)s * a.Hq + (size_t)kvh * a.G + h) * a.maxp + p] = u;
+      mx = fmaxf(mx, u);
+    }
+    a.bbox_uhat[((size_t)s * a.Hkv + kvh) * a.maxp + p] = mx;
+  }
+}
+
+// Gaussian page scores. Half a warp per page: lane l (0..15) of the half
+// covers the 16-byte chunks l, l+16, ... of the page's mean and m2 rows; the
+// q and q² values of those dims live in registers. GP = group padded up.
+template <typename TQ, int D, int GP>
+__global__ void __launch_bounds__(kThreads) gauss_kernel(DecodeArgs a) {
+  constexpr int CH = D / 64;  // float4 chunks per lane per row
+  const int kvh = blockIdx.y, s = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int half = lane >> 4, hl = lane & 15;
+  __shared__ float wmax[kWarps][GP];
+  const int seq = seq_row(a.seq_ids, s, a.max_seqs, threadIdx.x == 0 ? a.status : nullptr);
+  if (seq < 0) return;
+  const int L = seq_len_clamped(a.seq_lens, seq, a.maxp, a.P, threadIdx.x == 0 ? a.status : nullptr);
+  const int n_pages = (L + a.P - 1) / a.P;
+  if ((int)(blockIdx.x * kWarps * 2) >= n_pages) return;
+
+  float qv[GP][CH * 4], q2[GP][CH * 4];
+#pragma unroll
+  for (int h = 0; h < GP; ++h) {
+    const TQ* qh = (const TQ*)a.q + ((size_t)s * a.Hq + (size_t)kvh * a.G + (h < a.G ? h : 0)) * D;
+#pragma unroll
+    for (int j = 0; j < CH; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float x = h < a.G ? to_f(qh[4 * (hl + 16 * j) + e]) : 0.0f;
+        qv[h][4 * j + e] = x;
+        q2[h][4 * j + e] = x * x;
+      }
+  }
+  float runmax[GP];
+#pragma unroll
+  for (int h = 0; h < GP; ++h) runmax[h] = -CUDART_INF_F;
+  for (int pp = blockIdx.x * kWarps + warp; pp * 2 < n_pages; pp += gridDim.x * kWarps) {
+    const int p = pp * 2 + half;
+    const bool valid = p < n_pages;
+    const int ph = valid ? phys_page(a.block_table, seq, p, a.maxp, a.nphys, hl == 0 ? a.status : nullptr) : -1;
+    float mu[GP], sg[GP];
+#pragma unroll
+    for (int h = 0; h < GP; ++h) mu[h] = sg[h] = 0.0f;
+    if (ph >= 0) {
+      const size_t base = ((size_t)ph * a.Hkv + kvh) * D;
+#pragma unroll
+      for (int j = 0; j < CH; ++j) {
+        const uint4 mr = ld_stream(a.mean + base + 4 * (hl + 16 * j));
+        const uint4 vr = ld_stream(a.m2 + base + 4 * (hl + 16 * j));
+        const float mv[4] = {__uint_as_float(mr.x), __uint_as_float(mr.y), __uint_as_float(mr.z),
+                             __uint_as_float(mr.w)};
+        const float vv[4] = {__uint_as_float(vr.x), __uint_as_float(vr.y), __uint_as_float(vr.z),
+                             __uint_as_float(vr.w)};
+#pragma unroll
+        for (int h = 0; h < GP; ++h)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            mu[h] = fmaf(qv[h][4 * j + e], mv[e], mu[h]);
+            sg[h] = fmaf(q2[h][4 * j + e], vv[e], sg[h]);
+          }
+      }
+    }
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1)
+#pragma unroll
+      for (int h = 0; h < GP; ++h) {
+        mu[h] += __shfl_xor_sync(0xffffffffu, mu[h], o);
+        sg[h] += __shfl_xor_sync(0xffffffffu, sg[h], o);
+      }
+    if (valid && hl == 0) {
+      const int nv = min(a.P, L - p * a.P);
+#pragma unroll
+      for (int h = 0; h < GP; ++h) {
+        if (h < a.G) {
+          float2 msv;
+          if (ph >= 0) {
+            msv.x = a.a1 * mu[h] * a.inv_sqrt_d;
+            msv.y = a.a1 * sqrtf(fmaxf(sg[h], 0.0f) / ((float)nv * (float)D));
+            runmax[h] = fmaxf(runmax[h], msv.x);
+          } else {  // unreadable page: no mass, never selected
+            msv = make_float2(-CUDART_INF_F, 0.0f);
+          }
+          a.gauss_ms[((size_t)s * a.Hq + (size_t)kvh * a.G + h) * a.maxp + p] = msv;
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int h = 0; h < GP; ++h) {
+    const float m = warp_max(runmax[h]);
+    if (lane == 0) wmax[warp][h] = m;
+  }
+  __syncthreads();
+  if (threadIdx.x < a.G) {
+    float m = -CUDART_INF_F;
+    for (int w = 0; w < kWarps; ++w) m = fmaxf(m, wmax[w][threadIdx.x]);
+    if (m > -CUDART_INF_F)
+      atomicMax(&a.mmax[(size_t)s * a.Hq + (size_t)kvh * a.G + threadIdx.x], ord_enc(m));
+  }
+}
+
+static int grid_x_for(int units, int per_block, int sms, int other_blocks) {
+  int need = (units + per_block - 1) / per_block;
+  int cap = (sms * 8 + other_blocks - 1) / other_blocks;  // ~8 blocks per SM overall
+  if (cap < 1) cap = 1;
+  if (need < 1) need = 1;
+  return need < cap ? need : cap;
+}
+
+cudaError_t launch_bbox(const DecodeArgs& a, int kv_dtype, int sms, cudaStream_t st) {
+  const int other = a.Hkv * a.S;
+  if (kv_dtype == ENTMAXKV_BF16) {
+    dim3 grid(grid_x_for((a.maxp + 15) / 16, kWarps, sms, other), a.Hkv, a.S);
+    if (a.D == 128) bbox_bf16_kernel<128><<<grid, kThreads, 0, st>>>(a);
+    else bbox_bf16_kernel<64><<<grid, kThreads, 0, st>>>(a);
+  } else {
+    dim3 grid(grid_x_for(a.maxp, kThreads, sms, other), a.Hkv, a.S);
+    if (a.D == 128) bbox_f32_kernel<128><<<grid, kThreads, 0, st>>>(a);
+    else bbox_f32_kernel<64><<<grid, kThreads, 0, st>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+template <typename TQ, int D>
+static void gauss_dispatch_g(const DecodeArgs& a, dim3 grid, cudaStream_t st) {
+  if (a.G <= 1) gauss_kernel<TQ, D, 1><<<grid, kThreads, 0, st>>>(a);
+  else if (a.G <= 2) gauss_kernel<TQ, D, 2><<<grid, kThreads, 0, st>>>(a);
+  else if (a.G <= 4) gauss_kernel<TQ, D, 4><<<grid, kThreads, 0, st>>>(a);
+  else gauss_kernel<TQ, D, 8><<<grid, kThreads, 0, st>>>(a);
+}
+
+cudaError_t launch_gauss(const DecodeArgs& a, int kv_dtype, int sms, cudaStream_t st) {
+  dim3 grid(grid_x_for(a.maxp, kWarps * 2, sms, a.Hkv * a.S), a.Hkv, a.S);
+  if (kv_dtype == ENTMAXKV_BF16) {
+    if (a.D == 128) gauss_dispatch_g<__nv_bfloat16, 128>(a, grid, st);
+    else gauss_dispatch_g<__nv_bfloat16, 64>(a, grid, st);
+  } else {
+    if (a.D == 128) gauss_dispatch_g<float, 128>(a, grid, st);
+    else gauss_dispatch_g<float, 64>(a, grid, st);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace ekv

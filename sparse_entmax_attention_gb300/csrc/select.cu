@@ -1,0 +1,288 @@
+// select.cu -- candidate page selection (EntmaxKV, gist.science technical
+// summary §2B).
+//
+// Gaussian-aware selection (§2B.2): solve the approximate normalisation
+// equation for τ̂ from the page statistics, then keep the pages whose
+// estimated maximum score clears τ̂ lowered by the margin Δ. Here
+//   F(τ) = Σ_p n_p·E[(Z_p − τ)_+^β],  Z_p ~ N(m_p, ς_p²),  F(τ̂) = 1,
+// solved by safeguarded Newton steps on log F inside a bracket [lo, hi]
+// (lo starts at max_p m_p − 1, where F ≥ 1 by Jensen's inequality; a step
+// leaving the bracket is replaced by bisection). Each query head gets one
+// cluster of kTauhatCluster blocks; every iteration each block sums its share
+// of pages, the blocks exchange partial sums through distributed shared
+// memory, and every block takes the same step from the same totals. Then a
+// page is kept when m_p + ς_p·sqrt(2 ln n_p) ≥ τ̂ − (α−1)Δ (the estimated
+// maximum M̂_p = μ_p + σ_p·sqrt(2 ln n_p) against τ̂/(α−1) − Δ, on the z scale);
+// a KV head keeps the union over its query heads, as bits in a bitmap.
+//
+// Top-k selection (§2B.1): the k pages with the largest bound (max over the
+// group's query heads), ties to the lower logical page index, by an 8-bit
+// radix select over order-preserving keys in one block per (sequence, KV head).
+// The same select enforces an optional cap on the Gaussian selection, keyed
+// by the margin max_h (M̂_p − threshold_h) of the selected pages.
+#include <cooperative_groups.h>
+
+#include "common.cuh"
+
+namespace cg = cooperative_groups;
+
+namespace ekv {
+
+constexpr int kTauhatIters = 60;
+
+__device__ __forceinline__ int page_tokens(int p, int n_pages, int L, int P) {
+  return p == n_pages - 1 ? L - p * P : P;
+}
+
+__device__ __forceinline__ float sqrt_2ln(int n, int P, float c_full) {
+  return n == P ? c_full : sqrtf(2.0f * logf((float)n));
+}
+
+__global__ void __cluster_dims__(kTauhatCluster, 1, 1) __launch_bounds__(kThreads)
+    tauhat_kernel(DecodeArgs a) {
+  cg::cluster_group cluster = cg::this_cluster();
+  __shared__ double2 slot[2];
+  __shared__ double red_f[kWarps], red_d[kWarps];
+  __shared__ double tau_sh;
+  __shared__ int done_sh;
+  const int h = blockIdx.y, s = blockIdx.z;
+  const int kvh = h / a.G;
+  const int rank = (int)cluster.block_rank();
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // Every block of a cluster takes the same early exits, so no cluster
+  // barrier is ever left waiting.
+  const int seq = seq_row(a.seq_ids, s, a.max_seqs, nullptr);
+  const int L = seq_len_clamped(a.seq_lens, seq, a.maxp, a.P, nullptr);
+  const int n_pages = (L + a.P - 1) / a.P;
+  if (n_pages == 0) return;
+  const double M = (double)ord_dec(a.mmax[(size_t)s * a.Hq + h]);
+  if (!(M > -CUDART_INF)) return;  // no readable page
+  const bool beta2 = a.beta == 2.0f;
+  const float2* ms = a.gauss_ms + ((size_t)s * a.Hq + h) * a.maxp;
+  const int words = (n_pages + 31) / 32;
+  const int chunk = ((words + kTauhatCluster - 1) / kTauhatCluster) * 32;
+  const int p_lo = rank * chunk, p_hi = min(n_pages, p_lo + chunk);
+
+  double lo = M - 1.0, hi = CUDART_INF, tau = lo;
+  bool converged = false;
+  for (int it = 0; it < kTauhatIters; ++it) {
+    const float tf = (float)tau;
+    float f = 0.0f, df = 0.0f;
+    for (int p = p_lo + tid; p < p_hi; p += kThreads) {
+      const float2 v = ms[p];
+      float g, dg;
+      gauss_moment(v.x - tf, v.y, beta2, g, dg);
+      const float np = (float)page_tokens(p, n_pages, L, a.P);
+      f = fmaf(np, g, f);
+      df = fmaf(np, dg, df);
+    }
+    const double fd = warp_sum((double)f), dd = warp_sum((double)df);
+    if (lane == 0) {
+      red_f[warp] = fd;
+      red_d[warp] = dd;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      double sf = 0.0, sd = 0.0;
+      for (int w = 0; w < kWarps; ++w) {
+        sf += red_f[w];
+        sd += red_d[w];
+      }
+      slot[it & 1] = make_double2(sf, sd);
+    }
+    cluster.sync();
+    if (tid == 0) {
+      double F = 0.0, dF = 0.0;  // same order in every block: identical totals
+      for (int r = 0; r < kTauhatCluster; ++r) {
+        const double2 v = cluster.map_shared_rank(&slot[0], r)[it & 1];
+        F += v.x;
+        dF += v.y;
+      }
+      if (F >= 1.0) lo = tau;
+      else hi = tau;
+      double next;
+      bool stop;
+      if (F == 1.0) {
+        next = tau;
+        stop = true;
+      } else {
+        next = (F > 0.0 && dF > 0.0) ? tau + log(F) * F / dF : CUDART_NAN;  // Newton on log F
+        if (!(next > lo && next < hi)) next = isinf(hi) ? lo + 1.0 : 0.5 * (lo + hi);
+        const double tol = 1e-6 * fmax(1.0, fabs(next));
+        stop = fabs(next - tau) <= tol || (hi - lo) <= tol;
+      }
+      tau = next;
+      done_sh = stop ? 1 : 0;
+      tau_sh = tau;
+    }
+    __syncthreads();
+    if (done_sh) {
+      converged = true;
+      break;
+    }
+    tau = tau_sh;
+  }
+  const float th = (float)tau_sh;
+  cluster.sync();  // no block leaves while another may still read its slots
+  if (rank == 0 && tid == 0) {
+    a.tauhat[(size_t)s * a.Hq + h] = th;
+    if (!converged) raise_flag(a.status, ENTMAXKV_DEV_TAUHAT_NOCONV);
+  }
+  // Selection bits: each warp covers 32 consecutive pages starting on a word.
+  const float thr = th - a.margin_z;
+  const float c_full = sqrtf(2.0f * logf((float)a.P));
+  uint32_t* bm = a.bitmap + ((size_t)s * a.Hkv + kvh) * a.words;
+  for (int p0 = p_lo + warp * 32; p0 < p_hi; p0 += kThreads) {
+    const int p = p0 + lane;
+    bool sel = false;
+    if (p < p_hi) {
+      const float2 v = ms[p];
+      sel = v.x + v.y * sqrt_2ln(page_tokens(p, n_pages, L, a.P), a.P, c_full) >= thr;
+    }
+    const uint32_t bits = __ballot_sync(0xffffffffu, sel);
+    if (lane == 0 && bits) atomicOr(&bm[p0 >> 5], bits);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// top-k
+
+// mode 0: key = bounding-box bound max over the group (bbox_uhat).
+// mode 1: key = margin max_h (m + ς·sqrt(2 ln n) − (τ̂_h − (α−1)Δ)) of a page the
+//         Gaussian rule selected, −inf for the others.
+__device__ __forceinline__ float page_key(const DecodeArgs& a, int mode, int s, int kvh, int p,
+                                          int n, int L, const uint32_t* bm, const float* thr,
+                                          float c_full) {
+  if (mode == 0) return a.bbox_uhat[((size_t)s * a.Hkv + kvh) * a.maxp + p];
+  if (!((bm[p >> 5] >> (p & 31)) & 1u)) return -CUDART_INF_F;
+  const float cn = sqrt_2ln(page_tokens(p, n, L, a.P), a.P, c_full);
+  float best = -CUDART_INF_F;
+  for (int h = 0; h < a.G; ++h) {
+    const float2 v = a.gauss_ms[((size_t)s * a.Hq + (size_t)kvh * a.G + h) * a.maxp + p];
+    best = fmaxf(best, v.x + v.y * cn - thr[h]);
+  }
+  return best;
+}
+
+__global__ void __launch_bounds__(1024) topk_kernel(DecodeArgs a, int mode) {
+  __shared__ int hist[256];
+  __shared__ int sh_scan[32];
+  __shared__ float thr[8];
+  __shared__ uint32_t sh_prefix, sh_mask;
+  __shared__ int sh_remaining, sh_eq_count;
+  const int kvh = blockIdx.x, s = blockIdx.y;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int seq = seq_row(a.seq_ids, s, a.max_seqs, tid == 0 ? a.status : nullptr);
+  const int L = seq_len_clamped(a.seq_lens, seq, a.maxp, a.P, tid == 0 ? a.status : nullptr);
+  const int n = (L + a.P - 1) / a.P;
+  uint32_t* bm = a.bitmap + ((size_t)s * a.Hkv + kvh) * a.words;
+  const float c_full = sqrtf(2.0f * logf((float)a.P));
+  int k;
+  if (mode == 0) {
+    k = min(a.kpages, n);
+    if (k == n) {  // keep every page
+      for (int p0 = warp * 32; p0 < n; p0 += 1024) {
+        const uint32_t bits = __ballot_sync(0xffffffffu, p0 + lane < n);
+        if (lane == 0) bm[p0 >> 5] = bits;
+      }
+      return;
+    }
+  } else {
+    int cnt = 0;
+    for (int w = tid; w < (n + 31) / 32; w += 1024) cnt += __popc(bm[w]);
+    int total;
+    block_exclusive_scan(cnt, sh_scan, total);
+    k = a.gcap;
+    if (total <= k) return;  // within the cap: selection stands
+    if (tid == 0) raise_flag(a.status, ENTMAXKV_DEV_CAPACITY);
+    if (tid < a.G) thr[tid] = a.tauhat[(size_t)s * a.Hq + (size_t)kvh * a.G + tid] - a.margin_z;
+  }
+  if (tid == 0) {
+    sh_prefix = 0u;
+    sh_mask = 0u;
+    sh_remaining = k;
+  }
+  __syncthreads();
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    if (tid < 256) hist[tid] = 0;
+    __syncthreads();
+    const uint32_t prefix = sh_prefix, mask = sh_mask;
+    for (int p = tid; p < n; p += 1024) {
+      const uint32_t key = ord_enc(page_key(a, mode, s, kvh, p, n, L, bm, thr, c_full));
+      if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1);
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // lane l owns digits 255−8l … 248−8l (descending); find where the count
+      // from the top reaches `remaining`.
+      int cnt[8], tot = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        cnt[j] = hist[255 - 8 * lane - j];
+        tot += cnt[j];
+      }
+      int incl = tot;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const int excl = incl - tot;
+      const int rem = sh_remaining;
+      if (excl < rem && incl >= rem) {
+        int run = excl;
+        for (int j = 0; j < 8; ++j) {
+          if (run + cnt[j] >= rem) {
+            const uint32_t digit = 255u - 8u * lane - j;
+            sh_prefix = prefix | (digit << shift);
+            sh_mask = mask | (255u << shift);
+            sh_remaining = rem - run;
+            sh_eq_count = cnt[j];
+            break;
+          }
+          run += cnt[j];
+        }
+      }
+    }
+    __syncthreads();
+  }
+  // T is the k-th largest key: keep every key > T and the `remaining`
+  // lowest-index pages with key == T.
+  const uint32_t T = sh_prefix;
+  const int remaining = sh_remaining;
+  const bool split_ties = sh_eq_count > remaining;
+  __syncthreads();  // every thread has read the selection state
+  int taken = 0;    // ties kept so far (block-uniform)
+  for (int base = 0; base < n; base += 1024) {
+    const int p = base + tid;
+    const uint32_t key = p < n ? ord_enc(page_key(a, mode, s, kvh, p, n, L, bm, thr, c_full)) : 0u;
+    bool sel = p < n && key > T;
+    const bool eq = p < n && key == T;
+    if (!split_ties) {
+      sel = sel || eq;
+    } else {
+      int tot;
+      const int before = block_exclusive_scan(eq ? 1 : 0, sh_scan, tot);
+      sel = sel || (eq && taken + before < remaining);
+      taken += tot;
+    }
+    const uint32_t bits = __ballot_sync(0xffffffffu, sel);
+    __syncthreads();  // mode 1 reads the bitmap it is rewriting
+    if (lane == 0 && base + warp * 32 < n) bm[p >> 5] = bits;
+    __syncthreads();
+  }
+}
+
+cudaError_t launch_tauhat(const DecodeArgs& a, cudaStream_t st) {
+  dim3 grid(kTauhatCluster, a.Hq, a.S);
+  tauhat_kernel<<<grid, kThreads, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_topk(const DecodeArgs& a, int mode, cudaStream_t st) {
+  dim3 grid(a.Hkv, a.S);
+  topk_kernel<<<grid, 1024, 0, st>>>(a, mode);
+  return cudaGetLastError();
+}
+
+}  // namespace ekv
