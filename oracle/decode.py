@@ -41,6 +41,30 @@ def _beta(alpha):
     return 1.0 / (alpha - 1.0)
 
 
+def attend_pages(K, V, Q, alpha: float, page_size: int, page_ids):
+    """α-entmax attention of the g query heads over the tokens of the given
+    pages only (§2C). Returns (out [g, d], tau [g]); an empty page set gives a
+    zero output and τ = NaN."""
+    K = np.asarray(K, np.float64)
+    V = np.asarray(V, np.float64)
+    Q = np.atleast_2d(np.asarray(Q, np.float64))
+    g, d = Q.shape
+    n_tok = K.shape[0]
+    keep = np.zeros(n_tok, dtype=bool)
+    for p in np.asarray(page_ids, dtype=np.int64):
+        keep[p * page_size: min(n_tok, (p + 1) * page_size)] = True
+    idx = np.nonzero(keep)[0]
+    out = np.zeros((g, d))
+    tau = np.full(g, np.nan)
+    if idx.size == 0:
+        return out, tau
+    s = K[idx] @ Q.T / math.sqrt(d)
+    for h in range(g):
+        p, tau[h] = em.entmax(s[:, h], alpha)
+        out[h] = p @ V[idx]
+    return out, tau
+
+
 def decode_group(K, V, Q, alpha: float, policy: str, page_size: int,
                  budget_tokens: int = 0, margin: float = 0.0):
     """Decode the g query heads that share one KV head.

@@ -1,0 +1,212 @@
+"""Python binding of libentmaxkv (ctypes). Argument marshalling only.
+
+Every step of the decode runs in the library's CUDA kernels; this module
+allocates caller-owned buffers with torch, passes their device pointers and
+the current CUDA stream, and turns non-zero return codes into exceptions.
+There is no fallback: if the library is missing or fails to load, calls
+raise.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libentmaxkv.so")
+
+F32, BF16 = 0, 1
+POLICY_FULL, POLICY_TOPK, POLICY_GAUSSIAN, POLICY_SOFTMAX = 0, 1, 2, 3
+POLICIES = {"full": POLICY_FULL, "topk": POLICY_TOPK, "gaussian": POLICY_GAUSSIAN,
+            "softmax": POLICY_SOFTMAX}
+FLAG_DENSE_V = 0x1
+DEV_BAD_PAGE_TABLE, DEV_CAPACITY, DEV_TAUHAT_NOCONV = 0x1, 0x2, 0x4
+DEV_CAND_OVERFLOW, DEV_TAU_NOCONV, DEV_BAD_SEQ_ID = 0x8, 0x10, 0x20
+
+# Symbols the header declares (kept in step with include/entmaxkv.h by a test).
+EXPORTS = ("entmaxkv_version", "entmaxkv_status_string", "entmaxkv_append",
+           "entmaxkv_workspace_bytes", "entmaxkv_decode", "entmaxkv_workspace_layout")
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("num_kv_heads", ctypes.c_int32), ("group", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("page_size", ctypes.c_int32),
+                ("max_seqs", ctypes.c_int32), ("max_pages_per_seq", ctypes.c_int32),
+                ("num_phys_pages", ctypes.c_int32), ("kv_dtype", ctypes.c_int32)]
+
+
+class CacheView(ctypes.Structure):
+    _fields_ = [("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p),
+                ("kmin", ctypes.c_void_p), ("kmax", ctypes.c_void_p),
+                ("mean", ctypes.c_void_p), ("m2", ctypes.c_void_p),
+                ("block_table", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p),
+                ("status", ctypes.c_void_p)]
+
+
+class WorkspaceView(ctypes.Structure):
+    _fields_ = [("bbox_u", ctypes.c_size_t), ("bbox_uhat", ctypes.c_size_t),
+                ("gauss_ms", ctypes.c_size_t), ("tauhat", ctypes.c_size_t),
+                ("sel_bitmap", ctypes.c_size_t), ("total", ctypes.c_size_t)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libentmaxkv.so (build it with ``python -m sparse_entmax_attention_gb300.build``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libentmaxkv.so not built ({LIB_PATH}); run "
+                          "`python -m sparse_entmax_attention_gb300.build`")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i32, u32, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_uint32, ctypes.c_float, ctypes.c_size_t
+    L.entmaxkv_version.restype = i32
+    L.entmaxkv_status_string.restype = ctypes.c_char_p
+    L.entmaxkv_status_string.argtypes = [i32]
+    L.entmaxkv_append.restype = i32
+    L.entmaxkv_append.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(CacheView), vp, vp, vp, i32, i32, vp]
+    L.entmaxkv_workspace_bytes.restype = sz
+    L.entmaxkv_workspace_bytes.argtypes = [ctypes.POINTER(Config), i32, i32, i32]
+    L.entmaxkv_decode.restype = i32
+    L.entmaxkv_decode.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(CacheView), vp, vp, i32,
+                                  f32, i32, i32, f32, u32, vp, sz, vp, vp, i32, vp, vp, vp, vp]
+    L.entmaxkv_workspace_layout.restype = i32
+    L.entmaxkv_workspace_layout.argtypes = [ctypes.POINTER(Config), i32, i32, i32,
+                                            ctypes.POINTER(WorkspaceView)]
+    _lib = L
+    return L
+
+
+class EntmaxKVError(RuntimeError):
+    pass
+
+
+def _check(code: int):
+    if code != 0:
+        raise EntmaxKVError(f"entmaxkv: {lib().entmaxkv_status_string(code).decode()} (code {code})")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+_DT = {torch.float32: F32, torch.bfloat16: BF16}
+
+
+class PagedCache:
+    """Caller-owned paged KV cache plus per-page key metadata (torch memory)."""
+
+    def __init__(self, num_kv_heads, group, head_dim, page_size, max_seqs, max_pages_per_seq,
+                 num_phys_pages, kv_dtype=torch.bfloat16, device="cuda"):
+        self.cfg = Config(num_kv_heads, group, head_dim, page_size, max_seqs,
+                          max_pages_per_seq, num_phys_pages, _DT[kv_dtype])
+        self.dtype, self.device = kv_dtype, torch.device(device)
+        Hkv, d, P = num_kv_heads, head_dim, page_size
+        self.k_pool = torch.zeros(num_phys_pages, Hkv, P, d, dtype=kv_dtype, device=device)
+        self.v_pool = torch.zeros_like(self.k_pool)
+        self.kmin = torch.zeros(num_phys_pages, Hkv, d, dtype=kv_dtype, device=device)
+        self.kmax = torch.zeros_like(self.kmin)
+        self.mean = torch.zeros(num_phys_pages, Hkv, d, dtype=torch.float32, device=device)
+        self.m2 = torch.zeros_like(self.mean)
+        self.block_table = torch.zeros(max_seqs, max_pages_per_seq, dtype=torch.int32, device=device)
+        self.seq_lens = torch.zeros(max_seqs, dtype=torch.int32, device=device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        self.view = CacheView(self.k_pool.data_ptr(), self.v_pool.data_ptr(), self.kmin.data_ptr(),
+                              self.kmax.data_ptr(), self.mean.data_ptr(), self.m2.data_ptr(),
+                              self.block_table.data_ptr(), self.seq_lens.data_ptr(),
+                              self.status.data_ptr())
+
+    @property
+    def num_q_heads(self):
+        return self.cfg.num_kv_heads * self.cfg.group
+
+    def device_status(self) -> int:
+        return int(self.status.item()) & 0xffffffff
+
+
+def append(cache: PagedCache, k, v, seq_ids=None, stream=None):
+    """entmaxkv_append: k, v [n_seqs, Hkv, n_tokens, d] in the cache dtype."""
+    assert k.is_contiguous() and v.is_contiguous() and k.dtype == cache.dtype
+    n_seqs, _, n_tok, _ = k.shape
+    _check(lib().entmaxkv_append(ctypes.byref(cache.cfg), ctypes.byref(cache.view), _ptr(k),
+                                 _ptr(v), _ptr(seq_ids), n_seqs, n_tok, _stream(stream)))
+
+
+def workspace_bytes(cache: PagedCache, n_seqs, policy, budget_tokens=0) -> int:
+    return int(lib().entmaxkv_workspace_bytes(ctypes.byref(cache.cfg), n_seqs,
+                                              POLICIES.get(policy, policy), budget_tokens))
+
+
+def workspace_layout(cache: PagedCache, n_seqs, policy, budget_tokens=0) -> WorkspaceView:
+    v = WorkspaceView()
+    _check(lib().entmaxkv_workspace_layout(ctypes.byref(cache.cfg), n_seqs,
+                                           POLICIES.get(policy, policy), budget_tokens,
+                                           ctypes.byref(v)))
+    return v
+
+
+def alloc_workspace(cache: PagedCache, n_seqs, policy, budget_tokens=0):
+    n = workspace_bytes(cache, n_seqs, policy, budget_tokens)
+    if n == 0:
+        raise EntmaxKVError("invalid decode arguments for workspace sizing")
+    return torch.empty(n, dtype=torch.uint8, device=cache.device)  # caching allocator: 256-B aligned
+
+
+@dataclass
+class DecodeOutputs:
+    out: torch.Tensor
+    page_ids: torch.Tensor
+    n_sel: torch.Tensor
+    tau: torch.Tensor
+    delta: torch.Tensor
+
+
+def page_capacity(cache: PagedCache, policy, budget_tokens) -> int:
+    p = POLICIES.get(policy, policy)
+    maxp, P = cache.cfg.max_pages_per_seq, cache.cfg.page_size
+    if p == POLICY_TOPK:
+        return min(budget_tokens // P, maxp)
+    if p == POLICY_GAUSSIAN and budget_tokens > 0:
+        return min(budget_tokens // P, maxp)
+    return maxp
+
+
+def alloc_outputs(cache: PagedCache, n_seqs, policy, budget_tokens=0) -> DecodeOutputs:
+    dev, Hq, Hkv = cache.device, cache.num_q_heads, cache.cfg.num_kv_heads
+    cap = page_capacity(cache, policy, budget_tokens)
+    return DecodeOutputs(
+        out=torch.empty(n_seqs, Hq, cache.cfg.head_dim, dtype=torch.float32, device=dev),
+        page_ids=torch.full((n_seqs, Hkv, cap), -1, dtype=torch.int32, device=dev),
+        n_sel=torch.empty(n_seqs, Hkv, dtype=torch.int32, device=dev),
+        tau=torch.empty(n_seqs, Hq, dtype=torch.float32, device=dev),
+        delta=torch.empty(n_seqs, Hq, dtype=torch.float32, device=dev))
+
+
+def decode(cache: PagedCache, q, alpha=1.5, policy="gaussian", budget_tokens=0, margin=0.0,
+           flags=0, seq_ids=None, workspace=None, outputs: DecodeOutputs | None = None,
+           stream=None) -> DecodeOutputs:
+    """entmaxkv_decode: q [n_seqs, Hq, d] in the cache dtype."""
+    assert q.is_contiguous() and q.dtype == cache.dtype
+    n_seqs = q.shape[0]
+    pol = POLICIES.get(policy, policy)
+    if workspace is None:
+        workspace = alloc_workspace(cache, n_seqs, pol, budget_tokens)
+    if outputs is None:
+        outputs = alloc_outputs(cache, n_seqs, pol, budget_tokens)
+    o = outputs
+    _check(lib().entmaxkv_decode(
+        ctypes.byref(cache.cfg), ctypes.byref(cache.view), _ptr(q), _ptr(seq_ids), n_seqs,
+        float(alpha), pol, int(budget_tokens), float(margin), int(flags), _ptr(workspace),
+        workspace.numel(), _ptr(o.out), _ptr(o.page_ids), o.page_ids.shape[-1], _ptr(o.n_sel),
+        _ptr(o.tau), _ptr(o.delta), _stream(stream)))
+    return o
