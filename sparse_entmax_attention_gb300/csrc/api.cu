@@ -89,7 +89,7 @@ static int compute_layout(const entmaxkv_config* c, int S, int policy, int budge
   L.bitmap = bitmap ? take(nk * L.words * 4) : none;
   L.ctrl_end = off;
   L.tauhat = policy == ENTMAXKV_POLICY_GAUSSIAN ? take(nq * 4) : none;
-  L.tau_ws = take(nq * 4);
+  L.tau_ws = take(nq * 8);
   L.nsel_ws = take(nk * 4);
   L.sel_list = bitmap ? take(nk * (size_t)cap * 4) : none;
   L.bbox_u = policy == ENTMAXKV_POLICY_TOPK ? take(nq * (size_t)maxp * 4) : none;
@@ -260,7 +260,7 @@ int32_t entmaxkv_decode(const entmaxkv_config* cfg, const entmaxkv_cache* cache,
   a.dbar = at<float>(workspace, L.dbar);
   a.bitmap = at<uint32_t>(workspace, L.bitmap);
   a.tauhat = at<float>(workspace, L.tauhat);
-  a.tau_ws = at<float>(workspace, L.tau_ws);
+  a.tau_ws = at<double>(workspace, L.tau_ws);
   a.nsel_ws = at<int32_t>(workspace, L.nsel_ws);
   a.sel_list = at<int32_t>(workspace, L.sel_list);
   a.bbox_u = at<float>(workspace, L.bbox_u);

@@ -56,7 +56,7 @@ struct DecodeArgs {
   uint32_t* bitmap;    // [S][Hkv][words]
   // workspace: written before it is read in every decode
   float* tauhat;       // [S][Hq]
-  float* tau_ws;       // [S][Hq]
+  double* tau_ws;      // [S][Hq]   exact τ (double)
   int32_t* nsel_ws;    // [S][Hkv]
   int32_t* sel_list;   // [S][Hkv][cap_pages]
   float* bbox_u;       // [S][Hq][maxp]

@@ -335,6 +335,7 @@ __global__ void __launch_bounds__(kThreads) pass_a_kernel(DecodeArgs a) {
   const size_t hs = hq0 + hg;
   const float zm = ord_dec(__ldcg(&a.zmax[hs]));
   float tau_f = CUDART_NAN_F;
+  double tau_d = CUDART_NAN;
   if (zm > -CUDART_INF_F) {
     const float T0 = zm - 1.0f;
     TauSource src;
@@ -370,12 +371,12 @@ __global__ void __launch_bounds__(kThreads) pass_a_kernel(DecodeArgs a) {
       if (lane == 0) raise_flag(a.status, ENTMAXKV_DEV_CAND_OVERFLOW);
     }
     bool ok;
-    const double tau = solve_tau_warp(src, (double)T0, a.beta, ok);
+    tau_d = solve_tau_warp(src, (double)T0, a.beta, ok);
     if (!ok && lane == 0) raise_flag(a.status, ENTMAXKV_DEV_TAU_NOCONV);
-    tau_f = (float)tau;
+    tau_f = (float)tau_d;
   }
   if (lane == 0) {
-    a.tau_ws[hs] = tau_f;
+    a.tau_ws[hs] = tau_d;
     if (a.tau_out) a.tau_out[hs] = tau_f;
     if (a.delta_out) {
       if (a.policy == ENTMAXKV_POLICY_GAUSSIAN)
@@ -414,7 +415,7 @@ struct VTraits<__nv_bfloat16> {
 template <typename T, int D, int GP>
 __global__ void __launch_bounds__(kThreads) pass_b_kernel(DecodeArgs a) {
   constexpr int VEC = VTraits<T>::VEC, LPR = D / VEC, TG = 32 / LPR;
-  __shared__ float tau_sh[GP];
+  __shared__ double tau_sh[GP];
   __shared__ float red[kWarps][GP][D];
   __shared__ float dsum[kWarps][GP];
   __shared__ int last_sh;
@@ -431,11 +432,15 @@ __global__ void __launch_bounds__(kThreads) pass_b_kernel(DecodeArgs a) {
   const int n_sel = bitmap ? __ldcg(&a.nsel_ws[skv]) : n_pages;
   const int lo = (int)(((long long)n_sel * split) / a.splits);
   const int hi = (int)(((long long)n_sel * (split + 1)) / a.splits);
-  if (tid < GP) tau_sh[tid] = tid < G ? __ldcg(&a.tau_ws[hq0 + tid]) : CUDART_INF_F;
+  if (tid < GP) tau_sh[tid] = tid < G ? __ldcg(&a.tau_ws[hq0 + tid]) : CUDART_INF;
   __syncthreads();
-  float tau[GP];
+  float tau[GP];   // bf16 pages: p from fp32 z − τ
+  double taud[GP]; // fp32 pages: p from z − τ in double (z's own rounding only)
 #pragma unroll
-  for (int h = 0; h < GP; ++h) tau[h] = tau_sh[h];
+  for (int h = 0; h < GP; ++h) {
+    taud[h] = tau_sh[h];
+    tau[h] = (float)taud[h];
+  }
   const bool dense = (a.flags & ENTMAXKV_FLAG_DENSE_V) != 0;
   float acc[GP][VEC];
 #pragma unroll
@@ -464,7 +469,9 @@ __global__ void __launch_bounds__(kThreads) pass_b_kernel(DecodeArgs a) {
 #pragma unroll
       for (int h = 0; h < GP; ++h) {
         if (h < G) {
-          const float p = pos_pow(__ldcg(zb + t * G + h) - tau[h], a.beta);
+          const float zv = __ldcg(zb + t * G + h);
+          const float p = sizeof(T) == 4 ? pos_pow((float)((double)zv - taud[h]), a.beta)
+                                         : pos_pow(zv - tau[h], a.beta);
 #pragma unroll
           for (int j = 0; j < VEC; ++j) acc[h][j] = fmaf(p, v[j], acc[h][j]);
         }

@@ -69,25 +69,29 @@ __device__ __forceinline__ void page_scores_bf16(const __nv_bfloat16* slab, int 
   }
 }
 
-// fp32 pages: lane t scores token t for every head of the group.
+// fp32 pages: lane t scores token t for every head of the group. The dot
+// product is accumulated in double (each fp32 product is exact there), so the
+// only rounding is the final one to fp32: fp32 KV is the accuracy path.
 template <int D>
 __device__ __forceinline__ void page_scores_f32(const float* slab, int nv, const float (*qs)[D],
                                                 int G, float scale, int lane, float (&zt)[8]) {
-#pragma unroll
-  for (int h = 0; h < 8; ++h) zt[h] = 0.0f;
+  double acc[8] = {0.0, 0.0, 0.0, 0.0, 0.0, 0.0, 0.0, 0.0};
   if (lane < nv) {
     const float* row = slab + (size_t)lane * D;
     for (int d = 0; d < D; d += 4) {
       const float4 k4 = *reinterpret_cast<const float4*>(row + d);
 #pragma unroll
       for (int h = 0; h < 8; ++h)
-        if (h < G)
-          zt[h] = fmaf(qs[h][d], k4.x,
-                       fmaf(qs[h][d + 1], k4.y, fmaf(qs[h][d + 2], k4.z, fmaf(qs[h][d + 3], k4.w, zt[h]))));
+        if (h < G) {
+          acc[h] = fma((double)qs[h][d], (double)k4.x, acc[h]);
+          acc[h] = fma((double)qs[h][d + 1], (double)k4.y, acc[h]);
+          acc[h] = fma((double)qs[h][d + 2], (double)k4.z, acc[h]);
+          acc[h] = fma((double)qs[h][d + 3], (double)k4.w, acc[h]);
+        }
     }
   }
 #pragma unroll
-  for (int h = 0; h < 8; ++h) zt[h] = lane < nv ? zt[h] * scale : -CUDART_INF_F;
+  for (int h = 0; h < 8; ++h) zt[h] = lane < nv ? (float)(acc[h] * (double)scale) : -CUDART_INF_F;
 }
 
 }  // namespace ekv

@@ -1,0 +1,126 @@
+"""GPU edge cases: empty and one-token sequences, k ≥ pages, a bad block-table
+entry, the Gaussian cap, decoding a subset of sequences, token-by-token
+appends."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import decode as odec
+from oracle import pages as opg
+from sparse_entmax_attention_gb300 import binding as B
+from sparse_entmax_attention_gb300 import synth
+
+from harness import Built, rel_l2
+from test_parity_gpu import check_decode
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ragged():
+    spec = synth.custom(4, 1, 128, 16, [0, 1, 17, 333], torch.bfloat16, 1.5, n_needles=2,
+                        shuffled_table=True)
+    return Built(spec)
+
+
+@pytest.mark.parametrize("policy,budget", [("full", 0), ("softmax", 0), ("topk", 64),
+                                           ("topk", 100000), ("gaussian", 0)])
+def test_empty_and_tiny_sequences(ragged, policy, budget):
+    o, _ = check_decode(ragged, policy, 1.5, budget, 0.5, units=[(1, 0), (2, 0), (3, 0)])
+    # the empty sequence: zero output, NaN τ, nothing selected, no dropped mass
+    assert torch.all(o.out[0] == 0)
+    assert torch.all(torch.isnan(o.tau[0]))
+    assert int(o.n_sel[0, 0]) == 0
+    assert torch.all(o.delta[0] == 0)
+
+
+def test_bad_block_table_entry_is_flagged_not_fatal():
+    spec = synth.custom(4, 1, 128, 16, [320], torch.bfloat16, 1.5, n_needles=2)
+    built = Built(spec)
+    c = built.cache
+    good = c.block_table.clone()
+    c.block_table[0, 5] = -7
+    c.status.zero_()
+    B.decode(c, built.q, 1.5, "full")
+    B.decode(c, built.q, 1.5, "topk", 64)
+    B.decode(c, built.q, 1.5, "gaussian", 0, 0.5)
+    B.decode(c, built.q, 1.5, "softmax")
+    torch.cuda.synchronize()
+    assert c.device_status() & B.DEV_BAD_PAGE_TABLE
+    c.block_table.copy_(good)
+    c.status.zero_()
+    check_decode(built, "full", 1.5)
+
+
+def test_bad_seq_id_is_flagged():
+    spec = synth.custom(4, 1, 128, 16, [64], torch.bfloat16, 1.5)
+    built = Built(spec)
+    c = built.cache
+    c.status.zero_()
+    sid = torch.tensor([3], dtype=torch.int32, device="cuda")
+    B.decode(c, built.q, 1.5, "full", seq_ids=sid)
+    torch.cuda.synchronize()
+    assert c.device_status() & B.DEV_BAD_SEQ_ID
+
+
+def test_gaussian_cap_overflow_keeps_largest_margins():
+    spec = synth.custom(8, 2, 128, 16, [2000], torch.bfloat16, 1.5, n_needles=4, n_outliers=2)
+    built = Built(spec)
+    c = built.cache
+    cap_tokens = 5 * 16
+    c.status.zero_()
+    o = B.decode(c, built.q, 1.5, "gaussian", cap_tokens, 1.0)
+    torch.cuda.synchronize()
+    assert c.device_status() & B.DEV_CAPACITY
+    for j in range(2):
+        K, V = built.host_kv(0, j)
+        r = odec.decode_group(K, V, built.host_q(0, j), 1.5, "gaussian", 16, cap_tokens, 1.0)
+        assert r["capacity_flag"]
+        ids = o.page_ids[0, j, : int(o.n_sel[0, j])].cpu().tolist()
+        assert ids == list(r["page_ids"])
+        out, tau = odec.attend_pages(K, V, built.host_q(0, j), 1.5, 16, ids)
+        for h in range(4):
+            assert rel_l2(o.out[0, 4 * j + h].cpu().numpy(), out[h]) <= 2e-3
+
+
+def test_decode_subset_by_seq_ids():
+    spec = synth.custom(8, 2, 128, 32, [900, 2100, 40], torch.bfloat16, 1.5, n_needles=3,
+                        shuffled_table=True)
+    built = Built(spec)
+    allq = built.q
+    full = B.decode(built.cache, allq, 1.5, "topk", 256)
+    sid = torch.tensor([2, 1], dtype=torch.int32, device="cuda")
+    sub = B.decode(built.cache, allq[[2, 1]].contiguous(), 1.5, "topk", 256, seq_ids=sid)
+    torch.cuda.synchronize()
+    torch.testing.assert_close(sub.out, full.out[[2, 1]], rtol=0, atol=0)
+    torch.testing.assert_close(sub.page_ids, full.page_ids[[2, 1]], rtol=0, atol=0)
+
+
+def test_token_by_token_append_matches_bulk():
+    spec = synth.custom(4, 2, 64, 16, [100], torch.bfloat16, 1.5, n_needles=2)
+    bulk = Built(spec)
+    step = Built.__new__(Built)
+    step.spec = spec
+    bt, total, need = synth.block_tables(spec)
+    step.cache = B.PagedCache(2, 2, 64, 16, 1, bt.shape[1], total, torch.bfloat16, "cuda")
+    step.cache.block_table.copy_(bt.cuda())
+    step.q, step.K, step.V = bulk.q, bulk.K, bulk.V
+    for t in range(100):  # single tokens, then chunks that straddle pages
+        if t < 40:
+            B.append(step.cache, bulk.K[0][:, t:t + 1].unsqueeze(0).contiguous(),
+                     bulk.V[0][:, t:t + 1].unsqueeze(0).contiguous())
+    for t0, t1 in ((40, 45), (45, 77), (77, 100)):
+        B.append(step.cache, bulk.K[0][:, t0:t1].unsqueeze(0).contiguous(),
+                 bulk.V[0][:, t0:t1].unsqueeze(0).contiguous())
+    torch.cuda.synchronize()
+    assert int(step.cache.seq_lens[0]) == 100
+    a, b = step.cache, bulk.cache
+    n_pages = 7
+    assert torch.equal(a.k_pool[:n_pages], b.k_pool[:n_pages])
+    assert torch.equal(a.kmin[:n_pages], b.kmin[:n_pages]) and torch.equal(a.kmax[:n_pages], b.kmax[:n_pages])
+    torch.testing.assert_close(a.mean[:n_pages], b.mean[:n_pages], rtol=1e-5, atol=1e-6)
+    torch.testing.assert_close(a.m2[:n_pages], b.m2[:n_pages], rtol=1e-4, atol=1e-5)
+    check_decode(step, "gaussian", 1.5, 0, 0.5)

@@ -1,0 +1,87 @@
+"""GPU parity on the named synthetic workloads at their full sizes.
+
+The 32k-token GQA workload is checked on every KV head; the 128k, 1M and
+batched workloads on sampled (sequence, KV head) units, which the oracle
+computes one by one, in the same launch configuration the benchmark times.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from sparse_entmax_attention_gb300 import binding as B
+from sparse_entmax_attention_gb300 import synth
+
+from harness import Built
+from test_parity_gpu import check_decode
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def gqa32k():
+    return Built(synth.workload("gqa32x8-d128-32k-p16-bf16"))
+
+
+@pytest.mark.parametrize("policy,budget,margin", [
+    ("topk", 1024, 0.0), ("full", 0, 0.0), ("softmax", 0, 0.0), ("gaussian", 0, 0.5)])
+def test_gqa32k_all_heads(gqa32k, policy, budget, margin):
+    check_decode(gqa32k, policy, 1.5, budget, margin)
+
+
+@pytest.fixture(scope="module")
+def gqa128k():
+    return Built(synth.workload("gqa32x8-d128-128k-p32-bf16"))
+
+
+@pytest.mark.parametrize("alpha", [1.5, 2.0])
+@pytest.mark.parametrize("margin", [0.0, 0.5, 1.0])
+def test_gqa128k_rotated_steps(gqa128k, alpha, margin):
+    spec = gqa128k.spec
+    nk = [d.needle_keys() for d in gqa128k.draws[0]]
+    for step in (1, 2):
+        q = synth.step_queries(spec, 0, step, nk, device="cuda").unsqueeze(0).contiguous()
+        o, _ = check_decode(gqa128k, "gaussian", alpha, 0, margin, q=q, units=[(0, 0), (0, 5)])
+        n_sel = int(o.n_sel.float().mean().round())
+        check_decode(gqa128k, "topk", alpha, max(1, n_sel) * spec.page_size, 0.0, q=q,
+                     units=[(0, 0), (0, 5)], check_intermediates=False)
+
+
+@pytest.fixture(scope="module")
+def gqa1m():
+    return Built(synth.workload("gqa32x8-d128-1m-p32-bf16"))
+
+
+@pytest.mark.parametrize("policy,budget,margin", [
+    ("gaussian", 0, 0.5), ("topk", 2048, 0.0), ("full", 0, 0.0), ("softmax", 0, 0.0)])
+def test_gqa1m_sampled_heads(gqa1m, policy, budget, margin):
+    check_decode(gqa1m, policy, 1.5, budget, margin, units=[(0, 0), (0, 7)])
+
+
+def test_batched_shuffled_with_appends():
+    spec = synth.workload("batch16-loguniform-4k-256k-p16-bf16")
+    built = Built(spec)
+    c = built.cache
+    units = [(0, 0), (7, 3), (15, 6)]
+    for step in range(3):
+        ks, vs = [], []
+        for b in range(spec.batch):
+            kk, vv = [], []
+            pos = int(c.seq_lens[b].item())
+            for j in range(spec.num_kv_heads):
+                d = built.draws[b][j]
+                k, v = synth.append_token(spec, b, j, pos, step, d.centroids, d.out_ch,
+                                          d.out_off, device="cuda")
+                kk.append(k)
+                vv.append(v)
+            ks.append(torch.stack(kk))
+            vs.append(torch.stack(vv))
+        K = torch.stack(ks).unsqueeze(2).contiguous()  # [B, Hkv, 1, d]
+        V = torch.stack(vs).unsqueeze(2).contiguous()
+        B.append(c, K, V)
+        for b in range(spec.batch):
+            built.K[b] = torch.cat([built.K[b], K[b]], dim=1)
+            built.V[b] = torch.cat([built.V[b], V[b]], dim=1)
+        q = torch.stack([synth.step_queries(spec, b, step, None, device="cuda")
+                         for b in range(spec.batch)]).contiguous()
+        check_decode(built, "gaussian", 1.5, 0, 0.5, q=q, units=units)
