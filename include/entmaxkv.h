@@ -185,6 +185,27 @@ int32_t entmaxkv_decode(const entmaxkv_config* cfg, const entmaxkv_cache* cache,
                         int32_t* n_sel, float* tau, float* delta, void* stream);
 
 /*
+ * entmaxkv_decode with CUDA events recorded between its stages, for timing
+ * one kernel on the stream it runs on. `events` holds ENTMAXKV_STAGE_EVENTS
+ * cudaEvent_t handles (as void*) created by the caller: events[0] is recorded
+ * before the first stage and events[i+1] after stage i, where the stages are
+ *   0 workspace clear, 1 page scoring (bbox or Gaussian), 2 selection (top-k,
+ *   τ̂ + bits, Gaussian cap), 3 pass A (K pages, scores, exact τ),
+ *   4 pass B (V pages, output) or the softmax kernel.
+ * A stage a policy does not run records back-to-back events. Everything else
+ * is as entmaxkv_decode.
+ */
+#define ENTMAXKV_STAGE_EVENTS 6
+int32_t entmaxkv_decode_profiled(const entmaxkv_config* cfg, const entmaxkv_cache* cache,
+                                 const void* q, const int32_t* seq_ids, int32_t n_seqs,
+                                 float alpha, int32_t policy, int32_t budget_tokens,
+                                 float margin, uint32_t flags,
+                                 void* workspace, size_t workspace_bytes,
+                                 float* out, int32_t* page_ids, int32_t page_ids_stride,
+                                 int32_t* n_sel, float* tau, float* delta, void* stream,
+                                 void* const* events);
+
+/*
  * Where the decode keeps its intermediate results inside the workspace, so
  * that tests and tools can read the page scores, τ̂ and the selection of the
  * last decode. Offsets are in bytes from the workspace base; a region the
@@ -197,6 +218,10 @@ int32_t entmaxkv_decode(const entmaxkv_config* cfg, const entmaxkv_cache* cache,
  */
 typedef struct {
   size_t bbox_u, bbox_uhat, gauss_ms, tauhat, sel_bitmap;
+  size_t page_zmax;    /* float [n_seqs][Hkv][cap_pages][group]: max z of each kept page
+                          (index = rank in page_ids), SIZE_MAX for SOFTMAX        */
+  int32_t cap_pages;   /* most pages one (sequence, KV head) can keep              */
+  int32_t splits;      /* blocks per (sequence, KV head) in the decode kernels     */
   size_t total;
 } entmaxkv_workspace_view;
 

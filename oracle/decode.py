@@ -66,13 +66,17 @@ def attend_pages(K, V, Q, alpha: float, page_size: int, page_ids):
 
 
 def decode_group(K, V, Q, alpha: float, policy: str, page_size: int,
-                 budget_tokens: int = 0, margin: float = 0.0):
+                 budget_tokens: int = 0, margin: float = 0.0, meta=None,
+                 diagnostics: bool = True):
     """Decode the g query heads that share one KV head.
 
     K, V: [n_tokens, d] stored keys/values (converted exactly to float64);
     Q: [g, d] stored queries. budget_tokens: top-k budget in tokens (k =
     budget // page_size pages) or, for the Gaussian policy, a cap in tokens
-    (0 = no cap). margin: Δ in score units (Gaussian policy).
+    (0 = no cap). margin: Δ in score units (Gaussian policy). meta: page
+    metadata of K already built by ``pages.page_metadata`` (else built here).
+    diagnostics=False skips the full-cache quantities (delta_exact, recall),
+    which need the full-cache entmax.
 
     Returns a dict:
       out [g, d], tau [g], page_ids (ascending logical ids), delta [g],
@@ -95,10 +99,10 @@ def decode_group(K, V, Q, alpha: float, policy: str, page_size: int,
                    delta_kind=policy, delta_exact=np.zeros(g),
                    recall=np.ones(g))
         return res
-    meta = pg.page_metadata(K, P)
+    if meta is None:
+        meta = pg.page_metadata(K, P)
     n_pages = meta["n"].size
     res["meta"] = meta
-    scores = K @ Q.T / math.sqrt(d)          # [n_tok, g]
 
     # ---- selection -------------------------------------------------------
     if policy in ("full", "softmax"):
@@ -140,28 +144,30 @@ def decode_group(K, V, Q, alpha: float, policy: str, page_size: int,
     idx = np.nonzero(keep)[0]
 
     # ---- attention over the kept set --------------------------------------
+    scores = (K @ Q.T / math.sqrt(d)) if (diagnostics or policy == "softmax") else None
     out = np.zeros((g, d))
     tau = np.full(g, np.nan)
     delta = np.zeros(g)
     delta_exact = np.zeros(g)
     recall = np.ones(g)
     beta = _beta(alpha) if policy != "softmax" else None
+    s_kept = K[idx] @ Q.T / math.sqrt(d) if scores is None else scores[idx]
     for h in range(g):
-        s = scores[:, h]
         if policy == "softmax":
-            p, lse = em.softmax(s)
+            p, lse = em.softmax(scores[:, h])
             out[h] = p @ V
             tau[h] = lse
             continue
-        p_full, tau_full = em.entmax(s, alpha)
-        supp = p_full > 0
-        delta_exact[h] = float(p_full[~keep].sum())
-        recall[h] = float((supp & keep).sum()) / float(supp.sum())
+        if diagnostics:
+            p_full, tau_full = em.entmax(scores[:, h], alpha)
+            supp = p_full > 0
+            delta_exact[h] = float(p_full[~keep].sum())
+            recall[h] = float((supp & keep).sum()) / float(supp.sum())
         if idx.size == 0:
             # Nothing kept: zero output, undefined threshold, all mass dropped.
             delta[h] = 1.0
             continue
-        p_k, tau_k = em.entmax(s[idx], alpha)
+        p_k, tau_k = em.entmax(s_kept[:, h], alpha)
         out[h] = p_k @ V[idx]
         tau[h] = tau_k
         dropped = np.setdiff1d(np.arange(n_pages), sel)

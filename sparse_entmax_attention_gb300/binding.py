@@ -28,7 +28,10 @@ DEV_CAND_OVERFLOW, DEV_TAU_NOCONV, DEV_BAD_SEQ_ID = 0x8, 0x10, 0x20
 
 # Symbols the header declares (kept in step with include/entmaxkv.h by a test).
 EXPORTS = ("entmaxkv_version", "entmaxkv_status_string", "entmaxkv_append",
-           "entmaxkv_workspace_bytes", "entmaxkv_decode", "entmaxkv_workspace_layout")
+           "entmaxkv_workspace_bytes", "entmaxkv_decode", "entmaxkv_decode_profiled",
+           "entmaxkv_workspace_layout")
+STAGE_EVENTS = 6
+STAGES = ("clear", "score", "select", "pass_a", "pass_b")
 
 
 class Config(ctypes.Structure):
@@ -49,7 +52,9 @@ class CacheView(ctypes.Structure):
 class WorkspaceView(ctypes.Structure):
     _fields_ = [("bbox_u", ctypes.c_size_t), ("bbox_uhat", ctypes.c_size_t),
                 ("gauss_ms", ctypes.c_size_t), ("tauhat", ctypes.c_size_t),
-                ("sel_bitmap", ctypes.c_size_t), ("total", ctypes.c_size_t)]
+                ("sel_bitmap", ctypes.c_size_t), ("page_zmax", ctypes.c_size_t),
+                ("cap_pages", ctypes.c_int32), ("splits", ctypes.c_int32),
+                ("total", ctypes.c_size_t)]
 
 
 _lib = None
@@ -75,6 +80,8 @@ def lib() -> ctypes.CDLL:
     L.entmaxkv_decode.restype = i32
     L.entmaxkv_decode.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(CacheView), vp, vp, i32,
                                   f32, i32, i32, f32, u32, vp, sz, vp, vp, i32, vp, vp, vp, vp]
+    L.entmaxkv_decode_profiled.restype = i32
+    L.entmaxkv_decode_profiled.argtypes = L.entmaxkv_decode.argtypes + [ctypes.POINTER(ctypes.c_void_p)]
     L.entmaxkv_workspace_layout.restype = i32
     L.entmaxkv_workspace_layout.argtypes = [ctypes.POINTER(Config), i32, i32, i32,
                                             ctypes.POINTER(WorkspaceView)]
@@ -194,8 +201,12 @@ def alloc_outputs(cache: PagedCache, n_seqs, policy, budget_tokens=0) -> DecodeO
 
 def decode(cache: PagedCache, q, alpha=1.5, policy="gaussian", budget_tokens=0, margin=0.0,
            flags=0, seq_ids=None, workspace=None, outputs: DecodeOutputs | None = None,
-           stream=None) -> DecodeOutputs:
-    """entmaxkv_decode: q [n_seqs, Hq, d] in the cache dtype."""
+           stream=None, events=None) -> DecodeOutputs:
+    """entmaxkv_decode: q [n_seqs, Hq, d] in the cache dtype.
+
+    With ``events`` (STAGE_EVENTS torch.cuda.Event objects) this calls
+    entmaxkv_decode_profiled, which records them between the stages.
+    """
     assert q.is_contiguous() and q.dtype == cache.dtype
     n_seqs = q.shape[0]
     pol = POLICIES.get(policy, policy)
@@ -204,9 +215,23 @@ def decode(cache: PagedCache, q, alpha=1.5, policy="gaussian", budget_tokens=0, 
     if outputs is None:
         outputs = alloc_outputs(cache, n_seqs, pol, budget_tokens)
     o = outputs
-    _check(lib().entmaxkv_decode(
-        ctypes.byref(cache.cfg), ctypes.byref(cache.view), _ptr(q), _ptr(seq_ids), n_seqs,
-        float(alpha), pol, int(budget_tokens), float(margin), int(flags), _ptr(workspace),
-        workspace.numel(), _ptr(o.out), _ptr(o.page_ids), o.page_ids.shape[-1], _ptr(o.n_sel),
-        _ptr(o.tau), _ptr(o.delta), _stream(stream)))
+    args = [ctypes.byref(cache.cfg), ctypes.byref(cache.view), _ptr(q), _ptr(seq_ids), n_seqs,
+            float(alpha), pol, int(budget_tokens), float(margin), int(flags), _ptr(workspace),
+            workspace.numel(), _ptr(o.out), _ptr(o.page_ids), o.page_ids.shape[-1], _ptr(o.n_sel),
+            _ptr(o.tau), _ptr(o.delta), _stream(stream)]
+    if events is None:
+        _check(lib().entmaxkv_decode(*args))
+    else:
+        assert len(events) == STAGE_EVENTS
+        arr = (ctypes.c_void_p * STAGE_EVENTS)(*[ctypes.c_void_p(e.cuda_event) for e in events])
+        _check(lib().entmaxkv_decode_profiled(*args, arr))
     return o
+
+
+def stage_events():
+    """STAGE_EVENTS timing events with their CUDA handles already created."""
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(STAGE_EVENTS)]
+    for e in evs:
+        e.record()
+    torch.cuda.synchronize()
+    return evs

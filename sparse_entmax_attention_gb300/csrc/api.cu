@@ -145,6 +145,9 @@ int32_t entmaxkv_workspace_layout(const entmaxkv_config* cfg, int32_t n_seqs, in
   view->gauss_ms = L.gauss_ms;
   view->tauhat = L.tauhat;
   view->sel_bitmap = L.bitmap;
+  view->page_zmax = L.pmax;
+  view->cap_pages = L.cap_pages;
+  view->splits = L.splits;
   view->total = L.total;
   return ENTMAXKV_OK;
 }
@@ -185,12 +188,12 @@ int32_t entmaxkv_append(const entmaxkv_config* cfg, const entmaxkv_cache* cache,
                                                                              : ENTMAXKV_ERR_CUDA;
 }
 
-int32_t entmaxkv_decode(const entmaxkv_config* cfg, const entmaxkv_cache* cache, const void* q,
-                        const int32_t* seq_ids, int32_t n_seqs, float alpha, int32_t policy,
-                        int32_t budget_tokens, float margin, uint32_t flags, void* workspace,
-                        size_t workspace_bytes, float* out, int32_t* page_ids,
-                        int32_t page_ids_stride, int32_t* n_sel, float* tau, float* delta,
-                        void* stream) {
+static int32_t decode_impl(const entmaxkv_config* cfg, const entmaxkv_cache* cache, const void* q,
+                           const int32_t* seq_ids, int32_t n_seqs, float alpha, int32_t policy,
+                           int32_t budget_tokens, float margin, uint32_t flags, void* workspace,
+                           size_t workspace_bytes, float* out, int32_t* page_ids,
+                           int32_t page_ids_stride, int32_t* n_sel, float* tau, float* delta,
+                           void* stream, void* const* events) {
   int st = check_config(cfg);
   if (st) return st;
   if ((st = check_cache(cache))) return st;
@@ -272,29 +275,62 @@ int32_t entmaxkv_decode(const entmaxkv_config* cfg, const entmaxkv_cache* cache,
   a.partial = at<float>(workspace, L.partial);
 
   cudaStream_t s = (cudaStream_t)stream;
-  if (cudaMemsetAsync(workspace, 0, L.ctrl_end, s) != cudaSuccess) return ENTMAXKV_ERR_CUDA;
-  cudaError_t e = cudaSuccess;
+  auto mark = [&](int i) -> cudaError_t {
+    return events ? cudaEventRecord((cudaEvent_t)events[i], s) : cudaSuccess;
+  };
+  cudaError_t e = mark(0);
+  if (e == cudaSuccess) e = cudaMemsetAsync(workspace, 0, L.ctrl_end, s);
+  if (e == cudaSuccess) e = mark(1);
   const int dt = cfg->kv_dtype;
-  switch (policy) {
-    case ENTMAXKV_POLICY_FULL:
-      if ((e = launch_pass_a(a, dt, s)) == cudaSuccess) e = launch_pass_b(a, dt, s);
-      break;
-    case ENTMAXKV_POLICY_TOPK:
-      if ((e = launch_bbox(a, dt, kSmCount, s)) == cudaSuccess && (e = launch_topk(a, 0, s)) == cudaSuccess &&
-          (e = launch_pass_a(a, dt, s)) == cudaSuccess)
-        e = launch_pass_b(a, dt, s);
-      break;
-    case ENTMAXKV_POLICY_GAUSSIAN:
-      if ((e = launch_gauss(a, dt, kSmCount, s)) == cudaSuccess && (e = launch_tauhat(a, s)) == cudaSuccess &&
-          (L.gcap == 0 || (e = launch_topk(a, 1, s)) == cudaSuccess) &&
-          (e = launch_pass_a(a, dt, s)) == cudaSuccess)
-        e = launch_pass_b(a, dt, s);
-      break;
-    default:
-      e = launch_softmax(a, dt, s);
-      break;
+  // stage 1: page scoring
+  if (e == cudaSuccess) {
+    if (policy == ENTMAXKV_POLICY_TOPK) e = launch_bbox(a, dt, kSmCount, s);
+    else if (policy == ENTMAXKV_POLICY_GAUSSIAN) e = launch_gauss(a, dt, kSmCount, s);
   }
+  if (e == cudaSuccess) e = mark(2);
+  // stage 2: selection
+  if (e == cudaSuccess) {
+    if (policy == ENTMAXKV_POLICY_TOPK) {
+      e = launch_topk(a, 0, s);
+    } else if (policy == ENTMAXKV_POLICY_GAUSSIAN) {
+      e = launch_tauhat(a, s);
+      if (e == cudaSuccess && L.gcap > 0) e = launch_topk(a, 1, s);
+    }
+  }
+  if (e == cudaSuccess) e = mark(3);
+  // stage 3: pass A
+  if (e == cudaSuccess && policy != ENTMAXKV_POLICY_SOFTMAX) e = launch_pass_a(a, dt, s);
+  if (e == cudaSuccess) e = mark(4);
+  // stage 4: pass B or the softmax kernel
+  if (e == cudaSuccess) e = policy == ENTMAXKV_POLICY_SOFTMAX ? launch_softmax(a, dt, s) : launch_pass_b(a, dt, s);
+  if (e == cudaSuccess) e = mark(5);
   return e == cudaSuccess ? ENTMAXKV_OK : ENTMAXKV_ERR_CUDA;
+}
+
+int32_t entmaxkv_decode(const entmaxkv_config* cfg, const entmaxkv_cache* cache, const void* q,
+                        const int32_t* seq_ids, int32_t n_seqs, float alpha, int32_t policy,
+                        int32_t budget_tokens, float margin, uint32_t flags, void* workspace,
+                        size_t workspace_bytes, float* out, int32_t* page_ids,
+                        int32_t page_ids_stride, int32_t* n_sel, float* tau, float* delta,
+                        void* stream) {
+  return decode_impl(cfg, cache, q, seq_ids, n_seqs, alpha, policy, budget_tokens, margin, flags,
+                     workspace, workspace_bytes, out, page_ids, page_ids_stride, n_sel, tau, delta,
+                     stream, nullptr);
+}
+
+int32_t entmaxkv_decode_profiled(const entmaxkv_config* cfg, const entmaxkv_cache* cache,
+                                 const void* q, const int32_t* seq_ids, int32_t n_seqs,
+                                 float alpha, int32_t policy, int32_t budget_tokens, float margin,
+                                 uint32_t flags, void* workspace, size_t workspace_bytes,
+                                 float* out, int32_t* page_ids, int32_t page_ids_stride,
+                                 int32_t* n_sel, float* tau, float* delta, void* stream,
+                                 void* const* events) {
+  if (!events) return ENTMAXKV_ERR_INVALID_ARG;
+  for (int i = 0; i < ENTMAXKV_STAGE_EVENTS; ++i)
+    if (!events[i]) return ENTMAXKV_ERR_INVALID_ARG;
+  return decode_impl(cfg, cache, q, seq_ids, n_seqs, alpha, policy, budget_tokens, margin, flags,
+                     workspace, workspace_bytes, out, page_ids, page_ids_stride, n_sel, tau, delta,
+                     stream, events);
 }
 
 }  // extern "C"
