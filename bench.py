@@ -1,0 +1,460 @@
+#!/usr/bin/env python
+"""EntmaxKV decode-step benchmark on one GB300 (or N independent replicas).
+
+One step = append one new token to every sequence (page write + metadata
+update) and decode it with the Gaussian-aware selector (Δ = 0.5): page
+scoring, τ̂ solve and selection, sparse α-entmax over the kept pages. The
+workload is the 1M-token GQA cache (32 query / 8 KV heads, d = 128, page 32,
+bf16 K/V; seeded synthetic data). Besides the headline step the run times the
+top-k policy (2048 tokens), the full-cache entmax decode and the full-cache
+softmax decode on the same cache, the dominant kernel on its own stream, an
+end-to-end step from pinned host buffers, and the float64 oracle on a bounded
+sample of host cores.
+
+Prints one JSON line (rank 0). `--impl reference` times the oracle instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "μs/decode step and KV GB/s at 1M ctx; fraction of 8 TB/s HBM roofline"
+WORKLOAD = "gqa32x8-d128-1m-p32-bf16"
+ALPHA, MARGIN, TOPK_BUDGET = 1.5, 0.5, 2048
+NOMINAL_HBM_GBS = 8000.0
+L2_FLUSH_BYTES = 512 << 20   # > 129 MB L2: written between timed steps
+# DRAM bytes per launch of the dominant kernel from an ncu capture of the
+# same kernel, scaled to a full launch; None until the kernel is captured.
+NCU_TRAFFIC_PER_LAUNCH = None
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true", help="headline step only")
+    return ap.parse_args()
+
+
+# --------------------------------------------------------------------------
+# clocks
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.QUERY,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# --------------------------------------------------------------------------
+# our arm
+
+def algorithmic_bytes(wl, policy, o, ws, view):
+    """Bytes the method must move for one decode (page metadata it scans,
+    K pages it gathers, V pages with some p > 0, q in, outputs out)."""
+    import torch
+    spec, cache = wl.spec, wl.cache
+    P, d, Hkv, G = spec.page_size, spec.head_dim, spec.num_kv_heads, spec.group
+    el = torch.tensor([], dtype=spec.kv_dtype).element_size()
+    n_pages = sum(-(-int(L) // P) for L in cache.seq_lens.tolist())
+    page_kv = P * d * el                           # one (page, KV head) slab
+    io = spec.batch * spec.num_q_heads * d * (el + 4) + spec.batch * spec.num_q_heads * 8
+    if policy in ("full_dense", "softmax"):
+        return 2 * n_pages * Hkv * page_kv + io, {"k_pages": n_pages * Hkv, "v_pages": n_pages * Hkv}
+    meta = 0
+    if policy == "gaussian":
+        meta = n_pages * Hkv * d * 4 * 2           # mean + m2, fp32
+    elif policy == "topk":
+        meta = n_pages * Hkv * d * el * 2          # kmin + kmax
+    n_sel = o.n_sel.cpu()
+    k_pages = int(n_sel.sum())
+    # V pages actually read: some head's page max z above its τ
+    cap = view.cap_pages
+    pm = ws[view.page_zmax: view.page_zmax + spec.batch * Hkv * cap * G * 4].view(torch.float32)
+    pm = pm.view(spec.batch, Hkv, cap, G).cpu()
+    tau = o.tau.view(spec.batch, Hkv, G).cpu()
+    v_pages = 0
+    for b in range(spec.batch):
+        for j in range(Hkv):
+            n = int(n_sel[b, j])
+            if policy == "full_skipv":
+                n = -(-int(cache.seq_lens[b]) // P)
+            v_pages += int((pm[b, j, :n] > tau[b, j][None, :]).any(dim=1).sum())
+    return meta + (k_pages + v_pages) * page_kv + io, {"k_pages": k_pages, "v_pages": v_pages,
+                                                       "meta_bytes": meta}
+
+
+def run_ours(args, rank, world):
+    import torch
+    from sparse_entmax_attention_gb300 import binding as B
+    from sparse_entmax_attention_gb300 import runner, synth
+
+    local = int(os.environ.get("LOCAL_RANK", 0))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    K, W = args.steps, args.warmup
+    spec = synth.workload(WORKLOAD)
+    n_append = 2 * (K + W) + 4
+    wl = runner.Workload(spec, seed=0, device=dev, extra_steps=n_append)
+    cache = wl.cache
+    peaks, peak_kind = measured_peaks()
+    # inputs of every step, resident in HBM before timing
+    toks = [wl.step_tokens(i) for i in range(n_append)]
+    qs = [wl.step_queries(i) for i in range(K + W)]
+    kbuf, vbuf = toks[0][0].clone(), toks[0][1].clone()
+    qbuf = qs[0].clone()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    n_app = [0]
+
+    def set_step(i):
+        kbuf.copy_(toks[n_app[0]][0])
+        vbuf.copy_(toks[n_app[0]][1])
+        qbuf.copy_(qs[i % len(qs)])
+
+    ws_g = B.alloc_workspace(cache, spec.batch, "gaussian", 0)
+    out_g = B.alloc_outputs(cache, spec.batch, "gaussian", 0)
+
+    def step():
+        B.append(cache, kbuf, vbuf)
+        B.decode(cache, qbuf, ALPHA, "gaussian", 0, MARGIN, workspace=ws_g, outputs=out_g)
+
+    # eager warm-up (also loads every kernel), then capture one step as a graph
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        set_step(0)
+        step()
+        n_app[0] += 1
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+
+    def timed(fn, n, tag_steps):
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        for i in range(n):
+            tag_steps(i)
+            flush.zero_()
+            starts[i].record()
+            fn()
+            ends[i].record()
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) * 1e3 for a, b in zip(starts, ends)]  # μs
+
+    def adv(i):
+        set_step(i)
+        n_app[0] += 1
+
+    # graph capture appended nothing (capture does not execute); the counter
+    # tracks the appends the replays perform.
+    timed(graph.replay, W, adv)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clk = ClockSampler(local)
+    clk.start()
+    t0 = time.perf_counter()
+    step_us = timed(graph.replay, K, lambda i: adv(W + i))
+    wall = time.perf_counter() - t0
+    clocks = clk.stop()
+    if world > 1:
+        t = torch.tensor([statistics.mean(step_us)], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        mean_us = float(t.item())
+    else:
+        mean_us = statistics.mean(step_us)
+    assert cache.device_status() & ~B.DEV_CAND_OVERFLOW == 0, hex(cache.device_status())
+
+    view_g = B.workspace_layout(cache, spec.batch, "gaussian", 0)
+    bytes_g, counts_g = algorithmic_bytes(wl, "gaussian", out_g, ws_g, view_g)
+    append_bytes = spec.batch * spec.num_kv_heads * spec.head_dim * (2 * 2 + 2 * 2 + 2 * 4 * 2)
+    step_bytes = bytes_g + append_bytes
+    res = {
+        "metric": METRIC,
+        "value": round(mean_us, 2),
+        "unit": "us/step",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": round(mean_us / 1e3, 5),
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded generator: page centroids + noise, needles, outlier channels)",
+        "config": {"workload": WORKLOAD, "batch": 1, "context": spec.context_lens[0],
+                   "q_heads": spec.num_q_heads, "kv_heads": spec.num_kv_heads,
+                   "head_dim": spec.head_dim, "page_size": spec.page_size, "alpha": ALPHA,
+                   "policy": "gaussian", "margin": MARGIN,
+                   "step": "append 1 token + Gaussian-selector decode (CUDA graph)",
+                   "l2": "512 MiB written between timed steps (flush); per-step CUDA events",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "kv_gbs": round(step_bytes / (mean_us * 1e-6) / 1e9, 1),
+        "frac_8tbs": round(step_bytes / (mean_us * 1e-6) / 1e9 / NOMINAL_HBM_GBS, 4),
+        "frac_measured_hbm": round(step_bytes / (mean_us * 1e-6) / 1e9 / peaks["hbm_gbs"], 4),
+        "bytes_per_step": step_bytes,
+        "selected": counts_g,
+        "wall_s_timed_loop": round(wall, 4),
+        "gpu_launches": 6 * K,
+        "clocks": clocks,
+    }
+    if rank != 0:
+        return None
+    if not args.no_extras:
+        res["policies"] = policy_table(wl, B, flush, qbuf, timed, K, peaks)
+        res["roofline"] = roofline(wl, B, flush, qbuf, K, peaks, peak_kind)
+        res["e2e"] = e2e(wl, B, toks, qs, n_app, K, W)
+    if not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(wl, qbuf)
+    return res
+
+
+def policy_table(wl, B, flush, qbuf, timed, K, peaks):
+    import torch
+    cache, spec = wl.cache, wl.spec
+    rows = {}
+    cases = [("gaussian", "gaussian", 0, 0), ("topk", "topk", TOPK_BUDGET, 0),
+             ("full_dense", "full", 0, B.FLAG_DENSE_V), ("full_skipv", "full", 0, 0),
+             ("softmax", "softmax", 0, 0)]
+    for name, pol, budget, flags in cases:
+        ws = B.alloc_workspace(cache, spec.batch, pol, budget)
+        o = B.alloc_outputs(cache, spec.batch, pol, budget)
+        fn = lambda: B.decode(cache, qbuf, ALPHA, pol, budget, MARGIN, flags, workspace=ws, outputs=o)
+        fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        us = timed(g.replay, K, lambda i: None)
+        mean = statistics.mean(us)
+        view = B.workspace_layout(cache, spec.batch, pol, budget)
+        nbytes, counts = algorithmic_bytes(wl, name, o, ws, view)
+        rows[name] = {"us": round(mean, 2), "bytes": nbytes,
+                      "gbs": round(nbytes / (mean * 1e-6) / 1e9, 1),
+                      "frac_8tbs": round(nbytes / (mean * 1e-6) / 1e9 / NOMINAL_HBM_GBS, 4),
+                      **counts}
+        del ws
+    for name in ("topk", "full_dense", "full_skipv", "softmax"):
+        rows[name]["gaussian_speedup"] = round(rows[name]["us"] / rows["gaussian"]["us"], 2)
+    return rows
+
+
+def roofline(wl, B, flush, qbuf, K, peaks, peak_kind):
+    """Dominant kernel = Gaussian page scoring (streams mean + m2 of every
+    page): its per-launch time from CUDA events recorded around it on the
+    stream it runs on (the library's stage-timed decode)."""
+    import torch
+    cache, spec = wl.cache, wl.spec
+    ws = B.alloc_workspace(cache, spec.batch, "gaussian", 0)
+    o = B.alloc_outputs(cache, spec.batch, "gaussian", 0)
+    evs = B.stage_events()
+    per = {n: [] for n in B.STAGES}
+    for i in range(K + 1):
+        flush.zero_()
+        B.decode(cache, qbuf, ALPHA, "gaussian", 0, MARGIN, workspace=ws, outputs=o, events=evs)
+        torch.cuda.synchronize()
+        if i == 0:
+            continue
+        for k, n in enumerate(B.STAGES):
+            per[n].append(evs[k].elapsed_time(evs[k + 1]) * 1e3)
+    stages = {n: round(statistics.mean(v), 2) for n, v in per.items()}
+    n_pages = -(-int(cache.seq_lens[0]) // spec.page_size)
+    alg = n_pages * spec.num_kv_heads * spec.head_dim * 4 * 2   # mean + m2 bytes per launch
+    t = stages["score"] * 1e-6
+    ach = alg / t / 1e9
+    return {"kernel": "gauss_kernel (Gaussian page scoring)", "bound": "hbm",
+            "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": round(ach / peaks["hbm_gbs"], 4), "peak_kind": peak_kind + " (copy, burst)",
+            "traffic": NCU_TRAFFIC_PER_LAUNCH, "algorithmic_bytes": alg,
+            "stage_us": stages}
+
+
+def e2e(wl, B, toks, qs, n_app, K, W):
+    """Same step through the public API from pinned host buffers: H2D of the
+    new token and the queries, append + decode, D2H of out/τ/δ/n_sel."""
+    import torch
+    cache, spec = wl.cache, wl.spec
+    hk = [toks[n_app[0] + i][0].cpu().pin_memory() for i in range(K + W)]
+    hv = [toks[n_app[0] + i][1].cpu().pin_memory() for i in range(K + W)]
+    hq = [qs[i % len(qs)].cpu().pin_memory() for i in range(K + W)]
+    dk, dv, dq = hk[0].cuda(), hv[0].cuda(), hq[0].cuda()
+    ws = B.alloc_workspace(cache, spec.batch, "gaussian", 0)
+    o = B.alloc_outputs(cache, spec.batch, "gaussian", 0)
+    ho = [torch.empty_like(t, device="cpu").pin_memory() for t in (o.out, o.tau, o.delta, o.n_sel)]
+    us = []
+    for i in range(K + W):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        dk.copy_(hk[i], non_blocking=True)
+        dv.copy_(hv[i], non_blocking=True)
+        dq.copy_(hq[i], non_blocking=True)
+        B.append(cache, dk, dv)
+        B.decode(cache, dq, ALPHA, "gaussian", 0, MARGIN, workspace=ws, outputs=o)
+        for h, d in zip(ho, (o.out, o.tau, o.delta, o.n_sel)):
+            h.copy_(d, non_blocking=True)
+        b.record()
+        b.synchronize()
+        if i >= W:
+            us.append(a.elapsed_time(b) * 1e3)
+    h2d = sum(t.numel() * t.element_size() for t in (hk[0], hv[0], hq[0]))
+    d2h = sum(t.numel() * t.element_size() for t in ho)
+    return {"value": round(statistics.mean(us), 2), "unit": "us/step",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "how": "per-step CUDA events around H2D + append + decode + D2H (eager API calls)"}
+
+
+# --------------------------------------------------------------------------
+# oracle (CPU) legs
+
+def host_sample(wl, qdev, kvh=0):
+    """Stored K/V of one KV head (all pages, via the block table) and its g
+    queries, as float64 host arrays."""
+    import torch
+    cache, spec = wl.cache, wl.spec
+    L = int(cache.seq_lens[0])
+    n_pages = -(-L // spec.page_size)
+    phys = cache.block_table[0, :n_pages].long()
+    K = cache.k_pool[phys, kvh].reshape(-1, spec.head_dim)[:L].double().cpu().numpy()
+    V = cache.v_pool[phys, kvh].reshape(-1, spec.head_dim)[:L].double().cpu().numpy()
+    g = spec.group
+    Q = qdev[0, kvh * g:(kvh + 1) * g].double().cpu().numpy()
+    return K, V, Q
+
+
+def oracle_step_us(K, V, Q, P, n_kv_heads, meta):
+    from oracle import decode as odec
+    t0 = time.perf_counter()
+    odec.decode_group(K, V, Q, ALPHA, "gaussian", P, 0, MARGIN, meta=meta, diagnostics=False)
+    dt = time.perf_counter() - t0
+    return dt * n_kv_heads * 1e6, dt
+
+
+def cpu_baseline(wl, qdev):
+    from oracle import pages as opg
+    K, V, Q = host_sample(wl, qdev)
+    meta = opg.page_metadata(K, wl.spec.page_size)   # built once, like the cache metadata
+    us, dt = oracle_step_us(K, V, Q, wl.spec.page_size, wl.spec.num_kv_heads, meta)
+    return {"value": round(us, 1), "unit": "us/step", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"1 of {wl.spec.num_kv_heads} KV heads (its {wl.spec.group} query heads) of one "
+                      f"Gaussian decode step at 1M tokens, float64 numpy ({dt:.1f} s), scaled x"
+                      f"{wl.spec.num_kv_heads}; page metadata prebuilt; BLAS default threads"}
+
+
+def run_reference(args, rank, world):
+    """The oracle as the reference arm: each step is the float64 Gaussian
+    decode of one KV head of the 1M workload, scaled to all KV heads."""
+    if rank != 0:
+        return None
+    import torch
+    from oracle import pages as opg
+    from sparse_entmax_attention_gb300 import synth
+    spec = synth.workload(WORKLOAD)
+    q = synth.queries(spec, 0, 0, "cpu").unsqueeze(0)
+    hd = synth.HeadDraws(spec, 0, 0, q[0, :spec.group], 0, "cpu")
+    K, V = hd.k.double().numpy(), hd.v.double().numpy()
+    Q = q[0, :spec.group].double().numpy()
+    meta = opg.page_metadata(K, spec.page_size)
+    for _ in range(args.warmup):
+        oracle_step_us(K, V, Q, spec.page_size, spec.num_kv_heads, meta)
+    t0 = time.perf_counter()
+    us = [oracle_step_us(K, V, Q, spec.page_size, spec.num_kv_heads, meta)[0] for _ in range(args.steps)]
+    wall = time.perf_counter() - t0
+    v = statistics.mean(us)
+    return {"impl": "reference", "metric": METRIC, "value": round(v, 1), "unit": "us/step",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(v / 1e3, 3), "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (same seeded generator, CPU draws)",
+            "config": {"workload": WORKLOAD, "policy": "gaussian", "margin": MARGIN, "alpha": ALPHA},
+            "cpu_baseline": {"value": round(v, 1), "unit": "us/step", "cores": os.cpu_count(),
+                             "kind": "oracle",
+                             "sample": f"1 of {spec.num_kv_heads} KV heads per step, scaled"},
+            "e2e": {"value": round(v, 1), "unit": "us/step", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "wall_s_timed_loop": round(wall, 3)}
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        res = run_reference(args, rank, world)
+    else:
+        if world > 1:
+            import torch
+            torch.distributed.init_process_group("nccl")
+        res = run_ours(args, rank, world)
+        if world > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+    if res is not None and rank == 0:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()
