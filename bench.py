@@ -310,6 +310,7 @@ def roofline(wl, B, flush, qbuf, K, peaks, peak_kind):
     cache, spec = wl.cache, wl.spec
     ws = B.alloc_workspace(cache, spec.batch, "gaussian", 0)
     o = B.alloc_outputs(cache, spec.batch, "gaussian", 0)
+    view = B.workspace_layout(cache, spec.batch, "gaussian", 0)
     evs = B.stage_events()
     per = {n: [] for n in B.STAGES}
     for i in range(K + 1):
@@ -325,11 +326,12 @@ def roofline(wl, B, flush, qbuf, K, peaks, peak_kind):
     alg = n_pages * spec.num_kv_heads * spec.head_dim * 4 * 2   # mean + m2 bytes per launch
     t = stages["score"] * 1e-6
     ach = alg / t / 1e9
+    it = ws[view.tauhat_iters: view.tauhat_iters + spec.batch * spec.num_q_heads * 4].view(torch.int32)
     return {"kernel": "gauss_kernel (Gaussian page scoring)", "bound": "hbm",
             "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": round(ach / peaks["hbm_gbs"], 4), "peak_kind": peak_kind + " (copy, burst)",
             "traffic": NCU_TRAFFIC_PER_LAUNCH, "algorithmic_bytes": alg,
-            "stage_us": stages}
+            "stage_us": stages, "tauhat_iters_mean": round(float(it.float().mean()), 2)}
 
 
 def e2e(wl, B, toks, qs, n_app, K, W):

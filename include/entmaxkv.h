@@ -215,9 +215,11 @@ int32_t entmaxkv_decode_profiled(const entmaxkv_config* cfg, const entmaxkv_cach
  *   gauss_ms   float2 [n_seqs][Hq][max_pages_per_seq]  (m_p, ς_p) = (α−1)(μ_p, σ_p)
  *   tauhat     float [n_seqs][Hq]                      τ̂ on the z scale
  *   sel_bitmap uint32 [n_seqs][Hkv][ceil(max_pages_per_seq/32)]
+ *   tauhat_iters int32 [n_seqs][Hq]                    iterations of the τ̂ solve
  */
 typedef struct {
   size_t bbox_u, bbox_uhat, gauss_ms, tauhat, sel_bitmap;
+  size_t tauhat_iters;
   size_t page_zmax;    /* float [n_seqs][Hkv][cap_pages][group]: max z of each kept page
                           (index = rank in page_ids), SIZE_MAX for SOFTMAX        */
   int32_t cap_pages;   /* most pages one (sequence, KV head) can keep              */

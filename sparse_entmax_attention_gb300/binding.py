@@ -52,7 +52,8 @@ class CacheView(ctypes.Structure):
 class WorkspaceView(ctypes.Structure):
     _fields_ = [("bbox_u", ctypes.c_size_t), ("bbox_uhat", ctypes.c_size_t),
                 ("gauss_ms", ctypes.c_size_t), ("tauhat", ctypes.c_size_t),
-                ("sel_bitmap", ctypes.c_size_t), ("page_zmax", ctypes.c_size_t),
+                ("sel_bitmap", ctypes.c_size_t), ("tauhat_iters", ctypes.c_size_t),
+                ("page_zmax", ctypes.c_size_t),
                 ("cap_pages", ctypes.c_int32), ("splits", ctypes.c_int32),
                 ("total", ctypes.c_size_t)]
 

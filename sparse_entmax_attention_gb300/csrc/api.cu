@@ -12,9 +12,9 @@ constexpr int kTargetBlocks = 4 * kSmCount;   // decode blocks per launch to aim
 
 struct Layout {
   size_t zmax, mmax, cnt_a, cnt_b, cand_cnt, kept_mass, dbar, bitmap, ctrl_end;
-  size_t tauhat, tau_ws, nsel_ws, sel_list, bbox_u, bbox_uhat, gauss_ms, cand, z, pmax, partial;
+  size_t tauhat, tau_ws, nsel_ws, sel_list, bbox_u, bbox_uhat, gauss_ms, cand, z, pmax, partial, diag;
   size_t total;
-  int splits, cap_pages, words, kpages, gcap;
+  int splits, cap_pages, words, kpages, gcap, pstride;
 };
 
 static size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -95,10 +95,12 @@ static int compute_layout(const entmaxkv_config* c, int S, int policy, int budge
   L.bbox_u = policy == ENTMAXKV_POLICY_TOPK ? take(nq * (size_t)maxp * 4) : none;
   L.bbox_uhat = policy == ENTMAXKV_POLICY_TOPK ? take(nk * (size_t)maxp * 4) : none;
   L.gauss_ms = policy == ENTMAXKV_POLICY_GAUSSIAN ? take(nq * (size_t)maxp * 8) : none;
-  L.cand = entmax ? take(nq * (size_t)kCandCap * 4) : none;
+  L.cand = entmax ? take(nq * (size_t)kCandPages * 4) : none;
   L.z = entmax ? take(nk * (size_t)cap * P * G * 4) : none;
   L.pmax = entmax ? take(nk * (size_t)cap * G * 4) : none;
-  L.partial = take(nk * (size_t)L.splits * G * (D + 2) * 4);
+  L.pstride = (G * D + 2 * G + 3) & ~3;
+  L.partial = take(nk * (size_t)L.splits * L.pstride * 4);
+  L.diag = take(nq * 4);
   L.total = off;
   return ENTMAXKV_OK;
 }
@@ -145,6 +147,7 @@ int32_t entmaxkv_workspace_layout(const entmaxkv_config* cfg, int32_t n_seqs, in
   view->gauss_ms = L.gauss_ms;
   view->tauhat = L.tauhat;
   view->sel_bitmap = L.bitmap;
+  view->tauhat_iters = policy == ENTMAXKV_POLICY_GAUSSIAN ? L.diag : (size_t)-1;
   view->page_zmax = L.pmax;
   view->cap_pages = L.cap_pages;
   view->splits = L.splits;
@@ -269,10 +272,12 @@ static int32_t decode_impl(const entmaxkv_config* cfg, const entmaxkv_cache* cac
   a.bbox_u = at<float>(workspace, L.bbox_u);
   a.bbox_uhat = at<float>(workspace, L.bbox_uhat);
   a.gauss_ms = at<float2>(workspace, L.gauss_ms);
-  a.cand = at<float>(workspace, L.cand);
+  a.cand = at<int32_t>(workspace, L.cand);
   a.z = at<float>(workspace, L.z);
   a.pmax = at<float>(workspace, L.pmax);
   a.partial = at<float>(workspace, L.partial);
+  a.pstride = L.pstride;
+  a.diag = at<int32_t>(workspace, L.diag);
 
   cudaStream_t s = (cudaStream_t)stream;
   auto mark = [&](int i) -> cudaError_t {

@@ -13,8 +13,8 @@ namespace ekv {
 
 constexpr int kThreads = 256;       // decode / scoring blocks: 8 warps
 constexpr int kWarps = kThreads / 32;
-constexpr int kCandCap = 16384;     // exact-τ candidates kept per query head
-constexpr int kWarpCand = 1024;     // candidates a solver warp keeps in shared memory
+constexpr int kCandPages = 4096;    // candidate pages listed per query head for the exact τ
+constexpr int kSolveCap = 8192;     // candidate scores the τ solver keeps in shared memory
 constexpr int kListCap = 1024;      // selected pages one decode block handles
 constexpr int kTauhatCluster = 8;   // blocks per τ̂ cluster (one cluster per query head)
 
@@ -50,7 +50,7 @@ struct DecodeArgs {
   uint32_t* mmax;      // [S][Hq]   ordered-encoded max m (Gaussian)
   int32_t* cnt_a;      // [S][Hkv]  blocks of pass A done
   int32_t* cnt_b;      // [S][Hkv]  blocks of pass B done
-  int32_t* cand_cnt;   // [S][Hq]
+  int32_t* cand_cnt;   // [S][Hq]   candidate pages listed
   float* kept_mass;    // [S][Hq]   Gaussian model mass of the kept pages
   float* dbar;         // [S][Hq]   top-k certified dropped mass
   uint32_t* bitmap;    // [S][Hkv][words]
@@ -62,10 +62,12 @@ struct DecodeArgs {
   float* bbox_u;       // [S][Hq][maxp]
   float* bbox_uhat;    // [S][Hkv][maxp]
   float2* gauss_ms;    // [S][Hq][maxp]
-  float* cand;         // [S][Hq][kCandCap]
+  int32_t* cand;       // [S][Hq][kCandPages] ranks of candidate pages
   float* z;            // [S][Hkv][cap_pages][P][G]
   float* pmax;         // [S][Hkv][cap_pages][G]
-  float* partial;      // [S][Hkv][splits][G][D + 2]
+  float* partial;      // [S][Hkv][splits][pstride]: acc [G][D], then (m, l) per head
+  int pstride;         // floats per split partial: G·D + 2G rounded up to 4
+  int32_t* diag;       // [S][Hq] τ̂ iterations (Gaussian)
 };
 
 struct AppendArgs {

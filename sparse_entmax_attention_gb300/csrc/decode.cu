@@ -69,48 +69,60 @@ __device__ void block_page_range(const DecodeArgs& a, int s, int kvh, int n_page
 }
 
 // ---------------------------------------------------------------------------
-// Exact τ of one query head by one warp.
+// Exact τ of one query head by one warp. Candidates are the scores above
+// T0 = z_max − 1 (no other score can carry weight); normally they sit in
+// shared memory, and only when they do not fit does the solver walk the
+// candidate pages in global memory on every iteration.
 
-struct TauSource {
-  const float* wc;   // compacted candidates in shared memory (mode 0)
+struct SolveSrc {
+  const float* zs;      // compacted candidates (shared memory)
   int m;
-  const float* cand; // candidate list in global memory (mode 1)
-  int nc;
-  const float* z;    // all scores of the head (mode 2): z[(rank·P + t)·G + hg]
-  int n_sel, P, G, hg;
-  int mode;
+  bool big;             // candidates did not fit: walk the pages instead
+  const int32_t* pages; // candidate page ranks (nullptr = every rank < np)
+  int np;
+  const float* zbase;   // z of this (sequence, KV head): [rank][P][G]
+  const float* pmbase;  // page max z: [rank][G]
+  int P, G, hg;
+  float T0;
 };
 
-__device__ __forceinline__ int tau_src_count(const TauSource& S) {
-  return S.mode == 0 ? S.m : (S.mode == 1 ? S.nc : S.n_sel * S.P);
-}
-__device__ __forceinline__ float tau_src_get(const TauSource& S, int i) {
-  if (S.mode == 0) return S.wc[i];
-  if (S.mode == 1) return __ldcg(S.cand + i);
-  return __ldcg(S.z + (size_t)i * S.G + S.hg);
+template <class F>
+__device__ __forceinline__ void for_each_cand(const SolveSrc& S, F&& f) {
+  const int lane = threadIdx.x & 31;
+  if (!S.big) {
+    for (int i = lane; i < S.m; i += 32) f(S.zs[i]);
+    return;
+  }
+  for (int k = 0; k < S.np; ++k) {
+    const int rank = S.pages ? __ldcg(S.pages + k) : k;
+    if (!(__ldcg(S.pmbase + (size_t)rank * S.G + S.hg) > S.T0)) continue;
+    const float* zr = S.zbase + (size_t)rank * S.P * S.G;
+    for (int t = lane; t < S.P; t += 32) {
+      const float v = __ldcg(zr + t * S.G + S.hg);
+      if (v > S.T0) f(v);
+    }
+  }
 }
 
-__device__ double solve_tau_warp(const TauSource& S, double tau0, float beta, bool& ok) {
-  const int lane = threadIdx.x & 31;
-  const int n = tau_src_count(S);
+__device__ double solve_tau_warp(const SolveSrc& S, double tau0, float beta, bool& ok) {
   double tau = tau0;
   ok = false;
+  const bool b2 = beta == 2.0f, b1 = beta == 1.0f;
   for (int it = 0; it < kTauIters; ++it) {
     double k = 0.0, s1 = 0.0, s2 = 0.0, sb = 0.0, sb1 = 0.0, mn = CUDART_INF;
-    for (int i = lane; i < n; i += 32) {
-      const double zv = (double)tau_src_get(S, i);
-      if (zv > tau) {
-        const double y = zv - tau;
+    for_each_cand(S, [&](float zf) {
+      const double y = (double)zf - tau;
+      if (y > 0.0) {
         k += 1.0;
         s1 += y;
         s2 += y * y;
         mn = fmin(mn, y);
-        if (beta != 2.0f && beta != 1.0f) {
+        if (!b2 && !b1) {
           sb += pow(y, (double)beta);
           sb1 += pow(y, (double)beta - 1.0);
         }
       }
-    }
+    });
     k = warp_sum(k);
     s1 = warp_sum(s1);
     s2 = warp_sum(s2);
@@ -119,7 +131,7 @@ __device__ double solve_tau_warp(const TauSource& S, double tau0, float beta, bo
     mn = warp_min_d(mn);
     if (k == 0.0) break;  // cannot happen while τ < z_max
     double next;
-    if (beta == 2.0f) {
+    if (b2) {
       // root t = τ + δ of Σ_S (y − δ)² = 1 on the branch δ ≤ min y
       const double disc = s1 * s1 - k * (s2 - 1.0);
       if (disc >= 0.0) {
@@ -131,7 +143,7 @@ __device__ double solve_tau_warp(const TauSource& S, double tau0, float beta, bo
         }
       }
       next = tau + (s2 - 1.0) / (2.0 * s1);
-    } else if (beta == 1.0f) {
+    } else if (b1) {
       const double d = (s1 - 1.0) / k;
       if (d >= 0.0 && d <= mn) {
         tau += d;
@@ -168,7 +180,7 @@ __global__ void __launch_bounds__(kThreads) pass_a_kernel(DecodeArgs a) {
   __shared__ float thr_sh[8];
   __shared__ float th_sh[8];
   __shared__ int last_sh;
-  __shared__ float wcand[kWarps][kWarpCand];
+  __shared__ float zc[kSolveCap];
   const int split = blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = a.G, P = a.P;
@@ -189,10 +201,7 @@ __global__ void __launch_bounds__(kThreads) pass_a_kernel(DecodeArgs a) {
     if (a.page_ids) a.page_ids[skv * a.page_ids_stride + lo + i] = page;
   }
   const size_t hq0 = (size_t)s * a.Hq + (size_t)kvh * G;  // first query head of the group
-  if (tid < 8) {
-    wkept[0][tid] = 0.0f;
-    th_sh[tid] = (a.policy == ENTMAXKV_POLICY_GAUSSIAN && tid < G) ? a.tauhat[hq0 + tid] : 0.0f;
-  }
+  if (tid < 8) th_sh[tid] = (a.policy == ENTMAXKV_POLICY_GAUSSIAN && tid < G) ? a.tauhat[hq0 + tid] : 0.0f;
   uint32_t bq[D / 16][2];
   if constexpr (sizeof(T) == 2) {
     load_q_bfrag<D>((const __nv_bfloat16*)a.q + hq0 * D, G, lane, bq);
@@ -201,12 +210,9 @@ __global__ void __launch_bounds__(kThreads) pass_a_kernel(DecodeArgs a) {
   }
   __syncthreads();
 
-  float wm[8], kept[8];
+  float wm[8], kept = 0.0f;
 #pragma unroll
-  for (int h = 0; h < 8; ++h) {
-    wm[h] = -CUDART_INF_F;
-    kept[h] = 0.0f;
-  }
+  for (int h = 0; h < 8; ++h) wm[h] = -CUDART_INF_F;
   const bool beta2 = a.beta == 2.0f;
   for (int i = warp; i < hi - lo; i += kWarps) {
     const int rank = lo + i;
@@ -230,13 +236,18 @@ __global__ void __launch_bounds__(kThreads) pass_a_kernel(DecodeArgs a) {
       for (int mt = 0; mt < 2; ++mt) {
         if (16 * mt >= P) break;
         const int t0 = 16 * mt + r, t1 = t0 + 8;
-        if (h0 < G) {
-          zb[t0 * G + h0] = zf[mt][0];
-          zb[t1 * G + h0] = zf[mt][2];
-        }
-        if (h1 < G) {
-          zb[t0 * G + h1] = zf[mt][1];
-          zb[t1 * G + h1] = zf[mt][3];
+        if (h1 < G && (G & 1) == 0) {  // even G: the pair is 8-byte aligned
+          *reinterpret_cast<float2*>(zb + t0 * G + h0) = make_float2(zf[mt][0], zf[mt][1]);
+          *reinterpret_cast<float2*>(zb + t1 * G + h0) = make_float2(zf[mt][2], zf[mt][3]);
+        } else {
+          if (h0 < G) {
+            zb[t0 * G + h0] = zf[mt][0];
+            zb[t1 * G + h0] = zf[mt][2];
+          }
+          if (h1 < G) {
+            zb[t0 * G + h1] = zf[mt][1];
+            zb[t1 * G + h1] = zf[mt][3];
+          }
         }
         pm0 = fmaxf(pm0, fmaxf(zf[mt][0], zf[mt][2]));
         pm1 = fmaxf(pm1, fmaxf(zf[mt][1], zf[mt][3]));
@@ -270,21 +281,20 @@ __global__ void __launch_bounds__(kThreads) pass_a_kernel(DecodeArgs a) {
       const float2 v = a.gauss_ms[(hq0 + lane) * a.maxp + page];
       float g, dg;
       gauss_moment(v.x - th_sh[lane], v.y, beta2, g, dg);
-      kept[0] += (float)nv * g;  // lane h accumulates head h
+      kept += (float)nv * g;  // lane h accumulates head h
     }
   }
   // block max z per head → global max; candidate threshold per head
   if constexpr (sizeof(T) == 2) {
-    const int c = lane & 3;
     if (lane < 4) {
-      if (2 * c < 8) wmax[warp][2 * c] = wm[0];
-      if (2 * c + 1 < 8) wmax[warp][2 * c + 1] = wm[1];
+      wmax[warp][2 * lane] = wm[0];
+      wmax[warp][2 * lane + 1] = wm[1];
     }
   } else {
     if (lane == 0)
       for (int h = 0; h < 8; ++h) wmax[warp][h] = wm[h];
   }
-  if (lane < 8) wkept[warp][lane] = lane < G ? kept[0] : 0.0f;
+  if (lane < 8) wkept[warp][lane] = lane < G ? kept : 0.0f;
   __syncthreads();
   if (tid < G) {
     float m = -CUDART_INF_F, ks = 0.0f;
@@ -301,26 +311,21 @@ __global__ void __launch_bounds__(kThreads) pass_a_kernel(DecodeArgs a) {
     if (a.policy == ENTMAXKV_POLICY_GAUSSIAN && ks != 0.0f) atomicAdd(&a.kept_mass[hq0 + tid], ks);
   }
   __syncthreads();
-  // candidates: tokens above (best known max − 1) of pages whose max clears it
-  for (int i = warp; i < hi - lo; i += kWarps) {
+  // candidate pages: those whose max clears (best known max − 1)
+  for (int i0 = warp * 32; i0 < hi - lo; i0 += kThreads) {
+    const int i = i0 + lane;
+    const bool in = i < hi - lo;
     const int rank = lo + i;
-    const float* zb = a.z + (skv * a.cap_pages + rank) * (size_t)P * G;
-    const float* pm = a.pmax + (skv * a.cap_pages + rank) * (size_t)G;
+    const float* pm = a.pmax + (skv * a.cap_pages + (in ? rank : lo)) * (size_t)G;
     for (int hg = 0; hg < G; ++hg) {
-      const float thr = thr_sh[hg];
-      if (!(pm[hg] > thr)) continue;
-      for (int t0 = 0; t0 < P; t0 += 32) {
-        const int t = t0 + lane;
-        const float zv = t < P ? zb[t * G + hg] : -CUDART_INF_F;
-        const bool pred = zv > thr;
-        const uint32_t bits = __ballot_sync(0xffffffffu, pred);
-        if (!bits) continue;
-        int base = 0;
-        if (lane == 0) base = atomicAdd(&a.cand_cnt[hq0 + hg], __popc(bits));
-        base = __shfl_sync(0xffffffffu, base, 0);
-        const int idx = base + __popc(bits & ((1u << lane) - 1u));
-        if (pred && idx < kCandCap) a.cand[(hq0 + hg) * kCandCap + idx] = zv;
-      }
+      const bool pred = in && pm[hg] > thr_sh[hg];
+      const uint32_t bits = __ballot_sync(0xffffffffu, pred);
+      if (!bits) continue;
+      int base = 0;
+      if (lane == 0) base = atomicAdd(&a.cand_cnt[hq0 + hg], __popc(bits));
+      base = __shfl_sync(0xffffffffu, base, 0);
+      const int idx = base + __popc(bits & ((1u << lane) - 1u));
+      if (pred && idx < kCandPages) a.cand[(hq0 + hg) * kCandPages + idx] = rank;
     }
   }
   // the last block of this (sequence, KV head) solves τ
@@ -333,43 +338,52 @@ __global__ void __launch_bounds__(kThreads) pass_a_kernel(DecodeArgs a) {
   if (warp >= G) return;
   const int hg = warp;
   const size_t hs = hq0 + hg;
+  const int cap_h = kSolveCap / G;
+  float* zs = zc + hg * cap_h;
   const float zm = ord_dec(__ldcg(&a.zmax[hs]));
   float tau_f = CUDART_NAN_F;
   double tau_d = CUDART_NAN;
   if (zm > -CUDART_INF_F) {
     const float T0 = zm - 1.0f;
-    TauSource src;
-    src.wc = wcand[warp];
-    src.m = 0;
-    src.cand = a.cand + hs * kCandCap;
-    src.nc = __ldcg(&a.cand_cnt[hs]);
-    src.z = a.z + skv * a.cap_pages * (size_t)P * G;
-    src.n_sel = n_sel;
+    const int nc = __ldcg(&a.cand_cnt[hs]);
+    const bool all = nc > kCandPages;  // list overflowed: consider every page
+    const int np = all ? n_sel : nc;
+    const int32_t* clist = a.cand + hs * kCandPages;
+    const float* zbase = a.z + skv * a.cap_pages * (size_t)P * G;
+    const float* pmbase = a.pmax + skv * a.cap_pages * (size_t)G;
+    int m = 0;
+    for (int k0 = 0; k0 < np; k0 += 32) {
+      const int k = k0 + lane;
+      const int rank = k < np ? (all ? k : __ldcg(clist + k)) : -1;
+      const float pmv = rank >= 0 ? __ldcg(pmbase + (size_t)rank * G + hg) : -CUDART_INF_F;
+      uint32_t bits = __ballot_sync(0xffffffffu, pmv > T0);
+      while (bits) {
+        const int b = __ffs(bits) - 1;
+        bits &= bits - 1u;
+        const int r = __shfl_sync(0xffffffffu, rank, b);
+        const float* zr = zbase + (size_t)r * P * G;
+        const float v = lane < P ? __ldcg(zr + lane * G + hg) : -CUDART_INF_F;
+        const bool pv = v > T0;
+        const uint32_t vb = __ballot_sync(0xffffffffu, pv);
+        const int pos = m + __popc(vb & ((1u << lane) - 1u));
+        if (pv && pos < cap_h) zs[pos] = v;
+        m += __popc(vb);
+      }
+    }
+    __syncwarp();
+    SolveSrc src;
+    src.zs = zs;
+    src.m = m;
+    src.big = m > cap_h;
+    src.pages = all ? nullptr : clist;
+    src.np = np;
+    src.zbase = zbase;
+    src.pmbase = pmbase;
     src.P = P;
     src.G = G;
     src.hg = hg;
-    if (src.nc <= kCandCap) {
-      int m = 0;
-      for (int i0 = 0; i0 < src.nc; i0 += 32) {
-        const int i = i0 + lane;
-        const float zv = i < src.nc ? __ldcg(src.cand + i) : -CUDART_INF_F;
-        const bool pred = zv > T0;
-        const uint32_t bits = __ballot_sync(0xffffffffu, pred);
-        const int pos = m + __popc(bits & ((1u << lane) - 1u));
-        if (pred && pos < kWarpCand) wcand[warp][pos] = zv;
-        m += __popc(bits);
-      }
-      __syncwarp();
-      if (m <= kWarpCand) {
-        src.mode = 0;
-        src.m = m;
-      } else {
-        src.mode = 1;
-      }
-    } else {
-      src.mode = 2;
-      if (lane == 0) raise_flag(a.status, ENTMAXKV_DEV_CAND_OVERFLOW);
-    }
+    src.T0 = T0;
+    if ((src.big || all) && lane == 0) raise_flag(a.status, ENTMAXKV_DEV_CAND_OVERFLOW);
     bool ok;
     tau_d = solve_tau_warp(src, (double)T0, a.beta, ok);
     if (!ok && lane == 0) raise_flag(a.status, ENTMAXKV_DEV_TAU_NOCONV);
@@ -412,12 +426,55 @@ struct VTraits<__nv_bfloat16> {
   }
 };
 
+// Sum of the split partials of one (sequence, KV head) in split order, by the
+// last block: float4 columns, the block's threads split over the partials.
+__device__ __noinline__ void combine_partials(const DecodeArgs& a, size_t skv, float* out_rows,
+                                              float4* red4) {
+  const int G = a.G, D = a.D, tid = threadIdx.x;
+  const int cols = G * D / 4;
+  const int groups = kThreads / cols > 0 ? kThreads / cols : 1;
+  const int col = tid % cols, grp = tid / cols;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (grp < groups) {
+    const float* base = a.partial + skv * a.splits * (size_t)a.pstride;
+#pragma unroll 4
+    for (int sp = grp; sp < a.splits; sp += groups) {
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(base + (size_t)sp * a.pstride) + col);
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    red4[grp * cols + col] = acc;
+  }
+  __syncthreads();
+  if (tid < cols) {
+    float4 sum = red4[tid];
+    for (int g2 = 1; g2 < groups; ++g2) {
+      const float4 v = red4[g2 * cols + tid];
+      sum.x += v.x;
+      sum.y += v.y;
+      sum.z += v.z;
+      sum.w += v.w;
+    }
+    reinterpret_cast<float4*>(out_rows)[tid] = sum;
+  }
+}
+
+// Pass B: for each kept page with some z above τ (every page with
+// ENTMAXKV_FLAG_DENSE_V) the warp stages the page's z in shared memory, issues
+// all its V loads at once (lane: 16 bytes of a row, tokens tg, tg+TG, ...),
+// and accumulates p·v in fp32 registers.
 template <typename T, int D, int GP>
 __global__ void __launch_bounds__(kThreads) pass_b_kernel(DecodeArgs a) {
   constexpr int VEC = VTraits<T>::VEC, LPR = D / VEC, TG = 32 / LPR;
+  constexpr int MAXT = 32 / TG;                  // tokens per lane in a 32-token page
+  constexpr int CH = MAXT < 16 ? MAXT : 16;      // V rows in flight per lane
   __shared__ double tau_sh[GP];
-  __shared__ float red[kWarps][GP][D];
+  __shared__ __align__(16) float zs[kWarps][32 * 8];
+  __shared__ __align__(16) float red[kWarps][GP][D];
   __shared__ float dsum[kWarps][GP];
+  __shared__ float4 red4[kThreads];
   __shared__ int last_sh;
   const int split = blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -447,6 +504,7 @@ __global__ void __launch_bounds__(kThreads) pass_b_kernel(DecodeArgs a) {
   for (int h = 0; h < GP; ++h)
 #pragma unroll
     for (int j = 0; j < VEC; ++j) acc[h][j] = 0.0f;
+  float* zw = zs[warp];
 
   for (int i = warp; i < hi - lo; i += kWarps) {
     const int rank = lo + i;
@@ -460,23 +518,38 @@ __global__ void __launch_bounds__(kThreads) pass_b_kernel(DecodeArgs a) {
     const int ph = phys_page(a.block_table, seq, page, a.maxp, a.nphys, nullptr);
     if (ph < 0) continue;
     const int nv = min(P, L - page * P);
-    const T* vs = (const T*)a.v_pool + ((size_t)ph * a.Hkv + kvh) * P * D + dc * VEC;
     const float* zb = a.z + (skv * a.cap_pages + rank) * (size_t)P * G;
-    for (int t = tg; t < nv; t += TG) {
-      const uint4 raw = ld_stream(vs + (size_t)t * D);
-      float v[VEC];
-      VTraits<T>::unpack(raw, v);
+    for (int e = 4 * lane; e < P * G; e += 128)  // P·G is a multiple of 16
+      *reinterpret_cast<float4*>(zw + e) = __ldcg(reinterpret_cast<const float4*>(zb + e));
+    __syncwarp();
+    const T* vs = (const T*)a.v_pool + ((size_t)ph * a.Hkv + kvh) * P * D + dc * VEC;
+    for (int c0 = 0; c0 < MAXT; c0 += CH) {
+      uint4 raw[CH];
 #pragma unroll
-      for (int h = 0; h < GP; ++h) {
-        if (h < G) {
-          const float zv = __ldcg(zb + t * G + h);
-          const float p = sizeof(T) == 4 ? pos_pow((float)((double)zv - taud[h]), a.beta)
-                                         : pos_pow(zv - tau[h], a.beta);
+      for (int u = 0; u < CH; ++u) {
+        const int t = tg + TG * (c0 + u);
+        raw[u] = t < nv ? ld_stream(vs + (size_t)t * D) : make_uint4(0u, 0u, 0u, 0u);
+      }
 #pragma unroll
-          for (int j = 0; j < VEC; ++j) acc[h][j] = fmaf(p, v[j], acc[h][j]);
+      for (int u = 0; u < CH; ++u) {
+        const int t = tg + TG * (c0 + u);
+        if (t < nv) {
+          float v[VEC];
+          VTraits<T>::unpack(raw[u], v);
+#pragma unroll
+          for (int h = 0; h < GP; ++h) {
+            if (h < G) {
+              const float zv = zw[t * G + h];
+              const float p = sizeof(T) == 4 ? pos_pow((float)((double)zv - taud[h]), a.beta)
+                                             : pos_pow(zv - tau[h], a.beta);
+#pragma unroll
+              for (int j = 0; j < VEC; ++j) acc[h][j] = fmaf(p, v[j], acc[h][j]);
+            }
+          }
         }
       }
     }
+    __syncwarp();
   }
 #pragma unroll
   for (int o = LPR; o < 32; o <<= 1)
@@ -491,10 +564,10 @@ __global__ void __launch_bounds__(kThreads) pass_b_kernel(DecodeArgs a) {
       for (int j = 0; j < VEC; ++j) red[warp][h][dc * VEC + j] = acc[h][j];
   }
   // top-k: this block's share of the certified dropped mass
-  float dd[GP];
-#pragma unroll
-  for (int h = 0; h < GP; ++h) dd[h] = 0.0f;
   if (a.policy == ENTMAXKV_POLICY_TOPK) {
+    float dd[GP];
+#pragma unroll
+    for (int h = 0; h < GP; ++h) dd[h] = 0.0f;
     const uint32_t* bm = a.bitmap + skv * a.words;
     const int plo = (int)(((long long)n_pages * split) / a.splits);
     const int phi = (int)(((long long)n_pages * (split + 1)) / a.splits);
@@ -512,13 +585,13 @@ __global__ void __launch_bounds__(kThreads) pass_b_kernel(DecodeArgs a) {
     }
   }
   __syncthreads();
-  float* part = a.partial + (skv * a.splits + split) * (size_t)G * (D + 2);
+  float* part = a.partial + (skv * a.splits + split) * (size_t)a.pstride;
   for (int e = tid; e < G * D; e += kThreads) {
     const int h = e / D, d = e % D;
     float sum = 0.0f;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) sum += red[w][h][d];
-    part[h * (D + 2) + d] = sum;
+    part[e] = sum;
   }
   if (a.policy == ENTMAXKV_POLICY_TOPK && tid < G) {
     float sum = 0.0f;
@@ -531,13 +604,7 @@ __global__ void __launch_bounds__(kThreads) pass_b_kernel(DecodeArgs a) {
   __syncthreads();
   if (!last_sh) return;
   __threadfence();
-  for (int e = tid; e < G * D; e += kThreads) {
-    const int h = e / D, d = e % D;
-    float sum = 0.0f;
-    for (int sp = 0; sp < a.splits; ++sp)
-      sum += __ldcg(a.partial + (skv * a.splits + sp) * (size_t)G * (D + 2) + h * (D + 2) + d);
-    a.out[(hq0 + h) * D + d] = sum;
-  }
+  combine_partials(a, skv, a.out + hq0 * D, red4);
   if (a.policy == ENTMAXKV_POLICY_TOPK && a.delta_out && tid < G)
     a.delta_out[hq0 + tid] = L > 0 ? fminf(1.0f, __ldcg(&a.dbar[hq0 + tid])) : 0.0f;
 }

@@ -168,101 +168,146 @@ __global__ void __launch_bounds__(kThreads) bbox_f32_kernel(DecodeArgs a) {
   }
 }
 
-// Gaussian page scores. Half a warp per page: lane l (0..15) of the half
-// covers the 16-byte chunks l, l+16, ... of the page's mean and m2 rows; the
-// q and q² values of those dims live in registers. GP = group padded up.
+// Gaussian page scores. A warp scores PPI pages per iteration: lane l covers
+// dims [l·D/32, (l+1)·D/32) of each page's mean and m2 rows (q and q² of those
+// dims stay in registers) and all 2·PPI row loads are issued together. Each
+// lane then holds NV = PPI·2·GP partial sums; a butterfly reduce-scatter over
+// the 32 lanes (each step a lane keeps half its values and adds the partner's
+// copy of that half) leaves every total in some lane with ~NV shuffles
+// instead of 5·NV. GP = group padded up to a power of two.
 template <typename TQ, int D, int GP>
-__global__ void __launch_bounds__(kThreads) gauss_kernel(DecodeArgs a) {
-  constexpr int CH = D / 64;  // float4 chunks per lane per row
+__global__ void __launch_bounds__(kThreads, 2) gauss_kernel(DecodeArgs a) {
+  constexpr int DPL = D / 32;           // dims per lane
+  constexpr int PPI = 4;                // pages per warp iteration
+  constexpr int NV = PPI * 2 * GP;      // partial sums per lane
   const int kvh = blockIdx.y, s = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int half = lane >> 4, hl = lane & 15;
-  __shared__ float wmax[kWarps][GP];
+  __shared__ uint32_t smax[GP];
   const int seq = seq_row(a.seq_ids, s, a.max_seqs, threadIdx.x == 0 ? a.status : nullptr);
   if (seq < 0) return;
   const int L = seq_len_clamped(a.seq_lens, seq, a.maxp, a.P, threadIdx.x == 0 ? a.status : nullptr);
   const int n_pages = (L + a.P - 1) / a.P;
-  if ((int)(blockIdx.x * kWarps * 2) >= n_pages) return;
+  if ((int)(blockIdx.x * kWarps * PPI) >= n_pages) return;
+  if (threadIdx.x < GP) smax[threadIdx.x] = 0u;
 
-  float qv[GP][CH * 4], q2[GP][CH * 4];
+  float qv[GP][DPL], q2[GP][DPL];
 #pragma unroll
   for (int h = 0; h < GP; ++h) {
     const TQ* qh = (const TQ*)a.q + ((size_t)s * a.Hq + (size_t)kvh * a.G + (h < a.G ? h : 0)) * D;
 #pragma unroll
-    for (int j = 0; j < CH; ++j)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float x = h < a.G ? to_f(qh[4 * (hl + 16 * j) + e]) : 0.0f;
-        qv[h][4 * j + e] = x;
-        q2[h][4 * j + e] = x * x;
-      }
+    for (int e = 0; e < DPL; ++e) {
+      const float x = h < a.G ? to_f(qh[lane * DPL + e]) : 0.0f;
+      qv[h][e] = x;
+      q2[h][e] = x * x;
+    }
   }
-  float runmax[GP];
+  // which total this lane ends up holding (fixed by its lane bits)
+  int idx = 0, nfin = NV;
 #pragma unroll
-  for (int h = 0; h < GP; ++h) runmax[h] = -CUDART_INF_F;
-  for (int pp = blockIdx.x * kWarps + warp; pp * 2 < n_pages; pp += gridDim.x * kWarps) {
-    const int p = pp * 2 + half;
-    const bool valid = p < n_pages;
-    const int ph = valid ? phys_page(a.block_table, seq, p, a.maxp, a.nphys, hl == 0 ? a.status : nullptr) : -1;
-    float mu[GP], sg[GP];
+  for (int o = 16; o >= 1; o >>= 1)
+    if (nfin > 1) {
+      nfin >>= 1;
+      if (lane & o) idx += nfin;
+    }
+  constexpr int NFIN = NV > 32 ? NV / 32 : 1;  // totals per lane (indices idx .. idx+NFIN−1)
+  const int my_pg = idx / (2 * GP), my_qty = (idx / GP) & 1, my_h0 = idx % GP;
+  const bool writer = (NV >= 32) || ((lane & (32 / NV - 1)) == 0);
+  float runmax[NFIN];
 #pragma unroll
-    for (int h = 0; h < GP; ++h) mu[h] = sg[h] = 0.0f;
-    if (ph >= 0) {
-      const size_t base = ((size_t)ph * a.Hkv + kvh) * D;
+  for (int i = 0; i < NFIN; ++i) runmax[i] = -CUDART_INF_F;
+  __syncthreads();
+
+  for (int pb = (blockIdx.x * kWarps + warp) * PPI; pb < n_pages; pb += gridDim.x * kWarps * PPI) {
+    int ph_l = -1;
+    if (lane < PPI && pb + lane < n_pages)
+      ph_l = phys_page(a.block_table, seq, pb + lane, a.maxp, a.nphys, a.status);
+    float mv[PPI][DPL], vv[PPI][DPL];
 #pragma unroll
-      for (int j = 0; j < CH; ++j) {
-        const uint4 mr = ld_stream(a.mean + base + 4 * (hl + 16 * j));
-        const uint4 vr = ld_stream(a.m2 + base + 4 * (hl + 16 * j));
-        const float mv[4] = {__uint_as_float(mr.x), __uint_as_float(mr.y), __uint_as_float(mr.z),
-                             __uint_as_float(mr.w)};
-        const float vv[4] = {__uint_as_float(vr.x), __uint_as_float(vr.y), __uint_as_float(vr.z),
-                             __uint_as_float(vr.w)};
+    for (int pg = 0; pg < PPI; ++pg) {
+      const int ph = __shfl_sync(0xffffffffu, ph_l, pg);
+      if (ph >= 0) {
+        const size_t base = ((size_t)ph * a.Hkv + kvh) * D + lane * DPL;
+        if constexpr (DPL == 4) {
+          const uint4 mr = ld_stream(a.mean + base), vr = ld_stream(a.m2 + base);
+          mv[pg][0] = __uint_as_float(mr.x); mv[pg][1] = __uint_as_float(mr.y);
+          mv[pg][2] = __uint_as_float(mr.z); mv[pg][3] = __uint_as_float(mr.w);
+          vv[pg][0] = __uint_as_float(vr.x); vv[pg][1] = __uint_as_float(vr.y);
+          vv[pg][2] = __uint_as_float(vr.z); vv[pg][3] = __uint_as_float(vr.w);
+        } else {
 #pragma unroll
-        for (int h = 0; h < GP; ++h)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            mu[h] = fmaf(qv[h][4 * j + e], mv[e], mu[h]);
-            sg[h] = fmaf(q2[h][4 * j + e], vv[e], sg[h]);
+          for (int e = 0; e < DPL; ++e) {
+            mv[pg][e] = __ldg(a.mean + base + e);
+            vv[pg][e] = __ldg(a.m2 + base + e);
           }
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) mv[pg][e] = vv[pg][e] = 0.0f;
       }
     }
+    float v[NV];
 #pragma unroll
-    for (int o = 8; o > 0; o >>= 1)
+    for (int pg = 0; pg < PPI; ++pg)
 #pragma unroll
       for (int h = 0; h < GP; ++h) {
-        mu[h] += __shfl_xor_sync(0xffffffffu, mu[h], o);
-        sg[h] += __shfl_xor_sync(0xffffffffu, sg[h], o);
+        float mu = 0.0f, sg = 0.0f;
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) {
+          mu = fmaf(qv[h][e], mv[pg][e], mu);
+          sg = fmaf(q2[h][e], vv[pg][e], sg);
+        }
+        v[(pg * 2 + 0) * GP + h] = mu;
+        v[(pg * 2 + 1) * GP + h] = sg;
       }
-    if (valid && hl == 0) {
-      const int nv = min(a.P, L - p * a.P);
+    // butterfly reduce-scatter
+    int n = NV;
 #pragma unroll
-      for (int h = 0; h < GP; ++h) {
-        if (h < a.G) {
-          float2 msv;
-          if (ph >= 0) {
-            msv.x = a.a1 * mu[h] * a.inv_sqrt_d;
-            msv.y = a.a1 * sqrtf(fmaxf(sg[h], 0.0f) / ((float)nv * (float)D));
-            runmax[h] = fmaxf(runmax[h], msv.x);
-          } else {  // unreadable page: no mass, never selected
-            msv = make_float2(-CUDART_INF_F, 0.0f);
+    for (int o = 16; o >= 1; o >>= 1) {
+      if (n > 1) {
+        const int half = n >> 1;
+        const bool up = lane & o;
+#pragma unroll
+        for (int i = 0; i < NV / 2; ++i) {
+          if (i < half) {
+            const float send = up ? v[i] : v[i + half];
+            const float keep = up ? v[i + half] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
           }
-          a.gauss_ms[((size_t)s * a.Hq + (size_t)kvh * a.G + h) * a.maxp + p] = msv;
+        }
+        n = half;
+      } else {
+        v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
+      }
+    }
+    // lane holds totals idx.. = (page my_pg, quantity my_qty, heads my_h0..)
+    const int p = pb + my_pg;
+    const int ph = __shfl_sync(0xffffffffu, ph_l, my_pg);
+#pragma unroll
+    for (int i = 0; i < NFIN; ++i) {
+      const int my_h = my_h0 + i;
+      if (writer && my_h < a.G && p < n_pages) {
+        float* dst = reinterpret_cast<float*>(
+            a.gauss_ms + ((size_t)s * a.Hq + (size_t)kvh * a.G + my_h) * a.maxp + p);
+        if (ph < 0) {  // unreadable page: no mass, never selected
+          dst[my_qty] = my_qty == 0 ? -CUDART_INF_F : 0.0f;
+        } else if (my_qty == 0) {
+          const float m = a.a1 * v[i] * a.inv_sqrt_d;
+          dst[0] = m;
+          runmax[i] = fmaxf(runmax[i], m);
+        } else {
+          const int nv = min(a.P, L - p * a.P);
+          dst[1] = a.a1 * sqrtf(fmaxf(v[i], 0.0f) / ((float)nv * (float)D));
         }
       }
     }
   }
 #pragma unroll
-  for (int h = 0; h < GP; ++h) {
-    const float m = warp_max(runmax[h]);
-    if (lane == 0) wmax[warp][h] = m;
-  }
+  for (int i = 0; i < NFIN; ++i)
+    if (writer && my_qty == 0 && my_h0 + i < a.G && runmax[i] > -CUDART_INF_F)
+      atomicMax(&smax[my_h0 + i], ord_enc(runmax[i]));
   __syncthreads();
-  if (threadIdx.x < a.G) {
-    float m = -CUDART_INF_F;
-    for (int w = 0; w < kWarps; ++w) m = fmaxf(m, wmax[w][threadIdx.x]);
-    if (m > -CUDART_INF_F)
-      atomicMax(&a.mmax[(size_t)s * a.Hq + (size_t)kvh * a.G + threadIdx.x], ord_enc(m));
-  }
+  if (threadIdx.x < a.G && smax[threadIdx.x] != 0u)
+    atomicMax(&a.mmax[(size_t)s * a.Hq + (size_t)kvh * a.G + threadIdx.x], smax[threadIdx.x]);
 }
 
 static int grid_x_for(int units, int per_block, int sms, int other_blocks) {
@@ -296,7 +341,7 @@ static void gauss_dispatch_g(const DecodeArgs& a, dim3 grid, cudaStream_t st) {
 }
 
 cudaError_t launch_gauss(const DecodeArgs& a, int kv_dtype, int sms, cudaStream_t st) {
-  dim3 grid(grid_x_for(a.maxp, kWarps * 2, sms, a.Hkv * a.S), a.Hkv, a.S);
+  dim3 grid(grid_x_for(a.maxp, kWarps * 4, sms, a.Hkv * a.S), a.Hkv, a.S);
   if (kv_dtype == ENTMAXKV_BF16) {
     if (a.D == 128) gauss_dispatch_g<__nv_bfloat16, 128>(a, grid, st);
     else gauss_dispatch_g<__nv_bfloat16, 64>(a, grid, st);

@@ -63,12 +63,37 @@ __global__ void __cluster_dims__(kTauhatCluster, 1, 1) __launch_bounds__(kThread
   const int chunk = ((words + kTauhatCluster - 1) / kTauhatCluster) * 32;
   const int p_lo = rank * chunk, p_hi = min(n_pages, p_lo + chunk);
 
+  // This thread's pages stay in registers for every iteration (kRegPages
+  // each, which covers 8·256·kRegPages pages per query head); pages beyond
+  // that are re-read from memory.
+  constexpr int kRegPages = 16;
+  float2 mr[kRegPages];
+  float nr[kRegPages];
+#pragma unroll
+  for (int k = 0; k < kRegPages; ++k) {
+    const int p = p_lo + tid + k * kThreads;
+    if (p < p_hi) {
+      mr[k] = ms[p];
+      nr[k] = (float)page_tokens(p, n_pages, L, a.P);
+    } else {
+      mr[k] = make_float2(-CUDART_INF_F, 0.0f);
+      nr[k] = 0.0f;
+    }
+  }
   double lo = M - 1.0, hi = CUDART_INF, tau = lo;
   bool converged = false;
-  for (int it = 0; it < kTauhatIters; ++it) {
+  int it = 0;
+  for (; it < kTauhatIters; ++it) {
     const float tf = (float)tau;
     float f = 0.0f, df = 0.0f;
-    for (int p = p_lo + tid; p < p_hi; p += kThreads) {
+#pragma unroll
+    for (int k = 0; k < kRegPages; ++k) {
+      float g, dg;
+      gauss_moment(mr[k].x - tf, mr[k].y, beta2, g, dg);
+      f = fmaf(nr[k], g, f);
+      df = fmaf(nr[k], dg, df);
+    }
+    for (int p = p_lo + tid + kRegPages * kThreads; p < p_hi; p += kThreads) {
       const float2 v = ms[p];
       float g, dg;
       gauss_moment(v.x - tf, v.y, beta2, g, dg);
@@ -126,6 +151,7 @@ __global__ void __cluster_dims__(kTauhatCluster, 1, 1) __launch_bounds__(kThread
   cluster.sync();  // no block leaves while another may still read its slots
   if (rank == 0 && tid == 0) {
     a.tauhat[(size_t)s * a.Hq + h] = th;
+    a.diag[(size_t)s * a.Hq + h] = it + 1;
     if (!converged) raise_flag(a.status, ENTMAXKV_DEV_TAUHAT_NOCONV);
   }
   // Selection bits: each warp covers 32 consecutive pages starting on a word.

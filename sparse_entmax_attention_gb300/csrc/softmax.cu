@@ -16,11 +16,15 @@ namespace ekv {
 template <typename T, int D, int GP>
 __global__ void __launch_bounds__(kThreads) softmax_kernel(DecodeArgs a) {
   constexpr int VEC = 16 / sizeof(T), LPR = D / VEC, TG = 32 / LPR;
+  constexpr int MAXT = 32 / TG;                  // tokens per lane in a 32-token page
+  constexpr int CH = MAXT < 16 ? MAXT : 16;      // V rows in flight per lane
   __shared__ float qs[8][D];
   __shared__ float sbuf[kWarps][32][GP];
   __shared__ float pmx[kWarps][8];
-  __shared__ float red[kWarps][GP][D];
+  __shared__ __align__(16) float red[kWarps][GP][D];
   __shared__ float wm_sh[kWarps][GP], wl_sh[kWarps][GP];
+  __shared__ float4 red4[kThreads];
+  __shared__ float Mg_sh[8], Lg_sh[8];
   __shared__ int last_sh;
   const int split = blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -96,6 +100,14 @@ __global__ void __launch_bounds__(kThreads) softmax_kernel(DecodeArgs a) {
         if (lane == 0) pmx[warp][h] = mm;
       }
     }
+    // issue the page's V loads before the rescale so they overlap it
+    const T* vs = (const T*)a.v_pool + slab_off + dc * VEC;
+    uint4 raw[MAXT];
+#pragma unroll
+    for (int u = 0; u < MAXT; ++u) {
+      const int t = tg + TG * u;
+      if (u < CH) raw[u] = t < nv ? ld_stream(vs + (size_t)t * D) : make_uint4(0u, 0u, 0u, 0u);
+    }
     __syncwarp();
 #pragma unroll
     for (int h = 0; h < GP; ++h) {
@@ -108,24 +120,27 @@ __global__ void __launch_bounds__(kThreads) softmax_kernel(DecodeArgs a) {
         m[h] = mn;
       }
     }
-    const T* vs = (const T*)a.v_pool + slab_off + dc * VEC;
-    for (int t = tg; t < nv; t += TG) {
-      const uint4 raw = ld_stream(vs + (size_t)t * D);
-      float v[VEC];
-      if constexpr (sizeof(T) == 2) {
-        v[0] = bf_lo(raw.x); v[1] = bf_hi(raw.x); v[2] = bf_lo(raw.y); v[3] = bf_hi(raw.y);
-        v[4] = bf_lo(raw.z); v[5] = bf_hi(raw.z); v[6] = bf_lo(raw.w); v[7] = bf_hi(raw.w);
-      } else {
-        v[0] = __uint_as_float(raw.x); v[1] = __uint_as_float(raw.y);
-        v[2] = __uint_as_float(raw.z); v[3] = __uint_as_float(raw.w);
-      }
 #pragma unroll
-      for (int h = 0; h < GP; ++h) {
-        if (h < G && m[h] > -CUDART_INF_F) {
-          const float p = exp2f(sbuf[warp][t][h] - m[h]);
-          l[h] += p;
+    for (int u = 0; u < MAXT; ++u) {
+      const int t = tg + TG * u;
+      if (u >= CH && t < nv) raw[u] = ld_stream(vs + (size_t)t * D);  // beyond the first batch
+      if (t < nv) {
+        float v[VEC];
+        if constexpr (sizeof(T) == 2) {
+          v[0] = bf_lo(raw[u].x); v[1] = bf_hi(raw[u].x); v[2] = bf_lo(raw[u].y); v[3] = bf_hi(raw[u].y);
+          v[4] = bf_lo(raw[u].z); v[5] = bf_hi(raw[u].z); v[6] = bf_lo(raw[u].w); v[7] = bf_hi(raw[u].w);
+        } else {
+          v[0] = __uint_as_float(raw[u].x); v[1] = __uint_as_float(raw[u].y);
+          v[2] = __uint_as_float(raw[u].z); v[3] = __uint_as_float(raw[u].w);
+        }
 #pragma unroll
-          for (int j = 0; j < VEC; ++j) acc[h][j] = fmaf(p, v[j], acc[h][j]);
+        for (int h = 0; h < GP; ++h) {
+          if (h < G && m[h] > -CUDART_INF_F) {
+            const float p = exp2f(sbuf[warp][t][h] - m[h]);
+            l[h] += p;
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) acc[h][j] = fmaf(p, v[j], acc[h][j]);
+          }
         }
       }
     }
@@ -153,7 +168,7 @@ __global__ void __launch_bounds__(kThreads) softmax_kernel(DecodeArgs a) {
     }
   }
   __syncthreads();
-  float* part = a.partial + (skv * a.splits + split) * (size_t)G * (D + 2);
+  float* part = a.partial + (skv * a.splits + split) * (size_t)a.pstride;
   for (int e = tid; e < G * (D + 1); e += kThreads) {
     const int h = e / (D + 1), d = e % (D + 1);
     float M = -CUDART_INF_F;
@@ -164,10 +179,10 @@ __global__ void __launch_bounds__(kThreads) softmax_kernel(DecodeArgs a) {
       sum += wt * (d < D ? red[w][h][d] : wl_sh[w][h]);
     }
     if (d < D) {
-      part[h * (D + 2) + d] = sum;
+      part[h * D + d] = sum;
     } else {
-      part[h * (D + 2) + D] = M;
-      part[h * (D + 2) + D + 1] = sum;
+      part[G * D + h] = M;
+      part[G * D + G + h] = sum;
     }
   }
   __threadfence();
@@ -176,27 +191,65 @@ __global__ void __launch_bounds__(kThreads) softmax_kernel(DecodeArgs a) {
   __syncthreads();
   if (!last_sh) return;
   __threadfence();
-  for (int e = tid; e < G * (D + 1); e += kThreads) {
-    const int h = e / (D + 1), d = e % (D + 1);
+  // merge the split partials: per-head max and weighted sums, then columns
+  const float* base = a.partial + skv * a.splits * (size_t)a.pstride;
+  if (warp < G) {
     float M = -CUDART_INF_F;
-    for (int sp = 0; sp < a.splits; ++sp)
-      M = fmaxf(M, __ldcg(a.partial + (skv * a.splits + sp) * (size_t)G * (D + 2) + h * (D + 2) + D));
-    float num = 0.0f, den = 0.0f;
-    for (int sp = 0; sp < a.splits; ++sp) {
-      const float* pp = a.partial + (skv * a.splits + sp) * (size_t)G * (D + 2) + h * (D + 2);
-      const float Ms = __ldcg(pp + D);
+    for (int sp = lane; sp < a.splits; sp += 32)
+      M = fmaxf(M, __ldcg(base + (size_t)sp * a.pstride + G * D + warp));
+    M = warp_max(M);
+    float Ls = 0.0f;
+    for (int sp = lane; sp < a.splits; sp += 32) {
+      const float Ms = __ldcg(base + (size_t)sp * a.pstride + G * D + warp);
+      if (Ms > -CUDART_INF_F) Ls += exp2f(Ms - M) * __ldcg(base + (size_t)sp * a.pstride + G * D + G + warp);
+    }
+    Ls = warp_sum(Ls);
+    if (lane == 0) {
+      Mg_sh[warp] = M;
+      Lg_sh[warp] = Ls;
+    }
+  }
+  __syncthreads();
+  const int cols = G * D / 4;
+  const int groups = kThreads / cols > 0 ? kThreads / cols : 1;
+  const int col = tid % cols, grp = tid / cols;
+  const int h = (col * 4) / D;
+  if (grp < groups) {
+    float4 accv = make_float4(0.f, 0.f, 0.f, 0.f);
+    const float Mg = Mg_sh[h];
+#pragma unroll 4
+    for (int sp = grp; sp < a.splits; sp += groups) {
+      const float Ms = __ldcg(base + (size_t)sp * a.pstride + G * D + h);
       if (!(Ms > -CUDART_INF_F)) continue;
-      const float wt = exp2f(Ms - M);
-      den += wt * __ldcg(pp + D + 1);
-      if (d < D) num += wt * __ldcg(pp + d);
+      const float wt = exp2f(Ms - Mg);
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(base + (size_t)sp * a.pstride) + col);
+      accv.x += wt * v.x;
+      accv.y += wt * v.y;
+      accv.z += wt * v.z;
+      accv.w += wt * v.w;
     }
-    if (d < D) {
-      a.out[(hq0 + h) * D + d] = den > 0.0f ? num / den : 0.0f;
-    } else {
-      const float lse = den > 0.0f ? (M + log2f(den)) * 0.6931471805599453f : CUDART_NAN_F;
-      if (a.tau_out) a.tau_out[hq0 + h] = lse;
-      if (a.delta_out) a.delta_out[hq0 + h] = 0.0f;
+    red4[grp * cols + col] = accv;
+  }
+  __syncthreads();
+  if (tid < cols) {
+    float4 sum = red4[tid];
+    for (int g2 = 1; g2 < groups; ++g2) {
+      const float4 v = red4[g2 * cols + tid];
+      sum.x += v.x;
+      sum.y += v.y;
+      sum.z += v.z;
+      sum.w += v.w;
     }
+    const float Lg = Lg_sh[h];
+    const float inv = Lg > 0.0f ? 1.0f / Lg : 0.0f;
+    reinterpret_cast<float4*>(a.out + hq0 * D)[tid] =
+        make_float4(sum.x * inv, sum.y * inv, sum.z * inv, sum.w * inv);
+  }
+  if (tid < G) {
+    const float Lg = Lg_sh[tid], Mg = Mg_sh[tid];
+    const float lse = Lg > 0.0f ? (Mg + log2f(Lg)) * 0.6931471805599453f : CUDART_NAN_F;
+    if (a.tau_out) a.tau_out[hq0 + tid] = lse;
+    if (a.delta_out) a.delta_out[hq0 + tid] = 0.0f;
   }
 }
 
