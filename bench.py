@@ -54,6 +54,9 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="headline step only")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--policies", default="gaussian,topk,full_dense,full_skipv,softmax",
+                    help="rows of the per-policy table")
     return ap.parse_args()
 
 
@@ -264,15 +267,16 @@ def run_ours(args, rank, world):
     if rank != 0:
         return None
     if not args.no_extras:
-        res["policies"] = policy_table(wl, B, flush, qbuf, timed, K, peaks)
+        res["policies"] = policy_table(wl, B, flush, qbuf, timed, K, peaks, args.policies.split(","))
         res["roofline"] = roofline(wl, B, flush, qbuf, K, peaks, peak_kind)
-        res["e2e"] = e2e(wl, B, toks, qs, n_app, K, W)
+        if not args.no_e2e:
+            res["e2e"] = e2e(wl, B, toks, qs, n_app, K, W)
     if not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(wl, qbuf)
     return res
 
 
-def policy_table(wl, B, flush, qbuf, timed, K, peaks):
+def policy_table(wl, B, flush, qbuf, timed, K, peaks, names):
     import torch
     cache, spec = wl.cache, wl.spec
     rows = {}
@@ -280,6 +284,8 @@ def policy_table(wl, B, flush, qbuf, timed, K, peaks):
              ("full_dense", "full", 0, B.FLAG_DENSE_V), ("full_skipv", "full", 0, 0),
              ("softmax", "softmax", 0, 0)]
     for name, pol, budget, flags in cases:
+        if name not in names:
+            continue
         ws = B.alloc_workspace(cache, spec.batch, pol, budget)
         o = B.alloc_outputs(cache, spec.batch, pol, budget)
         fn = lambda: B.decode(cache, qbuf, ALPHA, pol, budget, MARGIN, flags, workspace=ws, outputs=o)
@@ -298,7 +304,8 @@ def policy_table(wl, B, flush, qbuf, timed, K, peaks):
                       **counts}
         del ws
     for name in ("topk", "full_dense", "full_skipv", "softmax"):
-        rows[name]["gaussian_speedup"] = round(rows[name]["us"] / rows["gaussian"]["us"], 2)
+        if name in rows and "gaussian" in rows:
+            rows[name]["gaussian_speedup"] = round(rows[name]["us"] / rows["gaussian"]["us"], 2)
     return rows
 
 

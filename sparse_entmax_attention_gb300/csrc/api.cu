@@ -95,7 +95,7 @@ static int compute_layout(const entmaxkv_config* c, int S, int policy, int budge
   L.bbox_u = policy == ENTMAXKV_POLICY_TOPK ? take(nq * (size_t)maxp * 4) : none;
   L.bbox_uhat = policy == ENTMAXKV_POLICY_TOPK ? take(nk * (size_t)maxp * 4) : none;
   L.gauss_ms = policy == ENTMAXKV_POLICY_GAUSSIAN ? take(nq * (size_t)maxp * 8) : none;
-  L.cand = entmax ? take(nq * (size_t)kCandPages * 4) : none;
+  L.cand = entmax ? take(nq * (size_t)cap * 4) : none;
   L.z = entmax ? take(nk * (size_t)cap * P * G * 4) : none;
   L.pmax = entmax ? take(nk * (size_t)cap * G * 4) : none;
   L.pstride = (G * D + 2 * G + 3) & ~3;

@@ -13,7 +13,6 @@ namespace ekv {
 
 constexpr int kThreads = 256;       // decode / scoring blocks: 8 warps
 constexpr int kWarps = kThreads / 32;
-constexpr int kCandPages = 4096;    // candidate pages listed per query head for the exact τ
 constexpr int kSolveCap = 8192;     // candidate scores the τ solver keeps in shared memory
 constexpr int kListCap = 1024;      // selected pages one decode block handles
 constexpr int kTauhatCluster = 8;   // blocks per τ̂ cluster (one cluster per query head)
@@ -62,7 +61,7 @@ struct DecodeArgs {
   float* bbox_u;       // [S][Hq][maxp]
   float* bbox_uhat;    // [S][Hkv][maxp]
   float2* gauss_ms;    // [S][Hq][maxp]
-  int32_t* cand;       // [S][Hq][kCandPages] ranks of candidate pages
+  int32_t* cand;       // [S][Hq][cap_pages] ranks of candidate pages
   float* z;            // [S][Hkv][cap_pages][P][G]
   float* pmax;         // [S][Hkv][cap_pages][G]
   float* partial;      // [S][Hkv][splits][pstride]: acc [G][D], then (m, l) per head

@@ -180,7 +180,9 @@ __global__ void __launch_bounds__(kThreads) pass_a_kernel(DecodeArgs a) {
   __shared__ float thr_sh[8];
   __shared__ float th_sh[8];
   __shared__ int last_sh;
-  __shared__ float zc[kSolveCap];
+  __shared__ __align__(16) float pool[kSolveCap];  // last block: page and score candidates
+  __shared__ float T0_sh[8], tlb_sh[8];
+  __shared__ int nc_sh[8], np_sh[8], nz_sh[8], big_sh[8];
   const int split = blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = a.G, P = a.P;
@@ -325,7 +327,7 @@ __global__ void __launch_bounds__(kThreads) pass_a_kernel(DecodeArgs a) {
       if (lane == 0) base = atomicAdd(&a.cand_cnt[hq0 + hg], __popc(bits));
       base = __shfl_sync(0xffffffffu, base, 0);
       const int idx = base + __popc(bits & ((1u << lane) - 1u));
-      if (pred && idx < kCandPages) a.cand[(hq0 + hg) * kCandPages + idx] = rank;
+      if (pred) a.cand[(hq0 + hg) * a.cap_pages + idx] = rank;  // a page enters once per head
     }
   }
   // the last block of this (sequence, KV head) solves τ
@@ -335,57 +337,103 @@ __global__ void __launch_bounds__(kThreads) pass_a_kernel(DecodeArgs a) {
   __syncthreads();
   if (!last_sh) return;
   __threadfence();
-  if (warp >= G) return;
-  const int hg = warp;
-  const size_t hs = hq0 + hg;
-  const int cap_h = kSolveCap / G;
-  float* zs = zc + hg * cap_h;
-  const float zm = ord_dec(__ldcg(&a.zmax[hs]));
-  float tau_f = CUDART_NAN_F;
-  double tau_d = CUDART_NAN;
-  if (zm > -CUDART_INF_F) {
-    const float T0 = zm - 1.0f;
-    const int nc = __ldcg(&a.cand_cnt[hs]);
-    const bool all = nc > kCandPages;  // list overflowed: consider every page
-    const int np = all ? n_sel : nc;
-    const int32_t* clist = a.cand + hs * kCandPages;
-    const float* zbase = a.z + skv * a.cap_pages * (size_t)P * G;
-    const float* pmbase = a.pmax + skv * a.cap_pages * (size_t)G;
-    int m = 0;
-    for (int k0 = 0; k0 < np; k0 += 32) {
-      const int k = k0 + lane;
-      const int rank = k < np ? (all ? k : __ldcg(clist + k)) : -1;
-      const float pmv = rank >= 0 ? __ldcg(pmbase + (size_t)rank * G + hg) : -CUDART_INF_F;
-      uint32_t bits = __ballot_sync(0xffffffffu, pmv > T0);
-      while (bits) {
-        const int b = __ffs(bits) - 1;
-        bits &= bits - 1u;
-        const int r = __shfl_sync(0xffffffffu, rank, b);
-        const float* zr = zbase + (size_t)r * P * G;
-        const float v = lane < P ? __ldcg(zr + lane * G + hg) : -CUDART_INF_F;
-        const bool pv = v > T0;
-        const uint32_t vb = __ballot_sync(0xffffffffu, pv);
-        const int pos = m + __popc(vb & ((1u << lane) - 1u));
-        if (pv && pos < cap_h) zs[pos] = v;
-        m += __popc(vb);
+  // Exact τ of the G query heads, block-parallel:
+  //  A  keep the listed candidate pages whose max clears T0 = z_max − 1;
+  //  B  τ_lb = exact threshold of those page maxima alone: they are real
+  //     token scores, so their normaliser is below the full one and τ ≥ τ_lb;
+  //  C  gather the scores above τ_lb from pages whose max clears τ_lb;
+  //  D  one warp per head solves exactly on that set, starting from τ_lb.
+  const int capP = kSolveCap / 4 / G;   // candidate pages per head (ranks + maxima)
+  const int capZ = kSolveCap / 2 / G;   // candidate scores per head
+  int* pr = reinterpret_cast<int*>(pool);
+  float* pv = pool + kSolveCap / 4;
+  float* zc = pool + kSolveCap / 2;
+  const float* zbase = a.z + skv * a.cap_pages * (size_t)P * G;
+  const float* pmbase = a.pmax + skv * a.cap_pages * (size_t)G;
+  const int32_t* clist = a.cand + hq0 * a.cap_pages;
+  if (tid < G) {
+    const float zm = ord_dec(__ldcg(&a.zmax[hq0 + tid]));
+    T0_sh[tid] = zm > -CUDART_INF_F ? zm - 1.0f : CUDART_INF_F;
+    nc_sh[tid] = min(__ldcg(&a.cand_cnt[hq0 + tid]), a.cap_pages);
+    np_sh[tid] = 0;
+    nz_sh[tid] = 0;
+  }
+  __syncthreads();
+  int E = 0;
+  for (int h = 0; h < G; ++h) E += nc_sh[h];
+  for (int e = tid; e < E; e += kThreads) {  // A
+    int h = 0, k = e;
+    while (k >= nc_sh[h]) {
+      k -= nc_sh[h];
+      ++h;
+    }
+    const int rank = __ldcg(clist + (size_t)h * a.cap_pages + k);
+    const float pmv = __ldcg(pmbase + (size_t)rank * G + h);
+    if (pmv > T0_sh[h]) {
+      const int pos = atomicAdd(&np_sh[h], 1);
+      if (pos < capP) {
+        pr[h * capP + pos] = rank;
+        pv[h * capP + pos] = pmv;
       }
     }
-    __syncwarp();
+  }
+  __syncthreads();
+  if (warp < G) {  // B
+    const int h = warp;
+    float tlb = T0_sh[h];
+    const int np = np_sh[h];
+    if (np > 0 && np <= capP) {
+      SolveSrc src;
+      src.zs = pv + h * capP;
+      src.m = np;
+      src.big = false;
+      bool ok;
+      tlb = fmaxf(tlb, (float)solve_tau_warp(src, (double)T0_sh[h], a.beta, ok));
+    }
+    if (lane == 0) {
+      tlb_sh[h] = tlb;
+      big_sh[h] = np > capP;
+    }
+  }
+  __syncthreads();
+  int W2 = 0;
+  for (int h = 0; h < G; ++h) W2 += min(np_sh[h], capP) * P;
+  for (int w = tid; w < W2; w += kThreads) {  // C
+    int h = 0, k = w;
+    while (k >= min(np_sh[h], capP) * P) {
+      k -= min(np_sh[h], capP) * P;
+      ++h;
+    }
+    const int j = k / P, t = k % P;
+    if (!(pv[h * capP + j] > tlb_sh[h])) continue;
+    const float v = __ldcg(zbase + ((size_t)pr[h * capP + j] * P + t) * G + h);
+    if (v > tlb_sh[h]) {
+      const int pos = atomicAdd(&nz_sh[h], 1);
+      if (pos < capZ) zc[h * capZ + pos] = v;
+    }
+  }
+  __syncthreads();
+  if (warp >= G) return;
+  const int hg = warp;  // D
+  const size_t hs = hq0 + hg;
+  float tau_f = CUDART_NAN_F;
+  double tau_d = CUDART_NAN;
+  if (T0_sh[hg] < CUDART_INF_F) {
     SolveSrc src;
-    src.zs = zs;
-    src.m = m;
-    src.big = m > cap_h;
-    src.pages = all ? nullptr : clist;
-    src.np = np;
+    src.zs = zc + hg * capZ;
+    src.m = nz_sh[hg];
+    src.big = big_sh[hg] || nz_sh[hg] > capZ;
+    src.pages = clist + (size_t)hg * a.cap_pages;
+    src.np = nc_sh[hg];
     src.zbase = zbase;
     src.pmbase = pmbase;
     src.P = P;
     src.G = G;
     src.hg = hg;
-    src.T0 = T0;
-    if ((src.big || all) && lane == 0) raise_flag(a.status, ENTMAXKV_DEV_CAND_OVERFLOW);
+    src.T0 = src.big ? T0_sh[hg] : tlb_sh[hg];
+    if (src.big && lane == 0) raise_flag(a.status, ENTMAXKV_DEV_CAND_OVERFLOW);
     bool ok;
-    tau_d = solve_tau_warp(src, (double)T0, a.beta, ok);
+    tau_d = solve_tau_warp(src, (double)src.T0, a.beta, ok);
     if (!ok && lane == 0) raise_flag(a.status, ENTMAXKV_DEV_TAU_NOCONV);
     tau_f = (float)tau_d;
   }

@@ -116,29 +116,35 @@ __global__ void __cluster_dims__(kTauhatCluster, 1, 1) __launch_bounds__(kThread
       slot[it & 1] = make_double2(sf, sd);
     }
     cluster.sync();
-    if (tid == 0) {
-      double F = 0.0, dF = 0.0;  // same order in every block: identical totals
-      for (int r = 0; r < kTauhatCluster; ++r) {
-        const double2 v = cluster.map_shared_rank(&slot[0], r)[it & 1];
-        F += v.x;
-        dF += v.y;
+    if (warp == 0) {
+      // lane r reads block r's partial sums; a fixed-order tree sum gives every
+      // block bit-identical totals, hence identical steps
+      double2 v = lane < kTauhatCluster ? cluster.map_shared_rank(&slot[0], lane)[it & 1]
+                                        : make_double2(0.0, 0.0);
+#pragma unroll
+      for (int o = kTauhatCluster / 2; o >= 1; o >>= 1) {
+        v.x += __shfl_down_sync(0xffffffffu, v.x, o);
+        v.y += __shfl_down_sync(0xffffffffu, v.y, o);
       }
-      if (F >= 1.0) lo = tau;
-      else hi = tau;
-      double next;
-      bool stop;
-      if (F == 1.0) {
-        next = tau;
-        stop = true;
-      } else {
-        next = (F > 0.0 && dF > 0.0) ? tau + log(F) * F / dF : CUDART_NAN;  // Newton on log F
-        if (!(next > lo && next < hi)) next = isinf(hi) ? lo + 1.0 : 0.5 * (lo + hi);
-        const double tol = 1e-6 * fmax(1.0, fabs(next));
-        stop = fabs(next - tau) <= tol || (hi - lo) <= tol;
+      if (lane == 0) {
+        const double F = v.x, dF = v.y;
+        if (F >= 1.0) lo = tau;
+        else hi = tau;
+        double next;
+        bool stop;
+        if (F == 1.0) {
+          next = tau;
+          stop = true;
+        } else {
+          next = (F > 0.0 && dF > 0.0) ? tau + log(F) * F / dF : CUDART_NAN;  // Newton on log F
+          if (!(next > lo && next < hi)) next = isinf(hi) ? lo + 1.0 : 0.5 * (lo + hi);
+          const double tol = 1e-6 * fmax(1.0, fabs(next));
+          stop = fabs(next - tau) <= tol || (hi - lo) <= tol;
+        }
+        tau = next;
+        done_sh = stop ? 1 : 0;
+        tau_sh = tau;
       }
-      tau = next;
-      done_sh = stop ? 1 : 0;
-      tau_sh = tau;
     }
     __syncthreads();
     if (done_sh) {
