@@ -298,7 +298,12 @@ def policy_table(wl, B, flush, qbuf, timed, K, peaks, names):
         mean = statistics.mean(us)
         view = B.workspace_layout(cache, spec.batch, pol, budget)
         nbytes, counts = algorithmic_bytes(wl, name, o, ws, view)
-        rows[name] = {"us": round(mean, 2), "bytes": nbytes,
+        evs = B.stage_events()
+        flush.zero_()
+        B.decode(cache, qbuf, ALPHA, pol, budget, MARGIN, flags, workspace=ws, outputs=o, events=evs)
+        torch.cuda.synchronize()
+        stage = {n: round(evs[k].elapsed_time(evs[k + 1]) * 1e3, 1) for k, n in enumerate(B.STAGES)}
+        rows[name] = {"us": round(mean, 2), "bytes": nbytes, "stage_us_once": stage,
                       "gbs": round(nbytes / (mean * 1e-6) / 1e9, 1),
                       "frac_8tbs": round(nbytes / (mean * 1e-6) / 1e9 / NOMINAL_HBM_GBS, 4),
                       **counts}

@@ -122,9 +122,9 @@ __device__ __forceinline__ float warp_max(float v) {
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
   return v;
 }
-__device__ __forceinline__ double warp_min_d(double v) {
+__device__ __forceinline__ float warp_min_f(float v) {
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmin(v, __shfl_xor_sync(0xffffffffu, v, o));
+  for (int o = 16; o > 0; o >>= 1) v = fminf(v, __shfl_xor_sync(0xffffffffu, v, o));
   return v;
 }
 
@@ -209,6 +209,50 @@ __device__ __forceinline__ void gauss_moment(float a, float sg, bool beta2, floa
   } else {
     g = a * Phi + sg * phi;
     dg = Phi;
+  }
+}
+
+// E[(a + σZ)_+^β] and its derivative from a shared-memory copy of the node
+// table (H, H1, Φ, φ) of normal_table.cuh by cubic Hermite interpolation in
+// t = a/σ: with H' = 2·H1, H1' = Φ, Φ' = φ the nodes carry their own slopes.
+//   β = 2: G = σ²·H(t), dG/da = 2σ·H1(t);   β = 1: G = σ·H1(t), dG/da = Φ(t).
+// Left of the table G and dG are below 1e-34 relative to σ^β and are taken as
+// 0; right of it Φ = 1 and φ = 0 to float precision.
+__device__ __forceinline__ void gauss_moment_tab(const float4* tab, float a, float sg, float inv_sg,
+                                                 bool beta2, float lo, float inv_h, int n_int,
+                                                 float& g, float& dg) {
+  if (!(sg > 0.0f)) {
+    const float ap = fmaxf(a, 0.0f);
+    g = beta2 ? ap * ap : ap;
+    dg = beta2 ? 2.0f * ap : (a > 0.0f ? 1.0f : 0.0f);
+    return;
+  }
+  const float t = a * inv_sg;
+  const float x = (t - lo) * inv_h;
+  if (!(x >= 0.0f)) {
+    g = dg = 0.0f;
+    return;
+  }
+  if (x >= (float)n_int) {
+    g = beta2 ? fmaf(a, a, sg * sg) : a;
+    dg = beta2 ? 2.0f * a : 1.0f;
+    return;
+  }
+  const int i = (int)x;
+  const float u = x - (float)i;
+  const float4 n0 = tab[i], n1 = tab[i + 1];
+  const float u2 = u * u, u3 = u2 * u;
+  const float h01 = fmaf(-2.0f, u3, 3.0f * u2), h00 = 1.0f - h01;
+  const float hh = 1.0f / inv_h;
+  const float h10 = hh * (u3 - 2.0f * u2 + u), h11 = hh * (u3 - u2);
+  const float H1 = fmaf(h00, n0.y, fmaf(h10, n0.z, fmaf(h01, n1.y, h11 * n1.z)));
+  if (beta2) {
+    const float H = fmaf(h00, n0.x, fmaf(2.0f * h10, n0.y, fmaf(h01, n1.x, 2.0f * h11 * n1.y)));
+    g = sg * sg * H;
+    dg = 2.0f * sg * H1;
+  } else {
+    g = sg * H1;
+    dg = fmaf(h00, n0.z, fmaf(h10, n0.w, fmaf(h01, n1.z, h11 * n1.w)));
   }
 }
 

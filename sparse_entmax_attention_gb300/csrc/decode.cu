@@ -104,31 +104,32 @@ __device__ __forceinline__ void for_each_cand(const SolveSrc& S, F&& f) {
   }
 }
 
+// Float accumulation per candidate (GB300 runs FP64 at a small fraction of
+// the FP32 rate): τ is carried as a double and split into hi + lo floats so
+// that y = z − τ keeps its accuracy; only the per-iteration totals are double.
 __device__ double solve_tau_warp(const SolveSrc& S, double tau0, float beta, bool& ok) {
   double tau = tau0;
   ok = false;
   const bool b2 = beta == 2.0f, b1 = beta == 1.0f;
   for (int it = 0; it < kTauIters; ++it) {
-    double k = 0.0, s1 = 0.0, s2 = 0.0, sb = 0.0, sb1 = 0.0, mn = CUDART_INF;
+    const float th = (float)tau, tl = (float)(tau - (double)th);
+    float kf = 0.0f, s1f = 0.0f, s2f = 0.0f, sbf = 0.0f, sb1f = 0.0f, mnf = CUDART_INF_F;
     for_each_cand(S, [&](float zf) {
-      const double y = (double)zf - tau;
-      if (y > 0.0) {
-        k += 1.0;
-        s1 += y;
-        s2 += y * y;
-        mn = fmin(mn, y);
+      const float y = (zf - th) - tl;
+      if (y > 0.0f) {
+        kf += 1.0f;
+        s1f += y;
+        s2f = fmaf(y, y, s2f);
+        mnf = fminf(mnf, y);
         if (!b2 && !b1) {
-          sb += pow(y, (double)beta);
-          sb1 += pow(y, (double)beta - 1.0);
+          sbf += powf(y, beta);
+          sb1f += powf(y, beta - 1.0f);
         }
       }
     });
-    k = warp_sum(k);
-    s1 = warp_sum(s1);
-    s2 = warp_sum(s2);
-    sb = warp_sum(sb);
-    sb1 = warp_sum(sb1);
-    mn = warp_min_d(mn);
+    const double k = (double)warp_sum(kf), s1 = (double)warp_sum(s1f), s2 = (double)warp_sum(s2f);
+    const double sb = (double)warp_sum(sbf), sb1 = (double)warp_sum(sb1f);
+    const double mn = (double)warp_min_f(mnf);
     if (k == 0.0) break;  // cannot happen while τ < z_max
     double next;
     if (b2) {
@@ -153,13 +154,13 @@ __device__ double solve_tau_warp(const SolveSrc& S, double tau0, float beta, boo
       next = tau + d;
     } else {
       next = tau + (sb - 1.0) / ((double)beta * sb1);
-      if (fabs(next - tau) <= 1e-13 * fmax(1.0, fabs(tau))) {
+      if (fabs(next - tau) <= 1e-9 * fmax(1.0, fabs(tau))) {
         tau = next;
         ok = true;
         break;
       }
     }
-    if (!(next > tau)) {  // no progress left in double precision
+    if (!(next > tau)) {  // no progress left
       ok = true;
       break;
     }

@@ -23,6 +23,7 @@
 #include <cooperative_groups.h>
 
 #include "common.cuh"
+#include "normal_table.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -38,9 +39,10 @@ __device__ __forceinline__ float sqrt_2ln(int n, int P, float c_full) {
   return n == P ? c_full : sqrtf(2.0f * logf((float)n));
 }
 
-__global__ void __cluster_dims__(kTauhatCluster, 1, 1) __launch_bounds__(kThreads)
+__global__ void __cluster_dims__(kTauhatCluster, 1, 1) __launch_bounds__(kThreads, 2)
     tauhat_kernel(DecodeArgs a) {
   cg::cluster_group cluster = cg::this_cluster();
+  __shared__ float4 tab[EKV_NTAB_N + 1];
   __shared__ double2 slot[2];
   __shared__ double red_f[kWarps], red_d[kWarps];
   __shared__ double tau_sh;
@@ -59,6 +61,7 @@ __global__ void __cluster_dims__(kTauhatCluster, 1, 1) __launch_bounds__(kThread
   if (!(M > -CUDART_INF)) return;  // no readable page
   const bool beta2 = a.beta == 2.0f;
   const float2* ms = a.gauss_ms + ((size_t)s * a.Hq + h) * a.maxp;
+  for (int i = tid; i <= EKV_NTAB_N; i += kThreads) tab[i] = kNormTab[i];
   const int words = (n_pages + 31) / 32;
   const int chunk = ((words + kTauhatCluster - 1) / kTauhatCluster) * 32;
   const int p_lo = rank * chunk, p_hi = min(n_pages, p_lo + chunk);
@@ -68,7 +71,7 @@ __global__ void __cluster_dims__(kTauhatCluster, 1, 1) __launch_bounds__(kThread
   // that are re-read from memory.
   constexpr int kRegPages = 16;
   float2 mr[kRegPages];
-  float nr[kRegPages];
+  float ir[kRegPages], nr[kRegPages];
 #pragma unroll
   for (int k = 0; k < kRegPages; ++k) {
     const int p = p_lo + tid + k * kThreads;
@@ -79,7 +82,9 @@ __global__ void __cluster_dims__(kTauhatCluster, 1, 1) __launch_bounds__(kThread
       mr[k] = make_float2(-CUDART_INF_F, 0.0f);
       nr[k] = 0.0f;
     }
+    ir[k] = mr[k].y > 0.0f ? 1.0f / mr[k].y : 0.0f;
   }
+  __syncthreads();  // node table in shared memory
   double lo = M - 1.0, hi = CUDART_INF, tau = lo;
   bool converged = false;
   int it = 0;
@@ -89,19 +94,21 @@ __global__ void __cluster_dims__(kTauhatCluster, 1, 1) __launch_bounds__(kThread
 #pragma unroll
     for (int k = 0; k < kRegPages; ++k) {
       float g, dg;
-      gauss_moment(mr[k].x - tf, mr[k].y, beta2, g, dg);
+      gauss_moment_tab(tab, mr[k].x - tf, mr[k].y, ir[k], beta2, EKV_NTAB_LO, EKV_NTAB_INV_H,
+                       EKV_NTAB_N, g, dg);
       f = fmaf(nr[k], g, f);
       df = fmaf(nr[k], dg, df);
     }
     for (int p = p_lo + tid + kRegPages * kThreads; p < p_hi; p += kThreads) {
       const float2 v = ms[p];
       float g, dg;
-      gauss_moment(v.x - tf, v.y, beta2, g, dg);
+      gauss_moment_tab(tab, v.x - tf, v.y, v.y > 0.0f ? 1.0f / v.y : 0.0f, beta2, EKV_NTAB_LO,
+                       EKV_NTAB_INV_H, EKV_NTAB_N, g, dg);
       const float np = (float)page_tokens(p, n_pages, L, a.P);
       f = fmaf(np, g, f);
       df = fmaf(np, dg, df);
     }
-    const double fd = warp_sum((double)f), dd = warp_sum((double)df);
+    const double fd = (double)warp_sum(f), dd = (double)warp_sum(df);
     if (lane == 0) {
       red_f[warp] = fd;
       red_d[warp] = dd;
@@ -136,7 +143,8 @@ __global__ void __cluster_dims__(kTauhatCluster, 1, 1) __launch_bounds__(kThread
           next = tau;
           stop = true;
         } else {
-          next = (F > 0.0 && dF > 0.0) ? tau + log(F) * F / dF : CUDART_NAN;  // Newton on log F
+          // Newton on log F (a float log is ample for the step)
+          next = (F > 0.0 && dF > 0.0) ? tau + (double)logf((float)F) * (F / dF) : CUDART_NAN;
           if (!(next > lo && next < hi)) next = isinf(hi) ? lo + 1.0 : 0.5 * (lo + hi);
           const double tol = 1e-6 * fmax(1.0, fabs(next));
           stop = fabs(next - tau) <= tol || (hi - lo) <= tol;

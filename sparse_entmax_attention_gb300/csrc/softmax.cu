@@ -14,10 +14,10 @@
 namespace ekv {
 
 template <typename T, int D, int GP>
-__global__ void __launch_bounds__(kThreads) softmax_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(kThreads, 2) softmax_kernel(DecodeArgs a) {
   constexpr int VEC = 16 / sizeof(T), LPR = D / VEC, TG = 32 / LPR;
   constexpr int MAXT = 32 / TG;                  // tokens per lane in a 32-token page
-  constexpr int CH = MAXT < 16 ? MAXT : 16;      // V rows in flight per lane
+  constexpr int CH = MAXT < 8 ? MAXT : 8;        // V rows in flight per lane
   __shared__ float qs[8][D];
   __shared__ float sbuf[kWarps][32][GP];
   __shared__ float pmx[kWarps][8];
@@ -100,14 +100,6 @@ __global__ void __launch_bounds__(kThreads) softmax_kernel(DecodeArgs a) {
         if (lane == 0) pmx[warp][h] = mm;
       }
     }
-    // issue the page's V loads before the rescale so they overlap it
-    const T* vs = (const T*)a.v_pool + slab_off + dc * VEC;
-    uint4 raw[MAXT];
-#pragma unroll
-    for (int u = 0; u < MAXT; ++u) {
-      const int t = tg + TG * u;
-      if (u < CH) raw[u] = t < nv ? ld_stream(vs + (size_t)t * D) : make_uint4(0u, 0u, 0u, 0u);
-    }
     __syncwarp();
 #pragma unroll
     for (int h = 0; h < GP; ++h) {
@@ -120,26 +112,34 @@ __global__ void __launch_bounds__(kThreads) softmax_kernel(DecodeArgs a) {
         m[h] = mn;
       }
     }
+    const T* vs = (const T*)a.v_pool + slab_off + dc * VEC;
+    for (int c0 = 0; c0 < MAXT; c0 += CH) {
+      uint4 raw[CH];
 #pragma unroll
-    for (int u = 0; u < MAXT; ++u) {
-      const int t = tg + TG * u;
-      if (u >= CH && t < nv) raw[u] = ld_stream(vs + (size_t)t * D);  // beyond the first batch
-      if (t < nv) {
-        float v[VEC];
-        if constexpr (sizeof(T) == 2) {
-          v[0] = bf_lo(raw[u].x); v[1] = bf_hi(raw[u].x); v[2] = bf_lo(raw[u].y); v[3] = bf_hi(raw[u].y);
-          v[4] = bf_lo(raw[u].z); v[5] = bf_hi(raw[u].z); v[6] = bf_lo(raw[u].w); v[7] = bf_hi(raw[u].w);
-        } else {
-          v[0] = __uint_as_float(raw[u].x); v[1] = __uint_as_float(raw[u].y);
-          v[2] = __uint_as_float(raw[u].z); v[3] = __uint_as_float(raw[u].w);
-        }
+      for (int u = 0; u < CH; ++u) {
+        const int t = tg + TG * (c0 + u);
+        raw[u] = t < nv ? ld_stream(vs + (size_t)t * D) : make_uint4(0u, 0u, 0u, 0u);
+      }
 #pragma unroll
-        for (int h = 0; h < GP; ++h) {
-          if (h < G && m[h] > -CUDART_INF_F) {
-            const float p = exp2f(sbuf[warp][t][h] - m[h]);
-            l[h] += p;
+      for (int u = 0; u < CH; ++u) {
+        const int t = tg + TG * (c0 + u);
+        if (t < nv) {
+          float v[VEC];
+          if constexpr (sizeof(T) == 2) {
+            v[0] = bf_lo(raw[u].x); v[1] = bf_hi(raw[u].x); v[2] = bf_lo(raw[u].y); v[3] = bf_hi(raw[u].y);
+            v[4] = bf_lo(raw[u].z); v[5] = bf_hi(raw[u].z); v[6] = bf_lo(raw[u].w); v[7] = bf_hi(raw[u].w);
+          } else {
+            v[0] = __uint_as_float(raw[u].x); v[1] = __uint_as_float(raw[u].y);
+            v[2] = __uint_as_float(raw[u].z); v[3] = __uint_as_float(raw[u].w);
+          }
 #pragma unroll
-            for (int j = 0; j < VEC; ++j) acc[h][j] = fmaf(p, v[j], acc[h][j]);
+          for (int h = 0; h < GP; ++h) {
+            if (h < G && m[h] > -CUDART_INF_F) {
+              const float p = exp2f(sbuf[warp][t][h] - m[h]);
+              l[h] += p;
+#pragma unroll
+              for (int j = 0; j < VEC; ++j) acc[h][j] = fmaf(p, v[j], acc[h][j]);
+            }
           }
         }
       }
