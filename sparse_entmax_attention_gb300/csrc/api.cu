@@ -95,7 +95,7 @@ static int compute_layout(const entmaxkv_config* c, int S, int policy, int budge
   L.bbox_u = policy == ENTMAXKV_POLICY_TOPK ? take(nq * (size_t)maxp * 4) : none;
   L.bbox_uhat = policy == ENTMAXKV_POLICY_TOPK ? take(nk * (size_t)maxp * 4) : none;
   L.gauss_ms = policy == ENTMAXKV_POLICY_GAUSSIAN ? take(nq * (size_t)maxp * 8) : none;
-  L.cand = entmax ? take(nq * (size_t)cap * 4) : none;
+  L.cand = entmax ? take(nq * (size_t)cap * 8) : none;
   L.z = entmax ? take(nk * (size_t)cap * P * G * 4) : none;
   L.pmax = entmax ? take(nk * (size_t)cap * G * 4) : none;
   L.pstride = (G * D + 2 * G + 3) & ~3;
@@ -272,7 +272,7 @@ static int32_t decode_impl(const entmaxkv_config* cfg, const entmaxkv_cache* cac
   a.bbox_u = at<float>(workspace, L.bbox_u);
   a.bbox_uhat = at<float>(workspace, L.bbox_uhat);
   a.gauss_ms = at<float2>(workspace, L.gauss_ms);
-  a.cand = at<int32_t>(workspace, L.cand);
+  a.cand = at<int2>(workspace, L.cand);
   a.z = at<float>(workspace, L.z);
   a.pmax = at<float>(workspace, L.pmax);
   a.partial = at<float>(workspace, L.partial);

@@ -61,7 +61,7 @@ struct DecodeArgs {
   float* bbox_u;       // [S][Hq][maxp]
   float* bbox_uhat;    // [S][Hkv][maxp]
   float2* gauss_ms;    // [S][Hq][maxp]
-  int32_t* cand;       // [S][Hq][cap_pages] ranks of candidate pages
+  int2* cand;          // [S][Hq][cap_pages] candidate pages: (rank, page max z bits)
   float* z;            // [S][Hkv][cap_pages][P][G]
   float* pmax;         // [S][Hkv][cap_pages][G]
   float* partial;      // [S][Hkv][splits][pstride]: acc [G][D], then (m, l) per head

@@ -77,13 +77,12 @@ __device__ void block_page_range(const DecodeArgs& a, int s, int kvh, int n_page
 struct SolveSrc {
   const float* zs;      // compacted candidates (shared memory)
   int m;
-  bool big;             // candidates did not fit: walk the pages instead
-  const int32_t* pages; // candidate page ranks (nullptr = every rank < np)
+  bool big;             // candidates did not fit: walk the candidate pages instead
+  const int2* pages;    // candidate pages (rank, page max bits)
   int np;
   const float* zbase;   // z of this (sequence, KV head): [rank][P][G]
-  const float* pmbase;  // page max z: [rank][G]
   int P, G, hg;
-  float T0;
+  float T0;             // every score that can carry weight is above T0
 };
 
 template <class F>
@@ -93,13 +92,19 @@ __device__ __forceinline__ void for_each_cand(const SolveSrc& S, F&& f) {
     for (int i = lane; i < S.m; i += 32) f(S.zs[i]);
     return;
   }
-  for (int k = 0; k < S.np; ++k) {
-    const int rank = S.pages ? __ldcg(S.pages + k) : k;
-    if (!(__ldcg(S.pmbase + (size_t)rank * S.G + S.hg) > S.T0)) continue;
-    const float* zr = S.zbase + (size_t)rank * S.P * S.G;
-    for (int t = lane; t < S.P; t += 32) {
-      const float v = __ldcg(zr + t * S.G + S.hg);
-      if (v > S.T0) f(v);
+  for (int k0 = 0; k0 < S.np; k0 += 32) {
+    const int k = k0 + lane;
+    const int2 e = k < S.np ? __ldcg(S.pages + k) : make_int2(0, __float_as_int(-CUDART_INF_F));
+    uint32_t bits = __ballot_sync(0xffffffffu, __int_as_float(e.y) > S.T0);
+    while (bits) {
+      const int b = __ffs(bits) - 1;
+      bits &= bits - 1u;
+      const int rank = __shfl_sync(0xffffffffu, e.x, b);
+      const float* zr = S.zbase + (size_t)rank * S.P * S.G;
+      for (int t = lane; t < S.P; t += 32) {
+        const float v = __ldcg(zr + t * S.G + S.hg);
+        if (v > S.T0) f(v);
+      }
     }
   }
 }
@@ -127,44 +132,45 @@ __device__ double solve_tau_warp(const SolveSrc& S, double tau0, float beta, boo
         }
       }
     });
-    const double k = (double)warp_sum(kf), s1 = (double)warp_sum(s1f), s2 = (double)warp_sum(s2f);
-    const double sb = (double)warp_sum(sbf), sb1 = (double)warp_sum(sb1f);
-    const double mn = (double)warp_min_f(mnf);
-    if (k == 0.0) break;  // cannot happen while τ < z_max
-    double next;
+    const float k = warp_sum(kf), s1 = warp_sum(s1f), s2 = warp_sum(s2f);
+    const float sb = warp_sum(sbf), sb1 = warp_sum(sb1f);
+    const float mn = warp_min_f(mnf);
+    if (k == 0.0f) break;  // cannot happen while τ < z_max
+    float step;
     if (b2) {
-      // root t = τ + δ of Σ_S (y − δ)² = 1 on the branch δ ≤ min y
-      const double disc = s1 * s1 - k * (s2 - 1.0);
-      if (disc >= 0.0) {
-        const double d = (s1 - sqrt(disc)) / k;
-        if (d >= 0.0 && d <= mn) {
-          tau += d;
+      // root t = τ + δ of Σ_S (y − δ)² = 1 on the branch δ ≤ min y, in the
+      // conjugate form δ = (s2 − 1)/(s1 + sqrt(s1² − k(s2 − 1))) (no cancellation)
+      const float disc = s1 * s1 - k * (s2 - 1.0f);
+      if (disc >= 0.0f) {
+        const float d = (s2 - 1.0f) / (s1 + sqrtf(disc));
+        if (d >= 0.0f && d <= mn) {
+          tau += (double)d;
           ok = true;
           break;
         }
       }
-      next = tau + (s2 - 1.0) / (2.0 * s1);
+      step = (s2 - 1.0f) / (2.0f * s1);
     } else if (b1) {
-      const double d = (s1 - 1.0) / k;
-      if (d >= 0.0 && d <= mn) {
-        tau += d;
+      const float d = (s1 - 1.0f) / k;
+      if (d >= 0.0f && d <= mn) {
+        tau += (double)d;
         ok = true;
         break;
       }
-      next = tau + d;
+      step = d;
     } else {
-      next = tau + (sb - 1.0) / ((double)beta * sb1);
-      if (fabs(next - tau) <= 1e-9 * fmax(1.0, fabs(tau))) {
-        tau = next;
+      step = (sb - 1.0f) / (beta * sb1);
+      if (fabsf(step) <= 1e-7f * fmaxf(1.0f, fabsf((float)tau))) {
+        tau += (double)step;
         ok = true;
         break;
       }
     }
-    if (!(next > tau)) {  // no progress left
+    if (!(step > 0.0f)) {  // no progress left
       ok = true;
       break;
     }
-    tau = next;
+    tau += (double)step;
   }
   return tau;
 }
@@ -183,7 +189,7 @@ __global__ void __launch_bounds__(kThreads) pass_a_kernel(DecodeArgs a) {
   __shared__ int last_sh;
   __shared__ __align__(16) float pool[kSolveCap];  // last block: page and score candidates
   __shared__ float T0_sh[8], tlb_sh[8];
-  __shared__ int nc_sh[8], np_sh[8], nz_sh[8], big_sh[8];
+  __shared__ int nc_sh[8], np_sh[8], nz_sh[8];
   const int split = blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = a.G, P = a.P;
@@ -328,7 +334,8 @@ __global__ void __launch_bounds__(kThreads) pass_a_kernel(DecodeArgs a) {
       if (lane == 0) base = atomicAdd(&a.cand_cnt[hq0 + hg], __popc(bits));
       base = __shfl_sync(0xffffffffu, base, 0);
       const int idx = base + __popc(bits & ((1u << lane) - 1u));
-      if (pred) a.cand[(hq0 + hg) * a.cap_pages + idx] = rank;  // a page enters once per head
+      if (pred)  // a page enters a head's list at most once
+        a.cand[(hq0 + hg) * a.cap_pages + idx] = make_int2(rank, __float_as_int(pm[hg]));
     }
   }
   // the last block of this (sequence, KV head) solves τ
@@ -340,18 +347,17 @@ __global__ void __launch_bounds__(kThreads) pass_a_kernel(DecodeArgs a) {
   __threadfence();
   // Exact τ of the G query heads, block-parallel:
   //  A  keep the listed candidate pages whose max clears T0 = z_max − 1;
-  //  B  τ_lb = exact threshold of those page maxima alone: they are real
-  //     token scores, so their normaliser is below the full one and τ ≥ τ_lb;
-  //  C  gather the scores above τ_lb from pages whose max clears τ_lb;
+  //  B  τ_lb = exact threshold of (a subset of) those page maxima: they are
+  //     real token scores, so their normaliser is below the full one, τ ≥ τ_lb;
+  //  C  gather the scores above τ_lb from the pages whose max clears τ_lb
+  //     (a warp per page, lanes over its tokens);
   //  D  one warp per head solves exactly on that set, starting from τ_lb.
-  const int capP = kSolveCap / 4 / G;   // candidate pages per head (ranks + maxima)
-  const int capZ = kSolveCap / 2 / G;   // candidate scores per head
-  int* pr = reinterpret_cast<int*>(pool);
-  float* pv = pool + kSolveCap / 4;
+  const int capP = kSolveCap / 2 / G;   // page maxima per head for B
+  const int capZ = kSolveCap / 2 / G;   // candidate scores per head for D
+  float* pv = pool;
   float* zc = pool + kSolveCap / 2;
   const float* zbase = a.z + skv * a.cap_pages * (size_t)P * G;
-  const float* pmbase = a.pmax + skv * a.cap_pages * (size_t)G;
-  const int32_t* clist = a.cand + hq0 * a.cap_pages;
+  const int2* clist = a.cand + hq0 * a.cap_pages;
   if (tid < G) {
     const float zm = ord_dec(__ldcg(&a.zmax[hq0 + tid]));
     T0_sh[tid] = zm > -CUDART_INF_F ? zm - 1.0f : CUDART_INF_F;
@@ -360,21 +366,14 @@ __global__ void __launch_bounds__(kThreads) pass_a_kernel(DecodeArgs a) {
     nz_sh[tid] = 0;
   }
   __syncthreads();
-  int E = 0;
-  for (int h = 0; h < G; ++h) E += nc_sh[h];
-  for (int e = tid; e < E; e += kThreads) {  // A
-    int h = 0, k = e;
-    while (k >= nc_sh[h]) {
-      k -= nc_sh[h];
-      ++h;
-    }
-    const int rank = __ldcg(clist + (size_t)h * a.cap_pages + k);
-    const float pmv = __ldcg(pmbase + (size_t)rank * G + h);
-    if (pmv > T0_sh[h]) {
-      const int pos = atomicAdd(&np_sh[h], 1);
-      if (pos < capP) {
-        pr[h * capP + pos] = rank;
-        pv[h * capP + pos] = pmv;
+  for (int h = 0; h < G; ++h) {  // A
+    const int nc = nc_sh[h];
+    const float T0 = T0_sh[h];
+    for (int k = tid; k < nc; k += kThreads) {
+      const float pmv = __int_as_float(__ldcg(clist + (size_t)h * a.cap_pages + k).y);
+      if (pmv > T0) {
+        const int pos = atomicAdd(&np_sh[h], 1);
+        if (pos < capP) pv[h * capP + pos] = pmv;
       }
     }
   }
@@ -382,8 +381,8 @@ __global__ void __launch_bounds__(kThreads) pass_a_kernel(DecodeArgs a) {
   if (warp < G) {  // B
     const int h = warp;
     float tlb = T0_sh[h];
-    const int np = np_sh[h];
-    if (np > 0 && np <= capP) {
+    const int np = min(np_sh[h], capP);
+    if (np > 0) {
       SolveSrc src;
       src.zs = pv + h * capP;
       src.m = np;
@@ -391,26 +390,31 @@ __global__ void __launch_bounds__(kThreads) pass_a_kernel(DecodeArgs a) {
       bool ok;
       tlb = fmaxf(tlb, (float)solve_tau_warp(src, (double)T0_sh[h], a.beta, ok));
     }
-    if (lane == 0) {
-      tlb_sh[h] = tlb;
-      big_sh[h] = np > capP;
-    }
+    if (lane == 0) tlb_sh[h] = tlb;
   }
   __syncthreads();
-  int W2 = 0;
-  for (int h = 0; h < G; ++h) W2 += min(np_sh[h], capP) * P;
-  for (int w = tid; w < W2; w += kThreads) {  // C
-    int h = 0, k = w;
-    while (k >= min(np_sh[h], capP) * P) {
-      k -= min(np_sh[h], capP) * P;
-      ++h;
-    }
-    const int j = k / P, t = k % P;
-    if (!(pv[h * capP + j] > tlb_sh[h])) continue;
-    const float v = __ldcg(zbase + ((size_t)pr[h * capP + j] * P + t) * G + h);
-    if (v > tlb_sh[h]) {
-      const int pos = atomicAdd(&nz_sh[h], 1);
-      if (pos < capZ) zc[h * capZ + pos] = v;
+  for (int h = 0; h < G; ++h) {  // C
+    const int nc = nc_sh[h];
+    const float tlb = tlb_sh[h];
+    for (int k0 = warp * 32; k0 < nc; k0 += kThreads) {
+      const int k = k0 + lane;
+      const int2 e = k < nc ? __ldcg(clist + (size_t)h * a.cap_pages + k)
+                            : make_int2(0, __float_as_int(-CUDART_INF_F));
+      uint32_t bits = __ballot_sync(0xffffffffu, __int_as_float(e.y) > tlb);
+      while (bits) {
+        const int b = __ffs(bits) - 1;
+        bits &= bits - 1u;
+        const int rank = __shfl_sync(0xffffffffu, e.x, b);
+        const float v = lane < P ? __ldcg(zbase + ((size_t)rank * P + lane) * G + h) : -CUDART_INF_F;
+        const bool pvd = v > tlb;
+        const uint32_t vb = __ballot_sync(0xffffffffu, pvd);
+        if (!vb) continue;
+        int base = 0;
+        if (lane == 0) base = atomicAdd(&nz_sh[h], __popc(vb));
+        base = __shfl_sync(0xffffffffu, base, 0);
+        const int pos = base + __popc(vb & ((1u << lane) - 1u));
+        if (pvd && pos < capZ) zc[h * capZ + pos] = v;
+      }
     }
   }
   __syncthreads();
@@ -423,15 +427,14 @@ __global__ void __launch_bounds__(kThreads) pass_a_kernel(DecodeArgs a) {
     SolveSrc src;
     src.zs = zc + hg * capZ;
     src.m = nz_sh[hg];
-    src.big = big_sh[hg] || nz_sh[hg] > capZ;
+    src.big = nz_sh[hg] > capZ;
     src.pages = clist + (size_t)hg * a.cap_pages;
     src.np = nc_sh[hg];
     src.zbase = zbase;
-    src.pmbase = pmbase;
     src.P = P;
     src.G = G;
     src.hg = hg;
-    src.T0 = src.big ? T0_sh[hg] : tlb_sh[hg];
+    src.T0 = tlb_sh[hg];
     if (src.big && lane == 0) raise_flag(a.status, ENTMAXKV_DEV_CAND_OVERFLOW);
     bool ok;
     tau_d = solve_tau_warp(src, (double)src.T0, a.beta, ok);
