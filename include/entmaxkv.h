@@ -54,6 +54,8 @@ typedef enum {
 #define ENTMAXKV_DEV_CAND_OVERFLOW   0x8u  /* informational: the exact-τ solve used its slow full-scan path */
 #define ENTMAXKV_DEV_TAU_NOCONV      0x10u /* the exact-τ solve stopped at its iteration limit              */
 #define ENTMAXKV_DEV_BAD_SEQ_ID      0x20u /* a seq_ids entry outside [0, max_seqs): that sequence skipped  */
+#define ENTMAXKV_DEV_TIMEOUT         0x40u /* a bounded wait on an asynchronous copy ran out; the block
+                                              stopped early and its results are incomplete              */
 
 /* KV storage types. */
 #define ENTMAXKV_F32  0

@@ -24,7 +24,7 @@ POLICIES = {"full": POLICY_FULL, "topk": POLICY_TOPK, "gaussian": POLICY_GAUSSIA
             "softmax": POLICY_SOFTMAX}
 FLAG_DENSE_V = 0x1
 DEV_BAD_PAGE_TABLE, DEV_CAPACITY, DEV_TAUHAT_NOCONV = 0x1, 0x2, 0x4
-DEV_CAND_OVERFLOW, DEV_TAU_NOCONV, DEV_BAD_SEQ_ID = 0x8, 0x10, 0x20
+DEV_CAND_OVERFLOW, DEV_TAU_NOCONV, DEV_BAD_SEQ_ID, DEV_TIMEOUT = 0x8, 0x10, 0x20, 0x40
 
 # Symbols the header declares (kept in step with include/entmaxkv.h by a test).
 EXPORTS = ("entmaxkv_version", "entmaxkv_status_string", "entmaxkv_append",

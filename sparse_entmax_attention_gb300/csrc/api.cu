@@ -8,7 +8,7 @@
 namespace ekv {
 
 constexpr int kSmCount = 152;                 // GB300: grids are sized for its 152 SMs
-constexpr int kTargetBlocks = 4 * kSmCount;   // decode blocks per launch to aim for
+constexpr int kTargetBlocks = 2 * kSmCount;   // decode blocks per launch: one wave at 2 per SM
 
 struct Layout {
   size_t zmax, mmax, cnt_a, cnt_b, cand_cnt, kept_mass, dbar, bitmap, ctrl_end;

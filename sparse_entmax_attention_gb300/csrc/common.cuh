@@ -256,6 +256,48 @@ __device__ __forceinline__ void gauss_moment_tab(const float4* tab, float a, flo
   }
 }
 
+// ---------------------------------------------------------------------------
+// Bulk asynchronous copies (global -> shared) completed on an mbarrier.
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_fence_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Wait for the phase with the given parity to complete; false when the
+// bounded number of polls ran out (the caller flags ENTMAXKV_DEV_TIMEOUT).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+  for (int i = 0; i < (1 << 22); ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+// size bytes from global src to shared dst (both 16-byte aligned, size a
+// multiple of 16), completing `size` transaction bytes on bar.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t size, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(size), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // Block-wide exclusive scan of one int per thread (blockDim multiple of 32).
 // Returns the sum below this thread; `total` receives the block sum.
 __device__ __forceinline__ int block_exclusive_scan(int v, int* sh, int& total) {

@@ -143,7 +143,7 @@ __device__ double solve_tau_warp(const SolveSrc& S, double tau0, float beta, boo
       const float disc = s1 * s1 - k * (s2 - 1.0f);
       if (disc >= 0.0f) {
         const float d = (s2 - 1.0f) / (s1 + sqrtf(disc));
-        if (d >= 0.0f && d <= mn) {
+        if (d >= -1e-7f && d <= mn * (1.0f + 1e-6f) + 1e-7f) {
           tau += (double)d;
           ok = true;
           break;
@@ -152,7 +152,7 @@ __device__ double solve_tau_warp(const SolveSrc& S, double tau0, float beta, boo
       step = (s2 - 1.0f) / (2.0f * s1);
     } else if (b1) {
       const float d = (s1 - 1.0f) / k;
-      if (d >= 0.0f && d <= mn) {
+      if (d >= -1e-7f && d <= mn * (1.0f + 1e-6f) + 1e-7f) {
         tau += (double)d;
         ok = true;
         break;
@@ -166,7 +166,8 @@ __device__ double solve_tau_warp(const SolveSrc& S, double tau0, float beta, boo
         break;
       }
     }
-    if (!(step > 0.0f)) {  // no progress left
+    if (!(step > 1e-7f * fmaxf(1.0f, fabsf((float)tau)))) {  // converged to float resolution
+      if (step > 0.0f) tau += (double)step;
       ok = true;
       break;
     }
@@ -393,27 +394,24 @@ __global__ void __launch_bounds__(kThreads) pass_a_kernel(DecodeArgs a) {
     if (lane == 0) tlb_sh[h] = tlb;
   }
   __syncthreads();
-  for (int h = 0; h < G; ++h) {  // C
+  for (int h = 0; h < G; ++h) {  // C: a lane per candidate page, its token loads in flight together
     const int nc = nc_sh[h];
     const float tlb = tlb_sh[h];
-    for (int k0 = warp * 32; k0 < nc; k0 += kThreads) {
-      const int k = k0 + lane;
-      const int2 e = k < nc ? __ldcg(clist + (size_t)h * a.cap_pages + k)
-                            : make_int2(0, __float_as_int(-CUDART_INF_F));
-      uint32_t bits = __ballot_sync(0xffffffffu, __int_as_float(e.y) > tlb);
-      while (bits) {
-        const int b = __ffs(bits) - 1;
-        bits &= bits - 1u;
-        const int rank = __shfl_sync(0xffffffffu, e.x, b);
-        const float v = lane < P ? __ldcg(zbase + ((size_t)rank * P + lane) * G + h) : -CUDART_INF_F;
-        const bool pvd = v > tlb;
-        const uint32_t vb = __ballot_sync(0xffffffffu, pvd);
-        if (!vb) continue;
-        int base = 0;
-        if (lane == 0) base = atomicAdd(&nz_sh[h], __popc(vb));
-        base = __shfl_sync(0xffffffffu, base, 0);
-        const int pos = base + __popc(vb & ((1u << lane) - 1u));
-        if (pvd && pos < capZ) zc[h * capZ + pos] = v;
+    for (int k = tid; k < nc; k += kThreads) {
+      const int2 e = __ldcg(clist + (size_t)h * a.cap_pages + k);
+      if (!(__int_as_float(e.y) > tlb)) continue;
+      const float* zr = zbase + (size_t)e.x * P * G + h;
+      for (int t0 = 0; t0 < P; t0 += 8) {
+        float v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = __ldcg(zr + (t0 + u) * G);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          if (v[u] > tlb) {
+            const int pos = atomicAdd(&nz_sh[h], 1);
+            if (pos < capZ) zc[h * capZ + pos] = v[u];
+          }
+        }
       }
     }
   }
@@ -489,13 +487,21 @@ __device__ __noinline__ void combine_partials(const DecodeArgs& a, size_t skv, f
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   if (grp < groups) {
     const float* base = a.partial + skv * a.splits * (size_t)a.pstride;
-#pragma unroll 4
-    for (int sp = grp; sp < a.splits; sp += groups) {
-      const float4 v = __ldcg(reinterpret_cast<const float4*>(base + (size_t)sp * a.pstride) + col);
-      acc.x += v.x;
-      acc.y += v.y;
-      acc.z += v.z;
-      acc.w += v.w;
+    for (int sp0 = grp; sp0 < a.splits; sp0 += 8 * groups) {  // 8 loads in flight, summed in order
+      float4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int sp = sp0 + u * groups;
+        v[u] = sp < a.splits ? __ldcg(reinterpret_cast<const float4*>(base + (size_t)sp * a.pstride) + col)
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        acc.x += v[u].x;
+        acc.y += v[u].y;
+        acc.z += v[u].z;
+        acc.w += v[u].w;
+      }
     }
     red4[grp * cols + col] = acc;
   }
@@ -558,50 +564,76 @@ __global__ void __launch_bounds__(kThreads) pass_b_kernel(DecodeArgs a) {
     for (int j = 0; j < VEC; ++j) acc[h][j] = 0.0f;
   float* zw = zs[warp];
 
-  for (int i = warp; i < hi - lo; i += kWarps) {
-    const int rank = lo + i;
-    const float* pm = a.pmax + (skv * a.cap_pages + rank) * (size_t)G;
-    bool need = dense;
+  // The warp takes 32 consecutive ranks of its block's share at a time: lane l
+  // checks rank l's page maxima, and the pages that need V are processed in
+  // turn, each with its z and V loads issued together.
+  const int nb = hi - lo;
+  for (int c0 = warp * 32; c0 < nb; c0 += kThreads) {
+    const int i = c0 + lane;
+    bool need = false;
+    int page = -1;
+    if (i < nb) {
+      const int rank = lo + i;
+      need = dense;
+      const float* pm = a.pmax + (skv * a.cap_pages + rank) * (size_t)G;
 #pragma unroll
-    for (int h = 0; h < GP; ++h)
-      if (h < G) need = need || (__ldcg(pm + h) > tau[h]);
-    if (!need) continue;
-    const int page = bitmap ? __ldcg(&a.sel_list[skv * a.cap_pages + rank]) : rank;
-    const int ph = phys_page(a.block_table, seq, page, a.maxp, a.nphys, nullptr);
-    if (ph < 0) continue;
-    const int nv = min(P, L - page * P);
-    const float* zb = a.z + (skv * a.cap_pages + rank) * (size_t)P * G;
-    for (int e = 4 * lane; e < P * G; e += 128)  // P·G is a multiple of 16
-      *reinterpret_cast<float4*>(zw + e) = __ldcg(reinterpret_cast<const float4*>(zb + e));
-    __syncwarp();
-    const T* vs = (const T*)a.v_pool + ((size_t)ph * a.Hkv + kvh) * P * D + dc * VEC;
-    for (int c0 = 0; c0 < MAXT; c0 += CH) {
-      uint4 raw[CH];
+      for (int h = 0; h < GP; ++h)
+        if (h < G) need = need || (__ldcg(pm + h) > tau[h]);
+      if (need) page = bitmap ? __ldcg(&a.sel_list[skv * a.cap_pages + rank]) : rank;
+    }
+    const int ph_l = need ? phys_page(a.block_table, seq, page, a.maxp, a.nphys, nullptr) : -1;
+    uint32_t bits = __ballot_sync(0xffffffffu, ph_l >= 0);
+    while (bits) {
+      const int b = __ffs(bits) - 1;
+      bits &= bits - 1u;
+      const int rank = lo + c0 + b;
+      const int pg = __shfl_sync(0xffffffffu, page, b);
+      const int ph = __shfl_sync(0xffffffffu, ph_l, b);
+      const int nv = min(P, L - pg * P);
+      const float* zb = a.z + (skv * a.cap_pages + rank) * (size_t)P * G;
+      const T* vs = (const T*)a.v_pool + ((size_t)ph * a.Hkv + kvh) * P * D + dc * VEC;
+      float4 zl[2];
 #pragma unroll
-      for (int u = 0; u < CH; ++u) {
-        const int t = tg + TG * (c0 + u);
-        raw[u] = t < nv ? ld_stream(vs + (size_t)t * D) : make_uint4(0u, 0u, 0u, 0u);
+      for (int u = 0; u < 2; ++u) {  // P·G ≤ 256 floats: two float4 per lane at most
+        const int e = 4 * lane + 128 * u;
+        zl[u] = e < P * G ? __ldcg(reinterpret_cast<const float4*>(zb + e)) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
+      for (int c1 = 0; c1 < MAXT; c1 += CH) {
+        uint4 raw[CH];
 #pragma unroll
-      for (int u = 0; u < CH; ++u) {
-        const int t = tg + TG * (c0 + u);
-        if (t < nv) {
-          float v[VEC];
-          VTraits<T>::unpack(raw[u], v);
+        for (int u = 0; u < CH; ++u) {
+          const int t = tg + TG * (c1 + u);
+          raw[u] = t < nv ? ld_stream(vs + (size_t)t * D) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        if (c1 == 0) {
 #pragma unroll
-          for (int h = 0; h < GP; ++h) {
-            if (h < G) {
-              const float zv = zw[t * G + h];
-              const float p = sizeof(T) == 4 ? pos_pow((float)((double)zv - taud[h]), a.beta)
-                                             : pos_pow(zv - tau[h], a.beta);
+          for (int u = 0; u < 2; ++u) {
+            const int e = 4 * lane + 128 * u;
+            if (e < P * G) *reinterpret_cast<float4*>(zw + e) = zl[u];
+          }
+          __syncwarp();
+        }
 #pragma unroll
-              for (int j = 0; j < VEC; ++j) acc[h][j] = fmaf(p, v[j], acc[h][j]);
+        for (int u = 0; u < CH; ++u) {
+          const int t = tg + TG * (c1 + u);
+          if (t < nv) {
+            float v[VEC];
+            VTraits<T>::unpack(raw[u], v);
+#pragma unroll
+            for (int h = 0; h < GP; ++h) {
+              if (h < G) {
+                const float zv = zw[t * G + h];
+                const float p = sizeof(T) == 4 ? pos_pow((float)((double)zv - taud[h]), a.beta)
+                                               : pos_pow(zv - tau[h], a.beta);
+#pragma unroll
+                for (int j = 0; j < VEC; ++j) acc[h][j] = fmaf(p, v[j], acc[h][j]);
+              }
             }
           }
         }
       }
+      __syncwarp();
     }
-    __syncwarp();
   }
 #pragma unroll
   for (int o = LPR; o < 32; o <<= 1)

@@ -168,27 +168,48 @@ __global__ void __launch_bounds__(kThreads) bbox_f32_kernel(DecodeArgs a) {
   }
 }
 
-// Gaussian page scores. A warp scores PPI pages per iteration: lane l covers
-// dims [l·D/32, (l+1)·D/32) of each page's mean and m2 rows (q and q² of those
-// dims stay in registers) and all 2·PPI row loads are issued together. Each
-// lane then holds NV = PPI·2·GP partial sums; a butterfly reduce-scatter over
-// the 32 lanes (each step a lane keeps half its values and adds the partner's
-// copy of that half) leaves every total in some lane with ~NV shuffles
-// instead of 5·NV. GP = group padded up to a power of two.
+// Gaussian page scores, streamed. Each warp owns a ring of NST shared-memory
+// stages; a stage holds the (mean, m2) rows of PPS consecutive pages, brought
+// in by one bulk asynchronous copy per row (lanes 0..2·PPS−1 each issue one)
+// that completes on the stage's mbarrier. While the warp scores one stage the
+// next NST−1 are in flight, so loads need no registers and every SM keeps
+// ~NST·PPS KiB per warp outstanding. Scoring: lane l covers dims
+// [l·D/32, (l+1)·D/32) of each row (q and q² of those dims in registers); a
+// butterfly reduce-scatter over the 32 lanes leaves each of the NV = PPS·2·GP
+// totals in some lane. GP = group padded up to a power of two.
+constexpr int kGaussWarps = 4, kGaussPPS = 4, kGaussNST = 4;
+
+template <int D>
+constexpr int gauss_smem_bytes() {
+  return kGaussWarps * kGaussNST * kGaussPPS * 2 * D * 4 + kGaussWarps * kGaussNST * (8 + kGaussPPS * 4);
+}
+
 template <typename TQ, int D, int GP>
-__global__ void __launch_bounds__(kThreads, 2) gauss_kernel(DecodeArgs a) {
-  constexpr int DPL = D / 32;           // dims per lane
-  constexpr int PPI = 4;                // pages per warp iteration
-  constexpr int NV = PPI * 2 * GP;      // partial sums per lane
+__global__ void __launch_bounds__(kGaussWarps * 32) gauss_kernel(DecodeArgs a) {
+  constexpr int DPL = D / 32;             // dims per lane
+  constexpr int PPS = kGaussPPS, NST = kGaussNST;
+  constexpr int NV = PPS * 2 * GP;        // partial sums per lane
+  constexpr int ROW = D * 4;              // bytes of one metadata row
+  extern __shared__ __align__(128) unsigned char dyn[];
   const int kvh = blockIdx.y, s = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float* stage_buf = reinterpret_cast<float*>(dyn) + (size_t)warp * NST * PPS * 2 * D;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(dyn + kGaussWarps * NST * PPS * 2 * ROW) + warp * NST;
+  int* phys_sm = reinterpret_cast<int*>(dyn + kGaussWarps * NST * PPS * 2 * ROW + kGaussWarps * NST * 8) +
+                 warp * NST * PPS;
   __shared__ uint32_t smax[GP];
   const int seq = seq_row(a.seq_ids, s, a.max_seqs, threadIdx.x == 0 ? a.status : nullptr);
   if (seq < 0) return;
   const int L = seq_len_clamped(a.seq_lens, seq, a.maxp, a.P, threadIdx.x == 0 ? a.status : nullptr);
   const int n_pages = (L + a.P - 1) / a.P;
-  if ((int)(blockIdx.x * kWarps * PPI) >= n_pages) return;
+  const int n_groups = (n_pages + PPS - 1) / PPS;
+  const int gstride = gridDim.x * kGaussWarps;
+  const int g0 = blockIdx.x * kGaussWarps + warp;
+  if ((int)(blockIdx.x * kGaussWarps) >= n_groups) return;
   if (threadIdx.x < GP) smax[threadIdx.x] = 0u;
+  if (lane < NST) mbar_init(&bars[lane], 1);
+  mbar_fence_init();
+  __syncwarp();
 
   float qv[GP][DPL], q2[GP][DPL];
 #pragma unroll
@@ -201,7 +222,6 @@ __global__ void __launch_bounds__(kThreads, 2) gauss_kernel(DecodeArgs a) {
       q2[h][e] = x * x;
     }
   }
-  // which total this lane ends up holding (fixed by its lane bits)
   int idx = 0, nfin = NV;
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1)
@@ -215,51 +235,70 @@ __global__ void __launch_bounds__(kThreads, 2) gauss_kernel(DecodeArgs a) {
   float runmax[NFIN];
 #pragma unroll
   for (int i = 0; i < NFIN; ++i) runmax[i] = -CUDART_INF_F;
-  __syncthreads();
 
-  for (int pb = (blockIdx.x * kWarps + warp) * PPI; pb < n_pages; pb += gridDim.x * kWarps * PPI) {
-    int ph_l = -1;
-    if (lane < PPI && pb + lane < n_pages)
-      ph_l = phys_page(a.block_table, seq, pb + lane, a.maxp, a.nphys, a.status);
-    float mv[PPI][DPL], vv[PPI][DPL];
-#pragma unroll
-    for (int pg = 0; pg < PPI; ++pg) {
-      const int ph = __shfl_sync(0xffffffffu, ph_l, pg);
-      if (ph >= 0) {
-        const size_t base = ((size_t)ph * a.Hkv + kvh) * D + lane * DPL;
-        if constexpr (DPL == 4) {
-          const uint4 mr = ld_stream(a.mean + base), vr = ld_stream(a.m2 + base);
-          mv[pg][0] = __uint_as_float(mr.x); mv[pg][1] = __uint_as_float(mr.y);
-          mv[pg][2] = __uint_as_float(mr.z); mv[pg][3] = __uint_as_float(mr.w);
-          vv[pg][0] = __uint_as_float(vr.x); vv[pg][1] = __uint_as_float(vr.y);
-          vv[pg][2] = __uint_as_float(vr.z); vv[pg][3] = __uint_as_float(vr.w);
-        } else {
-#pragma unroll
-          for (int e = 0; e < DPL; ++e) {
-            mv[pg][e] = __ldg(a.mean + base + e);
-            vv[pg][e] = __ldg(a.m2 + base + e);
-          }
-        }
-      } else {
-#pragma unroll
-        for (int e = 0; e < DPL; ++e) mv[pg][e] = vv[pg][e] = 0.0f;
-      }
+  // issue group g into stage st (whole warp calls)
+  auto issue = [&](int g, int st) {
+    const int p = g * PPS + (lane >> 1);
+    int ph = -1;
+    if (lane < 2 * PPS && p < n_pages)
+      ph = phys_page(a.block_table, seq, p, a.maxp, a.nphys, (lane & 1) ? nullptr : a.status);
+    const uint32_t valid = __ballot_sync(0xffffffffu, ph >= 0);  // two bits per page
+    if ((lane & 1) == 0 && lane < 2 * PPS) phys_sm[st * PPS + (lane >> 1)] = ph;
+    if (lane == 0) mbar_expect_tx(&bars[st], (uint32_t)__popc(valid) * ROW);
+    __syncwarp();
+    if (ph >= 0) {
+      const float* src = ((lane & 1) ? a.m2 : a.mean) + ((size_t)ph * a.Hkv + kvh) * D;
+      float* dst = stage_buf + ((size_t)st * PPS * 2 + (lane >> 1) * 2 + (lane & 1)) * D;
+      bulk_g2s(dst, src, ROW, &bars[st]);
     }
+  };
+  int n_mine = 0;
+  for (int g = g0; g < n_groups; g += gstride) ++n_mine;
+#pragma unroll
+  for (int j = 0; j < NST; ++j)
+    if (j < n_mine) issue(g0 + j * gstride, j);
+
+  int stuck = -1;
+  for (int j = 0; j < n_mine; ++j) {
+    const int st = j % NST;
+    const int g = g0 + j * gstride;
+    if (!mbar_wait_bounded(&bars[st], (uint32_t)((j / NST) & 1))) {
+      stuck = j;
+      break;
+    }
+    const float* sb = stage_buf + (size_t)st * PPS * 2 * D;
     float v[NV];
 #pragma unroll
-    for (int pg = 0; pg < PPI; ++pg)
+    for (int pg = 0; pg < PPS; ++pg) {
+      const bool pv = phys_sm[st * PPS + pg] >= 0;
+      float mv[DPL], vv[DPL];
+      if constexpr (DPL == 4) {
+        const float4 m4 = pv ? *reinterpret_cast<const float4*>(sb + (pg * 2) * D + lane * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 v4 = pv ? *reinterpret_cast<const float4*>(sb + (pg * 2 + 1) * D + lane * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+        mv[0] = m4.x; mv[1] = m4.y; mv[2] = m4.z; mv[3] = m4.w;
+        vv[0] = v4.x; vv[1] = v4.y; vv[2] = v4.z; vv[3] = v4.w;
+      } else {
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) {
+          mv[e] = pv ? sb[(pg * 2) * D + lane * DPL + e] : 0.0f;
+          vv[e] = pv ? sb[(pg * 2 + 1) * D + lane * DPL + e] : 0.0f;
+        }
+      }
 #pragma unroll
       for (int h = 0; h < GP; ++h) {
         float mu = 0.0f, sg = 0.0f;
 #pragma unroll
         for (int e = 0; e < DPL; ++e) {
-          mu = fmaf(qv[h][e], mv[pg][e], mu);
-          sg = fmaf(q2[h][e], vv[pg][e], sg);
+          mu = fmaf(qv[h][e], mv[e], mu);
+          sg = fmaf(q2[h][e], vv[e], sg);
         }
         v[(pg * 2 + 0) * GP + h] = mu;
         v[(pg * 2 + 1) * GP + h] = sg;
       }
-    // butterfly reduce-scatter
+    }
+    const int my_ph = phys_sm[st * PPS + my_pg];
+    __syncwarp();  // every lane has read the stage: it may be refilled
+    if (j + NST < n_mine) issue(g0 + (j + NST) * gstride, st);
     int n = NV;
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) {
@@ -279,16 +318,14 @@ __global__ void __launch_bounds__(kThreads, 2) gauss_kernel(DecodeArgs a) {
         v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
       }
     }
-    // lane holds totals idx.. = (page my_pg, quantity my_qty, heads my_h0..)
-    const int p = pb + my_pg;
-    const int ph = __shfl_sync(0xffffffffu, ph_l, my_pg);
+    const int p = g * PPS + my_pg;
 #pragma unroll
     for (int i = 0; i < NFIN; ++i) {
       const int my_h = my_h0 + i;
       if (writer && my_h < a.G && p < n_pages) {
         float* dst = reinterpret_cast<float*>(
             a.gauss_ms + ((size_t)s * a.Hq + (size_t)kvh * a.G + my_h) * a.maxp + p);
-        if (ph < 0) {  // unreadable page: no mass, never selected
+        if (my_ph < 0) {  // unreadable page: no mass, never selected
           dst[my_qty] = my_qty == 0 ? -CUDART_INF_F : 0.0f;
         } else if (my_qty == 0) {
           const float m = a.a1 * v[i] * a.inv_sqrt_d;
@@ -300,6 +337,11 @@ __global__ void __launch_bounds__(kThreads, 2) gauss_kernel(DecodeArgs a) {
         }
       }
     }
+  }
+  if (stuck >= 0) {  // a copy never completed: flag, let the later ones land (bounded), stop
+    if (lane == 0) raise_flag(a.status, ENTMAXKV_DEV_TIMEOUT);
+    for (int j = stuck + 1; j < n_mine && j < stuck + NST; ++j)
+      mbar_wait_bounded(&bars[j % NST], (uint32_t)((j / NST) & 1));
   }
 #pragma unroll
   for (int i = 0; i < NFIN; ++i)
@@ -332,24 +374,38 @@ cudaError_t launch_bbox(const DecodeArgs& a, int kv_dtype, int sms, cudaStream_t
   return cudaGetLastError();
 }
 
+template <typename TQ, int D, int GP>
+static cudaError_t gauss_launch(const DecodeArgs& a, dim3 grid, cudaStream_t st) {
+  constexpr int smem = gauss_smem_bytes<D>();
+  cudaError_t e = cudaFuncSetAttribute(gauss_kernel<TQ, D, GP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  gauss_kernel<TQ, D, GP><<<grid, kGaussWarps * 32, smem, st>>>(a);
+  return cudaSuccess;
+}
+
 template <typename TQ, int D>
-static void gauss_dispatch_g(const DecodeArgs& a, dim3 grid, cudaStream_t st) {
-  if (a.G <= 1) gauss_kernel<TQ, D, 1><<<grid, kThreads, 0, st>>>(a);
-  else if (a.G <= 2) gauss_kernel<TQ, D, 2><<<grid, kThreads, 0, st>>>(a);
-  else if (a.G <= 4) gauss_kernel<TQ, D, 4><<<grid, kThreads, 0, st>>>(a);
-  else gauss_kernel<TQ, D, 8><<<grid, kThreads, 0, st>>>(a);
+static cudaError_t gauss_dispatch_g(const DecodeArgs& a, dim3 grid, cudaStream_t st) {
+  if (a.G <= 1) return gauss_launch<TQ, D, 1>(a, grid, st);
+  if (a.G <= 2) return gauss_launch<TQ, D, 2>(a, grid, st);
+  if (a.G <= 4) return gauss_launch<TQ, D, 4>(a, grid, st);
+  return gauss_launch<TQ, D, 8>(a, grid, st);
 }
 
 cudaError_t launch_gauss(const DecodeArgs& a, int kv_dtype, int sms, cudaStream_t st) {
-  dim3 grid(grid_x_for(a.maxp, kWarps * 4, sms, a.Hkv * a.S), a.Hkv, a.S);
-  if (kv_dtype == ENTMAXKV_BF16) {
-    if (a.D == 128) gauss_dispatch_g<__nv_bfloat16, 128>(a, grid, st);
-    else gauss_dispatch_g<__nv_bfloat16, 64>(a, grid, st);
-  } else {
-    if (a.D == 128) gauss_dispatch_g<float, 128>(a, grid, st);
-    else gauss_dispatch_g<float, 64>(a, grid, st);
-  }
-  return cudaGetLastError();
+  // ~3 blocks per SM (64 KiB of stages each) across all (sequence, KV head) rows
+  const int groups = (a.maxp + kGaussPPS - 1) / kGaussPPS;
+  int gx = (groups + kGaussWarps - 1) / kGaussWarps;
+  const int cap = (3 * sms + a.Hkv * a.S - 1) / (a.Hkv * a.S);
+  if (gx > cap) gx = cap;
+  if (gx < 1) gx = 1;
+  dim3 grid(gx, a.Hkv, a.S);
+  cudaError_t e;
+  if (kv_dtype == ENTMAXKV_BF16)
+    e = a.D == 128 ? gauss_dispatch_g<__nv_bfloat16, 128>(a, grid, st)
+                   : gauss_dispatch_g<__nv_bfloat16, 64>(a, grid, st);
+  else
+    e = a.D == 128 ? gauss_dispatch_g<float, 128>(a, grid, st) : gauss_dispatch_g<float, 64>(a, grid, st);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace ekv
