@@ -8,6 +8,7 @@
 #include <stdint.h>
 
 #include "entmaxkv.h"
+#include "mills_poly.cuh"
 
 namespace ekv {
 
@@ -212,47 +213,55 @@ __device__ __forceinline__ void gauss_moment(float a, float sg, bool beta2, floa
   }
 }
 
-// E[(a + σZ)_+^β] and its derivative from a shared-memory copy of the node
-// table (H, H1, Φ, φ) of normal_table.cuh by cubic Hermite interpolation in
-// t = a/σ: with H' = 2·H1, H1' = Φ, Φ' = φ the nodes carry their own slopes.
-//   β = 2: G = σ²·H(t), dG/da = 2σ·H1(t);   β = 1: G = σ·H1(t), dG/da = Φ(t).
-// Left of the table G and dG are below 1e-34 relative to σ^β and are taken as
-// 0; right of it Φ = 1 and φ = 0 to float precision.
-__device__ __forceinline__ void gauss_moment_tab(const float4* tab, float a, float sg, float inv_sg,
-                                                 bool beta2, float lo, float inv_h, int n_int,
-                                                 float& g, float& dg) {
-  if (!(sg > 0.0f)) {
+// E[(a + σZ)_+^β] for Z ~ N(0, 1) and its first two derivatives in a, for
+// β ∈ {1, 2}, without special functions. With t = a/σ, x = |t|:
+//   H1(t) = t·Φ(t) + φ(t),  H(t) = (1 + t²)·Φ(t) + t·φ(t),
+//   G = σ²·H, G' = 2σ·H1, G'' = 2Φ  (β = 2);  G = σ·H1, G' = Φ, G'' = φ/σ  (β = 1).
+// For t ≤ 0: Φ = φ(x)·R(x), H1 = φ(x)·A(x), H = φ(x)·B(x) with the smooth,
+// cancellation-free R, A, B of mills_poly.cuh (polynomials in u = 1/(1+x/3));
+// for t > 0 the reflections Φ(t) = 1 − Φ(−t), H1(t) = t + H1(−t),
+// H(t) = 1 + t² − H(−t). Relative error of each function below ~5e-7.
+template <int N>
+__device__ __forceinline__ float horner(const float (&c)[N], float w) {
+  float r = c[N - 1];
+#pragma unroll
+  for (int i = N - 2; i >= 0; --i) r = fmaf(r, w, c[i]);
+  return r;
+}
+
+__device__ __forceinline__ void gauss_moment2(float a, float sg, float inv_sg, bool beta2, float& g,
+                                              float& dg, float& d2g) {
+  if (!(sg > 0.0f)) {  // point mass at a
     const float ap = fmaxf(a, 0.0f);
     g = beta2 ? ap * ap : ap;
     dg = beta2 ? 2.0f * ap : (a > 0.0f ? 1.0f : 0.0f);
+    d2g = beta2 ? (a > 0.0f ? 2.0f : 0.0f) : 0.0f;
     return;
   }
+  constexpr float cR[EKV_MILLS_DEG + 1] = {EKV_MILLS_R};
+  constexpr float cA[EKV_MILLS_DEG + 1] = {EKV_MILLS_A};
+  constexpr float cB[EKV_MILLS_DEG + 1] = {EKV_MILLS_B};
   const float t = a * inv_sg;
-  const float x = (t - lo) * inv_h;
-  if (!(x >= 0.0f)) {
-    g = dg = 0.0f;
-    return;
-  }
-  if (x >= (float)n_int) {
-    g = beta2 ? fmaf(a, a, sg * sg) : a;
-    dg = beta2 ? 2.0f * a : 1.0f;
-    return;
-  }
-  const int i = (int)x;
-  const float u = x - (float)i;
-  const float4 n0 = tab[i], n1 = tab[i + 1];
-  const float u2 = u * u, u3 = u2 * u;
-  const float h01 = fmaf(-2.0f, u3, 3.0f * u2), h00 = 1.0f - h01;
-  const float hh = 1.0f / inv_h;
-  const float h10 = hh * (u3 - 2.0f * u2 + u), h11 = hh * (u3 - u2);
-  const float H1 = fmaf(h00, n0.y, fmaf(h10, n0.z, fmaf(h01, n1.y, h11 * n1.z)));
+  const float x = fabsf(t);
+  const float u = __frcp_rn(fmaf(fminf(x, EKV_MILLS_XMAX), 0.33333334f, 1.0f));
+  const float w = fmaf(2.5f, u, -1.5f);
+  const float phi = 0.3989422804f * exp2f(-0.72134752f * x * x);
+  const float pu = phi * u;
+  const float R = pu * horner(cR, w);
+  const float A = pu * u * horner(cA, w);
+  const bool left = t <= 0.0f;
+  const float Phi = left ? R : 1.0f - R;
+  const float H1 = left ? A : t + A;
   if (beta2) {
-    const float H = fmaf(h00, n0.x, fmaf(2.0f * h10, n0.y, fmaf(h01, n1.x, 2.0f * h11 * n1.y)));
+    const float B = pu * u * u * horner(cB, w);
+    const float H = left ? B : fmaf(t, t, 1.0f) - B;
     g = sg * sg * H;
     dg = 2.0f * sg * H1;
+    d2g = 2.0f * Phi;
   } else {
     g = sg * H1;
-    dg = fmaf(h00, n0.z, fmaf(h10, n0.w, fmaf(h01, n1.z, h11 * n1.w)));
+    dg = Phi;
+    d2g = phi * inv_sg;
   }
 }
 
@@ -296,6 +305,25 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t si
           smem_u32(dst)),
       "l"(src), "r"(size), "r"(smem_u32(bar))
       : "memory");
+}
+
+// Packed fp32 pairs (two lanes of a 64-bit register) and the sm_100-family
+// paired FMA: d = a·b + c on both halves.
+__device__ __forceinline__ unsigned long long f2_pack(float lo, float hi) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float f2_sum(unsigned long long v) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  return lo + hi;
+}
+__device__ __forceinline__ unsigned long long f2_fma(unsigned long long a, unsigned long long b,
+                                                     unsigned long long c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
 }
 
 // Block-wide exclusive scan of one int per thread (blockDim multiple of 32).

@@ -169,14 +169,15 @@ __global__ void __launch_bounds__(kThreads) bbox_f32_kernel(DecodeArgs a) {
 }
 
 // Gaussian page scores, streamed. Each warp owns a ring of NST shared-memory
-// stages; a stage holds the (mean, m2) rows of PPS consecutive pages, brought
-// in by one bulk asynchronous copy per row (lanes 0..2·PPS−1 each issue one)
+// stages; a stage holds the (mean, m2) rows of PPS = 4 consecutive pages,
+// brought in by one bulk asynchronous copy per row (lanes 0..7 each issue one)
 // that completes on the stage's mbarrier. While the warp scores one stage the
-// next NST−1 are in flight, so loads need no registers and every SM keeps
-// ~NST·PPS KiB per warp outstanding. Scoring: lane l covers dims
-// [l·D/32, (l+1)·D/32) of each row (q and q² of those dims in registers); a
-// butterfly reduce-scatter over the 32 lanes leaves each of the NV = PPS·2·GP
-// totals in some lane. GP = group padded up to a power of two.
+// next NST−1 are in flight, so loads hold no registers. Scoring: half-warp h
+// takes pages h and h+2 of a stage; lane l of a half covers dims
+// [8·(l%16), +8) (q and q² of those dims live in registers as fp32 pairs for
+// the paired FMA), and a butterfly reduce-scatter over the 16 lanes of the
+// half leaves each of the 2·2·GP totals in some lane. GP = group padded up to
+// a power of two. Block-table lookups for a refill are issued one stage early.
 constexpr int kGaussWarps = 4, kGaussPPS = 4, kGaussNST = 4;
 
 template <int D>
@@ -186,13 +187,15 @@ constexpr int gauss_smem_bytes() {
 
 template <typename TQ, int D, int GP>
 __global__ void __launch_bounds__(kGaussWarps * 32) gauss_kernel(DecodeArgs a) {
-  constexpr int DPL = D / 32;             // dims per lane
+  constexpr int DPL = D / 16;             // dims per lane (a half-warp covers a row)
+  constexpr int NP2 = DPL / 2;            // fp32 pairs per lane
   constexpr int PPS = kGaussPPS, NST = kGaussNST;
-  constexpr int NV = PPS * 2 * GP;        // partial sums per lane
+  constexpr int NV = 2 * 2 * GP;          // totals per half-warp per stage: page × (μ, σ²) × head
   constexpr int ROW = D * 4;              // bytes of one metadata row
   extern __shared__ __align__(128) unsigned char dyn[];
   const int kvh = blockIdx.y, s = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int half = lane >> 4, hl = lane & 15;
   float* stage_buf = reinterpret_cast<float*>(dyn) + (size_t)warp * NST * PPS * 2 * D;
   uint64_t* bars = reinterpret_cast<uint64_t*>(dyn + kGaussWarps * NST * PPS * 2 * ROW) + warp * NST;
   int* phys_sm = reinterpret_cast<int*>(dyn + kGaussWarps * NST * PPS * 2 * ROW + kGaussWarps * NST * 8) +
@@ -211,37 +214,44 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_kernel(DecodeArgs a) {
   mbar_fence_init();
   __syncwarp();
 
-  float qv[GP][DPL], q2[GP][DPL];
+  unsigned long long qp[GP][NP2], q2p[GP][NP2];
 #pragma unroll
   for (int h = 0; h < GP; ++h) {
     const TQ* qh = (const TQ*)a.q + ((size_t)s * a.Hq + (size_t)kvh * a.G + (h < a.G ? h : 0)) * D;
 #pragma unroll
-    for (int e = 0; e < DPL; ++e) {
-      const float x = h < a.G ? to_f(qh[lane * DPL + e]) : 0.0f;
-      qv[h][e] = x;
-      q2[h][e] = x * x;
+    for (int e = 0; e < NP2; ++e) {
+      const float x0 = h < a.G ? to_f(qh[hl * DPL + 2 * e]) : 0.0f;
+      const float x1 = h < a.G ? to_f(qh[hl * DPL + 2 * e + 1]) : 0.0f;
+      qp[h][e] = f2_pack(x0, x1);
+      q2p[h][e] = f2_pack(x0 * x0, x1 * x1);
     }
   }
+  // which totals this lane ends up holding (fixed by its lane bits)
   int idx = 0, nfin = NV;
 #pragma unroll
-  for (int o = 16; o >= 1; o >>= 1)
+  for (int o = 8; o >= 1; o >>= 1)
     if (nfin > 1) {
       nfin >>= 1;
-      if (lane & o) idx += nfin;
+      if (hl & o) idx += nfin;
     }
-  constexpr int NFIN = NV > 32 ? NV / 32 : 1;  // totals per lane (indices idx .. idx+NFIN−1)
-  const int my_pg = idx / (2 * GP), my_qty = (idx / GP) & 1, my_h0 = idx % GP;
-  const bool writer = (NV >= 32) || ((lane & (32 / NV - 1)) == 0);
+  constexpr int NFIN = NV > 16 ? NV / 16 : 1;
+  const int my_i = idx / (2 * GP), my_qty = (idx / GP) & 1, my_h0 = idx % GP;
+  const int my_pg = 2 * my_i + half;  // page within the stage
+  const bool writer = (NV >= 16) || ((hl & (16 / NV - 1)) == 0);
   float runmax[NFIN];
 #pragma unroll
   for (int i = 0; i < NFIN; ++i) runmax[i] = -CUDART_INF_F;
+  const float inv_full = 1.0f / ((float)a.P * (float)D);
 
-  // issue group g into stage st (whole warp calls)
-  auto issue = [&](int g, int st) {
+  // block-table entry of the row lane `lane` (< 2·PPS) copies for group g
+  auto lookup = [&](int g) -> int {
     const int p = g * PPS + (lane >> 1);
-    int ph = -1;
     if (lane < 2 * PPS && p < n_pages)
-      ph = phys_page(a.block_table, seq, p, a.maxp, a.nphys, (lane & 1) ? nullptr : a.status);
+      return phys_page(a.block_table, seq, p, a.maxp, a.nphys, (lane & 1) ? nullptr : a.status);
+    return -1;
+  };
+  // fill stage st with the rows whose physical pages are ph (whole warp calls)
+  auto issue = [&](int ph, int st) {
     const uint32_t valid = __ballot_sync(0xffffffffu, ph >= 0);  // two bits per page
     if ((lane & 1) == 0 && lane < 2 * PPS) phys_sm[st * PPS + (lane >> 1)] = ph;
     if (lane == 0) mbar_expect_tx(&bars[st], (uint32_t)__popc(valid) * ROW);
@@ -256,12 +266,13 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_kernel(DecodeArgs a) {
   for (int g = g0; g < n_groups; g += gstride) ++n_mine;
 #pragma unroll
   for (int j = 0; j < NST; ++j)
-    if (j < n_mine) issue(g0 + j * gstride, j);
+    if (j < n_mine) issue(lookup(g0 + j * gstride), j);
 
   int stuck = -1;
   for (int j = 0; j < n_mine; ++j) {
     const int st = j % NST;
     const int g = g0 + j * gstride;
+    const int ph_next = j + NST < n_mine ? lookup(g0 + (j + NST) * gstride) : -1;
     if (!mbar_wait_bounded(&bars[st], (uint32_t)((j / NST) & 1))) {
       stuck = j;
       break;
@@ -269,51 +280,52 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_kernel(DecodeArgs a) {
     const float* sb = stage_buf + (size_t)st * PPS * 2 * D;
     float v[NV];
 #pragma unroll
-    for (int pg = 0; pg < PPS; ++pg) {
+    for (int i = 0; i < 2; ++i) {
+      const int pg = 2 * i + half;
       const bool pv = phys_sm[st * PPS + pg] >= 0;
-      float mv[DPL], vv[DPL];
-      if constexpr (DPL == 4) {
-        const float4 m4 = pv ? *reinterpret_cast<const float4*>(sb + (pg * 2) * D + lane * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
-        const float4 v4 = pv ? *reinterpret_cast<const float4*>(sb + (pg * 2 + 1) * D + lane * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
-        mv[0] = m4.x; mv[1] = m4.y; mv[2] = m4.z; mv[3] = m4.w;
-        vv[0] = v4.x; vv[1] = v4.y; vv[2] = v4.z; vv[3] = v4.w;
-      } else {
+      unsigned long long mu[GP], sg[GP];
 #pragma unroll
-        for (int e = 0; e < DPL; ++e) {
-          mv[e] = pv ? sb[(pg * 2) * D + lane * DPL + e] : 0.0f;
-          vv[e] = pv ? sb[(pg * 2 + 1) * D + lane * DPL + e] : 0.0f;
+      for (int h = 0; h < GP; ++h) mu[h] = sg[h] = 0ull;
+#pragma unroll
+      for (int c = 0; c < DPL / 4; ++c) {
+        const float4 m4 = pv ? *reinterpret_cast<const float4*>(sb + (pg * 2) * D + hl * DPL + 4 * c)
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 v4 = pv ? *reinterpret_cast<const float4*>(sb + (pg * 2 + 1) * D + hl * DPL + 4 * c)
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+        const unsigned long long m01 = f2_pack(m4.x, m4.y), m23 = f2_pack(m4.z, m4.w);
+        const unsigned long long v01 = f2_pack(v4.x, v4.y), v23 = f2_pack(v4.z, v4.w);
+#pragma unroll
+        for (int h = 0; h < GP; ++h) {
+          mu[h] = f2_fma(qp[h][2 * c], m01, mu[h]);
+          mu[h] = f2_fma(qp[h][2 * c + 1], m23, mu[h]);
+          sg[h] = f2_fma(q2p[h][2 * c], v01, sg[h]);
+          sg[h] = f2_fma(q2p[h][2 * c + 1], v23, sg[h]);
         }
       }
 #pragma unroll
       for (int h = 0; h < GP; ++h) {
-        float mu = 0.0f, sg = 0.0f;
-#pragma unroll
-        for (int e = 0; e < DPL; ++e) {
-          mu = fmaf(qv[h][e], mv[e], mu);
-          sg = fmaf(q2[h][e], vv[e], sg);
-        }
-        v[(pg * 2 + 0) * GP + h] = mu;
-        v[(pg * 2 + 1) * GP + h] = sg;
+        v[(i * 2 + 0) * GP + h] = f2_sum(mu[h]);
+        v[(i * 2 + 1) * GP + h] = f2_sum(sg[h]);
       }
     }
     const int my_ph = phys_sm[st * PPS + my_pg];
     __syncwarp();  // every lane has read the stage: it may be refilled
-    if (j + NST < n_mine) issue(g0 + (j + NST) * gstride, st);
+    if (j + NST < n_mine) issue(ph_next, st);
     int n = NV;
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) {
+    for (int o = 8; o >= 1; o >>= 1) {
       if (n > 1) {
-        const int half = n >> 1;
-        const bool up = lane & o;
+        const int hf = n >> 1;
+        const bool up = hl & o;
 #pragma unroll
         for (int i = 0; i < NV / 2; ++i) {
-          if (i < half) {
-            const float send = up ? v[i] : v[i + half];
-            const float keep = up ? v[i + half] : v[i];
+          if (i < hf) {
+            const float send = up ? v[i] : v[i + hf];
+            const float keep = up ? v[i + hf] : v[i];
             v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
           }
         }
-        n = half;
+        n = hf;
       } else {
         v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
       }
@@ -333,7 +345,8 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_kernel(DecodeArgs a) {
           runmax[i] = fmaxf(runmax[i], m);
         } else {
           const int nv = min(a.P, L - p * a.P);
-          dst[1] = a.a1 * sqrtf(fmaxf(v[i], 0.0f) / ((float)nv * (float)D));
+          const float inv_n = nv == a.P ? inv_full : 1.0f / ((float)nv * (float)D);
+          dst[1] = a.a1 * sqrtf(fmaxf(v[i], 0.0f) * inv_n);
         }
       }
     }

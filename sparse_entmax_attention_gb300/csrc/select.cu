@@ -5,9 +5,10 @@
 // equation for τ̂ from the page statistics, then keep the pages whose
 // estimated maximum score clears τ̂ lowered by the margin Δ. Here
 //   F(τ) = Σ_p n_p·E[(Z_p − τ)_+^β],  Z_p ~ N(m_p, ς_p²),  F(τ̂) = 1,
-// solved by safeguarded Newton steps on log F inside a bracket [lo, hi]
-// (lo starts at max_p m_p − 1, where F ≥ 1 by Jensen's inequality; a step
-// leaving the bracket is replaced by bisection). Each query head gets one
+// solved by safeguarded Halley steps on log F (cubic convergence; Newton
+// when the Halley step is not usable) inside a bracket [lo, hi] (lo starts at
+// max_p m_p − 1, where F ≥ 1 by Jensen's inequality; a step leaving the
+// bracket is replaced by bisection). Each query head gets one
 // cluster of kTauhatCluster blocks; every iteration each block sums its share
 // of pages, the blocks exchange partial sums through distributed shared
 // memory, and every block takes the same step from the same totals. Then a
@@ -23,7 +24,6 @@
 #include <cooperative_groups.h>
 
 #include "common.cuh"
-#include "normal_table.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -42,9 +42,8 @@ __device__ __forceinline__ float sqrt_2ln(int n, int P, float c_full) {
 __global__ void __cluster_dims__(kTauhatCluster, 1, 1) __launch_bounds__(kThreads, 2)
     tauhat_kernel(DecodeArgs a) {
   cg::cluster_group cluster = cg::this_cluster();
-  __shared__ float4 tab[EKV_NTAB_N + 1];
-  __shared__ double2 slot[2];
-  __shared__ double red_f[kWarps], red_d[kWarps];
+  __shared__ double4 slot[2];
+  __shared__ float red_f[kWarps], red_d[kWarps], red_e[kWarps];
   __shared__ double tau_sh;
   __shared__ int done_sh;
   const int h = blockIdx.y, s = blockIdx.z;
@@ -61,7 +60,6 @@ __global__ void __cluster_dims__(kTauhatCluster, 1, 1) __launch_bounds__(kThread
   if (!(M > -CUDART_INF)) return;  // no readable page
   const bool beta2 = a.beta == 2.0f;
   const float2* ms = a.gauss_ms + ((size_t)s * a.Hq + h) * a.maxp;
-  for (int i = tid; i <= EKV_NTAB_N; i += kThreads) tab[i] = kNormTab[i];
   const int words = (n_pages + 31) / 32;
   const int chunk = ((words + kTauhatCluster - 1) / kTauhatCluster) * 32;
   const int p_lo = rank * chunk, p_hi = min(n_pages, p_lo + chunk);
@@ -84,57 +82,61 @@ __global__ void __cluster_dims__(kTauhatCluster, 1, 1) __launch_bounds__(kThread
     }
     ir[k] = mr[k].y > 0.0f ? 1.0f / mr[k].y : 0.0f;
   }
-  __syncthreads();  // node table in shared memory
   double lo = M - 1.0, hi = CUDART_INF, tau = lo;
   bool converged = false;
   int it = 0;
   for (; it < kTauhatIters; ++it) {
     const float tf = (float)tau;
-    float f = 0.0f, df = 0.0f;
+    float f = 0.0f, df = 0.0f, d2f = 0.0f;
 #pragma unroll
     for (int k = 0; k < kRegPages; ++k) {
-      float g, dg;
-      gauss_moment_tab(tab, mr[k].x - tf, mr[k].y, ir[k], beta2, EKV_NTAB_LO, EKV_NTAB_INV_H,
-                       EKV_NTAB_N, g, dg);
+      float g, dg, d2g;
+      gauss_moment2(mr[k].x - tf, mr[k].y, ir[k], beta2, g, dg, d2g);
       f = fmaf(nr[k], g, f);
       df = fmaf(nr[k], dg, df);
+      d2f = fmaf(nr[k], d2g, d2f);
     }
     for (int p = p_lo + tid + kRegPages * kThreads; p < p_hi; p += kThreads) {
       const float2 v = ms[p];
-      float g, dg;
-      gauss_moment_tab(tab, v.x - tf, v.y, v.y > 0.0f ? 1.0f / v.y : 0.0f, beta2, EKV_NTAB_LO,
-                       EKV_NTAB_INV_H, EKV_NTAB_N, g, dg);
+      float g, dg, d2g;
+      gauss_moment2(v.x - tf, v.y, v.y > 0.0f ? 1.0f / v.y : 0.0f, beta2, g, dg, d2g);
       const float np = (float)page_tokens(p, n_pages, L, a.P);
       f = fmaf(np, g, f);
       df = fmaf(np, dg, df);
+      d2f = fmaf(np, d2g, d2f);
     }
-    const double fd = (double)warp_sum(f), dd = (double)warp_sum(df);
+    f = warp_sum(f);
+    df = warp_sum(df);
+    d2f = warp_sum(d2f);
     if (lane == 0) {
-      red_f[warp] = fd;
-      red_d[warp] = dd;
+      red_f[warp] = f;
+      red_d[warp] = df;
+      red_e[warp] = d2f;
     }
     __syncthreads();
     if (tid == 0) {
-      double sf = 0.0, sd = 0.0;
+      double sf = 0.0, sd = 0.0, se = 0.0;
       for (int w = 0; w < kWarps; ++w) {
         sf += red_f[w];
         sd += red_d[w];
+        se += red_e[w];
       }
-      slot[it & 1] = make_double2(sf, sd);
+      slot[it & 1] = make_double4(sf, sd, se, 0.0);
     }
     cluster.sync();
     if (warp == 0) {
       // lane r reads block r's partial sums; a fixed-order tree sum gives every
       // block bit-identical totals, hence identical steps
-      double2 v = lane < kTauhatCluster ? cluster.map_shared_rank(&slot[0], lane)[it & 1]
-                                        : make_double2(0.0, 0.0);
+      double4 v = lane < kTauhatCluster ? cluster.map_shared_rank(&slot[0], lane)[it & 1]
+                                        : make_double4(0.0, 0.0, 0.0, 0.0);
 #pragma unroll
       for (int o = kTauhatCluster / 2; o >= 1; o >>= 1) {
         v.x += __shfl_down_sync(0xffffffffu, v.x, o);
         v.y += __shfl_down_sync(0xffffffffu, v.y, o);
+        v.z += __shfl_down_sync(0xffffffffu, v.z, o);
       }
       if (lane == 0) {
-        const double F = v.x, dF = v.y;
+        const double F = v.x, dF = v.y, d2F = v.z;  // F, −dF/dτ, d²F/dτ²
         if (F >= 1.0) lo = tau;
         else hi = tau;
         double next;
@@ -143,8 +145,15 @@ __global__ void __cluster_dims__(kTauhatCluster, 1, 1) __launch_bounds__(kThread
           next = tau;
           stop = true;
         } else {
-          // Newton on log F (a float log is ample for the step)
-          next = (F > 0.0 && dF > 0.0) ? tau + (double)logf((float)F) * (F / dF) : CUDART_NAN;
+          // Halley on g = log F: g' = −dF/F, g'' = d2F/F − (dF/F)²
+          // (a float log is ample for the step); Newton when not usable
+          next = CUDART_NAN;
+          if (F > 0.0 && dF > 0.0) {
+            const double g = (double)logf((float)F), g1 = -dF / F, g2 = d2F / F - g1 * g1;
+            const double den = 2.0 * g1 * g1 - g * g2;
+            next = den > 0.0 ? tau - 2.0 * g * g1 / den : tau - g / g1;
+            if (!(next > lo && next < hi)) next = tau - g / g1;
+          }
           if (!(next > lo && next < hi)) next = isinf(hi) ? lo + 1.0 : 0.5 * (lo + hi);
           const double tol = 1e-6 * fmax(1.0, fabs(next));
           stop = fabs(next - tau) <= tol || (hi - lo) <= tol;
@@ -168,11 +177,21 @@ __global__ void __cluster_dims__(kTauhatCluster, 1, 1) __launch_bounds__(kThread
     a.diag[(size_t)s * a.Hq + h] = it + 1;
     if (!converged) raise_flag(a.status, ENTMAXKV_DEV_TAUHAT_NOCONV);
   }
-  // Selection bits: each warp covers 32 consecutive pages starting on a word.
+  // Selection bits from the cached pages: for each k the warp's lanes hold 32
+  // consecutive pages starting on a bitmap word.
   const float thr = th - a.margin_z;
   const float c_full = sqrtf(2.0f * logf((float)a.P));
   uint32_t* bm = a.bitmap + ((size_t)s * a.Hkv + kvh) * a.words;
-  for (int p0 = p_lo + warp * 32; p0 < p_hi; p0 += kThreads) {
+#pragma unroll
+  for (int k = 0; k < kRegPages; ++k) {
+    const int p0 = p_lo + warp * 32 + k * kThreads;
+    if (p0 >= p_hi) break;
+    const int p = p0 + lane;
+    const bool sel = p < p_hi && mr[k].x + mr[k].y * sqrt_2ln((int)nr[k], a.P, c_full) >= thr;
+    const uint32_t bits = __ballot_sync(0xffffffffu, sel);
+    if (lane == 0 && bits) atomicOr(&bm[p0 >> 5], bits);
+  }
+  for (int p0 = p_lo + warp * 32 + kRegPages * kThreads; p0 < p_hi; p0 += kThreads) {
     const int p = p0 + lane;
     bool sel = false;
     if (p < p_hi) {
