@@ -31,6 +31,10 @@ namespace ekv {
 
 constexpr int kTauhatIters = 60;
 
+struct Sums3 {
+  double f, d, e;
+};
+
 __device__ __forceinline__ int page_tokens(int p, int n_pages, int L, int P) {
   return p == n_pages - 1 ? L - p * P : P;
 }
@@ -42,7 +46,7 @@ __device__ __forceinline__ float sqrt_2ln(int n, int P, float c_full) {
 __global__ void __cluster_dims__(kTauhatCluster, 1, 1) __launch_bounds__(kThreads, 2)
     tauhat_kernel(DecodeArgs a) {
   cg::cluster_group cluster = cg::this_cluster();
-  __shared__ double4 slot[2];
+  __shared__ Sums3 slot[2];
   __shared__ float red_f[kWarps], red_d[kWarps], red_e[kWarps];
   __shared__ double tau_sh;
   __shared__ int done_sh;
@@ -121,22 +125,21 @@ __global__ void __cluster_dims__(kTauhatCluster, 1, 1) __launch_bounds__(kThread
         sd += red_d[w];
         se += red_e[w];
       }
-      slot[it & 1] = make_double4(sf, sd, se, 0.0);
+      slot[it & 1] = Sums3{sf, sd, se};
     }
     cluster.sync();
     if (warp == 0) {
       // lane r reads block r's partial sums; a fixed-order tree sum gives every
       // block bit-identical totals, hence identical steps
-      double4 v = lane < kTauhatCluster ? cluster.map_shared_rank(&slot[0], lane)[it & 1]
-                                        : make_double4(0.0, 0.0, 0.0, 0.0);
+      Sums3 v = lane < kTauhatCluster ? cluster.map_shared_rank(&slot[0], lane)[it & 1] : Sums3{0.0, 0.0, 0.0};
 #pragma unroll
       for (int o = kTauhatCluster / 2; o >= 1; o >>= 1) {
-        v.x += __shfl_down_sync(0xffffffffu, v.x, o);
-        v.y += __shfl_down_sync(0xffffffffu, v.y, o);
-        v.z += __shfl_down_sync(0xffffffffu, v.z, o);
+        v.f += __shfl_down_sync(0xffffffffu, v.f, o);
+        v.d += __shfl_down_sync(0xffffffffu, v.d, o);
+        v.e += __shfl_down_sync(0xffffffffu, v.e, o);
       }
       if (lane == 0) {
-        const double F = v.x, dF = v.y, d2F = v.z;  // F, −dF/dτ, d²F/dτ²
+        const double F = v.f, dF = v.d, d2F = v.e;  // F, −dF/dτ, d²F/dτ²
         if (F >= 1.0) lo = tau;
         else hi = tau;
         double next;
