@@ -168,65 +168,77 @@ __global__ void __launch_bounds__(kThreads) bbox_f32_kernel(DecodeArgs a) {
   }
 }
 
-// Gaussian page scores, streamed. Each warp owns a ring of NST shared-memory
-// stages; a stage holds the (mean, m2) rows of PPS = 4 consecutive pages,
-// brought in by one bulk asynchronous copy per row (lanes 0..7 each issue one)
-// that completes on the stage's mbarrier. While the warp scores one stage the
-// next NST−1 are in flight, so loads hold no registers. Scoring: half-warp h
-// takes pages h and h+2 of a stage; lane l of a half covers dims
-// [8·(l%16), +8) (q and q² of those dims live in registers as fp32 pairs for
-// the paired FMA), and a butterfly reduce-scatter over the 16 lanes of the
-// half leaves each of the 2·2·GP totals in some lane. GP = group padded up to
-// a power of two. Block-table lookups for a refill are issued one stage early.
-constexpr int kGaussWarps = 4, kGaussPPS = 4, kGaussNST = 4;
+// Gaussian page scores, streamed by page slab. A block covers a range of
+// pages for up to 8 KV heads at once, so each page's mean and m2 rows for
+// those heads are one contiguous run (KH·D floats) in each array: a stage of
+// PPS pages is filled by 2·PPS bulk asynchronous copies completing on the
+// stage's "full" mbarrier. Warp w scores KV head w of every staged page and
+// then arrives on the stage's "empty" mbarrier; the producer (lane 0 of
+// warp 0) refills a stage once all warps have released it, keeping NST−1
+// stages in flight. Scoring: half-warp h takes pages h and h+2 of a stage;
+// lane l of a half covers the 16-byte chunks l and l+16 of a row (conflict-
+// free shared loads), with q and q² of those dims in registers as fp32 pairs
+// for the paired FMA; a butterfly reduce-scatter over the 16 lanes leaves
+// each of the 2·2·GP totals in some lane. GP = group padded to a power of 2.
+constexpr int kGaussWarps = 8, kGaussPPS = 4, kGaussNST = 3;
 
 template <int D>
 constexpr int gauss_smem_bytes() {
-  return kGaussWarps * kGaussNST * kGaussPPS * 2 * D * 4 + kGaussWarps * kGaussNST * (8 + kGaussPPS * 4);
+  return kGaussNST * kGaussPPS * 2 * 8 * D * 4 + kGaussNST * (16 + kGaussPPS * 4);
 }
 
 template <typename TQ, int D, int GP>
 __global__ void __launch_bounds__(kGaussWarps * 32) gauss_kernel(DecodeArgs a) {
   constexpr int DPL = D / 16;             // dims per lane (a half-warp covers a row)
-  constexpr int NP2 = DPL / 2;            // fp32 pairs per lane
+  constexpr int CH = DPL / 4;             // 16-byte chunks per lane per row
   constexpr int PPS = kGaussPPS, NST = kGaussNST;
   constexpr int NV = 2 * 2 * GP;          // totals per half-warp per stage: page × (μ, σ²) × head
-  constexpr int ROW = D * 4;              // bytes of one metadata row
   extern __shared__ __align__(128) unsigned char dyn[];
-  const int kvh = blockIdx.y, s = blockIdx.z;
+  const int kv0 = blockIdx.y * 8, s = blockIdx.z;
+  const int KH = min(8, a.Hkv - kv0);     // KV heads of this block
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int half = lane >> 4, hl = lane & 15;
-  float* stage_buf = reinterpret_cast<float*>(dyn) + (size_t)warp * NST * PPS * 2 * D;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(dyn + kGaussWarps * NST * PPS * 2 * ROW) + warp * NST;
-  int* phys_sm = reinterpret_cast<int*>(dyn + kGaussWarps * NST * PPS * 2 * ROW + kGaussWarps * NST * 8) +
-                 warp * NST * PPS;
-  __shared__ uint32_t smax[GP];
+  const int kvh = kv0 + warp;
+  const bool active = warp < KH;
+  float* stages = reinterpret_cast<float*>(dyn);                         // [NST][PPS][2][KH][D]
+  uint64_t* full = reinterpret_cast<uint64_t*>(dyn + NST * PPS * 2 * 8 * D * 4);
+  uint64_t* empty = full + NST;
+  int* phys_sm = reinterpret_cast<int*>(empty + NST);                   // [NST][PPS]
+  __shared__ uint32_t smax[8][GP];
   const int seq = seq_row(a.seq_ids, s, a.max_seqs, threadIdx.x == 0 ? a.status : nullptr);
   if (seq < 0) return;
   const int L = seq_len_clamped(a.seq_lens, seq, a.maxp, a.P, threadIdx.x == 0 ? a.status : nullptr);
   const int n_pages = (L + a.P - 1) / a.P;
   const int n_groups = (n_pages + PPS - 1) / PPS;
-  const int gstride = gridDim.x * kGaussWarps;
-  const int g0 = blockIdx.x * kGaussWarps + warp;
-  if ((int)(blockIdx.x * kGaussWarps) >= n_groups) return;
-  if (threadIdx.x < GP) smax[threadIdx.x] = 0u;
-  if (lane < NST) mbar_init(&bars[lane], 1);
+  // contiguous share of page groups for this block
+  const int g_lo = (int)(((long long)n_groups * blockIdx.x) / gridDim.x);
+  const int g_hi = (int)(((long long)n_groups * (blockIdx.x + 1)) / gridDim.x);
+  const int n_mine = g_hi - g_lo;
+  if (n_mine <= 0) return;
+  const uint32_t row_bytes = (uint32_t)KH * D * 4;
+  if (threadIdx.x < 8 * GP) smax[threadIdx.x / GP][threadIdx.x % GP] = 0u;
+  if (threadIdx.x < NST) {
+    mbar_init(&full[threadIdx.x], 1);
+    mbar_init(&empty[threadIdx.x], kGaussWarps);
+  }
   mbar_fence_init();
-  __syncwarp();
+  __syncthreads();
 
-  unsigned long long qp[GP][NP2], q2p[GP][NP2];
+  unsigned long long qp[GP][DPL / 2], q2p[GP][DPL / 2];
 #pragma unroll
   for (int h = 0; h < GP; ++h) {
-    const TQ* qh = (const TQ*)a.q + ((size_t)s * a.Hq + (size_t)kvh * a.G + (h < a.G ? h : 0)) * D;
+    const bool hv = active && h < a.G;
+    const TQ* qh = (const TQ*)a.q + ((size_t)s * a.Hq + (size_t)(hv ? kvh : 0) * a.G + (hv ? h : 0)) * D;
 #pragma unroll
-    for (int e = 0; e < NP2; ++e) {
-      const float x0 = h < a.G ? to_f(qh[hl * DPL + 2 * e]) : 0.0f;
-      const float x1 = h < a.G ? to_f(qh[hl * DPL + 2 * e + 1]) : 0.0f;
-      qp[h][e] = f2_pack(x0, x1);
-      q2p[h][e] = f2_pack(x0 * x0, x1 * x1);
-    }
+    for (int c = 0; c < CH; ++c)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int d0 = 4 * (hl + 16 * c) + 2 * e;
+        const float x0 = hv ? to_f(qh[d0]) : 0.0f, x1 = hv ? to_f(qh[d0 + 1]) : 0.0f;
+        qp[h][2 * c + e] = f2_pack(x0, x1);
+        q2p[h][2 * c + e] = f2_pack(x0 * x0, x1 * x1);
+      }
   }
-  // which totals this lane ends up holding (fixed by its lane bits)
   int idx = 0, nfin = NV;
 #pragma unroll
   for (int o = 8; o >= 1; o >>= 1)
@@ -237,80 +249,84 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_kernel(DecodeArgs a) {
   constexpr int NFIN = NV > 16 ? NV / 16 : 1;
   const int my_i = idx / (2 * GP), my_qty = (idx / GP) & 1, my_h0 = idx % GP;
   const int my_pg = 2 * my_i + half;  // page within the stage
-  const bool writer = (NV >= 16) || ((hl & (16 / NV - 1)) == 0);
+  const bool writer = active && ((NV >= 16) || ((hl & (16 / NV - 1)) == 0));
   float runmax[NFIN];
 #pragma unroll
   for (int i = 0; i < NFIN; ++i) runmax[i] = -CUDART_INF_F;
   const float inv_full = 1.0f / ((float)a.P * (float)D);
 
-  // block-table entry of the row lane `lane` (< 2·PPS) copies for group g
-  auto lookup = [&](int g) -> int {
+  // producer (warp 0): fill stage st with group g (lanes 0..2·PPS−1 copy one run each)
+  auto issue = [&](int g, int st) {
     const int p = g * PPS + (lane >> 1);
+    int ph = -1;
     if (lane < 2 * PPS && p < n_pages)
-      return phys_page(a.block_table, seq, p, a.maxp, a.nphys, (lane & 1) ? nullptr : a.status);
-    return -1;
-  };
-  // fill stage st with the rows whose physical pages are ph (whole warp calls)
-  auto issue = [&](int ph, int st) {
-    const uint32_t valid = __ballot_sync(0xffffffffu, ph >= 0);  // two bits per page
+      ph = phys_page(a.block_table, seq, p, a.maxp, a.nphys, (lane & 1) ? nullptr : a.status);
+    const uint32_t valid = __ballot_sync(0xffffffffu, ph >= 0);
     if ((lane & 1) == 0 && lane < 2 * PPS) phys_sm[st * PPS + (lane >> 1)] = ph;
-    if (lane == 0) mbar_expect_tx(&bars[st], (uint32_t)__popc(valid) * ROW);
+    if (lane == 0) mbar_expect_tx(&full[st], (uint32_t)__popc(valid) * row_bytes);
     __syncwarp();
     if (ph >= 0) {
-      const float* src = ((lane & 1) ? a.m2 : a.mean) + ((size_t)ph * a.Hkv + kvh) * D;
-      float* dst = stage_buf + ((size_t)st * PPS * 2 + (lane >> 1) * 2 + (lane & 1)) * D;
-      bulk_g2s(dst, src, ROW, &bars[st]);
+      const float* src = ((lane & 1) ? a.m2 : a.mean) + ((size_t)ph * a.Hkv + kv0) * D;
+      float* dst = stages + (((size_t)st * PPS + (lane >> 1)) * 2 + (lane & 1)) * KH * D;
+      bulk_g2s(dst, src, row_bytes, &full[st]);
     }
   };
-  int n_mine = 0;
-  for (int g = g0; g < n_groups; g += gstride) ++n_mine;
-#pragma unroll
-  for (int j = 0; j < NST; ++j)
-    if (j < n_mine) issue(lookup(g0 + j * gstride), j);
+  if (warp == 0)
+    for (int j = 0; j < NST && j < n_mine; ++j) issue(g_lo + j, j);
 
-  int stuck = -1;
+  int stuck = 0;
   for (int j = 0; j < n_mine; ++j) {
     const int st = j % NST;
-    const int g = g0 + j * gstride;
-    const int ph_next = j + NST < n_mine ? lookup(g0 + (j + NST) * gstride) : -1;
-    if (!mbar_wait_bounded(&bars[st], (uint32_t)((j / NST) & 1))) {
-      stuck = j;
+    const uint32_t par = (uint32_t)((j / NST) & 1);
+    const int g = g_lo + j;
+    if (!mbar_wait_bounded(&full[st], par)) {
+      stuck = 1;
       break;
     }
-    const float* sb = stage_buf + (size_t)st * PPS * 2 * D;
     float v[NV];
+    int my_ph = -1;
+    if (active) {
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const int pg = 2 * i + half;
-      const bool pv = phys_sm[st * PPS + pg] >= 0;
-      unsigned long long mu[GP], sg[GP];
+      for (int i = 0; i < 2; ++i) {
+        const int pg = 2 * i + half;
+        const bool pv = phys_sm[st * PPS + pg] >= 0;
+        const float* mrow = stages + (((size_t)st * PPS + pg) * 2 * KH + warp) * D;
+        const float* vrow = mrow + (size_t)KH * D;
+        unsigned long long mu[GP], sg[GP];
 #pragma unroll
-      for (int h = 0; h < GP; ++h) mu[h] = sg[h] = 0ull;
+        for (int h = 0; h < GP; ++h) mu[h] = sg[h] = 0ull;
 #pragma unroll
-      for (int c = 0; c < DPL / 4; ++c) {
-        const float4 m4 = pv ? *reinterpret_cast<const float4*>(sb + (pg * 2) * D + hl * DPL + 4 * c)
-                             : make_float4(0.f, 0.f, 0.f, 0.f);
-        const float4 v4 = pv ? *reinterpret_cast<const float4*>(sb + (pg * 2 + 1) * D + hl * DPL + 4 * c)
-                             : make_float4(0.f, 0.f, 0.f, 0.f);
-        const unsigned long long m01 = f2_pack(m4.x, m4.y), m23 = f2_pack(m4.z, m4.w);
-        const unsigned long long v01 = f2_pack(v4.x, v4.y), v23 = f2_pack(v4.z, v4.w);
+        for (int c = 0; c < CH; ++c) {
+          const float4 m4 = pv ? *reinterpret_cast<const float4*>(mrow + 4 * (hl + 16 * c)) : make_float4(0.f, 0.f, 0.f, 0.f);
+          const float4 v4 = pv ? *reinterpret_cast<const float4*>(vrow + 4 * (hl + 16 * c)) : make_float4(0.f, 0.f, 0.f, 0.f);
+          const unsigned long long m01 = f2_pack(m4.x, m4.y), m23 = f2_pack(m4.z, m4.w);
+          const unsigned long long v01 = f2_pack(v4.x, v4.y), v23 = f2_pack(v4.z, v4.w);
+#pragma unroll
+          for (int h = 0; h < GP; ++h) {
+            mu[h] = f2_fma(qp[h][2 * c], m01, mu[h]);
+            mu[h] = f2_fma(qp[h][2 * c + 1], m23, mu[h]);
+            sg[h] = f2_fma(q2p[h][2 * c], v01, sg[h]);
+            sg[h] = f2_fma(q2p[h][2 * c + 1], v23, sg[h]);
+          }
+        }
 #pragma unroll
         for (int h = 0; h < GP; ++h) {
-          mu[h] = f2_fma(qp[h][2 * c], m01, mu[h]);
-          mu[h] = f2_fma(qp[h][2 * c + 1], m23, mu[h]);
-          sg[h] = f2_fma(q2p[h][2 * c], v01, sg[h]);
-          sg[h] = f2_fma(q2p[h][2 * c + 1], v23, sg[h]);
+          v[(i * 2 + 0) * GP + h] = f2_sum(mu[h]);
+          v[(i * 2 + 1) * GP + h] = f2_sum(sg[h]);
         }
       }
-#pragma unroll
-      for (int h = 0; h < GP; ++h) {
-        v[(i * 2 + 0) * GP + h] = f2_sum(mu[h]);
-        v[(i * 2 + 1) * GP + h] = f2_sum(sg[h]);
-      }
+      my_ph = phys_sm[st * PPS + my_pg];
     }
-    const int my_ph = phys_sm[st * PPS + my_pg];
-    __syncwarp();  // every lane has read the stage: it may be refilled
-    if (j + NST < n_mine) issue(ph_next, st);
+    __syncwarp();
+    if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(&empty[st])) : "memory");
+    if (warp == 0 && j + NST < n_mine) {  // refill once every warp released the stage
+      if (!mbar_wait_bounded(&empty[st], par)) {
+        stuck = 1;
+        break;
+      }
+      issue(g + NST, st);
+    }
+    if (!active) continue;
     int n = NV;
 #pragma unroll
     for (int o = 8; o >= 1; o >>= 1) {
@@ -351,18 +367,23 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_kernel(DecodeArgs a) {
       }
     }
   }
-  if (stuck >= 0) {  // a copy never completed: flag, let the later ones land (bounded), stop
+  if (stuck) {
+    // A copy or a stage release never arrived within the bound: flag it and
+    // stop. Copies already issued are waited for (bounded) before leaving.
     if (lane == 0) raise_flag(a.status, ENTMAXKV_DEV_TIMEOUT);
-    for (int j = stuck + 1; j < n_mine && j < stuck + NST; ++j)
-      mbar_wait_bounded(&bars[j % NST], (uint32_t)((j / NST) & 1));
+    if (warp == 0)
+      for (int st = 0; st < NST; ++st) mbar_wait_bounded(&full[st], 0u), mbar_wait_bounded(&full[st], 1u);
   }
 #pragma unroll
   for (int i = 0; i < NFIN; ++i)
     if (writer && my_qty == 0 && my_h0 + i < a.G && runmax[i] > -CUDART_INF_F)
-      atomicMax(&smax[my_h0 + i], ord_enc(runmax[i]));
+      atomicMax(&smax[warp][my_h0 + i], ord_enc(runmax[i]));
   __syncthreads();
-  if (threadIdx.x < a.G && smax[threadIdx.x] != 0u)
-    atomicMax(&a.mmax[(size_t)s * a.Hq + (size_t)kvh * a.G + threadIdx.x], smax[threadIdx.x]);
+  if (threadIdx.x < 8 * GP) {
+    const int w = threadIdx.x / GP, h = threadIdx.x % GP;
+    if (w < KH && h < a.G && smax[w][h] != 0u)
+      atomicMax(&a.mmax[(size_t)s * a.Hq + (size_t)(kv0 + w) * a.G + h], smax[w][h]);
+  }
 }
 
 static int grid_x_for(int units, int per_block, int sms, int other_blocks) {
@@ -390,6 +411,7 @@ cudaError_t launch_bbox(const DecodeArgs& a, int kv_dtype, int sms, cudaStream_t
 template <typename TQ, int D, int GP>
 static cudaError_t gauss_launch(const DecodeArgs& a, dim3 grid, cudaStream_t st) {
   constexpr int smem = gauss_smem_bytes<D>();
+  static_assert(gauss_smem_bytes<D>() <= 227 * 1024, "stages exceed shared memory");
   cudaError_t e = cudaFuncSetAttribute(gauss_kernel<TQ, D, GP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   gauss_kernel<TQ, D, GP><<<grid, kGaussWarps * 32, smem, st>>>(a);
@@ -405,13 +427,15 @@ static cudaError_t gauss_dispatch_g(const DecodeArgs& a, dim3 grid, cudaStream_t
 }
 
 cudaError_t launch_gauss(const DecodeArgs& a, int kv_dtype, int sms, cudaStream_t st) {
-  // ~3 blocks per SM (64 KiB of stages each) across all (sequence, KV head) rows
+  // ~2 blocks per SM (96 KiB of stages each) over all (sequence, 8-KV-head) rows,
+  // at least 8 page groups per block
   const int groups = (a.maxp + kGaussPPS - 1) / kGaussPPS;
-  int gx = (groups + kGaussWarps - 1) / kGaussWarps;
-  const int cap = (3 * sms + a.Hkv * a.S - 1) / (a.Hkv * a.S);
+  const int rows = ((a.Hkv + 7) / 8) * a.S;
+  int gx = (groups + 7) / 8;
+  const int cap = (2 * sms + rows - 1) / rows;
   if (gx > cap) gx = cap;
   if (gx < 1) gx = 1;
-  dim3 grid(gx, a.Hkv, a.S);
+  dim3 grid(gx, (a.Hkv + 7) / 8, a.S);
   cudaError_t e;
   if (kv_dtype == ENTMAXKV_BF16)
     e = a.D == 128 ? gauss_dispatch_g<__nv_bfloat16, 128>(a, grid, st)

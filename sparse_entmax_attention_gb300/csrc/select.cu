@@ -148,14 +148,17 @@ __global__ void __cluster_dims__(kTauhatCluster, 1, 1) __launch_bounds__(kThread
           next = tau;
           stop = true;
         } else {
-          // Halley on g = log F: g' = −dF/F, g'' = d2F/F − (dF/F)²
-          // (a float log is ample for the step); Newton when not usable
+          // Halley on g = log F: g' = −dF/F, g'' = d2F/F − (dF/F)², all in
+          // float (the step needs ~1e-7 relative, not FP64); Newton when not usable
           next = CUDART_NAN;
           if (F > 0.0 && dF > 0.0) {
-            const double g = (double)logf((float)F), g1 = -dF / F, g2 = d2F / F - g1 * g1;
-            const double den = 2.0 * g1 * g1 - g * g2;
-            next = den > 0.0 ? tau - 2.0 * g * g1 / den : tau - g / g1;
-            if (!(next > lo && next < hi)) next = tau - g / g1;
+            const float Ff = (float)F, g = logf(Ff), g1 = -(float)dF / Ff;
+            const float g2 = (float)d2F / Ff - g1 * g1;
+            const float den = 2.0f * g1 * g1 - g * g2;
+            const float newton = -g / g1;
+            const float halley = den > 0.0f ? -2.0f * g * g1 / den : newton;
+            next = tau + (double)halley;
+            if (!(next > lo && next < hi)) next = tau + (double)newton;
           }
           if (!(next > lo && next < hi)) next = isinf(hi) ? lo + 1.0 : 0.5 * (lo + hi);
           const double tol = 1e-6 * fmax(1.0, fabs(next));
