@@ -11,10 +11,10 @@ constexpr int kSmCount = 152;                 // GB300: grids are sized for its 
 constexpr int kTargetBlocks = 2 * kSmCount;   // decode blocks per launch: one wave at 2 per SM
 
 struct Layout {
-  size_t zmax, mmax, cnt_a, cnt_b, cand_cnt, kept_mass, dbar, bitmap, ctrl_end;
-  size_t tauhat, tau_ws, nsel_ws, sel_list, bbox_u, bbox_uhat, gauss_ms, cand, z, pmax, partial, diag;
+  size_t zmax, cnt_a, cnt_b, cand_cnt, kept_mass, dbar, bitmap, ctrl_end;
+  size_t tauhat, tau_ws, nsel_ws, sel_list, bbox_u, bbox_uhat, gauss_ms, cand, z, pmax, partial, diag, mslot;
   size_t total;
-  int splits, cap_pages, words, kpages, gcap, pstride;
+  int splits, cap_pages, words, kpages, gcap, pstride, mslots;
 };
 
 static size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -80,7 +80,6 @@ static int compute_layout(const entmaxkv_config* c, int S, int policy, int budge
   auto take = [&](size_t bytes) { size_t o = off; off = up256(off + bytes); return o; };
   const size_t none = (size_t)-1;
   L.zmax = take(nq * 4);
-  L.mmax = take(nq * 4);
   L.cnt_a = take(nk * 4);
   L.cnt_b = take(nk * 4);
   L.cand_cnt = take(nq * 4);
@@ -101,6 +100,8 @@ static int compute_layout(const entmaxkv_config* c, int S, int policy, int budge
   L.pstride = (G * D + 2 * G + 3) & ~3;
   L.partial = take(nk * (size_t)L.splits * L.pstride * 4);
   L.diag = take(nq * 4);
+  L.mslots = gauss_grid_x(maxp, Hkv, S, kSmCount);
+  L.mslot = policy == ENTMAXKV_POLICY_GAUSSIAN ? take(nq * (size_t)L.mslots * 4) : none;
   L.total = off;
   return ENTMAXKV_OK;
 }
@@ -258,7 +259,6 @@ static int32_t decode_impl(const entmaxkv_config* cfg, const entmaxkv_cache* cac
   a.tau_out = tau;
   a.delta_out = delta;
   a.zmax = at<uint32_t>(workspace, L.zmax);
-  a.mmax = at<uint32_t>(workspace, L.mmax);
   a.cnt_a = at<int32_t>(workspace, L.cnt_a);
   a.cnt_b = at<int32_t>(workspace, L.cnt_b);
   a.cand_cnt = at<int32_t>(workspace, L.cand_cnt);
@@ -278,13 +278,19 @@ static int32_t decode_impl(const entmaxkv_config* cfg, const entmaxkv_cache* cac
   a.partial = at<float>(workspace, L.partial);
   a.pstride = L.pstride;
   a.diag = at<int32_t>(workspace, L.diag);
+  a.mslot = at<uint32_t>(workspace, L.mslot);
+  a.mslots = L.mslots;
+  a.ctrl = reinterpret_cast<uint4*>(workspace);
+  a.ctrl_vec = (int)(L.ctrl_end / 16);
 
   cudaStream_t s = (cudaStream_t)stream;
   auto mark = [&](int i) -> cudaError_t {
     return events ? cudaEventRecord((cudaEvent_t)events[i], s) : cudaSuccess;
   };
   cudaError_t e = mark(0);
-  if (e == cudaSuccess) e = cudaMemsetAsync(workspace, 0, L.ctrl_end, s);
+  // The selective policies' first kernel clears the control words itself.
+  if (e == cudaSuccess && policy != ENTMAXKV_POLICY_TOPK && policy != ENTMAXKV_POLICY_GAUSSIAN)
+    e = cudaMemsetAsync(workspace, 0, L.ctrl_end, s);
   if (e == cudaSuccess) e = mark(1);
   const int dt = cfg->kv_dtype;
   // stage 1: page scoring

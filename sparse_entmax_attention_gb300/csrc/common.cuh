@@ -47,7 +47,6 @@ struct DecodeArgs {
   float* delta_out;
   // workspace: zeroed at the start of every decode
   uint32_t* zmax;      // [S][Hq]   ordered-encoded max z
-  uint32_t* mmax;      // [S][Hq]   ordered-encoded max m (Gaussian)
   int32_t* cnt_a;      // [S][Hkv]  blocks of pass A done
   int32_t* cnt_b;      // [S][Hkv]  blocks of pass B done
   int32_t* cand_cnt;   // [S][Hq]   candidate pages listed
@@ -68,6 +67,10 @@ struct DecodeArgs {
   float* partial;      // [S][Hkv][splits][pstride]: acc [G][D], then (m, l) per head
   int pstride;         // floats per split partial: G·D + 2G rounded up to 4
   int32_t* diag;       // [S][Hq] τ̂ iterations (Gaussian)
+  uint32_t* mslot;     // [S][Hq][mslots] ordered-encoded max m of each scoring block
+  int mslots;          // scoring blocks per (sequence, 8 KV heads) row
+  uint4* ctrl;         // the workspace words zeroed before each decode's counters are used
+  int ctrl_vec;        // their count in 16-byte units
 };
 
 struct AppendArgs {
@@ -88,6 +91,16 @@ struct AppendArgs {
 
 // ---------------------------------------------------------------------------
 // small helpers
+
+// Zero the decode's control words (counters, maxima, bitmap) with every block
+// of the launching grid taking a slice; run by the first kernel of a policy.
+__device__ __forceinline__ void clear_ctrl_slice(uint4* ctrl, int n_vec) {
+  const int nb = gridDim.x * gridDim.y * gridDim.z;
+  const int b = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+  const int per = (n_vec + nb - 1) / nb;
+  const int lo = b * per, hi = min(n_vec, lo + per);
+  for (int i = lo + (int)threadIdx.x; i < hi; i += blockDim.x) ctrl[i] = make_uint4(0u, 0u, 0u, 0u);
+}
 
 __device__ __forceinline__ void raise_flag(uint32_t* st, uint32_t bit) {
   if (st) atomicOr(st, bit);
@@ -358,6 +371,7 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* sh, int& total) 
 cudaError_t launch_append(const AppendArgs& a, int kv_dtype, cudaStream_t st);
 cudaError_t launch_bbox(const DecodeArgs& a, int kv_dtype, int sms, cudaStream_t st);
 cudaError_t launch_gauss(const DecodeArgs& a, int kv_dtype, int sms, cudaStream_t st);
+int gauss_grid_x(int maxp, int Hkv, int S, int sms);
 cudaError_t launch_tauhat(const DecodeArgs& a, cudaStream_t st);
 cudaError_t launch_topk(const DecodeArgs& a, int mode, cudaStream_t st);
 cudaError_t launch_pass_a(const DecodeArgs& a, int kv_dtype, cudaStream_t st);

@@ -47,6 +47,7 @@ __global__ void __launch_bounds__(kThreads) bbox_bf16_kernel(DecodeArgs a) {
   const int kvh = blockIdx.y, s = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = lane >> 2, c = lane & 3;
+  clear_ctrl_slice(a.ctrl, a.ctrl_vec);
   const int seq = seq_row(a.seq_ids, s, a.max_seqs, threadIdx.x == 0 ? a.status : nullptr);
   if (seq < 0) return;
   const int L = seq_len_clamped(a.seq_lens, seq, a.maxp, a.P, threadIdx.x == 0 ? a.status : nullptr);
@@ -129,6 +130,7 @@ template <int D>
 __global__ void __launch_bounds__(kThreads) bbox_f32_kernel(DecodeArgs a) {
   __shared__ float qs[8][D];
   const int kvh = blockIdx.y, s = blockIdx.z;
+  clear_ctrl_slice(a.ctrl, a.ctrl_vec);
   const int seq = seq_row(a.seq_ids, s, a.max_seqs, threadIdx.x == 0 ? a.status : nullptr);
   if (seq < 0) return;
   const int L = seq_len_clamped(a.seq_lens, seq, a.maxp, a.P, threadIdx.x == 0 ? a.status : nullptr);
@@ -205,6 +207,10 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_kernel(DecodeArgs a) {
   uint64_t* empty = full + NST;
   int* phys_sm = reinterpret_cast<int*>(empty + NST);                   // [NST][PPS]
   __shared__ uint32_t smax[8][GP];
+  clear_ctrl_slice(a.ctrl, a.ctrl_vec);
+  // this block's slot of the per-head maxima starts as "none"
+  for (int i = threadIdx.x; i < KH * a.G; i += blockDim.x)
+    a.mslot[((size_t)s * a.Hq + (size_t)kv0 * a.G + i) * a.mslots + blockIdx.x] = 0u;
   const int seq = seq_row(a.seq_ids, s, a.max_seqs, threadIdx.x == 0 ? a.status : nullptr);
   if (seq < 0) return;
   const int L = seq_len_clamped(a.seq_lens, seq, a.maxp, a.P, threadIdx.x == 0 ? a.status : nullptr);
@@ -381,8 +387,8 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_kernel(DecodeArgs a) {
   __syncthreads();
   if (threadIdx.x < 8 * GP) {
     const int w = threadIdx.x / GP, h = threadIdx.x % GP;
-    if (w < KH && h < a.G && smax[w][h] != 0u)
-      atomicMax(&a.mmax[(size_t)s * a.Hq + (size_t)(kv0 + w) * a.G + h], smax[w][h]);
+    if (w < KH && h < a.G)
+      a.mslot[((size_t)s * a.Hq + (size_t)(kv0 + w) * a.G + h) * a.mslots + blockIdx.x] = smax[w][h];
   }
 }
 
@@ -426,16 +432,19 @@ static cudaError_t gauss_dispatch_g(const DecodeArgs& a, dim3 grid, cudaStream_t
   return gauss_launch<TQ, D, 8>(a, grid, st);
 }
 
-cudaError_t launch_gauss(const DecodeArgs& a, int kv_dtype, int sms, cudaStream_t st) {
-  // ~2 blocks per SM (96 KiB of stages each) over all (sequence, 8-KV-head) rows,
-  // at least 8 page groups per block
-  const int groups = (a.maxp + kGaussPPS - 1) / kGaussPPS;
-  const int rows = ((a.Hkv + 7) / 8) * a.S;
+// ~2 blocks per SM (96 KiB of stages each) over all (sequence, 8-KV-head)
+// rows, at least 8 page groups per block.
+int gauss_grid_x(int maxp, int Hkv, int S, int sms) {
+  const int groups = (maxp + kGaussPPS - 1) / kGaussPPS;
+  const int rows = ((Hkv + 7) / 8) * S;
   int gx = (groups + 7) / 8;
   const int cap = (2 * sms + rows - 1) / rows;
   if (gx > cap) gx = cap;
-  if (gx < 1) gx = 1;
-  dim3 grid(gx, (a.Hkv + 7) / 8, a.S);
+  return gx < 1 ? 1 : gx;
+}
+
+cudaError_t launch_gauss(const DecodeArgs& a, int kv_dtype, int sms, cudaStream_t st) {
+  dim3 grid(a.mslots, (a.Hkv + 7) / 8, a.S);
   cudaError_t e;
   if (kv_dtype == ENTMAXKV_BF16)
     e = a.D == 128 ? gauss_dispatch_g<__nv_bfloat16, 128>(a, grid, st)

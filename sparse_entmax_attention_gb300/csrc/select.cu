@@ -31,10 +31,6 @@ namespace ekv {
 
 constexpr int kTauhatIters = 60;
 
-struct Sums3 {
-  double f, d, e;
-};
-
 __device__ __forceinline__ int page_tokens(int p, int n_pages, int L, int P) {
   return p == n_pages - 1 ? L - p * P : P;
 }
@@ -43,13 +39,18 @@ __device__ __forceinline__ float sqrt_2ln(int n, int P, float c_full) {
   return n == P ? c_full : sqrtf(2.0f * logf((float)n));
 }
 
+// All arithmetic is float, on offsets from base = max_p m_p − 1 (each page's
+// m_p − base is formed once), so every τ̂ is base + off with off = O(1).
+// Per iteration each warp publishes its partial (F, F', F'') in shared memory;
+// after one cluster barrier every warp of every block reads all
+// kTauhatCluster·kWarps partials over distributed shared memory, sums them in
+// a fixed butterfly order and takes the same step: all copies of the state
+// stay bit-identical without further synchronisation.
 __global__ void __cluster_dims__(kTauhatCluster, 1, 1) __launch_bounds__(kThreads, 2)
     tauhat_kernel(DecodeArgs a) {
+  static_assert(kTauhatCluster * kWarps == 64, "two partials per lane");
   cg::cluster_group cluster = cg::this_cluster();
-  __shared__ Sums3 slot[2];
-  __shared__ float red_f[kWarps], red_d[kWarps], red_e[kWarps];
-  __shared__ double tau_sh;
-  __shared__ int done_sh;
+  __shared__ float3 slot[2][kWarps];
   const int h = blockIdx.y, s = blockIdx.z;
   const int kvh = h / a.G;
   const int rank = (int)cluster.block_rank();
@@ -60,8 +61,12 @@ __global__ void __cluster_dims__(kTauhatCluster, 1, 1) __launch_bounds__(kThread
   const int L = seq_len_clamped(a.seq_lens, seq, a.maxp, a.P, nullptr);
   const int n_pages = (L + a.P - 1) / a.P;
   if (n_pages == 0) return;
-  const double M = (double)ord_dec(a.mmax[(size_t)s * a.Hq + h]);
-  if (!(M > -CUDART_INF)) return;  // no readable page
+  float M = -CUDART_INF_F;
+  const uint32_t* ms_slots = a.mslot + ((size_t)s * a.Hq + h) * a.mslots;
+  for (int i = lane; i < a.mslots; i += 32) M = fmaxf(M, ord_dec(__ldcg(ms_slots + i)));
+  M = warp_max(M);
+  if (!(M > -CUDART_INF_F)) return;  // no readable page
+  const float base = M - 1.0f;
   const bool beta2 = a.beta == 2.0f;
   const float2* ms = a.gauss_ms + ((size_t)s * a.Hq + h) * a.maxp;
   const int words = (n_pages + 31) / 32;
@@ -72,30 +77,29 @@ __global__ void __cluster_dims__(kTauhatCluster, 1, 1) __launch_bounds__(kThread
   // each, which covers 8·256·kRegPages pages per query head); pages beyond
   // that are re-read from memory.
   constexpr int kRegPages = 16;
-  float2 mr[kRegPages];
-  float ir[kRegPages], nr[kRegPages];
+  float mb[kRegPages], sr[kRegPages], ir[kRegPages], nr[kRegPages];
 #pragma unroll
   for (int k = 0; k < kRegPages; ++k) {
     const int p = p_lo + tid + k * kThreads;
+    float2 v = make_float2(-CUDART_INF_F, 0.0f);
+    nr[k] = 0.0f;
     if (p < p_hi) {
-      mr[k] = ms[p];
+      v = ms[p];
       nr[k] = (float)page_tokens(p, n_pages, L, a.P);
-    } else {
-      mr[k] = make_float2(-CUDART_INF_F, 0.0f);
-      nr[k] = 0.0f;
     }
-    ir[k] = mr[k].y > 0.0f ? 1.0f / mr[k].y : 0.0f;
+    mb[k] = v.x - base;
+    sr[k] = v.y;
+    ir[k] = v.y > 0.0f ? 1.0f / v.y : 0.0f;
   }
-  double lo = M - 1.0, hi = CUDART_INF, tau = lo;
+  float lo = 0.0f, hi = CUDART_INF_F, off = 0.0f;  // offsets from base; F(lo) ≥ 1
   bool converged = false;
   int it = 0;
   for (; it < kTauhatIters; ++it) {
-    const float tf = (float)tau;
     float f = 0.0f, df = 0.0f, d2f = 0.0f;
 #pragma unroll
     for (int k = 0; k < kRegPages; ++k) {
       float g, dg, d2g;
-      gauss_moment2(mr[k].x - tf, mr[k].y, ir[k], beta2, g, dg, d2g);
+      gauss_moment2(mb[k] - off, sr[k], ir[k], beta2, g, dg, d2g);
       f = fmaf(nr[k], g, f);
       df = fmaf(nr[k], dg, df);
       d2f = fmaf(nr[k], d2g, d2f);
@@ -103,7 +107,7 @@ __global__ void __cluster_dims__(kTauhatCluster, 1, 1) __launch_bounds__(kThread
     for (int p = p_lo + tid + kRegPages * kThreads; p < p_hi; p += kThreads) {
       const float2 v = ms[p];
       float g, dg, d2g;
-      gauss_moment2(v.x - tf, v.y, v.y > 0.0f ? 1.0f / v.y : 0.0f, beta2, g, dg, d2g);
+      gauss_moment2((v.x - base) - off, v.y, v.y > 0.0f ? 1.0f / v.y : 0.0f, beta2, g, dg, d2g);
       const float np = (float)page_tokens(p, n_pages, L, a.P);
       f = fmaf(np, g, f);
       df = fmaf(np, dg, df);
@@ -112,80 +116,51 @@ __global__ void __cluster_dims__(kTauhatCluster, 1, 1) __launch_bounds__(kThread
     f = warp_sum(f);
     df = warp_sum(df);
     d2f = warp_sum(d2f);
-    if (lane == 0) {
-      red_f[warp] = f;
-      red_d[warp] = df;
-      red_e[warp] = d2f;
-    }
-    __syncthreads();
-    if (tid == 0) {
-      double sf = 0.0, sd = 0.0, se = 0.0;
-      for (int w = 0; w < kWarps; ++w) {
-        sf += red_f[w];
-        sd += red_d[w];
-        se += red_e[w];
-      }
-      slot[it & 1] = Sums3{sf, sd, se};
-    }
+    if (lane == 0) slot[it & 1][warp] = make_float3(f, df, d2f);
     cluster.sync();
-    if (warp == 0) {
-      // lane r reads block r's partial sums; a fixed-order tree sum gives every
-      // block bit-identical totals, hence identical steps
-      Sums3 v = lane < kTauhatCluster ? cluster.map_shared_rank(&slot[0], lane)[it & 1] : Sums3{0.0, 0.0, 0.0};
-#pragma unroll
-      for (int o = kTauhatCluster / 2; o >= 1; o >>= 1) {
-        v.f += __shfl_down_sync(0xffffffffu, v.f, o);
-        v.d += __shfl_down_sync(0xffffffffu, v.d, o);
-        v.e += __shfl_down_sync(0xffffffffu, v.e, o);
+    const float3 e0 = cluster.map_shared_rank(&slot[it & 1][0], lane / kWarps)[lane % kWarps];
+    const float3 e1 = cluster.map_shared_rank(&slot[it & 1][0], (lane + 32) / kWarps)[lane % kWarps];
+    float F = e0.x + e1.x, D1 = e0.y + e1.y, D2 = e0.z + e1.z;  // F, −dF/dτ, d²F/dτ²
+    F = warp_sum(F);
+    D1 = warp_sum(D1);
+    D2 = warp_sum(D2);
+    if (F >= 1.0f) lo = off;
+    else hi = off;
+    float next;
+    bool stop;
+    if (F == 1.0f) {
+      next = off;
+      stop = true;
+    } else {
+      // Halley on g = log F: g' = −D1/F, g'' = D2/F − g'²; Newton when not usable
+      next = CUDART_NAN_F;
+      if (F > 0.0f && D1 > 0.0f) {
+        const float g = logf(F), g1 = -D1 / F, g2 = D2 / F - g1 * g1;
+        const float den = 2.0f * g1 * g1 - g * g2;
+        const float newton = -g / g1;
+        next = off + (den > 0.0f ? -2.0f * g * g1 / den : newton);
+        if (!(next > lo && next < hi)) next = off + newton;
       }
-      if (lane == 0) {
-        const double F = v.f, dF = v.d, d2F = v.e;  // F, −dF/dτ, d²F/dτ²
-        if (F >= 1.0) lo = tau;
-        else hi = tau;
-        double next;
-        bool stop;
-        if (F == 1.0) {
-          next = tau;
-          stop = true;
-        } else {
-          // Halley on g = log F: g' = −dF/F, g'' = d2F/F − (dF/F)², all in
-          // float (the step needs ~1e-7 relative, not FP64); Newton when not usable
-          next = CUDART_NAN;
-          if (F > 0.0 && dF > 0.0) {
-            const float Ff = (float)F, g = logf(Ff), g1 = -(float)dF / Ff;
-            const float g2 = (float)d2F / Ff - g1 * g1;
-            const float den = 2.0f * g1 * g1 - g * g2;
-            const float newton = -g / g1;
-            const float halley = den > 0.0f ? -2.0f * g * g1 / den : newton;
-            next = tau + (double)halley;
-            if (!(next > lo && next < hi)) next = tau + (double)newton;
-          }
-          if (!(next > lo && next < hi)) next = isinf(hi) ? lo + 1.0 : 0.5 * (lo + hi);
-          const double tol = 1e-6 * fmax(1.0, fabs(next));
-          stop = fabs(next - tau) <= tol || (hi - lo) <= tol;
-        }
-        tau = next;
-        done_sh = stop ? 1 : 0;
-        tau_sh = tau;
-      }
+      if (!(next > lo && next < hi)) next = isinf(hi) ? lo + 1.0f : 0.5f * (lo + hi);
+      const float tol = 1e-6f * fmaxf(1.0f, fabsf(base + next));
+      stop = fabsf(next - off) <= tol || (hi - lo) <= tol;
     }
-    __syncthreads();
-    if (done_sh) {
+    off = next;
+    if (stop) {
       converged = true;
       break;
     }
-    tau = tau_sh;
   }
-  const float th = (float)tau_sh;
   cluster.sync();  // no block leaves while another may still read its slots
   if (rank == 0 && tid == 0) {
-    a.tauhat[(size_t)s * a.Hq + h] = th;
+    a.tauhat[(size_t)s * a.Hq + h] = base + off;
     a.diag[(size_t)s * a.Hq + h] = it + 1;
     if (!converged) raise_flag(a.status, ENTMAXKV_DEV_TAUHAT_NOCONV);
   }
   // Selection bits from the cached pages: for each k the warp's lanes hold 32
-  // consecutive pages starting on a bitmap word.
-  const float thr = th - a.margin_z;
+  // consecutive pages starting on a bitmap word. Keep p iff
+  // m_p + ς_p·sqrt(2 ln n_p) ≥ τ̂ − (α−1)Δ, here on offsets from base.
+  const float thr = off - a.margin_z;
   const float c_full = sqrtf(2.0f * logf((float)a.P));
   uint32_t* bm = a.bitmap + ((size_t)s * a.Hkv + kvh) * a.words;
 #pragma unroll
@@ -193,7 +168,7 @@ __global__ void __cluster_dims__(kTauhatCluster, 1, 1) __launch_bounds__(kThread
     const int p0 = p_lo + warp * 32 + k * kThreads;
     if (p0 >= p_hi) break;
     const int p = p0 + lane;
-    const bool sel = p < p_hi && mr[k].x + mr[k].y * sqrt_2ln((int)nr[k], a.P, c_full) >= thr;
+    const bool sel = p < p_hi && mb[k] + sr[k] * sqrt_2ln((int)nr[k], a.P, c_full) >= thr;
     const uint32_t bits = __ballot_sync(0xffffffffu, sel);
     if (lane == 0 && bits) atomicOr(&bm[p0 >> 5], bits);
   }
@@ -202,7 +177,7 @@ __global__ void __cluster_dims__(kTauhatCluster, 1, 1) __launch_bounds__(kThread
     bool sel = false;
     if (p < p_hi) {
       const float2 v = ms[p];
-      sel = v.x + v.y * sqrt_2ln(page_tokens(p, n_pages, L, a.P), a.P, c_full) >= thr;
+      sel = (v.x - base) + v.y * sqrt_2ln(page_tokens(p, n_pages, L, a.P), a.P, c_full) >= thr;
     }
     const uint32_t bits = __ballot_sync(0xffffffffu, sel);
     if (lane == 0 && bits) atomicOr(&bm[p0 >> 5], bits);
