@@ -177,7 +177,7 @@ def run_ours(args, rank, world):
         # 129 MB L2 without leaving dirty lines behind to be written back.
         @staticmethod
         def zero_():
-            torch.sum(flush_buf, dtype=torch.int64, out=flush_out)
+            torch.sum(flush_buf, dim=0, dtype=torch.int64, out=flush_out)
 
     flush = _Flush()
     n_app = [0]
