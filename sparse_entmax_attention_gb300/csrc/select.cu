@@ -132,18 +132,29 @@ __global__ void __cluster_dims__(kTauhatCluster, 1, 1) __launch_bounds__(kThread
       next = off;
       stop = true;
     } else {
-      // Halley on g = log F: g' = −D1/F, g'' = D2/F − g'²; Newton when not usable
+      // Halley on g = log F: g' = −D1/F, g'' = D2/F − g'²; Newton when not
+      // usable. A step below the tolerance ends the solve (in float it may not
+      // even move off, so it must not be judged against the bracket).
       next = CUDART_NAN_F;
+      stop = false;
+      const float tol = 1e-6f * fmaxf(1.0f, fabsf(base + off));
       if (F > 0.0f && D1 > 0.0f) {
         const float g = logf(F), g1 = -D1 / F, g2 = D2 / F - g1 * g1;
         const float den = 2.0f * g1 * g1 - g * g2;
         const float newton = -g / g1;
-        next = off + (den > 0.0f ? -2.0f * g * g1 / den : newton);
-        if (!(next > lo && next < hi)) next = off + newton;
+        const float step = den > 0.0f ? -2.0f * g * g1 / den : newton;
+        if (fabsf(step) <= tol) {
+          next = off + step;
+          stop = true;
+        } else {
+          next = off + step;
+          if (!(next > lo && next < hi)) next = off + newton;
+        }
       }
-      if (!(next > lo && next < hi)) next = isinf(hi) ? lo + 1.0f : 0.5f * (lo + hi);
-      const float tol = 1e-6f * fmaxf(1.0f, fabsf(base + next));
-      stop = fabsf(next - off) <= tol || (hi - lo) <= tol;
+      if (!stop) {
+        if (!(next > lo && next < hi)) next = isinf(hi) ? lo + 1.0f : 0.5f * (lo + hi);
+        stop = fabsf(next - off) <= tol || (hi - lo) <= tol;
+      }
     }
     off = next;
     if (stop) {
