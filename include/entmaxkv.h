@@ -233,6 +233,35 @@ int32_t entmaxkv_workspace_layout(const entmaxkv_config* cfg, int32_t n_seqs,
                                   int32_t policy, int32_t budget_tokens,
                                   entmaxkv_workspace_view* view);
 
+/*
+ * Full-cache softmax decode for callers that cannot allocate device memory.
+ * No passage of the EntmaxKV pages corresponds to this call: it exists for
+ * embedders such as custom allocators' own callbacks, graph-building code
+ * that must not allocate, or runtimes whose device memory is owned by someone
+ * else, which cannot provide the scratch entmaxkv_decode needs.
+ *
+ * It runs the same computation as entmaxkv_decode with
+ * policy = ENTMAXKV_POLICY_SOFTMAX (out [n_seqs][Hq][head_dim] float32 and
+ * lse [n_seqs][Hq] = log Σ exp(s_i), lse may be NULL), but its scratch is a
+ * fixed array inside the library of entmaxkv_noalloc_scratch_bytes() bytes
+ * (8 MiB), which every GPU that loads the library holds until the process
+ * exits. It calls no cudaMalloc/cudaFree and no allocating library routine.
+ *   - Shapes whose softmax workspace (entmaxkv_workspace_bytes(cfg, n_seqs,
+ *     ENTMAXKV_POLICY_SOFTMAX, 0)) exceeds that size are rejected with
+ *     ENTMAXKV_ERR_WORKSPACE_TOO_SMALL before anything is queued.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Every call shares the one array: calls that may overlap on the GPU
+ *     (different streams, or different host threads) race and must be
+ *     serialised by the caller. The counters the decode relies on are cleared
+ *     at the start of each call; the array keeps the last call's partial sums.
+ */
+size_t entmaxkv_noalloc_scratch_bytes(void);
+int32_t entmaxkv_decode_softmax_noalloc(const entmaxkv_config* cfg, const entmaxkv_cache* cache,
+                                        const void* q, const int32_t* seq_ids, int32_t n_seqs,
+                                        float* out, float* lse, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -29,7 +29,8 @@ DEV_CAND_OVERFLOW, DEV_TAU_NOCONV, DEV_BAD_SEQ_ID, DEV_TIMEOUT = 0x8, 0x10, 0x20
 # Symbols the header declares (kept in step with include/entmaxkv.h by a test).
 EXPORTS = ("entmaxkv_version", "entmaxkv_status_string", "entmaxkv_append",
            "entmaxkv_workspace_bytes", "entmaxkv_decode", "entmaxkv_decode_profiled",
-           "entmaxkv_workspace_layout")
+           "entmaxkv_workspace_layout", "entmaxkv_noalloc_scratch_bytes",
+           "entmaxkv_decode_softmax_noalloc")
 STAGE_EVENTS = 6
 STAGES = ("clear", "score", "select", "pass_a", "pass_b")
 
@@ -83,6 +84,11 @@ def lib() -> ctypes.CDLL:
                                   f32, i32, i32, f32, u32, vp, sz, vp, vp, i32, vp, vp, vp, vp]
     L.entmaxkv_decode_profiled.restype = i32
     L.entmaxkv_decode_profiled.argtypes = L.entmaxkv_decode.argtypes + [ctypes.POINTER(ctypes.c_void_p)]
+    L.entmaxkv_noalloc_scratch_bytes.restype = sz
+    L.entmaxkv_noalloc_scratch_bytes.argtypes = []
+    L.entmaxkv_decode_softmax_noalloc.restype = i32
+    L.entmaxkv_decode_softmax_noalloc.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(CacheView),
+                                                  vp, vp, i32, vp, vp, vp]
     L.entmaxkv_workspace_layout.restype = i32
     L.entmaxkv_workspace_layout.argtypes = [ctypes.POINTER(Config), i32, i32, i32,
                                             ctypes.POINTER(WorkspaceView)]
