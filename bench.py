@@ -151,7 +151,7 @@ def algorithmic_bytes(wl, policy, o, ws, view):
 def run_ours(args, rank, world):
     import torch
     from sparse_entmax_attention_gb300 import binding as B
-    from sparse_entmax_attention_gb300 import runner, synth
+    from sparse_entmax_attention_gb300 import replicas, runner, synth
 
     local = int(os.environ.get("LOCAL_RANK", 0))
     torch.cuda.set_device(local)
@@ -226,21 +226,18 @@ def run_ours(args, rank, world):
     # graph capture appended nothing (capture does not execute); the counter
     # tracks the appends the replays perform.
     timed(graph.replay, W, adv)
-    if world > 1:
-        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    replicas.barrier()
     torch.cuda.synchronize()
     clk = ClockSampler(local)
     clk.start()
     t0 = time.perf_counter()
     step_us = timed(graph.replay, K, lambda i: adv(W + i))
+    replicas.barrier()
+    torch.cuda.synchronize()
     wall = time.perf_counter() - t0
     clocks = clk.stop()
-    if world > 1:
-        t = torch.tensor([statistics.mean(step_us)], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        mean_us = float(t.item())
-    else:
-        mean_us = statistics.mean(step_us)
+    mean_us = replicas.max_over_ranks(statistics.mean(step_us), device=dev)
     assert cache.device_status() & ~B.DEV_CAND_OVERFLOW == 0, hex(cache.device_status())
 
     view_g = B.workspace_layout(cache, spec.batch, "gaussian", 0)
@@ -255,6 +252,7 @@ def run_ours(args, rank, world):
         "steps": K,
         "warmup": W,
         "ms_per_step": round(mean_us / 1e3, 5),
+        "steps_per_s_all_ranks": round(world * 1e6 / mean_us, 1),
         "higher_is_better": False,
         "scaling": "weak",
         "vs_baseline": None,

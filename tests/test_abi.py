@@ -1,0 +1,114 @@
+"""The C ABI without a GPU: the library loads, exports every function the
+header declares, and rejects bad arguments on the host before any CUDA call
+(all pointers below are dummies that are never dereferenced)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from sparse_entmax_attention_gb300 import binding as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _header_functions():
+    src = open(os.path.join(ROOT, "include", "entmaxkv.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return set(re.findall(r"\b(entmaxkv_\w+)\s*\(", src))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(B.LIB_PATH):
+        from sparse_entmax_attention_gb300 import build
+        build.build_library()
+    return B.lib()
+
+
+def test_exports_every_declared_function(lib):
+    declared = _header_functions()
+    assert declared == set(B.EXPORTS), declared ^ set(B.EXPORTS)
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_version_and_status_strings(lib):
+    assert lib.entmaxkv_version() == 1
+    for code in range(5):
+        assert lib.entmaxkv_status_string(code)
+    assert lib.entmaxkv_status_string(99) == b"unknown status"
+
+
+def _cfg(**kw):
+    base = dict(num_kv_heads=8, group=4, head_dim=128, page_size=32, max_seqs=1,
+                max_pages_per_seq=32768, num_phys_pages=32768, kv_dtype=B.BF16)
+    base.update(kw)
+    return B.Config(*[base[f] for f, _ in B.Config._fields_])
+
+
+def _view():
+    return B.CacheView(*([256] * 8), None)
+
+
+def _decode(lib, cfg, **kw):
+    a = dict(q=256, seq_ids=None, n=1, alpha=1.5, policy=B.POLICY_GAUSSIAN, budget=0, margin=0.5,
+             flags=0, ws=256, ws_bytes=1 << 40, out=256, ids=None, stride=0, nsel=None, tau=None,
+             delta=None)
+    a.update(kw)
+    return lib.entmaxkv_decode(ctypes.byref(cfg), ctypes.byref(_view()), ctypes.c_void_p(a["q"]),
+                               a["seq_ids"], a["n"], a["alpha"], a["policy"], a["budget"],
+                               a["margin"], a["flags"], ctypes.c_void_p(a["ws"]), a["ws_bytes"],
+                               ctypes.c_void_p(a["out"]) if a["out"] else None, a["ids"], a["stride"],
+                               a["nsel"], a["tau"], a["delta"], None)
+
+
+def test_workspace_sizing(lib):
+    cfg = _cfg()
+    sizes = {p: lib.entmaxkv_workspace_bytes(ctypes.byref(cfg), 1, p, 2048) for p in range(4)}
+    assert all(v > 0 for v in sizes.values())
+    assert sizes[B.POLICY_TOPK] < sizes[B.POLICY_FULL]
+    assert lib.entmaxkv_workspace_bytes(ctypes.byref(cfg), 1, B.POLICY_TOPK, 16) == 0  # < 1 page
+    assert lib.entmaxkv_workspace_bytes(ctypes.byref(cfg), 1, 7, 0) == 0               # no policy
+    assert lib.entmaxkv_workspace_bytes(ctypes.byref(cfg), 0, 0, 0) == 0               # no sequences
+    v = B.WorkspaceView()
+    assert lib.entmaxkv_workspace_layout(ctypes.byref(cfg), 1, B.POLICY_GAUSSIAN, 0, ctypes.byref(v)) == 0
+    assert v.gauss_ms % 256 == 0 and v.tauhat % 256 == 0 and v.bbox_u == 2 ** 64 - 1
+    assert v.total == lib.entmaxkv_workspace_bytes(ctypes.byref(cfg), 1, B.POLICY_GAUSSIAN, 0)
+
+
+@pytest.mark.parametrize("field,value,code", [
+    ("head_dim", 96, 2), ("page_size", 8, 2), ("group", 9, 2), ("kv_dtype", 5, 1),
+    ("num_kv_heads", 0, 1), ("max_pages_per_seq", 0, 1)])
+def test_bad_config_is_rejected(lib, field, value, code):
+    assert _decode(lib, _cfg(**{field: value})) == code
+
+
+def test_bad_decode_arguments_are_rejected(lib):
+    cfg = _cfg()
+    assert _decode(lib, cfg, alpha=1.0, policy=B.POLICY_FULL) == 1          # α ≤ 1
+    assert _decode(lib, cfg, alpha=float("nan"), policy=B.POLICY_FULL) == 1
+    assert _decode(lib, cfg, alpha=1.25) == 2                               # Gaussian needs α ∈ {1.5, 2}
+    assert _decode(lib, cfg, policy=B.POLICY_TOPK, budget=8) == 1           # budget below one page
+    assert _decode(lib, cfg, margin=float("inf")) == 1
+    assert _decode(lib, cfg, out=0) == 1                                    # out is required
+    assert _decode(lib, cfg, ws=256 + 8) == 3                               # misaligned workspace
+    assert _decode(lib, cfg, ws_bytes=1024) == 3                            # too small
+    ids = ctypes.c_void_p(256)
+    assert _decode(lib, cfg, policy=B.POLICY_TOPK, budget=2048, ids=ids, stride=10) == 1
+    assert _decode(lib, cfg, n=0) == 0                                      # nothing to do
+    assert _decode(lib, cfg, n=-1) == 1
+
+
+def test_bad_append_arguments_are_rejected(lib):
+    cfg = _cfg()
+    view = _view()
+    f = lib.entmaxkv_append
+    p = ctypes.c_void_p(256)
+    assert f(ctypes.byref(cfg), ctypes.byref(view), p, p, None, 1, 0, None) == 0   # no tokens
+    assert f(ctypes.byref(cfg), ctypes.byref(view), None, p, None, 1, 4, None) == 1
+    assert f(ctypes.byref(cfg), ctypes.byref(view), p, p, None, -1, 4, None) == 1
+    assert f(ctypes.byref(cfg), ctypes.byref(view), p, p, None, 1, 32768 * 32 + 1, None) == 1
+    bad = B.CacheView(0, *([256] * 7), None)
+    assert f(ctypes.byref(cfg), ctypes.byref(bad), p, p, None, 1, 4, None) == 1
