@@ -417,15 +417,27 @@ def oracle_step_us(K, V, Q, P, n_kv_heads, meta):
     return dt * n_kv_heads * 1e6, dt
 
 
-def cpu_baseline(wl, qdev):
+def cpu_baseline(wl, qdev, min_s=10.0, max_reps=3):
+    """One whole Gaussian decode step (every KV head and its query heads) by
+    the oracle, repeated until at least `min_s` seconds of oracle time."""
     from oracle import pages as opg
-    K, V, Q = host_sample(wl, qdev)
-    meta = opg.page_metadata(K, wl.spec.page_size)   # built once, like the cache metadata
-    us, dt = oracle_step_us(K, V, Q, wl.spec.page_size, wl.spec.num_kv_heads, meta)
+    spec = wl.spec
+    per_step, total, reps = [], 0.0, 0
+    while reps < max_reps and (reps == 0 or total < min_s):
+        t_step = 0.0
+        for kvh in range(spec.num_kv_heads):
+            K, V, Q = host_sample(wl, qdev, kvh)
+            meta = opg.page_metadata(K, spec.page_size)   # kept by the cache, not per step
+            t_step += oracle_step_us(K, V, Q, spec.page_size, 1, meta)[1]
+            del K, V, meta
+        per_step.append(t_step)
+        total += t_step
+        reps += 1
+    us = statistics.mean(per_step) * 1e6
     return {"value": round(us, 1), "unit": "us/step", "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"1 of {wl.spec.num_kv_heads} KV heads (its {wl.spec.group} query heads) of one "
-                      f"Gaussian decode step at 1M tokens, float64 numpy ({dt:.1f} s), scaled x"
-                      f"{wl.spec.num_kv_heads}; page metadata prebuilt; BLAS default threads"}
+            "sample": f"{reps} x one whole Gaussian decode step at 1M tokens ({spec.num_kv_heads} KV "
+                      f"heads x {spec.group} query heads), float64 numpy, {total:.1f} s of oracle "
+                      f"time; page metadata prebuilt (the cache keeps it); BLAS default threads"}
 
 
 def run_reference(args, rank, world):

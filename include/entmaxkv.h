@@ -101,6 +101,9 @@ typedef struct {
  *   status         one uint32 the kernels OR ENTMAXKV_DEV_* bits into (may be NULL)
  * Metadata of a page covers its valid tokens only and is written by
  * entmaxkv_append; a partial last page holds n_p = len − P·(pages−1) tokens.
+ * Every pool and metadata array starts on a 16-byte boundary (the kernels
+ * move whole 16-byte vectors and page slabs); a misaligned pointer is
+ * rejected with ENTMAXKV_ERR_INVALID_ARG before any launch.
  */
 typedef struct {
   void* k_pool;

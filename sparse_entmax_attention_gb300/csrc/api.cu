@@ -12,7 +12,7 @@ constexpr int kTargetBlocks = 2 * kSmCount;   // decode blocks per launch: one w
 
 struct Layout {
   size_t zmax, cnt_a, cnt_b, cand_cnt, kept_mass, dbar, bitmap, ctrl_end;
-  size_t tauhat, tau_ws, nsel_ws, sel_list, bbox_u, bbox_uhat, gauss_ms, cand, z, pmax, partial, diag, mslot;
+  size_t tauhat, tau_ws, nsel_ws, sel_list, sel_pp, bbox_u, bbox_uhat, gauss_ms, cand, z, pmax, partial, diag, mslot;
   size_t total;
   int splits, cap_pages, words, kpages, gcap, pstride, mslots;
 };
@@ -36,6 +36,9 @@ static int check_cache(const entmaxkv_cache* k) {
   if (!k || !k->k_pool || !k->v_pool || !k->kmin || !k->kmax || !k->mean || !k->m2 ||
       !k->block_table || !k->seq_lens)
     return ENTMAXKV_ERR_INVALID_ARG;
+  const void* arrays[] = {k->k_pool, k->v_pool, k->kmin, k->kmax, k->mean, k->m2};
+  for (const void* p : arrays)
+    if ((uintptr_t)p & 15u) return ENTMAXKV_ERR_INVALID_ARG;
   return ENTMAXKV_OK;
 }
 
@@ -94,6 +97,7 @@ static int compute_layout(const entmaxkv_config* c, int S, int policy, int budge
   L.bbox_u = policy == ENTMAXKV_POLICY_TOPK ? take(nq * (size_t)maxp * 4) : none;
   L.bbox_uhat = policy == ENTMAXKV_POLICY_TOPK ? take(nk * (size_t)maxp * 4) : none;
   L.gauss_ms = policy == ENTMAXKV_POLICY_GAUSSIAN ? take(nq * (size_t)maxp * 8) : none;
+  L.sel_pp = entmax ? take(nk * (size_t)cap * 8) : none;
   L.cand = entmax ? take(nq * (size_t)cap * 8) : none;
   L.z = entmax ? take(nk * (size_t)cap * P * G * 4) : none;
   L.pmax = entmax ? take(nk * (size_t)cap * G * 4) : none;
@@ -269,6 +273,7 @@ static int32_t decode_impl(const entmaxkv_config* cfg, const entmaxkv_cache* cac
   a.tau_ws = at<double>(workspace, L.tau_ws);
   a.nsel_ws = at<int32_t>(workspace, L.nsel_ws);
   a.sel_list = at<int32_t>(workspace, L.sel_list);
+  a.sel_pp = at<int2>(workspace, L.sel_pp);
   a.bbox_u = at<float>(workspace, L.bbox_u);
   a.bbox_uhat = at<float>(workspace, L.bbox_uhat);
   a.gauss_ms = at<float2>(workspace, L.gauss_ms);

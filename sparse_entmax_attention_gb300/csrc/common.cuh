@@ -58,6 +58,7 @@ struct DecodeArgs {
   double* tau_ws;      // [S][Hq]   exact τ (double)
   int32_t* nsel_ws;    // [S][Hkv]
   int32_t* sel_list;   // [S][Hkv][cap_pages]
+  int2* sel_pp;        // [S][Hkv][cap_pages] (logical, physical) page of each rank; phys −1: unreadable
   float* bbox_u;       // [S][Hq][maxp]
   float* bbox_uhat;    // [S][Hkv][maxp]
   float2* gauss_ms;    // [S][Hq][maxp]
@@ -283,6 +284,11 @@ __device__ __forceinline__ void gauss_moment2(float a, float sg, float inv_sg, b
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
+}
+// Bulk prefetch of a contiguous global range into L2 (16-byte aligned start,
+// size a multiple of 16).
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(p), "r"(bytes) : "memory");
 }
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count) : "memory");

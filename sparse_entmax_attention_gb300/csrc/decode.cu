@@ -181,6 +181,7 @@ __device__ double solve_tau_warp(const SolveSrc& S, double tau0, float beta, boo
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads) pass_a_kernel(DecodeArgs a) {
   __shared__ int list[kListCap];
+  __shared__ int phys_sh[kListCap];
   __shared__ int sh_scan[32];
   __shared__ float qs[8][D];
   __shared__ float wmax[kWarps][8];
@@ -190,7 +191,7 @@ __global__ void __launch_bounds__(kThreads) pass_a_kernel(DecodeArgs a) {
   __shared__ int last_sh;
   __shared__ __align__(16) float pool[kSolveCap];  // last block: page and score candidates
   __shared__ float T0_sh[8], tlb_sh[8];
-  __shared__ int nc_sh[8], np_sh[8], nz_sh[8];
+  __shared__ int nc_sh[8], np_sh[8], nz_sh[8], off_sh[9];
   const int split = blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = a.G, P = a.P;
@@ -205,10 +206,24 @@ __global__ void __launch_bounds__(kThreads) pass_a_kernel(DecodeArgs a) {
     a.nsel_ws[skv] = n_sel;
     if (a.n_sel_out) a.n_sel_out[skv] = n_sel;
   }
+  // Every page of the block is looked up at once, and the K slabs of each
+  // warp's next kAhead pages are kept requested into L2 by bulk prefetches
+  // (≤ kAhead·8 pages a block in flight, well inside L2 for a full grid).
+  constexpr int kAhead = 3;
+  const bool staged = hi - lo <= kListCap;
+  const uint32_t slab_bytes = (uint32_t)(P * D * sizeof(T));
+  auto k_slab = [&](int ph) {
+    return (const char*)a.k_pool + ((size_t)ph * a.Hkv + kvh) * slab_bytes;
+  };
   for (int i = tid; i < hi - lo; i += kThreads) {
     const int page = bitmap ? list[i] : lo + i;
     if (bitmap) a.sel_list[skv * a.cap_pages + lo + i] = page;
     if (a.page_ids) a.page_ids[skv * a.page_ids_stride + lo + i] = page;
+    if (staged) {
+      const int ph = phys_page(a.block_table, seq, page, a.maxp, a.nphys, a.status);
+      phys_sh[i] = ph;
+      if (ph >= 0 && i < kAhead * kWarps) prefetch_l2_bulk(k_slab(ph), slab_bytes);
+    }
   }
   const size_t hq0 = (size_t)s * a.Hq + (size_t)kvh * G;  // first query head of the group
   if (tid < 8) th_sh[tid] = (a.policy == ENTMAXKV_POLICY_GAUSSIAN && tid < G) ? a.tauhat[hq0 + tid] : 0.0f;
@@ -227,10 +242,15 @@ __global__ void __launch_bounds__(kThreads) pass_a_kernel(DecodeArgs a) {
   for (int i = warp; i < hi - lo; i += kWarps) {
     const int rank = lo + i;
     const int page = bitmap ? list[i] : rank;
-    const int ph = phys_page(a.block_table, seq, page, a.maxp, a.nphys, lane == 0 ? a.status : nullptr);
+    const int ph = staged ? phys_sh[i] : phys_page(a.block_table, seq, page, a.maxp, a.nphys, lane == 0 ? a.status : nullptr);
+    if (staged && lane == 0 && i + kAhead * kWarps < hi - lo) {
+      const int ph_next = phys_sh[i + kAhead * kWarps];
+      if (ph_next >= 0) prefetch_l2_bulk(k_slab(ph_next), slab_bytes);
+    }
     const int nv = min(P, L - page * P);
     float* zb = a.z + (skv * a.cap_pages + rank) * (size_t)P * G;
     float* pm = a.pmax + (skv * a.cap_pages + rank) * (size_t)G;
+    if (lane == 0) a.sel_pp[skv * a.cap_pages + rank] = make_int2(page, ph);
     if (ph < 0) {  // unreadable page: no scores
       for (int e = lane; e < P * G; e += 32) zb[e] = -CUDART_INF_F;
       if (lane < G) pm[lane] = -CUDART_INF_F;
@@ -321,22 +341,32 @@ __global__ void __launch_bounds__(kThreads) pass_a_kernel(DecodeArgs a) {
     if (a.policy == ENTMAXKV_POLICY_GAUSSIAN && ks != 0.0f) atomicAdd(&a.kept_mass[hq0 + tid], ks);
   }
   __syncthreads();
-  // candidate pages: those whose max clears (best known max − 1)
+  // candidate pages: those whose max clears (best known max − 1). Lane l
+  // checks rank l of the warp's 32 for every head at once; lane h then
+  // reserves head h's slots, so each chunk costs one load and one atomic
+  // round trip.
   for (int i0 = warp * 32; i0 < hi - lo; i0 += kThreads) {
     const int i = i0 + lane;
     const bool in = i < hi - lo;
     const int rank = lo + i;
     const float* pm = a.pmax + (skv * a.cap_pages + (in ? rank : lo)) * (size_t)G;
-    for (int hg = 0; hg < G; ++hg) {
-      const bool pred = in && pm[hg] > thr_sh[hg];
-      const uint32_t bits = __ballot_sync(0xffffffffu, pred);
-      if (!bits) continue;
-      int base = 0;
-      if (lane == 0) base = atomicAdd(&a.cand_cnt[hq0 + hg], __popc(bits));
-      base = __shfl_sync(0xffffffffu, base, 0);
-      const int idx = base + __popc(bits & ((1u << lane) - 1u));
-      if (pred)  // a page enters a head's list at most once
-        a.cand[(hq0 + hg) * a.cap_pages + idx] = make_int2(rank, __float_as_int(pm[hg]));
+    float pmv[8];
+#pragma unroll
+    for (int hg = 0; hg < 8; ++hg) pmv[hg] = (in && hg < G) ? pm[hg] : -CUDART_INF_F;
+    uint32_t mine = 0u, bits[8];
+#pragma unroll
+    for (int hg = 0; hg < 8; ++hg) {
+      bits[hg] = __ballot_sync(0xffffffffu, hg < G && pmv[hg] > thr_sh[hg]);
+      if (lane == hg) mine = bits[hg];
+    }
+    int base = 0;
+    if (mine) base = atomicAdd(&a.cand_cnt[hq0 + lane], __popc(mine));
+#pragma unroll
+    for (int hg = 0; hg < 8; ++hg) {
+      const int b = __shfl_sync(0xffffffffu, base, hg);
+      if ((bits[hg] >> lane) & 1u)  // a page enters a head's list at most once
+        a.cand[(hq0 + hg) * a.cap_pages + b + __popc(bits[hg] & ((1u << lane) - 1u))] =
+            make_int2(rank, __float_as_int(pmv[hg]));
     }
   }
   // the last block of this (sequence, KV head) solves τ
@@ -347,15 +377,18 @@ __global__ void __launch_bounds__(kThreads) pass_a_kernel(DecodeArgs a) {
   if (!last_sh) return;
   __threadfence();
   // Exact τ of the G query heads, block-parallel:
-  //  A  keep the listed candidate pages whose max clears T0 = z_max − 1;
+  //  A  keep the listed candidate pages whose max clears T0 = z_max − 1
+  //     (all heads' lists at once, a thread per entry);
   //  B  τ_lb = exact threshold of (a subset of) those page maxima: they are
   //     real token scores, so their normaliser is below the full one, τ ≥ τ_lb;
   //  C  gather the scores above τ_lb from the pages whose max clears τ_lb
-  //     (a warp per page, lanes over its tokens);
+  //     (a thread per 8 tokens of a page, every head at once);
   //  D  one warp per head solves exactly on that set, starting from τ_lb.
-  const int capP = kSolveCap / 2 / G;   // page maxima per head for B
-  const int capZ = kSolveCap / 2 / G;   // candidate scores per head for D
+  // Shared pool: page maxima [G][capP], their ranks [G][capP], scores [G][capZ].
+  const int capP = kSolveCap / 4 / G;
+  const int capZ = kSolveCap / 2 / G;
   float* pv = pool;
+  int* pr = reinterpret_cast<int*>(pool + kSolveCap / 4);
   float* zc = pool + kSolveCap / 2;
   const float* zbase = a.z + skv * a.cap_pages * (size_t)P * G;
   const int2* clist = a.cand + hq0 * a.cap_pages;
@@ -367,14 +400,24 @@ __global__ void __launch_bounds__(kThreads) pass_a_kernel(DecodeArgs a) {
     nz_sh[tid] = 0;
   }
   __syncthreads();
-  for (int h = 0; h < G; ++h) {  // A
-    const int nc = nc_sh[h];
-    const float T0 = T0_sh[h];
-    for (int k = tid; k < nc; k += kThreads) {
-      const float pmv = __int_as_float(__ldcg(clist + (size_t)h * a.cap_pages + k).y);
-      if (pmv > T0) {
-        const int pos = atomicAdd(&np_sh[h], 1);
-        if (pos < capP) pv[h * capP + pos] = pmv;
+  if (tid == 0) {
+    int t = 0;
+    for (int h = 0; h < G; ++h) {
+      off_sh[h] = t;
+      t += nc_sh[h];
+    }
+    off_sh[G] = t;
+  }
+  __syncthreads();
+  for (int e = tid; e < off_sh[G]; e += kThreads) {  // A
+    int h = 0;
+    while (e >= off_sh[h + 1]) ++h;
+    const int2 c = __ldcg(clist + (size_t)h * a.cap_pages + (e - off_sh[h]));
+    if (__int_as_float(c.y) > T0_sh[h]) {
+      const int pos = atomicAdd(&np_sh[h], 1);
+      if (pos < capP) {
+        pv[h * capP + pos] = __int_as_float(c.y);
+        pr[h * capP + pos] = c.x;
       }
     }
   }
@@ -393,25 +436,42 @@ __global__ void __launch_bounds__(kThreads) pass_a_kernel(DecodeArgs a) {
     }
     if (lane == 0) tlb_sh[h] = tlb;
   }
+  // C walks the kept pages of A, or a head's whole list where A overflowed
+  const int cpp = P / 8;  // 8-token pieces per page
+  if (tid == 0) {
+    int t = 0;
+    for (int h = 0; h < G; ++h) {
+      off_sh[h] = t;
+      t += (np_sh[h] <= capP ? np_sh[h] : nc_sh[h]) * cpp;
+    }
+    off_sh[G] = t;
+  }
   __syncthreads();
-  for (int h = 0; h < G; ++h) {  // C: a lane per candidate page, its token loads in flight together
-    const int nc = nc_sh[h];
+  for (int e = tid; e < off_sh[G]; e += kThreads) {  // C
+    int h = 0;
+    while (e >= off_sh[h + 1]) ++h;
+    const int j = (e - off_sh[h]) / cpp, piece = (e - off_sh[h]) - j * cpp;
+    int rank;
+    float pmv;
+    if (np_sh[h] <= capP) {
+      rank = pr[h * capP + j];
+      pmv = pv[h * capP + j];
+    } else {
+      const int2 c = __ldcg(clist + (size_t)h * a.cap_pages + j);
+      rank = c.x;
+      pmv = __int_as_float(c.y);
+    }
     const float tlb = tlb_sh[h];
-    for (int k = tid; k < nc; k += kThreads) {
-      const int2 e = __ldcg(clist + (size_t)h * a.cap_pages + k);
-      if (!(__int_as_float(e.y) > tlb)) continue;
-      const float* zr = zbase + (size_t)e.x * P * G + h;
-      for (int t0 = 0; t0 < P; t0 += 8) {
-        float v[8];
+    if (!(pmv > tlb)) continue;
+    const float* zr = zbase + ((size_t)rank * P + 8 * piece) * G + h;
+    float v[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) v[u] = __ldcg(zr + (t0 + u) * G);
+    for (int u = 0; u < 8; ++u) v[u] = __ldcg(zr + u * G);
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          if (v[u] > tlb) {
-            const int pos = atomicAdd(&nz_sh[h], 1);
-            if (pos < capZ) zc[h * capZ + pos] = v[u];
-          }
-        }
+    for (int u = 0; u < 8; ++u) {
+      if (v[u] > tlb) {
+        const int pos = atomicAdd(&nz_sh[h], 1);
+        if (pos < capZ) zc[h * capZ + pos] = v[u];
       }
     }
   }
@@ -533,6 +593,9 @@ __global__ void __launch_bounds__(kThreads) pass_b_kernel(DecodeArgs a) {
   __shared__ __align__(16) float red[kWarps][GP][D];
   __shared__ float dsum[kWarps][GP];
   __shared__ float4 red4[kThreads];
+  static_assert(sizeof(red4) >= kListCap * sizeof(int), "the V page list shares the combine scratch");
+  int* list_sh = reinterpret_cast<int*>(red4);  // the page list is done before the combine starts
+  __shared__ int scan_sh[32];
   __shared__ int last_sh;
   const int split = blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -564,75 +627,123 @@ __global__ void __launch_bounds__(kThreads) pass_b_kernel(DecodeArgs a) {
     for (int j = 0; j < VEC; ++j) acc[h][j] = 0.0f;
   float* zw = zs[warp];
 
-  // The warp takes 32 consecutive ranks of its block's share at a time: lane l
-  // checks rank l's page maxima, and the pages that need V are processed in
-  // turn, each with its z and V loads issued together.
-  const int nb = hi - lo;
-  for (int c0 = warp * 32; c0 < nb; c0 += kThreads) {
-    const int i = c0 + lane;
-    bool need = false;
-    int page = -1;
-    if (i < nb) {
-      const int rank = lo + i;
-      need = dense;
-      const float* pm = a.pmax + (skv * a.cap_pages + rank) * (size_t)G;
+  // One page: its z staged in shared memory, all its V loads issued at once
+  // (lane: 16 bytes of a row, tokens tg, tg+TG, ...), p·v accumulated in fp32.
+  auto do_page = [&](int rank, int pg, int ph) {
+    const int nv = min(P, L - pg * P);
+    const float* zb = a.z + (skv * a.cap_pages + rank) * (size_t)P * G;
+    const T* vs = (const T*)a.v_pool + ((size_t)ph * a.Hkv + kvh) * P * D + dc * VEC;
+    float4 zl[2];
 #pragma unroll
-      for (int h = 0; h < GP; ++h)
-        if (h < G) need = need || (__ldcg(pm + h) > tau[h]);
-      if (need) page = bitmap ? __ldcg(&a.sel_list[skv * a.cap_pages + rank]) : rank;
+    for (int u = 0; u < 2; ++u) {  // P·G ≤ 256 floats: two float4 per lane at most
+      const int e = 4 * lane + 128 * u;
+      zl[u] = e < P * G ? __ldcg(reinterpret_cast<const float4*>(zb + e)) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    const int ph_l = need ? phys_page(a.block_table, seq, page, a.maxp, a.nphys, nullptr) : -1;
-    uint32_t bits = __ballot_sync(0xffffffffu, ph_l >= 0);
-    while (bits) {
-      const int b = __ffs(bits) - 1;
-      bits &= bits - 1u;
-      const int rank = lo + c0 + b;
-      const int pg = __shfl_sync(0xffffffffu, page, b);
-      const int ph = __shfl_sync(0xffffffffu, ph_l, b);
-      const int nv = min(P, L - pg * P);
-      const float* zb = a.z + (skv * a.cap_pages + rank) * (size_t)P * G;
-      const T* vs = (const T*)a.v_pool + ((size_t)ph * a.Hkv + kvh) * P * D + dc * VEC;
-      float4 zl[2];
+    for (int c1 = 0; c1 < MAXT; c1 += CH) {
+      uint4 raw[CH];
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {  // P·G ≤ 256 floats: two float4 per lane at most
-        const int e = 4 * lane + 128 * u;
-        zl[u] = e < P * G ? __ldcg(reinterpret_cast<const float4*>(zb + e)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int u = 0; u < CH; ++u) {
+        const int t = tg + TG * (c1 + u);
+        raw[u] = t < nv ? ld_stream(vs + (size_t)t * D) : make_uint4(0u, 0u, 0u, 0u);
       }
-      for (int c1 = 0; c1 < MAXT; c1 += CH) {
-        uint4 raw[CH];
+      if (c1 == 0) {
 #pragma unroll
-        for (int u = 0; u < CH; ++u) {
-          const int t = tg + TG * (c1 + u);
-          raw[u] = t < nv ? ld_stream(vs + (size_t)t * D) : make_uint4(0u, 0u, 0u, 0u);
+        for (int u = 0; u < 2; ++u) {
+          const int e = 4 * lane + 128 * u;
+          if (e < P * G) *reinterpret_cast<float4*>(zw + e) = zl[u];
         }
-        if (c1 == 0) {
+        __syncwarp();
+      }
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int e = 4 * lane + 128 * u;
-            if (e < P * G) *reinterpret_cast<float4*>(zw + e) = zl[u];
-          }
-          __syncwarp();
-        }
+      for (int u = 0; u < CH; ++u) {
+        const int t = tg + TG * (c1 + u);
+        if (t < nv) {
+          float v[VEC];
+          VTraits<T>::unpack(raw[u], v);
 #pragma unroll
-        for (int u = 0; u < CH; ++u) {
-          const int t = tg + TG * (c1 + u);
-          if (t < nv) {
-            float v[VEC];
-            VTraits<T>::unpack(raw[u], v);
+          for (int h = 0; h < GP; ++h) {
+            if (h < G) {
+              const float zv = zw[t * G + h];
+              const float p = sizeof(T) == 4 ? pos_pow((float)((double)zv - taud[h]), a.beta)
+                                             : pos_pow(zv - tau[h], a.beta);
 #pragma unroll
-            for (int h = 0; h < GP; ++h) {
-              if (h < G) {
-                const float zv = zw[t * G + h];
-                const float p = sizeof(T) == 4 ? pos_pow((float)((double)zv - taud[h]), a.beta)
-                                               : pos_pow(zv - tau[h], a.beta);
-#pragma unroll
-                for (int j = 0; j < VEC; ++j) acc[h][j] = fmaf(p, v[j], acc[h][j]);
-              }
+              for (int j = 0; j < VEC; ++j) acc[h][j] = fmaf(p, v[j], acc[h][j]);
             }
           }
         }
       }
-      __syncwarp();
+    }
+    __syncwarp();
+  };
+
+  // Pages that need V: some head's page max above its τ. Unless every page
+  // needs V, every block lists those ranks in rank order (a thread checks up
+  // to 32 consecutive ranks, one scan places them) and takes an even share of
+  // the list, a warp per page: pages that cluster in rank still spread over
+  // the whole grid. Larger selections fall back to the block's own rank range.
+  bool listed = false;
+  int n_list = 0;
+  if (!dense && n_sel <= 32 * kThreads) {
+    const int per = (n_sel + kThreads - 1) / kThreads;
+    const int r0 = tid * per;
+    uint32_t mask = 0u;
+    for (int k = 0; k < per; ++k) {
+      const int r = r0 + k;
+      if (r < n_sel) {
+        const float* pm = a.pmax + (skv * a.cap_pages + r) * (size_t)G;
+        bool need = false;
+#pragma unroll
+        for (int h = 0; h < GP; ++h)
+          if (h < G) need = need || (__ldcg(pm + h) > tau[h]);
+        if (need) mask |= 1u << k;
+      }
+    }
+    int nv_all;
+    int j = block_exclusive_scan(__popc(mask), scan_sh, nv_all);
+    const int s_lo = (int)(((long long)nv_all * split) / a.splits);
+    const int s_hi = (int)(((long long)nv_all * (split + 1)) / a.splits);
+    if (s_hi - s_lo <= kListCap) {
+      listed = true;
+      n_list = s_hi - s_lo;
+      while (mask && j < s_hi) {
+        const int k = __ffs(mask) - 1;
+        mask &= mask - 1u;
+        if (j >= s_lo) list_sh[j - s_lo] = r0 + k;
+        ++j;
+      }
+    }
+    __syncthreads();
+  }
+  if (listed) {
+    for (int j = warp; j < n_list; j += kWarps) {
+      const int rank = list_sh[j];
+      const int2 pp = __ldcg(&a.sel_pp[skv * a.cap_pages + rank]);
+      if (pp.y >= 0) do_page(rank, pp.x, pp.y);
+    }
+  } else {
+    // The warp takes 32 consecutive ranks of the block's range at a time:
+    // lane l checks rank l's page maxima, and the pages that need V are
+    // processed in turn.
+    const int nb = hi - lo;
+    for (int c0 = warp * 32; c0 < nb; c0 += kThreads) {
+      const int i = c0 + lane;
+      bool need = false;
+      int2 pp = make_int2(0, -1);
+      if (i < nb) {
+        const int rank = lo + i;
+        need = dense;
+        const float* pm = a.pmax + (skv * a.cap_pages + rank) * (size_t)G;
+#pragma unroll
+        for (int h = 0; h < GP; ++h)
+          if (h < G) need = need || (__ldcg(pm + h) > tau[h]);
+        if (need) pp = __ldcg(&a.sel_pp[skv * a.cap_pages + rank]);
+      }
+      uint32_t bits = __ballot_sync(0xffffffffu, pp.y >= 0);
+      while (bits) {
+        const int b = __ffs(bits) - 1;
+        bits &= bits - 1u;
+        do_page(lo + c0 + b, __shfl_sync(0xffffffffu, pp.x, b), __shfl_sync(0xffffffffu, pp.y, b));
+      }
     }
   }
 #pragma unroll

@@ -51,6 +51,7 @@ __global__ void __cluster_dims__(kTauhatCluster, 1, 1) __launch_bounds__(kThread
   static_assert(kTauhatCluster * kWarps == 64, "two partials per lane");
   cg::cluster_group cluster = cg::this_cluster();
   __shared__ float3 slot[2][kWarps];
+  __shared__ float wmax_sh[kWarps];
   const int h = blockIdx.y, s = blockIdx.z;
   const int kvh = h / a.G;
   const int rank = (int)cluster.block_rank();
@@ -61,12 +62,6 @@ __global__ void __cluster_dims__(kTauhatCluster, 1, 1) __launch_bounds__(kThread
   const int L = seq_len_clamped(a.seq_lens, seq, a.maxp, a.P, nullptr);
   const int n_pages = (L + a.P - 1) / a.P;
   if (n_pages == 0) return;
-  float M = -CUDART_INF_F;
-  const uint32_t* ms_slots = a.mslot + ((size_t)s * a.Hq + h) * a.mslots;
-  for (int i = lane; i < a.mslots; i += 32) M = fmaxf(M, ord_dec(__ldcg(ms_slots + i)));
-  M = warp_max(M);
-  if (!(M > -CUDART_INF_F)) return;  // no readable page
-  const float base = M - 1.0f;
   const bool beta2 = a.beta == 2.0f;
   const float2* ms = a.gauss_ms + ((size_t)s * a.Hq + h) * a.maxp;
   const int words = (n_pages + 31) / 32;
@@ -75,7 +70,8 @@ __global__ void __cluster_dims__(kTauhatCluster, 1, 1) __launch_bounds__(kThread
 
   // This thread's pages stay in registers for every iteration (kRegPages
   // each, which covers 8·256·kRegPages pages per query head); pages beyond
-  // that are re-read from memory.
+  // that are re-read from memory. Their loads are issued before the maximum
+  // is known.
   constexpr int kRegPages = 16;
   float mb[kRegPages], sr[kRegPages], ir[kRegPages], nr[kRegPages];
 #pragma unroll
@@ -87,9 +83,24 @@ __global__ void __cluster_dims__(kTauhatCluster, 1, 1) __launch_bounds__(kThread
       v = ms[p];
       nr[k] = (float)page_tokens(p, n_pages, L, a.P);
     }
-    mb[k] = v.x - base;
+    mb[k] = v.x;
     sr[k] = v.y;
-    ir[k] = v.y > 0.0f ? 1.0f / v.y : 0.0f;
+  }
+  // M = max_p m_p from the scoring blocks' maxima, split over the block
+  float M = -CUDART_INF_F;
+  const uint32_t* ms_slots = a.mslot + ((size_t)s * a.Hq + h) * a.mslots;
+  for (int i = tid; i < a.mslots; i += kThreads) M = fmaxf(M, ord_dec(__ldcg(ms_slots + i)));
+  M = warp_max(M);
+  if (lane == 0) wmax_sh[warp] = M;
+  __syncthreads();
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wmax_sh[w]);
+  if (!(M > -CUDART_INF_F)) return;  // no readable page
+  const float base = M - 1.0f;
+#pragma unroll
+  for (int k = 0; k < kRegPages; ++k) {
+    mb[k] -= base;
+    ir[k] = sr[k] > 0.0f ? 1.0f / sr[k] : 0.0f;
   }
   float lo = 0.0f, hi = CUDART_INF_F, off = 0.0f;  // offsets from base; F(lo) ≥ 1
   bool converged = false;
@@ -148,7 +159,14 @@ __global__ void __cluster_dims__(kTauhatCluster, 1, 1) __launch_bounds__(kThread
           stop = true;
         } else {
           next = off + step;
-          if (!(next > lo && next < hi)) next = off + newton;
+          if (!(next > lo && next < hi)) {
+            next = off + newton;
+          } else if (den > 0.0f && step * step * fabsf(step) <= 1e-2f * tol) {
+            // Halley converges cubically: the error left after this step is
+            // about K·step³ (K ≈ 0.1 on page-score models), far below tol,
+            // so the confirming evaluation is skipped.
+            stop = true;
+          }
         }
       }
       if (!stop) {

@@ -112,3 +112,15 @@ def test_bad_append_arguments_are_rejected(lib):
     assert f(ctypes.byref(cfg), ctypes.byref(view), p, p, None, 1, 32768 * 32 + 1, None) == 1
     bad = B.CacheView(0, *([256] * 7), None)
     assert f(ctypes.byref(cfg), ctypes.byref(bad), p, p, None, 1, 4, None) == 1
+
+
+def test_misaligned_cache_arrays_are_rejected(lib):
+    cfg = _cfg()
+    for i in range(6):  # k_pool, v_pool, kmin, kmax, mean, m2
+        ptrs = [256] * 8
+        ptrs[i] = 256 + 8
+        view = B.CacheView(*ptrs, None)
+        rc = lib.entmaxkv_decode(ctypes.byref(cfg), ctypes.byref(view), ctypes.c_void_p(256), None, 1,
+                                 1.5, B.POLICY_GAUSSIAN, 0, 0.5, 0, ctypes.c_void_p(256), 1 << 40,
+                                 ctypes.c_void_p(256), None, 0, None, None, None, None)
+        assert rc == 1, i
