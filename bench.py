@@ -33,9 +33,10 @@ WORKLOAD = "gqa32x8-d128-1m-p32-bf16"
 ALPHA, MARGIN, TOPK_BUDGET = 1.5, 0.5, 2048
 NOMINAL_HBM_GBS = 8000.0
 L2_FLUSH_BYTES = 512 << 20   # > 129 MB L2: read between timed steps
-# DRAM bytes per launch of the dominant kernel from an ncu capture of the
-# same kernel, scaled to a full launch; None until the kernel is captured.
-NCU_TRAFFIC_PER_LAUNCH = None
+# DRAM bytes (read + write) of one launch of the dominant kernel on this
+# workload, from an ncu capture of the bench command itself (no scaling);
+# reset to None whenever that kernel changes.
+NCU_TRAFFIC_PER_LAUNCH = 268887808 + 7936768
 
 
 def measured_peaks():
