@@ -179,17 +179,19 @@ __device__ double solve_tau_warp(const SolveSrc& S, double tau0, float beta, boo
 // ---------------------------------------------------------------------------
 
 template <typename T, int D>
-__global__ void __launch_bounds__(kThreads) pass_a_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(kThreads, 2) pass_a_kernel(DecodeArgs a) {
   __shared__ int list[kListCap];
   __shared__ int phys_sh[kListCap];
   __shared__ int sh_scan[32];
   __shared__ float qs[8][D];
   __shared__ float wmax[kWarps][8];
-  __shared__ float wkept[kWarps][8];
+  __shared__ float kept_sh[8];
   __shared__ float thr_sh[8];
-  __shared__ float th_sh[8];
   __shared__ int last_sh;
-  __shared__ __align__(16) float pool[kSolveCap];  // last block: page and score candidates
+  // Page maxima of the block's pages [rank][G] during the page loop; in the
+  // last block, the τ solver's page and score candidates.
+  __shared__ __align__(16) float pool[kSolveCap];
+  static_assert(kListCap * 8 <= kSolveCap, "page maxima of a block fit the pool");
   __shared__ float T0_sh[8], tlb_sh[8];
   __shared__ int nc_sh[8], np_sh[8], nz_sh[8], off_sh[9];
   const int split = blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
@@ -198,10 +200,14 @@ __global__ void __launch_bounds__(kThreads) pass_a_kernel(DecodeArgs a) {
   const int seq = seq_row(a.seq_ids, s, a.max_seqs, tid == 0 ? a.status : nullptr);
   const int L = seq_len_clamped(a.seq_lens, seq, a.maxp, P, tid == 0 ? a.status : nullptr);
   const int n_pages = (L + P - 1) / P;
+  if (tid < 8) kept_sh[tid] = 0.0f;  // published by the barriers of the page range
   int n_sel, lo, hi;
   block_page_range(a, s, kvh, n_pages, split, list, sh_scan, n_sel, lo, hi);
   const bool bitmap = uses_bitmap(a.policy);
   const size_t skv = (size_t)s * a.Hkv + kvh;
+  const size_t hq0 = (size_t)s * a.Hq + (size_t)kvh * G;  // first query head of the group
+  const bool beta2 = a.beta == 2.0f;
+  const bool gauss = a.policy == ENTMAXKV_POLICY_GAUSSIAN;
   if (split == 0 && tid == 0) {
     a.nsel_ws[skv] = n_sel;
     if (a.n_sel_out) a.n_sel_out[skv] = n_sel;
@@ -220,13 +226,32 @@ __global__ void __launch_bounds__(kThreads) pass_a_kernel(DecodeArgs a) {
     if (bitmap) a.sel_list[skv * a.cap_pages + lo + i] = page;
     if (a.page_ids) a.page_ids[skv * a.page_ids_stride + lo + i] = page;
     if (staged) {
+      // Gaussian model statistics of this kept page for each head of the
+      // group, loaded alongside the page lookup (summary §2B.2: 1 − kept
+      // mass estimates the dropped mass δ)
+      float2 v[8];
+      float th[8];
+#pragma unroll
+      for (int h = 0; h < 8; ++h) {
+        v[h] = (gauss && h < G) ? a.gauss_ms[(hq0 + h) * a.maxp + page] : make_float2(0.0f, 0.0f);
+        th[h] = (gauss && h < G) ? a.tauhat[hq0 + h] : 0.0f;
+      }
       const int ph = phys_page(a.block_table, seq, page, a.maxp, a.nphys, a.status);
       phys_sh[i] = ph;
       if (ph >= 0 && i < kAhead * kWarps) prefetch_l2_bulk(k_slab(ph), slab_bytes);
+      if (gauss && ph >= 0) {
+        const float nv = (float)min(P, L - page * P);
+#pragma unroll
+        for (int h = 0; h < 8; ++h) {
+          if (h < G) {
+            float g, dg;
+            gauss_moment(v[h].x - th[h], v[h].y, beta2, g, dg);
+            atomicAdd(&kept_sh[h], nv * g);
+          }
+        }
+      }
     }
   }
-  const size_t hq0 = (size_t)s * a.Hq + (size_t)kvh * G;  // first query head of the group
-  if (tid < 8) th_sh[tid] = (a.policy == ENTMAXKV_POLICY_GAUSSIAN && tid < G) ? a.tauhat[hq0 + tid] : 0.0f;
   uint32_t bq[D / 16][2];
   if constexpr (sizeof(T) == 2) {
     load_q_bfrag<D>((const __nv_bfloat16*)a.q + hq0 * D, G, lane, bq);
@@ -235,10 +260,9 @@ __global__ void __launch_bounds__(kThreads) pass_a_kernel(DecodeArgs a) {
   }
   __syncthreads();
 
-  float wm[8], kept = 0.0f;
+  float wm[8];
 #pragma unroll
   for (int h = 0; h < 8; ++h) wm[h] = -CUDART_INF_F;
-  const bool beta2 = a.beta == 2.0f;
   for (int i = warp; i < hi - lo; i += kWarps) {
     const int rank = lo + i;
     const int page = bitmap ? list[i] : rank;
@@ -253,7 +277,10 @@ __global__ void __launch_bounds__(kThreads) pass_a_kernel(DecodeArgs a) {
     if (lane == 0) a.sel_pp[skv * a.cap_pages + rank] = make_int2(page, ph);
     if (ph < 0) {  // unreadable page: no scores
       for (int e = lane; e < P * G; e += 32) zb[e] = -CUDART_INF_F;
-      if (lane < G) pm[lane] = -CUDART_INF_F;
+      if (lane < G) {
+        pm[lane] = -CUDART_INF_F;
+        if (staged) pool[i * G + lane] = -CUDART_INF_F;
+      }
       continue;
     }
     const size_t slab_off = ((size_t)ph * a.Hkv + kvh) * P * D;
@@ -290,6 +317,10 @@ __global__ void __launch_bounds__(kThreads) pass_a_kernel(DecodeArgs a) {
       if (r == 0) {
         if (h0 < G) pm[h0] = pm0;
         if (h1 < G) pm[h1] = pm1;
+        if (staged) {
+          if (h0 < G) pool[i * G + h0] = pm0;
+          if (h1 < G) pool[i * G + h1] = pm1;
+        }
       }
       // lane c keeps the running max of heads 2c, 2c+1 in wm[0], wm[1]
       wm[0] = fmaxf(wm[0], pm0);
@@ -302,16 +333,13 @@ __global__ void __launch_bounds__(kThreads) pass_a_kernel(DecodeArgs a) {
         if (h < G) {
           if (lane < P) zb[lane * G + h] = zt[h];
           const float m = warp_max(zt[h]);
-          if (lane == 0) pm[h] = m;
+          if (lane == 0) {
+            pm[h] = m;
+            if (staged) pool[i * G + h] = m;
+          }
           wm[h] = fmaxf(wm[h], m);
         }
       }
-    }
-    if (a.policy == ENTMAXKV_POLICY_GAUSSIAN && lane < G) {
-      const float2 v = a.gauss_ms[(hq0 + lane) * a.maxp + page];
-      float g, dg;
-      gauss_moment(v.x - th_sh[lane], v.y, beta2, g, dg);
-      kept += (float)nv * g;  // lane h accumulates head h
     }
   }
   // block max z per head → global max; candidate threshold per head
@@ -324,21 +352,18 @@ __global__ void __launch_bounds__(kThreads) pass_a_kernel(DecodeArgs a) {
     if (lane == 0)
       for (int h = 0; h < 8; ++h) wmax[warp][h] = wm[h];
   }
-  if (lane < 8) wkept[warp][lane] = lane < G ? kept : 0.0f;
   __syncthreads();
   if (tid < G) {
-    float m = -CUDART_INF_F, ks = 0.0f;
-    for (int w = 0; w < kWarps; ++w) {
-      m = fmaxf(m, wmax[w][tid]);
-      ks += wkept[w][tid];
-    }
+    float m = -CUDART_INF_F;
+    const float ks = kept_sh[tid];
+    for (int w = 0; w < kWarps; ++w) m = fmaxf(m, wmax[w][tid]);
     float gm = m;
     if (m > -CUDART_INF_F) {
       const uint32_t old = atomicMax(&a.zmax[hq0 + tid], ord_enc(m));
       gm = fmaxf(m, ord_dec(old));
     }
     thr_sh[tid] = gm - 1.0f;
-    if (a.policy == ENTMAXKV_POLICY_GAUSSIAN && ks != 0.0f) atomicAdd(&a.kept_mass[hq0 + tid], ks);
+    if (gauss && ks != 0.0f) atomicAdd(&a.kept_mass[hq0 + tid], ks);
   }
   __syncthreads();
   // candidate pages: those whose max clears (best known max − 1). Lane l
@@ -349,16 +374,23 @@ __global__ void __launch_bounds__(kThreads) pass_a_kernel(DecodeArgs a) {
     const int i = i0 + lane;
     const bool in = i < hi - lo;
     const int rank = lo + i;
-    const float* pm = a.pmax + (skv * a.cap_pages + (in ? rank : lo)) * (size_t)G;
+    const float* pm = staged ? pool + (in ? i : 0) * G : a.pmax + (skv * a.cap_pages + (in ? rank : lo)) * (size_t)G;
     float pmv[8];
 #pragma unroll
     for (int hg = 0; hg < 8; ++hg) pmv[hg] = (in && hg < G) ? pm[hg] : -CUDART_INF_F;
     uint32_t mine = 0u, bits[8];
+    bool cand = false;
 #pragma unroll
     for (int hg = 0; hg < 8; ++hg) {
-      bits[hg] = __ballot_sync(0xffffffffu, hg < G && pmv[hg] > thr_sh[hg]);
+      const bool c = hg < G && pmv[hg] > thr_sh[hg];
+      cand = cand || c;
+      bits[hg] = __ballot_sync(0xffffffffu, c);
       if (lane == hg) mine = bits[hg];
     }
+    // Only candidate pages can need V (τ ≥ z_max − 1): request their V slabs
+    // into L2 now, so that pass B finds them there.
+    if (cand && staged && phys_sh[i] >= 0)
+      prefetch_l2_bulk((const char*)a.v_pool + ((size_t)phys_sh[i] * a.Hkv + kvh) * slab_bytes, slab_bytes);
     int base = 0;
     if (mine) base = atomicAdd(&a.cand_cnt[hq0 + lane], __popc(mine));
 #pragma unroll
@@ -538,8 +570,8 @@ struct VTraits<__nv_bfloat16> {
 
 // Sum of the split partials of one (sequence, KV head) in split order, by the
 // last block: float4 columns, the block's threads split over the partials.
-__device__ __noinline__ void combine_partials(const DecodeArgs& a, size_t skv, float* out_rows,
-                                              float4* red4) {
+__device__ __noinline__ void combine_partials(const DecodeArgs& a, size_t skv, int parts,
+                                              float* out_rows, float4* red4) {
   const int G = a.G, D = a.D, tid = threadIdx.x;
   const int cols = G * D / 4;
   const int groups = kThreads / cols > 0 ? kThreads / cols : 1;
@@ -547,12 +579,12 @@ __device__ __noinline__ void combine_partials(const DecodeArgs& a, size_t skv, f
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   if (grp < groups) {
     const float* base = a.partial + skv * a.splits * (size_t)a.pstride;
-    for (int sp0 = grp; sp0 < a.splits; sp0 += 8 * groups) {  // 8 loads in flight, summed in order
+    for (int sp0 = grp; sp0 < parts; sp0 += 8 * groups) {  // 8 loads in flight, summed in order
       float4 v[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const int sp = sp0 + u * groups;
-        v[u] = sp < a.splits ? __ldcg(reinterpret_cast<const float4*>(base + (size_t)sp * a.pstride) + col)
+        v[u] = sp < parts ? __ldcg(reinterpret_cast<const float4*>(base + (size_t)sp * a.pstride) + col)
                              : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
@@ -584,15 +616,16 @@ __device__ __noinline__ void combine_partials(const DecodeArgs& a, size_t skv, f
 // all its V loads at once (lane: 16 bytes of a row, tokens tg, tg+TG, ...),
 // and accumulates p·v in fp32 registers.
 template <typename T, int D, int GP>
-__global__ void __launch_bounds__(kThreads) pass_b_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(kThreads, GP <= 4 ? 2 : 1) pass_b_kernel(DecodeArgs a) {
   constexpr int VEC = VTraits<T>::VEC, LPR = D / VEC, TG = 32 / LPR;
-  constexpr int MAXT = 32 / TG;                  // tokens per lane in a 32-token page
-  constexpr int CH = MAXT < 16 ? MAXT : 16;      // V rows in flight per lane
+  constexpr int MAXT = 32 / TG;                  // rows per lane in a 32-token page
   __shared__ double tau_sh[GP];
   __shared__ __align__(16) float zs[kWarps][32 * 8];
   __shared__ __align__(16) float red[kWarps][GP][D];
   __shared__ float dsum[kWarps][GP];
   __shared__ float4 red4[kThreads];
+  __shared__ uint64_t vbar[kWarps];
+  extern __shared__ __align__(128) unsigned char vstage[];  // [kWarps][P][D] of T
   static_assert(sizeof(red4) >= kListCap * sizeof(int), "the V page list shares the combine scratch");
   int* list_sh = reinterpret_cast<int*>(red4);  // the page list is done before the combine starts
   __shared__ int scan_sh[32];
@@ -627,61 +660,71 @@ __global__ void __launch_bounds__(kThreads) pass_b_kernel(DecodeArgs a) {
     for (int j = 0; j < VEC; ++j) acc[h][j] = 0.0f;
   float* zw = zs[warp];
 
-  // One page: its z staged in shared memory, all its V loads issued at once
-  // (lane: 16 bytes of a row, tokens tg, tg+TG, ...), p·v accumulated in fp32.
+  // One page: its V slab (P rows × D) arrives in this warp's shared buffer
+  // by one bulk copy completing on the warp's mbarrier, its z is staged next
+  // to it, and a compact row loop accumulates p·v in fp32 (lane: VEC columns
+  // of rows tg, tg+TG, ...). The loop is kept small on purpose: it runs once
+  // per page, usually with cold instruction caches.
+  T* vbuf = reinterpret_cast<T*>(vstage) + (size_t)warp * P * D;
+  if (lane == 0) {
+    mbar_init(&vbar[warp], 1);
+    mbar_fence_init();
+  }
+  __syncwarp();
+  uint32_t vphase = 0u;
+  bool stuck = false;  // a copy did not arrive within the bound (warp-uniform)
   auto do_page = [&](int rank, int pg, int ph) {
+    if (stuck) return;
     const int nv = min(P, L - pg * P);
+    const uint32_t bytes = (uint32_t)(P * D * sizeof(T));
+    if (lane == 0) {
+      mbar_expect_tx(&vbar[warp], bytes);
+      bulk_g2s(vbuf, (const T*)a.v_pool + ((size_t)ph * a.Hkv + kvh) * P * D, bytes, &vbar[warp]);
+    }
     const float* zb = a.z + (skv * a.cap_pages + rank) * (size_t)P * G;
-    const T* vs = (const T*)a.v_pool + ((size_t)ph * a.Hkv + kvh) * P * D + dc * VEC;
-    float4 zl[2];
 #pragma unroll
     for (int u = 0; u < 2; ++u) {  // P·G ≤ 256 floats: two float4 per lane at most
       const int e = 4 * lane + 128 * u;
-      zl[u] = e < P * G ? __ldcg(reinterpret_cast<const float4*>(zb + e)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      if (e < P * G) *reinterpret_cast<float4*>(zw + e) = __ldcg(reinterpret_cast<const float4*>(zb + e));
     }
-    for (int c1 = 0; c1 < MAXT; c1 += CH) {
-      uint4 raw[CH];
+    const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&vbar[warp], vphase));
+    if (!ok) {
+      stuck = true;
+      return;
+    }
+    vphase ^= 1u;
+    const T* vrow = vbuf + dc * VEC;
+#pragma unroll 2
+    for (int u = 0; u < MAXT; ++u) {
+      const int t = tg + TG * u;
+      if (t < nv) {
+        float v[VEC];
+        VTraits<T>::unpack(*reinterpret_cast<const uint4*>(vrow + (size_t)t * D), v);
 #pragma unroll
-      for (int u = 0; u < CH; ++u) {
-        const int t = tg + TG * (c1 + u);
-        raw[u] = t < nv ? ld_stream(vs + (size_t)t * D) : make_uint4(0u, 0u, 0u, 0u);
-      }
-      if (c1 == 0) {
+        for (int h = 0; h < GP; ++h) {
+          if (h < G) {
+            const float zv = zw[t * G + h];
+            const float p = sizeof(T) == 4 ? pos_pow((float)((double)zv - taud[h]), a.beta)
+                                           : pos_pow(zv - tau[h], a.beta);
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int e = 4 * lane + 128 * u;
-          if (e < P * G) *reinterpret_cast<float4*>(zw + e) = zl[u];
-        }
-        __syncwarp();
-      }
-#pragma unroll
-      for (int u = 0; u < CH; ++u) {
-        const int t = tg + TG * (c1 + u);
-        if (t < nv) {
-          float v[VEC];
-          VTraits<T>::unpack(raw[u], v);
-#pragma unroll
-          for (int h = 0; h < GP; ++h) {
-            if (h < G) {
-              const float zv = zw[t * G + h];
-              const float p = sizeof(T) == 4 ? pos_pow((float)((double)zv - taud[h]), a.beta)
-                                             : pos_pow(zv - tau[h], a.beta);
-#pragma unroll
-              for (int j = 0; j < VEC; ++j) acc[h][j] = fmaf(p, v[j], acc[h][j]);
-            }
+            for (int j = 0; j < VEC; ++j) acc[h][j] = fmaf(p, v[j], acc[h][j]);
           }
         }
       }
     }
-    __syncwarp();
+    __syncwarp();  // the buffer and zw are refilled for the next page
   };
 
-  // Pages that need V: some head's page max above its τ. Unless every page
-  // needs V, every block lists those ranks in rank order (a thread checks up
-  // to 32 consecutive ranks, one scan places them) and takes an even share of
-  // the list, a warp per page: pages that cluster in rank still spread over
-  // the whole grid. Larger selections fall back to the block's own rank range.
-  bool listed = false;
+  // Pages that need V: some head's page max above its τ (every page with
+  // ENTMAXKV_FLAG_DENSE_V). Unless every page needs V, each block lists those
+  // ranks of the whole selection in rank order (a thread checks up to 32
+  // consecutive ranks, one scan places them); the first `parts` blocks take
+  // even shares of the list, a warp per page, so pages that cluster in rank
+  // still spread over the grid, and only those blocks write partials. Larger
+  // selections are walked in the block's own rank range, kListCap ranks at a
+  // time. Either way the block's pages sit in list_sh in rank order.
+  int parts = a.splits;
+  bool global_list = false;
   int n_list = 0;
   if (!dense && n_sel <= 32 * kThreads) {
     const int per = (n_sel + kThreads - 1) / kThreads;
@@ -700,10 +743,15 @@ __global__ void __launch_bounds__(kThreads) pass_b_kernel(DecodeArgs a) {
     }
     int nv_all;
     int j = block_exclusive_scan(__popc(mask), scan_sh, nv_all);
-    const int s_lo = (int)(((long long)nv_all * split) / a.splits);
-    const int s_hi = (int)(((long long)nv_all * (split + 1)) / a.splits);
-    if (s_hi - s_lo <= kListCap) {
-      listed = true;
+    // top-k keeps every block: each one also sums its share of the δ̄ bound
+    const int pb = a.policy == ENTMAXKV_POLICY_TOPK
+                       ? a.splits
+                       : max(1, min(a.splits, (nv_all + kWarps - 1) / kWarps));
+    if ((nv_all + pb - 1) / pb <= kListCap) {
+      global_list = true;
+      parts = pb;
+      const int s_lo = split < pb ? (int)(((long long)nv_all * split) / pb) : 0;
+      const int s_hi = split < pb ? (int)(((long long)nv_all * (split + 1)) / pb) : 0;
       n_list = s_hi - s_lo;
       while (mask && j < s_hi) {
         const int k = __ffs(mask) - 1;
@@ -714,37 +762,46 @@ __global__ void __launch_bounds__(kThreads) pass_b_kernel(DecodeArgs a) {
     }
     __syncthreads();
   }
-  if (listed) {
-    for (int j = warp; j < n_list; j += kWarps) {
-      const int rank = list_sh[j];
+  if (split >= parts) return;  // no pages and no partial (block-uniform)
+  const int nb = hi - lo;
+  for (int c0 = 0; c0 < (global_list ? 1 : nb); c0 += kListCap) {
+    if (!global_list) {  // this chunk of the block's range: 4 ranks a thread
+      const int cn = min(kListCap, nb - c0);
+      uint32_t mask = 0u;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int i = 4 * tid + k;
+        if (i < cn) {
+          bool need = dense;
+          const float* pm = a.pmax + (skv * a.cap_pages + lo + c0 + i) * (size_t)G;
+#pragma unroll
+          for (int h = 0; h < GP; ++h)
+            if (h < G) need = need || (__ldcg(pm + h) > tau[h]);
+          if (need) mask |= 1u << k;
+        }
+      }
+      int j = block_exclusive_scan(__popc(mask), scan_sh, n_list);
+      while (mask) {
+        const int k = __ffs(mask) - 1;
+        mask &= mask - 1u;
+        list_sh[j++] = lo + c0 + 4 * tid + k;
+      }
+      __syncthreads();
+    }
+    for (int jj = warp; jj < n_list; jj += kWarps) {
+      const int rank = list_sh[jj];
       const int2 pp = __ldcg(&a.sel_pp[skv * a.cap_pages + rank]);
       if (pp.y >= 0) do_page(rank, pp.x, pp.y);
     }
-  } else {
-    // The warp takes 32 consecutive ranks of the block's range at a time:
-    // lane l checks rank l's page maxima, and the pages that need V are
-    // processed in turn.
-    const int nb = hi - lo;
-    for (int c0 = warp * 32; c0 < nb; c0 += kThreads) {
-      const int i = c0 + lane;
-      bool need = false;
-      int2 pp = make_int2(0, -1);
-      if (i < nb) {
-        const int rank = lo + i;
-        need = dense;
-        const float* pm = a.pmax + (skv * a.cap_pages + rank) * (size_t)G;
-#pragma unroll
-        for (int h = 0; h < GP; ++h)
-          if (h < G) need = need || (__ldcg(pm + h) > tau[h]);
-        if (need) pp = __ldcg(&a.sel_pp[skv * a.cap_pages + rank]);
-      }
-      uint32_t bits = __ballot_sync(0xffffffffu, pp.y >= 0);
-      while (bits) {
-        const int b = __ffs(bits) - 1;
-        bits &= bits - 1u;
-        do_page(lo + c0 + b, __shfl_sync(0xffffffffu, pp.x, b), __shfl_sync(0xffffffffu, pp.y, b));
-      }
+    __syncthreads();  // list_sh is rewritten by the next chunk
+  }
+  if (stuck) {
+    // flag it; the copy still in flight is waited for (bounded) before leaving
+    if (lane == 0) {
+      raise_flag(a.status, ENTMAXKV_DEV_TIMEOUT);
+      mbar_wait_bounded(&vbar[warp], vphase);
     }
+    __syncwarp();
   }
 #pragma unroll
   for (int o = LPR; o < 32; o <<= 1)
@@ -795,11 +852,11 @@ __global__ void __launch_bounds__(kThreads) pass_b_kernel(DecodeArgs a) {
   }
   __threadfence();
   __syncthreads();
-  if (tid == 0) last_sh = atomicAdd(&a.cnt_b[skv], 1) == a.splits - 1;
+  if (tid == 0) last_sh = atomicAdd(&a.cnt_b[skv], 1) == parts - 1;
   __syncthreads();
   if (!last_sh) return;
   __threadfence();
-  combine_partials(a, skv, a.out + hq0 * D, red4);
+  combine_partials(a, skv, parts, a.out + hq0 * D, red4);
   if (a.policy == ENTMAXKV_POLICY_TOPK && a.delta_out && tid < G)
     a.delta_out[hq0 + tid] = L > 0 ? fminf(1.0f, __ldcg(&a.dbar[hq0 + tid])) : 0.0f;
 }
@@ -820,26 +877,31 @@ cudaError_t launch_pass_a(const DecodeArgs& a, int kv_dtype, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+template <typename T, int D, int GP>
+static cudaError_t pass_b_launch(const DecodeArgs& a, dim3 grid, cudaStream_t st) {
+  const int smem = kWarps * a.P * D * (int)sizeof(T);  // one V slab per warp
+  const cudaError_t e = cudaFuncSetAttribute(pass_b_kernel<T, D, GP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             kWarps * 32 * D * (int)sizeof(T));
+  if (e != cudaSuccess) return e;
+  pass_b_kernel<T, D, GP><<<grid, kThreads, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
 template <typename T, int D>
-static void pass_b_g(const DecodeArgs& a, dim3 grid, cudaStream_t st) {
+static cudaError_t pass_b_g(const DecodeArgs& a, dim3 grid, cudaStream_t st) {
   switch (pick_gp(a.G)) {
-    case 1: pass_b_kernel<T, D, 1><<<grid, kThreads, 0, st>>>(a); break;
-    case 2: pass_b_kernel<T, D, 2><<<grid, kThreads, 0, st>>>(a); break;
-    case 4: pass_b_kernel<T, D, 4><<<grid, kThreads, 0, st>>>(a); break;
-    default: pass_b_kernel<T, D, 8><<<grid, kThreads, 0, st>>>(a); break;
+    case 1: return pass_b_launch<T, D, 1>(a, grid, st);
+    case 2: return pass_b_launch<T, D, 2>(a, grid, st);
+    case 4: return pass_b_launch<T, D, 4>(a, grid, st);
+    default: return pass_b_launch<T, D, 8>(a, grid, st);
   }
 }
 
 cudaError_t launch_pass_b(const DecodeArgs& a, int kv_dtype, cudaStream_t st) {
   dim3 grid(a.splits, a.Hkv, a.S);
-  if (kv_dtype == ENTMAXKV_BF16) {
-    if (a.D == 128) pass_b_g<__nv_bfloat16, 128>(a, grid, st);
-    else pass_b_g<__nv_bfloat16, 64>(a, grid, st);
-  } else {
-    if (a.D == 128) pass_b_g<float, 128>(a, grid, st);
-    else pass_b_g<float, 64>(a, grid, st);
-  }
-  return cudaGetLastError();
+  if (kv_dtype == ENTMAXKV_BF16)
+    return a.D == 128 ? pass_b_g<__nv_bfloat16, 128>(a, grid, st) : pass_b_g<__nv_bfloat16, 64>(a, grid, st);
+  return a.D == 128 ? pass_b_g<float, 128>(a, grid, st) : pass_b_g<float, 64>(a, grid, st);
 }
 
 }  // namespace ekv
