@@ -18,19 +18,14 @@ struct alignas(N * sizeof(T)) Vec {
   T v[N];
 };
 
-// One warp per (sequence, KV head, touched page); lane j covers elements
-// [j·D/32, (j+1)·D/32) of every row.
+// Touched page i of (slot b, KV head kvh) by one warp: lane j covers
+// elements [j·D/32, (j+1)·D/32) of every row. L is the sequence's length
+// before this append.
 template <typename T, int D>
-__global__ void __launch_bounds__(128) append_kernel(AppendArgs a) {
+__device__ __forceinline__ void append_page(const AppendArgs& a, int b, int seq, int L, int kvh, int i,
+                                            int lane) {
   constexpr int EPL = D / 32;
   using V = Vec<T, EPL>;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int b = blockIdx.z, kvh = blockIdx.y;
-  const int i = blockIdx.x * 4 + warp;
-  const int seq = seq_row(a.seq_ids, b, a.max_seqs, lane == 0 ? a.status : nullptr);
-  if (seq < 0) return;
-  int L = a.seq_lens[seq];
-  if (L < 0) L = 0;
   const int P = a.P, T_new = a.n_tokens;
   const int first = L / P, last = (L + T_new - 1) / P;
   const int lp = first + i;
@@ -115,6 +110,32 @@ __global__ void __launch_bounds__(128) append_kernel(AppendArgs a) {
   *kmaxp = vmax;
 }
 
+// Bulk appends: a warp per (slot, KV head, touched page); the lengths are
+// advanced by a second kernel once every page is written.
+template <typename T, int D>
+__global__ void __launch_bounds__(128) append_kernel(AppendArgs a) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = blockIdx.z, kvh = blockIdx.y;
+  const int seq = seq_row(a.seq_ids, b, a.max_seqs, lane == 0 ? a.status : nullptr);
+  if (seq < 0) return;
+  append_page<T, D>(a, b, seq, max(a.seq_lens[seq], 0), kvh, blockIdx.x * 4 + warp, lane);
+}
+
+// Small appends (a decode step's token): one block per slot writes every
+// touched page of every KV head, then advances the slot's length itself.
+template <typename T, int D>
+__global__ void __launch_bounds__(512) append_step_kernel(AppendArgs a, int pages) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  const int b = blockIdx.x;
+  const int seq = seq_row(a.seq_ids, b, a.max_seqs, threadIdx.x == 0 ? a.status : nullptr);
+  if (seq < 0) return;  // block-uniform
+  const int L = max(a.seq_lens[seq], 0);
+  for (int item = warp; item < a.Hkv * pages; item += nw)
+    append_page<T, D>(a, b, seq, L, item / pages, item % pages, lane);
+  __syncthreads();  // every read of the old length is done
+  if (threadIdx.x == 0) a.seq_lens[seq] += a.n_tokens;
+}
+
 __global__ void advance_lens_kernel(AppendArgs a) {
   int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= a.n_seqs) return;
@@ -126,10 +147,14 @@ __global__ void advance_lens_kernel(AppendArgs a) {
 template <typename T, int D>
 static cudaError_t launch_append_t(const AppendArgs& a, cudaStream_t st) {
   const int pages = (a.n_tokens + a.P - 1) / a.P + 1;  // pages one append can touch
+  if ((long long)a.Hkv * pages <= 64) {
+    const int warps = a.Hkv * pages < 16 ? a.Hkv * pages : 16;
+    return launch_k(append_step_kernel<T, D>, dim3(a.n_seqs), dim3(32 * warps), 0, st, a, pages);
+  }
   dim3 grid((pages + 3) / 4, a.Hkv, a.n_seqs);
-  append_kernel<T, D><<<grid, 128, 0, st>>>(a);
-  advance_lens_kernel<<<(a.n_seqs + 127) / 128, 128, 0, st>>>(a);
-  return cudaGetLastError();
+  cudaError_t e = launch_k(append_kernel<T, D>, grid, dim3(128), 0, st, a);
+  if (e == cudaSuccess) e = launch_k(advance_lens_kernel, dim3((a.n_seqs + 127) / 128), dim3(128), 0, st, a);
+  return e;
 }
 
 cudaError_t launch_append(const AppendArgs& a, int kv_dtype, cudaStream_t st) {

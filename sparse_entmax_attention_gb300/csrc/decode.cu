@@ -112,7 +112,7 @@ __device__ __forceinline__ void for_each_cand(const SolveSrc& S, F&& f) {
 // Float accumulation per candidate (GB300 runs FP64 at a small fraction of
 // the FP32 rate): τ is carried as a double and split into hi + lo floats so
 // that y = z − τ keeps its accuracy; only the per-iteration totals are double.
-__device__ double solve_tau_warp(const SolveSrc& S, double tau0, float beta, bool& ok) {
+__device__ __noinline__ double solve_tau_warp(const SolveSrc& S, double tau0, float beta, bool& ok) {
   double tau = tau0;
   ok = false;
   const bool b2 = beta == 2.0f, b1 = beta == 1.0f;
@@ -221,35 +221,32 @@ __global__ void __launch_bounds__(kThreads, 2) pass_a_kernel(DecodeArgs a) {
   auto k_slab = [&](int ph) {
     return (const char*)a.k_pool + ((size_t)ph * a.Hkv + kvh) * slab_bytes;
   };
-  for (int i = tid; i < hi - lo; i += kThreads) {
+  // One item per (page, head of the group) for the Gaussian policy (its
+  // kept model mass), one per page otherwise; the head-0 item of a page also
+  // records and looks up the page. Loads of both kinds are in flight together.
+  const int GI = gauss ? G : 1;
+  for (int e = tid; e < (hi - lo) * GI; e += kThreads) {
+    const int i = e / GI, h = e - i * GI;
     const int page = bitmap ? list[i] : lo + i;
-    if (bitmap) a.sel_list[skv * a.cap_pages + lo + i] = page;
-    if (a.page_ids) a.page_ids[skv * a.page_ids_stride + lo + i] = page;
-    if (staged) {
-      // Gaussian model statistics of this kept page for each head of the
-      // group, loaded alongside the page lookup (summary §2B.2: 1 − kept
-      // mass estimates the dropped mass δ)
-      float2 v[8];
-      float th[8];
-#pragma unroll
-      for (int h = 0; h < 8; ++h) {
-        v[h] = (gauss && h < G) ? a.gauss_ms[(hq0 + h) * a.maxp + page] : make_float2(0.0f, 0.0f);
-        th[h] = (gauss && h < G) ? a.tauhat[hq0 + h] : 0.0f;
+    float2 v = make_float2(0.0f, 0.0f);
+    float th = 0.0f;
+    if (gauss) {  // summary §2B.2: 1 − kept model mass estimates the dropped mass δ
+      v = a.gauss_ms[(hq0 + h) * a.maxp + page];
+      th = a.tauhat[hq0 + h];
+    }
+    if (h == 0) {
+      if (bitmap) a.sel_list[skv * a.cap_pages + lo + i] = page;
+      if (a.page_ids) a.page_ids[skv * a.page_ids_stride + lo + i] = page;
+      if (staged) {
+        const int ph = phys_page(a.block_table, seq, page, a.maxp, a.nphys, a.status);
+        phys_sh[i] = ph;
+        if (ph >= 0 && i < kAhead * kWarps) prefetch_l2_bulk(k_slab(ph), slab_bytes);
       }
-      const int ph = phys_page(a.block_table, seq, page, a.maxp, a.nphys, a.status);
-      phys_sh[i] = ph;
-      if (ph >= 0 && i < kAhead * kWarps) prefetch_l2_bulk(k_slab(ph), slab_bytes);
-      if (gauss && ph >= 0) {
-        const float nv = (float)min(P, L - page * P);
-#pragma unroll
-        for (int h = 0; h < 8; ++h) {
-          if (h < G) {
-            float g, dg;
-            gauss_moment(v[h].x - th[h], v[h].y, beta2, g, dg);
-            atomicAdd(&kept_sh[h], nv * g);
-          }
-        }
-      }
+    }
+    if (gauss) {
+      float g, dg;
+      gauss_moment(v.x - th, v.y, beta2, g, dg);
+      atomicAdd(&kept_sh[h], (float)min(P, L - page * P) * g);
     }
   }
   uint32_t bq[D / 16][2];
@@ -868,11 +865,11 @@ static int pick_gp(int G) { return G <= 1 ? 1 : (G <= 2 ? 2 : (G <= 4 ? 4 : 8));
 cudaError_t launch_pass_a(const DecodeArgs& a, int kv_dtype, cudaStream_t st) {
   dim3 grid(a.splits, a.Hkv, a.S);
   if (kv_dtype == ENTMAXKV_BF16) {
-    if (a.D == 128) pass_a_kernel<__nv_bfloat16, 128><<<grid, kThreads, 0, st>>>(a);
-    else pass_a_kernel<__nv_bfloat16, 64><<<grid, kThreads, 0, st>>>(a);
+    if (a.D == 128) launch_k(pass_a_kernel<__nv_bfloat16, 128>, dim3(grid), dim3(kThreads), 0, st, a);
+    else launch_k(pass_a_kernel<__nv_bfloat16, 64>, dim3(grid), dim3(kThreads), 0, st, a);
   } else {
-    if (a.D == 128) pass_a_kernel<float, 128><<<grid, kThreads, 0, st>>>(a);
-    else pass_a_kernel<float, 64><<<grid, kThreads, 0, st>>>(a);
+    if (a.D == 128) launch_k(pass_a_kernel<float, 128>, dim3(grid), dim3(kThreads), 0, st, a);
+    else launch_k(pass_a_kernel<float, 64>, dim3(grid), dim3(kThreads), 0, st, a);
   }
   return cudaGetLastError();
 }
@@ -883,7 +880,7 @@ static cudaError_t pass_b_launch(const DecodeArgs& a, dim3 grid, cudaStream_t st
   const cudaError_t e = cudaFuncSetAttribute(pass_b_kernel<T, D, GP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              kWarps * 32 * D * (int)sizeof(T));
   if (e != cudaSuccess) return e;
-  pass_b_kernel<T, D, GP><<<grid, kThreads, smem, st>>>(a);
+  launch_k(pass_b_kernel<T, D, GP>, dim3(grid), dim3(kThreads), smem, st, a);
   return cudaGetLastError();
 }
 

@@ -404,12 +404,12 @@ cudaError_t launch_bbox(const DecodeArgs& a, int kv_dtype, int sms, cudaStream_t
   const int other = a.Hkv * a.S;
   if (kv_dtype == ENTMAXKV_BF16) {
     dim3 grid(grid_x_for((a.maxp + 15) / 16, kWarps, sms, other), a.Hkv, a.S);
-    if (a.D == 128) bbox_bf16_kernel<128><<<grid, kThreads, 0, st>>>(a);
-    else bbox_bf16_kernel<64><<<grid, kThreads, 0, st>>>(a);
+    if (a.D == 128) launch_k(bbox_bf16_kernel<128>, dim3(grid), dim3(kThreads), 0, st, a);
+    else launch_k(bbox_bf16_kernel<64>, dim3(grid), dim3(kThreads), 0, st, a);
   } else {
     dim3 grid(grid_x_for(a.maxp, kThreads, sms, other), a.Hkv, a.S);
-    if (a.D == 128) bbox_f32_kernel<128><<<grid, kThreads, 0, st>>>(a);
-    else bbox_f32_kernel<64><<<grid, kThreads, 0, st>>>(a);
+    if (a.D == 128) launch_k(bbox_f32_kernel<128>, dim3(grid), dim3(kThreads), 0, st, a);
+    else launch_k(bbox_f32_kernel<64>, dim3(grid), dim3(kThreads), 0, st, a);
   }
   return cudaGetLastError();
 }
@@ -420,8 +420,7 @@ static cudaError_t gauss_launch(const DecodeArgs& a, dim3 grid, cudaStream_t st)
   static_assert(gauss_smem_bytes<D>() <= 227 * 1024, "stages exceed shared memory");
   cudaError_t e = cudaFuncSetAttribute(gauss_kernel<TQ, D, GP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  gauss_kernel<TQ, D, GP><<<grid, kGaussWarps * 32, smem, st>>>(a);
-  return cudaSuccess;
+  return launch_k(gauss_kernel<TQ, D, GP>, dim3(grid), dim3(kGaussWarps * 32), smem, st, a);
 }
 
 template <typename TQ, int D>

@@ -344,13 +344,13 @@ __global__ void __launch_bounds__(1024) topk_kernel(DecodeArgs a, int mode) {
 
 cudaError_t launch_tauhat(const DecodeArgs& a, cudaStream_t st) {
   dim3 grid(kTauhatCluster, a.Hq, a.S);
-  tauhat_kernel<<<grid, kThreads, 0, st>>>(a);
+  launch_k(tauhat_kernel, dim3(grid), dim3(kThreads), 0, st, a);
   return cudaGetLastError();
 }
 
 cudaError_t launch_topk(const DecodeArgs& a, int mode, cudaStream_t st) {
   dim3 grid(a.Hkv, a.S);
-  topk_kernel<<<grid, 1024, 0, st>>>(a, mode);
+  launch_k(topk_kernel, dim3(grid), dim3(1024), 0, st, a, mode);
   return cudaGetLastError();
 }
 
