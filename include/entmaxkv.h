@@ -72,6 +72,19 @@ typedef enum {
                                        (the dense full-cache entmax baseline); without it a
                                        page whose scores all sit at or below τ is skipped,
                                        which is exact since its weights are 0.            */
+#define ENTMAXKV_FLAG_EXACT_DELTA 0x2u  /* also compute the exact dropped mass
+                                         δ = 1 − Σ_{i kept} p_i^full (summary §3: the
+                                         mass of the full-cache α-entmax outside the
+                                         kept pages) by a full-cache pass over every
+                                         K page; a diagnostic, not for timed steps.
+                                         The workspace must then hold
+                                         entmaxkv_workspace_bytes_flags(...) bytes. */
+
+/* What the delta output of a decode holds (entmaxkv_delta_kind). */
+#define ENTMAXKV_DELTA_ZERO      0  /* FULL, SOFTMAX: nothing is dropped            */
+#define ENTMAXKV_DELTA_CERTIFIED 1  /* TOPK: an upper bound on the dropped mass      */
+#define ENTMAXKV_DELTA_MODEL     2  /* GAUSSIAN: the page model's estimate           */
+#define ENTMAXKV_DELTA_EXACT     3  /* any policy with ENTMAXKV_FLAG_EXACT_DELTA     */
 
 /*
  * Cache geometry. Supported: head_dim ∈ {64, 128}; page_size ∈ {16, 32};
@@ -149,6 +162,28 @@ size_t entmaxkv_workspace_bytes(const entmaxkv_config* cfg, int32_t n_seqs,
                                 int32_t policy, int32_t budget_tokens);
 
 /*
+ * Workspace bytes for a decode with the given flags: entmaxkv_workspace_bytes
+ * for flags without ENTMAXKV_FLAG_EXACT_DELTA; with it, that plus a second
+ * region laid out for the full-cache policy. 0 for an invalid configuration.
+ */
+size_t entmaxkv_workspace_bytes_flags(const entmaxkv_config* cfg, int32_t n_seqs, int32_t policy,
+                                      int32_t budget_tokens, uint32_t flags);
+
+/* The ENTMAXKV_DELTA_* kind of the delta output of a decode with this policy
+ * and these flags; -1 for an unknown policy. */
+int32_t entmaxkv_delta_kind(int32_t policy, uint32_t flags);
+
+/*
+ * Copy the cache's device status word (the ENTMAXKV_DEV_* bits the kernels
+ * have raised) to *status_out after the work queued on `stream` has finished
+ * (this call synchronises the stream). With clear ≠ 0 the word is reset to 0
+ * afterwards. Returns ENTMAXKV_ERR_INVALID_ARG when the cache has no status
+ * word or status_out is NULL, ENTMAXKV_ERR_CUDA when a CUDA call fails.
+ */
+int32_t entmaxkv_read_status(const entmaxkv_cache* cache, uint32_t* status_out, int32_t clear,
+                             void* stream);
+
+/*
  * One decode step for n_seqs sequences (summary §2A-§2C; δ from §3).
  *   q          (device) [n_seqs][Hq][head_dim], kv_dtype (Hq = Hkv·group)
  *   seq_ids    (device) [n_seqs] sequence rows, or NULL for 0..n_seqs−1
@@ -161,7 +196,7 @@ size_t entmaxkv_workspace_bytes(const entmaxkv_config* cfg, int32_t n_seqs,
  *                  FULL/SOFTMAX: ignored
  *   margin     Δ in score units (GAUSSIAN)
  *   flags      ENTMAXKV_FLAG_*
- *   workspace  (device) ≥ entmaxkv_workspace_bytes(...) bytes, 256-byte
+ *   workspace  (device) ≥ entmaxkv_workspace_bytes_flags(...) bytes, 256-byte
  *              aligned; contents need no initialisation and are scratch
  *              afterwards. One workspace must not be shared by decodes that
  *              may run concurrently.
@@ -175,7 +210,9 @@ size_t entmaxkv_workspace_bytes(const entmaxkv_config* cfg, int32_t n_seqs,
  *              an empty kept set
  *   delta      [n_seqs][Hq] float32 dropped mass: FULL/SOFTMAX 0; TOPK the
  *              certified bound min(1, Σ_dropped n_p·[(α−1)U_p − τ]_+^β);
- *              GAUSSIAN the page model's estimate of the dropped mass
+ *              GAUSSIAN the page model's estimate of the dropped mass;
+ *              with ENTMAXKV_FLAG_EXACT_DELTA, for every policy, the exact
+ *              max(0, 1 − Σ_{i in the kept pages} p_i^full)
  * page_ids_stride must be ≥ the most pages the policy can select
  * (TOPK: k; GAUSSIAN: the cap in pages, or max_pages_per_seq; otherwise
  * max_pages_per_seq) when page_ids is not NULL.

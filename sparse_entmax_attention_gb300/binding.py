@@ -22,7 +22,8 @@ F32, BF16 = 0, 1
 POLICY_FULL, POLICY_TOPK, POLICY_GAUSSIAN, POLICY_SOFTMAX = 0, 1, 2, 3
 POLICIES = {"full": POLICY_FULL, "topk": POLICY_TOPK, "gaussian": POLICY_GAUSSIAN,
             "softmax": POLICY_SOFTMAX}
-FLAG_DENSE_V = 0x1
+FLAG_DENSE_V, FLAG_EXACT_DELTA = 0x1, 0x2
+DELTA_ZERO, DELTA_CERTIFIED, DELTA_MODEL, DELTA_EXACT = 0, 1, 2, 3
 DEV_BAD_PAGE_TABLE, DEV_CAPACITY, DEV_TAUHAT_NOCONV = 0x1, 0x2, 0x4
 DEV_CAND_OVERFLOW, DEV_TAU_NOCONV, DEV_BAD_SEQ_ID, DEV_TIMEOUT = 0x8, 0x10, 0x20, 0x40
 
@@ -30,7 +31,8 @@ DEV_CAND_OVERFLOW, DEV_TAU_NOCONV, DEV_BAD_SEQ_ID, DEV_TIMEOUT = 0x8, 0x10, 0x20
 EXPORTS = ("entmaxkv_version", "entmaxkv_status_string", "entmaxkv_append",
            "entmaxkv_workspace_bytes", "entmaxkv_decode", "entmaxkv_decode_profiled",
            "entmaxkv_workspace_layout", "entmaxkv_noalloc_scratch_bytes",
-           "entmaxkv_decode_softmax_noalloc")
+           "entmaxkv_decode_softmax_noalloc", "entmaxkv_workspace_bytes_flags",
+           "entmaxkv_delta_kind", "entmaxkv_read_status")
 STAGE_EVENTS = 6
 STAGES = ("clear", "score", "select", "pass_a", "pass_b")
 
@@ -79,6 +81,12 @@ def lib() -> ctypes.CDLL:
     L.entmaxkv_append.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(CacheView), vp, vp, vp, i32, i32, vp]
     L.entmaxkv_workspace_bytes.restype = sz
     L.entmaxkv_workspace_bytes.argtypes = [ctypes.POINTER(Config), i32, i32, i32]
+    L.entmaxkv_workspace_bytes_flags.restype = sz
+    L.entmaxkv_workspace_bytes_flags.argtypes = [ctypes.POINTER(Config), i32, i32, i32, ctypes.c_uint32]
+    L.entmaxkv_delta_kind.restype = i32
+    L.entmaxkv_delta_kind.argtypes = [i32, ctypes.c_uint32]
+    L.entmaxkv_read_status.restype = i32
+    L.entmaxkv_read_status.argtypes = [ctypes.POINTER(CacheView), ctypes.POINTER(ctypes.c_uint32), i32, vp]
     L.entmaxkv_decode.restype = i32
     L.entmaxkv_decode.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(CacheView), vp, vp, i32,
                                   f32, i32, i32, f32, u32, vp, sz, vp, vp, i32, vp, vp, vp, vp]
@@ -147,6 +155,13 @@ class PagedCache:
     def device_status(self) -> int:
         return int(self.status.item()) & 0xffffffff
 
+    def read_status(self, clear=False, stream=None) -> int:
+        """entmaxkv_read_status: the ENTMAXKV_DEV_* bits after the stream's work."""
+        out = ctypes.c_uint32(0)
+        _check(lib().entmaxkv_read_status(ctypes.byref(self.view), ctypes.byref(out), int(bool(clear)),
+                                          _stream(stream)))
+        return int(out.value)
+
 
 def append(cache: PagedCache, k, v, seq_ids=None, stream=None):
     """entmaxkv_append: k, v [n_seqs, Hkv, n_tokens, d] in the cache dtype."""
@@ -156,9 +171,14 @@ def append(cache: PagedCache, k, v, seq_ids=None, stream=None):
                                  _ptr(v), _ptr(seq_ids), n_seqs, n_tok, _stream(stream)))
 
 
-def workspace_bytes(cache: PagedCache, n_seqs, policy, budget_tokens=0) -> int:
-    return int(lib().entmaxkv_workspace_bytes(ctypes.byref(cache.cfg), n_seqs,
-                                              POLICIES.get(policy, policy), budget_tokens))
+def workspace_bytes(cache: PagedCache, n_seqs, policy, budget_tokens=0, flags=0) -> int:
+    return int(lib().entmaxkv_workspace_bytes_flags(ctypes.byref(cache.cfg), n_seqs,
+                                                    POLICIES.get(policy, policy), budget_tokens,
+                                                    int(flags)))
+
+
+def delta_kind(policy, flags=0) -> int:
+    return int(lib().entmaxkv_delta_kind(POLICIES.get(policy, policy), int(flags)))
 
 
 def workspace_layout(cache: PagedCache, n_seqs, policy, budget_tokens=0) -> WorkspaceView:
@@ -169,8 +189,8 @@ def workspace_layout(cache: PagedCache, n_seqs, policy, budget_tokens=0) -> Work
     return v
 
 
-def alloc_workspace(cache: PagedCache, n_seqs, policy, budget_tokens=0):
-    n = workspace_bytes(cache, n_seqs, policy, budget_tokens)
+def alloc_workspace(cache: PagedCache, n_seqs, policy, budget_tokens=0, flags=0):
+    n = workspace_bytes(cache, n_seqs, policy, budget_tokens, flags)
     if n == 0:
         raise EntmaxKVError("invalid decode arguments for workspace sizing")
     return torch.empty(n, dtype=torch.uint8, device=cache.device)  # caching allocator: 256-B aligned
@@ -218,7 +238,7 @@ def decode(cache: PagedCache, q, alpha=1.5, policy="gaussian", budget_tokens=0, 
     n_seqs = q.shape[0]
     pol = POLICIES.get(policy, policy)
     if workspace is None:
-        workspace = alloc_workspace(cache, n_seqs, pol, budget_tokens)
+        workspace = alloc_workspace(cache, n_seqs, pol, budget_tokens, flags)
     if outputs is None:
         outputs = alloc_outputs(cache, n_seqs, pol, budget_tokens)
     o = outputs

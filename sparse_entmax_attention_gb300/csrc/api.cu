@@ -115,6 +115,53 @@ static T* at(void* base, size_t off) {
   return off == (size_t)-1 ? nullptr : reinterpret_cast<T*>(static_cast<char*>(base) + off);
 }
 
+// Point the workspace members of `a` at the regions of layout L in ws.
+static void bind_workspace(DecodeArgs& a, void* ws, const Layout& L) {
+  a.splits = L.splits;
+  a.cap_pages = L.cap_pages;
+  a.kpages = L.kpages;
+  a.gcap = L.gcap;
+  a.words = L.words;
+  a.zmax = at<uint32_t>(ws, L.zmax);
+  a.cnt_a = at<int32_t>(ws, L.cnt_a);
+  a.cnt_b = at<int32_t>(ws, L.cnt_b);
+  a.cand_cnt = at<int32_t>(ws, L.cand_cnt);
+  a.kept_mass = at<float>(ws, L.kept_mass);
+  a.dbar = at<float>(ws, L.dbar);
+  a.bitmap = at<uint32_t>(ws, L.bitmap);
+  a.tauhat = at<float>(ws, L.tauhat);
+  a.tau_ws = at<double>(ws, L.tau_ws);
+  a.nsel_ws = at<int32_t>(ws, L.nsel_ws);
+  a.sel_list = at<int32_t>(ws, L.sel_list);
+  a.sel_pp = at<int2>(ws, L.sel_pp);
+  a.bbox_u = at<float>(ws, L.bbox_u);
+  a.bbox_uhat = at<float>(ws, L.bbox_uhat);
+  a.gauss_ms = at<float2>(ws, L.gauss_ms);
+  a.cand = at<int2>(ws, L.cand);
+  a.z = at<float>(ws, L.z);
+  a.pmax = at<float>(ws, L.pmax);
+  a.partial = at<float>(ws, L.partial);
+  a.pstride = L.pstride;
+  a.diag = at<int32_t>(ws, L.diag);
+  a.mslot = at<uint32_t>(ws, L.mslot);
+  a.mslots = L.mslots;
+  a.ctrl = reinterpret_cast<uint4*>(ws);
+  a.ctrl_vec = (int)(L.ctrl_end / 16);
+}
+
+// Bytes of the workspace with the given flags (0 for an invalid
+// configuration); L gets the policy's layout, LF the full-cache one that the
+// exact dropped mass needs.
+static size_t total_bytes(const entmaxkv_config* c, int S, int policy, int budget, uint32_t flags,
+                          Layout& L, Layout& LF) {
+  if (compute_layout(c, S, policy, budget, L) != ENTMAXKV_OK) return 0;
+  if (!(flags & ENTMAXKV_FLAG_EXACT_DELTA) || policy == ENTMAXKV_POLICY_SOFTMAX ||
+      policy == ENTMAXKV_POLICY_FULL)
+    return L.total;
+  if (compute_layout(c, S, ENTMAXKV_POLICY_FULL, 0, LF) != ENTMAXKV_OK) return 0;
+  return up256(L.total) + LF.total;
+}
+
 }  // namespace ekv
 
 using namespace ekv;
@@ -139,6 +186,34 @@ size_t entmaxkv_workspace_bytes(const entmaxkv_config* cfg, int32_t n_seqs, int3
   Layout L;
   if (compute_layout(cfg, n_seqs, policy, budget_tokens, L) != ENTMAXKV_OK) return 0;
   return L.total;
+}
+
+size_t entmaxkv_workspace_bytes_flags(const entmaxkv_config* cfg, int32_t n_seqs, int32_t policy,
+                                      int32_t budget_tokens, uint32_t flags) {
+  Layout L, LF;
+  return total_bytes(cfg, n_seqs, policy, budget_tokens, flags, L, LF);
+}
+
+int32_t entmaxkv_delta_kind(int32_t policy, uint32_t flags) {
+  switch (policy) {
+    case ENTMAXKV_POLICY_FULL:
+    case ENTMAXKV_POLICY_SOFTMAX: return ENTMAXKV_DELTA_ZERO;
+    case ENTMAXKV_POLICY_TOPK:
+      return (flags & ENTMAXKV_FLAG_EXACT_DELTA) ? ENTMAXKV_DELTA_EXACT : ENTMAXKV_DELTA_CERTIFIED;
+    case ENTMAXKV_POLICY_GAUSSIAN:
+      return (flags & ENTMAXKV_FLAG_EXACT_DELTA) ? ENTMAXKV_DELTA_EXACT : ENTMAXKV_DELTA_MODEL;
+    default: return -1;
+  }
+}
+
+int32_t entmaxkv_read_status(const entmaxkv_cache* cache, uint32_t* status_out, int32_t clear,
+                             void* stream) {
+  if (!cache || !cache->status || !status_out) return ENTMAXKV_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = cudaMemcpyAsync(status_out, cache->status, sizeof(uint32_t), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess && clear) e = cudaMemsetAsync(cache->status, 0, sizeof(uint32_t), s);
+  return e == cudaSuccess ? ENTMAXKV_OK : ENTMAXKV_ERR_CUDA;
 }
 
 int32_t entmaxkv_workspace_layout(const entmaxkv_config* cfg, int32_t n_seqs, int32_t policy,
@@ -214,9 +289,11 @@ static int32_t decode_impl(const entmaxkv_config* cfg, const entmaxkv_cache* cac
     if (!isfinite(margin)) return ENTMAXKV_ERR_INVALID_ARG;
     if (alpha != 1.5f && alpha != 2.0f) return ENTMAXKV_ERR_UNSUPPORTED;
   }
-  Layout L;
+  Layout L, LF;
   if ((st = compute_layout(cfg, n_seqs, policy, budget_tokens, L))) return st;
-  if (!workspace || ((uintptr_t)workspace & 255u) || workspace_bytes < L.total)
+  const size_t need = total_bytes(cfg, n_seqs, policy, budget_tokens, flags, L, LF);
+  const bool exact_delta = need != L.total;  // a second, full-cache region follows
+  if (!workspace || ((uintptr_t)workspace & 255u) || workspace_bytes < need)
     return ENTMAXKV_ERR_WORKSPACE_TOO_SMALL;
   if (page_ids && page_ids_stride < L.cap_pages) return ENTMAXKV_ERR_INVALID_ARG;
 
@@ -262,31 +339,7 @@ static int32_t decode_impl(const entmaxkv_config* cfg, const entmaxkv_cache* cac
   a.n_sel_out = n_sel;
   a.tau_out = tau;
   a.delta_out = delta;
-  a.zmax = at<uint32_t>(workspace, L.zmax);
-  a.cnt_a = at<int32_t>(workspace, L.cnt_a);
-  a.cnt_b = at<int32_t>(workspace, L.cnt_b);
-  a.cand_cnt = at<int32_t>(workspace, L.cand_cnt);
-  a.kept_mass = at<float>(workspace, L.kept_mass);
-  a.dbar = at<float>(workspace, L.dbar);
-  a.bitmap = at<uint32_t>(workspace, L.bitmap);
-  a.tauhat = at<float>(workspace, L.tauhat);
-  a.tau_ws = at<double>(workspace, L.tau_ws);
-  a.nsel_ws = at<int32_t>(workspace, L.nsel_ws);
-  a.sel_list = at<int32_t>(workspace, L.sel_list);
-  a.sel_pp = at<int2>(workspace, L.sel_pp);
-  a.bbox_u = at<float>(workspace, L.bbox_u);
-  a.bbox_uhat = at<float>(workspace, L.bbox_uhat);
-  a.gauss_ms = at<float2>(workspace, L.gauss_ms);
-  a.cand = at<int2>(workspace, L.cand);
-  a.z = at<float>(workspace, L.z);
-  a.pmax = at<float>(workspace, L.pmax);
-  a.partial = at<float>(workspace, L.partial);
-  a.pstride = L.pstride;
-  a.diag = at<int32_t>(workspace, L.diag);
-  a.mslot = at<uint32_t>(workspace, L.mslot);
-  a.mslots = L.mslots;
-  a.ctrl = reinterpret_cast<uint4*>(workspace);
-  a.ctrl_vec = (int)(L.ctrl_end / 16);
+  bind_workspace(a, workspace, L);
 
   cudaStream_t s = (cudaStream_t)stream;
   auto mark = [&](int i) -> cudaError_t {
@@ -320,6 +373,22 @@ static int32_t decode_impl(const entmaxkv_config* cfg, const entmaxkv_cache* cac
   // stage 4: pass B or the softmax kernel
   if (e == cudaSuccess) e = policy == ENTMAXKV_POLICY_SOFTMAX ? launch_softmax(a, dt, s) : launch_pass_b(a, dt, s);
   if (e == cudaSuccess) e = mark(5);
+  // exact dropped mass: full-cache pass A in the second region, then the
+  // full-cache weights of the kept pages' tokens
+  if (e == cudaSuccess && exact_delta) {
+    void* ws2 = static_cast<char*>(workspace) + up256(L.total);
+    DecodeArgs f = a;
+    f.policy = ENTMAXKV_POLICY_FULL;
+    f.flags = 0;
+    f.page_ids = nullptr;
+    f.n_sel_out = nullptr;
+    f.tau_out = nullptr;
+    f.delta_out = nullptr;
+    bind_workspace(f, ws2, LF);
+    e = cudaMemsetAsync(ws2, 0, LF.ctrl_end, s);
+    if (e == cudaSuccess) e = launch_pass_a(f, dt, s);
+    if (e == cudaSuccess) e = launch_exact_delta(a, f, s);
+  }
   return e == cudaSuccess ? ENTMAXKV_OK : ENTMAXKV_ERR_CUDA;
 }
 

@@ -397,6 +397,7 @@ cudaError_t launch_gauss(const DecodeArgs& a, int kv_dtype, int sms, cudaStream_
 int gauss_grid_x(int maxp, int Hkv, int S, int sms);
 cudaError_t launch_tauhat(const DecodeArgs& a, cudaStream_t st);
 cudaError_t launch_topk(const DecodeArgs& a, int mode, cudaStream_t st);
+cudaError_t launch_exact_delta(const DecodeArgs& m, const DecodeArgs& f, cudaStream_t st);
 cudaError_t launch_pass_a(const DecodeArgs& a, int kv_dtype, cudaStream_t st);
 cudaError_t launch_pass_b(const DecodeArgs& a, int kv_dtype, cudaStream_t st);
 cudaError_t launch_softmax(const DecodeArgs& a, int kv_dtype, cudaStream_t st);

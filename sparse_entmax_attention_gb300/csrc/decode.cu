@@ -860,6 +860,56 @@ __global__ void __launch_bounds__(kThreads, GP <= 4 ? 2 : 1) pass_b_kernel(Decod
 
 // ---------------------------------------------------------------------------
 
+// Exact dropped mass (summary §3): with τ and z of the full-cache solve in
+// f's workspace and the kept pages of the decode in m's, one block per
+// (sequence, KV head) sums p_i^full = [z_i − τ_full]_+^β over the kept pages'
+// tokens (a warp per page, lanes over tokens) and writes
+// δ = max(0, 1 − Σ kept p_i^full) for every query head of the group.
+__global__ void __launch_bounds__(kThreads) exact_delta_kernel(DecodeArgs m, DecodeArgs f) {
+  __shared__ float part[kWarps][8];
+  const int kvh = blockIdx.x, s = blockIdx.y;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = m.G, P = m.P;
+  const int seq = seq_row(m.seq_ids, s, m.max_seqs, nullptr);
+  const int L = seq_len_clamped(m.seq_lens, seq, m.maxp, P, nullptr);
+  const int n_pages = (L + P - 1) / P;
+  const size_t skv = (size_t)s * m.Hkv + kvh;
+  const size_t hq0 = (size_t)s * m.Hq + (size_t)kvh * G;
+  const bool bitmap = uses_bitmap(m.policy);
+  const int n_sel = bitmap ? __ldcg(&m.nsel_ws[skv]) : n_pages;
+  double tau[8];
+  float acc[8];
+#pragma unroll
+  for (int h = 0; h < 8; ++h) {
+    tau[h] = h < G ? __ldcg(&f.tau_ws[hq0 + h]) : 0.0;
+    acc[h] = 0.0f;
+  }
+  for (int r = warp; r < n_sel; r += kWarps) {
+    const int page = bitmap ? __ldcg(&m.sel_list[skv * m.cap_pages + r]) : r;
+    const float* zr = f.z + (skv * f.cap_pages + page) * (size_t)P * G;  // full cache: rank = page
+    if (lane < P) {
+#pragma unroll
+      for (int h = 0; h < 8; ++h)
+        if (h < G) acc[h] += pos_pow((float)((double)__ldcg(zr + lane * G + h) - tau[h]), f.beta);
+    }
+  }
+#pragma unroll
+  for (int h = 0; h < 8; ++h) {
+    const float w = warp_sum(acc[h]);
+    if (lane == 0) part[warp][h] = w;
+  }
+  __syncthreads();
+  if (tid < G && m.delta_out) {
+    float kept = 0.0f;
+    for (int w = 0; w < kWarps; ++w) kept += part[w][tid];
+    m.delta_out[hq0 + tid] = isnan(tau[tid]) ? 0.0f : fmaxf(0.0f, 1.0f - kept);
+  }
+}
+
+cudaError_t launch_exact_delta(const DecodeArgs& m, const DecodeArgs& f, cudaStream_t st) {
+  return launch_k(exact_delta_kernel, dim3(m.Hkv, m.S), dim3(kThreads), 0, st, m, f);
+}
+
 static int pick_gp(int G) { return G <= 1 ? 1 : (G <= 2 ? 2 : (G <= 4 ? 4 : 8)); }
 
 cudaError_t launch_pass_a(const DecodeArgs& a, int kv_dtype, cudaStream_t st) {

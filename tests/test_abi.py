@@ -124,3 +124,28 @@ def test_misaligned_cache_arrays_are_rejected(lib):
                                  1.5, B.POLICY_GAUSSIAN, 0, 0.5, 0, ctypes.c_void_p(256), 1 << 40,
                                  ctypes.c_void_p(256), None, 0, None, None, None, None)
         assert rc == 1, i
+
+
+def test_exact_delta_sizing_and_delta_kinds(lib):
+    cfg = _cfg()
+    f = lib.entmaxkv_workspace_bytes_flags
+    for pol, budget in ((B.POLICY_TOPK, 2048), (B.POLICY_GAUSSIAN, 0)):
+        plain = lib.entmaxkv_workspace_bytes(ctypes.byref(cfg), 1, pol, budget)
+        assert f(ctypes.byref(cfg), 1, pol, budget, 0) == plain
+        assert f(ctypes.byref(cfg), 1, pol, budget, B.FLAG_EXACT_DELTA) >= plain + \
+            lib.entmaxkv_workspace_bytes(ctypes.byref(cfg), 1, B.POLICY_FULL, 0)
+    for pol in (B.POLICY_FULL, B.POLICY_SOFTMAX):
+        assert f(ctypes.byref(cfg), 1, pol, 0, B.FLAG_EXACT_DELTA) == \
+            lib.entmaxkv_workspace_bytes(ctypes.byref(cfg), 1, pol, 0)
+    k = lib.entmaxkv_delta_kind
+    assert (k(B.POLICY_FULL, 0), k(B.POLICY_SOFTMAX, B.FLAG_EXACT_DELTA)) == (B.DELTA_ZERO, B.DELTA_ZERO)
+    assert (k(B.POLICY_TOPK, 0), k(B.POLICY_GAUSSIAN, 0)) == (B.DELTA_CERTIFIED, B.DELTA_MODEL)
+    assert k(B.POLICY_TOPK, B.FLAG_EXACT_DELTA) == B.DELTA_EXACT == k(B.POLICY_GAUSSIAN, B.FLAG_EXACT_DELTA)
+    assert k(9, 0) == -1
+
+
+def test_read_status_needs_a_status_word(lib):
+    view = B.CacheView(*([256] * 8), None)  # no status word
+    out = ctypes.c_uint32(7)
+    assert lib.entmaxkv_read_status(ctypes.byref(view), ctypes.byref(out), 0, None) == 1
+    assert lib.entmaxkv_read_status(None, ctypes.byref(out), 0, None) == 1
