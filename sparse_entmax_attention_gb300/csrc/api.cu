@@ -12,7 +12,7 @@ constexpr int kTargetBlocks = 2 * kSmCount;   // decode blocks per launch: one w
 
 struct Layout {
   size_t zmax, cnt_a, cnt_b, cand_cnt, kept_mass, dbar, bitmap, ctrl_end;
-  size_t tauhat, tau_ws, nsel_ws, sel_list, sel_pp, bbox_u, bbox_uhat, gauss_ms, cand, z, pmax, partial, diag, mslot;
+  size_t tauhat, tau_ws, nsel_ws, sel_list, sel_pp, vlist, vcount, bbox_u, bbox_uhat, gauss_ms, cand, z, pmax, partial, diag, mslot;
   size_t total;
   int splits, cap_pages, words, kpages, gcap, pstride, mslots;
 };
@@ -98,6 +98,8 @@ static int compute_layout(const entmaxkv_config* c, int S, int policy, int budge
   L.bbox_uhat = policy == ENTMAXKV_POLICY_TOPK ? take(nk * (size_t)maxp * 4) : none;
   L.gauss_ms = policy == ENTMAXKV_POLICY_GAUSSIAN ? take(nq * (size_t)maxp * 8) : none;
   L.sel_pp = entmax ? take(nk * (size_t)cap * 8) : none;
+  L.vlist = entmax ? take(nk * (size_t)cap * 16) : none;
+  L.vcount = entmax ? take(nk * 4) : none;
   L.cand = entmax ? take(nq * (size_t)cap * 8) : none;
   L.z = entmax ? take(nk * (size_t)cap * P * G * 4) : none;
   L.pmax = entmax ? take(nk * (size_t)cap * G * 4) : none;
@@ -134,6 +136,8 @@ static void bind_workspace(DecodeArgs& a, void* ws, const Layout& L) {
   a.nsel_ws = at<int32_t>(ws, L.nsel_ws);
   a.sel_list = at<int32_t>(ws, L.sel_list);
   a.sel_pp = at<int2>(ws, L.sel_pp);
+  a.vlist = at<int4>(ws, L.vlist);
+  a.vcount = at<int32_t>(ws, L.vcount);
   a.bbox_u = at<float>(ws, L.bbox_u);
   a.bbox_uhat = at<float>(ws, L.bbox_uhat);
   a.gauss_ms = at<float2>(ws, L.gauss_ms);

@@ -114,6 +114,7 @@ __device__ __forceinline__ void append_page(const AppendArgs& a, int b, int seq,
 // advanced by a second kernel once every page is written.
 template <typename T, int D>
 __global__ void __launch_bounds__(128) append_kernel(AppendArgs a) {
+  pdl_enter();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = blockIdx.z, kvh = blockIdx.y;
   const int seq = seq_row(a.seq_ids, b, a.max_seqs, lane == 0 ? a.status : nullptr);
@@ -125,6 +126,7 @@ __global__ void __launch_bounds__(128) append_kernel(AppendArgs a) {
 // touched page of every KV head, then advances the slot's length itself.
 template <typename T, int D>
 __global__ void __launch_bounds__(512) append_step_kernel(AppendArgs a, int pages) {
+  pdl_enter();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
   const int b = blockIdx.x;
   const int seq = seq_row(a.seq_ids, b, a.max_seqs, threadIdx.x == 0 ? a.status : nullptr);
@@ -137,6 +139,7 @@ __global__ void __launch_bounds__(512) append_step_kernel(AppendArgs a, int page
 }
 
 __global__ void advance_lens_kernel(AppendArgs a) {
+  pdl_enter();
   int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= a.n_seqs) return;
   int seq = a.seq_ids ? a.seq_ids[b] : b;
@@ -149,11 +152,11 @@ static cudaError_t launch_append_t(const AppendArgs& a, cudaStream_t st) {
   const int pages = (a.n_tokens + a.P - 1) / a.P + 1;  // pages one append can touch
   if ((long long)a.Hkv * pages <= 64) {
     const int warps = a.Hkv * pages < 16 ? a.Hkv * pages : 16;
-    return launch_k(append_step_kernel<T, D>, dim3(a.n_seqs), dim3(32 * warps), 0, st, a, pages);
+    return launch_k(false, append_step_kernel<T, D>, dim3(a.n_seqs), dim3(32 * warps), 0, st, a, pages);
   }
   dim3 grid((pages + 3) / 4, a.Hkv, a.n_seqs);
-  cudaError_t e = launch_k(append_kernel<T, D>, grid, dim3(128), 0, st, a);
-  if (e == cudaSuccess) e = launch_k(advance_lens_kernel, dim3((a.n_seqs + 127) / 128), dim3(128), 0, st, a);
+  cudaError_t e = launch_k(false, append_kernel<T, D>, grid, dim3(128), 0, st, a);
+  if (e == cudaSuccess) e = launch_k(false, advance_lens_kernel, dim3((a.n_seqs + 127) / 128), dim3(128), 0, st, a);
   return e;
 }
 

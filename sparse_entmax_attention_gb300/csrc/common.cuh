@@ -59,6 +59,9 @@ struct DecodeArgs {
   int32_t* nsel_ws;    // [S][Hkv]
   int32_t* sel_list;   // [S][Hkv][cap_pages]
   int2* sel_pp;        // [S][Hkv][cap_pages] (logical, physical) page of each rank; phys −1: unreadable
+  int4* vlist;         // [S][Hkv][cap_pages] (rank, logical page, physical page, 0) of the ranks whose
+                       //   page max clears τ for some head, rank ascending
+  int32_t* vcount;     // [S][Hkv] entries of vlist; −1: not built (pass B scans the ranks itself)
   float* bbox_u;       // [S][Hq][maxp]
   float* bbox_uhat;    // [S][Hkv][maxp]
   float2* gauss_ms;    // [S][Hq][maxp]
@@ -338,6 +341,9 @@ __device__ __forceinline__ float f2_sum(unsigned long long v) {
   asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
   return lo + hi;
 }
+__device__ __forceinline__ void f2_unpack(unsigned long long v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
 __device__ __forceinline__ unsigned long long f2_fma(unsigned long long a, unsigned long long b,
                                                      unsigned long long c) {
   unsigned long long d;
@@ -374,19 +380,31 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* sh, int& total) 
 }
 
 // ---------------------------------------------------------------------------
-// Every kernel is launched through cudaLaunchKernelEx. (Programmatic
-// dependent launch was measured on the 1M-token decode step and made it
-// slower, 126 µs against 121 µs, so no launch attribute is set.)
+// Launches. Every kernel is launched through cudaLaunchKernelEx and starts
+// with pdl_enter(): griddepcontrol.wait returns once the previous grid in the
+// stream has completed and its memory is visible (at once when the launch
+// did not allow programmatic overlap), then the next grid is allowed to
+// launch. A launch with pdl = true lets its blocks be scheduled while the
+// previous kernel drains; since every kernel waits before its first access,
+// each waits transitively for all earlier ones.
+__device__ __forceinline__ void pdl_enter() {
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
 template <typename... KArgs, typename... Args>
-inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
-                            Args... args) {
+inline cudaError_t launch_k(bool pdl, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                            cudaStream_t st, Args... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cfg.attrs = nullptr;
-  cfg.numAttrs = 0;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 

@@ -112,7 +112,7 @@ __device__ __forceinline__ void for_each_cand(const SolveSrc& S, F&& f) {
 // Float accumulation per candidate (GB300 runs FP64 at a small fraction of
 // the FP32 rate): τ is carried as a double and split into hi + lo floats so
 // that y = z − τ keeps its accuracy; only the per-iteration totals are double.
-__device__ __noinline__ double solve_tau_warp(const SolveSrc& S, double tau0, float beta, bool& ok) {
+__device__ double solve_tau_warp(const SolveSrc& S, double tau0, float beta, bool& ok) {
   double tau = tau0;
   ok = false;
   const bool b2 = beta == 2.0f, b1 = beta == 1.0f;
@@ -180,6 +180,7 @@ __device__ __noinline__ double solve_tau_warp(const SolveSrc& S, double tau0, fl
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads, 2) pass_a_kernel(DecodeArgs a) {
+  pdl_enter();
   __shared__ int list[kListCap];
   __shared__ int phys_sh[kListCap];
   __shared__ int sh_scan[32];
@@ -194,6 +195,7 @@ __global__ void __launch_bounds__(kThreads, 2) pass_a_kernel(DecodeArgs a) {
   static_assert(kListCap * 8 <= kSolveCap, "page maxima of a block fit the pool");
   __shared__ float T0_sh[8], tlb_sh[8];
   __shared__ int nc_sh[8], np_sh[8], nz_sh[8], off_sh[9];
+  __shared__ float tauf_sh[8];
   const int split = blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = a.G, P = a.P;
@@ -505,39 +507,105 @@ __global__ void __launch_bounds__(kThreads, 2) pass_a_kernel(DecodeArgs a) {
     }
   }
   __syncthreads();
-  if (warp >= G) return;
-  const int hg = warp;  // D
-  const size_t hs = hq0 + hg;
-  float tau_f = CUDART_NAN_F;
-  double tau_d = CUDART_NAN;
-  if (T0_sh[hg] < CUDART_INF_F) {
-    SolveSrc src;
-    src.zs = zc + hg * capZ;
-    src.m = nz_sh[hg];
-    src.big = nz_sh[hg] > capZ;
-    src.pages = clist + (size_t)hg * a.cap_pages;
-    src.np = nc_sh[hg];
-    src.zbase = zbase;
-    src.P = P;
-    src.G = G;
-    src.hg = hg;
-    src.T0 = tlb_sh[hg];
-    if (src.big && lane == 0) raise_flag(a.status, ENTMAXKV_DEV_CAND_OVERFLOW);
-    bool ok;
-    tau_d = solve_tau_warp(src, (double)src.T0, a.beta, ok);
-    if (!ok && lane == 0) raise_flag(a.status, ENTMAXKV_DEV_TAU_NOCONV);
-    tau_f = (float)tau_d;
-  }
-  if (lane == 0) {
-    a.tau_ws[hs] = tau_d;
-    if (a.tau_out) a.tau_out[hs] = tau_f;
-    if (a.delta_out) {
-      if (a.policy == ENTMAXKV_POLICY_GAUSSIAN)
-        a.delta_out[hs] = L > 0 ? fminf(1.0f, fmaxf(0.0f, 1.0f - __ldcg(&a.kept_mass[hs]))) : 0.0f;
-      else if (a.policy == ENTMAXKV_POLICY_FULL)
-        a.delta_out[hs] = 0.0f;
+  if (warp < G) {  // D
+    const int hg = warp;
+    const size_t hs = hq0 + hg;
+    float tau_f = CUDART_NAN_F;
+    double tau_d = CUDART_NAN;
+    if (T0_sh[hg] < CUDART_INF_F) {
+      SolveSrc src;
+      src.zs = zc + hg * capZ;
+      src.m = nz_sh[hg];
+      src.big = nz_sh[hg] > capZ;
+      src.pages = clist + (size_t)hg * a.cap_pages;
+      src.np = nc_sh[hg];
+      src.zbase = zbase;
+      src.P = P;
+      src.G = G;
+      src.hg = hg;
+      src.T0 = tlb_sh[hg];
+      if (src.big && lane == 0) raise_flag(a.status, ENTMAXKV_DEV_CAND_OVERFLOW);
+      bool ok;
+      tau_d = solve_tau_warp(src, (double)src.T0, a.beta, ok);
+      if (!ok && lane == 0) raise_flag(a.status, ENTMAXKV_DEV_TAU_NOCONV);
+      tau_f = (float)tau_d;
+    }
+    if (lane == 0) {
+      tauf_sh[hg] = tau_f;
+      a.tau_ws[hs] = tau_d;
+      if (a.tau_out) a.tau_out[hs] = tau_f;
+      if (a.delta_out) {
+        if (a.policy == ENTMAXKV_POLICY_GAUSSIAN)
+          a.delta_out[hs] = L > 0 ? fminf(1.0f, fmaxf(0.0f, 1.0f - __ldcg(&a.kept_mass[hs]))) : 0.0f;
+        else if (a.policy == ENTMAXKV_POLICY_FULL)
+          a.delta_out[hs] = 0.0f;
+      }
     }
   }
+  // The pages pass B must read: some head's page max above its τ. τ ≥ T0, so
+  // every such page is among the pages step A kept (in shared memory unless
+  // a head overflowed, then in its global candidate list). They are marked
+  // in a rank bitmap (in the score region, free after D), read back in rank
+  // order into a shared list over the page maxima (free now), and written
+  // out with their logical and physical pages.
+  const int W = (n_sel + 31) >> 5;
+  uint32_t* vbm = reinterpret_cast<uint32_t*>(zc);
+  int* vls = reinterpret_cast<int*>(pool);
+  if (W > kSolveCap / 2) {  // more ranks than the region holds bits: pass B scans them itself
+    if (tid == 0) a.vcount[skv] = -1;
+    return;
+  }
+  __syncthreads();  // the solves are done with the scores
+  for (int i = tid; i < W; i += kThreads) vbm[i] = 0u;
+  if (tid == 0) {
+    int t = 0;
+    for (int h = 0; h < G; ++h) {
+      off_sh[h] = t;
+      t += np_sh[h] <= capP ? np_sh[h] : nc_sh[h];
+    }
+    off_sh[G] = t;
+  }
+  __syncthreads();
+  for (int e = tid; e < off_sh[G]; e += kThreads) {
+    int h = 0;
+    while (e >= off_sh[h + 1]) ++h;
+    const int j = e - off_sh[h];
+    int rank;
+    float pmv;
+    if (np_sh[h] <= capP) {
+      rank = pr[h * capP + j];
+      pmv = pv[h * capP + j];
+    } else {
+      const int2 c = __ldcg(clist + (size_t)h * a.cap_pages + j);
+      rank = c.x;
+      pmv = __int_as_float(c.y);
+    }
+    if (pmv > tauf_sh[h]) atomicOr(&vbm[rank >> 5], 1u << (rank & 31));
+  }
+  __syncthreads();
+  const int wpt = (W + kThreads - 1) / kThreads, w0 = tid * wpt;
+  int cnt = 0;
+  for (int j = 0; j < wpt && w0 + j < W; ++j) cnt += __popc(vbm[w0 + j]);
+  int total;
+  int r = block_exclusive_scan(cnt, sh_scan, total);
+  if (total > kSolveCap / 2) {  // the shared list would overrun the bitmap
+    if (tid == 0) a.vcount[skv] = -1;
+    return;
+  }
+  for (int j = 0; j < wpt && w0 + j < W; ++j) {
+    uint32_t bits = vbm[w0 + j];
+    while (bits) {
+      vls[r++] = (w0 + j) * 32 + __ffs(bits) - 1;
+      bits &= bits - 1u;
+    }
+  }
+  __syncthreads();
+  for (int i = tid; i < total; i += kThreads) {  // all lookups in flight together
+    const int rank = vls[i];
+    const int2 pp = __ldcg(&a.sel_pp[skv * a.cap_pages + rank]);
+    a.vlist[skv * a.cap_pages + i] = make_int4(rank, pp.x, pp.y, 0);
+  }
+  if (tid == 0) a.vcount[skv] = total;
 }
 
 // ---------------------------------------------------------------------------
@@ -614,6 +682,7 @@ __device__ __noinline__ void combine_partials(const DecodeArgs& a, size_t skv, i
 // and accumulates p·v in fp32 registers.
 template <typename T, int D, int GP>
 __global__ void __launch_bounds__(kThreads, GP <= 4 ? 2 : 1) pass_b_kernel(DecodeArgs a) {
+  pdl_enter();
   constexpr int VEC = VTraits<T>::VEC, LPR = D / VEC, TG = 32 / LPR;
   constexpr int MAXT = 32 / TG;                  // rows per lane in a 32-token page
   __shared__ double tau_sh[GP];
@@ -650,11 +719,11 @@ __global__ void __launch_bounds__(kThreads, GP <= 4 ? 2 : 1) pass_b_kernel(Decod
     tau[h] = (float)taud[h];
   }
   const bool dense = (a.flags & ENTMAXKV_FLAG_DENSE_V) != 0;
-  float acc[GP][VEC];
+  unsigned long long accp[GP][VEC / 2];  // fp32 pairs of columns, for the paired FMA
 #pragma unroll
   for (int h = 0; h < GP; ++h)
 #pragma unroll
-    for (int j = 0; j < VEC; ++j) acc[h][j] = 0.0f;
+    for (int i = 0; i < VEC / 2; ++i) accp[h][i] = 0ull;
   float* zw = zs[warp];
 
   // One page: its V slab (P rows × D) arrives in this warp's shared buffer
@@ -684,6 +753,23 @@ __global__ void __launch_bounds__(kThreads, GP <= 4 ? 2 : 1) pass_b_kernel(Decod
       const int e = 4 * lane + 128 * u;
       if (e < P * G) *reinterpret_cast<float4*>(zw + e) = __ldcg(reinterpret_cast<const float4*>(zb + e));
     }
+    __syncwarp();  // the staged z is visible to the whole warp
+    // p of every (row, head) once, in place: [z − τ_h]_+^β, 0 past the valid rows
+    for (int e = lane; e < P * G; e += 32) {
+      const int t = e / G, h = e - t * G;
+      float th = tau[0];
+      double thd = taud[0];
+#pragma unroll
+      for (int hh = 1; hh < GP; ++hh)
+        if (h == hh) {
+          th = tau[hh];
+          thd = taud[hh];
+        }
+      const float zv = zw[e];
+      zw[e] = t >= nv ? 0.0f
+                      : (sizeof(T) == 4 ? pos_pow((float)((double)zv - thd), a.beta) : pos_pow(zv - th, a.beta));
+    }
+    __syncwarp();
     const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&vbar[warp], vphase));
     if (!ok) {
       stuck = true;
@@ -697,14 +783,16 @@ __global__ void __launch_bounds__(kThreads, GP <= 4 ? 2 : 1) pass_b_kernel(Decod
       if (t < nv) {
         float v[VEC];
         VTraits<T>::unpack(*reinterpret_cast<const uint4*>(vrow + (size_t)t * D), v);
+        unsigned long long vp[VEC / 2];
+#pragma unroll
+        for (int i = 0; i < VEC / 2; ++i) vp[i] = f2_pack(v[2 * i], v[2 * i + 1]);
 #pragma unroll
         for (int h = 0; h < GP; ++h) {
           if (h < G) {
-            const float zv = zw[t * G + h];
-            const float p = sizeof(T) == 4 ? pos_pow((float)((double)zv - taud[h]), a.beta)
-                                           : pos_pow(zv - tau[h], a.beta);
+            const float pw = zw[t * G + h];
+            const unsigned long long pp = f2_pack(pw, pw);
 #pragma unroll
-            for (int j = 0; j < VEC; ++j) acc[h][j] = fmaf(p, v[j], acc[h][j]);
+            for (int i = 0; i < VEC / 2; ++i) accp[h][i] = f2_fma(pp, vp[i], accp[h][i]);
           }
         }
       }
@@ -723,7 +811,18 @@ __global__ void __launch_bounds__(kThreads, GP <= 4 ? 2 : 1) pass_b_kernel(Decod
   int parts = a.splits;
   bool global_list = false;
   int n_list = 0;
-  if (!dense && n_sel <= 32 * kThreads) {
+  const int vc = dense ? -1 : __ldcg(&a.vcount[skv]);
+  const int4* vl = nullptr;  // this block's share of pass A's list, when it built one
+  if (vc >= 0) {
+    // top-k keeps every block: each one also sums its share of the δ̄ bound
+    parts = a.policy == ENTMAXKV_POLICY_TOPK ? a.splits : max(1, min(a.splits, (vc + kWarps - 1) / kWarps));
+    global_list = true;
+    if (split < parts) {
+      const int s_lo = (int)(((long long)vc * split) / parts);
+      n_list = (int)(((long long)vc * (split + 1)) / parts) - s_lo;
+      vl = a.vlist + skv * a.cap_pages + s_lo;
+    }
+  } else if (!dense && n_sel <= 32 * kThreads) {
     const int per = (n_sel + kThreads - 1) / kThreads;
     const int r0 = tid * per;
     uint32_t mask = 0u;
@@ -786,12 +885,22 @@ __global__ void __launch_bounds__(kThreads, GP <= 4 ? 2 : 1) pass_b_kernel(Decod
       __syncthreads();
     }
     for (int jj = warp; jj < n_list; jj += kWarps) {
-      const int rank = list_sh[jj];
-      const int2 pp = __ldcg(&a.sel_pp[skv * a.cap_pages + rank]);
-      if (pp.y >= 0) do_page(rank, pp.x, pp.y);
+      if (vl) {
+        const int4 e = __ldcg(vl + jj);
+        if (e.z >= 0) do_page(e.x, e.y, e.z);
+      } else {
+        const int rank = list_sh[jj];
+        const int2 pp = __ldcg(&a.sel_pp[skv * a.cap_pages + rank]);
+        if (pp.y >= 0) do_page(rank, pp.x, pp.y);
+      }
     }
     __syncthreads();  // list_sh is rewritten by the next chunk
   }
+  float acc[GP][VEC];
+#pragma unroll
+  for (int h = 0; h < GP; ++h)
+#pragma unroll
+    for (int i = 0; i < VEC / 2; ++i) f2_unpack(accp[h][i], acc[h][2 * i], acc[h][2 * i + 1]);
   if (stuck) {
     // flag it; the copy still in flight is waited for (bounded) before leaving
     if (lane == 0) {
@@ -866,6 +975,7 @@ __global__ void __launch_bounds__(kThreads, GP <= 4 ? 2 : 1) pass_b_kernel(Decod
 // tokens (a warp per page, lanes over tokens) and writes
 // δ = max(0, 1 − Σ kept p_i^full) for every query head of the group.
 __global__ void __launch_bounds__(kThreads) exact_delta_kernel(DecodeArgs m, DecodeArgs f) {
+  pdl_enter();
   __shared__ float part[kWarps][8];
   const int kvh = blockIdx.x, s = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -907,7 +1017,7 @@ __global__ void __launch_bounds__(kThreads) exact_delta_kernel(DecodeArgs m, Dec
 }
 
 cudaError_t launch_exact_delta(const DecodeArgs& m, const DecodeArgs& f, cudaStream_t st) {
-  return launch_k(exact_delta_kernel, dim3(m.Hkv, m.S), dim3(kThreads), 0, st, m, f);
+  return launch_k(false, exact_delta_kernel, dim3(m.Hkv, m.S), dim3(kThreads), 0, st, m, f);
 }
 
 static int pick_gp(int G) { return G <= 1 ? 1 : (G <= 2 ? 2 : (G <= 4 ? 4 : 8)); }
@@ -915,11 +1025,11 @@ static int pick_gp(int G) { return G <= 1 ? 1 : (G <= 2 ? 2 : (G <= 4 ? 4 : 8));
 cudaError_t launch_pass_a(const DecodeArgs& a, int kv_dtype, cudaStream_t st) {
   dim3 grid(a.splits, a.Hkv, a.S);
   if (kv_dtype == ENTMAXKV_BF16) {
-    if (a.D == 128) launch_k(pass_a_kernel<__nv_bfloat16, 128>, dim3(grid), dim3(kThreads), 0, st, a);
-    else launch_k(pass_a_kernel<__nv_bfloat16, 64>, dim3(grid), dim3(kThreads), 0, st, a);
+    if (a.D == 128) launch_k(false, pass_a_kernel<__nv_bfloat16, 128>, dim3(grid), dim3(kThreads), 0, st, a);
+    else launch_k(false, pass_a_kernel<__nv_bfloat16, 64>, dim3(grid), dim3(kThreads), 0, st, a);
   } else {
-    if (a.D == 128) launch_k(pass_a_kernel<float, 128>, dim3(grid), dim3(kThreads), 0, st, a);
-    else launch_k(pass_a_kernel<float, 64>, dim3(grid), dim3(kThreads), 0, st, a);
+    if (a.D == 128) launch_k(false, pass_a_kernel<float, 128>, dim3(grid), dim3(kThreads), 0, st, a);
+    else launch_k(false, pass_a_kernel<float, 64>, dim3(grid), dim3(kThreads), 0, st, a);
   }
   return cudaGetLastError();
 }
@@ -930,7 +1040,7 @@ static cudaError_t pass_b_launch(const DecodeArgs& a, dim3 grid, cudaStream_t st
   const cudaError_t e = cudaFuncSetAttribute(pass_b_kernel<T, D, GP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              kWarps * 32 * D * (int)sizeof(T));
   if (e != cudaSuccess) return e;
-  launch_k(pass_b_kernel<T, D, GP>, dim3(grid), dim3(kThreads), smem, st, a);
+  launch_k(false, pass_b_kernel<T, D, GP>, dim3(grid), dim3(kThreads), smem, st, a);
   return cudaGetLastError();
 }
 

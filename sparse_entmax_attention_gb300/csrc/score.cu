@@ -42,6 +42,7 @@ __device__ __forceinline__ void split_sign(uint32_t w, uint32_t& pos, uint32_t& 
 
 template <int D>
 __global__ void __launch_bounds__(kThreads) bbox_bf16_kernel(DecodeArgs a) {
+  pdl_enter();
   constexpr int KS = D / 16;   // k-steps per half of the 2d contraction
   constexpr int C16 = D / 32;  // 16-byte chunks per row per lane
   const int kvh = blockIdx.y, s = blockIdx.z;
@@ -128,6 +129,7 @@ __global__ void __launch_bounds__(kThreads) bbox_bf16_kernel(DecodeArgs a) {
 // fp32 metadata: one thread per page, q in shared memory.
 template <int D>
 __global__ void __launch_bounds__(kThreads) bbox_f32_kernel(DecodeArgs a) {
+  pdl_enter();
   __shared__ float qs[8][D];
   const int kvh = blockIdx.y, s = blockIdx.z;
   clear_ctrl_slice(a.ctrl, a.ctrl_vec);
@@ -191,6 +193,7 @@ constexpr int gauss_smem_bytes() {
 
 template <typename TQ, int D, int GP>
 __global__ void __launch_bounds__(kGaussWarps * 32) gauss_kernel(DecodeArgs a) {
+  pdl_enter();
   constexpr int DPL = D / 16;             // dims per lane (a half-warp covers a row)
   constexpr int CH = DPL / 4;             // 16-byte chunks per lane per row
   constexpr int PPS = kGaussPPS, NST = kGaussNST;
@@ -404,12 +407,12 @@ cudaError_t launch_bbox(const DecodeArgs& a, int kv_dtype, int sms, cudaStream_t
   const int other = a.Hkv * a.S;
   if (kv_dtype == ENTMAXKV_BF16) {
     dim3 grid(grid_x_for((a.maxp + 15) / 16, kWarps, sms, other), a.Hkv, a.S);
-    if (a.D == 128) launch_k(bbox_bf16_kernel<128>, dim3(grid), dim3(kThreads), 0, st, a);
-    else launch_k(bbox_bf16_kernel<64>, dim3(grid), dim3(kThreads), 0, st, a);
+    if (a.D == 128) launch_k(false, bbox_bf16_kernel<128>, dim3(grid), dim3(kThreads), 0, st, a);
+    else launch_k(false, bbox_bf16_kernel<64>, dim3(grid), dim3(kThreads), 0, st, a);
   } else {
     dim3 grid(grid_x_for(a.maxp, kThreads, sms, other), a.Hkv, a.S);
-    if (a.D == 128) launch_k(bbox_f32_kernel<128>, dim3(grid), dim3(kThreads), 0, st, a);
-    else launch_k(bbox_f32_kernel<64>, dim3(grid), dim3(kThreads), 0, st, a);
+    if (a.D == 128) launch_k(false, bbox_f32_kernel<128>, dim3(grid), dim3(kThreads), 0, st, a);
+    else launch_k(false, bbox_f32_kernel<64>, dim3(grid), dim3(kThreads), 0, st, a);
   }
   return cudaGetLastError();
 }
@@ -420,7 +423,7 @@ static cudaError_t gauss_launch(const DecodeArgs& a, dim3 grid, cudaStream_t st)
   static_assert(gauss_smem_bytes<D>() <= 227 * 1024, "stages exceed shared memory");
   cudaError_t e = cudaFuncSetAttribute(gauss_kernel<TQ, D, GP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  return launch_k(gauss_kernel<TQ, D, GP>, dim3(grid), dim3(kGaussWarps * 32), smem, st, a);
+  return launch_k(false, gauss_kernel<TQ, D, GP>, dim3(grid), dim3(kGaussWarps * 32), smem, st, a);
 }
 
 template <typename TQ, int D>

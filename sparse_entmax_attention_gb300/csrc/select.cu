@@ -48,6 +48,7 @@ __device__ __forceinline__ float sqrt_2ln(int n, int P, float c_full) {
 // stay bit-identical without further synchronisation.
 __global__ void __cluster_dims__(kTauhatCluster, 1, 1) __launch_bounds__(kThreads, 2)
     tauhat_kernel(DecodeArgs a) {
+  pdl_enter();
   static_assert(kTauhatCluster * kWarps == 64, "two partials per lane");
   cg::cluster_group cluster = cg::this_cluster();
   __shared__ float3 slot[2][kWarps];
@@ -234,6 +235,7 @@ __device__ __forceinline__ float page_key(const DecodeArgs& a, int mode, int s, 
 }
 
 __global__ void __launch_bounds__(1024) topk_kernel(DecodeArgs a, int mode) {
+  pdl_enter();
   __shared__ int hist[256];
   __shared__ int sh_scan[32];
   __shared__ float thr[8];
@@ -344,13 +346,13 @@ __global__ void __launch_bounds__(1024) topk_kernel(DecodeArgs a, int mode) {
 
 cudaError_t launch_tauhat(const DecodeArgs& a, cudaStream_t st) {
   dim3 grid(kTauhatCluster, a.Hq, a.S);
-  launch_k(tauhat_kernel, dim3(grid), dim3(kThreads), 0, st, a);
+  launch_k(false, tauhat_kernel, dim3(grid), dim3(kThreads), 0, st, a);
   return cudaGetLastError();
 }
 
 cudaError_t launch_topk(const DecodeArgs& a, int mode, cudaStream_t st) {
   dim3 grid(a.Hkv, a.S);
-  launch_k(topk_kernel, dim3(grid), dim3(1024), 0, st, a, mode);
+  launch_k(false, topk_kernel, dim3(grid), dim3(1024), 0, st, a, mode);
   return cudaGetLastError();
 }
 

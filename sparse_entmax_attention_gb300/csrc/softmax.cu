@@ -15,6 +15,7 @@ namespace ekv {
 
 template <typename T, int D, int GP>
 __global__ void __launch_bounds__(kThreads, 2) softmax_kernel(DecodeArgs a) {
+  pdl_enter();
   constexpr int VEC = 16 / sizeof(T), LPR = D / VEC, TG = 32 / LPR;
   constexpr int MAXT = 32 / TG;                  // tokens per lane in a 32-token page
   constexpr int CH = MAXT < 8 ? MAXT : 8;        // V rows in flight per lane
@@ -255,10 +256,10 @@ __global__ void __launch_bounds__(kThreads, 2) softmax_kernel(DecodeArgs a) {
 
 template <typename T, int D>
 static void softmax_g(const DecodeArgs& a, dim3 grid, cudaStream_t st) {
-  if (a.G <= 1) launch_k(softmax_kernel<T, D, 1>, dim3(grid), dim3(kThreads), 0, st, a);
-  else if (a.G <= 2) launch_k(softmax_kernel<T, D, 2>, dim3(grid), dim3(kThreads), 0, st, a);
-  else if (a.G <= 4) launch_k(softmax_kernel<T, D, 4>, dim3(grid), dim3(kThreads), 0, st, a);
-  else launch_k(softmax_kernel<T, D, 8>, dim3(grid), dim3(kThreads), 0, st, a);
+  if (a.G <= 1) launch_k(false, softmax_kernel<T, D, 1>, dim3(grid), dim3(kThreads), 0, st, a);
+  else if (a.G <= 2) launch_k(false, softmax_kernel<T, D, 2>, dim3(grid), dim3(kThreads), 0, st, a);
+  else if (a.G <= 4) launch_k(false, softmax_kernel<T, D, 4>, dim3(grid), dim3(kThreads), 0, st, a);
+  else launch_k(false, softmax_kernel<T, D, 8>, dim3(grid), dim3(kThreads), 0, st, a);
 }
 
 cudaError_t launch_softmax(const DecodeArgs& a, int kv_dtype, cudaStream_t st) {
