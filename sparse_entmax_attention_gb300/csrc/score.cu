@@ -210,6 +210,8 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_kernel(DecodeArgs a) {
   uint64_t* empty = full + NST;
   int* phys_sm = reinterpret_cast<int*>(empty + NST);                   // [NST][PPS]
   __shared__ uint32_t smax[8][GP];
+  static_assert(kGaussNST * kGaussPPS <= 32, "warp 0 looks up the first stages' pages at once");
+  // every block, with pages or not, clears its slice of the control words
   clear_ctrl_slice(a.ctrl, a.ctrl_vec);
   // this block's slot of the per-head maxima starts as "none"
   for (int i = threadIdx.x; i < KH * a.G; i += blockDim.x)
@@ -226,12 +228,47 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_kernel(DecodeArgs a) {
   if (n_mine <= 0) return;
   const uint32_t row_bytes = (uint32_t)KH * D * 4;
   if (threadIdx.x < 8 * GP) smax[threadIdx.x / GP][threadIdx.x % GP] = 0u;
-  if (threadIdx.x < NST) {
-    mbar_init(&full[threadIdx.x], 1);
-    mbar_init(&empty[threadIdx.x], kGaussWarps);
+
+  // producer (warp 0): copy stage st's pages, whose physical ids are in
+  // phys_sm (lanes 0..2·PPS−1 copy one run each: page lane/2, array lane%2)
+  auto issue_copies = [&](int st) {
+    const int ph = lane < 2 * PPS ? phys_sm[st * PPS + (lane >> 1)] : -1;
+    const uint32_t valid = __ballot_sync(0xffffffffu, ph >= 0);
+    if (lane == 0) mbar_expect_tx(&full[st], (uint32_t)__popc(valid) * row_bytes);
+    __syncwarp();
+    if (ph >= 0) {
+      const float* src = ((lane & 1) ? a.m2 : a.mean) + ((size_t)ph * a.Hkv + kv0) * D;
+      float* dst = stages + (((size_t)st * PPS + (lane >> 1)) * 2 + (lane & 1)) * KH * D;
+      bulk_g2s(dst, src, row_bytes, &full[st]);
+    }
+  };
+  // refill stage st with group g: look its pages up, then copy
+  auto issue = [&](int g, int st) {
+    if (lane < PPS) {
+      const int p = g * PPS + lane;
+      phys_sm[st * PPS + lane] = p < n_pages ? phys_page(a.block_table, seq, p, a.maxp, a.nphys, a.status) : -1;
+    }
+    __syncwarp();
+    issue_copies(st);
+  };
+  if (warp == 0) {
+    // The pipeline starts before anything else: barriers, then every page of
+    // the first NST stages looked up in one round trip, then their copies.
+    if (lane < NST) {
+      mbar_init(&full[lane], 1);
+      mbar_init(&empty[lane], kGaussWarps);
+    }
+    mbar_fence_init();
+    __syncwarp();
+    const int nfill = min(NST, n_mine);
+    if (lane < NST * PPS) {
+      const int j = lane / PPS, p = (g_lo + j) * PPS + lane % PPS;
+      phys_sm[lane] = (j < nfill && p < n_pages)
+                          ? phys_page(a.block_table, seq, p, a.maxp, a.nphys, a.status) : -1;
+    }
+    __syncwarp();
+    for (int j = 0; j < nfill; ++j) issue_copies(j);
   }
-  mbar_fence_init();
-  __syncthreads();
 
   unsigned long long qp[GP][DPL / 2], q2p[GP][DPL / 2];
 #pragma unroll
@@ -264,24 +301,7 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_kernel(DecodeArgs a) {
   for (int i = 0; i < NFIN; ++i) runmax[i] = -CUDART_INF_F;
   const float inv_full = 1.0f / ((float)a.P * (float)D);
 
-  // producer (warp 0): fill stage st with group g (lanes 0..2·PPS−1 copy one run each)
-  auto issue = [&](int g, int st) {
-    const int p = g * PPS + (lane >> 1);
-    int ph = -1;
-    if (lane < 2 * PPS && p < n_pages)
-      ph = phys_page(a.block_table, seq, p, a.maxp, a.nphys, (lane & 1) ? nullptr : a.status);
-    const uint32_t valid = __ballot_sync(0xffffffffu, ph >= 0);
-    if ((lane & 1) == 0 && lane < 2 * PPS) phys_sm[st * PPS + (lane >> 1)] = ph;
-    if (lane == 0) mbar_expect_tx(&full[st], (uint32_t)__popc(valid) * row_bytes);
-    __syncwarp();
-    if (ph >= 0) {
-      const float* src = ((lane & 1) ? a.m2 : a.mean) + ((size_t)ph * a.Hkv + kv0) * D;
-      float* dst = stages + (((size_t)st * PPS + (lane >> 1)) * 2 + (lane & 1)) * KH * D;
-      bulk_g2s(dst, src, row_bytes, &full[st]);
-    }
-  };
-  if (warp == 0)
-    for (int j = 0; j < NST && j < n_mine; ++j) issue(g_lo + j, j);
+  __syncthreads();  // barriers initialised, q in registers
 
   int stuck = 0;
   for (int j = 0; j < n_mine; ++j) {
