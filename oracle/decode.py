@@ -22,7 +22,13 @@ analysis of §3):
             every token of page p scores ≤ U_p^h;
   gaussian  the page model's estimate Σ_{dropped pages} n_p·E[(Z_p − τ̂)_+^β];
   softmax   δ = 0 and the "τ" slot carries log Σ_i exp(s_i).
-The exact δ = Σ_{i∉I} p_i^full is always returned as ``delta_exact``.
+  softmax_topk  softmax over the top-k kept set (the comparison the summary's
+            §1/§4 draw against softmax attention); "τ" carries log Σ_{i∈I} exp(s_i)
+            and δ is the certified bound D/(1 + D), D = Σ_{dropped pages}
+            n_p·exp(U_p^h − lse_kept): with A = Σ_I e^{s} and B = Σ_{i∉I} e^{s}
+            ≤ B̄ = Σ_dropped n_p e^{U_p}, δ = B/(A + B) ≤ B̄/(A + B̄) since it grows in B.
+The exact δ = Σ_{i∉I} p_i^full (the full-cache weights of the same kind of
+attention) is always returned as ``delta_exact``.
 """
 
 from __future__ import annotations
@@ -34,7 +40,7 @@ import numpy as np
 from . import entmax as em
 from . import pages as pg
 
-POLICIES = ("full", "topk", "gaussian", "softmax")
+POLICIES = ("full", "topk", "gaussian", "softmax", "softmax_topk")
 
 
 def _beta(alpha):
@@ -107,7 +113,7 @@ def decode_group(K, V, Q, alpha: float, policy: str, page_size: int,
     # ---- selection -------------------------------------------------------
     if policy in ("full", "softmax"):
         sel = np.arange(n_pages, dtype=np.int64)
-    elif policy == "topk":
+    elif policy in ("topk", "softmax_topk"):
         k = budget_tokens // P
         if k <= 0:
             raise ValueError("top-k needs budget_tokens >= page_size")
@@ -145,12 +151,13 @@ def decode_group(K, V, Q, alpha: float, policy: str, page_size: int,
 
     # ---- attention over the kept set --------------------------------------
     scores = (K @ Q.T / math.sqrt(d)) if (diagnostics or policy == "softmax") else None
+    soft = policy in ("softmax", "softmax_topk")
     out = np.zeros((g, d))
     tau = np.full(g, np.nan)
     delta = np.zeros(g)
     delta_exact = np.zeros(g)
     recall = np.ones(g)
-    beta = _beta(alpha) if policy != "softmax" else None
+    beta = _beta(alpha) if not soft else None
     s_kept = K[idx] @ Q.T / math.sqrt(d) if scores is None else scores[idx]
     for h in range(g):
         if policy == "softmax":
@@ -159,7 +166,7 @@ def decode_group(K, V, Q, alpha: float, policy: str, page_size: int,
             tau[h] = lse
             continue
         if diagnostics:
-            p_full, tau_full = em.entmax(scores[:, h], alpha)
+            p_full, tau_full = em.softmax(scores[:, h]) if soft else em.entmax(scores[:, h], alpha)
             supp = p_full > 0
             delta_exact[h] = float(p_full[~keep].sum())
             recall[h] = float((supp & keep).sum()) / float(supp.sum())
@@ -167,10 +174,13 @@ def decode_group(K, V, Q, alpha: float, policy: str, page_size: int,
             # Nothing kept: zero output, undefined threshold, all mass dropped.
             delta[h] = 1.0
             continue
-        p_k, tau_k = em.entmax(s_kept[:, h], alpha)
+        p_k, tau_k = em.softmax(s_kept[:, h]) if soft else em.entmax(s_kept[:, h], alpha)
         out[h] = p_k @ V[idx]
         tau[h] = tau_k
         dropped = np.setdiff1d(np.arange(n_pages), sel)
+        if policy == "softmax_topk":
+            D = float(np.sum(meta["n"][dropped] * np.exp(res["U"][h, dropped] - tau_k)))
+            delta[h] = D / (1.0 + D)
         if policy == "topk":
             zb = (alpha - 1.0) * res["U"][h, dropped] - tau_k
             delta[h] = min(1.0, float(np.sum(meta["n"][dropped] * np.clip(zb, 0.0, None) ** beta)))

@@ -172,3 +172,45 @@ def test_gaussian_selector_exact_on_constant_pages(alpha):
     assert set(r["page_ids"]) == supp
     np.testing.assert_allclose(r["out"], full["out"], atol=1e-12)
     np.testing.assert_allclose(r["delta"], 0.0, atol=1e-12)
+
+
+def test_softmax_topk_bound_and_renormalisation():
+    # kept-set softmax = full softmax restricted to the kept tokens and
+    # renormalised by 1 − δ; the certified bound D/(1 + D) is ≥ δ
+    rng = np.random.default_rng(27)
+    for _ in range(6):
+        K, V, Q = _case(rng, n_tok=300, needles=4, g=2)
+        r = dec.decode_group(K, V, Q, 1.5, "softmax_topk", 16, 64)
+        s = K @ Q.T / math.sqrt(K.shape[1])
+        keep = np.zeros(K.shape[0], bool)
+        for p in r["page_ids"]:
+            keep[p * 16:(p + 1) * 16] = True
+        for h in range(2):
+            p_full, lse_full = em.softmax(s[:, h])
+            de = p_full[~keep].sum()
+            assert abs(r["delta_exact"][h] - de) < 1e-12
+            np.testing.assert_allclose(r["out"][h], (p_full[keep] @ V[keep]) / (1.0 - de), atol=1e-12)
+            assert abs(r["tau"][h] - (lse_full + math.log1p(-de))) < 1e-12
+            assert r["delta_exact"][h] <= r["delta"][h] < 1.0
+
+
+def test_softmax_topk_whole_budget_is_full_softmax():
+    rng = np.random.default_rng(28)
+    K, V, Q = _case(rng, n_tok=200)
+    r = dec.decode_group(K, V, Q, 1.5, "softmax_topk", 16, 16 * 13)
+    full = dec.decode_group(K, V, Q, 1.5, "softmax", 16)
+    np.testing.assert_allclose(r["out"], full["out"], atol=1e-12)
+    np.testing.assert_allclose(r["tau"], full["tau"], atol=1e-12)
+    assert np.all(r["delta"] == 0.0) and np.all(np.abs(r["delta_exact"]) < 1e-15)
+
+
+def test_softmax_topk_bound_is_tight_on_constant_pages():
+    # every token of a page equal: U_p is each token's exact score, so the
+    # bound B̄ equals the dropped mass B and D/(1 + D) is the exact δ
+    rng = np.random.default_rng(29)
+    P, n_pages, d = 8, 30, 16
+    K = np.repeat(rng.normal(size=(n_pages, d)), P, axis=0)
+    V = rng.normal(size=(n_pages * P, d))
+    Q = rng.normal(size=(2, d))
+    r = dec.decode_group(K, V, Q, 1.5, "softmax_topk", P, 5 * P)
+    np.testing.assert_allclose(r["delta"], r["delta_exact"], rtol=1e-12, atol=1e-15)
