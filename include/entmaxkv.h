@@ -66,6 +66,8 @@ typedef enum {
 #define ENTMAXKV_POLICY_TOPK     1  /* the k = budget/page_size pages with the largest bound */
 #define ENTMAXKV_POLICY_GAUSSIAN 2  /* pages whose estimated max clears τ̂ − Δ               */
 #define ENTMAXKV_POLICY_SOFTMAX  3  /* full-cache softmax (FlashDecoding-style baseline)     */
+#define ENTMAXKV_POLICY_SOFTMAX_TOPK 4  /* softmax over the top-k pages (the softmax side of the
+                                           summary's comparison at equal budget, §1/§4)     */
 
 /* Decode flags. */
 #define ENTMAXKV_FLAG_DENSE_V 0x1u  /* read every selected V page even where all p_i = 0
@@ -187,9 +189,9 @@ int32_t entmaxkv_read_status(const entmaxkv_cache* cache, uint32_t* status_out, 
  * One decode step for n_seqs sequences (summary §2A-§2C; δ from §3).
  *   q          (device) [n_seqs][Hq][head_dim], kv_dtype (Hq = Hkv·group)
  *   seq_ids    (device) [n_seqs] sequence rows, or NULL for 0..n_seqs−1
- *   alpha      α > 1 (GAUSSIAN needs α ∈ {1.5, 2}); ignored by SOFTMAX
+ *   alpha      α > 1 (GAUSSIAN needs α ∈ {1.5, 2}); ignored by SOFTMAX and SOFTMAX_TOPK
  *   policy     ENTMAXKV_POLICY_*
- *   budget_tokens  TOPK: k = budget_tokens / page_size pages (must be ≥ 1);
+ *   budget_tokens  TOPK, SOFTMAX_TOPK: k = budget_tokens / page_size pages (must be ≥ 1);
  *                  GAUSSIAN: a cap in tokens (0 = none; on overflow the pages
  *                  with the largest margin max_h(M̂_p − threshold_h) are kept,
  *                  ties to the lower index, and ENTMAXKV_DEV_CAPACITY is set);
@@ -206,15 +208,17 @@ int32_t entmaxkv_read_status(const entmaxkv_cache* cache, uint32_t* status_out, 
  *              ids, ascending (FULL/SOFTMAX: every page)
  *   n_sel      [n_seqs][Hkv] int32 selected pages
  *   tau        [n_seqs][Hq] float32: the exact α-entmax threshold over the
- *              kept tokens on the z scale (SOFTMAX: log Σ exp(s_i)); NaN for
- *              an empty kept set
+ *              kept tokens on the z scale (SOFTMAX, SOFTMAX_TOPK: log Σ exp(s_i)
+ *              over the kept tokens); NaN for an empty kept set
  *   delta      [n_seqs][Hq] float32 dropped mass: FULL/SOFTMAX 0; TOPK the
  *              certified bound min(1, Σ_dropped n_p·[(α−1)U_p − τ]_+^β);
  *              GAUSSIAN the page model's estimate of the dropped mass;
+ *              SOFTMAX_TOPK the certified bound D/(1 + D) with
+ *              D = Σ_dropped n_p·exp(U_p − log Σ_kept exp(s_i));
  *              with ENTMAXKV_FLAG_EXACT_DELTA, for every policy, the exact
  *              max(0, 1 − Σ_{i in the kept pages} p_i^full)
  * page_ids_stride must be ≥ the most pages the policy can select
- * (TOPK: k; GAUSSIAN: the cap in pages, or max_pages_per_seq; otherwise
+ * (TOPK, SOFTMAX_TOPK: k; GAUSSIAN: the cap in pages, or max_pages_per_seq; otherwise
  * max_pages_per_seq) when page_ids is not NULL.
  * An empty sequence yields out = 0, tau = NaN, delta = 0, n_sel = 0.
  */

@@ -47,10 +47,11 @@ def _beta(alpha):
     return 1.0 / (alpha - 1.0)
 
 
-def attend_pages(K, V, Q, alpha: float, page_size: int, page_ids):
+def attend_pages(K, V, Q, alpha: float, page_size: int, page_ids, softmax: bool = False):
     """α-entmax attention of the g query heads over the tokens of the given
-    pages only (§2C). Returns (out [g, d], tau [g]); an empty page set gives a
-    zero output and τ = NaN."""
+    pages only (§2C), or softmax attention over them with ``softmax`` (then the
+    τ slot is log Σ exp(s_i) over those tokens). Returns (out [g, d], tau [g]);
+    an empty page set gives a zero output and τ = NaN."""
     K = np.asarray(K, np.float64)
     V = np.asarray(V, np.float64)
     Q = np.atleast_2d(np.asarray(Q, np.float64))
@@ -66,7 +67,7 @@ def attend_pages(K, V, Q, alpha: float, page_size: int, page_ids):
         return out, tau
     s = K[idx] @ Q.T / math.sqrt(d)
     for h in range(g):
-        p, tau[h] = em.entmax(s[:, h], alpha)
+        p, tau[h] = em.softmax(s[:, h]) if softmax else em.entmax(s[:, h], alpha)
         out[h] = p @ V[idx]
     return out, tau
 

@@ -19,9 +19,9 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libentmaxkv.so")
 
 F32, BF16 = 0, 1
-POLICY_FULL, POLICY_TOPK, POLICY_GAUSSIAN, POLICY_SOFTMAX = 0, 1, 2, 3
+POLICY_FULL, POLICY_TOPK, POLICY_GAUSSIAN, POLICY_SOFTMAX, POLICY_SOFTMAX_TOPK = 0, 1, 2, 3, 4
 POLICIES = {"full": POLICY_FULL, "topk": POLICY_TOPK, "gaussian": POLICY_GAUSSIAN,
-            "softmax": POLICY_SOFTMAX}
+            "softmax": POLICY_SOFTMAX, "softmax_topk": POLICY_SOFTMAX_TOPK}
 FLAG_DENSE_V, FLAG_EXACT_DELTA = 0x1, 0x2
 DELTA_ZERO, DELTA_CERTIFIED, DELTA_MODEL, DELTA_EXACT = 0, 1, 2, 3
 DEV_BAD_PAGE_TABLE, DEV_CAPACITY, DEV_TAUHAT_NOCONV = 0x1, 0x2, 0x4
@@ -208,7 +208,7 @@ class DecodeOutputs:
 def page_capacity(cache: PagedCache, policy, budget_tokens) -> int:
     p = POLICIES.get(policy, policy)
     maxp, P = cache.cfg.max_pages_per_seq, cache.cfg.page_size
-    if p == POLICY_TOPK:
+    if p in (POLICY_TOPK, POLICY_SOFTMAX_TOPK):
         return min(budget_tokens // P, maxp)
     if p == POLICY_GAUSSIAN and budget_tokens > 0:
         return min(budget_tokens // P, maxp)

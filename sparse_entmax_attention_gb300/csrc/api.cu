@@ -46,7 +46,7 @@ static int compute_layout(const entmaxkv_config* c, int S, int policy, int budge
   int st = check_config(c);
   if (st) return st;
   if (S < 1 || S > 65535) return ENTMAXKV_ERR_INVALID_ARG;
-  if (policy < ENTMAXKV_POLICY_FULL || policy > ENTMAXKV_POLICY_SOFTMAX) return ENTMAXKV_ERR_INVALID_ARG;
+  if (policy < ENTMAXKV_POLICY_FULL || policy > ENTMAXKV_POLICY_SOFTMAX_TOPK) return ENTMAXKV_ERR_INVALID_ARG;
   const int Hkv = c->num_kv_heads, G = c->group, Hq = Hkv * G, D = c->head_dim, P = c->page_size;
   const int maxp = c->max_pages_per_seq;
   memset(&L, 0, sizeof(L));
@@ -54,7 +54,8 @@ static int compute_layout(const entmaxkv_config* c, int S, int policy, int budge
   L.kpages = 0;
   L.gcap = 0;
   int cap = maxp;
-  if (policy == ENTMAXKV_POLICY_TOPK) {
+  const bool topk = policy == ENTMAXKV_POLICY_TOPK || policy == ENTMAXKV_POLICY_SOFTMAX_TOPK;
+  if (topk) {
     if (budget < P) return ENTMAXKV_ERR_INVALID_ARG;
     L.kpages = budget / P;
     cap = L.kpages < maxp ? L.kpages : maxp;
@@ -71,13 +72,13 @@ static int compute_layout(const entmaxkv_config* c, int S, int policy, int budge
   long long splits = (cap + 7) / 8;
   long long tgt = (kTargetBlocks + units - 1) / units;
   if (splits > tgt) splits = tgt;
-  const bool bitmap = policy == ENTMAXKV_POLICY_TOPK || policy == ENTMAXKV_POLICY_GAUSSIAN;
+  const bool bitmap = topk || policy == ENTMAXKV_POLICY_GAUSSIAN;
   const long long need = (cap + kListCap - 1) / kListCap;
   if (bitmap && splits < need) splits = need;
   if (splits < 1) splits = 1;
   if (splits > 65535) return ENTMAXKV_ERR_UNSUPPORTED;
   L.splits = (int)splits;
-  const bool entmax = policy != ENTMAXKV_POLICY_SOFTMAX;
+  const bool entmax = policy != ENTMAXKV_POLICY_SOFTMAX && policy != ENTMAXKV_POLICY_SOFTMAX_TOPK;
   const size_t nq = (size_t)S * Hq, nk = (size_t)S * Hkv;
   size_t off = 0;
   auto take = [&](size_t bytes) { size_t o = off; off = up256(off + bytes); return o; };
@@ -94,8 +95,8 @@ static int compute_layout(const entmaxkv_config* c, int S, int policy, int budge
   L.tau_ws = take(nq * 8);
   L.nsel_ws = take(nk * 4);
   L.sel_list = bitmap ? take(nk * (size_t)cap * 4) : none;
-  L.bbox_u = policy == ENTMAXKV_POLICY_TOPK ? take(nq * (size_t)maxp * 4) : none;
-  L.bbox_uhat = policy == ENTMAXKV_POLICY_TOPK ? take(nk * (size_t)maxp * 4) : none;
+  L.bbox_u = topk ? take(nq * (size_t)maxp * 4) : none;
+  L.bbox_uhat = topk ? take(nk * (size_t)maxp * 4) : none;
   L.gauss_ms = policy == ENTMAXKV_POLICY_GAUSSIAN ? take(nq * (size_t)maxp * 8) : none;
   L.sel_pp = entmax ? take(nk * (size_t)cap * 8) : none;
   L.vlist = entmax ? take(nk * (size_t)cap * 16) : none;
@@ -103,7 +104,7 @@ static int compute_layout(const entmaxkv_config* c, int S, int policy, int budge
   L.cand = entmax ? take(nq * (size_t)cap * 8) : none;
   L.z = entmax ? take(nk * (size_t)cap * P * G * 4) : none;
   L.pmax = entmax ? take(nk * (size_t)cap * G * 4) : none;
-  L.pstride = (G * D + 2 * G + 3) & ~3;
+  L.pstride = (G * D + 4 * G + 3) & ~3;  // acc [G][D], then 4 floats per head
   L.partial = take(nk * (size_t)L.splits * L.pstride * 4);
   L.diag = take(nq * 4);
   L.mslots = gauss_grid_x(maxp, Hkv, S, kSmCount);
@@ -153,6 +154,11 @@ static void bind_workspace(DecodeArgs& a, void* ws, const Layout& L) {
   a.ctrl_vec = (int)(L.ctrl_end / 16);
 }
 
+// The full-cache policy whose result defines the exact dropped mass.
+static int full_policy_of(int policy) {
+  return policy == ENTMAXKV_POLICY_SOFTMAX_TOPK ? ENTMAXKV_POLICY_SOFTMAX : ENTMAXKV_POLICY_FULL;
+}
+
 // Bytes of the workspace with the given flags (0 for an invalid
 // configuration); L gets the policy's layout, LF the full-cache one that the
 // exact dropped mass needs.
@@ -162,7 +168,7 @@ static size_t total_bytes(const entmaxkv_config* c, int S, int policy, int budge
   if (!(flags & ENTMAXKV_FLAG_EXACT_DELTA) || policy == ENTMAXKV_POLICY_SOFTMAX ||
       policy == ENTMAXKV_POLICY_FULL)
     return L.total;
-  if (compute_layout(c, S, ENTMAXKV_POLICY_FULL, 0, LF) != ENTMAXKV_OK) return 0;
+  if (compute_layout(c, S, full_policy_of(policy), 0, LF) != ENTMAXKV_OK) return 0;
   return up256(L.total) + LF.total;
 }
 
@@ -203,6 +209,7 @@ int32_t entmaxkv_delta_kind(int32_t policy, uint32_t flags) {
     case ENTMAXKV_POLICY_FULL:
     case ENTMAXKV_POLICY_SOFTMAX: return ENTMAXKV_DELTA_ZERO;
     case ENTMAXKV_POLICY_TOPK:
+    case ENTMAXKV_POLICY_SOFTMAX_TOPK:
       return (flags & ENTMAXKV_FLAG_EXACT_DELTA) ? ENTMAXKV_DELTA_EXACT : ENTMAXKV_DELTA_CERTIFIED;
     case ENTMAXKV_POLICY_GAUSSIAN:
       return (flags & ENTMAXKV_FLAG_EXACT_DELTA) ? ENTMAXKV_DELTA_EXACT : ENTMAXKV_DELTA_MODEL;
@@ -287,7 +294,9 @@ static int32_t decode_impl(const entmaxkv_config* cfg, const entmaxkv_cache* cac
   if (n_seqs < 0) return ENTMAXKV_ERR_INVALID_ARG;
   if (n_seqs == 0) return ENTMAXKV_OK;
   if (!q || !out) return ENTMAXKV_ERR_INVALID_ARG;
-  if (policy != ENTMAXKV_POLICY_SOFTMAX && !(alpha > 1.0f && isfinite(alpha)))
+  const bool soft = policy == ENTMAXKV_POLICY_SOFTMAX || policy == ENTMAXKV_POLICY_SOFTMAX_TOPK;
+  const bool topk = policy == ENTMAXKV_POLICY_TOPK || policy == ENTMAXKV_POLICY_SOFTMAX_TOPK;
+  if (!soft && !(alpha > 1.0f && isfinite(alpha)))
     return ENTMAXKV_ERR_INVALID_ARG;
   if (policy == ENTMAXKV_POLICY_GAUSSIAN) {
     if (!isfinite(margin)) return ENTMAXKV_ERR_INVALID_ARG;
@@ -319,7 +328,7 @@ static int32_t decode_impl(const entmaxkv_config* cfg, const entmaxkv_cache* cac
   a.kpages = L.kpages;
   a.gcap = L.gcap;
   a.flags = flags;
-  const float al = policy == ENTMAXKV_POLICY_SOFTMAX ? 2.0f : alpha;
+  const float al = soft ? 2.0f : alpha;
   a.alpha = al;
   a.a1 = al - 1.0f;
   a.beta = (float)(1.0 / ((double)al - 1.0));
@@ -351,19 +360,19 @@ static int32_t decode_impl(const entmaxkv_config* cfg, const entmaxkv_cache* cac
   };
   cudaError_t e = mark(0);
   // The selective policies' first kernel clears the control words itself.
-  if (e == cudaSuccess && policy != ENTMAXKV_POLICY_TOPK && policy != ENTMAXKV_POLICY_GAUSSIAN)
+  if (e == cudaSuccess && !topk && policy != ENTMAXKV_POLICY_GAUSSIAN)
     e = cudaMemsetAsync(workspace, 0, L.ctrl_end, s);
   if (e == cudaSuccess) e = mark(1);
   const int dt = cfg->kv_dtype;
   // stage 1: page scoring
   if (e == cudaSuccess) {
-    if (policy == ENTMAXKV_POLICY_TOPK) e = launch_bbox(a, dt, kSmCount, s);
+    if (topk) e = launch_bbox(a, dt, kSmCount, s);
     else if (policy == ENTMAXKV_POLICY_GAUSSIAN) e = launch_gauss(a, dt, kSmCount, s);
   }
   if (e == cudaSuccess) e = mark(2);
   // stage 2: selection
   if (e == cudaSuccess) {
-    if (policy == ENTMAXKV_POLICY_TOPK) {
+    if (topk) {
       e = launch_topk(a, 0, s);
     } else if (policy == ENTMAXKV_POLICY_GAUSSIAN) {
       e = launch_tauhat(a, s);
@@ -372,17 +381,19 @@ static int32_t decode_impl(const entmaxkv_config* cfg, const entmaxkv_cache* cac
   }
   if (e == cudaSuccess) e = mark(3);
   // stage 3: pass A
-  if (e == cudaSuccess && policy != ENTMAXKV_POLICY_SOFTMAX) e = launch_pass_a(a, dt, s);
+  if (e == cudaSuccess && !soft) e = launch_pass_a(a, dt, s);
   if (e == cudaSuccess) e = mark(4);
   // stage 4: pass B or the softmax kernel
-  if (e == cudaSuccess) e = policy == ENTMAXKV_POLICY_SOFTMAX ? launch_softmax(a, dt, s) : launch_pass_b(a, dt, s);
+  if (e == cudaSuccess) e = soft ? launch_softmax(a, dt, s) : launch_pass_b(a, dt, s);
   if (e == cudaSuccess) e = mark(5);
-  // exact dropped mass: full-cache pass A in the second region, then the
-  // full-cache weights of the kept pages' tokens
+  // exact dropped mass: the full-cache solve in the second region (entmax:
+  // pass A, for τ and z of every page; softmax: the full softmax, for its
+  // log-normaliser), then the dropped mass from both
   if (e == cudaSuccess && exact_delta) {
     void* ws2 = static_cast<char*>(workspace) + up256(L.total);
     DecodeArgs f = a;
-    f.policy = ENTMAXKV_POLICY_FULL;
+    f.policy = full_policy_of(policy);
+    f.out = static_cast<float*>(nullptr);
     f.flags = 0;
     f.page_ids = nullptr;
     f.n_sel_out = nullptr;
@@ -390,7 +401,7 @@ static int32_t decode_impl(const entmaxkv_config* cfg, const entmaxkv_cache* cac
     f.delta_out = nullptr;
     bind_workspace(f, ws2, LF);
     e = cudaMemsetAsync(ws2, 0, LF.ctrl_end, s);
-    if (e == cudaSuccess) e = launch_pass_a(f, dt, s);
+    if (e == cudaSuccess) e = soft ? launch_softmax(f, dt, s) : launch_pass_a(f, dt, s);
     if (e == cudaSuccess) e = launch_exact_delta(a, f, s);
   }
   return e == cudaSuccess ? ENTMAXKV_OK : ENTMAXKV_ERR_CUDA;

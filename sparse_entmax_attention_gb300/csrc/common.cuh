@@ -408,6 +408,47 @@ inline cudaError_t launch_k(bool pdl, void (*kernel)(KArgs...), dim3 grid, dim3 
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
+// Policies whose selection is a bitmap of pages (top-k, Gaussian, softmax top-k).
+__device__ __forceinline__ bool uses_bitmap(int policy) {
+  return policy == ENTMAXKV_POLICY_TOPK || policy == ENTMAXKV_POLICY_GAUSSIAN ||
+         policy == ENTMAXKV_POLICY_SOFTMAX_TOPK;
+}
+
+// This block's share [lo, hi) of the n_sel selected pages; for bitmap
+// policies the page ids of that share go to list[0 .. hi−lo).
+__device__ __forceinline__ void block_page_range(const DecodeArgs& a, int s, int kvh, int n_pages, int split,
+                                 int* list, int* sh_scan, int& n_sel, int& lo, int& hi) {
+  if (!uses_bitmap(a.policy)) {
+    n_sel = n_pages;
+    lo = (int)(((long long)n_sel * split) / a.splits);
+    hi = (int)(((long long)n_sel * (split + 1)) / a.splits);
+    return;
+  }
+  const uint32_t* bm = a.bitmap + ((size_t)s * a.Hkv + kvh) * a.words;
+  const int W = (n_pages + 31) / 32;
+  const int wpt = (W + kThreads - 1) / kThreads;
+  const int w0 = threadIdx.x * wpt;
+  int cnt = 0;
+  for (int j = 0; j < wpt; ++j)
+    if (w0 + j < W) cnt += __popc(bm[w0 + j]);
+  int total;
+  int r = block_exclusive_scan(cnt, sh_scan, total);
+  n_sel = total;
+  lo = (int)(((long long)n_sel * split) / a.splits);
+  hi = (int)(((long long)n_sel * (split + 1)) / a.splits);
+  for (int j = 0; j < wpt; ++j) {
+    if (w0 + j >= W || r >= hi) break;
+    uint32_t bits = bm[w0 + j];
+    while (bits) {
+      const int b = __ffs(bits) - 1;
+      if (r >= lo && r < hi) list[r - lo] = (w0 + j) * 32 + b;
+      ++r;
+      bits &= bits - 1u;
+    }
+  }
+  __syncthreads();
+}
+
 // Launchers (one translation unit each).
 cudaError_t launch_append(const AppendArgs& a, int kv_dtype, cudaStream_t st);
 cudaError_t launch_bbox(const DecodeArgs& a, int kv_dtype, int sms, cudaStream_t st);

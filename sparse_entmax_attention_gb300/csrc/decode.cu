@@ -29,45 +29,6 @@ namespace ekv {
 
 constexpr int kTauIters = 64;
 
-__device__ __forceinline__ bool uses_bitmap(int policy) {
-  return policy == ENTMAXKV_POLICY_TOPK || policy == ENTMAXKV_POLICY_GAUSSIAN;
-}
-
-// This block's share [lo, hi) of the n_sel selected pages; for bitmap
-// policies the page ids of that share go to list[0 .. hi−lo).
-__device__ void block_page_range(const DecodeArgs& a, int s, int kvh, int n_pages, int split,
-                                 int* list, int* sh_scan, int& n_sel, int& lo, int& hi) {
-  if (!uses_bitmap(a.policy)) {
-    n_sel = n_pages;
-    lo = (int)(((long long)n_sel * split) / a.splits);
-    hi = (int)(((long long)n_sel * (split + 1)) / a.splits);
-    return;
-  }
-  const uint32_t* bm = a.bitmap + ((size_t)s * a.Hkv + kvh) * a.words;
-  const int W = (n_pages + 31) / 32;
-  const int wpt = (W + kThreads - 1) / kThreads;
-  const int w0 = threadIdx.x * wpt;
-  int cnt = 0;
-  for (int j = 0; j < wpt; ++j)
-    if (w0 + j < W) cnt += __popc(bm[w0 + j]);
-  int total;
-  int r = block_exclusive_scan(cnt, sh_scan, total);
-  n_sel = total;
-  lo = (int)(((long long)n_sel * split) / a.splits);
-  hi = (int)(((long long)n_sel * (split + 1)) / a.splits);
-  for (int j = 0; j < wpt; ++j) {
-    if (w0 + j >= W || r >= hi) break;
-    uint32_t bits = bm[w0 + j];
-    while (bits) {
-      const int b = __ffs(bits) - 1;
-      if (r >= lo && r < hi) list[r - lo] = (w0 + j) * 32 + b;
-      ++r;
-      bits &= bits - 1u;
-    }
-  }
-  __syncthreads();
-}
-
 // ---------------------------------------------------------------------------
 // Exact τ of one query head by one warp. Candidates are the scores above
 // T0 = z_max − 1 (no other score can carry weight); normally they sit in
@@ -969,11 +930,14 @@ __global__ void __launch_bounds__(kThreads, GP <= 4 ? 2 : 1) pass_b_kernel(Decod
 
 // ---------------------------------------------------------------------------
 
-// Exact dropped mass (summary §3): with τ and z of the full-cache solve in
-// f's workspace and the kept pages of the decode in m's, one block per
-// (sequence, KV head) sums p_i^full = [z_i − τ_full]_+^β over the kept pages'
-// tokens (a warp per page, lanes over tokens) and writes
-// δ = max(0, 1 − Σ kept p_i^full) for every query head of the group.
+// Exact dropped mass (summary §3).
+// - Softmax over the top-k pages: δ = 1 − exp(lse_kept − lse_full), from the
+//   two log-normalisers.
+// - Entmax: with τ and z of the full-cache solve in f's workspace and the
+//   kept pages of the decode in m's, one block per (sequence, KV head) sums
+//   p_i^full = [z_i − τ_full]_+^β over the kept pages' tokens (a warp per
+//   page, lanes over tokens) and writes δ = max(0, 1 − Σ kept p_i^full) for
+//   every query head of the group.
 __global__ void __launch_bounds__(kThreads) exact_delta_kernel(DecodeArgs m, DecodeArgs f) {
   pdl_enter();
   __shared__ float part[kWarps][8];
@@ -986,6 +950,14 @@ __global__ void __launch_bounds__(kThreads) exact_delta_kernel(DecodeArgs m, Dec
   const size_t skv = (size_t)s * m.Hkv + kvh;
   const size_t hq0 = (size_t)s * m.Hq + (size_t)kvh * G;
   const bool bitmap = uses_bitmap(m.policy);
+  if (m.policy == ENTMAXKV_POLICY_SOFTMAX_TOPK) {
+    // softmax: the kept share of the full normaliser is exp(lse_kept − lse_full)
+    if (tid < G && m.delta_out) {
+      const double lk = __ldcg(&m.tau_ws[hq0 + tid]), lf = __ldcg(&f.tau_ws[hq0 + tid]);
+      m.delta_out[hq0 + tid] = isnan(lf) ? 0.0f : (isnan(lk) ? 1.0f : (float)fmax(0.0, -expm1(lk - lf)));
+    }
+    return;
+  }
   const int n_sel = bitmap ? __ldcg(&m.nsel_ws[skv]) : n_pages;
   double tau[8];
   float acc[8];

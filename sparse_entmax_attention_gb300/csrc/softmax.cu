@@ -7,6 +7,14 @@
 // Σ 2^{s−m} v) per query head in the base-2 domain, the block merges its warps
 // and writes (m, l, acc) as a partial, and the last block to finish merges the
 // partials in split order. The "τ" output carries log Σ_i exp(s_i).
+//
+// With ENTMAXKV_POLICY_SOFTMAX_TOPK the same kernel runs over the top-k
+// selected pages only (the softmax side of the summary's comparison at equal
+// budget), and δ is certified: the full normaliser A + B has B, the mass of
+// the dropped tokens, at most B̄ = Σ_dropped n_p·e^{U_p} (every token of page
+// p scores ≤ U_p), and δ = B/(A + B) grows in B, so δ ≤ D/(1 + D) with
+// D = B̄/A. Each block also folds its share of the dropped pages into a
+// per-head (max, Σ n_p·e^{U_p − max}) pair that the last block merges.
 #include "common.cuh"
 
 #include "page_scores.cuh"
@@ -19,13 +27,21 @@ __global__ void __launch_bounds__(kThreads, 2) softmax_kernel(DecodeArgs a) {
   constexpr int VEC = 16 / sizeof(T), LPR = D / VEC, TG = 32 / LPR;
   constexpr int MAXT = 32 / TG;                  // tokens per lane in a 32-token page
   constexpr int CH = MAXT < 8 ? MAXT : 8;        // V rows in flight per lane
-  __shared__ float qs[8][D];
-  __shared__ float sbuf[kWarps][32][GP];
+  // q and the page scores live during the page loop, the per-warp sums after
+  // it: one buffer, with a barrier between the two uses
+  constexpr int kLoopFloats = 8 * D + kWarps * 32 * GP, kRedFloats = kWarps * GP * D;
+  __shared__ __align__(16) float buf_sm[kLoopFloats > kRedFloats ? kLoopFloats : kRedFloats];
+  float(*qs)[D] = reinterpret_cast<float(*)[D]>(buf_sm);
+  float(*sbuf)[32][GP] = reinterpret_cast<float(*)[32][GP]>(buf_sm + 8 * D);
+  float(*red)[GP][D] = reinterpret_cast<float(*)[GP][D]>(buf_sm);
   __shared__ float pmx[kWarps][8];
-  __shared__ __align__(16) float red[kWarps][GP][D];
   __shared__ float wm_sh[kWarps][GP], wl_sh[kWarps][GP];
   __shared__ float4 red4[kThreads];
   __shared__ float Mg_sh[8], Lg_sh[8];
+  __shared__ float um_sh[kWarps][8], us_sh[kWarps][8];
+  static_assert(sizeof(red4) >= kListCap * sizeof(int), "the page list shares the combine scratch");
+  int* list = reinterpret_cast<int*>(red4);  // the page list is done before the combine starts
+  __shared__ int sh_scan[32];
   __shared__ int last_sh;
   const int split = blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -34,13 +50,15 @@ __global__ void __launch_bounds__(kThreads, 2) softmax_kernel(DecodeArgs a) {
   const int seq = seq_row(a.seq_ids, s, a.max_seqs, tid == 0 ? a.status : nullptr);
   const int L = seq_len_clamped(a.seq_lens, seq, a.maxp, P, tid == 0 ? a.status : nullptr);
   const int n_pages = (L + P - 1) / P;
-  const int lo = (int)(((long long)n_pages * split) / a.splits);
-  const int hi = (int)(((long long)n_pages * (split + 1)) / a.splits);
+  const bool bitmap = uses_bitmap(a.policy);  // softmax over the top-k pages
+  int n_sel, lo, hi;
+  block_page_range(a, s, kvh, n_pages, split, list, sh_scan, n_sel, lo, hi);
   const size_t skv = (size_t)s * a.Hkv + kvh;
   const size_t hq0 = (size_t)s * a.Hq + (size_t)kvh * G;
-  if (split == 0 && tid == 0 && a.n_sel_out) a.n_sel_out[skv] = n_pages;
+  if (split == 0 && tid == 0 && a.n_sel_out) a.n_sel_out[skv] = n_sel;
   if (a.page_ids)
-    for (int p = lo + tid; p < hi; p += kThreads) a.page_ids[skv * a.page_ids_stride + p] = p;
+    for (int i = tid; i < hi - lo; i += kThreads)
+      a.page_ids[skv * a.page_ids_stride + lo + i] = bitmap ? list[i] : lo + i;
   const float scale2 = a.inv_sqrt_d * 1.4426950408889634f;  // scores in log2 units
   uint32_t bq[D / 16][2];
   if constexpr (sizeof(T) == 2) {
@@ -57,7 +75,8 @@ __global__ void __launch_bounds__(kThreads, 2) softmax_kernel(DecodeArgs a) {
 #pragma unroll
     for (int j = 0; j < VEC; ++j) acc[h][j] = 0.0f;
   }
-  for (int page = lo + warp; page < hi; page += kWarps) {
+  for (int i = warp; i < hi - lo; i += kWarps) {
+    const int page = bitmap ? list[i] : lo + i;
     const int ph = phys_page(a.block_table, seq, page, a.maxp, a.nphys, lane == 0 ? a.status : nullptr);
     if (ph < 0) continue;
     const int nv = min(P, L - page * P);
@@ -155,6 +174,7 @@ __global__ void __launch_bounds__(kThreads, 2) softmax_kernel(DecodeArgs a) {
 #pragma unroll
       for (int j = 0; j < VEC; ++j) acc[h][j] += __shfl_xor_sync(0xffffffffu, acc[h][j], o);
     }
+  __syncthreads();  // every warp is done with qs and sbuf
   if (tg == 0) {
 #pragma unroll
     for (int h = 0; h < GP; ++h)
@@ -166,6 +186,42 @@ __global__ void __launch_bounds__(kThreads, 2) softmax_kernel(DecodeArgs a) {
     for (int h = 0; h < GP; ++h) {
       wm_sh[warp][h] = m[h];
       wl_sh[warp][h] = l[h];
+    }
+  }
+  if (bitmap) {  // this block's share of all pages: the dropped ones' Σ n_p·e^{U_p}, online
+    float um[GP], us[GP];
+#pragma unroll
+    for (int h = 0; h < GP; ++h) {
+      um[h] = -CUDART_INF_F;
+      us[h] = 0.0f;
+    }
+    const uint32_t* bm = a.bitmap + skv * a.words;
+    const int plo = (int)(((long long)n_pages * split) / a.splits);
+    const int phi = (int)(((long long)n_pages * (split + 1)) / a.splits);
+    for (int p = plo + tid; p < phi; p += kThreads) {
+      if ((bm[p >> 5] >> (p & 31)) & 1u) continue;
+      const float np = (float)min(P, L - p * P);
+#pragma unroll
+      for (int h = 0; h < GP; ++h) {
+        if (h < G) {
+          const float u = a.bbox_u[(hq0 + h) * a.maxp + p];
+          if (u > um[h]) {
+            us[h] = us[h] * expf(um[h] - u) + np;
+            um[h] = u;
+          } else {
+            us[h] += np * expf(u - um[h]);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < GP; ++h) {  // merge the warp's (max, sum) pairs
+      float M = warp_max(um[h]);
+      const float sw = warp_sum(um[h] > -CUDART_INF_F ? us[h] * expf(um[h] - M) : 0.0f);
+      if (lane == 0) {
+        um_sh[warp][h] = M;
+        us_sh[warp][h] = sw;
+      }
     }
   }
   __syncthreads();
@@ -185,6 +241,14 @@ __global__ void __launch_bounds__(kThreads, 2) softmax_kernel(DecodeArgs a) {
       part[G * D + h] = M;
       part[G * D + G + h] = sum;
     }
+  }
+  if (bitmap && tid < G) {
+    float M = -CUDART_INF_F, sum = 0.0f;
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, um_sh[w][tid]);
+    for (int w = 0; w < kWarps; ++w)
+      if (um_sh[w][tid] > -CUDART_INF_F) sum += us_sh[w][tid] * expf(um_sh[w][tid] - M);
+    part[G * D + 2 * G + tid] = M;
+    part[G * D + 3 * G + tid] = sum;
   }
   __threadfence();
   __syncthreads();
@@ -243,14 +307,28 @@ __global__ void __launch_bounds__(kThreads, 2) softmax_kernel(DecodeArgs a) {
     }
     const float Lg = Lg_sh[h];
     const float inv = Lg > 0.0f ? 1.0f / Lg : 0.0f;
-    reinterpret_cast<float4*>(a.out + hq0 * D)[tid] =
-        make_float4(sum.x * inv, sum.y * inv, sum.z * inv, sum.w * inv);
+    if (a.out)
+      reinterpret_cast<float4*>(a.out + hq0 * D)[tid] =
+          make_float4(sum.x * inv, sum.y * inv, sum.z * inv, sum.w * inv);
   }
   if (tid < G) {
     const float Lg = Lg_sh[tid], Mg = Mg_sh[tid];
     const float lse = Lg > 0.0f ? (Mg + log2f(Lg)) * 0.6931471805599453f : CUDART_NAN_F;
+    a.tau_ws[hq0 + tid] = lse;
     if (a.tau_out) a.tau_out[hq0 + tid] = lse;
-    if (a.delta_out) a.delta_out[hq0 + tid] = 0.0f;
+    if (a.delta_out) {
+      float dl = 0.0f;
+      if (bitmap && L > 0) {  // certified D/(1 + D); all dropped when nothing was kept
+        double Dd = 0.0;
+        for (int sp = 0; sp < a.splits; ++sp) {
+          const float um = __ldcg(base + (size_t)sp * a.pstride + G * D + 2 * G + tid);
+          if (um > -CUDART_INF_F)
+            Dd += (double)__ldcg(base + (size_t)sp * a.pstride + G * D + 3 * G + tid) * exp((double)um - (double)lse);
+        }
+        dl = Lg > 0.0f ? (float)(Dd / (1.0 + Dd)) : 1.0f;
+      }
+      a.delta_out[hq0 + tid] = dl;
+    }
   }
 }
 

@@ -66,7 +66,7 @@ def _decode(lib, cfg, **kw):
 
 def test_workspace_sizing(lib):
     cfg = _cfg()
-    sizes = {p: lib.entmaxkv_workspace_bytes(ctypes.byref(cfg), 1, p, 2048) for p in range(4)}
+    sizes = {p: lib.entmaxkv_workspace_bytes(ctypes.byref(cfg), 1, p, 2048) for p in range(5)}
     assert all(v > 0 for v in sizes.values())
     assert sizes[B.POLICY_TOPK] < sizes[B.POLICY_FULL]
     assert lib.entmaxkv_workspace_bytes(ctypes.byref(cfg), 1, B.POLICY_TOPK, 16) == 0  # < 1 page
@@ -141,6 +141,8 @@ def test_exact_delta_sizing_and_delta_kinds(lib):
     assert (k(B.POLICY_FULL, 0), k(B.POLICY_SOFTMAX, B.FLAG_EXACT_DELTA)) == (B.DELTA_ZERO, B.DELTA_ZERO)
     assert (k(B.POLICY_TOPK, 0), k(B.POLICY_GAUSSIAN, 0)) == (B.DELTA_CERTIFIED, B.DELTA_MODEL)
     assert k(B.POLICY_TOPK, B.FLAG_EXACT_DELTA) == B.DELTA_EXACT == k(B.POLICY_GAUSSIAN, B.FLAG_EXACT_DELTA)
+    assert k(B.POLICY_SOFTMAX_TOPK, 0) == B.DELTA_CERTIFIED
+    assert k(B.POLICY_SOFTMAX_TOPK, B.FLAG_EXACT_DELTA) == B.DELTA_EXACT
     assert k(9, 0) == -1
 
 

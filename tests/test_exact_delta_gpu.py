@@ -36,18 +36,20 @@ def built_f32():
     return Built(synth.workload("single-head-d64-4k-p16-fp32"))
 
 
-def _exact_delta_on(K, Q, alpha, P, page_ids):
-    """Full-cache entmax mass outside the given pages, per query head."""
+def _exact_delta_on(K, Q, alpha, P, page_ids, soft=False):
+    """Full-cache entmax (softmax with ``soft``) mass outside the given pages,
+    per query head."""
     keep = np.zeros(K.shape[0], bool)
     for p in page_ids:
         keep[p * P:(p + 1) * P] = True
     s = K @ Q.T / np.sqrt(K.shape[1])
-    return np.array([oem.entmax(s[:, h], alpha)[0][~keep].sum() for h in range(Q.shape[0])])
+    full = (lambda x: oem.softmax(x)) if soft else (lambda x: oem.entmax(x, alpha))
+    return np.array([full(s[:, h])[0][~keep].sum() for h in range(Q.shape[0])])
 
 
 @pytest.mark.parametrize("policy,budget,margin,alpha", [
     ("topk", 256, 0.0, 1.5), ("topk", 512, 0.0, 2.0), ("gaussian", 0, 0.5, 1.5),
-    ("gaussian", 0, 0.0, 2.0)])
+    ("gaussian", 0, 0.0, 2.0), ("softmax_topk", 256, 0.0, 1.5)])
 @pytest.mark.parametrize("which", ["bf16", "f32"])
 def test_exact_delta_matches_oracle(built_bf16, built_f32, which, policy, budget, margin, alpha):
     built = built_bf16 if which == "bf16" else built_f32
@@ -73,13 +75,13 @@ def test_exact_delta_matches_oracle(built_bf16, built_f32, which, policy, budget
             if list(got) == list(r["page_ids"]):
                 want = r["delta_exact"]
             else:
-                want = _exact_delta_on(K, Q, alpha, P, got)
+                want = _exact_delta_on(K, Q, alpha, P, got, soft=policy == "softmax_topk")
             np.testing.assert_allclose(delta[b, j * g:(j + 1) * g], want, atol=TOL_DELTA, rtol=0)
 
 
 def test_exact_delta_workspace_and_kinds(built_f32):
     c = built_f32.cache
-    for pol in ("topk", "gaussian"):
+    for pol in ("topk", "gaussian", "softmax_topk"):
         assert B.workspace_bytes(c, 1, pol, 256, B.FLAG_EXACT_DELTA) > B.workspace_bytes(c, 1, pol, 256)
     for pol in ("full", "softmax"):
         assert B.workspace_bytes(c, 1, pol, 0, B.FLAG_EXACT_DELTA) == B.workspace_bytes(c, 1, pol, 0)

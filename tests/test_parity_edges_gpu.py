@@ -27,7 +27,8 @@ def ragged():
 
 
 @pytest.mark.parametrize("policy,budget", [("full", 0), ("softmax", 0), ("topk", 64),
-                                           ("topk", 100000), ("gaussian", 0)])
+                                           ("topk", 100000), ("gaussian", 0),
+                                           ("softmax_topk", 64)])
 def test_empty_and_tiny_sequences(ragged, policy, budget):
     o, _ = check_decode(ragged, policy, 1.5, budget, 0.5, units=[(1, 0), (2, 0), (3, 0)])
     # the empty sequence: zero output, NaN τ, nothing selected, no dropped mass

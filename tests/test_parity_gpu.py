@@ -65,14 +65,14 @@ def check_decode(built, policy, alpha=1.5, budget=0, margin=0.0, flags=0, q=None
             assert n_sel[b, j] == len(want)
         if list(got_ids) != list(want):
             diff = set(got_ids.tolist()) ^ set(want.tolist())
-            if policy == "topk":
+            if policy in ("topk", "softmax_topk"):
                 allowed = near_tie_topk(r["uhat"], budget // P)
             else:
                 eps = TOL_TAU / (alpha - 1.0) + 1e-5 * max(1.0, float(np.abs(r["thr"]).max()))
                 allowed = near_tie_gauss(r["mhat"], r["thr"], eps)
             assert diff <= allowed, (b, j, sorted(diff - allowed)[:10])
             near += len(diff)
-            ref_out, ref_tau = odec.attend_pages(K, V, Q, alpha, P, got_ids)
+            ref_out, ref_tau = odec.attend_pages(K, V, Q, alpha, P, got_ids, softmax=policy == "softmax_topk")
         else:
             ref_out, ref_tau = r["out"], r["tau"]
         assert np.all(np.diff(got_ids) > 0)
@@ -87,7 +87,7 @@ def check_decode(built, policy, alpha=1.5, budget=0, margin=0.0, flags=0, q=None
             assert np.all(delta[b, hs] == 0.0)
         elif list(got_ids) == list(want):
             np.testing.assert_allclose(delta[b, hs], r["delta"], atol=2e-4, rtol=2e-3)
-        if check_intermediates and policy == "topk":
+        if check_intermediates and policy in ("topk", "softmax_topk"):
             U = _ws_array(ws, view.bbox_u, torch.float32, (S, spec.num_q_heads, maxp)).numpy()
             n_pages = len(r["uhat"])
             np.testing.assert_allclose(U[b, hs, :n_pages], r["U"], rtol=1e-5, atol=1e-4)
@@ -147,6 +147,7 @@ def test_append_metadata(small_bf16, small_f32):
 
 @pytest.mark.parametrize("policy,budget,margin", [
     ("full", 0, 0.0), ("softmax", 0, 0.0), ("topk", 256, 0.0), ("topk", 512, 0.0),
+    ("softmax_topk", 256, 0.0),
     ("gaussian", 0, 0.0), ("gaussian", 0, 0.5), ("gaussian", 0, 1.0)])
 @pytest.mark.parametrize("alpha", [1.5, 2.0])
 def test_decode_small_bf16(small_bf16, policy, budget, margin, alpha):
@@ -156,13 +157,15 @@ def test_decode_small_bf16(small_bf16, policy, budget, margin, alpha):
 
 
 @pytest.mark.parametrize("policy,budget,margin", [
-    ("full", 0, 0.0), ("softmax", 0, 0.0), ("topk", 1024, 0.0), ("gaussian", 0, 0.5)])
+    ("full", 0, 0.0), ("softmax", 0, 0.0), ("topk", 1024, 0.0), ("gaussian", 0, 0.5),
+    ("softmax_topk", 1024, 0.0)])
 def test_decode_small_bf16_p32(small_bf16_p32, policy, budget, margin):
     check_decode(small_bf16_p32, policy, 1.5, budget, margin)
 
 
 @pytest.mark.parametrize("policy,budget,margin", [
-    ("full", 0, 0.0), ("softmax", 0, 0.0), ("topk", 512, 0.0), ("gaussian", 0, 0.5)])
+    ("full", 0, 0.0), ("softmax", 0, 0.0), ("topk", 512, 0.0), ("gaussian", 0, 0.5),
+    ("softmax_topk", 512, 0.0)])
 @pytest.mark.parametrize("alpha", [1.5, 2.0, 1.25])
 def test_decode_single_head_fp32(small_f32, policy, budget, margin, alpha):
     if policy == "gaussian" and alpha not in (1.5, 2.0):

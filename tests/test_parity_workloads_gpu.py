@@ -24,7 +24,8 @@ def gqa32k():
 
 
 @pytest.mark.parametrize("policy,budget,margin", [
-    ("topk", 1024, 0.0), ("full", 0, 0.0), ("softmax", 0, 0.0), ("gaussian", 0, 0.5)])
+    ("topk", 1024, 0.0), ("full", 0, 0.0), ("softmax", 0, 0.0), ("gaussian", 0, 0.5),
+    ("softmax_topk", 1024, 0.0)])
 def test_gqa32k_all_heads(gqa32k, policy, budget, margin):
     check_decode(gqa32k, policy, 1.5, budget, margin)
 
@@ -53,7 +54,8 @@ def gqa1m():
 
 
 @pytest.mark.parametrize("policy,budget,margin", [
-    ("gaussian", 0, 0.5), ("topk", 2048, 0.0), ("full", 0, 0.0), ("softmax", 0, 0.0)])
+    ("gaussian", 0, 0.5), ("topk", 2048, 0.0), ("full", 0, 0.0), ("softmax", 0, 0.0),
+    ("softmax_topk", 2048, 0.0)])
 def test_gqa1m_sampled_heads(gqa1m, policy, budget, margin):
     check_decode(gqa1m, policy, 1.5, budget, margin, units=[(0, 0), (0, 7)])
 
