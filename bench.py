@@ -56,7 +56,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="headline step only")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--policies", default="gaussian,topk,full_dense,full_skipv,softmax",
+    ap.add_argument("--policies", default="gaussian,topk,softmax_topk,full_dense,full_skipv,softmax",
                     help="rows of the per-policy table")
     return ap.parse_args()
 
@@ -129,10 +129,13 @@ def algorithmic_bytes(wl, policy, o, ws, view):
     meta = 0
     if policy == "gaussian":
         meta = n_pages * Hkv * d * 4 * 2           # mean + m2, fp32
-    elif policy == "topk":
+    elif policy in ("topk", "softmax_topk"):
         meta = n_pages * Hkv * d * el * 2          # kmin + kmax
     n_sel = o.n_sel.cpu()
     k_pages = int(n_sel.sum())
+    if policy == "softmax_topk":                   # softmax reads V of every kept page
+        return meta + 2 * k_pages * page_kv + io, {"k_pages": k_pages, "v_pages": k_pages,
+                                                   "meta_bytes": meta}
     # V pages actually read: some head's page max z above its τ
     cap = view.cap_pages
     pm = ws[view.page_zmax: view.page_zmax + spec.batch * Hkv * cap * G * 4].view(torch.float32)
@@ -273,13 +276,14 @@ def run_ours(args, rank, world):
         "bytes_per_step": step_bytes,
         "selected": counts_g,
         "wall_s_timed_loop": round(wall, 4),
-        "gpu_launches": 6 * K,
+        "gpu_launches": 5 * K,  # per step: append, scoring, τ̂ + bits, pass A, pass B
         "clocks": clocks,
     }
     if rank != 0:
         return None
     if not args.no_extras:
         res["policies"] = policy_table(wl, B, flush, qbuf, timed, K, peaks, args.policies.split(","))
+        res["dropped_mass_exact"] = dropped_mass(wl, B, qbuf)
         res["roofline"] = roofline(wl, B, flush, qbuf, K, peaks, peak_kind)
         if not args.no_e2e:
             res["e2e"] = e2e(wl, B, toks, qs, n_app, K, W)
@@ -293,6 +297,7 @@ def policy_table(wl, B, flush, qbuf, timed, K, peaks, names):
     cache, spec = wl.cache, wl.spec
     rows = {}
     cases = [("gaussian", "gaussian", 0, 0), ("topk", "topk", TOPK_BUDGET, 0),
+             ("softmax_topk", "softmax_topk", TOPK_BUDGET, 0),
              ("full_dense", "full", 0, B.FLAG_DENSE_V), ("full_skipv", "full", 0, 0),
              ("softmax", "softmax", 0, 0)]
     for name, pol, budget, flags in cases:
@@ -320,10 +325,27 @@ def policy_table(wl, B, flush, qbuf, timed, K, peaks, names):
                       "frac_8tbs": round(nbytes / (mean * 1e-6) / 1e9 / NOMINAL_HBM_GBS, 4),
                       **counts}
         del ws
-    for name in ("topk", "full_dense", "full_skipv", "softmax"):
+    for name in ("topk", "softmax_topk", "full_dense", "full_skipv", "softmax"):
         if name in rows and "gaussian" in rows:
             rows[name]["gaussian_speedup"] = round(rows[name]["us"] / rows["gaussian"]["us"], 2)
     return rows
+
+
+def dropped_mass(wl, B, qbuf):
+    """Exact dropped mass δ per query head (untimed, ENTMAXKV_FLAG_EXACT_DELTA)
+    of entmax top-k, softmax top-k at the same budget, and the Gaussian
+    selector: how much of the full-cache attention each kept set loses."""
+    import torch
+    cache, spec = wl.cache, wl.spec
+    res = {"budget_tokens": TOPK_BUDGET}
+    for name, pol, budget in (("entmax_topk", "topk", TOPK_BUDGET),
+                              ("softmax_topk", "softmax_topk", TOPK_BUDGET), ("gaussian", "gaussian", 0)):
+        o = B.decode(cache, qbuf, ALPHA, pol, budget, MARGIN, B.FLAG_EXACT_DELTA)
+        torch.cuda.synchronize()
+        dl = o.delta.float().cpu()
+        res[name] = {"mean": round(float(dl.mean()), 5), "max": round(float(dl.max()), 5),
+                     "pages_per_kv_head": round(float(o.n_sel.float().mean()), 1)}
+    return res
 
 
 def roofline(wl, B, flush, qbuf, K, peaks, peak_kind):
