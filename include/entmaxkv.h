@@ -36,7 +36,7 @@
 extern "C" {
 #endif
 
-#define ENTMAXKV_VERSION 1
+#define ENTMAXKV_VERSION 2
 
 /* Return codes of every call. */
 typedef enum {
@@ -114,6 +114,12 @@ typedef struct {
  *   block_table    [max_seqs][max_pages_per_seq] int32: logical page → physical page
  *   seq_lens       [max_seqs] int32 valid tokens per sequence
  *   status         one uint32 the kernels OR ENTMAXKV_DEV_* bits into (may be NULL)
+ *   mean_bf16, m2_bf16  [num_phys_pages][num_kv_heads][head_dim] bfloat16, or both NULL:
+ *                  round-to-nearest-even copies of mean and m2, which append
+ *                  keeps in step. When present, the Gaussian scorer streams
+ *                  these instead of the fp32 arrays (half the bytes, summary §4:
+ *                  the cost moves to page selection). The fp32 arrays stay the
+ *                  ones appends merge into, so no rounding accumulates.
  * Metadata of a page covers its valid tokens only and is written by
  * entmaxkv_append; a partial last page holds n_p = len − P·(pages−1) tokens.
  * Every pool and metadata array starts on a 16-byte boundary (the kernels
@@ -130,6 +136,8 @@ typedef struct {
   const int32_t* block_table;
   int32_t* seq_lens;
   uint32_t* status;
+  void* mean_bf16;
+  void* m2_bf16;
 } entmaxkv_cache;
 
 /* Library version (ENTMAXKV_VERSION). */

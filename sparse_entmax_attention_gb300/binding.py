@@ -49,7 +49,8 @@ class CacheView(ctypes.Structure):
                 ("kmin", ctypes.c_void_p), ("kmax", ctypes.c_void_p),
                 ("mean", ctypes.c_void_p), ("m2", ctypes.c_void_p),
                 ("block_table", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p),
-                ("status", ctypes.c_void_p)]
+                ("status", ctypes.c_void_p), ("mean_bf16", ctypes.c_void_p),
+                ("m2_bf16", ctypes.c_void_p)]
 
 
 class WorkspaceView(ctypes.Structure):
@@ -126,10 +127,14 @@ _DT = {torch.float32: F32, torch.bfloat16: BF16}
 
 
 class PagedCache:
-    """Caller-owned paged KV cache plus per-page key metadata (torch memory)."""
+    """Caller-owned paged KV cache plus per-page key metadata (torch memory).
+
+    meta_bf16: also keep bf16 copies of the page means and m2, which the
+    Gaussian scorer then streams instead of the fp32 arrays.
+    """
 
     def __init__(self, num_kv_heads, group, head_dim, page_size, max_seqs, max_pages_per_seq,
-                 num_phys_pages, kv_dtype=torch.bfloat16, device="cuda"):
+                 num_phys_pages, kv_dtype=torch.bfloat16, device="cuda", meta_bf16=False):
         self.cfg = Config(num_kv_heads, group, head_dim, page_size, max_seqs,
                           max_pages_per_seq, num_phys_pages, _DT[kv_dtype])
         self.dtype, self.device = kv_dtype, torch.device(device)
@@ -143,10 +148,16 @@ class PagedCache:
         self.block_table = torch.zeros(max_seqs, max_pages_per_seq, dtype=torch.int32, device=device)
         self.seq_lens = torch.zeros(max_seqs, dtype=torch.int32, device=device)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        self.mean_bf16 = self.m2_bf16 = None
+        if meta_bf16:
+            self.mean_bf16 = torch.zeros(num_phys_pages, Hkv, d, dtype=torch.bfloat16, device=device)
+            self.m2_bf16 = torch.zeros_like(self.mean_bf16)
         self.view = CacheView(self.k_pool.data_ptr(), self.v_pool.data_ptr(), self.kmin.data_ptr(),
                               self.kmax.data_ptr(), self.mean.data_ptr(), self.m2.data_ptr(),
                               self.block_table.data_ptr(), self.seq_lens.data_ptr(),
-                              self.status.data_ptr())
+                              self.status.data_ptr(),
+                              self.mean_bf16.data_ptr() if meta_bf16 else None,
+                              self.m2_bf16.data_ptr() if meta_bf16 else None)
 
     @property
     def num_q_heads(self):

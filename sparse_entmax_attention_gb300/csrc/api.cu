@@ -36,7 +36,8 @@ static int check_cache(const entmaxkv_cache* k) {
   if (!k || !k->k_pool || !k->v_pool || !k->kmin || !k->kmax || !k->mean || !k->m2 ||
       !k->block_table || !k->seq_lens)
     return ENTMAXKV_ERR_INVALID_ARG;
-  const void* arrays[] = {k->k_pool, k->v_pool, k->kmin, k->kmax, k->mean, k->m2};
+  if ((k->mean_bf16 == nullptr) != (k->m2_bf16 == nullptr)) return ENTMAXKV_ERR_INVALID_ARG;
+  const void* arrays[] = {k->k_pool, k->v_pool, k->kmin, k->kmax, k->mean, k->m2, k->mean_bf16, k->m2_bf16};
   for (const void* p : arrays)
     if ((uintptr_t)p & 15u) return ENTMAXKV_ERR_INVALID_ARG;
   return ENTMAXKV_OK;
@@ -275,6 +276,8 @@ int32_t entmaxkv_append(const entmaxkv_config* cfg, const entmaxkv_cache* cache,
   a.kmax = cache->kmax;
   a.mean = cache->mean;
   a.m2 = cache->m2;
+  a.mean_lo = static_cast<__nv_bfloat16*>(cache->mean_bf16);
+  a.m2_lo = static_cast<__nv_bfloat16*>(cache->m2_bf16);
   a.block_table = cache->block_table;
   a.seq_lens = cache->seq_lens;
   a.status = cache->status;
@@ -341,6 +344,8 @@ static int32_t decode_impl(const entmaxkv_config* cfg, const entmaxkv_cache* cac
   a.kmax = cache->kmax;
   a.mean = cache->mean;
   a.m2 = cache->m2;
+  a.mean_lo = static_cast<const __nv_bfloat16*>(cache->mean_bf16);
+  a.m2_lo = static_cast<const __nv_bfloat16*>(cache->m2_bf16);
   a.block_table = cache->block_table;
   a.seq_lens = cache->seq_lens;
   a.status = cache->status;

@@ -108,6 +108,17 @@ __device__ __forceinline__ void append_page(const AppendArgs& a, int b, int seq,
   }
   *kminp = vmin;
   *kmaxp = vmax;
+  if (a.mean_lo) {  // the copies the scorer streams: each rounded once from the fp32 values
+    using VB = Vec<__nv_bfloat16, EPL>;
+    VB ml, vl;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+      ml.v[e] = __float2bfloat16_rn(mean[e]);
+      vl.v[e] = __float2bfloat16_rn(m2[e]);
+    }
+    *reinterpret_cast<VB*>(a.mean_lo + meta) = ml;
+    *reinterpret_cast<VB*>(a.m2_lo + meta) = vl;
+  }
 }
 
 // Bulk appends: a warp per (slot, KV head, touched page); the lengths are

@@ -32,6 +32,8 @@ struct DecodeArgs {
   const void* kmax;
   const float* mean;
   const float* m2;
+  const __nv_bfloat16* mean_lo;  // bf16 copies of mean and m2 the Gaussian scorer streams, or null
+  const __nv_bfloat16* m2_lo;
   const int32_t* block_table;
   const int32_t* seq_lens;
   uint32_t* status;
@@ -88,6 +90,8 @@ struct AppendArgs {
   void* kmax;
   float* mean;
   float* m2;
+  __nv_bfloat16* mean_lo;  // bf16 copies kept in step with mean and m2, or null
+  __nv_bfloat16* m2_lo;
   const int32_t* block_table;
   int32_t* seq_lens;
   uint32_t* status;

@@ -184,19 +184,57 @@ __global__ void __launch_bounds__(kThreads) bbox_f32_kernel(DecodeArgs a) {
 // free shared loads), with q and q² of those dims in registers as fp32 pairs
 // for the paired FMA; a butterfly reduce-scatter over the 16 lanes leaves
 // each of the 2·2·GP totals in some lane. GP = group padded to a power of 2.
-constexpr int kGaussWarps = 8, kGaussPPS = 4, kGaussNST = 3;
+// TM is the type of the streamed metadata: the fp32 mean and m2, or their
+// bf16 copies (half the bytes; twice the stages, so as many bytes in flight).
+constexpr int kGaussWarps = 8, kGaussPPS = 4;
 
-template <int D>
-constexpr int gauss_smem_bytes() {
-  return kGaussNST * kGaussPPS * 2 * 8 * D * 4 + kGaussNST * (16 + kGaussPPS * 4);
+template <typename TM>
+__host__ __device__ constexpr int gauss_nst() {
+  return sizeof(TM) == 4 ? 3 : 6;
 }
 
-template <typename TQ, int D, int GP>
+template <typename TM, int D>
+__host__ __device__ constexpr int gauss_smem_bytes() {
+  return gauss_nst<TM>() * kGaussPPS * 2 * 8 * D * (int)sizeof(TM) + gauss_nst<TM>() * (16 + kGaussPPS * 4);
+}
+
+// The metadata arrays of type TM: mean (which = 0) or m2 (which = 1).
+template <typename TM>
+__device__ __forceinline__ const TM* gauss_meta(const DecodeArgs& a, int which) {
+  if constexpr (sizeof(TM) == 4) return which ? a.m2 : a.mean;
+  else return which ? a.m2_lo : a.mean_lo;
+}
+
+// N metadata values of one chunk (16 bytes, or 8 for 4 bf16 values) as floats.
+template <typename TM, int N>
+__device__ __forceinline__ void load_chunk(const TM* p, bool valid, float (&f)[N]) {
+  static_assert(N * sizeof(TM) == 16 || N * sizeof(TM) == 8, "16- or 8-byte chunks");
+  uint4 r = make_uint4(0u, 0u, 0u, 0u);
+  if (valid) {
+    if constexpr (N * sizeof(TM) == 16) {
+      r = *reinterpret_cast<const uint4*>(p);
+    } else {
+      const uint2 h = *reinterpret_cast<const uint2*>(p);
+      r.x = h.x;
+      r.y = h.y;
+    }
+  }
+  const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    if constexpr (sizeof(TM) == 4) f[i] = __uint_as_float(w[i]);
+    else f[i] = (i & 1) ? bf_hi(w[i >> 1]) : bf_lo(w[i >> 1]);
+  }
+}
+
+template <typename TQ, typename TM, int D, int GP>
 __global__ void __launch_bounds__(kGaussWarps * 32) gauss_kernel(DecodeArgs a) {
   pdl_enter();
   constexpr int DPL = D / 16;             // dims per lane (a half-warp covers a row)
-  constexpr int CH = DPL / 4;             // 16-byte chunks per lane per row
-  constexpr int PPS = kGaussPPS, NST = kGaussNST;
+  // metadata values in one chunk load: 16 bytes, capped at the lane's share of a row
+  constexpr int VECM = (int)(16 / sizeof(TM)) < DPL ? (int)(16 / sizeof(TM)) : DPL;
+  constexpr int CH = DPL / VECM;          // chunks per lane per row
+  constexpr int PPS = kGaussPPS, NST = gauss_nst<TM>();
   constexpr int NV = 2 * 2 * GP;          // totals per half-warp per stage: page × (μ, σ²) × head
   extern __shared__ __align__(128) unsigned char dyn[];
   const int kv0 = blockIdx.y * 8, s = blockIdx.z;
@@ -205,12 +243,12 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_kernel(DecodeArgs a) {
   const int half = lane >> 4, hl = lane & 15;
   const int kvh = kv0 + warp;
   const bool active = warp < KH;
-  float* stages = reinterpret_cast<float*>(dyn);                         // [NST][PPS][2][KH][D]
-  uint64_t* full = reinterpret_cast<uint64_t*>(dyn + NST * PPS * 2 * 8 * D * 4);
+  TM* stages = reinterpret_cast<TM*>(dyn);                               // [NST][PPS][2][KH][D]
+  uint64_t* full = reinterpret_cast<uint64_t*>(dyn + NST * PPS * 2 * 8 * D * sizeof(TM));
   uint64_t* empty = full + NST;
   int* phys_sm = reinterpret_cast<int*>(empty + NST);                   // [NST][PPS]
   __shared__ uint32_t smax[8][GP];
-  static_assert(kGaussNST * kGaussPPS <= 32, "warp 0 looks up the first stages' pages at once");
+  static_assert(NST * PPS <= 32, "warp 0 looks up the first stages' pages at once");
   // every block, with pages or not, clears its slice of the control words
   clear_ctrl_slice(a.ctrl, a.ctrl_vec);
   // this block's slot of the per-head maxima starts as "none"
@@ -226,7 +264,7 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_kernel(DecodeArgs a) {
   const int g_hi = (int)(((long long)n_groups * (blockIdx.x + 1)) / gridDim.x);
   const int n_mine = g_hi - g_lo;
   if (n_mine <= 0) return;
-  const uint32_t row_bytes = (uint32_t)KH * D * 4;
+  const uint32_t row_bytes = (uint32_t)(KH * D * sizeof(TM));
   if (threadIdx.x < 8 * GP) smax[threadIdx.x / GP][threadIdx.x % GP] = 0u;
 
   // producer (warp 0): copy stage st's pages, whose physical ids are in
@@ -237,8 +275,8 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_kernel(DecodeArgs a) {
     if (lane == 0) mbar_expect_tx(&full[st], (uint32_t)__popc(valid) * row_bytes);
     __syncwarp();
     if (ph >= 0) {
-      const float* src = ((lane & 1) ? a.m2 : a.mean) + ((size_t)ph * a.Hkv + kv0) * D;
-      float* dst = stages + (((size_t)st * PPS + (lane >> 1)) * 2 + (lane & 1)) * KH * D;
+      const TM* src = gauss_meta<TM>(a, lane & 1) + ((size_t)ph * a.Hkv + kv0) * D;
+      TM* dst = stages + (((size_t)st * PPS + (lane >> 1)) * 2 + (lane & 1)) * KH * D;
       bulk_g2s(dst, src, row_bytes, &full[st]);
     }
   };
@@ -278,11 +316,11 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_kernel(DecodeArgs a) {
 #pragma unroll
     for (int c = 0; c < CH; ++c)
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int d0 = 4 * (hl + 16 * c) + 2 * e;
+      for (int e = 0; e < VECM / 2; ++e) {  // dims of lane hl's chunk c, in pairs
+        const int d0 = VECM * (hl + 16 * c) + 2 * e;
         const float x0 = hv ? to_f(qh[d0]) : 0.0f, x1 = hv ? to_f(qh[d0 + 1]) : 0.0f;
-        qp[h][2 * c + e] = f2_pack(x0, x1);
-        q2p[h][2 * c + e] = f2_pack(x0 * x0, x1 * x1);
+        qp[h][c * (VECM / 2) + e] = f2_pack(x0, x1);
+        q2p[h][c * (VECM / 2) + e] = f2_pack(x0 * x0, x1 * x1);
       }
   }
   int idx = 0, nfin = NV;
@@ -319,23 +357,25 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_kernel(DecodeArgs a) {
       for (int i = 0; i < 2; ++i) {
         const int pg = 2 * i + half;
         const bool pv = phys_sm[st * PPS + pg] >= 0;
-        const float* mrow = stages + (((size_t)st * PPS + pg) * 2 * KH + warp) * D;
-        const float* vrow = mrow + (size_t)KH * D;
+        const TM* mrow = stages + (((size_t)st * PPS + pg) * 2 * KH + warp) * D;
+        const TM* vrow = mrow + (size_t)KH * D;
         unsigned long long mu[GP], sg[GP];
 #pragma unroll
         for (int h = 0; h < GP; ++h) mu[h] = sg[h] = 0ull;
 #pragma unroll
         for (int c = 0; c < CH; ++c) {
-          const float4 m4 = pv ? *reinterpret_cast<const float4*>(mrow + 4 * (hl + 16 * c)) : make_float4(0.f, 0.f, 0.f, 0.f);
-          const float4 v4 = pv ? *reinterpret_cast<const float4*>(vrow + 4 * (hl + 16 * c)) : make_float4(0.f, 0.f, 0.f, 0.f);
-          const unsigned long long m01 = f2_pack(m4.x, m4.y), m23 = f2_pack(m4.z, m4.w);
-          const unsigned long long v01 = f2_pack(v4.x, v4.y), v23 = f2_pack(v4.z, v4.w);
+          float mf[VECM], vf[VECM];
+          load_chunk<TM, VECM>(mrow + VECM * (hl + 16 * c), pv, mf);
+          load_chunk<TM, VECM>(vrow + VECM * (hl + 16 * c), pv, vf);
 #pragma unroll
-          for (int h = 0; h < GP; ++h) {
-            mu[h] = f2_fma(qp[h][2 * c], m01, mu[h]);
-            mu[h] = f2_fma(qp[h][2 * c + 1], m23, mu[h]);
-            sg[h] = f2_fma(q2p[h][2 * c], v01, sg[h]);
-            sg[h] = f2_fma(q2p[h][2 * c + 1], v23, sg[h]);
+          for (int e = 0; e < VECM / 2; ++e) {
+            const unsigned long long mp = f2_pack(mf[2 * e], mf[2 * e + 1]);
+            const unsigned long long vp = f2_pack(vf[2 * e], vf[2 * e + 1]);
+#pragma unroll
+            for (int h = 0; h < GP; ++h) {
+              mu[h] = f2_fma(qp[h][c * (VECM / 2) + e], mp, mu[h]);
+              sg[h] = f2_fma(q2p[h][c * (VECM / 2) + e], vp, sg[h]);
+            }
           }
         }
 #pragma unroll
@@ -437,21 +477,27 @@ cudaError_t launch_bbox(const DecodeArgs& a, int kv_dtype, int sms, cudaStream_t
   return cudaGetLastError();
 }
 
-template <typename TQ, int D, int GP>
+template <typename TQ, typename TM, int D, int GP>
 static cudaError_t gauss_launch(const DecodeArgs& a, dim3 grid, cudaStream_t st) {
-  constexpr int smem = gauss_smem_bytes<D>();
-  static_assert(gauss_smem_bytes<D>() <= 227 * 1024, "stages exceed shared memory");
-  cudaError_t e = cudaFuncSetAttribute(gauss_kernel<TQ, D, GP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  constexpr int smem = gauss_smem_bytes<TM, D>();
+  static_assert(gauss_smem_bytes<TM, D>() <= 227 * 1024, "stages exceed shared memory");
+  cudaError_t e = cudaFuncSetAttribute(gauss_kernel<TQ, TM, D, GP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  return launch_k(false, gauss_kernel<TQ, D, GP>, dim3(grid), dim3(kGaussWarps * 32), smem, st, a);
+  return launch_k(false, gauss_kernel<TQ, TM, D, GP>, dim3(grid), dim3(kGaussWarps * 32), smem, st, a);
+}
+
+template <typename TQ, typename TM, int D>
+static cudaError_t gauss_dispatch_gm(const DecodeArgs& a, dim3 grid, cudaStream_t st) {
+  if (a.G <= 1) return gauss_launch<TQ, TM, D, 1>(a, grid, st);
+  if (a.G <= 2) return gauss_launch<TQ, TM, D, 2>(a, grid, st);
+  if (a.G <= 4) return gauss_launch<TQ, TM, D, 4>(a, grid, st);
+  return gauss_launch<TQ, TM, D, 8>(a, grid, st);
 }
 
 template <typename TQ, int D>
 static cudaError_t gauss_dispatch_g(const DecodeArgs& a, dim3 grid, cudaStream_t st) {
-  if (a.G <= 1) return gauss_launch<TQ, D, 1>(a, grid, st);
-  if (a.G <= 2) return gauss_launch<TQ, D, 2>(a, grid, st);
-  if (a.G <= 4) return gauss_launch<TQ, D, 4>(a, grid, st);
-  return gauss_launch<TQ, D, 8>(a, grid, st);
+  return a.mean_lo ? gauss_dispatch_gm<TQ, __nv_bfloat16, D>(a, grid, st)
+                   : gauss_dispatch_gm<TQ, float, D>(a, grid, st);
 }
 
 // ~2 blocks per SM (96 KiB of stages each) over all (sequence, 8-KV-head)

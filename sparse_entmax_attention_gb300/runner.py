@@ -13,7 +13,7 @@ class Workload:
     """A cache holding a workload's prefilled context, on one device."""
 
     def __init__(self, spec: synth.Spec, seed: int = 0, device="cuda", extra_steps: int = 0,
-                 keep_kv: bool = False):
+                 keep_kv: bool = False, meta_bf16: bool = False):
         self.spec, self.seed, self.device = spec, seed, torch.device(device)
         steps = max(spec.steps if spec.append_per_step else 0, extra_steps)
         if steps != (spec.steps if spec.append_per_step else 0):
@@ -21,7 +21,8 @@ class Workload:
             self.spec = spec
         bt, total, need = synth.block_tables(spec, seed)
         self.cache = B.PagedCache(spec.num_kv_heads, spec.group, spec.head_dim, spec.page_size,
-                                  spec.batch, bt.shape[1], total, spec.kv_dtype, device)
+                                  spec.batch, bt.shape[1], total, spec.kv_dtype, device,
+                                  meta_bf16=meta_bf16)
         self.cache.block_table.copy_(bt.to(device))
         self.q = torch.stack([synth.queries(spec, b, seed, device)
                               for b in range(spec.batch)]).contiguous()

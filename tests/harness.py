@@ -18,12 +18,12 @@ from sparse_entmax_attention_gb300 import synth
 class Built:
     """A filled cache plus the stored K/V/q it was filled from (on the GPU)."""
 
-    def __init__(self, spec, seed=0, device="cuda", prefill_chunk=None):
+    def __init__(self, spec, seed=0, device="cuda", prefill_chunk=None, meta_bf16=False):
         self.spec = spec
         bt, total, need = synth.block_tables(spec, seed)
         maxp = bt.shape[1]
         self.cache = B.PagedCache(spec.num_kv_heads, spec.group, spec.head_dim, spec.page_size,
-                                  spec.batch, maxp, total, spec.kv_dtype, device)
+                                  spec.batch, maxp, total, spec.kv_dtype, device, meta_bf16=meta_bf16)
         self.cache.block_table.copy_(bt.to(device))
         self.q = torch.stack([synth.queries(spec, b, seed, device) for b in range(spec.batch)]).contiguous()
         self.K, self.V, self.draws = [], [], []
@@ -53,6 +53,21 @@ class Built:
         """Stored keys/values of (sequence b, KV head j) as float64 numpy."""
         L = int(self.cache.seq_lens[b].item())
         return (self.K[b][j, :L].double().cpu().numpy(), self.V[b][j, :L].double().cpu().numpy())
+
+    def host_meta(self, b, j):
+        """Page metadata of (sequence b, KV head j) as the Gaussian scorer reads
+        it: the oracle's float64 metadata of the stored keys, with the mean and
+        variance replaced by the stored bf16 copies when the cache keeps them
+        (None otherwise: the oracle then builds its own)."""
+        c = self.cache
+        if c.mean_bf16 is None:
+            return None
+        K, _ = self.host_kv(b, j)
+        meta = opg.page_metadata(K, self.spec.page_size)
+        phys = c.block_table[b, : len(meta["n"])].long()
+        meta["mean"] = c.mean_bf16[phys, j].double().cpu().numpy()
+        meta["var"] = c.m2_bf16[phys, j].double().cpu().numpy() / meta["n"][:, None]
+        return meta
 
     def host_q(self, b, j, q=None):
         q = self.q if q is None else q

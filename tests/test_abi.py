@@ -35,7 +35,7 @@ def test_exports_every_declared_function(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert lib.entmaxkv_version() == 1
+    assert lib.entmaxkv_version() == 2
     for code in range(5):
         assert lib.entmaxkv_status_string(code)
     assert lib.entmaxkv_status_string(99) == b"unknown status"
@@ -151,3 +151,17 @@ def test_read_status_needs_a_status_word(lib):
     out = ctypes.c_uint32(7)
     assert lib.entmaxkv_read_status(ctypes.byref(view), ctypes.byref(out), 0, None) == 1
     assert lib.entmaxkv_read_status(None, ctypes.byref(out), 0, None) == 1
+
+
+def test_bf16_metadata_copies_come_in_pairs(lib):
+    cfg = _cfg()
+    view = B.CacheView(*([256] * 8), None, 256, None)  # mean copy without its m2 copy
+    rc = lib.entmaxkv_decode(ctypes.byref(cfg), ctypes.byref(view), ctypes.c_void_p(256), None, 1,
+                             1.5, B.POLICY_GAUSSIAN, 0, 0.5, 0, ctypes.c_void_p(256), 1 << 40,
+                             ctypes.c_void_p(256), None, 0, None, None, None, None)
+    assert rc == 1
+    view = B.CacheView(*([256] * 8), None, 264, 256)  # misaligned copy
+    rc = lib.entmaxkv_decode(ctypes.byref(cfg), ctypes.byref(view), ctypes.c_void_p(256), None, 1,
+                             1.5, B.POLICY_GAUSSIAN, 0, 0.5, 0, ctypes.c_void_p(256), 1 << 40,
+                             ctypes.c_void_p(256), None, 0, None, None, None, None)
+    assert rc == 1

@@ -1,0 +1,70 @@
+"""GPU: caches that keep bf16 copies of the page mean and m2 for the Gaussian
+scorer.
+
+Metadata parity is exact by construction: every copy must equal the
+round-to-nearest-even bf16 of the fp32 value append keeps (which the fp32
+metadata tests pin to the float64 page statistics), including pages filled
+token by token. Decode parity is then checked against the oracle run on the
+metadata the scorer reads (the stored bf16 values in float64), with the same
+tolerances as the fp32-metadata path.
+"""
+
+import pytest
+import torch
+
+from sparse_entmax_attention_gb300 import binding as B
+from sparse_entmax_attention_gb300 import synth
+
+from harness import Built
+from test_parity_gpu import check_decode
+
+pytestmark = pytest.mark.gpu
+
+
+def _copies_match(cache):
+    assert torch.equal(cache.mean_bf16, cache.mean.to(torch.bfloat16))
+    assert torch.equal(cache.m2_bf16, cache.m2.to(torch.bfloat16))
+
+
+@pytest.fixture(scope="module")
+def built_meta16():
+    spec = synth.custom(8, 2, 128, 16, [3000, 1217], torch.bfloat16, 1.5, n_needles=6,
+                        n_outliers=2, shuffled_table=True)
+    return Built(spec, prefill_chunk=700, meta_bf16=True)
+
+
+def test_copies_are_the_rounded_fp32_metadata(built_meta16):
+    _copies_match(built_meta16.cache)
+
+
+@pytest.mark.parametrize("alpha,margin", [(1.5, 0.5), (2.0, 0.0), (1.5, 1.0)])
+def test_gaussian_decode_on_bf16_metadata(built_meta16, alpha, margin):
+    check_decode(built_meta16, "gaussian", alpha, 0, margin)
+
+
+def test_bf16_metadata_appended_token_by_token():
+    spec = synth.custom(2, 2, 64, 16, [77], torch.float32, 1.5, n_needles=2)
+    built = Built(spec, prefill_chunk=1, meta_bf16=True)
+    _copies_match(built.cache)
+    check_decode(built, "gaussian", 1.5, 0, 0.5)
+
+
+def test_other_policies_ignore_the_copies(built_meta16):
+    for policy, budget in (("topk", 256), ("full", 0)):
+        check_decode(built_meta16, policy, 1.5, budget, 0.0)
+
+
+def test_copies_must_come_in_pairs():
+    spec = synth.custom(2, 1, 64, 16, [40], torch.bfloat16, 1.5, n_needles=1)
+    built = Built(spec, meta_bf16=True)
+    c = built.cache
+    view = B.CacheView(*[getattr(c.view, f) for f, _ in B.CacheView._fields_])
+    view.m2_bf16 = None
+    ws = B.alloc_workspace(c, 1, "gaussian")
+    o = B.alloc_outputs(c, 1, "gaussian")
+    import ctypes
+    rc = B.lib().entmaxkv_decode(ctypes.byref(c.cfg), ctypes.byref(view), ctypes.c_void_p(built.q.data_ptr()),
+                                 None, 1, 1.5, B.POLICY_GAUSSIAN, 0, 0.5, 0, ctypes.c_void_p(ws.data_ptr()),
+                                 ws.numel(), ctypes.c_void_p(o.out.data_ptr()), None, 0, None, None, None,
+                                 None)
+    assert rc == 1

@@ -57,7 +57,7 @@ def check_decode(built, policy, alpha=1.5, budget=0, margin=0.0, flags=0, q=None
     for b, j in units:
         K, V = built.host_kv(b, j)
         Q = built.host_q(b, j, q)
-        r = odec.decode_group(K, V, Q, alpha, policy, P, budget, margin)
+        r = odec.decode_group(K, V, Q, alpha, policy, P, budget, margin, meta=built.host_meta(b, j))
         hs = slice(j * g, (j + 1) * g)
         got_ids = pids[b, j, : n_sel[b, j]]
         want = r["page_ids"]
