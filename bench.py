@@ -36,7 +36,7 @@ L2_FLUSH_BYTES = 512 << 20   # > 129 MB L2: read between timed steps
 # DRAM bytes (read + write) of one launch of the dominant kernel on this
 # workload, from an ncu capture of the bench command itself (no scaling);
 # reset to None whenever that kernel changes.
-NCU_TRAFFIC_PER_LAUNCH = 268887808 + 7936768
+NCU_TRAFFIC_PER_LAUNCH = None
 
 
 def measured_peaks():
@@ -56,7 +56,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="headline step only")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--policies", default="gaussian,topk,softmax_topk,full_dense,full_skipv,softmax",
+    ap.add_argument("--policies", default="gaussian,gaussian_meta_f32,topk,softmax_topk,full_dense,full_skipv,softmax",
                     help="rows of the per-policy table")
     return ap.parse_args()
 
@@ -127,8 +127,10 @@ def algorithmic_bytes(wl, policy, o, ws, view):
     if policy in ("full_dense", "softmax"):
         return 2 * n_pages * Hkv * page_kv + io, {"k_pages": n_pages * Hkv, "v_pages": n_pages * Hkv}
     meta = 0
-    if policy == "gaussian":
-        meta = n_pages * Hkv * d * 4 * 2           # mean + m2, fp32
+    if policy == "gaussian":                       # mean + m2: the bf16 copies when the cache keeps them
+        meta = n_pages * Hkv * d * (2 if cache.mean_bf16 is not None else 4) * 2
+    elif policy == "gaussian_meta_f32":
+        meta = n_pages * Hkv * d * 4 * 2
     elif policy in ("topk", "softmax_topk"):
         meta = n_pages * Hkv * d * el * 2          # kmin + kmax
     n_sel = o.n_sel.cpu()
@@ -163,7 +165,7 @@ def run_ours(args, rank, world):
     K, W = args.steps, args.warmup
     spec = synth.workload(WORKLOAD)
     n_append = 2 * (K + W) + 4
-    wl = runner.Workload(spec, seed=0, device=dev, extra_steps=n_append)
+    wl = runner.Workload(spec, seed=0, device=dev, extra_steps=n_append, meta_bf16=True)
     cache = wl.cache
     peaks, peak_kind = measured_peaks()
     # inputs of every step, resident in HBM before timing
@@ -266,6 +268,7 @@ def run_ours(args, rank, world):
                    "q_heads": spec.num_q_heads, "kv_heads": spec.num_kv_heads,
                    "head_dim": spec.head_dim, "page_size": spec.page_size, "alpha": ALPHA,
                    "policy": "gaussian", "margin": MARGIN,
+                   "metadata": "fp32 mean/m2 kept for appends; their bf16 copies streamed by the scorer",
                    "step": "append 1 token + Gaussian-selector decode (CUDA graph)",
                    "queries": "the workload's decode queries (needles planted for them)",
                    "l2": "flushed between timed steps by reading a 512 MiB buffer; per-step CUDA events",
@@ -296,16 +299,18 @@ def policy_table(wl, B, flush, qbuf, timed, K, peaks, names):
     import torch
     cache, spec = wl.cache, wl.spec
     rows = {}
-    cases = [("gaussian", "gaussian", 0, 0), ("topk", "topk", TOPK_BUDGET, 0),
+    cases = [("gaussian", "gaussian", 0, 0), ("gaussian_meta_f32", "gaussian", 0, 0),
+             ("topk", "topk", TOPK_BUDGET, 0),
              ("softmax_topk", "softmax_topk", TOPK_BUDGET, 0),
              ("full_dense", "full", 0, B.FLAG_DENSE_V), ("full_skipv", "full", 0, 0),
              ("softmax", "softmax", 0, 0)]
     for name, pol, budget, flags in cases:
         if name not in names:
             continue
-        ws = B.alloc_workspace(cache, spec.batch, pol, budget)
-        o = B.alloc_outputs(cache, spec.batch, pol, budget)
-        fn = lambda: B.decode(cache, qbuf, ALPHA, pol, budget, MARGIN, flags, workspace=ws, outputs=o)
+        c = cache.fp32_metadata() if name == "gaussian_meta_f32" else cache
+        ws = B.alloc_workspace(c, spec.batch, pol, budget)
+        o = B.alloc_outputs(c, spec.batch, pol, budget)
+        fn = lambda: B.decode(c, qbuf, ALPHA, pol, budget, MARGIN, flags, workspace=ws, outputs=o)
         fn()
         torch.cuda.synchronize()
         g = torch.cuda.CUDAGraph()
@@ -317,7 +322,7 @@ def policy_table(wl, B, flush, qbuf, timed, K, peaks, names):
         nbytes, counts = algorithmic_bytes(wl, name, o, ws, view)
         evs = B.stage_events()
         flush.zero_()
-        B.decode(cache, qbuf, ALPHA, pol, budget, MARGIN, flags, workspace=ws, outputs=o, events=evs)
+        B.decode(c, qbuf, ALPHA, pol, budget, MARGIN, flags, workspace=ws, outputs=o, events=evs)
         torch.cuda.synchronize()
         stage = {n: round(evs[k].elapsed_time(evs[k + 1]) * 1e3, 1) for k, n in enumerate(B.STAGES)}
         rows[name] = {"us": round(mean, 2), "bytes": nbytes, "stage_us_once": stage,
@@ -325,7 +330,7 @@ def policy_table(wl, B, flush, qbuf, timed, K, peaks, names):
                       "frac_8tbs": round(nbytes / (mean * 1e-6) / 1e9 / NOMINAL_HBM_GBS, 4),
                       **counts}
         del ws
-    for name in ("topk", "softmax_topk", "full_dense", "full_skipv", "softmax"):
+    for name in ("gaussian_meta_f32", "topk", "softmax_topk", "full_dense", "full_skipv", "softmax"):
         if name in rows and "gaussian" in rows:
             rows[name]["gaussian_speedup"] = round(rows[name]["us"] / rows["gaussian"]["us"], 2)
     return rows
@@ -369,11 +374,14 @@ def roofline(wl, B, flush, qbuf, K, peaks, peak_kind):
             per[n].append(evs[k].elapsed_time(evs[k + 1]) * 1e3)
     stages = {n: round(statistics.mean(v), 2) for n, v in per.items()}
     n_pages = -(-int(cache.seq_lens[0]) // spec.page_size)
-    alg = n_pages * spec.num_kv_heads * spec.head_dim * 4 * 2   # mean + m2 bytes per launch
+    el = 2 if cache.mean_bf16 is not None else 4             # the metadata the scorer streams
+    alg = n_pages * spec.num_kv_heads * spec.head_dim * el * 2  # mean + m2 bytes per launch
     t = stages["score"] * 1e-6
     ach = alg / t / 1e9
     it = ws[view.tauhat_iters: view.tauhat_iters + spec.batch * spec.num_q_heads * 4].view(torch.int32)
-    return {"kernel": "gauss_kernel (Gaussian page scoring)", "bound": "hbm",
+    kname = ("gauss_mma_kernel (Gaussian page scoring on the tensor cores, bf16 metadata)"
+             if el == 2 else "gauss_kernel (Gaussian page scoring, fp32 metadata)")
+    return {"kernel": kname, "bound": "hbm",
             "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": round(ach / peaks["hbm_gbs"], 4), "peak_kind": peak_kind + " (copy, burst)",
             "traffic": NCU_TRAFFIC_PER_LAUNCH, "algorithmic_bytes": alg,

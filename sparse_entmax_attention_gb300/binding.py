@@ -9,6 +9,7 @@ raise.
 
 from __future__ import annotations
 
+import copy
 import ctypes
 import os
 from dataclasses import dataclass
@@ -158,6 +159,15 @@ class PagedCache:
                               self.status.data_ptr(),
                               self.mean_bf16.data_ptr() if meta_bf16 else None,
                               self.m2_bf16.data_ptr() if meta_bf16 else None)
+
+    def fp32_metadata(self) -> "PagedCache":
+        """The same cache seen without its bf16 metadata copies (the Gaussian
+        scorer then streams the fp32 mean and m2); tensors are shared."""
+        other = copy.copy(self)
+        other.view = CacheView(*[getattr(self.view, f) for f, _ in CacheView._fields_])
+        other.view.mean_bf16 = None
+        other.view.m2_bf16 = None
+        return other
 
     @property
     def num_q_heads(self):

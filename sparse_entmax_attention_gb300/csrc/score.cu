@@ -455,6 +455,207 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_kernel(DecodeArgs a) {
   }
 }
 
+// Gaussian page scores on the tensor cores, for bf16 queries with the bf16
+// metadata copies: μ = q·mean and σ² = Σ_d q_d²·m2_d are a dense contraction
+// (pages × dims × heads). One m16n8k16 tile puts the group's query heads in
+// its rows (padded to 16) and 8 pages in its columns. The products are exact
+// in fp32: q·mean is bf16 × bf16, and q² (at most 16 significant bits) is
+// split exactly into bf16 hi + lo, two MMAs into one accumulator. The
+// accumulator hands lane l the totals of head l/4 for pages 2(l%4) and
+// 2(l%4)+1, so no cross-lane reduction is left. The streaming is the one of
+// gauss_kernel: stages of 8 pages (for up to 8 KV heads) filled by bulk
+// copies on full/empty mbarriers. Page runs sit 16 bytes apart modulo 128, so
+// the 8 page rows an ldmatrix reads fall in different banks.
+constexpr int kGaussMmaPPS = 8, kGaussMmaNST = 3;
+
+__host__ __device__ constexpr int gauss_mma_stage_bytes(int D) {
+  return kGaussMmaPPS * (2 * 8 * D * 2 + 16);
+}
+__host__ __device__ constexpr int gauss_mma_smem_bytes(int D) {
+  return kGaussMmaNST * gauss_mma_stage_bytes(D) + kGaussMmaNST * (16 + kGaussMmaPPS * 4);
+}
+
+__device__ __forceinline__ void ldsm_x2(uint32_t& r0, uint32_t& r1, const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];\n"
+               : "=r"(r0), "=r"(r1)
+               : "r"(smem_u32(p)));
+}
+
+__device__ __forceinline__ uint32_t bf2_pack(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kGaussWarps * 32) gauss_mma_kernel(DecodeArgs a) {
+  pdl_enter();
+  constexpr int PPS = kGaussMmaPPS, NST = kGaussMmaNST, KS = D / 16;
+  extern __shared__ __align__(128) unsigned char dyn[];
+  const int kv0 = blockIdx.y * 8, s = blockIdx.z;
+  const int KH = min(8, a.Hkv - kv0);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int kvh = kv0 + warp;
+  const bool active = warp < KH;
+  const int run = KH * D * 2;                 // bytes of one (page, array) run: KH rows of D
+  const int pstride = 2 * run + 16;           // bytes from one page's runs to the next's
+  const int sstride = PPS * pstride;          // bytes of one stage
+  uint64_t* full = reinterpret_cast<uint64_t*>(dyn + NST * gauss_mma_stage_bytes(D));
+  uint64_t* empty = full + NST;
+  int* phys_sm = reinterpret_cast<int*>(empty + NST);  // [NST][PPS]
+  __shared__ uint32_t smax[8][8];
+  static_assert(NST * PPS <= 32, "warp 0 looks up the first stages' pages at once");
+  clear_ctrl_slice(a.ctrl, a.ctrl_vec);
+  for (int i = threadIdx.x; i < KH * a.G; i += blockDim.x)
+    a.mslot[((size_t)s * a.Hq + (size_t)kv0 * a.G + i) * a.mslots + blockIdx.x] = 0u;
+  const int seq = seq_row(a.seq_ids, s, a.max_seqs, threadIdx.x == 0 ? a.status : nullptr);
+  if (seq < 0) return;
+  const int L = seq_len_clamped(a.seq_lens, seq, a.maxp, a.P, threadIdx.x == 0 ? a.status : nullptr);
+  const int n_pages = (L + a.P - 1) / a.P;
+  const int n_groups = (n_pages + PPS - 1) / PPS;
+  const int g_lo = (int)(((long long)n_groups * blockIdx.x) / gridDim.x);
+  const int g_hi = (int)(((long long)n_groups * (blockIdx.x + 1)) / gridDim.x);
+  const int n_mine = g_hi - g_lo;
+  if (n_mine <= 0) return;
+  if (threadIdx.x < 64) smax[threadIdx.x >> 3][threadIdx.x & 7] = 0u;
+
+  // producer (warp 0): lanes 0..2·PPS−1 copy one run each (page lane/2, array lane%2)
+  auto issue_copies = [&](int st) {
+    const int ph = lane < 2 * PPS ? phys_sm[st * PPS + (lane >> 1)] : -1;
+    const uint32_t valid = __ballot_sync(0xffffffffu, ph >= 0);
+    if (lane == 0) mbar_expect_tx(&full[st], (uint32_t)__popc(valid) * (uint32_t)run);
+    __syncwarp();
+    if (ph >= 0) {
+      const __nv_bfloat16* src = ((lane & 1) ? a.m2_lo : a.mean_lo) + ((size_t)ph * a.Hkv + kv0) * D;
+      bulk_g2s(dyn + st * sstride + (lane >> 1) * pstride + (lane & 1) * run, src, (uint32_t)run, &full[st]);
+    }
+  };
+  auto issue = [&](int g, int st) {
+    if (lane < PPS) {
+      const int p = g * PPS + lane;
+      phys_sm[st * PPS + lane] = p < n_pages ? phys_page(a.block_table, seq, p, a.maxp, a.nphys, a.status) : -1;
+    }
+    __syncwarp();
+    issue_copies(st);
+  };
+  if (warp == 0) {
+    if (lane < NST) {
+      mbar_init(&full[lane], 1);
+      mbar_init(&empty[lane], kGaussWarps);
+    }
+    mbar_fence_init();
+    __syncwarp();
+    const int nfill = min(NST, n_mine);
+    if (lane < NST * PPS) {
+      const int j = lane / PPS, p = (g_lo + j) * PPS + lane % PPS;
+      phys_sm[lane] = (j < nfill && p < n_pages)
+                          ? phys_page(a.block_table, seq, p, a.maxp, a.nphys, a.status) : -1;
+    }
+    __syncwarp();
+    for (int j = 0; j < nfill; ++j) issue_copies(j);
+  }
+
+  // A fragments: row lane/4 (a query head of the group), dims 2(lane%4)+{0,1}
+  // and +8 of each 16-dim step; rows 8..15 are zero. q, q² hi, q² lo.
+  const int r = lane >> 2, cpair = 2 * (lane & 3);
+  const bool hv = active && r < a.G;
+  const __nv_bfloat16* qh = (const __nv_bfloat16*)a.q + ((size_t)s * a.Hq + (size_t)(hv ? kvh : 0) * a.G + (hv ? r : 0)) * D;
+  uint32_t aq[KS][2], ah[KS][2], al[KS][2];
+#pragma unroll
+  for (int k = 0; k < KS; ++k)
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int d0 = 16 * k + 8 * u + cpair;
+      const uint32_t w = hv ? *reinterpret_cast<const uint32_t*>(qh + d0) : 0u;
+      aq[k][u] = w;
+      const float x0 = bf_lo(w), x1 = bf_hi(w);
+      const float s0 = x0 * x0, s1 = x1 * x1;  // exact: at most 16 significant bits
+      const float h0 = __bfloat162float(__float2bfloat16_rn(s0)), h1 = __bfloat162float(__float2bfloat16_rn(s1));
+      ah[k][u] = bf2_pack(h0, h1);
+      al[k][u] = bf2_pack(s0 - h0, s1 - h1);  // the exact remainders, representable in bf16
+    }
+  __syncthreads();  // barriers initialised
+
+  const float inv_full = 1.0f / ((float)a.P * (float)D);
+  float runmax = -CUDART_INF_F;
+  const int lrow = lane & 7, lk = ((lane >> 3) & 1) * 16;  // ldmatrix: page row, byte offset in the step
+  int stuck = 0;
+  for (int j = 0; j < n_mine; ++j) {
+    const int st = j % NST;
+    const uint32_t par = (uint32_t)((j / NST) & 1);
+    const int g = g_lo + j;
+    if (!mbar_wait_bounded(&full[st], par)) {
+      stuck = 1;
+      break;
+    }
+    float mu[4] = {0.f, 0.f, 0.f, 0.f}, sg[4] = {0.f, 0.f, 0.f, 0.f};
+    int ph0 = -1, ph1 = -1;
+    if (active) {
+      const unsigned char* rowm = dyn + st * sstride + lrow * pstride + warp * D * 2 + lk;
+      const unsigned char* rowv = rowm + run;
+#pragma unroll
+      for (int k = 0; k < KS; ++k) {
+        uint32_t bm0, bm1, bv0, bv1;
+        ldsm_x2(bm0, bm1, rowm + 32 * k);
+        ldsm_x2(bv0, bv1, rowv + 32 * k);
+        mma_bf16(mu, aq[k][0], 0u, aq[k][1], 0u, bm0, bm1);
+        mma_bf16(sg, ah[k][0], 0u, ah[k][1], 0u, bv0, bv1);
+        mma_bf16(sg, al[k][0], 0u, al[k][1], 0u, bv0, bv1);
+      }
+      ph0 = phys_sm[st * PPS + cpair];
+      ph1 = phys_sm[st * PPS + cpair + 1];
+    }
+    __syncwarp();
+    if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(&empty[st])) : "memory");
+    if (warp == 0 && j + NST < n_mine) {
+      if (!mbar_wait_bounded(&empty[st], par)) {
+        stuck = 1;
+        break;
+      }
+      issue(g + NST, st);
+    }
+    if (!hv) continue;
+    float2* dst = a.gauss_ms + ((size_t)s * a.Hq + (size_t)kvh * a.G + r) * a.maxp;
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int p = g * PPS + cpair + u;
+      if (p >= n_pages) continue;
+      const int ph = u ? ph1 : ph0;
+      if (ph < 0) {  // unreadable page: no mass, never selected
+        dst[p] = make_float2(-CUDART_INF_F, 0.0f);
+        continue;
+      }
+      const int nv = min(a.P, L - p * a.P);
+      const float inv_n = nv == a.P ? inv_full : 1.0f / ((float)nv * (float)D);
+      const float m = a.a1 * mu[u] * a.inv_sqrt_d;
+      dst[p] = make_float2(m, a.a1 * sqrtf(fmaxf(sg[u], 0.0f) * inv_n));
+      runmax = fmaxf(runmax, m);
+    }
+  }
+  if (stuck) {
+    if (lane == 0) raise_flag(a.status, ENTMAXKV_DEV_TIMEOUT);
+    if (warp == 0)
+      for (int st = 0; st < NST; ++st) mbar_wait_bounded(&full[st], 0u), mbar_wait_bounded(&full[st], 1u);
+  }
+  runmax = fmaxf(runmax, __shfl_xor_sync(0xffffffffu, runmax, 1));
+  runmax = fmaxf(runmax, __shfl_xor_sync(0xffffffffu, runmax, 2));
+  if (hv && (lane & 3) == 0 && runmax > -CUDART_INF_F) smax[warp][r] = ord_enc(runmax);
+  __syncthreads();
+  if (threadIdx.x < 64) {
+    const int w = threadIdx.x >> 3, h = threadIdx.x & 7;
+    if (w < KH && h < a.G)
+      a.mslot[((size_t)s * a.Hq + (size_t)(kv0 + w) * a.G + h) * a.mslots + blockIdx.x] = smax[w][h];
+  }
+}
+
+template <int D>
+static cudaError_t gauss_mma_launch(const DecodeArgs& a, dim3 grid, cudaStream_t st) {
+  constexpr int smem = gauss_mma_smem_bytes(D);
+  static_assert(gauss_mma_smem_bytes(D) <= 227 * 1024, "stages exceed shared memory");
+  cudaError_t e = cudaFuncSetAttribute(gauss_mma_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  return launch_k(false, gauss_mma_kernel<D>, dim3(grid), dim3(kGaussWarps * 32), smem, st, a);
+}
+
 static int grid_x_for(int units, int per_block, int sms, int other_blocks) {
   int need = (units + per_block - 1) / per_block;
   int cap = (sms * 8 + other_blocks - 1) / other_blocks;  // ~8 blocks per SM overall
@@ -514,7 +715,9 @@ int gauss_grid_x(int maxp, int Hkv, int S, int sms) {
 cudaError_t launch_gauss(const DecodeArgs& a, int kv_dtype, int sms, cudaStream_t st) {
   dim3 grid(a.mslots, (a.Hkv + 7) / 8, a.S);
   cudaError_t e;
-  if (kv_dtype == ENTMAXKV_BF16)
+  if (kv_dtype == ENTMAXKV_BF16 && a.mean_lo)  // bf16 q and metadata: tensor cores
+    e = a.D == 128 ? gauss_mma_launch<128>(a, grid, st) : gauss_mma_launch<64>(a, grid, st);
+  else if (kv_dtype == ENTMAXKV_BF16)
     e = a.D == 128 ? gauss_dispatch_g<__nv_bfloat16, 128>(a, grid, st)
                    : gauss_dispatch_g<__nv_bfloat16, 64>(a, grid, st);
   else
