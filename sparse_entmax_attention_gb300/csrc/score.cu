@@ -467,6 +467,7 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_kernel(DecodeArgs a) {
 // copies on full/empty mbarriers. Page runs sit 16 bytes apart modulo 128, so
 // the 8 page rows an ldmatrix reads fall in different banks.
 constexpr int kGaussMmaPPS = 8, kGaussMmaNST = 3;
+constexpr int kGaussMmaPre = 512;  // physical ids of a block's pages looked up at the start
 
 __host__ __device__ constexpr int gauss_mma_stage_bytes(int D) {
   return kGaussMmaPPS * (2 * 8 * D * 2 + 16);
@@ -503,6 +504,7 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_mma_kernel(DecodeArgs 
   uint64_t* empty = full + NST;
   int* phys_sm = reinterpret_cast<int*>(empty + NST);  // [NST][PPS]
   __shared__ uint32_t smax[8][8];
+  __shared__ int phys_pre[kGaussMmaPre];
   static_assert(NST * PPS <= 32, "warp 0 looks up the first stages' pages at once");
   clear_ctrl_slice(a.ctrl, a.ctrl_vec);
   for (int i = threadIdx.x; i < KH * a.G; i += blockDim.x)
@@ -517,6 +519,13 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_mma_kernel(DecodeArgs 
   const int n_mine = g_hi - g_lo;
   if (n_mine <= 0) return;
   if (threadIdx.x < 64) smax[threadIdx.x >> 3][threadIdx.x & 7] = 0u;
+  // the block's later pages (after the first NST stages) are looked up now,
+  // all at once, so that a refill issues its copies without a dependent load
+  const int n_pre = min(kGaussMmaPre, n_mine * PPS);
+  for (int i = NST * PPS + (int)threadIdx.x; i < n_pre; i += blockDim.x) {
+    const int p = g_lo * PPS + i;
+    phys_pre[i] = p < n_pages ? phys_page(a.block_table, seq, p, a.maxp, a.nphys, a.status) : -1;
+  }
 
   // producer (warp 0): lanes 0..2·PPS−1 copy one run each (page lane/2, array lane%2)
   auto issue_copies = [&](int st) {
@@ -531,8 +540,10 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_mma_kernel(DecodeArgs 
   };
   auto issue = [&](int g, int st) {
     if (lane < PPS) {
-      const int p = g * PPS + lane;
-      phys_sm[st * PPS + lane] = p < n_pages ? phys_page(a.block_table, seq, p, a.maxp, a.nphys, a.status) : -1;
+      const int p = g * PPS + lane, i = p - g_lo * PPS;
+      phys_sm[st * PPS + lane] = p >= n_pages ? -1
+                                 : i < n_pre ? phys_pre[i]
+                                             : phys_page(a.block_table, seq, p, a.maxp, a.nphys, a.status);
     }
     __syncwarp();
     issue_copies(st);
