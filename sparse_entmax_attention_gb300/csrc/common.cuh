@@ -264,9 +264,16 @@ __device__ __forceinline__ void gauss_moment2(float a, float sg, float inv_sg, b
   constexpr float cB[EKV_MILLS_DEG + 1] = {EKV_MILLS_B};
   const float t = a * inv_sg;
   const float x = fabsf(t);
-  const float u = __frcp_rn(fmaf(fminf(x, EKV_MILLS_XMAX), 0.33333334f, 1.0f));
+  // u and φ need only the accuracy of the fits (relative 4.4e-7): the PTX
+  // approximate reciprocal (within about 1 ulp) and base-2 exponential
+  // (relative error about 2^-22; it flushes to 0 below 2^-126, where every
+  // moment is negligible) are enough, and each is a single instruction.
+  float u;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(u) : "f"(fmaf(fminf(x, EKV_MILLS_XMAX), 0.33333334f, 1.0f)));
   const float w = fmaf(2.5f, u, -1.5f);
-  const float phi = 0.3989422804f * exp2f(-0.72134752f * x * x);
+  float e2;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e2) : "f"(-0.72134752f * x * x));
+  const float phi = 0.3989422804f * e2;
   const float pu = phi * u;
   const float R = pu * horner(cR, w);
   const float A = pu * u * horner(cA, w);
