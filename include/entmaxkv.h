@@ -23,8 +23,10 @@
  *     range, an append past the block table, ...) are OR-ed as
  *     ENTMAXKV_DEV_* bits into the caller's device status word
  *     (entmaxkv_cache.status, may be NULL). Nothing prints, traps or throws.
- *   - No kernel spins: kernels never wait on other kernels or on flags; the
- *     split-K combines use a "last block to finish combines" counter.
+ *   - No kernel spins: kernels never wait on other kernels or on flags. The
+ *     entmax split-K blocks add their sums into `out` with float atomics, so
+ *     the last bits of `out` depend on the order blocks finish in; the
+ *     softmax split-K combine uses a "last block to finish combines" counter.
  */
 #ifndef ENTMAXKV_H
 #define ENTMAXKV_H

@@ -15,8 +15,10 @@
 //           query head from the candidates (one warp per head).
 //   pass B  gathers V only for pages with some z above τ (all pages for the
 //           dense baseline), accumulates Σ p_i v_i with p_i = [z_i − τ]_+^β in
-//           fp32, writes a per-block partial, and the last block to finish
-//           sums the partials in split order (deterministic).
+//           fp32, and adds each block's sums into the output rows (zeroed
+//           by pass A) with vector float atomics; the order of those
+//           additions, and so the last bits of the output, vary from run to
+//           run.
 // Exact τ: τ solves Σ_i [z_i − τ]_+^β = 1. Starting from τ = z_max − 1
 // (where the sum is ≥ 1) Newton steps on this convex decreasing function stay
 // below the root; after each step the closed-form root on the current support
@@ -171,6 +173,8 @@ __global__ void __launch_bounds__(kThreads, 2) pass_a_kernel(DecodeArgs a) {
   const size_t hq0 = (size_t)s * a.Hq + (size_t)kvh * G;  // first query head of the group
   const bool beta2 = a.beta == 2.0f;
   const bool gauss = a.policy == ENTMAXKV_POLICY_GAUSSIAN;
+  if (split == 0 && a.out)  // pass B adds its blocks' sums into these rows
+    for (int e = tid; e < G * a.D; e += kThreads) a.out[hq0 * a.D + e] = 0.0f;
   if (split == 0 && tid == 0) {
     a.nsel_ws[skv] = n_sel;
     if (a.n_sel_out) a.n_sel_out[skv] = n_sel;
@@ -594,49 +598,6 @@ struct VTraits<__nv_bfloat16> {
   }
 };
 
-// Sum of the split partials of one (sequence, KV head) in split order, by the
-// last block: float4 columns, the block's threads split over the partials.
-__device__ __noinline__ void combine_partials(const DecodeArgs& a, size_t skv, int parts,
-                                              float* out_rows, float4* red4) {
-  const int G = a.G, D = a.D, tid = threadIdx.x;
-  const int cols = G * D / 4;
-  const int groups = kThreads / cols > 0 ? kThreads / cols : 1;
-  const int col = tid % cols, grp = tid / cols;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (grp < groups) {
-    const float* base = a.partial + skv * a.splits * (size_t)a.pstride;
-    for (int sp0 = grp; sp0 < parts; sp0 += 8 * groups) {  // 8 loads in flight, summed in order
-      float4 v[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int sp = sp0 + u * groups;
-        v[u] = sp < parts ? __ldcg(reinterpret_cast<const float4*>(base + (size_t)sp * a.pstride) + col)
-                             : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        acc.x += v[u].x;
-        acc.y += v[u].y;
-        acc.z += v[u].z;
-        acc.w += v[u].w;
-      }
-    }
-    red4[grp * cols + col] = acc;
-  }
-  __syncthreads();
-  if (tid < cols) {
-    float4 sum = red4[tid];
-    for (int g2 = 1; g2 < groups; ++g2) {
-      const float4 v = red4[g2 * cols + tid];
-      sum.x += v.x;
-      sum.y += v.y;
-      sum.z += v.z;
-      sum.w += v.w;
-    }
-    reinterpret_cast<float4*>(out_rows)[tid] = sum;
-  }
-}
-
 // Pass B: for each kept page with some z above τ (every page with
 // ENTMAXKV_FLAG_DENSE_V) the warp stages the page's z in shared memory, issues
 // all its V loads at once (lane: 16 bytes of a row, tokens tg, tg+TG, ...),
@@ -650,11 +611,9 @@ __global__ void __launch_bounds__(kThreads, GP <= 4 ? 2 : 1) pass_b_kernel(Decod
   __shared__ __align__(16) float zs[kWarps][32 * 8];
   __shared__ __align__(16) float red[kWarps][GP][D];
   __shared__ float dsum[kWarps][GP];
-  __shared__ float4 red4[kThreads];
+  __shared__ int list_sh[kListCap];
   __shared__ uint64_t vbar[kWarps];
   extern __shared__ __align__(128) unsigned char vstage[];  // [kWarps][P][D] of T
-  static_assert(sizeof(red4) >= kListCap * sizeof(int), "the V page list shares the combine scratch");
-  int* list_sh = reinterpret_cast<int*>(red4);  // the page list is done before the combine starts
   __shared__ int scan_sh[32];
   __shared__ int last_sh;
   const int split = blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
@@ -766,7 +725,7 @@ __global__ void __launch_bounds__(kThreads, GP <= 4 ? 2 : 1) pass_b_kernel(Decod
   // ranks of the whole selection in rank order (a thread checks up to 32
   // consecutive ranks, one scan places them); the first `parts` blocks take
   // even shares of the list, a warp per page, so pages that cluster in rank
-  // still spread over the grid, and only those blocks write partials. Larger
+  // still spread over the grid, and only those blocks add to the output. Larger
   // selections are walked in the block's own rank range, kListCap ranks at a
   // time. Either way the block's pages sit in list_sh in rank order.
   int parts = a.splits;
@@ -904,15 +863,26 @@ __global__ void __launch_bounds__(kThreads, GP <= 4 ? 2 : 1) pass_b_kernel(Decod
     }
   }
   __syncthreads();
-  float* part = a.partial + (skv * a.splits + split) * (size_t)a.pstride;
-  for (int e = tid; e < G * D; e += kThreads) {
-    const int h = e / D, d = e % D;
-    float sum = 0.0f;
+  // The block's sums go straight into the output (zeroed by pass A) as
+  // vector float additions: no partials, no ticket, no combine. The order of
+  // the additions is the order blocks finish in.
+  float4* orow = reinterpret_cast<float4*>(a.out + hq0 * D);
+  for (int e = tid; e < G * D / 4; e += kThreads) {
+    const int h = (4 * e) / D, d = (4 * e) % D;
+    float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) sum += red[w][h][d];
-    part[e] = sum;
+    for (int w = 0; w < kWarps; ++w) {
+      const float4 r = *reinterpret_cast<const float4*>(&red[w][h][d]);
+      sum.x += r.x;
+      sum.y += r.y;
+      sum.z += r.z;
+      sum.w += r.w;
+    }
+    atomicAdd(orow + e, sum);
   }
-  if (a.policy == ENTMAXKV_POLICY_TOPK && tid < G) {
+  if (a.policy != ENTMAXKV_POLICY_TOPK) return;
+  // top-k: the last block turns the summed dropped-mass terms into δ̄
+  if (tid < G) {
     float sum = 0.0f;
     for (int w = 0; w < kWarps; ++w) sum += dsum[w][tid];
     if (sum != 0.0f) atomicAdd(&a.dbar[hq0 + tid], sum);
@@ -923,8 +893,7 @@ __global__ void __launch_bounds__(kThreads, GP <= 4 ? 2 : 1) pass_b_kernel(Decod
   __syncthreads();
   if (!last_sh) return;
   __threadfence();
-  combine_partials(a, skv, parts, a.out + hq0 * D, red4);
-  if (a.policy == ENTMAXKV_POLICY_TOPK && a.delta_out && tid < G)
+  if (a.delta_out && tid < G)
     a.delta_out[hq0 + tid] = L > 0 ? fminf(1.0f, __ldcg(&a.dbar[hq0 + tid])) : 0.0f;
 }
 
