@@ -362,6 +362,18 @@ __device__ __forceinline__ unsigned long long f2_fma(unsigned long long a, unsig
   return d;
 }
 
+__device__ __forceinline__ unsigned long long f2_mul(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ unsigned long long f2_add(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ unsigned long long f2_splat(float c) { return f2_pack(c, c); }
+
 // Block-wide exclusive scan of one int per thread (blockDim multiple of 32).
 // Returns the sum below this thread; `total` receives the block sum.
 __device__ __forceinline__ int block_exclusive_scan(int v, int* sh, int& total) {

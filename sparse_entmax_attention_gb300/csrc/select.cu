@@ -39,6 +39,69 @@ __device__ __forceinline__ float sqrt_2ln(int n, int P, float c_full) {
   return n == P ? c_full : sqrtf(2.0f * logf((float)n));
 }
 
+using u64 = unsigned long long;
+
+template <int N>
+__device__ __forceinline__ u64 horner_x2(const float (&c)[N], u64 w) {
+  u64 r = f2_splat(c[N - 1]);
+#pragma unroll
+  for (int i = N - 2; i >= 0; --i) r = f2_fma(r, w, f2_splat(c[i]));
+  return r;
+}
+
+// The moments of gauss_moment2 for two pages at once, in packed f32x2
+// arithmetic (one instruction for both pages wherever the step is a plain
+// add, multiply or fused multiply-add), accumulated with the pages' token
+// counts into (F, D1, D2) pairs. For β = 2 the D1 and D2 pairs come out
+// halved. The branches on the sign of t become arithmetic on h = [t > 0]:
+//   Φ = σ·R + h,  H1 = A + h·t,  H = σ·B + h·(1 + t²),  σ = 1 − 2h,
+// with R, A, B the Mills-ratio forms at x = |t| (R → Q(x) on the left,
+// 1 − Q(x) on the right, and likewise for the first and second partial
+// moments). Every input must be finite with ς > 0 (the caller floors ς).
+template <bool B2>
+__device__ __forceinline__ void moments_x2(u64 mb, u64 sr, u64 ir, u64 nr, u64 noff, u64& f,
+                                           u64& d1, u64& d2) {
+  constexpr float cR[EKV_MILLS_DEG + 1] = {EKV_MILLS_R};
+  constexpr float cA[EKV_MILLS_DEG + 1] = {EKV_MILLS_A};
+  constexpr float cB[EKV_MILLS_DEG + 1] = {EKV_MILLS_B};
+  const u64 t = f2_mul(f2_add(mb, noff), ir);
+  float t0, t1;
+  f2_unpack(t, t0, t1);
+  const u64 y = f2_fma(f2_pack(fminf(fabsf(t0), EKV_MILLS_XMAX), fminf(fabsf(t1), EKV_MILLS_XMAX)),
+                       f2_splat(0.33333334f), f2_splat(1.0f));
+  float y0, y1, u0, u1;
+  f2_unpack(y, y0, y1);
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(u0) : "f"(y0));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(u1) : "f"(y1));
+  const u64 u = f2_pack(u0, u1);
+  const u64 w = f2_fma(u, f2_splat(2.5f), f2_splat(-1.5f));
+  const u64 tt = f2_mul(t, t);
+  float a0, a1, e0, e1;
+  f2_unpack(f2_mul(tt, f2_splat(-0.72134752f)), a0, a1);  // −t²/(2 ln 2)
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e0) : "f"(a0));
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e1) : "f"(a1));
+  const u64 phi = f2_mul(f2_pack(e0, e1), f2_splat(0.3989422804f));
+  const u64 pu = f2_mul(phi, u);
+  const u64 pu2 = f2_mul(pu, u);
+  const u64 R = f2_mul(pu, horner_x2(cR, w));
+  const u64 A = f2_mul(pu2, horner_x2(cA, w));
+  const u64 h = f2_pack(t0 > 0.0f ? 1.0f : 0.0f, t1 > 0.0f ? 1.0f : 0.0f);
+  const u64 sg = f2_fma(h, f2_splat(-2.0f), f2_splat(1.0f));
+  const u64 Phi = f2_fma(sg, R, h);
+  const u64 H1 = f2_fma(h, t, A);
+  if (B2) {
+    const u64 B = f2_mul(f2_mul(pu2, u), horner_x2(cB, w));
+    const u64 H = f2_fma(sg, B, f2_fma(h, tt, h));
+    f = f2_fma(nr, f2_mul(f2_mul(sr, sr), H), f);  // n·ς²·H
+    d1 = f2_fma(nr, f2_mul(sr, H1), d1);            // n·ς·H1  (D1/2)
+    d2 = f2_fma(nr, Phi, d2);                       // n·Φ     (D2/2)
+  } else {
+    f = f2_fma(nr, f2_mul(sr, H1), f);   // n·ς·H1
+    d1 = f2_fma(nr, Phi, d1);            // n·Φ
+    d2 = f2_fma(nr, f2_mul(phi, ir), d2);  // n·φ/ς
+  }
+}
+
 // All arithmetic is float, on offsets from base = max_p m_p − 1 (each page's
 // m_p − base is formed once), so every τ̂ is base + off with off = O(1).
 // Per iteration each warp publishes its partial (F, F', F'') in shared memory;
@@ -46,6 +109,7 @@ __device__ __forceinline__ float sqrt_2ln(int n, int P, float c_full) {
 // kTauhatCluster·kWarps partials over distributed shared memory, sums them in
 // a fixed butterfly order and takes the same step: all copies of the state
 // stay bit-identical without further synchronisation.
+template <bool B2>
 __global__ void __cluster_dims__(kTauhatCluster, 1, 1) __launch_bounds__(kThreads, 2)
     tauhat_kernel(DecodeArgs a) {
   pdl_enter();
@@ -63,22 +127,22 @@ __global__ void __cluster_dims__(kTauhatCluster, 1, 1) __launch_bounds__(kThread
   const int L = seq_len_clamped(a.seq_lens, seq, a.maxp, a.P, nullptr);
   const int n_pages = (L + a.P - 1) / a.P;
   if (n_pages == 0) return;
-  const bool beta2 = a.beta == 2.0f;
   const float2* ms = a.gauss_ms + ((size_t)s * a.Hq + h) * a.maxp;
   const int words = (n_pages + 31) / 32;
   const int chunk = ((words + kTauhatCluster - 1) / kTauhatCluster) * 32;
   const int p_lo = rank * chunk, p_hi = min(n_pages, p_lo + chunk);
 
   // This thread's pages stay in registers for every iteration (kRegPages
-  // each, which covers 8·256·kRegPages pages per query head); pages beyond
-  // that are re-read from memory. Their loads are issued before the maximum
-  // is known.
-  constexpr int kRegPages = 16;
-  float mb[kRegPages], sr[kRegPages], ir[kRegPages], nr[kRegPages];
+  // each, which covers 8·256·kRegPages pages per query head), as pairs for
+  // the packed arithmetic; pages beyond that are re-read from memory. Their
+  // loads are issued before the maximum is known. An empty slot holds a
+  // finite page of zero weight far below every threshold.
+  constexpr int kRegPages = 16, kPairs = kRegPages / 2;
+  float mb[kRegPages], sr[kRegPages], nr[kRegPages];
 #pragma unroll
   for (int k = 0; k < kRegPages; ++k) {
     const int p = p_lo + tid + k * kThreads;
-    float2 v = make_float2(-CUDART_INF_F, 0.0f);
+    float2 v = make_float2(-1e18f, 1.0f);
     nr[k] = 0.0f;
     if (p < p_hi) {
       v = ms[p];
@@ -98,28 +162,40 @@ __global__ void __cluster_dims__(kTauhatCluster, 1, 1) __launch_bounds__(kThread
   for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wmax_sh[w]);
   if (!(M > -CUDART_INF_F)) return;  // no readable page
   const float base = M - 1.0f;
+  // ς is floored at 2^-24·max(1, |m − base|): a point mass (ς = 0) then
+  // becomes a Gaussian whose moments differ from the point mass's by
+  // O(ς²) ≈ 1e-14 relative, and t = (m − τ)/ς stays finite, so the packed
+  // evaluation needs no branch per page.
+  u64 mb2[kPairs], sr2[kPairs], ir2[kPairs], nr2[kPairs];
 #pragma unroll
   for (int k = 0; k < kRegPages; ++k) {
     mb[k] -= base;
-    ir[k] = sr[k] > 0.0f ? 1.0f / sr[k] : 0.0f;
+    sr[k] = fmaxf(sr[k], 0x1p-24f * fmaxf(1.0f, fabsf(mb[k])));
+  }
+#pragma unroll
+  for (int i = 0; i < kPairs; ++i) {
+    mb2[i] = f2_pack(mb[2 * i], mb[2 * i + 1]);
+    sr2[i] = f2_pack(sr[2 * i], sr[2 * i + 1]);
+    ir2[i] = f2_pack(1.0f / sr[2 * i], 1.0f / sr[2 * i + 1]);
+    nr2[i] = f2_pack(nr[2 * i], nr[2 * i + 1]);
   }
   float lo = 0.0f, hi = CUDART_INF_F, off = 0.0f;  // offsets from base; F(lo) ≥ 1
   bool converged = false;
   int it = 0;
   for (; it < kTauhatIters; ++it) {
-    float f = 0.0f, df = 0.0f, d2f = 0.0f;
+    u64 f2 = 0ull, df2 = 0ull, d2f2 = 0ull;
+    const u64 noff = f2_splat(-off);
 #pragma unroll
-    for (int k = 0; k < kRegPages; ++k) {
-      float g, dg, d2g;
-      gauss_moment2(mb[k] - off, sr[k], ir[k], beta2, g, dg, d2g);
-      f = fmaf(nr[k], g, f);
-      df = fmaf(nr[k], dg, df);
-      d2f = fmaf(nr[k], d2g, d2f);
+    for (int i = 0; i < kPairs; ++i) moments_x2<B2>(mb2[i], sr2[i], ir2[i], nr2[i], noff, f2, df2, d2f2);
+    float f = f2_sum(f2), df = f2_sum(df2), d2f = f2_sum(d2f2);
+    if (B2) {
+      df *= 2.0f;
+      d2f *= 2.0f;
     }
     for (int p = p_lo + tid + kRegPages * kThreads; p < p_hi; p += kThreads) {
       const float2 v = ms[p];
       float g, dg, d2g;
-      gauss_moment2((v.x - base) - off, v.y, v.y > 0.0f ? 1.0f / v.y : 0.0f, beta2, g, dg, d2g);
+      gauss_moment2((v.x - base) - off, v.y, v.y > 0.0f ? 1.0f / v.y : 0.0f, B2, g, dg, d2g);
       const float np = (float)page_tokens(p, n_pages, L, a.P);
       f = fmaf(np, g, f);
       df = fmaf(np, dg, df);
@@ -198,7 +274,12 @@ __global__ void __cluster_dims__(kTauhatCluster, 1, 1) __launch_bounds__(kThread
     const int p0 = p_lo + warp * 32 + k * kThreads;
     if (p0 >= p_hi) break;
     const int p = p0 + lane;
-    const bool sel = p < p_hi && mb[k] + sr[k] * sqrt_2ln((int)nr[k], a.P, c_full) >= thr;
+    float m_lo, m_hi, s_lo, s_hi, n_lo, n_hi;
+    f2_unpack(mb2[k / 2], m_lo, m_hi);
+    f2_unpack(sr2[k / 2], s_lo, s_hi);
+    f2_unpack(nr2[k / 2], n_lo, n_hi);
+    const float mk = k & 1 ? m_hi : m_lo, sk = k & 1 ? s_hi : s_lo, nk = k & 1 ? n_hi : n_lo;
+    const bool sel = p < p_hi && mk + sk * sqrt_2ln((int)nk, a.P, c_full) >= thr;
     const uint32_t bits = __ballot_sync(0xffffffffu, sel);
     if (lane == 0 && bits) atomicOr(&bm[p0 >> 5], bits);
   }
@@ -346,7 +427,8 @@ __global__ void __launch_bounds__(1024) topk_kernel(DecodeArgs a, int mode) {
 
 cudaError_t launch_tauhat(const DecodeArgs& a, cudaStream_t st) {
   dim3 grid(kTauhatCluster, a.Hq, a.S);
-  launch_k(false, tauhat_kernel, dim3(grid), dim3(kThreads), 0, st, a);
+  if (a.beta == 2.0f) launch_k(false, tauhat_kernel<true>, dim3(grid), dim3(kThreads), 0, st, a);
+  else launch_k(false, tauhat_kernel<false>, dim3(grid), dim3(kThreads), 0, st, a);
   return cudaGetLastError();
 }
 
