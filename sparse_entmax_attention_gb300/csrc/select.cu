@@ -115,7 +115,9 @@ __global__ void __cluster_dims__(kTauhatCluster, 1, 1) __launch_bounds__(kThread
   pdl_enter();
   static_assert(kTauhatCluster * kWarps == 64, "two partials per lane");
   cg::cluster_group cluster = cg::this_cluster();
-  __shared__ float3 slot[2][kWarps];
+  // Every warp of the cluster pushes its partial (F, D1, D2) into this slot
+  // of every block, so after the cluster barrier all reads are local.
+  __shared__ float4 slot[2][kTauhatCluster * kWarps];
   __shared__ float wmax_sh[kWarps];
   const int h = blockIdx.y, s = blockIdx.z;
   const int kvh = h / a.G;
@@ -161,6 +163,7 @@ __global__ void __cluster_dims__(kTauhatCluster, 1, 1) __launch_bounds__(kThread
 #pragma unroll
   for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wmax_sh[w]);
   if (!(M > -CUDART_INF_F)) return;  // no readable page
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;\n" ::: "memory");
   const float base = M - 1.0f;
   // ς is floored at 2^-24·max(1, |m − base|): a point mass (ς = 0) then
   // becomes a Gaussian whose moments differ from the point mass's by
@@ -204,10 +207,15 @@ __global__ void __cluster_dims__(kTauhatCluster, 1, 1) __launch_bounds__(kThread
     f = warp_sum(f);
     df = warp_sum(df);
     d2f = warp_sum(d2f);
-    if (lane == 0) slot[it & 1][warp] = make_float3(f, df, d2f);
+    // Before the first push every block of the cluster must be running (the
+    // arrive was posted after the early exits). A slot half is rewritten two
+    // iterations later, and no block gets there before every block has passed
+    // the next barrier, i.e. finished reading it.
+    if (it == 0) asm volatile("barrier.cluster.wait.aligned;\n" ::: "memory");
+    if (lane < kTauhatCluster)
+      cluster.map_shared_rank(&slot[it & 1][0], lane)[rank * kWarps + warp] = make_float4(f, df, d2f, 0.0f);
     cluster.sync();
-    const float3 e0 = cluster.map_shared_rank(&slot[it & 1][0], lane / kWarps)[lane % kWarps];
-    const float3 e1 = cluster.map_shared_rank(&slot[it & 1][0], (lane + 32) / kWarps)[lane % kWarps];
+    const float4 e0 = slot[it & 1][lane], e1 = slot[it & 1][lane + 32];
     float F = e0.x + e1.x, D1 = e0.y + e1.y, D2 = e0.z + e1.z;  // F, −dF/dτ, d²F/dτ²
     F = warp_sum(F);
     D1 = warp_sum(D1);
@@ -257,7 +265,9 @@ __global__ void __cluster_dims__(kTauhatCluster, 1, 1) __launch_bounds__(kThread
       break;
     }
   }
-  cluster.sync();  // no block leaves while another may still read its slots
+  // Every block leaves the loop at the same iteration with the same state,
+  // and all pushes into this block landed before the last barrier: no
+  // block touches another's shared memory from here on.
   if (rank == 0 && tid == 0) {
     a.tauhat[(size_t)s * a.Hq + h] = base + off;
     a.diag[(size_t)s * a.Hq + h] = it + 1;
