@@ -447,8 +447,11 @@ __device__ __forceinline__ void block_page_range(const DecodeArgs& a, int s, int
     hi = (int)(((long long)n_sel * (split + 1)) / a.splits);
     return;
   }
+  // Every word of the row is read, so the loads need not wait for the
+  // sequence length: the decode clears the bitmap before any bit is set, and
+  // no bit past the sequence's last page is ever set.
   const uint32_t* bm = a.bitmap + ((size_t)s * a.Hkv + kvh) * a.words;
-  const int W = (n_pages + 31) / 32;
+  const int W = a.words;
   const int wpt = (W + kThreads - 1) / kThreads;
   const int w0 = threadIdx.x * wpt;
   int cnt = 0;

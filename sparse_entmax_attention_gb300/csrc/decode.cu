@@ -159,6 +159,7 @@ __global__ void __launch_bounds__(kThreads, 2) pass_a_kernel(DecodeArgs a) {
   __shared__ float T0_sh[8], tlb_sh[8];
   __shared__ int nc_sh[8], np_sh[8], nz_sh[8], off_sh[9];
   __shared__ float tauf_sh[8];
+  __shared__ int vcnt_sh, spec_all_sh;
   const int split = blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = a.G, P = a.P;
@@ -166,11 +167,18 @@ __global__ void __launch_bounds__(kThreads, 2) pass_a_kernel(DecodeArgs a) {
   const int L = seq_len_clamped(a.seq_lens, seq, a.maxp, P, tid == 0 ? a.status : nullptr);
   const int n_pages = (L + P - 1) / P;
   if (tid < 8) kept_sh[tid] = 0.0f;  // published by the barriers of the page range
+  const size_t skv = (size_t)s * a.Hkv + kvh;
+  const size_t hq0 = (size_t)s * a.Hq + (size_t)kvh * G;  // first query head of the group
+  // q depends on nothing: its loads overlap the page range's
+  uint32_t bq[D / 16][2];
+  if constexpr (sizeof(T) == 2) {
+    load_q_bfrag<D>((const __nv_bfloat16*)a.q + hq0 * D, G, lane, bq);
+  } else {
+    for (int i = tid; i < G * D; i += kThreads) qs[i / D][i % D] = ((const float*)a.q)[hq0 * D + i];
+  }
   int n_sel, lo, hi;
   block_page_range(a, s, kvh, n_pages, split, list, sh_scan, n_sel, lo, hi);
   const bool bitmap = uses_bitmap(a.policy);
-  const size_t skv = (size_t)s * a.Hkv + kvh;
-  const size_t hq0 = (size_t)s * a.Hq + (size_t)kvh * G;  // first query head of the group
   const bool beta2 = a.beta == 2.0f;
   const bool gauss = a.policy == ENTMAXKV_POLICY_GAUSSIAN;
   if (split == 0 && a.out)  // pass B adds its blocks' sums into these rows
@@ -215,12 +223,6 @@ __global__ void __launch_bounds__(kThreads, 2) pass_a_kernel(DecodeArgs a) {
       gauss_moment(v.x - th, v.y, beta2, g, dg);
       atomicAdd(&kept_sh[h], (float)min(P, L - page * P) * g);
     }
-  }
-  uint32_t bq[D / 16][2];
-  if constexpr (sizeof(T) == 2) {
-    load_q_bfrag<D>((const __nv_bfloat16*)a.q + hq0 * D, G, lane, bq);
-  } else {
-    for (int i = tid; i < G * D; i += kThreads) qs[i / D][i % D] = ((const float*)a.q)[hq0 * D + i];
   }
   __syncthreads();
 
@@ -388,6 +390,19 @@ __global__ void __launch_bounds__(kThreads, 2) pass_a_kernel(DecodeArgs a) {
   float* zc = pool + kSolveCap / 2;
   const float* zbase = a.z + skv * a.cap_pages * (size_t)P * G;
   const int2* clist = a.cand + hq0 * a.cap_pages;
+  // Thread tid also loads, with the counts, entry js of head hs's list (a
+  // fixed slot; stale past the count, so used only below it). When every list
+  // fits its slots, step A needs no further load, and a thread whose entry
+  // clears T0 starts the page's (page, phys) lookup for the V list at once.
+  const int SPH = kThreads / G;
+  const int hs = tid / SPH, js = tid - hs * SPH;
+  int2 ce = make_int2(0, __float_as_int(-CUDART_INF_F));
+  if (hs < G) ce = __ldcg(clist + (size_t)hs * a.cap_pages + js);
+  // V-list page bitmap over the selection's ranks (the page-id arrays are free now)
+  const int Wv = (n_sel + 31) >> 5;
+  uint32_t* vb = reinterpret_cast<uint32_t*>(phys_sh);
+  if (Wv <= kListCap)
+    for (int i = tid; i < Wv; i += kThreads) vb[i] = 0u;
   if (tid < G) {
     const float zm = ord_dec(__ldcg(&a.zmax[hq0 + tid]));
     T0_sh[tid] = zm > -CUDART_INF_F ? zm - 1.0f : CUDART_INF_F;
@@ -398,22 +413,41 @@ __global__ void __launch_bounds__(kThreads, 2) pass_a_kernel(DecodeArgs a) {
   __syncthreads();
   if (tid == 0) {
     int t = 0;
+    bool fits = Wv <= kListCap;
     for (int h = 0; h < G; ++h) {
       off_sh[h] = t;
       t += nc_sh[h];
+      fits = fits && nc_sh[h] <= SPH;
     }
     off_sh[G] = t;
+    spec_all_sh = fits;
+    vcnt_sh = 0;
   }
   __syncthreads();
-  for (int e = tid; e < off_sh[G]; e += kThreads) {  // A
-    int h = 0;
-    while (e >= off_sh[h + 1]) ++h;
-    const int2 c = __ldcg(clist + (size_t)h * a.cap_pages + (e - off_sh[h]));
-    if (__int_as_float(c.y) > T0_sh[h]) {
-      const int pos = atomicAdd(&np_sh[h], 1);
+  const bool spec_all = spec_all_sh;
+  bool kept = false;  // this thread's slot entry clears T0 (spec_all only)
+  int2 kpp = make_int2(0, -1);
+  if (spec_all) {  // A, from the slots
+    if (hs < G && js < nc_sh[hs] && __int_as_float(ce.y) > T0_sh[hs]) {
+      kept = true;
+      kpp = __ldcg(&a.sel_pp[skv * a.cap_pages + ce.x]);  // consumed after D
+      const int pos = atomicAdd(&np_sh[hs], 1);
       if (pos < capP) {
-        pv[h * capP + pos] = __int_as_float(c.y);
-        pr[h * capP + pos] = c.x;
+        pv[hs * capP + pos] = __int_as_float(ce.y);
+        pr[hs * capP + pos] = ce.x;
+      }
+    }
+  } else {
+    for (int e = tid; e < off_sh[G]; e += kThreads) {  // A
+      int h = 0;
+      while (e >= off_sh[h + 1]) ++h;
+      const int2 c = __ldcg(clist + (size_t)h * a.cap_pages + (e - off_sh[h]));
+      if (__int_as_float(c.y) > T0_sh[h]) {
+        const int pos = atomicAdd(&np_sh[h], 1);
+        if (pos < capP) {
+          pv[h * capP + pos] = __int_as_float(c.y);
+          pr[h * capP + pos] = c.x;
+        }
       }
     }
   }
@@ -513,6 +547,20 @@ __global__ void __launch_bounds__(kThreads, 2) pass_a_kernel(DecodeArgs a) {
   // in a rank bitmap (in the score region, free after D), read back in rank
   // order into a shared list over the page maxima (free now), and written
   // out with their logical and physical pages.
+  __syncthreads();  // the solves are done with the scores; τ of every head is in tauf_sh
+  if (spec_all) {
+    // Every page of the V list is the page of some kept slot entry (its max
+    // clears τ_h ≥ T0_h); the first entry to set the page's bit writes it,
+    // with the (page, phys) its thread looked up in step A.
+    if (kept && __int_as_float(ce.y) > tauf_sh[hs]) {
+      const uint32_t bit = 1u << (ce.x & 31);
+      if (!(atomicOr(&vb[ce.x >> 5], bit) & bit))
+        a.vlist[skv * a.cap_pages + atomicAdd(&vcnt_sh, 1)] = make_int4(ce.x, kpp.x, kpp.y, 0);
+    }
+    __syncthreads();
+    if (tid == 0) a.vcount[skv] = vcnt_sh;
+    return;
+  }
   const int W = (n_sel + 31) >> 5;
   uint32_t* vbm = reinterpret_cast<uint32_t*>(zc);
   int* vls = reinterpret_cast<int*>(pool);
@@ -520,7 +568,6 @@ __global__ void __launch_bounds__(kThreads, 2) pass_a_kernel(DecodeArgs a) {
     if (tid == 0) a.vcount[skv] = -1;
     return;
   }
-  __syncthreads();  // the solves are done with the scores
   for (int i = tid; i < W; i += kThreads) vbm[i] = 0u;
   if (tid == 0) {
     int t = 0;
@@ -630,6 +677,15 @@ __global__ void __launch_bounds__(kThreads, GP <= 4 ? 2 : 1) pass_b_kernel(Decod
   const int lo = (int)(((long long)n_sel * split) / a.splits);
   const int hi = (int)(((long long)n_sel * (split + 1)) / a.splits);
   if (tid < GP) tau_sh[tid] = tid < G ? __ldcg(&a.tau_ws[hq0 + tid]) : CUDART_INF;
+  const bool dense = (a.flags & ENTMAXKV_FLAG_DENSE_V) != 0;
+  // Pass A's count of pages that need V, and this warp's entry of its list at
+  // the fixed position block·kWarps + warp (where it is whenever the list
+  // holds at most kWarps pages a block), both loaded with the values above so
+  // the V copy can be issued after one round trip.
+  const int vc = dense ? -1 : __ldcg(&a.vcount[skv]);
+  const int spec_i = split * kWarps + warp;
+  int4 spec_e = make_int4(0, 0, -1, 0);
+  if (!dense && spec_i < a.cap_pages) spec_e = __ldcg(&a.vlist[skv * a.cap_pages + spec_i]);
   __syncthreads();
   float tau[GP];   // bf16 pages: p from fp32 z − τ
   double taud[GP]; // fp32 pages: p from z − τ in double (z's own rounding only)
@@ -638,7 +694,6 @@ __global__ void __launch_bounds__(kThreads, GP <= 4 ? 2 : 1) pass_b_kernel(Decod
     taud[h] = tau_sh[h];
     tau[h] = (float)taud[h];
   }
-  const bool dense = (a.flags & ENTMAXKV_FLAG_DENSE_V) != 0;
   unsigned long long accp[GP][VEC / 2];  // fp32 pairs of columns, for the paired FMA
 #pragma unroll
   for (int h = 0; h < GP; ++h)
@@ -730,14 +785,17 @@ __global__ void __launch_bounds__(kThreads, GP <= 4 ? 2 : 1) pass_b_kernel(Decod
   // time. Either way the block's pages sit in list_sh in rank order.
   int parts = a.splits;
   bool global_list = false;
+  bool spec_ok = false;  // this block's share starts at split·kWarps: the warps hold their entries
   int n_list = 0;
-  const int vc = dense ? -1 : __ldcg(&a.vcount[skv]);
   const int4* vl = nullptr;  // this block's share of pass A's list, when it built one
   if (vc >= 0) {
     // top-k keeps every block: each one also sums its share of the δ̄ bound
     parts = a.policy == ENTMAXKV_POLICY_TOPK ? a.splits : max(1, min(a.splits, (vc + kWarps - 1) / kWarps));
     global_list = true;
-    if (split < parts) {
+    if (vc <= kWarps * a.splits) {  // kWarps pages a block, in list order
+      spec_ok = true;
+      n_list = max(0, min(kWarps, vc - split * kWarps));
+    } else if (split < parts) {
       const int s_lo = (int)(((long long)vc * split) / parts);
       n_list = (int)(((long long)vc * (split + 1)) / parts) - s_lo;
       vl = a.vlist + skv * a.cap_pages + s_lo;
@@ -805,7 +863,9 @@ __global__ void __launch_bounds__(kThreads, GP <= 4 ? 2 : 1) pass_b_kernel(Decod
       __syncthreads();
     }
     for (int jj = warp; jj < n_list; jj += kWarps) {
-      if (vl) {
+      if (spec_ok) {
+        if (spec_e.z >= 0) do_page(spec_e.x, spec_e.y, spec_e.z);
+      } else if (vl) {
         const int4 e = __ldcg(vl + jj);
         if (e.z >= 0) do_page(e.x, e.y, e.z);
       } else {

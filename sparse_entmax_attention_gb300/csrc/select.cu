@@ -230,15 +230,20 @@ __global__ void __cluster_dims__(kTauhatCluster, 1, 1) __launch_bounds__(kThread
     } else {
       // Halley on g = log F: g' = −D1/F, g'' = D2/F − g'²; Newton when not
       // usable. A step below the tolerance ends the solve (in float it may not
-      // even move off, so it must not be judged against the bracket).
+      // even move off, so it must not be judged against the bracket). The
+      // step is computed with the fast log and divide: F itself is evaluated
+      // exactly at every point, and the last step, which is not re-evaluated,
+      // inherits only the fast log's absolute error near F = 1 (about 2^-21,
+      // divided by |g'| ≈ 2–5), under the solve's tolerance.
       next = CUDART_NAN_F;
       stop = false;
       const float tol = 1e-6f * fmaxf(1.0f, fabsf(base + off));
       if (F > 0.0f && D1 > 0.0f) {
-        const float g = logf(F), g1 = -D1 / F, g2 = D2 / F - g1 * g1;
+        const float rF = __frcp_rn(F);
+        const float g = __logf(F), g1 = -D1 * rF, g2 = D2 * rF - g1 * g1;
         const float den = 2.0f * g1 * g1 - g * g2;
-        const float newton = -g / g1;
-        const float step = den > 0.0f ? -2.0f * g * g1 / den : newton;
+        const float newton = -__fdividef(g, g1);
+        const float step = den > 0.0f ? -2.0f * __fdividef(g * g1, den) : newton;
         if (fabsf(step) <= tol) {
           next = off + step;
           stop = true;
