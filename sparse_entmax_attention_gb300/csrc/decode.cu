@@ -139,6 +139,42 @@ __device__ double solve_tau_warp(const SolveSrc& S, double tau0, float beta, boo
   return tau;
 }
 
+// Exact threshold of at most 32 values (β = 1 or 2) without iterating. Lane i
+// takes the set {z_j ≥ z_i} and its closed-form root δ_i (β = 2: Σ (y − δ)² = 1
+// on the branch δ ≤ min y, in the conjugate form; β = 1: Σ (y − δ) = 1), with
+// y = z − base > 0. A root that does not exceed its set's smallest value is a
+// lower bound of the threshold (the normaliser is ≥ 1 there), and the root of
+// the true support is the threshold itself, so the threshold is the largest
+// such root. Float arithmetic: about 1e-6 from the exact value. Returns NaN
+// for an empty set.
+__device__ __forceinline__ float direct_tau_warp(const float* zs, int m, float base, bool b2) {
+  const int lane = threadIdx.x & 31;
+  const float yi = lane < m ? zs[lane] - base : -CUDART_INF_F;
+  float k = 0.0f, s1 = 0.0f, s2 = 0.0f;
+#pragma unroll 8
+  for (int j = 0; j < 32; ++j) {
+    const float yj = __shfl_sync(0xffffffffu, yi, j);
+    if (yj >= yi) {
+      k += 1.0f;
+      s1 += yj;
+      s2 = fmaf(yj, yj, s2);
+    }
+  }
+  float d = -CUDART_INF_F;
+  if (lane < m) {
+    float r = CUDART_NAN_F;
+    if (b2) {
+      const float disc = s1 * s1 - k * (s2 - 1.0f);
+      if (disc >= 0.0f) r = (s2 - 1.0f) / (s1 + sqrtf(disc));
+    } else {
+      r = (s1 - 1.0f) / k;
+    }
+    if (r <= yi) d = r;
+  }
+  d = warp_max(d);
+  return m > 0 ? base + d : CUDART_NAN_F;
+}
+
 // ---------------------------------------------------------------------------
 
 template <typename T, int D>
@@ -158,7 +194,7 @@ __global__ void __launch_bounds__(kThreads, 2) pass_a_kernel(DecodeArgs a) {
   static_assert(kListCap * 8 <= kSolveCap, "page maxima of a block fit the pool");
   __shared__ float T0_sh[8], tlb_sh[8];
   __shared__ int nc_sh[8], np_sh[8], nz_sh[8], off_sh[9];
-  __shared__ float tauf_sh[8];
+  __shared__ float tauf_sh[8], km_sh[8];
   __shared__ int vcnt_sh, spec_all_sh;
   const int split = blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -390,14 +426,20 @@ __global__ void __launch_bounds__(kThreads, 2) pass_a_kernel(DecodeArgs a) {
   float* zc = pool + kSolveCap / 2;
   const float* zbase = a.z + skv * a.cap_pages * (size_t)P * G;
   const int2* clist = a.cand + hq0 * a.cap_pages;
-  // Thread tid also loads, with the counts, entry js of head hs's list (a
-  // fixed slot; stale past the count, so used only below it). When every list
-  // fits its slots, step A needs no further load, and a thread whose entry
-  // clears T0 starts the page's (page, phys) lookup for the V list at once.
-  const int SPH = kThreads / G;
-  const int hs = tid / SPH, js = tid - hs * SPH;
-  int2 ce = make_int2(0, __float_as_int(-CUDART_INF_F));
-  if (hs < G) ce = __ldcg(clist + (size_t)hs * a.cap_pages + js);
+  // Thread tid also loads, with the counts, entries js + k·SPT (k < kSlots)
+  // of head hs's list (fixed slots; stale past the count, so used only below
+  // it). When every list fits its slots, step A needs no further load, and a
+  // thread whose entry clears T0 starts the page's (page, phys) lookup for the
+  // V list at once.
+  constexpr int kSlots = 4;
+  const int SPT = kThreads / G, SPH = kSlots * SPT;  // slots per head
+  const int hs = tid / SPT, js = tid - hs * SPT;
+  int2 ce[kSlots];
+#pragma unroll
+  for (int k = 0; k < kSlots; ++k) {
+    ce[k] = make_int2(0, __float_as_int(-CUDART_INF_F));
+    if (hs < G && js + k * SPT < a.cap_pages) ce[k] = __ldcg(clist + (size_t)hs * a.cap_pages + js + k * SPT);
+  }
   // V-list page bitmap over the selection's ranks (the page-id arrays are free now)
   const int Wv = (n_sel + 31) >> 5;
   uint32_t* vb = reinterpret_cast<uint32_t*>(phys_sh);
@@ -407,6 +449,7 @@ __global__ void __launch_bounds__(kThreads, 2) pass_a_kernel(DecodeArgs a) {
     const float zm = ord_dec(__ldcg(&a.zmax[hq0 + tid]));
     T0_sh[tid] = zm > -CUDART_INF_F ? zm - 1.0f : CUDART_INF_F;
     nc_sh[tid] = min(__ldcg(&a.cand_cnt[hq0 + tid]), a.cap_pages);
+    km_sh[tid] = gauss ? __ldcg(&a.kept_mass[hq0 + tid]) : 0.0f;
     np_sh[tid] = 0;
     nz_sh[tid] = 0;
   }
@@ -425,16 +468,20 @@ __global__ void __launch_bounds__(kThreads, 2) pass_a_kernel(DecodeArgs a) {
   }
   __syncthreads();
   const bool spec_all = spec_all_sh;
-  bool kept = false;  // this thread's slot entry clears T0 (spec_all only)
-  int2 kpp = make_int2(0, -1);
+  uint32_t kept = 0u;  // bit k: slot k's entry clears T0 (spec_all only)
+  int2 kpp[kSlots];
   if (spec_all) {  // A, from the slots
-    if (hs < G && js < nc_sh[hs] && __int_as_float(ce.y) > T0_sh[hs]) {
-      kept = true;
-      kpp = __ldcg(&a.sel_pp[skv * a.cap_pages + ce.x]);  // consumed after D
-      const int pos = atomicAdd(&np_sh[hs], 1);
-      if (pos < capP) {
-        pv[hs * capP + pos] = __int_as_float(ce.y);
-        pr[hs * capP + pos] = ce.x;
+#pragma unroll
+    for (int k = 0; k < kSlots; ++k) {
+      kpp[k] = make_int2(0, -1);
+      if (hs < G && js + k * SPT < nc_sh[hs] && __int_as_float(ce[k].y) > T0_sh[hs]) {
+        kept |= 1u << k;
+        kpp[k] = __ldcg(&a.sel_pp[skv * a.cap_pages + ce[k].x]);  // consumed after D
+        const int pos = atomicAdd(&np_sh[hs], 1);
+        if (pos < capP) {
+          pv[hs * capP + pos] = __int_as_float(ce[k].y);
+          pr[hs * capP + pos] = ce[k].x;
+        }
       }
     }
   } else {
@@ -456,7 +503,12 @@ __global__ void __launch_bounds__(kThreads, 2) pass_a_kernel(DecodeArgs a) {
     const int h = warp;
     float tlb = T0_sh[h];
     const int np = min(np_sh[h], capP);
-    if (np > 0) {
+    if (np > 0 && np <= 32 && (a.beta == 2.0f || a.beta == 1.0f)) {
+      // a lower bound needs no more than float accuracy: the direct root,
+      // lowered by a margin well above its error
+      const float tb = direct_tau_warp(pv + h * capP, np, tlb, a.beta == 2.0f);
+      if (tb > tlb) tlb = fmaxf(tlb, tb - 1e-5f * fmaxf(1.0f, fabsf(tb)));
+    } else if (np > 0) {
       SolveSrc src;
       src.zs = pv + h * capP;
       src.m = np;
@@ -524,8 +576,16 @@ __global__ void __launch_bounds__(kThreads, 2) pass_a_kernel(DecodeArgs a) {
       src.hg = hg;
       src.T0 = tlb_sh[hg];
       if (src.big && lane == 0) raise_flag(a.status, ENTMAXKV_DEV_CAND_OVERFLOW);
+      // With few scores the direct root, lowered by a margin above its error,
+      // starts the solve just below τ: usually one closed-form check on the
+      // final support ends it.
+      double t0 = (double)src.T0;
+      if (!src.big && src.m <= 32 && (a.beta == 2.0f || a.beta == 1.0f)) {
+        const float td = direct_tau_warp(src.zs, src.m, src.T0, a.beta == 2.0f);
+        if (td > src.T0) t0 = fmax(t0, (double)td - 1e-5 * fmax(1.0, fabs((double)td)));
+      }
       bool ok;
-      tau_d = solve_tau_warp(src, (double)src.T0, a.beta, ok);
+      tau_d = solve_tau_warp(src, t0, a.beta, ok);
       if (!ok && lane == 0) raise_flag(a.status, ENTMAXKV_DEV_TAU_NOCONV);
       tau_f = (float)tau_d;
     }
@@ -535,7 +595,7 @@ __global__ void __launch_bounds__(kThreads, 2) pass_a_kernel(DecodeArgs a) {
       if (a.tau_out) a.tau_out[hs] = tau_f;
       if (a.delta_out) {
         if (a.policy == ENTMAXKV_POLICY_GAUSSIAN)
-          a.delta_out[hs] = L > 0 ? fminf(1.0f, fmaxf(0.0f, 1.0f - __ldcg(&a.kept_mass[hs]))) : 0.0f;
+          a.delta_out[hs] = L > 0 ? fminf(1.0f, fmaxf(0.0f, 1.0f - km_sh[hg])) : 0.0f;
         else if (a.policy == ENTMAXKV_POLICY_FULL)
           a.delta_out[hs] = 0.0f;
       }
@@ -552,10 +612,13 @@ __global__ void __launch_bounds__(kThreads, 2) pass_a_kernel(DecodeArgs a) {
     // Every page of the V list is the page of some kept slot entry (its max
     // clears τ_h ≥ T0_h); the first entry to set the page's bit writes it,
     // with the (page, phys) its thread looked up in step A.
-    if (kept && __int_as_float(ce.y) > tauf_sh[hs]) {
-      const uint32_t bit = 1u << (ce.x & 31);
-      if (!(atomicOr(&vb[ce.x >> 5], bit) & bit))
-        a.vlist[skv * a.cap_pages + atomicAdd(&vcnt_sh, 1)] = make_int4(ce.x, kpp.x, kpp.y, 0);
+#pragma unroll
+    for (int k = 0; k < kSlots; ++k) {
+      if (((kept >> k) & 1u) && __int_as_float(ce[k].y) > tauf_sh[hs]) {
+        const uint32_t bit = 1u << (ce[k].x & 31);
+        if (!(atomicOr(&vb[ce[k].x >> 5], bit) & bit))
+          a.vlist[skv * a.cap_pages + atomicAdd(&vcnt_sh, 1)] = make_int4(ce[k].x, kpp[k].x, kpp[k].y, 0);
+      }
     }
     __syncthreads();
     if (tid == 0) a.vcount[skv] = vcnt_sh;
