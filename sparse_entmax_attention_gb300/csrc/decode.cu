@@ -408,7 +408,15 @@ __global__ void __launch_bounds__(kThreads, 2) pass_a_kernel(DecodeArgs a) {
   __syncthreads();
   if (tid == 0) last_sh = atomicAdd(&a.cnt_a[skv], 1) == a.splits - 1;
   __syncthreads();
-  if (!last_sh) return;
+  // A block that is not the last runs the tail below once as a dry run:
+  // every candidate's rank reads as 0 and each head's list as at most one
+  // entry, so all its loads stay in bounds and it is short, and it stores
+  // nothing to global memory. The tail runs once per decode, after the
+  // scorer's stream has left none of its code in L2; the dry runs bring that
+  // code into L2 (and into their SMs' instruction caches) before the last
+  // block needs it.
+  const bool dry = !last_sh;
+  if (dry && a.cap_pages <= 0) return;
   __threadfence();
   // Exact τ of the G query heads, block-parallel:
   //  A  keep the listed candidate pages whose max clears T0 = z_max − 1
@@ -439,6 +447,7 @@ __global__ void __launch_bounds__(kThreads, 2) pass_a_kernel(DecodeArgs a) {
   for (int k = 0; k < kSlots; ++k) {
     ce[k] = make_int2(0, __float_as_int(-CUDART_INF_F));
     if (hs < G && js + k * SPT < a.cap_pages) ce[k] = __ldcg(clist + (size_t)hs * a.cap_pages + js + k * SPT);
+    if (dry) ce[k].x = 0;
   }
   // V-list page bitmap over the selection's ranks (the page-id arrays are free now)
   const int Wv = (n_sel + 31) >> 5;
@@ -448,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 2) pass_a_kernel(DecodeArgs a) {
   if (tid < G) {
     const float zm = ord_dec(__ldcg(&a.zmax[hq0 + tid]));
     T0_sh[tid] = zm > -CUDART_INF_F ? zm - 1.0f : CUDART_INF_F;
-    nc_sh[tid] = min(__ldcg(&a.cand_cnt[hq0 + tid]), a.cap_pages);
+    nc_sh[tid] = min(__ldcg(&a.cand_cnt[hq0 + tid]), dry ? 1 : a.cap_pages);
     km_sh[tid] = gauss ? __ldcg(&a.kept_mass[hq0 + tid]) : 0.0f;
     np_sh[tid] = 0;
     nz_sh[tid] = 0;
@@ -456,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 2) pass_a_kernel(DecodeArgs a) {
   __syncthreads();
   if (tid == 0) {
     int t = 0;
-    bool fits = Wv <= kListCap;
+    bool fits = dry || Wv <= kListCap;
     for (int h = 0; h < G; ++h) {
       off_sh[h] = t;
       t += nc_sh[h];
@@ -575,7 +584,7 @@ __global__ void __launch_bounds__(kThreads, 2) pass_a_kernel(DecodeArgs a) {
       src.G = G;
       src.hg = hg;
       src.T0 = tlb_sh[hg];
-      if (src.big && lane == 0) raise_flag(a.status, ENTMAXKV_DEV_CAND_OVERFLOW);
+      if (src.big && lane == 0 && !dry) raise_flag(a.status, ENTMAXKV_DEV_CAND_OVERFLOW);
       // With few scores the direct root, lowered by a margin above its error,
       // starts the solve just below τ: usually one closed-form check on the
       // final support ends it.
@@ -586,11 +595,11 @@ __global__ void __launch_bounds__(kThreads, 2) pass_a_kernel(DecodeArgs a) {
       }
       bool ok;
       tau_d = solve_tau_warp(src, t0, a.beta, ok);
-      if (!ok && lane == 0) raise_flag(a.status, ENTMAXKV_DEV_TAU_NOCONV);
+      if (!ok && lane == 0 && !dry) raise_flag(a.status, ENTMAXKV_DEV_TAU_NOCONV);
       tau_f = (float)tau_d;
     }
-    if (lane == 0) {
-      tauf_sh[hg] = tau_f;
+    if (lane == 0) tauf_sh[hg] = tau_f;
+    if (lane == 0 && !dry) {
       a.tau_ws[hs] = tau_d;
       if (a.tau_out) a.tau_out[hs] = tau_f;
       if (a.delta_out) {
@@ -616,14 +625,17 @@ __global__ void __launch_bounds__(kThreads, 2) pass_a_kernel(DecodeArgs a) {
     for (int k = 0; k < kSlots; ++k) {
       if (((kept >> k) & 1u) && __int_as_float(ce[k].y) > tauf_sh[hs]) {
         const uint32_t bit = 1u << (ce[k].x & 31);
-        if (!(atomicOr(&vb[ce[k].x >> 5], bit) & bit))
-          a.vlist[skv * a.cap_pages + atomicAdd(&vcnt_sh, 1)] = make_int4(ce[k].x, kpp[k].x, kpp[k].y, 0);
+        if (!(atomicOr(&vb[ce[k].x >> 5], bit) & bit)) {
+          const int pos = atomicAdd(&vcnt_sh, 1);
+          if (!dry) a.vlist[skv * a.cap_pages + pos] = make_int4(ce[k].x, kpp[k].x, kpp[k].y, 0);
+        }
       }
     }
     __syncthreads();
-    if (tid == 0) a.vcount[skv] = vcnt_sh;
+    if (tid == 0 && !dry) a.vcount[skv] = vcnt_sh;
     return;
   }
+  if (dry) return;  // (a dry run always takes the path above)
   const int W = (n_sel + 31) >> 5;
   uint32_t* vbm = reinterpret_cast<uint32_t*>(zc);
   int* vls = reinterpret_cast<int*>(pool);
