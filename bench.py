@@ -288,6 +288,7 @@ def run_ours(args, rank, world):
         res["policies"] = policy_table(wl, B, flush, qbuf, timed, K, peaks, args.policies.split(","))
         res["dropped_mass_exact"] = dropped_mass(wl, B, qbuf)
         res["roofline"] = roofline(wl, B, flush, qbuf, K, peaks, peak_kind)
+        res["prefill"] = prefill(wl, B, K, W, peaks)
         if not args.no_e2e:
             res["e2e"] = e2e(wl, B, toks, qs, n_app, K, W)
     if not args.no_cpu_baseline:
@@ -351,6 +352,48 @@ def dropped_mass(wl, B, qbuf):
         res[name] = {"mean": round(float(dl.mean()), 5), "max": round(float(dl.max()), 5),
                      "pages_per_kv_head": round(float(o.n_sel.float().mean()), 1)}
     return res
+
+
+def prefill(wl, B, K, W, peaks):
+    """Bulk prefill of the whole context of sequence 0 into a second cache of
+    the same shape (same block table, bf16 metadata copies on): one
+    entmaxkv_append that writes every token and builds every page's bounding
+    box, mean, m2 and their bf16 copies in the same kernel. Inputs are
+    device-resident synthetic keys and values (4.3 GB at 1M tokens, far above
+    L2); before each timed append the length is reset to 0, so every page is
+    new and its metadata is built from scratch."""
+    import torch
+    spec, dev = wl.spec, wl.cache.device
+    L, P, Hkv, d = spec.context_lens[0], spec.page_size, spec.num_kv_heads, spec.head_dim
+    c = B.PagedCache(Hkv, spec.group, d, P, 1, wl.cache.block_table.shape[1], wl.cache.cfg.num_phys_pages,
+                     spec.kv_dtype, dev, meta_bf16=True)
+    c.block_table[0].copy_(wl.cache.block_table[0])
+    g = torch.Generator(device=dev)
+    g.manual_seed(12345)
+    k = torch.randn(1, Hkv, L, d, generator=g, device=dev, dtype=spec.kv_dtype)
+    v = torch.randn(1, Hkv, L, d, generator=g, device=dev, dtype=spec.kv_dtype)
+    us = []
+    for i in range(W + K):
+        c.seq_lens.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        B.append(c, k, v)
+        b.record()
+        torch.cuda.synchronize()
+        if i >= W:
+            us.append(a.elapsed_time(b) * 1e3)
+    assert c.device_status() == 0, hex(c.device_status())
+    n_pages = -(-L // P)
+    esz = torch.tensor([], dtype=spec.kv_dtype).element_size()
+    # read k, v; write them into the pool; per (page, KV head): kmin, kmax in the
+    # KV dtype, mean and m2 in fp32, their bf16 copies
+    nbytes = 4 * Hkv * L * d * esz + Hkv * n_pages * d * (2 * esz + 2 * 4 + 2 * 2)
+    mean = statistics.mean(us)
+    gbs = nbytes / (mean * 1e-6) / 1e9
+    del c, k, v
+    return {"us": round(mean, 1), "tokens": L, "tokens_per_s": round(L / (mean * 1e-6), 1),
+            "bytes": nbytes, "gbs": round(gbs, 1), "frac_measured_hbm": round(gbs / peaks["hbm_gbs"], 4),
+            "steps": K, "what": "one bulk entmaxkv_append of the whole context (tokens + page metadata)"}
 
 
 def roofline(wl, B, flush, qbuf, K, peaks, peak_kind):

@@ -87,3 +87,31 @@ def test_batched_shuffled_with_appends():
         q = torch.stack([synth.step_queries(spec, b, step, None, device="cuda")
                          for b in range(spec.batch)]).contiguous()
         check_decode(built, "gaussian", 1.5, 0, 0.5, q=q, units=units)
+
+
+def test_gqa1m_bulk_prefill_metadata(gqa1m):
+    """The 1M-token prefill is one bulk append that writes the tokens and
+    builds every page's metadata in the same kernel. On sampled pages of two
+    KV heads (plus the last page) the stored tokens equal the input, the
+    bounding box equals the oracle's exactly, and the mean and variance match
+    the oracle's float64 statistics of the same keys."""
+    from oracle import pages as opg
+    spec, c = gqa1m.spec, gqa1m.cache
+    P = spec.page_size
+    rng = np.random.default_rng(7)
+    bt = c.block_table[0].cpu().numpy()
+    for j in (0, 7):
+        L = int(c.seq_lens[0].item())
+        n_pages = -(-L // P)
+        pages = np.unique(np.concatenate([rng.choice(n_pages, 64, replace=False), [n_pages - 1]]))
+        K = gqa1m.K[0][j, :L]
+        for p in pages:
+            rows = K[p * P:min(L, (p + 1) * P)].double().cpu().numpy()
+            meta = opg.page_metadata(rows, P)
+            ph = int(bt[p])
+            assert np.array_equal(c.k_pool[ph, j, :rows.shape[0]].double().cpu().numpy(), rows)
+            assert np.array_equal(c.kmin[ph, j].double().cpu().numpy(), meta["kmin"][0])
+            assert np.array_equal(c.kmax[ph, j].double().cpu().numpy(), meta["kmax"][0])
+            np.testing.assert_allclose(c.mean[ph, j].double().cpu().numpy(), meta["mean"][0], atol=2e-6, rtol=1e-5)
+            np.testing.assert_allclose(c.m2[ph, j].double().cpu().numpy() / rows.shape[0], meta["var"][0],
+                                       atol=1e-5, rtol=1e-4)
