@@ -123,8 +123,6 @@ def decode_group(K, V, Q, alpha: float, policy: str, page_size: int,
         sel = pg.select_topk(uhat, k)
         res["U"], res["uhat"] = U, uhat
     else:  # gaussian
-        if alpha not in (1.5, 2.0):
-            raise NotImplementedError("Gaussian selector covers α ∈ {1.5, 2}")
         mu = np.empty((g, n_pages))
         sigma = np.empty((g, n_pages))
         for h in range(g):

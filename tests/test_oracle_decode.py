@@ -115,7 +115,7 @@ def test_topk_certified_delta_bounds_exact(alpha):
                 assert err <= 2 * B * r["delta_exact"][h] + 1e-12
 
 
-@pytest.mark.parametrize("alpha", [1.5, 2.0])
+@pytest.mark.parametrize("alpha", [1.5, 2.0, 1.25, 1.75, 3.0])
 def test_gaussian_policy_consistency(alpha):
     rng = np.random.default_rng(24)
     K, V, Q = _case(rng, n_tok=512, d=32, g=4, needles=6)

@@ -5,6 +5,7 @@ import math
 import os
 
 import numpy as np
+import pytest
 
 from oracle import entmax as em
 from oracle import pages as pg
@@ -173,3 +174,104 @@ def test_gaussian_selection_monotone_in_margin():
 
 def test_est_max_one_token_page_is_mean():
     assert pg.est_max(np.array([0.3]), np.array([5.0]), np.array([1]))[0] == 0.3
+
+
+# --------------------------------------------------------------------------
+# General entmax order in the Gaussian selector: J_ν(t) = E[(t + Z)_+^ν]
+# --------------------------------------------------------------------------
+
+def test_jfun_reduces_to_the_integer_closed_forms():
+    # ν = 0: Φ(t); ν = 1: tΦ + φ; ν = 2: (1+t²)Φ + tφ; ν = 3: (t³+3t)Φ + (t²+2)φ
+    # (integrate (t + z)^n φ(z) over z > −t term by term); both routes of jfun.
+    from scipy.special import ndtr
+    t = np.concatenate([np.linspace(-10.0, 19.5, 60), np.linspace(20.0, 40.0, 9)])
+    ph, Ph = np.exp(-0.5 * t * t) / math.sqrt(2 * math.pi), ndtr(t)
+    forms = {0: Ph, 1: t * Ph + ph, 2: (1 + t * t) * Ph + t * ph, 3: (t ** 3 + 3 * t) * Ph + (t * t + 2) * ph}
+    for nu, ref in forms.items():
+        # for ν ≥ 1 the closed forms cancel in the far left tail (tΦ against φ),
+        # so they are compared where they keep their digits
+        keep = t >= (-10.0 if nu == 0 else -4.0)
+        got = pg.jfun(t[keep], float(nu))
+        np.testing.assert_allclose(got, ref[keep], rtol=1e-11, atol=1e-300)
+
+
+def test_jfun_matches_quadrature_of_its_definition():
+    from scipy.integrate import quad
+    for nu in (-0.5, 0.5, 1.5, 3.3, 6.0):
+        for t in (-6.0, -2.5, 0.0, 1.0, 4.0, 12.0, 19.0, 21.0, 25.0):
+            f = lambda y: y ** nu * math.exp(-0.5 * (y - t) ** 2) / math.sqrt(2 * math.pi)
+            ref = quad(f, 0.0, max(1.0, t) + 40.0, points=[max(t, 1e-3)], limit=400,
+                       epsabs=0.0, epsrel=1e-13)[0]
+            got = float(pg.jfun(np.array([t]), nu)[0])
+            # quad's own accuracy next to the y^ν end point (ν < 0) is about 1e-9
+            assert abs(got - ref) <= 5e-9 * abs(ref), (nu, t, got, ref)
+
+
+def test_jfun_derivative_is_nu_times_the_next_lower_order():
+    # d/dt ∫_0^∞ y^ν φ(y − t) dy = ν·J_{ν−1}(t) (integrate by parts), so the
+    # Halley step's D1 and D2 come from the orders β − 1 and β − 2.
+    h = 1e-5
+    for nu in (1.7, 2.5, 4.0):
+        for t in (-3.0, 0.0, 2.0, 25.0):
+            fd = (pg.jfun(np.array([t + h]), nu)[0] - pg.jfun(np.array([t - h]), nu)[0]) / (2 * h)
+            ref = nu * pg.jfun(np.array([t]), nu - 1.0)[0]
+            assert abs(fd - ref) <= 1e-6 * max(1.0, abs(ref)), (nu, t, fd, ref)
+
+
+def test_jfun_is_continuous_across_the_series_switch():
+    for nu in (0.5, 3.3, 7.0):
+        a = pg.jfun(np.array([pg.J_SERIES_FROM * (1 - 1e-12)]), nu)[0]
+        b = pg.jfun(np.array([pg.J_SERIES_FROM]), nu)[0]
+        assert abs(a - b) <= 1e-11 * abs(b)
+
+
+def test_partial_moment_general_beta_matches_quadrature():
+    from scipy.integrate import quad
+    rng = np.random.default_rng(17)
+    for beta in (0.5, 1.5, 3.3):
+        for _ in range(15):
+            a, sg = rng.normal() * 2.0, rng.uniform(0.05, 2.0)
+            f = lambda x: max(x, 0.0) ** beta * math.exp(-0.5 * ((x - a) / sg) ** 2) / (sg * math.sqrt(2 * math.pi))
+            lo = max(0.0, a - 14 * sg)
+            if lo >= a + 14 * sg:
+                continue
+            ref = quad(f, lo, a + 14 * sg, points=[max(a, lo + 1e-12)], limit=400, epsabs=0.0, epsrel=1e-12)[0]
+            got = float(pg.partial_moment(a, sg, beta))
+            assert abs(got - ref) <= 1e-9 * max(abs(ref), 1e-300), (beta, a, sg, got, ref)
+        assert float(pg.partial_moment(0.7, 0.0, beta)) == 0.7 ** beta
+
+
+@pytest.mark.parametrize("alpha", [1.25, 1.75, 3.0])
+def test_tauhat_general_alpha(alpha):
+    beta = 1.0 / (alpha - 1.0)
+    rng = np.random.default_rng(18)
+    # point masses: the exact entmax threshold of the repeated means
+    m = rng.normal(size=30)
+    n = rng.integers(1, 33, size=30)
+    assert abs(pg.tauhat(m, np.zeros(30), n, alpha) - em.threshold(np.repeat(m, n), alpha)) < 1e-10
+    # Gaussian pages: F(τ̂) = 1, F decreasing, τ̂ ≥ max m − 1
+    m = rng.normal(size=150) * 0.4
+    sg = rng.uniform(0.1, 0.8, size=150)
+    n = np.full(150, 32)
+    th = pg.tauhat(m, sg, n, alpha)
+    assert abs(pg.normaliser(th, m, sg, n, beta) - 1.0) < 1e-10
+    F = [pg.normaliser(t, m, sg, n, beta) for t in np.linspace(m.max() - 1.0, th + 2.0, 30)]
+    assert all(F[i] > F[i + 1] for i in range(len(F) - 1))
+    assert th >= m.max() - 1.0
+
+
+def test_jfun_matches_high_precision_quadrature():
+    # 40-digit tanh-sinh quadrature of the defining integral (mpmath), across
+    # all three routes of jfun and both sides of each switch
+    mp = pytest.importorskip("mpmath")
+    mp.mp.dps = 40
+    for nu in (-0.5, 0.5, 1.5, 3.3, 6.0):
+        for t in (-14.0, -6.0, -2.0, -1.999, 0.0, 3.0, 12.0, 19.99, 20.0, 30.0):
+            if t < 0:  # φ(y − t) = φ(t)·e^{−y²/2 − |t|y}: integrate the factor, split at its scale
+                x = mp.mpf(-t)
+                ref = mp.npdf(x) * mp.quad(lambda y: y ** nu * mp.exp(-y * y / 2 - x * y),
+                                           [0, 1 / x, 10 / x, mp.inf])
+            else:
+                ref = mp.quad(lambda y: y ** nu * mp.npdf(y - t), [0, max(t, 1.0), mp.inf])
+            got = pg.jfun(np.array([t]), nu)[0]
+            assert abs(got - float(ref)) <= 1e-12 * abs(float(ref)), (nu, t, got, float(ref))
