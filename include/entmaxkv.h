@@ -199,7 +199,12 @@ int32_t entmaxkv_read_status(const entmaxkv_cache* cache, uint32_t* status_out, 
  * One decode step for n_seqs sequences (summary §2A-§2C; δ from §3).
  *   q          (device) [n_seqs][Hq][head_dim], kv_dtype (Hq = Hkv·group)
  *   seq_ids    (device) [n_seqs] sequence rows, or NULL for 0..n_seqs−1
- *   alpha      α > 1 (GAUSSIAN needs α ∈ {1.5, 2}); ignored by SOFTMAX and SOFTMAX_TOPK
+ *   alpha      α > 1; ignored by SOFTMAX and SOFTMAX_TOPK. GAUSSIAN uses closed
+ *              forms at α ∈ {1.5, 2} and, at any other α, fits of the partial
+ *              moments E[(t + Z)_+^ν] that the first call with that α builds on
+ *              the host (about 0.1-0.4 s, cached for later calls). The fits
+ *              are checked to 1e-6 relative; an α whose fits fail that check
+ *              (outside about [1.14, 6]) returns ENTMAXKV_ERR_UNSUPPORTED.
  *   policy     ENTMAXKV_POLICY_*
  *   budget_tokens  TOPK, SOFTMAX_TOPK: k = budget_tokens / page_size pages (must be ≥ 1);
  *                  GAUSSIAN: a cap in tokens (0 = none; on overflow the pages

@@ -20,7 +20,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libentmaxkv.so")
 
-SOURCES = ["api.cu", "append.cu", "score.cu", "select.cu", "decode.cu", "softmax.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "append.cu", "score.cu", "select.cu", "decode.cu", "softmax.cu", "noalloc.cu",
+           "moment_fit.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
 

@@ -301,10 +301,7 @@ static int32_t decode_impl(const entmaxkv_config* cfg, const entmaxkv_cache* cac
   const bool topk = policy == ENTMAXKV_POLICY_TOPK || policy == ENTMAXKV_POLICY_SOFTMAX_TOPK;
   if (!soft && !(alpha > 1.0f && isfinite(alpha)))
     return ENTMAXKV_ERR_INVALID_ARG;
-  if (policy == ENTMAXKV_POLICY_GAUSSIAN) {
-    if (!isfinite(margin)) return ENTMAXKV_ERR_INVALID_ARG;
-    if (alpha != 1.5f && alpha != 2.0f) return ENTMAXKV_ERR_UNSUPPORTED;
-  }
+  if (policy == ENTMAXKV_POLICY_GAUSSIAN && !isfinite(margin)) return ENTMAXKV_ERR_INVALID_ARG;
   Layout L, LF;
   if ((st = compute_layout(cfg, n_seqs, policy, budget_tokens, L))) return st;
   const size_t need = total_bytes(cfg, n_seqs, policy, budget_tokens, flags, L, LF);
@@ -338,6 +335,12 @@ static int32_t decode_impl(const entmaxkv_config* cfg, const entmaxkv_cache* cac
   a.inv_sqrt_d = (float)(1.0 / sqrt((double)a.D));
   a.zscale = (float)(((double)al - 1.0) / sqrt((double)a.D));
   a.margin_z = (float)(((double)al - 1.0) * (double)margin);
+  // The Gaussian selector at an order without closed forms takes its partial
+  // moments from fits built on the host for this β (cached); an order whose
+  // fits miss their accuracy check is refused before anything is queued.
+  if (policy == ENTMAXKV_POLICY_GAUSSIAN && al != 1.5f && al != 2.0f &&
+      moment_fit_for(a.beta, &a.fit))
+    return ENTMAXKV_ERR_UNSUPPORTED;
   a.k_pool = cache->k_pool;
   a.v_pool = cache->v_pool;
   a.kmin = cache->kmin;

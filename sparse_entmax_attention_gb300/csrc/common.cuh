@@ -18,6 +18,26 @@ constexpr int kSolveCap = 8192;     // candidate scores the τ solver keeps in s
 constexpr int kListCap = 1024;      // selected pages one decode block handles
 constexpr int kTauhatCluster = 8;   // blocks per τ̂ cluster (one cluster per query head)
 
+// Chebyshev fits of J_ν(t) = E[(t + Z)_+^ν], Z ~ N(0, 1), for the Gaussian
+// selector at an entmax order other than α ∈ {1.5, 2} (β = 1/(α−1)); the
+// orders are ν = β, β − 1 and, for β > 1, β − 2 (F and its first two
+// τ-derivatives). Built on the host per β (moment_fit.cu) and passed with the
+// kernel arguments, so the kernels read the coefficients from constant memory.
+//   t ≤ 0:  J_ν(t) = φ(x)·u^{ν+1}·Σ_k cl[k]·T_k(w),  x = min(−t, 12),
+//           u = 1/(1 + x/3), w = 2.5u − 1.5 (φ at the true −t);
+//   0 < t ≤ 16:  J_ν(t) = (1 + t)^ν·Σ_k cr[k]·T_k(t/8 − 1), or with rlog set
+//           2^{ν·log2(1 + t) + Σ_k cr[k]·T_k(t/8 − 1)};
+//   t > 16: J_ν(t) = t^ν·(1 + Σ_{k=1..5} ca[k−1]·t^{−2k}).
+constexpr int kFitN = 33;  // Chebyshev coefficients per fit (degree 32)
+struct MomentFit {
+  float cl[3][kFitN];
+  float cr[3][kFitN];
+  float ca[3][5];
+  float nu[3];
+  int rlog[3];  // the right fit is of log2 J_ν(t)/(1 + t)^ν
+  int orders;  // 0: the closed forms (β ∈ {1, 2}); 2: no second derivative (β ≤ 1); 3
+};
+
 // Everything a decode kernel needs, passed by value (well under 4 KB).
 struct DecodeArgs {
   // geometry
@@ -77,6 +97,7 @@ struct DecodeArgs {
   int mslots;          // scoring blocks per (sequence, 8 KV heads) row
   uint4* ctrl;         // the workspace words zeroed before each decode's counters are used
   int ctrl_vec;        // their count in 16-byte units
+  MomentFit fit;       // Gaussian selector at a general α (orders == 0 otherwise)
 };
 
 struct AppendArgs {
@@ -293,6 +314,80 @@ __device__ __forceinline__ void gauss_moment2(float a, float sg, float inv_sg, b
   }
 }
 
+// Σ_k c[k]·T_k(x) (Clenshaw), x ∈ [−1, 1], coefficients in constant memory.
+__device__ __forceinline__ float clenshaw(const float (&c)[kFitN], float x) {
+  const float x2 = 2.0f * x;
+  float b1 = 0.0f, b2 = 0.0f;
+#pragma unroll 4
+  for (int k = kFitN - 1; k >= 1; --k) {
+    const float b = fmaf(x2, b1, c[k] - b2);
+    b2 = b1;
+    b1 = b;
+  }
+  return fmaf(x, b1, c[0] - b2);
+}
+
+// J_ν(t) of order fit.nu[k] from its fits (layout at MomentFit). Powers and
+// φ use the single-instruction base-2 exponential and logarithm (relative
+// error about 2^-22), inside the fits' accuracy.
+__device__ __forceinline__ float jfit(const MomentFit& F, int k, float t) {
+  const float nu = F.nu[k];
+  float l2, e;
+  if (t <= 0.0f) {
+    const float x = -t, xc = fminf(x, 12.0f);
+    const float u = 1.0f / (1.0f + xc * 0.33333334f);
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(l2) : "f"(u));
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(fmaf(-0.72134752f, x * x, (nu + 1.0f) * l2)));
+    return 0.3989422804f * e * clenshaw(F.cl[k], fmaf(2.5f, u, -1.5f));
+  }
+  if (t <= 16.0f) {
+    const float c = clenshaw(F.cr[k], fmaf(t, 0.125f, -1.0f));
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(l2) : "f"(1.0f + t));
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(F.rlog[k] ? fmaf(nu, l2, c) : nu * l2));
+    return F.rlog[k] ? e : e * c;
+  }
+  const float it2 = 1.0f / (t * t);
+  const float s = fmaf(it2, fmaf(it2, fmaf(it2, fmaf(it2, fmaf(it2, F.ca[k][4], F.ca[k][3]), F.ca[k][2]),
+                                           F.ca[k][1]), F.ca[k][0]), 1.0f);
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(l2) : "f"(t));
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(nu * l2));
+  return e * s;
+}
+
+// The general-order counterpart of gauss_moment2, for Z ~ N(m, ς²) against τ,
+// with t = (m − τ)/ς and lsg = log2 ς (ς > 0):
+//   g = E[(Z − τ)_+^β] = ς^β·J_β(t);
+//   dg = β·ς^{β−1}·J_{β−1}(t), minus the τ-derivative of g (as gauss_moment2);
+//   d2g = β(β−1)·ς^{β−2}·J_{β−2}(t), its second τ-derivative (0 when β ≤ 1,
+//   where it does not exist).
+__device__ __forceinline__ void gauss_moment_gen(const MomentFit& F, float beta, float t, float lsg,
+                                                 float& g, float& dg, float& d2g) {
+  float e0, e1;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e0) : "f"(beta * lsg));
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e1) : "f"((beta - 1.0f) * lsg));
+  // (a vanishing J gives 0 even where the power of ς is out of range)
+  const float j0 = jfit(F, 0, t), j1 = jfit(F, 1, t);
+  g = j0 != 0.0f ? e0 * j0 : 0.0f;
+  dg = j1 != 0.0f ? beta * e1 * j1 : 0.0f;
+  d2g = 0.0f;
+  if (F.orders == 3) {
+    float e2;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e2) : "f"((beta - 2.0f) * lsg));
+    const float j2 = jfit(F, 2, t);
+    d2g = j2 != 0.0f ? beta * (beta - 1.0f) * e2 * j2 : 0.0f;
+  }
+}
+
+// E[(a + σZ)_+^β] alone at a general order (σ = 0: the point mass a_+^β).
+__device__ __forceinline__ float gauss_mass_gen(const MomentFit& F, float beta, float a, float sg) {
+  if (!(sg > 0.0f)) return a > 0.0f ? powf(a, beta) : 0.0f;
+  float l2, e;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(l2) : "f"(sg));
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(beta * l2));
+  const float j = jfit(F, 0, a / sg);
+  return j != 0.0f ? e * j : 0.0f;
+}
+
 // ---------------------------------------------------------------------------
 // Bulk asynchronous copies (global -> shared) completed on an mbarrier.
 
@@ -474,6 +569,9 @@ __device__ __forceinline__ void block_page_range(const DecodeArgs& a, int s, int
   }
   __syncthreads();
 }
+
+// Host: the fits for order β (cached); 0 when they pass their accuracy check.
+int moment_fit_for(float beta, MomentFit* out);
 
 // Launchers (one translation unit each).
 cudaError_t launch_append(const AppendArgs& a, int kv_dtype, cudaStream_t st);

@@ -75,8 +75,13 @@ __device__ __forceinline__ void for_each_cand(const SolveSrc& S, F&& f) {
 // Float accumulation per candidate (GB300 runs FP64 at a small fraction of
 // the FP32 rate): τ is carried as a double and split into hi + lo floats so
 // that y = z − τ keeps its accuracy; only the per-iteration totals are double.
+// Other orders: Newton inside a bracket [lo, hi] kept by the sign of the
+// normaliser minus 1 (for β < 1 it is concave, so a step from below can
+// overshoot the root, and a step leaving the bracket is replaced by
+// bisection); it ends when the step or the bracket is below the tolerance.
 __device__ double solve_tau_warp(const SolveSrc& S, double tau0, float beta, bool& ok) {
   double tau = tau0;
+  double lo = tau0, hi = CUDART_INF;
   ok = false;
   const bool b2 = beta == 2.0f, b1 = beta == 1.0f;
   for (int it = 0; it < kTauIters; ++it) {
@@ -98,6 +103,28 @@ __device__ double solve_tau_warp(const SolveSrc& S, double tau0, float beta, boo
     const float k = warp_sum(kf), s1 = warp_sum(s1f), s2 = warp_sum(s2f);
     const float sb = warp_sum(sbf), sb1 = warp_sum(sb1f);
     const float mn = warp_min_f(mnf);
+    if (!b2 && !b1) {
+      const float tol = 1e-7f * fmaxf(1.0f, fabsf((float)tau));
+      if (k == 0.0f || sb < 1.0f) hi = tau;  // above the root (no score above τ counts as 0 < 1)
+      else lo = tau;
+      if (k > 0.0f) {
+        const float step = (sb - 1.0f) / (beta * sb1);
+        if (fabsf(step) <= tol) {
+          tau += (double)step;
+          ok = true;
+          break;
+        }
+        const double nt = tau + (double)step;
+        tau = (nt > lo && nt < hi) ? nt : 0.5 * (lo + hi);
+      } else {
+        tau = 0.5 * (lo + hi);
+      }
+      if (hi - lo <= (double)tol) {
+        ok = true;
+        break;
+      }
+      continue;
+    }
     if (k == 0.0f) break;  // cannot happen while τ < z_max
     float step;
     if (b2) {
@@ -122,12 +149,7 @@ __device__ double solve_tau_warp(const SolveSrc& S, double tau0, float beta, boo
       }
       step = d;
     } else {
-      step = (sb - 1.0f) / (beta * sb1);
-      if (fabsf(step) <= 1e-7f * fmaxf(1.0f, fabsf((float)tau))) {
-        tau += (double)step;
-        ok = true;
-        break;
-      }
+      step = 0.0f;  // (other orders take the bracketed branch above)
     }
     if (!(step > 1e-7f * fmaxf(1.0f, fabsf((float)tau)))) {  // converged to float resolution
       if (step > 0.0f) tau += (double)step;
@@ -256,7 +278,8 @@ __global__ void __launch_bounds__(kThreads, 2) pass_a_kernel(DecodeArgs a) {
     }
     if (gauss) {
       float g, dg;
-      gauss_moment(v.x - th, v.y, beta2, g, dg);
+      if (a.fit.orders) g = gauss_mass_gen(a.fit, a.beta, v.x - th, v.y);
+      else gauss_moment(v.x - th, v.y, beta2, g, dg);
       atomicAdd(&kept_sh[h], (float)min(P, L - page * P) * g);
     }
   }
@@ -523,7 +546,9 @@ __global__ void __launch_bounds__(kThreads, 2) pass_a_kernel(DecodeArgs a) {
       src.m = np;
       src.big = false;
       bool ok;
-      tlb = fmaxf(tlb, (float)solve_tau_warp(src, (double)T0_sh[h], a.beta, ok));
+      const float tb = (float)solve_tau_warp(src, (double)T0_sh[h], a.beta, ok);
+      // the solve ends within its tolerance on either side of the root
+      if (tb > tlb) tlb = fmaxf(tlb, tb - 1e-5f * fmaxf(1.0f, fabsf(tb)));
     }
     if (lane == 0) tlb_sh[h] = tlb;
   }

@@ -109,9 +109,13 @@ __device__ __forceinline__ void moments_x2(u64 mb, u64 sr, u64 ir, u64 nr, u64 n
 // kTauhatCluster·kWarps partials over distributed shared memory, sums them in
 // a fixed butterfly order and takes the same step: all copies of the state
 // stay bit-identical without further synchronisation.
-template <bool B2>
+// MODE 0: β = 1, 1: β = 2 (closed forms, packed), 2: any other β (the fits of
+// a.fit, one page at a time; Newton steps when β ≤ 1, where F has no second
+// derivative).
+template <int MODE>
 __global__ void __cluster_dims__(kTauhatCluster, 1, 1) __launch_bounds__(kThreads, 2)
     tauhat_kernel(DecodeArgs a) {
+  constexpr bool B2 = MODE == 1;
   pdl_enter();
   static_assert(kTauhatCluster * kWarps == 64, "two partials per lane");
   cg::cluster_group cluster = cg::this_cluster();
@@ -144,7 +148,9 @@ __global__ void __cluster_dims__(kTauhatCluster, 1, 1) __launch_bounds__(kThread
 #pragma unroll
   for (int k = 0; k < kRegPages; ++k) {
     const int p = p_lo + tid + k * kThreads;
-    float2 v = make_float2(-1e18f, 1.0f);
+    // (an empty slot: far below every threshold, yet with ς = 1 after the
+    // floor below, so no power of ς overflows at a large β)
+    float2 v = make_float2(-3.0e4f, 1.0f);
     nr[k] = 0.0f;
     if (p < p_hi) {
       v = ms[p];
@@ -186,19 +192,51 @@ __global__ void __cluster_dims__(kTauhatCluster, 1, 1) __launch_bounds__(kThread
   bool converged = false;
   int it = 0;
   for (; it < kTauhatIters; ++it) {
-    u64 f2 = 0ull, df2 = 0ull, d2f2 = 0ull;
-    const u64 noff = f2_splat(-off);
+    float f = 0.0f, df = 0.0f, d2f = 0.0f;
+    if constexpr (MODE == 2) {
 #pragma unroll
-    for (int i = 0; i < kPairs; ++i) moments_x2<B2>(mb2[i], sr2[i], ir2[i], nr2[i], noff, f2, df2, d2f2);
-    float f = f2_sum(f2), df = f2_sum(df2), d2f = f2_sum(d2f2);
-    if (B2) {
-      df *= 2.0f;
-      d2f *= 2.0f;
+      for (int i = 0; i < kPairs; ++i) {
+        float m0, m1, s0, s1, i0, i1, n0, n1;
+        f2_unpack(mb2[i], m0, m1);
+        f2_unpack(sr2[i], s0, s1);
+        f2_unpack(ir2[i], i0, i1);
+        f2_unpack(nr2[i], n0, n1);
+        float g, dg, d2g, l0, l1;
+        asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(l0) : "f"(s0));
+        asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(l1) : "f"(s1));
+        gauss_moment_gen(a.fit, a.beta, (m0 - off) * i0, l0, g, dg, d2g);
+        f = fmaf(n0, g, f);
+        df = fmaf(n0, dg, df);
+        d2f = fmaf(n0, d2g, d2f);
+        gauss_moment_gen(a.fit, a.beta, (m1 - off) * i1, l1, g, dg, d2g);
+        f = fmaf(n1, g, f);
+        df = fmaf(n1, dg, df);
+        d2f = fmaf(n1, d2g, d2f);
+      }
+    } else {
+      u64 f2 = 0ull, df2 = 0ull, d2f2 = 0ull;
+      const u64 noff = f2_splat(-off);
+#pragma unroll
+      for (int i = 0; i < kPairs; ++i) moments_x2<B2>(mb2[i], sr2[i], ir2[i], nr2[i], noff, f2, df2, d2f2);
+      f = f2_sum(f2);
+      df = f2_sum(df2);
+      d2f = f2_sum(d2f2);
+      if (B2) {
+        df *= 2.0f;
+        d2f *= 2.0f;
+      }
     }
     for (int p = p_lo + tid + kRegPages * kThreads; p < p_hi; p += kThreads) {
       const float2 v = ms[p];
       float g, dg, d2g;
-      gauss_moment2((v.x - base) - off, v.y, v.y > 0.0f ? 1.0f / v.y : 0.0f, B2, g, dg, d2g);
+      if constexpr (MODE == 2) {
+        const float mk = v.x - base, sk = fmaxf(v.y, 0x1p-24f * fmaxf(1.0f, fabsf(mk)));
+        float lk;
+        asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(lk) : "f"(sk));
+        gauss_moment_gen(a.fit, a.beta, (mk - off) / sk, lk, g, dg, d2g);
+      } else {
+        gauss_moment2((v.x - base) - off, v.y, v.y > 0.0f ? 1.0f / v.y : 0.0f, B2, g, dg, d2g);
+      }
       const float np = (float)page_tokens(p, n_pages, L, a.P);
       f = fmaf(np, g, f);
       df = fmaf(np, dg, df);
@@ -241,7 +279,8 @@ __global__ void __cluster_dims__(kTauhatCluster, 1, 1) __launch_bounds__(kThread
       if (F > 0.0f && D1 > 0.0f) {
         const float rF = __frcp_rn(F);
         const float g = __logf(F), g1 = -D1 * rF, g2 = D2 * rF - g1 * g1;
-        const float den = 2.0f * g1 * g1 - g * g2;
+        // (a negative den selects the Newton step: no second derivative for β ≤ 1)
+        const float den = (MODE != 2 || a.fit.orders == 3) ? 2.0f * g1 * g1 - g * g2 : -1.0f;
         const float newton = -__fdividef(g, g1);
         const float step = den > 0.0f ? -2.0f * __fdividef(g * g1, den) : newton;
         if (fabsf(step) <= tol) {
@@ -442,8 +481,9 @@ __global__ void __launch_bounds__(1024) topk_kernel(DecodeArgs a, int mode) {
 
 cudaError_t launch_tauhat(const DecodeArgs& a, cudaStream_t st) {
   dim3 grid(kTauhatCluster, a.Hq, a.S);
-  if (a.beta == 2.0f) launch_k(false, tauhat_kernel<true>, dim3(grid), dim3(kThreads), 0, st, a);
-  else launch_k(false, tauhat_kernel<false>, dim3(grid), dim3(kThreads), 0, st, a);
+  if (a.fit.orders) launch_k(false, tauhat_kernel<2>, dim3(grid), dim3(kThreads), 0, st, a);
+  else if (a.beta == 2.0f) launch_k(false, tauhat_kernel<1>, dim3(grid), dim3(kThreads), 0, st, a);
+  else launch_k(false, tauhat_kernel<0>, dim3(grid), dim3(kThreads), 0, st, a);
   return cudaGetLastError();
 }
 

@@ -49,7 +49,7 @@ def _exact_delta_on(K, Q, alpha, P, page_ids, soft=False):
 
 @pytest.mark.parametrize("policy,budget,margin,alpha", [
     ("topk", 256, 0.0, 1.5), ("topk", 512, 0.0, 2.0), ("gaussian", 0, 0.5, 1.5),
-    ("gaussian", 0, 0.0, 2.0), ("softmax_topk", 256, 0.0, 1.5)])
+    ("gaussian", 0, 0.0, 2.0), ("gaussian", 0, 0.5, 1.25), ("softmax_topk", 256, 0.0, 1.5)])
 @pytest.mark.parametrize("which", ["bf16", "f32"])
 def test_exact_delta_matches_oracle(built_bf16, built_f32, which, policy, budget, margin, alpha):
     built = built_bf16 if which == "bf16" else built_f32

@@ -37,7 +37,7 @@ def test_copies_are_the_rounded_fp32_metadata(built_meta16):
     _copies_match(built_meta16.cache)
 
 
-@pytest.mark.parametrize("alpha,margin", [(1.5, 0.5), (2.0, 0.0), (1.5, 1.0)])
+@pytest.mark.parametrize("alpha,margin", [(1.5, 0.5), (2.0, 0.0), (1.5, 1.0), (1.25, 0.5), (3.0, 0.0)])
 def test_gaussian_decode_on_bf16_metadata(built_meta16, alpha, margin):
     check_decode(built_meta16, "gaussian", alpha, 0, margin)
 

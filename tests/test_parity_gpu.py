@@ -180,3 +180,23 @@ def test_dense_v_flag_same_result(small_bf16):
     out_sparse_v = a.out.clone()
     b, _ = check_decode(small_bf16, "full", 1.5, flags=B.FLAG_DENSE_V)
     torch.testing.assert_close(b.out, out_sparse_v, rtol=1e-6, atol=1e-6)
+
+
+@pytest.mark.parametrize("alpha", [1.25, 1.75, 3.0])
+@pytest.mark.parametrize("margin", [0.0, 0.5])
+def test_gaussian_general_alpha(small_bf16, small_f32, alpha, margin):
+    """The Gaussian selector at orders without closed forms (β = 4, 4/3, 1/2):
+    τ̂ from the fitted partial moments against the oracle's, then the same
+    selection, τ and output bars as at α ∈ {1.5, 2}."""
+    check_decode(small_bf16, "gaussian", alpha, 0, margin)
+    check_decode(small_f32, "gaussian", alpha, 0, margin)
+
+
+@pytest.mark.parametrize("alpha", [1.25, 3.0])
+@pytest.mark.parametrize("policy,budget", [("full", 0), ("topk", 256)])
+def test_exact_tau_general_alpha(small_bf16, small_f32, alpha, policy, budget):
+    """The exact threshold at orders other than 1.5 and 2: β = 4 (convex
+    normaliser) and β = 1/2 (concave: Newton from below overshoots the root,
+    so the solve keeps a bracket)."""
+    check_decode(small_bf16, policy, alpha, budget)
+    check_decode(small_f32, policy, alpha, budget)

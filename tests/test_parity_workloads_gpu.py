@@ -30,6 +30,11 @@ def test_gqa32k_all_heads(gqa32k, policy, budget, margin):
     check_decode(gqa32k, policy, 1.5, budget, margin)
 
 
+@pytest.mark.parametrize("alpha", [1.25, 3.0])
+def test_gqa32k_gaussian_general_alpha(gqa32k, alpha):
+    check_decode(gqa32k, "gaussian", alpha, 0, 0.5)
+
+
 @pytest.fixture(scope="module")
 def gqa128k():
     return Built(synth.workload("gqa32x8-d128-128k-p32-bf16"))
