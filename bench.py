@@ -56,7 +56,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="headline step only")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--policies", default="gaussian,gaussian_meta_f32,topk,softmax_topk,full_dense,full_skipv,softmax",
+    ap.add_argument("--policies", default="gaussian,gaussian_meta_f32,gaussian_alpha1.25,topk,softmax_topk,full_dense,full_skipv,softmax",
                     help="rows of the per-policy table")
     return ap.parse_args()
 
@@ -127,7 +127,7 @@ def algorithmic_bytes(wl, policy, o, ws, view):
     if policy in ("full_dense", "softmax"):
         return 2 * n_pages * Hkv * page_kv + io, {"k_pages": n_pages * Hkv, "v_pages": n_pages * Hkv}
     meta = 0
-    if policy == "gaussian":                       # mean + m2: the bf16 copies when the cache keeps them
+    if policy in ("gaussian", "gaussian_alpha1.25"):  # mean + m2: the bf16 copies when the cache keeps them
         meta = n_pages * Hkv * d * (2 if cache.mean_bf16 is not None else 4) * 2
     elif policy == "gaussian_meta_f32":
         meta = n_pages * Hkv * d * 4 * 2
@@ -300,18 +300,21 @@ def policy_table(wl, B, flush, qbuf, timed, K, peaks, names):
     import torch
     cache, spec = wl.cache, wl.spec
     rows = {}
-    cases = [("gaussian", "gaussian", 0, 0), ("gaussian_meta_f32", "gaussian", 0, 0),
-             ("topk", "topk", TOPK_BUDGET, 0),
-             ("softmax_topk", "softmax_topk", TOPK_BUDGET, 0),
-             ("full_dense", "full", 0, B.FLAG_DENSE_V), ("full_skipv", "full", 0, 0),
-             ("softmax", "softmax", 0, 0)]
-    for name, pol, budget, flags in cases:
+    # (name, policy, budget, flags, α); α = 1.25 runs the selector on the
+    # fitted partial moments of order β = 4
+    cases = [("gaussian", "gaussian", 0, 0, ALPHA), ("gaussian_meta_f32", "gaussian", 0, 0, ALPHA),
+             ("gaussian_alpha1.25", "gaussian", 0, 0, 1.25),
+             ("topk", "topk", TOPK_BUDGET, 0, ALPHA),
+             ("softmax_topk", "softmax_topk", TOPK_BUDGET, 0, ALPHA),
+             ("full_dense", "full", 0, B.FLAG_DENSE_V, ALPHA), ("full_skipv", "full", 0, 0, ALPHA),
+             ("softmax", "softmax", 0, 0, ALPHA)]
+    for name, pol, budget, flags, alpha in cases:
         if name not in names:
             continue
         c = cache.fp32_metadata() if name == "gaussian_meta_f32" else cache
         ws = B.alloc_workspace(c, spec.batch, pol, budget)
         o = B.alloc_outputs(c, spec.batch, pol, budget)
-        fn = lambda: B.decode(c, qbuf, ALPHA, pol, budget, MARGIN, flags, workspace=ws, outputs=o)
+        fn = lambda: B.decode(c, qbuf, alpha, pol, budget, MARGIN, flags, workspace=ws, outputs=o)
         fn()
         torch.cuda.synchronize()
         g = torch.cuda.CUDAGraph()
@@ -323,7 +326,7 @@ def policy_table(wl, B, flush, qbuf, timed, K, peaks, names):
         nbytes, counts = algorithmic_bytes(wl, name, o, ws, view)
         evs = B.stage_events()
         flush.zero_()
-        B.decode(c, qbuf, ALPHA, pol, budget, MARGIN, flags, workspace=ws, outputs=o, events=evs)
+        B.decode(c, qbuf, alpha, pol, budget, MARGIN, flags, workspace=ws, outputs=o, events=evs)
         torch.cuda.synchronize()
         stage = {n: round(evs[k].elapsed_time(evs[k + 1]) * 1e3, 1) for k, n in enumerate(B.STAGES)}
         rows[name] = {"us": round(mean, 2), "bytes": nbytes, "stage_us_once": stage,
