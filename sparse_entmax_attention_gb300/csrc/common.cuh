@@ -327,31 +327,44 @@ __device__ __forceinline__ float clenshaw(const float (&c)[kFitN], float x) {
   return fmaf(x, b1, c[0] - b2);
 }
 
-// J_ν(t) of order fit.nu[k] from its fits (layout at MomentFit). Powers and
-// φ use the single-instruction base-2 exponential and logarithm (relative
-// error about 2^-22), inside the fits' accuracy.
-__device__ __forceinline__ float jfit(const MomentFit& F, int k, float t) {
+// J_ν(t) of order fit.nu[k] from its fits (layout at MomentFit), as
+// 2^E·M: the caller adds the exponent of its power of ς to E before one ex2,
+// so ς^p·J stays in range where ς^p and J alone would not (a page with a tiny
+// ς has t ~ 2^24, and t^ν alone overflows for ν > 5). Powers and φ use the
+// single-instruction base-2 logarithm and exponential (relative error about
+// 2^-22), inside the fits' accuracy.
+__device__ __forceinline__ void jfit(const MomentFit& F, int k, float t, float& E, float& M) {
   const float nu = F.nu[k];
-  float l2, e;
+  float l2;
   if (t <= 0.0f) {
     const float x = -t, xc = fminf(x, 12.0f);
     const float u = 1.0f / (1.0f + xc * 0.33333334f);
     asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(l2) : "f"(u));
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(fmaf(-0.72134752f, x * x, (nu + 1.0f) * l2)));
-    return 0.3989422804f * e * clenshaw(F.cl[k], fmaf(2.5f, u, -1.5f));
+    E = fmaf(-0.72134752f, x * x, (nu + 1.0f) * l2);
+    M = 0.3989422804f * clenshaw(F.cl[k], fmaf(2.5f, u, -1.5f));
+    return;
   }
   if (t <= 16.0f) {
     const float c = clenshaw(F.cr[k], fmaf(t, 0.125f, -1.0f));
     asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(l2) : "f"(1.0f + t));
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(F.rlog[k] ? fmaf(nu, l2, c) : nu * l2));
-    return F.rlog[k] ? e : e * c;
+    E = F.rlog[k] ? fmaf(nu, l2, c) : nu * l2;
+    M = F.rlog[k] ? 1.0f : c;
+    return;
   }
   const float it2 = 1.0f / (t * t);
-  const float s = fmaf(it2, fmaf(it2, fmaf(it2, fmaf(it2, fmaf(it2, F.ca[k][4], F.ca[k][3]), F.ca[k][2]),
-                                           F.ca[k][1]), F.ca[k][0]), 1.0f);
+  M = fmaf(it2, fmaf(it2, fmaf(it2, fmaf(it2, fmaf(it2, F.ca[k][4], F.ca[k][3]), F.ca[k][2]),
+                               F.ca[k][1]), F.ca[k][0]), 1.0f);
   asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(l2) : "f"(t));
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(nu * l2));
-  return e * s;
+  E = nu * l2;
+}
+
+// ς^p·J_ν(t) for the fit of order k: one ex2 of the summed exponent (a
+// vanishing multiplier gives 0 whatever the exponent).
+__device__ __forceinline__ float spow_j(const MomentFit& F, int k, float t, float p, float lsg) {
+  float E, M, e;
+  jfit(F, k, t, E, M);
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(fmaf(p, lsg, E)));
+  return M != 0.0f ? e * M : 0.0f;
 }
 
 // The general-order counterpart of gauss_moment2, for Z ~ N(m, ς²) against τ,
@@ -362,30 +375,17 @@ __device__ __forceinline__ float jfit(const MomentFit& F, int k, float t) {
 //   where it does not exist).
 __device__ __forceinline__ void gauss_moment_gen(const MomentFit& F, float beta, float t, float lsg,
                                                  float& g, float& dg, float& d2g) {
-  float e0, e1;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e0) : "f"(beta * lsg));
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e1) : "f"((beta - 1.0f) * lsg));
-  // (a vanishing J gives 0 even where the power of ς is out of range)
-  const float j0 = jfit(F, 0, t), j1 = jfit(F, 1, t);
-  g = j0 != 0.0f ? e0 * j0 : 0.0f;
-  dg = j1 != 0.0f ? beta * e1 * j1 : 0.0f;
-  d2g = 0.0f;
-  if (F.orders == 3) {
-    float e2;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e2) : "f"((beta - 2.0f) * lsg));
-    const float j2 = jfit(F, 2, t);
-    d2g = j2 != 0.0f ? beta * (beta - 1.0f) * e2 * j2 : 0.0f;
-  }
+  g = spow_j(F, 0, t, beta, lsg);
+  dg = beta * spow_j(F, 1, t, beta - 1.0f, lsg);
+  d2g = F.orders == 3 ? beta * (beta - 1.0f) * spow_j(F, 2, t, beta - 2.0f, lsg) : 0.0f;
 }
 
 // E[(a + σZ)_+^β] alone at a general order (σ = 0: the point mass a_+^β).
 __device__ __forceinline__ float gauss_mass_gen(const MomentFit& F, float beta, float a, float sg) {
   if (!(sg > 0.0f)) return a > 0.0f ? powf(a, beta) : 0.0f;
-  float l2, e;
+  float l2;
   asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(l2) : "f"(sg));
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(beta * l2));
-  const float j = jfit(F, 0, a / sg);
-  return j != 0.0f ? e * j : 0.0f;
+  return spow_j(F, 0, a / sg, beta, l2);
 }
 
 // ---------------------------------------------------------------------------
