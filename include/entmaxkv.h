@@ -38,7 +38,7 @@
 extern "C" {
 #endif
 
-#define ENTMAXKV_VERSION 2
+#define ENTMAXKV_VERSION 3
 
 /* Return codes of every call. */
 typedef enum {
@@ -194,6 +194,26 @@ int32_t entmaxkv_delta_kind(int32_t policy, uint32_t flags);
  */
 int32_t entmaxkv_read_status(const entmaxkv_cache* cache, uint32_t* status_out, int32_t clear,
                              void* stream);
+
+/*
+ * Whether the GAUSSIAN policy supports this α (summary §2B.2: the
+ * normalisation equation at entmax order α). α ∈ {1.5, 2} use closed forms;
+ * any other α > 1 uses fits of the partial moments E[(t + Z)_+^ν] that this
+ * call (or the first decode with that α) builds on the host, about 0.1-0.4 s,
+ * and caches; they must pass a 1e-6 relative check. Returns 1 or 0. Host
+ * only: no CUDA call.
+ */
+int32_t entmaxkv_gaussian_alpha_supported(float alpha);
+
+/*
+ * Diagnostic: the fitted J_ν(t) = E[(t + Z)_+^ν], Z ~ N(0, 1), for
+ * ν = β − order (β = 1/(α−1); order 0, 1, or 2 when β > 1), at the n points
+ * t[i] (host arrays), computed on the host in the float arithmetic the
+ * kernels use, into out[i]. Returns ENTMAXKV_ERR_UNSUPPORTED when α has no
+ * fits (α ∈ {1.5, 2}, which use closed forms, or fits that fail their check)
+ * and ENTMAXKV_ERR_INVALID_ARG for a bad order, count or pointer. Host only.
+ */
+int32_t entmaxkv_moment_fit_eval(float alpha, int32_t order, const float* t, int32_t n, float* out);
 
 /*
  * One decode step for n_seqs sequences (summary §2A-§2C; δ from §3).

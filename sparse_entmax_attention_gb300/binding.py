@@ -33,7 +33,8 @@ EXPORTS = ("entmaxkv_version", "entmaxkv_status_string", "entmaxkv_append",
            "entmaxkv_workspace_bytes", "entmaxkv_decode", "entmaxkv_decode_profiled",
            "entmaxkv_workspace_layout", "entmaxkv_noalloc_scratch_bytes",
            "entmaxkv_decode_softmax_noalloc", "entmaxkv_workspace_bytes_flags",
-           "entmaxkv_delta_kind", "entmaxkv_read_status")
+           "entmaxkv_delta_kind", "entmaxkv_read_status", "entmaxkv_gaussian_alpha_supported",
+           "entmaxkv_moment_fit_eval")
 STAGE_EVENTS = 6
 STAGES = ("clear", "score", "select", "pass_a", "pass_b")
 
@@ -89,6 +90,10 @@ def lib() -> ctypes.CDLL:
     L.entmaxkv_delta_kind.argtypes = [i32, ctypes.c_uint32]
     L.entmaxkv_read_status.restype = i32
     L.entmaxkv_read_status.argtypes = [ctypes.POINTER(CacheView), ctypes.POINTER(ctypes.c_uint32), i32, vp]
+    L.entmaxkv_gaussian_alpha_supported.restype = i32
+    L.entmaxkv_gaussian_alpha_supported.argtypes = [ctypes.c_float]
+    L.entmaxkv_moment_fit_eval.restype = i32
+    L.entmaxkv_moment_fit_eval.argtypes = [ctypes.c_float, i32, vp, i32, vp]
     L.entmaxkv_decode.restype = i32
     L.entmaxkv_decode.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(CacheView), vp, vp, i32,
                                   f32, i32, i32, f32, u32, vp, sz, vp, vp, i32, vp, vp, vp, vp]
@@ -283,3 +288,19 @@ def stage_events():
         e.record()
     torch.cuda.synchronize()
     return evs
+
+
+def gaussian_alpha_supported(alpha: float) -> bool:
+    """entmaxkv_gaussian_alpha_supported (host only)."""
+    return bool(lib().entmaxkv_gaussian_alpha_supported(float(alpha)))
+
+
+def moment_fit_eval(alpha: float, order: int, t):
+    """entmaxkv_moment_fit_eval: the fitted J_ν(t), ν = β − order, on the host
+    in the kernels' float arithmetic. t: 1-d float32 array-like."""
+    import numpy as np
+    ta = np.ascontiguousarray(np.asarray(t, dtype=np.float32))
+    out = np.empty_like(ta)
+    _check(lib().entmaxkv_moment_fit_eval(float(alpha), int(order), ta.ctypes.data_as(ctypes.c_void_p),
+                                          int(ta.size), out.ctypes.data_as(ctypes.c_void_p)))
+    return out

@@ -153,3 +153,53 @@ int moment_fit_for(float beta, MomentFit* out) {
 }
 
 }  // namespace ekv
+
+// ---------------------------------------------------------------------------
+// C ABI: support query and the host evaluation of the fits.
+
+namespace {
+
+float beta_of(float alpha) { return (float)(1.0 / ((double)alpha - 1.0)); }
+
+// The kernels' evaluation (jfit, then 2^E·M), in host float arithmetic.
+float jfit_host(const ekv::MomentFit& F, int k, float t) {
+  const float nu = F.nu[k];
+  float E, M;
+  if (t <= 0.0f) {
+    const float x = -t, xc = fminf(x, 12.0f);
+    const float u = 1.0f / (1.0f + xc * 0.33333334f);
+    E = fmaf(-0.72134752f, x * x, (nu + 1.0f) * log2f(u));
+    M = 0.3989422804f * ekv::clenshaw_host(F.cl[k], fmaf(2.5f, u, -1.5f));
+  } else if (t <= 16.0f) {
+    const float c = ekv::clenshaw_host(F.cr[k], fmaf(t, 0.125f, -1.0f));
+    const float l2 = log2f(1.0f + t);
+    E = F.rlog[k] ? fmaf(nu, l2, c) : nu * l2;
+    M = F.rlog[k] ? 1.0f : c;
+  } else {
+    const float it2 = 1.0f / (t * t);
+    M = fmaf(it2, fmaf(it2, fmaf(it2, fmaf(it2, fmaf(it2, F.ca[k][4], F.ca[k][3]), F.ca[k][2]),
+                                 F.ca[k][1]), F.ca[k][0]), 1.0f);
+    E = nu * log2f(t);
+  }
+  return M != 0.0f ? exp2f(E) * M : 0.0f;
+}
+
+}  // namespace
+
+extern "C" int32_t entmaxkv_gaussian_alpha_supported(float alpha) {
+  if (!(alpha > 1.0f) || !std::isfinite(alpha)) return 0;
+  if (alpha == 1.5f || alpha == 2.0f) return 1;
+  ekv::MomentFit F;
+  return ekv::moment_fit_for(beta_of(alpha), &F) == 0 ? 1 : 0;
+}
+
+extern "C" int32_t entmaxkv_moment_fit_eval(float alpha, int32_t order, const float* t, int32_t n, float* out) {
+  if (n < 0 || (n > 0 && (!t || !out)) || order < 0 || order > 2) return ENTMAXKV_ERR_INVALID_ARG;
+  if (!(alpha > 1.0f) || !std::isfinite(alpha)) return ENTMAXKV_ERR_INVALID_ARG;
+  if (alpha == 1.5f || alpha == 2.0f) return ENTMAXKV_ERR_UNSUPPORTED;
+  ekv::MomentFit F;
+  if (ekv::moment_fit_for(beta_of(alpha), &F)) return ENTMAXKV_ERR_UNSUPPORTED;
+  if (order >= F.orders) return ENTMAXKV_ERR_INVALID_ARG;
+  for (int i = 0; i < n; ++i) out[i] = jfit_host(F, order, t[i]);
+  return ENTMAXKV_OK;
+}

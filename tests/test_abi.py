@@ -6,6 +6,7 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 
 from sparse_entmax_attention_gb300 import binding as B
@@ -35,7 +36,7 @@ def test_exports_every_declared_function(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert lib.entmaxkv_version() == 2
+    assert lib.entmaxkv_version() == 3
     for code in range(5):
         assert lib.entmaxkv_status_string(code)
     assert lib.entmaxkv_status_string(99) == b"unknown status"
@@ -167,3 +168,35 @@ def test_bf16_metadata_copies_come_in_pairs(lib):
                              1.5, B.POLICY_GAUSSIAN, 0, 0.5, 0, ctypes.c_void_p(256), 1 << 40,
                              ctypes.c_void_p(256), None, 0, None, None, None, None)
     assert rc == 1
+
+
+def test_gaussian_alpha_support_query(lib):
+    assert B.gaussian_alpha_supported(1.5) and B.gaussian_alpha_supported(2.0)
+    assert B.gaussian_alpha_supported(1.25) and B.gaussian_alpha_supported(3.0)
+    assert not B.gaussian_alpha_supported(1.05)   # β = 20: the fits fail their check
+    assert not B.gaussian_alpha_supported(1.0) and not B.gaussian_alpha_supported(float("nan"))
+
+
+@pytest.mark.parametrize("alpha", [1.15, 1.25, 1.75, 3.0, 5.0])
+def test_moment_fits_match_the_oracle(lib, alpha):
+    """The host-built fits of J_ν(t) = E[(t + Z)_+^ν] (ν = β, β − 1, β − 2),
+    evaluated in the kernels' float arithmetic, against the oracle's float64
+    J on both sides of t = 0 and past the series switch at t = 16. The value
+    is 2^E·M with a float exponent E of size up to about 100 (−t²/(2 ln 2) in
+    the left tail, ν·log2 t far right), whose rounding alone is about
+    |E|·2^-24 relative in 2^E; hence 1e-5. Where J is below 1e-30 (far left
+    tail) only the absolute size is checked."""
+    from oracle import pages as opg
+    beta = 1.0 / (alpha - 1.0)
+    t = np.concatenate([np.linspace(-12.0, 0.0, 97), np.linspace(0.05, 16.0, 160), np.linspace(16.5, 60.0, 30)])
+    for order in range(3 if beta > 1.0 else 2):
+        got = B.moment_fit_eval(alpha, order, t).astype(np.float64)
+        ref = opg.jfun(t.astype(np.float32).astype(np.float64), beta - order)
+        big = ref > 1e-30
+        rel = np.abs(got[big] - ref[big]) / ref[big]
+        assert rel.max() < 1e-5, (alpha, order, float(rel.max()), float(t[big][rel.argmax()]))
+        assert np.all(np.abs(got[~big]) < 1e-29)
+    with pytest.raises(B.EntmaxKVError):
+        B.moment_fit_eval(1.5, 0, t)   # closed forms: no fits
+    with pytest.raises(B.EntmaxKVError):
+        B.moment_fit_eval(alpha, 3, t)
