@@ -80,49 +80,56 @@ float clenshaw_host(const float* c, float x) {  // the device's float Clenshaw
   return fmaf(x, b1, c[0] - b2);
 }
 
+// The fit of order k (ν = β − k) into F; false when it misses its check.
+bool build_order(double beta, int k, MomentFit& F) {
+  const double nu = beta - k;
+  F.nu[k] = (float)nu;
+  // left: w ↦ u = (w + 1.5)/2.5 ↦ x = 3(1/u − 1); fit J_ν(−x)/φ(x)·u^{−(ν+1)}
+  auto gl = [nu](double w) {
+    const double u = (w + 1.5) / 2.5, x = 3.0 * (1.0 / u - 1.0);
+    return j_left_ratio(x, nu) * pow(u, -(nu + 1.0));
+  };
+  // right: z ↦ t = 8(z + 1); fit J_ν(t)/(1 + t)^ν, or its log2 for ν ≥ 1
+  // (there the ratio spans orders of magnitude; for ν near −1 the log has
+  // complex singularities close to the axis and the ratio itself is tame)
+  const bool lg = nu >= 1.0;
+  F.rlog[k] = lg;
+  auto gr = [nu, lg](double z) {
+    const double t = 8.0 * (z + 1.0);
+    return lg ? log2(j_right(t, nu)) - nu * log2(1.0 + t) : j_right(t, nu) * pow(1.0 + t, -nu);
+  };
+  cheb_fit(gl, F.cl[k]);
+  cheb_fit(gr, F.cr[k]);
+  double dfact = 1.0;
+  for (int m = 1; m <= 5; ++m) {
+    dfact *= 2 * m - 1;
+    F.ca[k][m - 1] = (float)(binom(nu, 2 * m) * dfact);
+  }
+  // checks, in the float arithmetic the kernels use for the fitted factors
+  for (int i = 0; i <= 200; ++i) {
+    const double v = -1.0 + 2.0 * i / 200.0;
+    const double rl = gl(v), rr = gr(v);
+    if (!(fabs(clenshaw_host(F.cl[k], (float)v) - rl) <= 1e-6 * fabs(rl))) return false;
+    const double er = fabs(clenshaw_host(F.cr[k], (float)v) - rr);
+    if (!(lg ? er <= 1e-6 / M_LN2 : er <= 1e-6 * fabs(rr))) return false;
+  }
+  for (double t = 16.0; t <= 64.0; t += 4.0) {
+    const double it2 = 1.0 / (t * t);
+    double s = 1.0, p = 1.0;
+    for (int m = 0; m < 5; ++m) s += F.ca[k][m] * (p *= it2);
+    const double ref = j_right(t, nu);
+    if (!(fabs(pow(t, nu) * s - ref) <= 1e-6 * fabs(ref))) return false;
+  }
+  return true;
+}
+
+// Orders β and β − 1 must pass. Order β − 2 only feeds the τ̂ solve's Halley
+// correction: where it fails (β just above 1, ν near −1, where J_ν is nearly
+// singular) the solve takes Newton steps instead, as for β ≤ 1.
 bool build(double beta, MomentFit& F) {
   memset(&F, 0, sizeof(F));
-  F.orders = beta > 1.0 ? 3 : 2;
-  for (int k = 0; k < F.orders; ++k) {
-    const double nu = beta - k;
-    F.nu[k] = (float)nu;
-    // left: w ↦ u = (w + 1.5)/2.5 ↦ x = 3(1/u − 1); fit J_ν(−x)/φ(x)·u^{−(ν+1)}
-    auto gl = [nu](double w) {
-      const double u = (w + 1.5) / 2.5, x = 3.0 * (1.0 / u - 1.0);
-      return j_left_ratio(x, nu) * pow(u, -(nu + 1.0));
-    };
-    // right: z ↦ t = 8(z + 1); fit J_ν(t)/(1 + t)^ν, or its log2 for ν ≥ 1
-    // (there the ratio spans orders of magnitude; for ν near −1 the log has
-    // complex singularities close to the axis and the ratio itself is tame)
-    const bool lg = nu >= 1.0;
-    F.rlog[k] = lg;
-    auto gr = [nu, lg](double z) {
-      const double t = 8.0 * (z + 1.0);
-      return lg ? log2(j_right(t, nu)) - nu * log2(1.0 + t) : j_right(t, nu) * pow(1.0 + t, -nu);
-    };
-    cheb_fit(gl, F.cl[k]);
-    cheb_fit(gr, F.cr[k]);
-    double dfact = 1.0;
-    for (int m = 1; m <= 5; ++m) {
-      dfact *= 2 * m - 1;
-      F.ca[k][m - 1] = (float)(binom(nu, 2 * m) * dfact);
-    }
-    // checks, in the float arithmetic the kernels use for the fitted factors
-    for (int i = 0; i <= 200; ++i) {
-      const double v = -1.0 + 2.0 * i / 200.0;
-      const double rl = gl(v), rr = gr(v);
-      if (!(fabs(clenshaw_host(F.cl[k], (float)v) - rl) <= 1e-6 * fabs(rl))) return false;
-      const double er = fabs(clenshaw_host(F.cr[k], (float)v) - rr);
-      if (!(lg ? er <= 1e-6 / M_LN2 : er <= 1e-6 * fabs(rr))) return false;
-    }
-    for (double t = 16.0; t <= 64.0; t += 4.0) {
-      const double it2 = 1.0 / (t * t);
-      double s = 1.0, p = 1.0;
-      for (int m = 0; m < 5; ++m) s += F.ca[k][m] * (p *= it2);
-      const double ref = j_right(t, nu);
-      if (!(fabs(pow(t, nu) * s - ref) <= 1e-6 * fabs(ref))) return false;
-    }
-  }
+  if (!build_order(beta, 0, F) || !build_order(beta, 1, F)) return false;
+  F.orders = (beta > 1.0 && build_order(beta, 2, F)) ? 3 : 2;
   return true;
 }
 

@@ -182,7 +182,7 @@ def test_dense_v_flag_same_result(small_bf16):
     torch.testing.assert_close(b.out, out_sparse_v, rtol=1e-6, atol=1e-6)
 
 
-@pytest.mark.parametrize("alpha", [1.15, 1.25, 1.75, 3.0, 5.0])
+@pytest.mark.parametrize("alpha", [1.15, 1.25, 1.75, 1.95, 3.0, 5.0])
 @pytest.mark.parametrize("margin", [0.0, 0.5])
 def test_gaussian_general_alpha(small_bf16, small_f32, alpha, margin):
     """The Gaussian selector at orders without closed forms (β = 4, 4/3, 1/2):
