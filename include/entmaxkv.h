@@ -56,8 +56,9 @@ typedef enum {
 #define ENTMAXKV_DEV_CAND_OVERFLOW   0x8u  /* informational: the exact-τ solve used its slow full-scan path */
 #define ENTMAXKV_DEV_TAU_NOCONV      0x10u /* the exact-τ solve stopped at its iteration limit              */
 #define ENTMAXKV_DEV_BAD_SEQ_ID      0x20u /* a seq_ids entry outside [0, max_seqs): that sequence skipped  */
-#define ENTMAXKV_DEV_TIMEOUT         0x40u /* a bounded wait on an asynchronous copy ran out; the block
-                                              stopped early and its results are incomplete              */
+#define ENTMAXKV_DEV_TIMEOUT         0x40u /* a bounded wait on an asynchronous copy ran out (about
+                                              4M polls); the block waited for its copies in flight,
+                                              stopped early, and its results are incomplete             */
 
 /* KV storage types. */
 #define ENTMAXKV_F32  0
@@ -83,6 +84,17 @@ typedef enum {
                                          K page; a diagnostic, not for timed steps.
                                          The workspace must then hold
                                          entmaxkv_workspace_bytes_flags(...) bytes. */
+
+#define ENTMAXKV_FLAG_EXPIRE_WAITS 0x100u  /* diagnostic, for testing the device-side
+                                          timeout path: the Gaussian page scorer's
+                                          waits for its staged copies give up at once
+                                          instead of polling, as a wait that runs out
+                                          of its bound does. The scorer then raises
+                                          ENTMAXKV_DEV_TIMEOUT, waits (bounded) for
+                                          the copies it issued and stops; the decode
+                                          completes with every page unscored, so out
+                                          is 0, n_sel 0 and tau NaN. Never set it for
+                                          real work.                              */
 
 /* What the delta output of a decode holds (entmaxkv_delta_kind). */
 #define ENTMAXKV_DELTA_ZERO      0  /* FULL, SOFTMAX: nothing is dropped            */

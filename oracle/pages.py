@@ -66,6 +66,39 @@ def page_metadata(keys, page_size: int):
     return {"kmin": kmin, "kmax": kmax, "mean": mean, "var": var, "n": n}
 
 
+def bf16_round(x):
+    """Round float64 values to the nearest bfloat16 value, ties to even.
+
+    bfloat16 keeps 8 significant bits and float32's exponent range. With
+    x = m·2^e (frexp, 0.5 ≤ |m| < 1) the nearest value is round(m·2^8)·2^(e−8);
+    both scalings are exact in float64 and ``np.round`` rounds halves to
+    even. Below the smallest normal (2^-126) the spacing stays 2^-133.
+    Returned as float64 (every bfloat16 value is exact there).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    m, e = np.frexp(x)
+    shift = np.maximum(e - 8, -133)
+    return np.ldexp(np.round(np.ldexp(x, -shift)), shift)
+
+
+def bf16_metadata(meta):
+    """The page statistics rounded the way a cache that streams bfloat16
+    copies of them stores them.
+
+    Reading (the summary's §4 says the cost of decoding moves to page
+    selection; the copies halve the bytes the Gaussian scorer streams): the
+    stored mean and the sum of squared deviations m2 = n_p·var are each
+    rounded to the nearest bfloat16 (ties to even) from their exact values;
+    the scorer then uses var = bf16(m2)/n_p. Bounding box and counts are
+    unchanged. Returns a new dict.
+    """
+    out = dict(meta)
+    n = np.asarray(meta["n"], np.float64)[:, None]
+    out["mean"] = bf16_round(meta["mean"])
+    out["var"] = bf16_round(np.asarray(meta["var"], np.float64) * n) / n
+    return out
+
+
 def welford_append(n: int, mean, m2, x):
     """One-token update of (count, mean, sum of squared deviations).
 
@@ -242,7 +275,8 @@ def est_max(mu, sigma, n):
     """Estimated maximum score of a page: M̂_p = μ_p + σ_p·sqrt(2 ln n_p).
 
     The textbook leading term for the maximum of n Gaussian draws; a
-    one-token page gives M̂_p = μ_p.
+    one-token page gives M̂_p = μ_p. n_p is the page's count of valid
+    tokens (a partly filled last page uses its own count, not the page size).
     """
     n = np.asarray(n, dtype=np.float64)
     return np.asarray(mu) + np.asarray(sigma) * np.sqrt(2.0 * np.log(n))

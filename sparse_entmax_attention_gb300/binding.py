@@ -23,7 +23,7 @@ F32, BF16 = 0, 1
 POLICY_FULL, POLICY_TOPK, POLICY_GAUSSIAN, POLICY_SOFTMAX, POLICY_SOFTMAX_TOPK = 0, 1, 2, 3, 4
 POLICIES = {"full": POLICY_FULL, "topk": POLICY_TOPK, "gaussian": POLICY_GAUSSIAN,
             "softmax": POLICY_SOFTMAX, "softmax_topk": POLICY_SOFTMAX_TOPK}
-FLAG_DENSE_V, FLAG_EXACT_DELTA = 0x1, 0x2
+FLAG_DENSE_V, FLAG_EXACT_DELTA, FLAG_EXPIRE_WAITS = 0x1, 0x2, 0x100
 DELTA_ZERO, DELTA_CERTIFIED, DELTA_MODEL, DELTA_EXACT = 0, 1, 2, 3
 DEV_BAD_PAGE_TABLE, DEV_CAPACITY, DEV_TAUHAT_NOCONV = 0x1, 0x2, 0x4
 DEV_CAND_OVERFLOW, DEV_TAU_NOCONV, DEV_BAD_SEQ_ID, DEV_TIMEOUT = 0x8, 0x10, 0x20, 0x40
@@ -172,6 +172,8 @@ class PagedCache:
         other.view = CacheView(*[getattr(self.view, f) for f, _ in CacheView._fields_])
         other.view.mean_bf16 = None
         other.view.m2_bf16 = None
+        other.mean_bf16 = None  # (this view streams none; self keeps the tensors alive)
+        other.m2_bf16 = None
         return other
 
     @property

@@ -3,12 +3,31 @@
 #include <math.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "common.cuh"
 
 namespace ekv {
 
-constexpr int kSmCount = 152;                 // GB300: grids are sized for its 152 SMs
-constexpr int kTargetBlocks = 2 * kSmCount;   // decode blocks per launch: one wave at 2 per SM
+// The workspace is laid out for at most this many decode blocks per launch,
+// whatever the device; a launch uses one wave of 2 blocks per SM of the
+// current device, capped at the layout's count.
+constexpr int kLayoutBlocks = 2048;
+
+// Streaming multiprocessors of the current device, queried once per device
+// (0 when the query fails).
+constexpr int kMaxDevices = 64;
+static std::atomic<int> g_sms[kMaxDevices];
+
+static int device_sms() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  int n = g_sms[dev].load(std::memory_order_relaxed);
+  if (n > 0) return n;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) return 0;
+  g_sms[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
 
 struct Layout {
   size_t zmax, cnt_a, cnt_b, cand_cnt, kept_mass, dbar, bitmap, ctrl_end;
@@ -71,7 +90,7 @@ static int compute_layout(const entmaxkv_config* c, int S, int policy, int budge
   L.cap_pages = cap;
   const long long units = (long long)S * Hkv;
   long long splits = (cap + 7) / 8;
-  long long tgt = (kTargetBlocks + units - 1) / units;
+  long long tgt = (kLayoutBlocks + units - 1) / units;
   if (splits > tgt) splits = tgt;
   const bool bitmap = topk || policy == ENTMAXKV_POLICY_GAUSSIAN;
   const long long need = (cap + kListCap - 1) / kListCap;
@@ -106,9 +125,9 @@ static int compute_layout(const entmaxkv_config* c, int S, int policy, int budge
   L.z = entmax ? take(nk * (size_t)cap * P * G * 4) : none;
   L.pmax = entmax ? take(nk * (size_t)cap * G * 4) : none;
   L.pstride = (G * D + 4 * G + 3) & ~3;  // acc [G][D], then 4 floats per head
-  L.partial = take(nk * (size_t)L.splits * L.pstride * 4);
+  L.partial = entmax ? none : take(nk * (size_t)L.splits * L.pstride * 4);
   L.diag = take(nq * 4);
-  L.mslots = gauss_grid_x(maxp, Hkv, S, kSmCount);
+  L.mslots = gauss_grid_x(maxp, Hkv, S, 0);
   L.mslot = policy == ENTMAXKV_POLICY_GAUSSIAN ? take(nq * (size_t)L.mslots * 4) : none;
   L.total = off;
   return ENTMAXKV_OK;
@@ -171,6 +190,23 @@ static size_t total_bytes(const entmaxkv_config* c, int S, int policy, int budge
     return L.total;
   if (compute_layout(c, S, full_policy_of(policy), 0, LF) != ENTMAXKV_OK) return 0;
   return up256(L.total) + LF.total;
+}
+
+// Blocks per (sequence, KV head) of one decode launch: one wave of 2 blocks
+// per SM over all units, at most one per 8 kept pages and at most the
+// layout's count, but at least enough that no block holds more than kListCap
+// pages of a bitmap policy (the layout's lower bound).
+static int launch_splits(const Layout& L, int S, int Hkv, int policy, int sms) {
+  const long long units = (long long)S * Hkv;
+  long long splits = (L.cap_pages + 7) / 8;
+  const long long tgt = (2LL * sms + units - 1) / units;
+  if (splits > tgt) splits = tgt;
+  const bool bitmap = policy == ENTMAXKV_POLICY_TOPK || policy == ENTMAXKV_POLICY_SOFTMAX_TOPK ||
+                      policy == ENTMAXKV_POLICY_GAUSSIAN;
+  const long long need = (L.cap_pages + kListCap - 1) / kListCap;
+  if (bitmap && splits < need) splits = need;
+  if (splits > L.splits) splits = L.splits;
+  return splits < 1 ? 1 : (int)splits;
 }
 
 }  // namespace ekv
@@ -341,6 +377,9 @@ static int32_t decode_impl(const entmaxkv_config* cfg, const entmaxkv_cache* cac
   if (policy == ENTMAXKV_POLICY_GAUSSIAN && al != 1.5f && al != 2.0f &&
       moment_fit_for(a.beta, &a.fit))
     return ENTMAXKV_ERR_UNSUPPORTED;
+  // Every argument is checked; the launch shapes come from the device.
+  const int sms = device_sms();
+  if (sms < 1) return ENTMAXKV_ERR_CUDA;
   a.k_pool = cache->k_pool;
   a.v_pool = cache->v_pool;
   a.kmin = cache->kmin;
@@ -361,6 +400,8 @@ static int32_t decode_impl(const entmaxkv_config* cfg, const entmaxkv_cache* cac
   a.tau_out = tau;
   a.delta_out = delta;
   bind_workspace(a, workspace, L);
+  a.splits = launch_splits(L, n_seqs, cfg->num_kv_heads, policy, sms);
+  a.mslots = gauss_grid_x(cfg->max_pages_per_seq, cfg->num_kv_heads, n_seqs, sms);
 
   cudaStream_t s = (cudaStream_t)stream;
   auto mark = [&](int i) -> cudaError_t {
@@ -374,8 +415,8 @@ static int32_t decode_impl(const entmaxkv_config* cfg, const entmaxkv_cache* cac
   const int dt = cfg->kv_dtype;
   // stage 1: page scoring
   if (e == cudaSuccess) {
-    if (topk) e = launch_bbox(a, dt, kSmCount, s);
-    else if (policy == ENTMAXKV_POLICY_GAUSSIAN) e = launch_gauss(a, dt, kSmCount, s);
+    if (topk) e = launch_bbox(a, dt, sms, s);
+    else if (policy == ENTMAXKV_POLICY_GAUSSIAN) e = launch_gauss(a, dt, sms, s);
   }
   if (e == cudaSuccess) e = mark(2);
   // stage 2: selection
@@ -408,6 +449,8 @@ static int32_t decode_impl(const entmaxkv_config* cfg, const entmaxkv_cache* cac
     f.tau_out = nullptr;
     f.delta_out = nullptr;
     bind_workspace(f, ws2, LF);
+    f.splits = launch_splits(LF, n_seqs, cfg->num_kv_heads, f.policy, sms);
+    f.mslots = 0;
     e = cudaMemsetAsync(ws2, 0, LF.ctrl_end, s);
     if (e == cudaSuccess) e = soft ? launch_softmax(f, dt, s) : launch_pass_a(f, dt, s);
     if (e == cudaSuccess) e = launch_exact_delta(a, f, s);

@@ -418,12 +418,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Wait for the phase with the given parity to complete; false when the
-// bounded number of polls ran out (the caller flags ENTMAXKV_DEV_TIMEOUT).
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
-  for (int i = 0; i < (1 << 22); ++i)
+// Wait for the phase with the given parity to complete; false when `limit`
+// polls ran out (the caller flags ENTMAXKV_DEV_TIMEOUT). A limit of 0 gives
+// up at once (ENTMAXKV_FLAG_EXPIRE_WAITS).
+constexpr int kPollLimit = 1 << 22;
+__device__ __forceinline__ bool mbar_wait_limit(uint64_t* bar, uint32_t parity, int limit) {
+  for (int i = 0; i < limit; ++i)
     if (mbar_try_wait(bar, parity)) return true;
   return false;
+}
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+  return mbar_wait_limit(bar, parity, kPollLimit);
+}
+// The phase parity of the n-th fill (counted from 1) of a stage of a ring of
+// nst stages whose fills are issued in order, stage = fill index % nst: a
+// stopped ring waits for these to land before its block exits.
+__device__ __forceinline__ int ring_fills(int n_issued, int st, int nst) {
+  return n_issued > st ? (n_issued - st + nst - 1) / nst : 0;
 }
 // size bytes from global src to shared dst (both 16-byte aligned, size a
 // multiple of 16), completing `size` transaction bytes on bar.

@@ -281,6 +281,7 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_kernel(DecodeArgs a) {
     }
   };
   // refill stage st with group g: look its pages up, then copy
+  int n_issued = 0;  // fills issued so far (warp 0)
   auto issue = [&](int g, int st) {
     if (lane < PPS) {
       const int p = g * PPS + lane;
@@ -288,6 +289,7 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_kernel(DecodeArgs a) {
     }
     __syncwarp();
     issue_copies(st);
+    ++n_issued;
   };
   if (warp == 0) {
     // The pipeline starts before anything else: barriers, then every page of
@@ -306,6 +308,7 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_kernel(DecodeArgs a) {
     }
     __syncwarp();
     for (int j = 0; j < nfill; ++j) issue_copies(j);
+    n_issued = nfill;
   }
 
   unsigned long long qp[GP][DPL / 2], q2p[GP][DPL / 2];
@@ -341,12 +344,13 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_kernel(DecodeArgs a) {
 
   __syncthreads();  // barriers initialised, q in registers
 
+  const int wait_limit = (a.flags & ENTMAXKV_FLAG_EXPIRE_WAITS) ? 0 : kPollLimit;
   int stuck = 0;
   for (int j = 0; j < n_mine; ++j) {
     const int st = j % NST;
     const uint32_t par = (uint32_t)((j / NST) & 1);
     const int g = g_lo + j;
-    if (!mbar_wait_bounded(&full[st], par)) {
+    if (!mbar_wait_limit(&full[st], par, wait_limit)) {
       stuck = 1;
       break;
     }
@@ -438,10 +442,14 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_kernel(DecodeArgs a) {
   }
   if (stuck) {
     // A copy or a stage release never arrived within the bound: flag it and
-    // stop. Copies already issued are waited for (bounded) before leaving.
+    // stop. The producer waits (bounded) for the last fill it issued into
+    // each stage, so no copy is still landing when the block exits.
     if (lane == 0) raise_flag(a.status, ENTMAXKV_DEV_TIMEOUT);
     if (warp == 0)
-      for (int st = 0; st < NST; ++st) mbar_wait_bounded(&full[st], 0u), mbar_wait_bounded(&full[st], 1u);
+      for (int st = 0; st < NST; ++st) {
+        const int f = ring_fills(n_issued, st, NST);
+        if (f > 0) mbar_wait_bounded(&full[st], (uint32_t)((f - 1) & 1));
+      }
   }
 #pragma unroll
   for (int i = 0; i < NFIN; ++i)
@@ -538,6 +546,7 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_mma_kernel(DecodeArgs 
       bulk_g2s(dyn + st * sstride + (lane >> 1) * pstride + (lane & 1) * run, src, (uint32_t)run, &full[st]);
     }
   };
+  int n_issued = 0;  // fills issued so far (warp 0)
   auto issue = [&](int g, int st) {
     if (lane < PPS) {
       const int p = g * PPS + lane, i = p - g_lo * PPS;
@@ -547,6 +556,7 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_mma_kernel(DecodeArgs 
     }
     __syncwarp();
     issue_copies(st);
+    ++n_issued;
   };
   if (warp == 0) {
     if (lane < NST) {
@@ -563,6 +573,7 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_mma_kernel(DecodeArgs 
     }
     __syncwarp();
     for (int j = 0; j < nfill; ++j) issue_copies(j);
+    n_issued = nfill;
   }
 
   // A fragments: row lane/4 (a query head of the group), dims 2(lane%4)+{0,1}
@@ -589,12 +600,13 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_mma_kernel(DecodeArgs 
   const float inv_full = 1.0f / ((float)a.P * (float)D);
   float runmax = -CUDART_INF_F;
   const int lrow = lane & 7, lk = ((lane >> 3) & 1) * 16;  // ldmatrix: page row, byte offset in the step
+  const int wait_limit = (a.flags & ENTMAXKV_FLAG_EXPIRE_WAITS) ? 0 : kPollLimit;
   int stuck = 0;
   for (int j = 0; j < n_mine; ++j) {
     const int st = j % NST;
     const uint32_t par = (uint32_t)((j / NST) & 1);
     const int g = g_lo + j;
-    if (!mbar_wait_bounded(&full[st], par)) {
+    if (!mbar_wait_limit(&full[st], par, wait_limit)) {
       stuck = 1;
       break;
     }
@@ -642,10 +654,13 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_mma_kernel(DecodeArgs 
       runmax = fmaxf(runmax, m);
     }
   }
-  if (stuck) {
+  if (stuck) {  // as in gauss_kernel: flag, then let the issued fills land
     if (lane == 0) raise_flag(a.status, ENTMAXKV_DEV_TIMEOUT);
     if (warp == 0)
-      for (int st = 0; st < NST; ++st) mbar_wait_bounded(&full[st], 0u), mbar_wait_bounded(&full[st], 1u);
+      for (int st = 0; st < NST; ++st) {
+        const int f = ring_fills(n_issued, st, NST);
+        if (f > 0) mbar_wait_bounded(&full[st], (uint32_t)((f - 1) & 1));
+      }
   }
   runmax = fmaxf(runmax, __shfl_xor_sync(0xffffffffu, runmax, 1));
   runmax = fmaxf(runmax, __shfl_xor_sync(0xffffffffu, runmax, 2));
@@ -713,13 +728,16 @@ static cudaError_t gauss_dispatch_g(const DecodeArgs& a, dim3 grid, cudaStream_t
 }
 
 // ~2 blocks per SM (96 KiB of stages each) over all (sequence, 8-KV-head)
-// rows, at least 8 page groups per block.
+// rows, at least 8 page groups per block; sms = 0 gives the largest grid any
+// device uses (the workspace's count of per-block maxima slots).
 int gauss_grid_x(int maxp, int Hkv, int S, int sms) {
   const int groups = (maxp + kGaussPPS - 1) / kGaussPPS;
   const int rows = ((Hkv + 7) / 8) * S;
   int gx = (groups + 7) / 8;
-  const int cap = (2 * sms + rows - 1) / rows;
-  if (gx > cap) gx = cap;
+  if (sms > 0) {
+    const int cap = (2 * sms + rows - 1) / rows;
+    if (gx > cap) gx = cap;
+  }
   return gx < 1 ? 1 : gx;
 }
 

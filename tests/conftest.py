@@ -26,3 +26,21 @@ def pytest_collection_modifyitems(config, items):
     for it in items:
         if "gpu" in it.keywords:
             it.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    """Selected-page parity of the GPU tests: how many (sequence, KV head)
+    units were compared with the oracle, every page decided differently (each
+    inside its ε_sel or bf16 rounding band, else its test failed), and the
+    smallest float64 decision margin met."""
+    h = sys.modules.get("harness")
+    if h is None or not h.PARITY["checks"]:
+        return
+    p = h.PARITY
+    tr = terminalreporter
+    tr.write_line(f"selected-page parity: {p['checks']} decodes, {p['units']} (sequence, KV head) units, "
+                  f"{p['pages']} page decisions, {len(p['flips'])} flips")
+    if p["min_margin_at"] is not None:
+        tr.write_line(f"smallest |decision margin|: {p['min_margin']:.3e} at {p['min_margin_at']}")
+    for f in p["flips"]:
+        tr.write_line("  flip " + f)

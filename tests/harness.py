@@ -54,20 +54,14 @@ class Built:
         L = int(self.cache.seq_lens[b].item())
         return (self.K[b][j, :L].double().cpu().numpy(), self.V[b][j, :L].double().cpu().numpy())
 
-    def host_meta(self, b, j):
-        """Page metadata of (sequence b, KV head j) as the Gaussian scorer reads
-        it: the oracle's float64 metadata of the stored keys, with the mean and
-        variance replaced by the stored bf16 copies when the cache keeps them
-        (None otherwise: the oracle then builds its own)."""
-        c = self.cache
-        if c.mean_bf16 is None:
-            return None
+    def host_meta(self, b, j, bf16=False):
+        """The oracle's own float64 page metadata of the stored keys of
+        (sequence b, KV head j); with ``bf16`` the mean and m2 are rounded to
+        bfloat16 from their exact values (the oracle's reading of a cache that
+        streams bf16 copies). Nothing here is read back from the GPU."""
         K, _ = self.host_kv(b, j)
         meta = opg.page_metadata(K, self.spec.page_size)
-        phys = c.block_table[b, : len(meta["n"])].long()
-        meta["mean"] = c.mean_bf16[phys, j].double().cpu().numpy()
-        meta["var"] = c.m2_bf16[phys, j].double().cpu().numpy() / meta["n"][:, None]
-        return meta
+        return opg.bf16_metadata(meta) if bf16 else meta
 
     def host_q(self, b, j, q=None):
         q = self.q if q is None else q
@@ -82,18 +76,69 @@ def rel_l2(a, b):
     return float(np.linalg.norm(a - b) / (den if den > 0 else 1.0))
 
 
-def near_tie_topk(uhat, k, eps_rel=1e-5):
-    """Pages whose key sits within eps of the k-th key (a flip there is a near tie)."""
-    u = np.asarray(uhat, np.float64)
-    if k >= u.size:
-        return set()
-    kth = np.sort(u)[::-1][k - 1]
-    eps = eps_rel * max(1.0, abs(kth))
-    return set(np.nonzero(np.abs(u - kth) <= eps)[0].tolist())
+# --------------------------------------------------------------------------
+# bf16 statistics: the rounding-boundary band
+# --------------------------------------------------------------------------
+
+def bf16_stat_band(K, P, Q):
+    """How far a page's (μ_p^h, σ_p^h) in score units can move between the
+    oracle's reading (exact statistics rounded to bfloat16) and the GPU's
+    copies (float32 statistics rounded to bfloat16).
+
+    The GPU's float32 mean is within w = 2^-18·max_t |k_t,d| of the exact one
+    (a float32 sum of at most 32 terms and one division, or their pairwise
+    merges), and its m2 within w = 2^-17·Σ_t k_t,d². An element whose
+    window [x − w, x + w] rounds to two different bfloat16 values may be
+    stored as either; every other element is stored exactly as the oracle
+    reads it. Returns (dmu, dsig) [g, n_pages]: bounds on |Δμ| and |Δσ|.
+    """
+    K = np.asarray(K, np.float64)
+    Q = np.atleast_2d(np.asarray(Q, np.float64))
+    n_tok, d = K.shape
+    n_pages = -(-n_tok // P)
+    Kp = np.zeros((n_pages * P, d))
+    Kp[:n_tok] = K
+    Kp = Kp.reshape(n_pages, P, d)
+    meta = opg.page_metadata(K, P)
+    n = meta["n"].astype(np.float64)[:, None]
+    mean, m2 = meta["mean"], meta["var"] * n
+    w_mean = 2.0 ** -18 * np.abs(Kp).max(axis=1)
+    w_m2 = 2.0 ** -17 * (Kp * Kp).sum(axis=1)
+
+    def spread(x, w):
+        lo, hi, r = opg.bf16_round(x - w), opg.bf16_round(x + w), opg.bf16_round(x)
+        return np.maximum(np.abs(hi - r), np.abs(lo - r))
+
+    dmean, dm2 = spread(mean, w_mean), spread(m2, w_m2)
+    dmu = np.abs(Q) @ dmean.T / math.sqrt(d)                 # [g, n_pages]
+    dvar = (Q * Q) @ (dm2 / n).T / d
+    bm = opg.bf16_metadata(meta)
+    _, sig = zip(*[opg.gauss_page_scores(Q[h], bm["mean"], bm["var"]) for h in range(Q.shape[0])])
+    s2 = np.stack(sig) ** 2
+    dsig = np.sqrt(s2 + dvar) - np.sqrt(np.maximum(s2 - dvar, 0.0))
+    return dmu, dsig
 
 
-def near_tie_gauss(mhat, thr, eps):
-    """Pages whose decision M̂ ≥ threshold is within eps for some head."""
-    mh = np.asarray(mhat)
-    t = np.asarray(thr)[:, None]
-    return set(np.nonzero((np.abs(mh - t) <= eps).any(axis=0))[0].tolist())
+# --------------------------------------------------------------------------
+# Selected-page parity record (printed at the end of the session)
+# --------------------------------------------------------------------------
+
+PARITY = {"checks": 0, "units": 0, "pages": 0, "flips": [], "min_margin": math.inf,
+          "min_margin_at": None}
+
+
+def record_unit(tag, n_pages, margins, eps):
+    """Count one compared (sequence, KV head) unit and keep the smallest
+    decision margin, relative to its ε_sel, seen so far."""
+    PARITY["units"] += 1
+    PARITY["pages"] += int(n_pages)
+    if margins is not None and np.size(margins):
+        m = float(np.min(np.abs(margins)))
+        if m < PARITY["min_margin"]:
+            PARITY["min_margin"] = m
+            PARITY["min_margin_at"] = f"{tag} (ε_sel {eps:.2e})"
+
+
+def record_flip(tag, page, margin, eps, band, why):
+    PARITY["flips"].append(f"{tag}: page {page} margin {margin:+.3e} (ε_sel {eps:.2e}, "
+                           f"bf16 band {band:.2e}; {why})")

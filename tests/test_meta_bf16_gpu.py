@@ -1,12 +1,14 @@
 """GPU: caches that keep bf16 copies of the page mean and m2 for the Gaussian
 scorer.
 
-Metadata parity is exact by construction: every copy must equal the
-round-to-nearest-even bf16 of the fp32 value append keeps (which the fp32
-metadata tests pin to the float64 page statistics), including pages filled
-token by token. Decode parity is then checked against the oracle run on the
-metadata the scorer reads (the stored bf16 values in float64), with the same
-tolerances as the fp32-metadata path.
+The copies themselves must equal the round-to-nearest-even bf16 of the fp32
+value append keeps (which the fp32 metadata tests pin to the float64 page
+statistics), including pages filled token by token. Decode parity is checked
+against the oracle's own reading of such a cache: its exact float64 mean and
+m2 rounded to bfloat16 (no value is read back from the GPU). Where the GPU's
+float32 statistic and the exact one round to different bfloat16 neighbours
+the pages can differ inside a small band; check_decode accepts and records
+those as rounding-boundary near ties and fails on any other difference.
 """
 
 import pytest

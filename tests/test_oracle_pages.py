@@ -275,3 +275,79 @@ def test_jfun_matches_high_precision_quadrature():
                 ref = mp.quad(lambda y: y ** nu * mp.npdf(y - t), [0, max(t, 1.0), mp.inf])
             got = pg.jfun(np.array([t]), nu)[0]
             assert abs(got - float(ref)) <= 1e-12 * abs(float(ref)), (nu, t, got, float(ref))
+
+
+# --------------------------------------------------------------------------
+# Estimated maximum with n_p > 1, the Gaussian cap, bf16 statistics
+# --------------------------------------------------------------------------
+
+def test_est_max_golden_pages():
+    """μ_p, σ_p and M̂_p = μ_p + σ_p·sqrt(2 ln n_p) of hand-built pages (a full
+    page and a partly filled one), through page_metadata, gauss_page_scores
+    and est_max: a missing factor 2 in the log, or the page size in place of
+    the valid count, fails here."""
+    c = json.load(open(os.path.join(GOLD, "est_max_cases.json")))
+    q = np.array(c["q"])
+    for pg_case in c["pages"]:
+        cols = [eval(pg_case["k%d" % i]) for i in range(c["d"])]
+        keys = np.array(cols, dtype=np.float64).T
+        assert keys.shape[0] == pg_case["n"]
+        meta = pg.page_metadata(keys, c["page_size"])
+        assert list(meta["n"]) == [pg_case["n"]]
+        mu, sig = pg.gauss_page_scores(q, meta["mean"], meta["var"])
+        assert abs(mu[0] - eval(pg_case["mu"])) < 1e-14
+        assert abs(sig[0] - eval(pg_case["sigma"])) < 1e-14
+        mh = pg.est_max(mu, sig, meta["n"])
+        assert abs(mh[0] - eval(pg_case["mhat"])) < 1e-13, (mh[0], pg_case["mhat"])
+
+
+def test_gaussian_cap_golden_case():
+    """The Gaussian selector's cap on hand-built point-mass pages: τ̂, the
+    uncapped selection, and which pages survive each cap (ties to the lower
+    page index), with the capacity flag."""
+    from oracle import decode as odec
+    c = json.load(open(os.path.join(GOLD, "gaussian_cap_case.json")))
+    P, other = c["page_size"], c["other_dims"]
+    keys = np.array([[s] + other for s in c["page_scores"] for _ in range(P)])
+    vals = np.arange(keys.shape[0] * 4, dtype=np.float64).reshape(-1, 4)
+    Q = np.array(c["q"])
+    r = odec.decode_group(keys, vals, Q, c["alpha"], "gaussian", P, 0, c["margin"])
+    assert abs(r["tauhat"][0] - eval(c["tauhat"])) < 1e-10
+    assert list(r["page_ids"]) == c["uncapped_page_ids"] and not r["capacity_flag"]
+    for case in c["capped"]:
+        r = odec.decode_group(keys, vals, Q, c["alpha"], "gaussian", P, case["budget_tokens"],
+                              c["margin"])
+        assert list(r["page_ids"]) == case["page_ids"], (case, r["page_ids"])
+        assert r["capacity_flag"] == case["capacity_flag"]
+
+
+def test_bf16_round_hand_cases_and_library_conversion():
+    """Round-to-nearest-even to bfloat16 (8 significant bits): halfway cases
+    go to the even neighbour, and on float32-representable inputs the result
+    equals torch's float32 → bfloat16 conversion (a library routine)."""
+    r = pg.bf16_round
+    assert r(1.0 + 2.0 ** -8) == 1.0                      # tie between 1 and 1 + 2^-7: even is 1
+    assert r(1.0 + 3 * 2.0 ** -8) == 1.0 + 2.0 ** -6      # tie: 1 + 2^-6 has the even last bit
+    assert r(1.0 + 2.0 ** -8 + 2.0 ** -30) == 1.0 + 2.0 ** -7  # just above the tie
+    assert r(-(1.0 + 3 * 2.0 ** -8)) == -(1.0 + 2.0 ** -6)
+    assert r(0.0) == 0.0 and r(2.0 ** -130) == 2.0 ** -130 and r(3.0) == 3.0
+    assert r(255.5) == 256.0 and r(254.5) == 254.0       # spacing 1 in [128, 256): ties to even
+    import torch
+    rng = np.random.default_rng(21)
+    x = np.concatenate([rng.normal(size=20000) * 10.0 ** rng.integers(-6, 6, size=20000),
+                        rng.uniform(-3, 3, size=5000)]).astype(np.float32)
+    want = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(r(x.astype(np.float64)), want)
+
+
+def test_bf16_metadata_rounds_mean_and_m2():
+    rng = np.random.default_rng(22)
+    keys = rng.normal(size=(70, 8)) * 2.0 + 0.3
+    meta = pg.page_metadata(keys, 16)
+    b = pg.bf16_metadata(meta)
+    n = meta["n"][:, None].astype(np.float64)
+    assert np.array_equal(b["mean"], pg.bf16_round(meta["mean"]))
+    assert np.array_equal(b["var"] * n, pg.bf16_round(meta["var"] * n))
+    assert np.array_equal(b["kmin"], meta["kmin"]) and np.array_equal(b["kmax"], meta["kmax"])
+    # within half a bfloat16 spacing (at most 2^-8 of the value) of the exact statistics
+    assert np.all(np.abs(b["mean"] - meta["mean"]) <= 2.0 ** -8 * np.abs(meta["mean"]))

@@ -125,3 +125,27 @@ def test_token_by_token_append_matches_bulk():
     torch.testing.assert_close(a.mean[:n_pages], b.mean[:n_pages], rtol=1e-5, atol=1e-6)
     torch.testing.assert_close(a.m2[:n_pages], b.m2[:n_pages], rtol=1e-4, atol=1e-5)
     check_decode(step, "gaussian", 1.5, 0, 0.5)
+
+
+@pytest.mark.parametrize("meta_bf16", [True, False])
+def test_scorer_wait_timeout_is_flagged_and_the_context_stays_usable(meta_bf16):
+    """The device-side timeout path, made to run without a fault: with
+    ENTMAXKV_FLAG_EXPIRE_WAITS the Gaussian scorer's waits for its staged
+    copies give up at once. The decode must raise ENTMAXKV_DEV_TIMEOUT on the
+    status word, let the copies it issued land, and complete with every page
+    unscored (zero output, nothing selected, NaN τ); the next ordinary decode
+    on the same context must match the oracle again."""
+    spec = synth.custom(8, 2, 128, 32, [5000, 3000], torch.bfloat16, 1.5, n_needles=4,
+                        n_outliers=2)
+    built = Built(spec, meta_bf16=meta_bf16)
+    c = built.cache
+    assert c.read_status(clear=True) == 0
+    o = B.decode(c, built.q, 1.5, "gaussian", 0, 0.5, B.FLAG_EXPIRE_WAITS)
+    st = c.read_status(clear=True)
+    assert st & B.DEV_TIMEOUT, hex(st)
+    assert st & ~(B.DEV_TIMEOUT | B.DEV_CAND_OVERFLOW) == 0, hex(st)
+    assert torch.all(o.out == 0)
+    assert torch.all(o.n_sel == 0)
+    assert torch.all(torch.isnan(o.tau))
+    check_decode(built, "gaussian", 1.5, 0, 0.5)
+    assert c.read_status() == 0

@@ -1,10 +1,19 @@
 """GPU parity: the CUDA path against the float64 oracle on seeded inputs.
 
 Tolerances (stated by the task for this method): selected page ids bit-exact
-(ties to the lower index; flips inside a 1e-5-relative decision margin are
-reported as near ties and then compared on the GPU's own kept set), relative
-L2 output error ≤ 2e-3 for bf16 KV and ≤ 1e-5 for fp32 KV, |τ − τ_oracle| ≤ 1e-4
-(also used for τ̂).
+with ties to the lower index, relative L2 output error ≤ 2e-3 for bf16 KV and
+≤ 1e-5 for fp32 KV, |τ − τ_oracle| ≤ 1e-4 (also used for τ̂).
+
+Page ids: every page the GPU and the oracle decide differently must sit
+within ε_sel = 1e-5·max(1, |threshold|) of the oracle's float64 decision
+boundary (the k-th key for top-k, the threshold τ̂/(α−1) − Δ for the
+Gaussian selector), or, for caches that stream bf16 copies of the page
+statistics, within the band where the GPU's float32 statistics and the
+oracle's exact ones may round to different bfloat16 neighbours. Any other
+difference fails. Every accepted flip is recorded with its margin, and the
+session summary prints the flip count and the smallest decision margin seen
+(tests/conftest.py). With a flip the output and τ are compared on the GPU's
+own kept set.
 """
 
 import math
@@ -18,17 +27,13 @@ from oracle import pages as opg
 from sparse_entmax_attention_gb300 import binding as B
 from sparse_entmax_attention_gb300 import synth
 
-from harness import Built, near_tie_gauss, near_tie_topk, rel_l2
+from harness import Built, bf16_stat_band, record_flip, record_unit, rel_l2, PARITY
 
 pytestmark = pytest.mark.gpu
 
 TOL_OUT = {torch.bfloat16: 2e-3, torch.float32: 1e-5}
 TOL_TAU = 1e-4
-
-
-def _ws_view(built, n_seqs, policy, budget, ws):
-    v = B.workspace_layout(built.cache, n_seqs, policy, budget)
-    return v
+EPS_SEL = 1e-5
 
 
 def _ws_array(ws, off, dtype, shape):
@@ -36,16 +41,38 @@ def _ws_array(ws, off, dtype, shape):
     return ws[off:off + n].view(dtype).view(*shape).cpu()
 
 
+def _decision(r, policy, P, budget):
+    """Per page, the oracle's float64 decision margin (positive: selected)
+    and ε_sel of the boundary it is measured against."""
+    if policy in ("topk", "softmax_topk"):
+        u = np.asarray(r["uhat"], np.float64)
+        k = budget // P
+        if k >= u.size:
+            return np.full(u.size, np.inf), EPS_SEL
+        kth = np.sort(u)[::-1][k - 1]
+        return u - kth, EPS_SEL * max(1.0, abs(kth))
+    margin = (r["mhat"] - r["thr"][:, None]).max(axis=0)
+    eps = EPS_SEL * max(1.0, float(np.abs(r["thr"]).max()))
+    if r["capacity_flag"]:
+        key = np.where(margin >= 0.0, margin, -np.inf)
+        kth = np.sort(key)[::-1][budget // P - 1]
+        margin = np.where(np.abs(key - kth) < np.abs(margin), key - kth, margin)
+        eps = max(eps, EPS_SEL * max(1.0, abs(kth)))
+    return margin, eps
+
+
 def check_decode(built, policy, alpha=1.5, budget=0, margin=0.0, flags=0, q=None,
-                 units=None, check_intermediates=True):
-    spec, cache = built.spec, built.cache
+                 units=None, check_intermediates=True, cache=None):
+    spec = built.spec
+    cache = built.cache if cache is None else cache
+    meta_bf16 = policy == "gaussian" and cache.mean_bf16 is not None
     q = built.q if q is None else q
     S = q.shape[0]
     ws = B.alloc_workspace(cache, S, policy, budget)
     o = B.decode(cache, q, alpha, policy, budget, margin, flags, workspace=ws)
     torch.cuda.synchronize()
     assert cache.device_status() & ~B.DEV_CAND_OVERFLOW == 0, hex(cache.device_status())
-    view = _ws_view(built, S, policy, budget, ws)
+    view = B.workspace_layout(cache, S, policy, budget)
     g, P, d = spec.group, spec.page_size, spec.head_dim
     maxp = cache.cfg.max_pages_per_seq
     out, tau, delta = o.out.cpu().numpy(), o.tau.cpu().numpy(), o.delta.cpu().numpy()
@@ -53,24 +80,43 @@ def check_decode(built, policy, alpha=1.5, budget=0, margin=0.0, flags=0, q=None
     tol = TOL_OUT[spec.kv_dtype]
     if units is None:
         units = [(b, j) for b in range(S) for j in range(spec.num_kv_heads)]
+    PARITY["checks"] += 1
     near = 0
     for b, j in units:
+        tag = f"{policy} a={alpha} D={margin} b={budget} unit=({b},{j}) {spec.name}"
         K, V = built.host_kv(b, j)
         Q = built.host_q(b, j, q)
-        r = odec.decode_group(K, V, Q, alpha, policy, P, budget, margin, meta=built.host_meta(b, j))
+        meta = built.host_meta(b, j, bf16=meta_bf16) if K.shape[0] else None
+        r = odec.decode_group(K, V, Q, alpha, policy, P, budget, margin, meta=meta)
         hs = slice(j * g, (j + 1) * g)
         got_ids = pids[b, j, : n_sel[b, j]]
         want = r["page_ids"]
         if policy in ("full", "softmax"):
             assert n_sel[b, j] == len(want)
+        dmu = dsig = None
+        if meta_bf16 and K.shape[0]:
+            dmu, dsig = bf16_stat_band(K, P, Q)
+        dec = None
+        if policy in ("topk", "softmax_topk", "gaussian") and K.shape[0]:
+            dec, eps = _decision(r, policy, P, budget)
+            record_unit(tag, dec.size, dec, eps)
+        else:
+            record_unit(tag, len(want), None, 0.0)
         if list(got_ids) != list(want):
-            diff = set(got_ids.tolist()) ^ set(want.tolist())
-            if policy in ("topk", "softmax_topk"):
-                allowed = near_tie_topk(r["uhat"], budget // P)
-            else:
-                eps = TOL_TAU / (alpha - 1.0) + 1e-5 * max(1.0, float(np.abs(r["thr"]).max()))
-                allowed = near_tie_gauss(r["mhat"], r["thr"], eps)
-            assert diff <= allowed, (b, j, sorted(diff - allowed)[:10])
+            diff = sorted(set(got_ids.tolist()) ^ set(want.tolist()))
+            band = np.zeros(dec.size)
+            if dmu is not None:
+                band = (dmu + dsig * np.sqrt(2.0 * np.log(r["meta"]["n"].astype(np.float64)))).max(axis=0)
+            bad = []
+            for p in diff:
+                m = float(dec[p])
+                if abs(m) <= eps:
+                    record_flip(tag, p, m, eps, float(band[p]), "inside ε_sel")
+                elif abs(m) <= eps + band[p]:
+                    record_flip(tag, p, m, eps, float(band[p]), "bf16 rounding boundary")
+                else:
+                    bad.append((p, m))
+            assert not bad, (tag, "pages decided differently outside ε_sel", bad[:10], eps)
             near += len(diff)
             ref_out, ref_tau = odec.attend_pages(K, V, Q, alpha, P, got_ids, softmax=policy == "softmax_topk")
         else:
@@ -95,8 +141,11 @@ def check_decode(built, policy, alpha=1.5, budget=0, margin=0.0, flags=0, q=None
             ms = _ws_array(ws, view.gauss_ms, torch.float32, (S, spec.num_q_heads, maxp, 2)).numpy()
             n_pages = r["mu"].shape[1]
             a1 = alpha - 1.0
-            np.testing.assert_allclose(ms[b, hs, :n_pages, 0], a1 * r["mu"], atol=2e-5, rtol=1e-5)
-            np.testing.assert_allclose(ms[b, hs, :n_pages, 1], a1 * r["sigma"], atol=2e-5, rtol=1e-4)
+            bm = 0.0 if dmu is None else a1 * dmu
+            bs = 0.0 if dsig is None else a1 * dsig
+            got_m, got_s = ms[b, hs, :n_pages, 0], ms[b, hs, :n_pages, 1]
+            assert np.all(np.abs(got_m - a1 * r["mu"]) <= 2e-5 + 1e-5 * np.abs(a1 * r["mu"]) + bm)
+            assert np.all(np.abs(got_s - a1 * r["sigma"]) <= 2e-5 + 1e-4 * np.abs(a1 * r["sigma"]) + bs)
             th = _ws_array(ws, view.tauhat, torch.float32, (S, spec.num_q_heads)).numpy()
             assert np.all(np.abs(th[b, hs] - r["tauhat"]) <= TOL_TAU), (th[b, hs], r["tauhat"])
     return o, near

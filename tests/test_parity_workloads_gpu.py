@@ -55,14 +55,25 @@ def test_gqa128k_rotated_steps(gqa128k, alpha, margin):
 
 @pytest.fixture(scope="module")
 def gqa1m():
-    return Built(synth.workload("gqa32x8-d128-1m-p32-bf16"))
+    # the benchmark's cache: fp32 statistics plus the bf16 copies the
+    # Gaussian scorer streams
+    return Built(synth.workload("gqa32x8-d128-1m-p32-bf16"), meta_bf16=True)
 
 
 @pytest.mark.parametrize("policy,budget,margin", [
     ("gaussian", 0, 0.5), ("topk", 2048, 0.0), ("full", 0, 0.0), ("softmax", 0, 0.0),
     ("softmax_topk", 2048, 0.0)])
 def test_gqa1m_sampled_heads(gqa1m, policy, budget, margin):
-    check_decode(gqa1m, policy, 1.5, budget, margin, units=[(0, 0), (0, 7)])
+    """The 1M-token cache in the launch configuration the benchmark times; the
+    Gaussian selector here streams the bf16 copies (tensor-core scorer)."""
+    check_decode(gqa1m, policy, 1.5, budget, margin, units=[(0, 0), (0, 3), (0, 7)])
+
+
+def test_gqa1m_gaussian_fp32_metadata(gqa1m):
+    """The same Gaussian decode from the fp32 statistics (the scorer for caches
+    without bf16 copies)."""
+    check_decode(gqa1m, "gaussian", 1.5, 0, 0.5, units=[(0, 0), (0, 7)],
+                 cache=gqa1m.cache.fp32_metadata())
 
 
 def test_batched_shuffled_with_appends():
@@ -98,8 +109,9 @@ def test_gqa1m_bulk_prefill_metadata(gqa1m):
     """The 1M-token prefill is one bulk append that writes the tokens and
     builds every page's metadata in the same kernel. On sampled pages of two
     KV heads (plus the last page) the stored tokens equal the input, the
-    bounding box equals the oracle's exactly, and the mean and variance match
-    the oracle's float64 statistics of the same keys."""
+    bounding box equals the oracle's exactly, the mean and variance match
+    the oracle's float64 statistics of the same keys, and the bf16 copies are
+    the rounded fp32 statistics."""
     from oracle import pages as opg
     spec, c = gqa1m.spec, gqa1m.cache
     P = spec.page_size
@@ -120,3 +132,5 @@ def test_gqa1m_bulk_prefill_metadata(gqa1m):
             np.testing.assert_allclose(c.mean[ph, j].double().cpu().numpy(), meta["mean"][0], atol=2e-6, rtol=1e-5)
             np.testing.assert_allclose(c.m2[ph, j].double().cpu().numpy() / rows.shape[0], meta["var"][0],
                                        atol=1e-5, rtol=1e-4)
+            assert torch.equal(c.mean_bf16[ph, j], c.mean[ph, j].to(torch.bfloat16))
+            assert torch.equal(c.m2_bf16[ph, j], c.m2[ph, j].to(torch.bfloat16))
