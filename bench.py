@@ -56,6 +56,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="headline step only")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the timed rows of the other synthetic workloads")
     ap.add_argument("--policies", default="gaussian,gaussian_meta_f32,gaussian_alpha1.25,topk,softmax_topk,full_dense,full_skipv,softmax",
                     help="rows of the per-policy table")
     return ap.parse_args()
@@ -291,6 +293,9 @@ def run_ours(args, rank, world):
         res["prefill"] = prefill(wl, B, K, W, peaks)
         if not args.no_e2e:
             res["e2e"] = e2e(wl, B, toks, qs, n_app, K, W)
+    del ws_g, out_g, graph
+    if not args.no_workloads:
+        res["workloads"] = workload_rows(B, flush, min(K, 20), peaks, dev)
     if not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(wl, qbuf)
     return res
@@ -469,6 +474,270 @@ def e2e(wl, B, toks, qs, n_app, K, W):
 
 
 # --------------------------------------------------------------------------
+# the other synthetic workloads: timed rows and quality reports
+
+def graph_of(fn):
+    import torch
+    fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    return g
+
+
+def time_replays(g, n, flush, before=None):
+    """µs of n replays of graph g, each after `before(i)` (untimed input
+    copies) and a 512 MiB L2-flushing read; CUDA events on the current stream."""
+    import torch
+    us = []
+    for i in range(n):
+        if before is not None:
+            before(i)
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        us.append(a.elapsed_time(b) * 1e3)
+    return us
+
+
+class FullRef:
+    """The full-cache α-entmax decode of the same queries (the library's own
+    policy-full path): output, τ and every token's z, for the quality report."""
+
+    def __init__(self, B, cache, q, alpha):
+        import torch
+        S = q.shape[0]
+        self.ws = B.alloc_workspace(cache, S, "full")
+        self.o = B.decode(cache, q, alpha, "full", workspace=self.ws)
+        view = B.workspace_layout(cache, S, "full")
+        cfg = cache.cfg
+        shape = (S, cfg.num_kv_heads, view.cap_pages, cfg.page_size, cfg.group)
+        n = 4 * math.prod(shape)
+        torch.cuda.synchronize()
+        self.z = self.ws[view.z_scores: view.z_scores + n].view(torch.float32).view(*shape)
+
+
+def quality(B, cache, q, alpha, policy, budget, margin, o, ref):
+    """δ (exact dropped mass, the library's EXACT_DELTA decode), support recall
+    (the full-cache support's tokens inside the kept pages) and the relative
+    L2 error of the output against the full-cache output, per query head;
+    returned as means and extremes."""
+    import torch
+    S, Hq = q.shape[0], cache.num_q_heads
+    Hkv, G = cache.cfg.num_kv_heads, cache.cfg.group
+    ex = B.decode(cache, q, alpha, policy, budget, margin, B.FLAG_EXACT_DELTA)
+    torch.cuda.synchronize()
+    maxp = ref.z.shape[2]
+    kept = torch.zeros(S, Hkv, maxp, dtype=torch.bool, device=q.device)
+    n_sel = o.n_sel.long()
+    for b in range(S):
+        for j in range(Hkv):
+            ids = o.page_ids[b, j, : int(n_sel[b, j])].long()
+            kept[b, j, ids] = True
+    tau_full = ref.o.tau.view(S, Hkv, 1, 1, G)
+    supp = ref.z > tau_full                                    # [S, Hkv, maxp, P, G]
+    n_supp = supp.sum(dim=(2, 3)).double()                      # [S, Hkv, G]
+    n_hit = (supp & kept[:, :, :, None, None]).sum(dim=(2, 3)).double()
+    recall = (n_hit / n_supp.clamp_min(1)).view(S, Hq)
+    err = ((o.out - ref.o.out).norm(dim=-1) / ref.o.out.norm(dim=-1).clamp_min(1e-30)).view(S, Hq)
+    d = ex.delta.float()
+    return {"delta_exact_mean": round(float(d.mean()), 5), "delta_exact_max": round(float(d.max()), 5),
+            "recall_mean": round(float(recall.mean()), 5), "recall_min": round(float(recall.min()), 5),
+            "rel_err_mean": round(float(err.mean()), 6), "rel_err_max": round(float(err.max()), 6),
+            "pages_per_kv_head": round(float(o.n_sel.float().mean()), 1)}
+
+
+def timed_row(B, wl, q, alpha, policy, budget, margin, flags, flush, n, peaks, ref=None):
+    """One policy on one workload: µs per decode (graph replay, L2 flushed),
+    algorithmic bytes and GB/s, and the quality report against `ref`."""
+    import torch
+    cache, spec = wl.cache, wl.spec
+    S = q.shape[0]
+    ws = B.alloc_workspace(cache, S, policy, budget)
+    o = B.alloc_outputs(cache, S, policy, budget)
+    g = graph_of(lambda: B.decode(cache, q, alpha, policy, budget, margin, flags, workspace=ws, outputs=o))
+    us = statistics.mean(time_replays(g, n, flush))
+    view = B.workspace_layout(cache, S, policy, budget)
+    name = "full_dense" if (policy == "full" and flags & B.FLAG_DENSE_V) else \
+        ("full_skipv" if policy == "full" else policy)
+    nbytes, counts = algorithmic_bytes(wl, name, o, ws, view)
+    gbs = nbytes / (us * 1e-6) / 1e9
+    row = {"us": round(us, 2), "bytes": nbytes, "gbs": round(gbs, 1),
+           "frac_8tbs": round(gbs / NOMINAL_HBM_GBS, 4), "frac_measured_hbm": round(gbs / peaks["hbm_gbs"], 4),
+           **counts}
+    if ref is not None and policy not in ("full", "softmax"):
+        row.update(quality(B, cache, q, alpha, policy, budget, margin, o, ref))
+    del g
+    return row
+
+
+def workload_rows(B, flush, n, peaks, dev):
+    """The four other synthetic workloads, each timed per decode step (CUDA
+    graph replays, L2 flushed before each) with δ, support recall and
+    relative output error of every selective policy against the full-cache
+    α-entmax decode of the same query."""
+    import torch
+    from sparse_entmax_attention_gb300 import runner, synth
+    rows = {}
+    # 4k tokens, one head, d = 64, fp32: full vs top-k 32 pages (launch-bound sizes)
+    spec = synth.workload("single-head-d64-4k-p16-fp32")
+    wl = runner.Workload(spec, device=dev)
+    ref = FullRef(B, wl.cache, wl.q, 1.5)
+    rows[spec.name] = {
+        "full_dense": timed_row(B, wl, wl.q, 1.5, "full", 0, 0.0, B.FLAG_DENSE_V, flush, n, peaks),
+        "topk_512": timed_row(B, wl, wl.q, 1.5, "topk", 512, 0.0, 0, flush, n, peaks, ref),
+        "note": "8 MB of K/V: launch-bound, the roofline fraction is not meaningful"}
+    del wl, ref
+    # 32k tokens, GQA 32/8, bf16: top-k 1024 tokens vs full
+    spec = synth.workload("gqa32x8-d128-32k-p16-bf16")
+    wl = runner.Workload(spec, device=dev)
+    ref = FullRef(B, wl.cache, wl.q, 1.5)
+    rows[spec.name] = {
+        "full_dense": timed_row(B, wl, wl.q, 1.5, "full", 0, 0.0, B.FLAG_DENSE_V, flush, n, peaks),
+        "softmax": timed_row(B, wl, wl.q, 1.5, "softmax", 0, 0.0, 0, flush, n, peaks),
+        "topk_1024": timed_row(B, wl, wl.q, 1.5, "topk", 1024, 0.0, 0, flush, n, peaks, ref),
+        "softmax_topk_1024": timed_row(B, wl, wl.q, 1.5, "softmax_topk", 1024, 0.0, 0, flush, n, peaks)}
+    del wl, ref
+    rows["gqa32x8-d128-128k-p32-bf16"] = rotated_steps(B, flush, peaks, dev)
+    rows["batch16-loguniform-4k-256k-p16-bf16"] = batched_serving(B, flush, peaks, dev)
+    torch.cuda.empty_cache()
+    return rows
+
+
+def rotated_steps(B, flush, peaks, dev):
+    """128k tokens, page 32: 64 decode steps, each with fresh queries rotated
+    30% toward a needle key. Gaussian selector at α ∈ {1.5, 2}, Δ ∈ {0, 0.5, 1},
+    against top-k with its k matched to the Gaussian n_sel of the same step
+    (mean over KV heads). µs per step from one graph replay per step."""
+    import torch
+    from sparse_entmax_attention_gb300 import runner, synth
+    spec = synth.workload("gqa32x8-d128-128k-p32-bf16")
+    wl = runner.Workload(spec, device=dev, meta_bf16=True)
+    cache, P = wl.cache, spec.page_size
+    qs = [wl.step_queries(i) for i in range(spec.steps)]
+    qbuf = qs[0].clone()
+    out = {"steps": spec.steps}
+    for alpha in spec.extra["alphas"]:
+        refs = []
+        for i in range(spec.steps):
+            qbuf.copy_(qs[i])
+            r = FullRef(B, cache, qbuf, alpha)
+            refs.append((r.o, r.z.clone()))  # per step: full output, τ and z
+            del r
+        for margin in spec.extra["margins"]:
+            ws = B.alloc_workspace(cache, 1, "gaussian")
+            o = B.alloc_outputs(cache, 1, "gaussian")
+            g = graph_of(lambda: B.decode(cache, qbuf, alpha, "gaussian", 0, margin, workspace=ws, outputs=o))
+            us_g, us_t, qual_g, qual_t, ksel, bytes_g = [], [], [], [], [], []
+            graphs_t = {}
+            for i in range(spec.steps):
+                us_g += time_replays(g, 1, flush, lambda _i: qbuf.copy_(qs[i]))
+                view = B.workspace_layout(cache, 1, "gaussian")
+                bytes_g.append(algorithmic_bytes(wl, "gaussian", o, ws, view)[0])
+                ref = _Ref(*refs[i])
+                qual_g.append(quality(B, cache, qbuf, alpha, "gaussian", 0, margin, o, ref))
+                k = max(1, int(round(float(o.n_sel.float().mean()))))
+                ksel.append(k)
+                if k not in graphs_t:
+                    wt = B.alloc_workspace(cache, 1, "topk", k * P)
+                    ot = B.alloc_outputs(cache, 1, "topk", k * P)
+                    gt = graph_of(lambda: B.decode(cache, qbuf, alpha, "topk", k * P, 0.0, workspace=wt,
+                                                   outputs=ot))
+                    graphs_t[k] = (gt, wt, ot)
+                gt, wt, ot = graphs_t[k]
+                us_t += time_replays(gt, 1, flush)
+                qual_t.append(quality(B, cache, qbuf, alpha, "topk", k * P, 0.0, ot, ref))
+            mg, mt = statistics.mean(us_g), statistics.mean(us_t)
+            gbs = statistics.mean(bytes_g) / (mg * 1e-6) / 1e9
+            out[f"alpha{alpha}_margin{margin}"] = {
+                "gaussian": {"us": round(mg, 2), "gbs": round(gbs, 1),
+                             "frac_8tbs": round(gbs / NOMINAL_HBM_GBS, 4), **_mean_quality(qual_g)},
+                "topk_matched": {"us": round(mt, 2), "pages_per_kv_head": round(statistics.mean(ksel), 1),
+                                 **{k: v for k, v in _mean_quality(qual_t).items() if k != "pages_per_kv_head"}}}
+            del g, graphs_t
+    del wl
+    return out
+
+
+class _Ref:
+    def __init__(self, o, z):
+        self.o, self.z = o, z
+
+
+def _mean_quality(rows):
+    keys = rows[0].keys()
+    agg = {}
+    for k in keys:
+        vals = [r[k] for r in rows]
+        agg[k] = round(max(vals) if k.endswith("_max") else min(vals) if k.endswith("_min")
+                       else statistics.mean(vals), 6)
+    return agg
+
+
+def batched_serving(B, flush, peaks, dev):
+    """16 sequences (lengths log-uniform in [4096, 262144], shuffled block
+    table, page 16): 128 steps, each appending one token to every sequence
+    (page metadata updated in place) and decoding all 16 with the Gaussian
+    selector (Δ = 0.5). µs per step from one graph replay per step; quality
+    on every 32nd step."""
+    import torch
+    from sparse_entmax_attention_gb300 import runner, synth
+    spec = synth.workload("batch16-loguniform-4k-256k-p16-bf16")
+    wl = runner.Workload(spec, device=dev, meta_bf16=True)
+    cache = wl.cache
+    toks = [wl.step_tokens(i) for i in range(spec.steps)]
+    qs = [wl.step_queries(i) for i in range(spec.steps)]
+    kb, vb, qb = toks[0][0].clone(), toks[0][1].clone(), qs[0].clone()
+    ws = B.alloc_workspace(cache, spec.batch, "gaussian")
+    o = B.alloc_outputs(cache, spec.batch, "gaussian")
+
+    def step():
+        B.append(cache, kb, vb)
+        B.decode(cache, qb, 1.5, "gaussian", 0, 0.5, workspace=ws, outputs=o)
+
+    # kernels loaded by an eager decode (no state change), then the step is
+    # captured without executing it: the first replay is step 0
+    B.decode(cache, qb, 1.5, "gaussian", 0, 0.5, workspace=ws, outputs=o)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        step()
+    torch.cuda.synchronize()
+
+    def before(i):
+        kb.copy_(toks[i][0])
+        vb.copy_(toks[i][1])
+        qb.copy_(qs[i])
+
+    us, qual, nbytes = [], [], []
+    view = B.workspace_layout(cache, spec.batch, "gaussian")
+    for i in range(spec.steps):
+        us += time_replays(g, 1, flush, lambda _i: before(i))
+        nbytes.append(algorithmic_bytes(wl, "gaussian", o, ws, view)[0])
+        if i % 32 == 31:
+            ref = FullRef(B, cache, qb, 1.5)
+            qual.append(quality(B, cache, qb, 1.5, "gaussian", 0, 0.5, o, ref))
+            del ref
+    assert cache.device_status() & ~B.DEV_CAND_OVERFLOW == 0, hex(cache.device_status())
+    append_bytes = spec.batch * spec.num_kv_heads * spec.head_dim * (2 * 2 + 2 * 2 + 2 * 4 * 2)
+    m = statistics.mean(us)
+    gbs = (statistics.mean(nbytes) + append_bytes) / (m * 1e-6) / 1e9
+    del g, wl
+    return {"steps": spec.steps, "us_per_step": round(m, 2), "us_first": round(us[0], 2),
+            "us_last": round(us[-1], 2), "tokens_per_s": round(spec.batch / (m * 1e-6), 1),
+            "gbs": round(gbs, 1), "frac_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
+            "frac_measured_hbm": round(gbs / peaks["hbm_gbs"], 4),
+            "context_tokens": sum(spec.context_lens), "quality_every_32_steps": _mean_quality(qual),
+            "step": "append 1 token to each of 16 sequences + Gaussian decode of all 16 (CUDA graph)"}
+
+
+# --------------------------------------------------------------------------
 # oracle (CPU) legs
 
 def host_sample(wl, qdev, kvh=0):
@@ -486,65 +755,120 @@ def host_sample(wl, qdev, kvh=0):
     return K, V, Q
 
 
-def oracle_step_us(K, V, Q, P, n_kv_heads, meta):
+def oracle_decode_step(heads, P):
+    """One whole Gaussian decode step by the oracle: every KV head with its
+    query heads; (K, V, Q, page metadata) per KV head."""
     from oracle import decode as odec
-    t0 = time.perf_counter()
-    odec.decode_group(K, V, Q, ALPHA, "gaussian", P, 0, MARGIN, meta=meta, diagnostics=False)
-    dt = time.perf_counter() - t0
-    return dt * n_kv_heads * 1e6, dt
+    for K, V, Q, meta in heads:
+        odec.decode_group(K, V, Q, ALPHA, "gaussian", P, 0, MARGIN, meta=meta, diagnostics=False)
+
+
+def oracle_heads_from_cache(wl, qdev):
+    """The stored K/V bits of every KV head of the cache (as float32, exact for
+    bf16) with the oracle's reading of the page statistics the GPU path
+    streams (exact statistics rounded to bf16: the cache keeps bf16 copies)."""
+    from oracle import pages as opg
+    spec = wl.spec
+    heads = []
+    for kvh in range(spec.num_kv_heads):
+        K, V, Q = host_sample(wl, qdev, kvh)
+        K, V = K.astype("float32"), V.astype("float32")
+        meta = opg.page_metadata(K, spec.page_size)
+        heads.append((K, V, Q, opg.bf16_metadata(meta) if wl.cache.mean_bf16 is not None else meta))
+    return heads
 
 
 def cpu_baseline(wl, qdev, min_s=10.0, max_reps=3):
-    """One whole Gaussian decode step (every KV head and its query heads) by
-    the oracle, repeated until at least `min_s` seconds of oracle time."""
-    from oracle import pages as opg
+    """Whole Gaussian decode steps (every KV head and its query heads) by the
+    oracle on the cache's stored bits, repeated until at least `min_s` seconds
+    of oracle time."""
     spec = wl.spec
+    heads = oracle_heads_from_cache(wl, qdev)   # the cache keeps the metadata: not per step
     per_step, total, reps = [], 0.0, 0
     while reps < max_reps and (reps == 0 or total < min_s):
-        t_step = 0.0
-        for kvh in range(spec.num_kv_heads):
-            K, V, Q = host_sample(wl, qdev, kvh)
-            meta = opg.page_metadata(K, spec.page_size)   # kept by the cache, not per step
-            t_step += oracle_step_us(K, V, Q, spec.page_size, 1, meta)[1]
-            del K, V, meta
-        per_step.append(t_step)
-        total += t_step
+        t0 = time.perf_counter()
+        oracle_decode_step(heads, spec.page_size)
+        dt = time.perf_counter() - t0
+        per_step.append(dt)
+        total += dt
         reps += 1
     us = statistics.mean(per_step) * 1e6
     return {"value": round(us, 1), "unit": "us/step", "cores": os.cpu_count(), "kind": "oracle",
             "sample": f"{reps} x one whole Gaussian decode step at 1M tokens ({spec.num_kv_heads} KV "
-                      f"heads x {spec.group} query heads), float64 numpy, {total:.1f} s of oracle "
-                      f"time; page metadata prebuilt (the cache keeps it); BLAS default threads"}
+                      f"heads x {spec.group} query heads) on the cache's stored bits, float64 numpy, "
+                      f"{total:.1f} s of oracle time; page metadata prebuilt (the cache keeps it); "
+                      f"BLAS default threads"}
 
 
-def run_reference(args, rank, world):
-    """The oracle as the reference arm: each step is the float64 Gaussian
-    decode of one KV head of the 1M workload, scaled to all KV heads."""
-    if rank != 0:
-        return None
+def reference_inputs(K, W):
+    """The bench's 1M-token workload with the same spec the GPU arm uses (its
+    appended steps change how much each generator draws), drawn by the same
+    seeded generator on the GPU when one is present (torch's Philox: the GPU
+    arm's exact bits) and copied to the host; per KV head (K, V, Q, metadata)."""
     import torch
     from oracle import pages as opg
     from sparse_entmax_attention_gb300 import synth
     spec = synth.workload(WORKLOAD)
-    q = synth.queries(spec, 0, 0, "cpu").unsqueeze(0)
-    hd = synth.HeadDraws(spec, 0, 0, q[0, :spec.group], 0, "cpu")
-    K, V = hd.k.double().numpy(), hd.v.double().numpy()
-    Q = q[0, :spec.group].double().numpy()
-    meta = opg.page_metadata(K, spec.page_size)
+    n_append = 2 * (K + W) + 4
+    spec = synth.Spec(**{**spec.__dict__, "steps": n_append, "append_per_step": True})
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    q = synth.queries(spec, 0, 0, dev)
+    g = spec.group
+    heads = []
+    for j in range(spec.num_kv_heads):
+        hd = synth.HeadDraws(spec, 0, j, q[j * g:(j + 1) * g], 0, dev)
+        Kh = hd.k.float().cpu().numpy()
+        Vh = hd.v.float().cpu().numpy()
+        Q = q[j * g:(j + 1) * g].double().cpu().numpy()
+        del hd
+        heads.append((Kh, Vh, Q, opg.bf16_metadata(opg.page_metadata(Kh, spec.page_size))))
+    return spec, heads, dev
+
+
+def one_thread_step_s(K, W):
+    """One whole oracle step with BLAS and OpenMP held to one thread (a child
+    process, since thread pools are fixed when numpy loads)."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    code = ("import bench, time; spec, heads, _ = bench.reference_inputs(%d, %d); t = time.perf_counter(); "
+            "bench.oracle_decode_step(heads, spec.page_size); print(time.perf_counter() - t)" % (K, W))
+    try:
+        r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True, text=True,
+                           timeout=900)
+        return float(r.stdout.strip().splitlines()[-1])
+    except (subprocess.SubprocessError, ValueError, IndexError):
+        return None
+
+
+def run_reference(args, rank, world):
+    """The oracle as the reference arm: each step is one whole float64
+    Gaussian decode step of the 1M workload (all 8 KV heads and their query
+    heads) on the GPU arm's stored bits, timed on the host cores."""
+    if rank != 0:
+        return None
+    spec, heads, dev = reference_inputs(args.steps, args.warmup)
     for _ in range(args.warmup):
-        oracle_step_us(K, V, Q, spec.page_size, spec.num_kv_heads, meta)
+        oracle_decode_step(heads, spec.page_size)
     t0 = time.perf_counter()
-    us = [oracle_step_us(K, V, Q, spec.page_size, spec.num_kv_heads, meta)[0] for _ in range(args.steps)]
+    us = []
+    for _ in range(args.steps):
+        t = time.perf_counter()
+        oracle_decode_step(heads, spec.page_size)
+        us.append((time.perf_counter() - t) * 1e6)
     wall = time.perf_counter() - t0
     v = statistics.mean(us)
+    del heads
+    one = one_thread_step_s(args.steps, args.warmup)
     return {"impl": "reference", "metric": METRIC, "value": round(v, 1), "unit": "us/step",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(v / 1e3, 3), "higher_is_better": False, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f64", "data": "synthetic (same seeded generator, CPU draws)",
+            "vs_baseline": None, "dtype": "f64",
+            "data": f"synthetic: the GPU arm's seeded generator, drawn on {dev} and copied to the host",
             "config": {"workload": WORKLOAD, "policy": "gaussian", "margin": MARGIN, "alpha": ALPHA},
             "cpu_baseline": {"value": round(v, 1), "unit": "us/step", "cores": os.cpu_count(),
                              "kind": "oracle",
-                             "sample": f"1 of {spec.num_kv_heads} KV heads per step, scaled"},
+                             "sample": f"{args.steps} whole decode steps ({spec.num_kv_heads} KV heads x "
+                                       f"{spec.group} query heads, 1M tokens each), BLAS default threads",
+                             "one_thread_us_per_step": None if one is None else round(one * 1e6, 1)},
             "e2e": {"value": round(v, 1), "unit": "us/step", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0},
             "wall_s_timed_loop": round(wall, 3)}

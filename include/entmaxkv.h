@@ -38,7 +38,7 @@
 extern "C" {
 #endif
 
-#define ENTMAXKV_VERSION 3
+#define ENTMAXKV_VERSION 4
 
 /* Return codes of every call. */
 typedef enum {
@@ -212,8 +212,9 @@ int32_t entmaxkv_read_status(const entmaxkv_cache* cache, uint32_t* status_out, 
  * normalisation equation at entmax order α). α ∈ {1.5, 2} use closed forms;
  * any other α > 1 uses fits of the partial moments E[(t + Z)_+^ν] that this
  * call (or the first decode with that α) builds on the host, about 0.1-0.4 s,
- * and caches; they must pass a 1e-6 relative check. Returns 1 or 0. Host
- * only: no CUDA call.
+ * and caches (the 8 most recently used orders; a caller cycling through more
+ * rebuilds on each miss); they must pass a 1e-6 relative check. Returns 1 or
+ * 0. Host only: no CUDA call.
  */
 int32_t entmaxkv_gaussian_alpha_supported(float alpha);
 
@@ -259,7 +260,11 @@ int32_t entmaxkv_moment_fit_eval(float alpha, int32_t order, const float* t, int
  *              over the kept tokens); NaN for an empty kept set
  *   delta      [n_seqs][Hq] float32 dropped mass: FULL/SOFTMAX 0; TOPK the
  *              certified bound min(1, Σ_dropped n_p·[(α−1)U_p − τ]_+^β);
- *              GAUSSIAN the page model's estimate of the dropped mass;
+ *              GAUSSIAN the page model's estimate of the dropped mass: it
+ *              is not certified and can be far below the true dropped mass
+ *              (a single outlier token raises a page's true score spread
+ *              much more than the per-coordinate variances show); use
+ *              ENTMAXKV_FLAG_EXACT_DELTA for the exact value;
  *              SOFTMAX_TOPK the certified bound D/(1 + D) with
  *              D = Σ_dropped n_p·exp(U_p − log Σ_kept exp(s_i));
  *              with ENTMAXKV_FLAG_EXACT_DELTA, for every policy, the exact
@@ -316,8 +321,12 @@ typedef struct {
   size_t page_zmax;    /* float [n_seqs][Hkv][cap_pages][group]: max z of each kept page
                           (index = rank in page_ids), SIZE_MAX for SOFTMAX        */
   int32_t cap_pages;   /* most pages one (sequence, KV head) can keep              */
-  int32_t splits;      /* blocks per (sequence, KV head) in the decode kernels     */
+  int32_t splits;      /* most blocks per (sequence, KV head) of the decode kernels
+                          (a launch uses fewer on a device with fewer SMs)         */
   size_t total;
+  size_t z_scores;     /* float [n_seqs][Hkv][cap_pages][page_size][group]: z = (α−1)·s of
+                          every token of each kept page (index = rank in page_ids), −inf
+                          past a page's valid tokens; SIZE_MAX for SOFTMAX policies  */
 } entmaxkv_workspace_view;
 
 int32_t entmaxkv_workspace_layout(const entmaxkv_config* cfg, int32_t n_seqs,
@@ -342,7 +351,10 @@ int32_t entmaxkv_workspace_layout(const entmaxkv_config* cfg, int32_t n_seqs,
  *     ENTMAXKV_ERR_WORKSPACE_TOO_SMALL before anything is queued.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *     before any stream capture. The address is kept for the process, so
+ *     the library must not be used across a reset of that device
+ *     (cudaDeviceReset, or another library resetting the primary context),
+ *     after which the array may live elsewhere.
  *   - Every call shares the one array: calls that may overlap on the GPU
  *     (different streams, or different host threads) race and must be
  *     serialised by the caller. The counters the decode relies on are cleared

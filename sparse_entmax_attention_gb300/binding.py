@@ -61,7 +61,7 @@ class WorkspaceView(ctypes.Structure):
                 ("sel_bitmap", ctypes.c_size_t), ("tauhat_iters", ctypes.c_size_t),
                 ("page_zmax", ctypes.c_size_t),
                 ("cap_pages", ctypes.c_int32), ("splits", ctypes.c_int32),
-                ("total", ctypes.c_size_t)]
+                ("total", ctypes.c_size_t), ("z_scores", ctypes.c_size_t)]
 
 
 _lib = None

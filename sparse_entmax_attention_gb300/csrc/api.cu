@@ -280,6 +280,7 @@ int32_t entmaxkv_workspace_layout(const entmaxkv_config* cfg, int32_t n_seqs, in
   view->cap_pages = L.cap_pages;
   view->splits = L.splits;
   view->total = L.total;
+  view->z_scores = L.z;
   return ENTMAXKV_OK;
 }
 

@@ -136,25 +136,49 @@ bool build(double beta, MomentFit& F) {
 struct Entry {
   float beta;
   bool ok;
+  unsigned long long used;  // last use (a counter): the least recently used entry is replaced
   MomentFit fit;
 };
+constexpr int kCacheSlots = 8;
 std::mutex g_mu;
-Entry g_cache[8];
+Entry g_cache[kCacheSlots];
 int g_used = 0;
+unsigned long long g_clock = 0;
 
 }  // namespace
 
+// The fits of order β from the cache of the kCacheSlots most recently used
+// orders; a miss builds them (0.1-0.4 s of host quadrature) without holding
+// the lock, so decodes with cached orders on other threads do not wait, then
+// inserts them over the least recently used entry. A caller that cycles
+// through more than kCacheSlots orders rebuilds on every miss.
 int moment_fit_for(float beta, MomentFit* out) {
-  std::lock_guard<std::mutex> lock(g_mu);
-  for (int i = 0; i < g_used; ++i)
-    if (g_cache[i].beta == beta) {
-      if (g_cache[i].ok) *out = g_cache[i].fit;
-      return g_cache[i].ok ? 0 : 1;
-    }
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    for (int i = 0; i < g_used; ++i)
+      if (g_cache[i].beta == beta) {
+        g_cache[i].used = ++g_clock;
+        if (g_cache[i].ok) *out = g_cache[i].fit;
+        return g_cache[i].ok ? 0 : 1;
+      }
+  }
   Entry e;
   e.beta = beta;
   e.ok = beta > 0.0f && std::isfinite(beta) && build((double)beta, e.fit);
-  g_cache[g_used < 8 ? g_used++ : 7] = e;  // a ninth order replaces the last slot
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    int slot = -1;
+    for (int i = 0; i < g_used; ++i)
+      if (g_cache[i].beta == beta) slot = i;  // built meanwhile by another thread
+    if (slot < 0 && g_used < kCacheSlots) slot = g_used++;
+    if (slot < 0) {
+      slot = 0;
+      for (int i = 1; i < kCacheSlots; ++i)
+        if (g_cache[i].used < g_cache[slot].used) slot = i;
+    }
+    e.used = ++g_clock;
+    g_cache[slot] = e;
+  }
   if (e.ok) *out = e.fit;
   return e.ok ? 0 : 1;
 }

@@ -36,7 +36,7 @@ def test_exports_every_declared_function(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert lib.entmaxkv_version() == 3
+    assert lib.entmaxkv_version() == 4
     for code in range(5):
         assert lib.entmaxkv_status_string(code)
     assert lib.entmaxkv_status_string(99) == b"unknown status"
@@ -77,6 +77,9 @@ def test_workspace_sizing(lib):
     assert lib.entmaxkv_workspace_layout(ctypes.byref(cfg), 1, B.POLICY_GAUSSIAN, 0, ctypes.byref(v)) == 0
     assert v.gauss_ms % 256 == 0 and v.tauhat % 256 == 0 and v.bbox_u == 2 ** 64 - 1
     assert v.total == lib.entmaxkv_workspace_bytes(ctypes.byref(cfg), 1, B.POLICY_GAUSSIAN, 0)
+    assert v.z_scores % 256 == 0 and v.z_scores < v.total
+    assert lib.entmaxkv_workspace_layout(ctypes.byref(cfg), 1, B.POLICY_SOFTMAX, 0, ctypes.byref(v)) == 0
+    assert v.z_scores == 2 ** 64 - 1 and v.page_zmax == 2 ** 64 - 1
 
 
 @pytest.mark.parametrize("field,value,code", [
@@ -200,3 +203,17 @@ def test_moment_fits_match_the_oracle(lib, alpha):
         B.moment_fit_eval(1.5, 0, t)   # closed forms: no fits
     with pytest.raises(B.EntmaxKVError):
         B.moment_fit_eval(alpha, 3, t)
+
+
+def test_moment_fit_cache_beyond_its_slots(lib):
+    """More orders than the fit cache holds: each still builds (or comes from
+    the cache) and evaluates the same as on its first use."""
+    alphas = [1.2, 1.3, 1.35, 1.4, 1.45, 1.6, 1.7, 1.8, 2.5]  # nine orders, eight slots
+    t = (ctypes.c_float * 3)(-1.0, 0.5, 3.0)
+    first = {}
+    for a in alphas + alphas[:2]:
+        assert lib.entmaxkv_gaussian_alpha_supported(ctypes.c_float(a)) == 1
+        out = (ctypes.c_float * 3)()
+        assert lib.entmaxkv_moment_fit_eval(ctypes.c_float(a), 0, t, 3, out) == 0
+        first.setdefault(a, list(out))
+        assert list(out) == first[a]
