@@ -4,6 +4,8 @@
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+
+#include <mutex>
 #include <math_constants.h>
 #include <stdint.h>
 
@@ -519,6 +521,34 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* sh, int& total) 
 __device__ __forceinline__ void pdl_enter() {
   asm volatile("griddepcontrol.wait;\n" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
+// Raise a kernel's dynamic shared memory limit to at least `bytes` on the
+// current device, remembering what was set, so that a decode's launches make
+// no attribute call after the first one (host time per decode).
+inline cudaError_t ensure_smem(const void* kernel, int bytes) {
+  struct Entry {
+    const void* fn;
+    int dev, bytes;
+  };
+  static Entry table[256];
+  static int used = 0;
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  int slot = -1;
+  for (int i = 0; i < used; ++i)
+    if (table[i].fn == kernel && table[i].dev == dev) {
+      if (table[i].bytes >= bytes) return cudaSuccess;
+      slot = i;
+    }
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  if (slot < 0 && used < 256) slot = used++;
+  if (slot >= 0) table[slot] = Entry{kernel, dev, bytes};
+  return cudaSuccess;
 }
 
 template <typename... KArgs, typename... Args>

@@ -1009,12 +1009,26 @@ __global__ void __launch_bounds__(kThreads, GP <= 4 ? 2 : 1) pass_b_kernel(Decod
     const uint32_t* bm = a.bitmap + skv * a.words;
     const int plo = (int)(((long long)n_pages * split) / a.splits);
     const int phi = (int)(((long long)n_pages * (split + 1)) / a.splits);
-    for (int p = plo + tid; p < phi; p += kThreads) {
-      if ((bm[p >> 5] >> (p & 31)) & 1u) continue;
-      const float np = (float)(p == n_pages - 1 ? L - p * P : P);
+    // four pages a thread per round, their loads issued together
+    for (int p0 = plo + tid; p0 < phi; p0 += 4 * kThreads) {
+      uint32_t w[4];
+      float u[4][GP];
 #pragma unroll
-      for (int h = 0; h < GP; ++h)
-        if (h < G) dd[h] += np * pos_pow(a.a1 * a.bbox_u[(hq0 + h) * a.maxp + p] - tau[h], a.beta);
+      for (int j = 0; j < 4; ++j) {
+        const int p = p0 + j * kThreads;
+        w[j] = p < phi ? bm[p >> 5] : 0xffffffffu;
+#pragma unroll
+        for (int h = 0; h < GP; ++h) u[j][h] = (p < phi && h < G) ? a.bbox_u[(hq0 + h) * a.maxp + p] : 0.0f;
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int p = p0 + j * kThreads;
+        if (p >= phi || ((w[j] >> (p & 31)) & 1u)) continue;  // kept pages carry no dropped mass
+        const float np = (float)(p == n_pages - 1 ? L - p * P : P);
+#pragma unroll
+        for (int h = 0; h < GP; ++h)
+          if (h < G) dd[h] += np * pos_pow(a.a1 * u[j][h] - tau[h], a.beta);
+      }
     }
 #pragma unroll
     for (int h = 0; h < GP; ++h) {
@@ -1138,8 +1152,7 @@ cudaError_t launch_pass_a(const DecodeArgs& a, int kv_dtype, cudaStream_t st) {
 template <typename T, int D, int GP>
 static cudaError_t pass_b_launch(const DecodeArgs& a, dim3 grid, cudaStream_t st) {
   const int smem = kWarps * a.P * D * (int)sizeof(T);  // one V slab per warp
-  const cudaError_t e = cudaFuncSetAttribute(pass_b_kernel<T, D, GP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kWarps * 32 * D * (int)sizeof(T));
+  const cudaError_t e = ensure_smem((const void*)pass_b_kernel<T, D, GP>, kWarps * 32 * D * (int)sizeof(T));
   if (e != cudaSuccess) return e;
   launch_k(false, pass_b_kernel<T, D, GP>, dim3(grid), dim3(kThreads), smem, st, a);
   return cudaGetLastError();

@@ -8,28 +8,13 @@
 //    with μ_p = q·mean_p/√d and σ_p² = Σ_d q_d²·var_{p,d}/d (diagonal model),
 //    reported on the z scale: m_p = (α−1)μ_p, ς_p = (α−1)σ_p.
 //
-// bf16 metadata: the group's g query heads against 16 pages form a
-// [16 pages × 2d] · [2d × 8 heads] tile: one m16n8k16 bf16 MMA chain per 16
-// pages (products of bf16 values are exact in the fp32 accumulator). The
-// tile's A operand is read straight from global memory with 16-byte loads in
-// a permuted k order; the B operand ([q⁺; q⁻]) is permuted identically, so
-// the contraction is unchanged.
+// bf16 metadata (both kinds): the group's query heads against 8 pages form an
+// m16n8k16 tile (products of bf16 values are exact in the fp32 accumulator),
+// with the pages' rows streamed through a ring of shared-memory stages by
+// bulk copies (gauss_mma_kernel).
 #include "common.cuh"
 
 namespace ekv {
-
-// B fragment words of query head n (= lane/4) for k-step (s2, u):
-// dims 32·s2 + 8·c + 4·u + {0,1} and {2,3}, c = lane%4.
-__device__ __forceinline__ void load_q_frag_bf16(const __nv_bfloat16* qh, bool valid, int s2,
-                                                 int u, int c, uint32_t& w0, uint32_t& w1) {
-  if (!valid) {
-    w0 = w1 = 0u;
-    return;
-  }
-  const uint2 x = *reinterpret_cast<const uint2*>(qh + 32 * s2 + 8 * c + 4 * u);
-  w0 = x.x;
-  w1 = x.y;
-}
 
 // Split a bf16 pair into its positive and negative parts (exact).
 __device__ __forceinline__ void split_sign(uint32_t w, uint32_t& pos, uint32_t& neg) {
@@ -38,92 +23,6 @@ __device__ __forceinline__ void split_sign(uint32_t w, uint32_t& pos, uint32_t& 
   uint32_t phi = (hi & 0x8000u) ? 0u : hi, nhi = (hi & 0x8000u) ? hi : 0u;
   pos = plo | (phi << 16);
   neg = nlo | (nhi << 16);
-}
-
-template <int D>
-__global__ void __launch_bounds__(kThreads) bbox_bf16_kernel(DecodeArgs a) {
-  pdl_enter();
-  constexpr int KS = D / 16;   // k-steps per half of the 2d contraction
-  constexpr int C16 = D / 32;  // 16-byte chunks per row per lane
-  const int kvh = blockIdx.y, s = blockIdx.z;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r = lane >> 2, c = lane & 3;
-  clear_ctrl_slice(a.ctrl, a.ctrl_vec);
-  const int seq = seq_row(a.seq_ids, s, a.max_seqs, threadIdx.x == 0 ? a.status : nullptr);
-  if (seq < 0) return;
-  const int L = seq_len_clamped(a.seq_lens, seq, a.maxp, a.P, threadIdx.x == 0 ? a.status : nullptr);
-  const int n_pages = (L + a.P - 1) / a.P;
-  const int tiles = (n_pages + 15) / 16;
-  if ((int)(blockIdx.x * kWarps) >= tiles) return;
-
-  // B operand: [q⁺ ; q⁻] of head n = r.
-  const bool hv = r < a.G;
-  const __nv_bfloat16* qh =
-      (const __nv_bfloat16*)a.q + ((size_t)s * a.Hq + (size_t)kvh * a.G + (hv ? r : 0)) * D;
-  uint32_t bp[KS][2], bn[KS][2];
-#pragma unroll
-  for (int ks = 0; ks < KS; ++ks) {
-    uint32_t w0, w1;
-    load_q_frag_bf16(qh, hv, ks >> 1, ks & 1, c, w0, w1);
-    split_sign(w0, bp[ks][0], bn[ks][0]);
-    split_sign(w1, bp[ks][1], bn[ks][1]);
-  }
-  const size_t ustride = (size_t)a.maxp;
-  float* urow = a.bbox_u + ((size_t)s * a.Hq + (size_t)kvh * a.G) * ustride;
-  float* uhat = a.bbox_uhat + ((size_t)s * a.Hkv + kvh) * ustride;
-  const __nv_bfloat16* kmax = (const __nv_bfloat16*)a.kmax;
-  const __nv_bfloat16* kmin = (const __nv_bfloat16*)a.kmin;
-
-  for (int tile = blockIdx.x * kWarps + warp; tile < tiles; tile += gridDim.x * kWarps) {
-    const int p0 = tile * 16 + r, p1 = p0 + 8;
-    const int ph0 = p0 < n_pages ? phys_page(a.block_table, seq, p0, a.maxp, a.nphys, a.status) : -1;
-    const int ph1 = p1 < n_pages ? phys_page(a.block_table, seq, p1, a.maxp, a.nphys, a.status) : -1;
-    uint4 hx0[C16], hx1[C16], lo0[C16], lo1[C16];
-    const size_t m0 = ((size_t)(ph0 < 0 ? 0 : ph0) * a.Hkv + kvh) * D + 8 * c;
-    const size_t m1 = ((size_t)(ph1 < 0 ? 0 : ph1) * a.Hkv + kvh) * D + 8 * c;
-#pragma unroll
-    for (int j = 0; j < C16; ++j) {
-      const uint4 zz = make_uint4(0u, 0u, 0u, 0u);
-      hx0[j] = ph0 >= 0 ? ld_stream(kmax + m0 + 32 * j) : zz;
-      hx1[j] = ph1 >= 0 ? ld_stream(kmax + m1 + 32 * j) : zz;
-      lo0[j] = ph0 >= 0 ? ld_stream(kmin + m0 + 32 * j) : zz;
-      lo1[j] = ph1 >= 0 ? ld_stream(kmin + m1 + 32 * j) : zz;
-    }
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-      const int j = ks >> 1;
-      const bool u = ks & 1;
-      mma_bf16(acc, u ? hx0[j].z : hx0[j].x, u ? hx1[j].z : hx1[j].x, u ? hx0[j].w : hx0[j].y,
-               u ? hx1[j].w : hx1[j].y, bp[ks][0], bp[ks][1]);
-      mma_bf16(acc, u ? lo0[j].z : lo0[j].x, u ? lo1[j].z : lo1[j].x, u ? lo0[j].w : lo0[j].y,
-               u ? lo1[j].w : lo1[j].y, bn[ks][0], bn[ks][1]);
-    }
-    const int h0 = 2 * c, h1 = 2 * c + 1;
-    // an unreadable page gets −inf: no bound mass, never preferred by top-k
-    const float u00 = ph0 >= 0 ? acc[0] * a.inv_sqrt_d : -CUDART_INF_F;
-    const float u01 = ph0 >= 0 ? acc[1] * a.inv_sqrt_d : -CUDART_INF_F;
-    const float u10 = ph1 >= 0 ? acc[2] * a.inv_sqrt_d : -CUDART_INF_F;
-    const float u11 = ph1 >= 0 ? acc[3] * a.inv_sqrt_d : -CUDART_INF_F;
-    if (p0 < n_pages) {
-      if (h0 < a.G) urow[h0 * ustride + p0] = u00;
-      if (h1 < a.G) urow[h1 * ustride + p0] = u01;
-    }
-    if (p1 < n_pages) {
-      if (h0 < a.G) urow[h0 * ustride + p1] = u10;
-      if (h1 < a.G) urow[h1 * ustride + p1] = u11;
-    }
-    float mx0 = fmaxf(h0 < a.G ? u00 : -CUDART_INF_F, h1 < a.G ? u01 : -CUDART_INF_F);
-    float mx1 = fmaxf(h0 < a.G ? u10 : -CUDART_INF_F, h1 < a.G ? u11 : -CUDART_INF_F);
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-    if (c == 0) {
-      if (p0 < n_pages) uhat[p0] = mx0;
-      if (p1 < n_pages) uhat[p1] = mx1;
-    }
-  }
 }
 
 // fp32 metadata: one thread per page, q in shared memory.
@@ -350,7 +249,7 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_kernel(DecodeArgs a) {
     const int st = j % NST;
     const uint32_t par = (uint32_t)((j / NST) & 1);
     const int g = g_lo + j;
-    if (!mbar_wait_limit(&full[st], par, wait_limit)) {
+    if (!__all_sync(0xffffffffu, mbar_wait_limit(&full[st], par, wait_limit))) {  // warp-uniform
       stuck = 1;
       break;
     }
@@ -393,7 +292,7 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_kernel(DecodeArgs a) {
     __syncwarp();
     if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(&empty[st])) : "memory");
     if (warp == 0 && j + NST < n_mine) {  // refill once every warp released the stage
-      if (!mbar_wait_bounded(&empty[st], par)) {
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(&empty[st], par))) {
         stuck = 1;
         break;
       }
@@ -495,7 +394,10 @@ __device__ __forceinline__ uint32_t bf2_pack(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-template <int D>
+// MODE 0: the Gaussian statistics (μ, σ) from the bf16 mean and m2 copies;
+// MODE 1: the bounding box U = (q⁺·kmax + q⁻·kmin)/√d from the bf16 kmax and
+// kmin (exact term by term), per query head and as the group's maximum.
+template <int D, int MODE>
 __global__ void __launch_bounds__(kGaussWarps * 32) gauss_mma_kernel(DecodeArgs a) {
   pdl_enter();
   constexpr int PPS = kGaussMmaPPS, NST = kGaussMmaNST, KS = D / 16;
@@ -515,8 +417,9 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_mma_kernel(DecodeArgs 
   __shared__ int phys_pre[kGaussMmaPre];
   static_assert(NST * PPS <= 32, "warp 0 looks up the first stages' pages at once");
   clear_ctrl_slice(a.ctrl, a.ctrl_vec);
-  for (int i = threadIdx.x; i < KH * a.G; i += blockDim.x)
-    a.mslot[((size_t)s * a.Hq + (size_t)kv0 * a.G + i) * a.mslots + blockIdx.x] = 0u;
+  if (MODE == 0)
+    for (int i = threadIdx.x; i < KH * a.G; i += blockDim.x)
+      a.mslot[((size_t)s * a.Hq + (size_t)kv0 * a.G + i) * a.mslots + blockIdx.x] = 0u;
   const int seq = seq_row(a.seq_ids, s, a.max_seqs, threadIdx.x == 0 ? a.status : nullptr);
   if (seq < 0) return;
   const int L = seq_len_clamped(a.seq_lens, seq, a.maxp, a.P, threadIdx.x == 0 ? a.status : nullptr);
@@ -542,7 +445,9 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_mma_kernel(DecodeArgs 
     if (lane == 0) mbar_expect_tx(&full[st], (uint32_t)__popc(valid) * (uint32_t)run);
     __syncwarp();
     if (ph >= 0) {
-      const __nv_bfloat16* src = ((lane & 1) ? a.m2_lo : a.mean_lo) + ((size_t)ph * a.Hkv + kv0) * D;
+      const __nv_bfloat16* arr = MODE == 0 ? ((lane & 1) ? a.m2_lo : a.mean_lo)
+                                           : (const __nv_bfloat16*)((lane & 1) ? a.kmin : a.kmax);
+      const __nv_bfloat16* src = arr + ((size_t)ph * a.Hkv + kv0) * D;
       bulk_g2s(dyn + st * sstride + (lane >> 1) * pstride + (lane & 1) * run, src, (uint32_t)run, &full[st]);
     }
   };
@@ -577,7 +482,8 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_mma_kernel(DecodeArgs 
   }
 
   // A fragments: row lane/4 (a query head of the group), dims 2(lane%4)+{0,1}
-  // and +8 of each 16-dim step; rows 8..15 are zero. q, q² hi, q² lo.
+  // and +8 of each 16-dim step; rows 8..15 are zero. MODE 0: q, q² hi,
+  // q² lo; MODE 1: q⁺ and q⁻ (in aq and ah; al unused).
   const int r = lane >> 2, cpair = 2 * (lane & 3);
   const bool hv = active && r < a.G;
   const __nv_bfloat16* qh = (const __nv_bfloat16*)a.q + ((size_t)s * a.Hq + (size_t)(hv ? kvh : 0) * a.G + (hv ? r : 0)) * D;
@@ -588,6 +494,11 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_mma_kernel(DecodeArgs 
     for (int u = 0; u < 2; ++u) {
       const int d0 = 16 * k + 8 * u + cpair;
       const uint32_t w = hv ? *reinterpret_cast<const uint32_t*>(qh + d0) : 0u;
+      if (MODE == 1) {
+        split_sign(w, aq[k][u], ah[k][u]);
+        al[k][u] = 0u;
+        continue;
+      }
       aq[k][u] = w;
       const float x0 = bf_lo(w), x1 = bf_hi(w);
       const float s0 = x0 * x0, s1 = x1 * x1;  // exact: at most 16 significant bits
@@ -606,7 +517,7 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_mma_kernel(DecodeArgs 
     const int st = j % NST;
     const uint32_t par = (uint32_t)((j / NST) & 1);
     const int g = g_lo + j;
-    if (!mbar_wait_limit(&full[st], par, wait_limit)) {
+    if (!__all_sync(0xffffffffu, mbar_wait_limit(&full[st], par, wait_limit))) {  // warp-uniform
       stuck = 1;
       break;
     }
@@ -620,9 +531,13 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_mma_kernel(DecodeArgs 
         uint32_t bm0, bm1, bv0, bv1;
         ldsm_x2(bm0, bm1, rowm + 32 * k);
         ldsm_x2(bv0, bv1, rowv + 32 * k);
-        mma_bf16(mu, aq[k][0], 0u, aq[k][1], 0u, bm0, bm1);
-        mma_bf16(sg, ah[k][0], 0u, ah[k][1], 0u, bv0, bv1);
-        mma_bf16(sg, al[k][0], 0u, al[k][1], 0u, bv0, bv1);
+        mma_bf16(mu, aq[k][0], 0u, aq[k][1], 0u, bm0, bm1);  // μ (MODE 1: q⁺·kmax)
+        if (MODE == 0) {
+          mma_bf16(sg, ah[k][0], 0u, ah[k][1], 0u, bv0, bv1);
+          mma_bf16(sg, al[k][0], 0u, al[k][1], 0u, bv0, bv1);
+        } else {
+          mma_bf16(mu, ah[k][0], 0u, ah[k][1], 0u, bv0, bv1);  // + q⁻·kmin
+        }
       }
       ph0 = phys_sm[st * PPS + cpair];
       ph1 = phys_sm[st * PPS + cpair + 1];
@@ -630,11 +545,30 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_mma_kernel(DecodeArgs 
     __syncwarp();
     if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(&empty[st])) : "memory");
     if (warp == 0 && j + NST < n_mine) {
-      if (!mbar_wait_bounded(&empty[st], par)) {
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(&empty[st], par))) {
         stuck = 1;
         break;
       }
       issue(g + NST, st);
+    }
+    if (MODE == 1) {
+      // U per query head, and the group's maximum per page (the lanes of one
+      // page column differ in bits 2..4: the head)
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int p = g * PPS + cpair + u;
+        const int ph = u ? ph1 : ph0;
+        const float uv = (hv && ph >= 0) ? mu[u] * a.inv_sqrt_d : -CUDART_INF_F;  // unreadable: no bound mass
+        float mx = uv;
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        if (p < n_pages && active) {
+          if (hv) a.bbox_u[((size_t)s * a.Hq + (size_t)kvh * a.G + r) * a.maxp + p] = uv;
+          if (r == 0) a.bbox_uhat[((size_t)s * a.Hkv + kvh) * a.maxp + p] = mx;
+        }
+      }
+      continue;
     }
     if (!hv) continue;
     float2* dst = a.gauss_ms + ((size_t)s * a.Hq + (size_t)kvh * a.G + r) * a.maxp;
@@ -662,6 +596,7 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_mma_kernel(DecodeArgs 
         if (f > 0) mbar_wait_bounded(&full[st], (uint32_t)((f - 1) & 1));
       }
   }
+  if (MODE == 1) return;
   runmax = fmaxf(runmax, __shfl_xor_sync(0xffffffffu, runmax, 1));
   runmax = fmaxf(runmax, __shfl_xor_sync(0xffffffffu, runmax, 2));
   if (hv && (lane & 3) == 0 && runmax > -CUDART_INF_F) smax[warp][r] = ord_enc(runmax);
@@ -673,13 +608,13 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_mma_kernel(DecodeArgs 
   }
 }
 
-template <int D>
+template <int D, int MODE>
 static cudaError_t gauss_mma_launch(const DecodeArgs& a, dim3 grid, cudaStream_t st) {
   constexpr int smem = gauss_mma_smem_bytes(D);
   static_assert(gauss_mma_smem_bytes(D) <= 227 * 1024, "stages exceed shared memory");
-  cudaError_t e = cudaFuncSetAttribute(gauss_mma_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = ensure_smem((const void*)gauss_mma_kernel<D, MODE>, smem);
   if (e != cudaSuccess) return e;
-  return launch_k(false, gauss_mma_kernel<D>, dim3(grid), dim3(kGaussWarps * 32), smem, st, a);
+  return launch_k(false, gauss_mma_kernel<D, MODE>, dim3(grid), dim3(kGaussWarps * 32), smem, st, a);
 }
 
 static int grid_x_for(int units, int per_block, int sms, int other_blocks) {
@@ -693,9 +628,10 @@ static int grid_x_for(int units, int per_block, int sms, int other_blocks) {
 cudaError_t launch_bbox(const DecodeArgs& a, int kv_dtype, int sms, cudaStream_t st) {
   const int other = a.Hkv * a.S;
   if (kv_dtype == ENTMAXKV_BF16) {
-    dim3 grid(grid_x_for((a.maxp + 15) / 16, kWarps, sms, other), a.Hkv, a.S);
-    if (a.D == 128) launch_k(false, bbox_bf16_kernel<128>, dim3(grid), dim3(kThreads), 0, st, a);
-    else launch_k(false, bbox_bf16_kernel<64>, dim3(grid), dim3(kThreads), 0, st, a);
+    // the streamed tensor-core kernel, rows of up to 8 KV heads
+    dim3 grid(gauss_grid_x(a.maxp, a.Hkv, a.S, sms), (a.Hkv + 7) / 8, a.S);
+    const cudaError_t e = a.D == 128 ? gauss_mma_launch<128, 1>(a, grid, st) : gauss_mma_launch<64, 1>(a, grid, st);
+    if (e != cudaSuccess) return e;
   } else {
     dim3 grid(grid_x_for(a.maxp, kThreads, sms, other), a.Hkv, a.S);
     if (a.D == 128) launch_k(false, bbox_f32_kernel<128>, dim3(grid), dim3(kThreads), 0, st, a);
@@ -708,7 +644,7 @@ template <typename TQ, typename TM, int D, int GP>
 static cudaError_t gauss_launch(const DecodeArgs& a, dim3 grid, cudaStream_t st) {
   constexpr int smem = gauss_smem_bytes<TM, D>();
   static_assert(gauss_smem_bytes<TM, D>() <= 227 * 1024, "stages exceed shared memory");
-  cudaError_t e = cudaFuncSetAttribute(gauss_kernel<TQ, TM, D, GP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = ensure_smem((const void*)gauss_kernel<TQ, TM, D, GP>, smem);
   if (e != cudaSuccess) return e;
   return launch_k(false, gauss_kernel<TQ, TM, D, GP>, dim3(grid), dim3(kGaussWarps * 32), smem, st, a);
 }
@@ -745,7 +681,7 @@ cudaError_t launch_gauss(const DecodeArgs& a, int kv_dtype, int sms, cudaStream_
   dim3 grid(a.mslots, (a.Hkv + 7) / 8, a.S);
   cudaError_t e;
   if (kv_dtype == ENTMAXKV_BF16 && a.mean_lo)  // bf16 q and metadata: tensor cores
-    e = a.D == 128 ? gauss_mma_launch<128>(a, grid, st) : gauss_mma_launch<64>(a, grid, st);
+    e = a.D == 128 ? gauss_mma_launch<128, 0>(a, grid, st) : gauss_mma_launch<64, 0>(a, grid, st);
   else if (kv_dtype == ENTMAXKV_BF16)
     e = a.D == 128 ? gauss_dispatch_g<__nv_bfloat16, 128>(a, grid, st)
                    : gauss_dispatch_g<__nv_bfloat16, 64>(a, grid, st);

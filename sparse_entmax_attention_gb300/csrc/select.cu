@@ -117,7 +117,8 @@ __global__ void __cluster_dims__(kTauhatCluster, 1, 1) __launch_bounds__(kThread
     tauhat_kernel(DecodeArgs a) {
   constexpr bool B2 = MODE == 1;
   pdl_enter();
-  static_assert(kTauhatCluster * kWarps == 64, "two partials per lane");
+  constexpr int kParts = kTauhatCluster * kWarps / 32;  // partials per lane after the exchange
+  static_assert(kTauhatCluster * kWarps % 32 == 0, "whole partials per lane");
   cg::cluster_group cluster = cg::this_cluster();
   // Every warp of the cluster pushes its partial (F, D1, D2) into this slot
   // of every block, so after the cluster barrier all reads are local.
@@ -185,7 +186,7 @@ __global__ void __cluster_dims__(kTauhatCluster, 1, 1) __launch_bounds__(kThread
   for (int i = 0; i < kPairs; ++i) {
     mb2[i] = f2_pack(mb[2 * i], mb[2 * i + 1]);
     sr2[i] = f2_pack(sr[2 * i], sr[2 * i + 1]);
-    ir2[i] = f2_pack(1.0f / sr[2 * i], 1.0f / sr[2 * i + 1]);
+    ir2[i] = f2_pack(__frcp_rn(sr[2 * i]), __frcp_rn(sr[2 * i + 1]));
     nr2[i] = f2_pack(nr[2 * i], nr[2 * i + 1]);
   }
   float lo = 0.0f, hi = CUDART_INF_F, off = 0.0f;  // offsets from base; F(lo) ≥ 1
@@ -253,8 +254,14 @@ __global__ void __cluster_dims__(kTauhatCluster, 1, 1) __launch_bounds__(kThread
     if (lane < kTauhatCluster)
       cluster.map_shared_rank(&slot[it & 1][0], lane)[rank * kWarps + warp] = make_float4(f, df, d2f, 0.0f);
     cluster.sync();
-    const float4 e0 = slot[it & 1][lane], e1 = slot[it & 1][lane + 32];
-    float F = e0.x + e1.x, D1 = e0.y + e1.y, D2 = e0.z + e1.z;  // F, −dF/dτ, d²F/dτ²
+    float F = 0.0f, D1 = 0.0f, D2 = 0.0f;  // F, −dF/dτ, d²F/dτ²
+#pragma unroll
+    for (int q = 0; q < kParts; ++q) {  // a fixed order: every warp sums alike
+      const float4 e = slot[it & 1][lane + 32 * q];
+      F += e.x;
+      D1 += e.y;
+      D2 += e.z;
+    }
     F = warp_sum(F);
     D1 = warp_sum(D1);
     D2 = warp_sum(D2);
@@ -369,12 +376,17 @@ __device__ __forceinline__ float page_key(const DecodeArgs& a, int mode, int s, 
   return best;
 }
 
+// Keys of up to kTopkKeys pages are computed once and kept in shared memory
+// for the radix passes; longer rows recompute them from global memory.
+constexpr int kTopkKeys = 48 * 1024;
+
 __global__ void __launch_bounds__(1024) topk_kernel(DecodeArgs a, int mode) {
   pdl_enter();
+  extern __shared__ uint32_t keys_sh[];  // [min(maxp, kTopkKeys)] order-preserving keys
   __shared__ int hist[256];
   __shared__ int sh_scan[32];
   __shared__ float thr[8];
-  __shared__ uint32_t sh_prefix, sh_mask;
+  __shared__ uint32_t sh_prefix, sh_mask, sh_kmin, sh_kmax;
   __shared__ int sh_remaining, sh_eq_count;
   const int kvh = blockIdx.x, s = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -383,6 +395,7 @@ __global__ void __launch_bounds__(1024) topk_kernel(DecodeArgs a, int mode) {
   const int n = (L + a.P - 1) / a.P;
   uint32_t* bm = a.bitmap + ((size_t)s * a.Hkv + kvh) * a.words;
   const float c_full = sqrtf(2.0f * logf((float)a.P));
+  const bool staged = n <= kTopkKeys && n <= a.maxp;
   int k;
   if (mode == 0) {
     k = min(a.kpages, n);
@@ -404,17 +417,64 @@ __global__ void __launch_bounds__(1024) topk_kernel(DecodeArgs a, int mode) {
     if (tid < a.G) thr[tid] = a.tauhat[(size_t)s * a.Hq + (size_t)kvh * a.G + tid] - a.margin_z;
   }
   if (tid == 0) {
-    sh_prefix = 0u;
-    sh_mask = 0u;
+    sh_kmin = 0xffffffffu;
+    sh_kmax = 0u;
     sh_remaining = k;
   }
   __syncthreads();
-  for (int shift = 24; shift >= 0; shift -= 8) {
+  auto key_of = [&](int p) -> uint32_t {
+    return staged ? keys_sh[p] : ord_enc(page_key(a, mode, s, kvh, p, n, L, bm, thr, c_full));
+  };
+  // Every key once from global memory (eight loads in flight a thread), kept
+  // in shared memory when it fits, with the smallest and largest key.
+  {
+    uint32_t lo_k = 0xffffffffu, hi_k = 0u;
+    for (int p0 = 0; p0 < n; p0 += 8 * 1024) {
+      uint32_t kk[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int p = p0 + u * 1024 + tid;
+        kk[u] = p < n ? ord_enc(page_key(a, mode, s, kvh, p, n, L, bm, thr, c_full)) : 0u;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int p = p0 + u * 1024 + tid;
+        if (p < n) {
+          if (staged) keys_sh[p] = kk[u];
+          lo_k = min(lo_k, kk[u]);
+          hi_k = max(hi_k, kk[u]);
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      lo_k = min(lo_k, __shfl_xor_sync(0xffffffffu, lo_k, o));
+      hi_k = max(hi_k, __shfl_xor_sync(0xffffffffu, hi_k, o));
+    }
+    if (lane == 0) {
+      atomicMin(&sh_kmin, lo_k);
+      atomicMax(&sh_kmax, hi_k);
+    }
+  }
+  __syncthreads();
+  // Radix select of the k-th largest key, 8 bits a pass, starting below the
+  // leading bits every key shares (keys of similar scores agree in sign and
+  // exponent, so a first digit there would put them all in one bin).
+  const uint32_t kmin = sh_kmin, kmax = sh_kmax;
+  const int rb = (kmin ^ kmax) ? 32 - __clz((int)(kmin ^ kmax)) : 0;  // bits below the common prefix
+  if (tid == 0) {
+    sh_mask = rb >= 32 ? 0u : (0xffffffffu << rb);
+    sh_prefix = kmin & sh_mask;
+    sh_eq_count = n;  // (all keys equal: every page ties at T = kmin)
+  }
+  __syncthreads();
+  for (int sh = rb - 8; rb > 0; sh -= 8) {
+    const int shift = sh > 0 ? sh : 0;  // the last digit may overlap the decided bits
     if (tid < 256) hist[tid] = 0;
     __syncthreads();
     const uint32_t prefix = sh_prefix, mask = sh_mask;
     for (int p = tid; p < n; p += 1024) {
-      const uint32_t key = ord_enc(page_key(a, mode, s, kvh, p, n, L, bm, thr, c_full));
+      const uint32_t key = key_of(p);
       if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1);
     }
     __syncthreads();
@@ -451,17 +511,28 @@ __global__ void __launch_bounds__(1024) topk_kernel(DecodeArgs a, int mode) {
       }
     }
     __syncthreads();
+    if (shift == 0) break;
   }
   // T is the k-th largest key: keep every key > T and the `remaining`
   // lowest-index pages with key == T.
   const uint32_t T = sh_prefix;
   const int remaining = sh_remaining;
   const bool split_ties = sh_eq_count > remaining;
+  if (mode == 0 && !split_ties) {
+    // no tie to split and no bitmap read back: each warp writes its words
+    // without block barriers
+    for (int p0 = warp * 32; p0 < n; p0 += 1024) {
+      const int p = p0 + lane;
+      const uint32_t bits = __ballot_sync(0xffffffffu, p < n && key_of(p) >= T);
+      if (lane == 0) bm[p0 >> 5] = bits;
+    }
+    return;
+  }
   __syncthreads();  // every thread has read the selection state
   int taken = 0;    // ties kept so far (block-uniform)
   for (int base = 0; base < n; base += 1024) {
     const int p = base + tid;
-    const uint32_t key = p < n ? ord_enc(page_key(a, mode, s, kvh, p, n, L, bm, thr, c_full)) : 0u;
+    const uint32_t key = p < n ? key_of(p) : 0u;
     bool sel = p < n && key > T;
     const bool eq = p < n && key == T;
     if (!split_ties) {
@@ -489,7 +560,10 @@ cudaError_t launch_tauhat(const DecodeArgs& a, cudaStream_t st) {
 
 cudaError_t launch_topk(const DecodeArgs& a, int mode, cudaStream_t st) {
   dim3 grid(a.Hkv, a.S);
-  launch_k(false, topk_kernel, dim3(grid), dim3(1024), 0, st, a, mode);
+  const int smem = 4 * (a.maxp < kTopkKeys ? a.maxp : kTopkKeys);
+  const cudaError_t e = ensure_smem((const void*)topk_kernel, smem);
+  if (e != cudaSuccess) return e;
+  launch_k(false, topk_kernel, dim3(grid), dim3(1024), (size_t)smem, st, a, mode);
   return cudaGetLastError();
 }
 

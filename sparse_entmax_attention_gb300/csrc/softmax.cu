@@ -43,6 +43,8 @@ __global__ void __launch_bounds__(kThreads, 2) softmax_kernel(DecodeArgs a) {
   int* list = reinterpret_cast<int*>(red4);  // the page list is done before the combine starts
   __shared__ int sh_scan[32];
   __shared__ int last_sh;
+  __shared__ uint64_t vbar[kWarps];
+  extern __shared__ __align__(128) unsigned char vstage_sm[];  // bf16: [kWarps][P][D], a V slab per warp
   const int split = blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = a.G, P = a.P;
@@ -75,15 +77,48 @@ __global__ void __launch_bounds__(kThreads, 2) softmax_kernel(DecodeArgs a) {
 #pragma unroll
     for (int j = 0; j < VEC; ++j) acc[h][j] = 0.0f;
   }
-  for (int i = warp; i < hi - lo; i += kWarps) {
+  // bf16 pages: the V slab is requested by one bulk copy into the warp's
+  // buffer before the page's scores are computed, so its transfer overlaps
+  // the K loads and the scores, and the weighted sum reads it from shared
+  // memory (no V registers in flight)
+  T* vbuf = reinterpret_cast<T*>(vstage_sm) + (size_t)warp * P * D;
+  uint32_t vphase = 0u;
+  bool stuck = false;
+  if constexpr (sizeof(T) == 2) {
+    if (lane == 0) {
+      mbar_init(&vbar[warp], 1);
+      mbar_fence_init();
+    }
+    __syncwarp();
+  }
+  for (int i = warp; i < hi - lo && !stuck; i += kWarps) {
     const int page = bitmap ? list[i] : lo + i;
     const int ph = phys_page(a.block_table, seq, page, a.maxp, a.nphys, lane == 0 ? a.status : nullptr);
     if (ph < 0) continue;
     const int nv = min(P, L - page * P);
     const size_t slab_off = ((size_t)ph * a.Hkv + kvh) * P * D;
     if constexpr (sizeof(T) == 2) {
+      if (lane == 0) {
+        const uint32_t bytes = (uint32_t)(P * D * sizeof(T));
+        mbar_expect_tx(&vbar[warp], bytes);
+        bulk_g2s(vbuf, (const T*)a.v_pool + slab_off, bytes, &vbar[warp]);
+      }
+    }
+    if constexpr (sizeof(T) == 2) {
       float zf[2][4];
-      page_scores_bf16<D>((const __nv_bfloat16*)a.k_pool + slab_off, P, nv, bq, scale2, lane, zf);
+      // one 16-token tile at a time: half the K fragments live at once
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+        if (16 * mt >= P) {
+          zf[mt][0] = zf[mt][1] = zf[mt][2] = zf[mt][3] = -CUDART_INF_F;
+          continue;
+        }
+        float zt[2][4];
+        page_scores_bf16<D>((const __nv_bfloat16*)a.k_pool + slab_off + (size_t)16 * mt * D, 16,
+                            nv - 16 * mt, bq, scale2, lane, zt);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) zf[mt][e] = zt[0][e];
+      }
       const int r = lane >> 2, c = lane & 3, h0 = 2 * c, h1 = h0 + 1;
       float pm0 = -CUDART_INF_F, pm1 = -CUDART_INF_F;
 #pragma unroll
@@ -132,6 +167,35 @@ __global__ void __launch_bounds__(kThreads, 2) softmax_kernel(DecodeArgs a) {
         m[h] = mn;
       }
     }
+    if constexpr (sizeof(T) == 2) {
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(&vbar[warp], vphase))) {
+        stuck = true;
+        break;
+      }
+      vphase ^= 1u;
+      const T* vrow = vbuf + dc * VEC;
+#pragma unroll 4
+      for (int u = 0; u < MAXT; ++u) {
+        const int t = tg + TG * u;
+        if (t < nv) {
+          const uint4 raw = *reinterpret_cast<const uint4*>(vrow + (size_t)t * D);
+          float v[VEC];
+          v[0] = bf_lo(raw.x); v[1] = bf_hi(raw.x); v[2] = bf_lo(raw.y); v[3] = bf_hi(raw.y);
+          v[4] = bf_lo(raw.z); v[5] = bf_hi(raw.z); v[6] = bf_lo(raw.w); v[7] = bf_hi(raw.w);
+#pragma unroll
+          for (int h = 0; h < GP; ++h) {
+            if (h < G && m[h] > -CUDART_INF_F) {
+              const float p = exp2f(sbuf[warp][t][h] - m[h]);
+              l[h] += p;
+#pragma unroll
+              for (int j = 0; j < VEC; ++j) acc[h][j] = fmaf(p, v[j], acc[h][j]);
+            }
+          }
+        }
+      }
+      __syncwarp();  // the buffer is refilled for the next page
+      continue;
+    }
     const T* vs = (const T*)a.v_pool + slab_off + dc * VEC;
     for (int c0 = 0; c0 < MAXT; c0 += CH) {
       uint4 raw[CH];
@@ -163,6 +227,13 @@ __global__ void __launch_bounds__(kThreads, 2) softmax_kernel(DecodeArgs a) {
           }
         }
       }
+    }
+    __syncwarp();
+  }
+  if (stuck) {  // a copy did not arrive within the bound: flag it, let it land, stop
+    if (lane == 0) {
+      raise_flag(a.status, ENTMAXKV_DEV_TIMEOUT);
+      mbar_wait_bounded(&vbar[warp], vphase);
     }
     __syncwarp();
   }
@@ -332,12 +403,21 @@ __global__ void __launch_bounds__(kThreads, 2) softmax_kernel(DecodeArgs a) {
   }
 }
 
+template <typename T, int D, int GP>
+static void softmax_l(const DecodeArgs& a, dim3 grid, cudaStream_t st) {
+  // bf16: a V slab per warp in dynamic shared memory
+  const int smem = sizeof(T) == 2 ? kWarps * a.P * D * (int)sizeof(T) : 0;
+  if (smem && ensure_smem((const void*)softmax_kernel<T, D, GP>, smem) != cudaSuccess)
+    return;
+  launch_k(false, softmax_kernel<T, D, GP>, dim3(grid), dim3(kThreads), (size_t)smem, st, a);
+}
+
 template <typename T, int D>
 static void softmax_g(const DecodeArgs& a, dim3 grid, cudaStream_t st) {
-  if (a.G <= 1) launch_k(false, softmax_kernel<T, D, 1>, dim3(grid), dim3(kThreads), 0, st, a);
-  else if (a.G <= 2) launch_k(false, softmax_kernel<T, D, 2>, dim3(grid), dim3(kThreads), 0, st, a);
-  else if (a.G <= 4) launch_k(false, softmax_kernel<T, D, 4>, dim3(grid), dim3(kThreads), 0, st, a);
-  else launch_k(false, softmax_kernel<T, D, 8>, dim3(grid), dim3(kThreads), 0, st, a);
+  if (a.G <= 1) softmax_l<T, D, 1>(a, grid, st);
+  else if (a.G <= 2) softmax_l<T, D, 2>(a, grid, st);
+  else if (a.G <= 4) softmax_l<T, D, 4>(a, grid, st);
+  else softmax_l<T, D, 8>(a, grid, st);
 }
 
 cudaError_t launch_softmax(const DecodeArgs& a, int kv_dtype, cudaStream_t st) {

@@ -96,8 +96,12 @@ def test_decode_subset_by_seq_ids():
     sid = torch.tensor([2, 1], dtype=torch.int32, device="cuda")
     sub = B.decode(built.cache, allq[[2, 1]].contiguous(), 1.5, "topk", 256, seq_ids=sid)
     torch.cuda.synchronize()
-    torch.testing.assert_close(sub.out, full.out[[2, 1]], rtol=0, atol=0)
+    # the page ids are exact; the output is summed with float atomics whose
+    # order varies from run to run, so its last bits may differ
     torch.testing.assert_close(sub.page_ids, full.page_ids[[2, 1]], rtol=0, atol=0)
+    torch.testing.assert_close(sub.n_sel, full.n_sel[[2, 1]], rtol=0, atol=0)
+    torch.testing.assert_close(sub.out, full.out[[2, 1]], rtol=1e-6, atol=1e-7)
+    torch.testing.assert_close(sub.tau, full.tau[[2, 1]], rtol=1e-6, atol=1e-7)
 
 
 def test_token_by_token_append_matches_bulk():

@@ -49,15 +49,20 @@ def _decision(r, policy, P, budget):
         k = budget // P
         if k >= u.size:
             return np.full(u.size, np.inf), EPS_SEL
-        kth = np.sort(u)[::-1][k - 1]
-        return u - kth, EPS_SEL * max(1.0, abs(kth))
+        srt = np.sort(u)[::-1]
+        # the boundary between the k-th and the (k+1)-th key: the k pages
+        # above it are kept (an exact tie sits on it, broken by page index)
+        bnd = 0.5 * (srt[k - 1] + srt[k])
+        return u - bnd, EPS_SEL * max(1.0, abs(bnd))
     margin = (r["mhat"] - r["thr"][:, None]).max(axis=0)
     eps = EPS_SEL * max(1.0, float(np.abs(r["thr"]).max()))
     if r["capacity_flag"]:
         key = np.where(margin >= 0.0, margin, -np.inf)
-        kth = np.sort(key)[::-1][budget // P - 1]
-        margin = np.where(np.abs(key - kth) < np.abs(margin), key - kth, margin)
-        eps = max(eps, EPS_SEL * max(1.0, abs(kth)))
+        srt = np.sort(key)[::-1]
+        cap = budget // P
+        bnd = 0.5 * (srt[cap - 1] + srt[cap])  # overflow: more than cap pages cleared the threshold
+        margin = np.where(np.abs(key - bnd) < np.abs(margin), key - bnd, margin)
+        eps = max(eps, EPS_SEL * max(1.0, abs(bnd)))
     return margin, eps
 
 
