@@ -521,9 +521,43 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_mma_kernel(DecodeArgs 
       stuck = 1;
       break;
     }
-    float mu[4] = {0.f, 0.f, 0.f, 0.f}, sg[4] = {0.f, 0.f, 0.f, 0.f};
+    // three independent accumulator chains (μ, σ² hi, σ² lo; MODE 1: q⁺·kmax,
+    // q⁻·kmin), added at the end: each chain waits on its own MMAs only
+    float mu[4] = {0.f, 0.f, 0.f, 0.f}, sg[4] = {0.f, 0.f, 0.f, 0.f}, sl[4] = {0.f, 0.f, 0.f, 0.f};
     int ph0 = -1, ph1 = -1;
-    if (active) {
+    if constexpr (MODE == 1) {
+      // the bounding box's fragments fit in registers at once: the stage is
+      // released before the MMA chains run, so its refill does not wait on them
+      uint32_t bm[KS][2], bv[KS][2];
+      if (active) {
+        const unsigned char* rowm = dyn + st * sstride + lrow * pstride + warp * D * 2 + lk;
+#pragma unroll
+        for (int k = 0; k < KS; ++k) {
+          ldsm_x2(bm[k][0], bm[k][1], rowm + 32 * k);
+          ldsm_x2(bv[k][0], bv[k][1], rowm + run + 32 * k);
+        }
+        ph0 = phys_sm[st * PPS + cpair];
+        ph1 = phys_sm[st * PPS + cpair + 1];
+      }
+      __syncwarp();
+      if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(&empty[st])) : "memory");
+      if (warp == 0 && j + NST < n_mine) {
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&empty[st], par))) {
+          stuck = 1;
+          break;
+        }
+        issue(g + NST, st);
+      }
+      if (active) {
+#pragma unroll
+        for (int k = 0; k < KS; ++k) {
+          mma_bf16(mu, aq[k][0], 0u, aq[k][1], 0u, bm[k][0], bm[k][1]);  // q⁺·kmax
+          mma_bf16(sg, ah[k][0], 0u, ah[k][1], 0u, bv[k][0], bv[k][1]);  // q⁻·kmin
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) mu[i] += sg[i];
+      }
+    } else if (active) {
       const unsigned char* rowm = dyn + st * sstride + lrow * pstride + warp * D * 2 + lk;
       const unsigned char* rowv = rowm + run;
 #pragma unroll
@@ -531,25 +565,25 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_mma_kernel(DecodeArgs 
         uint32_t bm0, bm1, bv0, bv1;
         ldsm_x2(bm0, bm1, rowm + 32 * k);
         ldsm_x2(bv0, bv1, rowv + 32 * k);
-        mma_bf16(mu, aq[k][0], 0u, aq[k][1], 0u, bm0, bm1);  // μ (MODE 1: q⁺·kmax)
-        if (MODE == 0) {
-          mma_bf16(sg, ah[k][0], 0u, ah[k][1], 0u, bv0, bv1);
-          mma_bf16(sg, al[k][0], 0u, al[k][1], 0u, bv0, bv1);
-        } else {
-          mma_bf16(mu, ah[k][0], 0u, ah[k][1], 0u, bv0, bv1);  // + q⁻·kmin
-        }
+        mma_bf16(mu, aq[k][0], 0u, aq[k][1], 0u, bm0, bm1);  // μ: q · mean
+        mma_bf16(sg, ah[k][0], 0u, ah[k][1], 0u, bv0, bv1);  // σ²: q² hi · m2
+        mma_bf16(sl, al[k][0], 0u, al[k][1], 0u, bv0, bv1);  //   + q² lo · m2
       }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) sg[i] += sl[i];
       ph0 = phys_sm[st * PPS + cpair];
       ph1 = phys_sm[st * PPS + cpair + 1];
     }
-    __syncwarp();
-    if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(&empty[st])) : "memory");
-    if (warp == 0 && j + NST < n_mine) {
-      if (!__all_sync(0xffffffffu, mbar_wait_bounded(&empty[st], par))) {
-        stuck = 1;
-        break;
+    if constexpr (MODE == 0) {
+      __syncwarp();
+      if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(&empty[st])) : "memory");
+      if (warp == 0 && j + NST < n_mine) {
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&empty[st], par))) {
+          stuck = 1;
+          break;
+        }
+        issue(g + NST, st);
       }
-      issue(g + NST, st);
     }
     if (MODE == 1) {
       // U per query head, and the group's maximum per page (the lanes of one
