@@ -19,6 +19,7 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kSolveCap = 8192;     // candidate scores the τ solver keeps in shared memory
 constexpr int kListCap = 1024;      // selected pages one decode block handles
 constexpr int kTauhatCluster = 8;   // blocks per τ̂ cluster (one cluster per query head)
+constexpr int kTopkCluster = 8;     // blocks per top-k cluster (one cluster per (sequence, KV head))
 
 // Chebyshev fits of J_ν(t) = E[(t + Z)_+^ν], Z ~ N(0, 1), for the Gaussian
 // selector at an entmax order other than α ∈ {1.5, 2} (β = 1/(α−1)); the

@@ -18,9 +18,12 @@
 //
 // Top-k selection (§2B.1): the k pages with the largest bound (max over the
 // group's query heads), ties to the lower logical page index, by an 8-bit
-// radix select over order-preserving keys in one block per (sequence, KV head).
-// The same select enforces an optional cap on the Gaussian selection, keyed
-// by the margin max_h (M̂_p − threshold_h) of the selected pages.
+// radix select over order-preserving keys, in a cluster of blocks per
+// (sequence, KV head) that exchange digit histograms through distributed
+// shared memory (rows of up to kTopkClusterKeys pages), else in one block.
+// The one-block select also enforces an optional cap on the Gaussian
+// selection, keyed by the margin max_h (M̂_p − threshold_h) of the selected
+// pages.
 #include <cooperative_groups.h>
 
 #include "common.cuh"
@@ -550,6 +553,184 @@ __global__ void __launch_bounds__(1024) topk_kernel(DecodeArgs a, int mode) {
   }
 }
 
+// Top-k by bound (mode 0) over a cluster of kTopkCluster blocks per
+// (sequence, KV head). Block r owns the pages [r·chunk, (r+1)·chunk), chunk a
+// whole number of bitmap words, and keeps its keys in registers (page
+// p_lo + j·kTopkThreads + tid in slot j). The smallest and largest key and,
+// per 8-bit digit, every block's histogram are pushed into all blocks of the
+// cluster through distributed shared memory; after one cluster barrier each
+// block sums the same histograms in the same order and takes the same digit,
+// so every block ends with the same k-th largest key T. Keys equal to T are
+// kept lowest page first: the last digit's histograms already hold each
+// block's count of them, which gives this block's offset among the ties.
+constexpr int kTopkThreads = 1024, kTopkKpt = 8;
+constexpr int kTopkClusterKeys = kTopkCluster * kTopkThreads * kTopkKpt;
+
+__global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThreads)
+    topk_cluster_kernel(DecodeArgs a) {
+  pdl_enter();
+  cg::cluster_group cluster = cg::this_cluster();
+  __shared__ int hist[256];
+  __shared__ int all_hist[2][kTopkCluster][256];  // pushed by every block, one half per digit parity
+  __shared__ uint2 all_mm[kTopkCluster];           // every block's (smallest, largest) key
+  __shared__ uint2 warp_mm[kTopkThreads / 32];
+  __shared__ int sh_scan[32];
+  __shared__ uint32_t sh_prefix, sh_mask;
+  __shared__ int sh_remaining, sh_eq_count, sh_eq_before;
+  const int kvh = blockIdx.y, s = blockIdx.z;
+  const int rank = (int)cluster.block_rank();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // Every block of the cluster takes the same exits, so no cluster barrier
+  // is left waiting.
+  const int seq = seq_row(a.seq_ids, s, a.max_seqs, (rank == 0 && tid == 0) ? a.status : nullptr);
+  const int L = seq_len_clamped(a.seq_lens, seq, a.maxp, a.P, (rank == 0 && tid == 0) ? a.status : nullptr);
+  const int n = (L + a.P - 1) / a.P;
+  const int words = (n + 31) / 32;
+  const int chunk = ((words + kTopkCluster - 1) / kTopkCluster) * 32;
+  const int p_lo = rank * chunk, p_hi = min(n, p_lo + chunk);
+  uint32_t* bm = a.bitmap + ((size_t)s * a.Hkv + kvh) * a.words;
+  const int k = min(a.kpages, n);
+  if (k == n) {  // keep every page (also n = 0)
+    for (int p0 = p_lo + warp * 32; p0 < p_hi; p0 += kTopkThreads) {
+      const uint32_t bits = __ballot_sync(0xffffffffu, p0 + lane < p_hi);
+      if (lane == 0) bm[p0 >> 5] = bits;
+    }
+    return;
+  }
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;\n" ::: "memory");
+  const float* u = a.bbox_uhat + ((size_t)s * a.Hkv + kvh) * a.maxp;
+  uint32_t key[kTopkKpt];
+  uint32_t lo_k = 0xffffffffu, hi_k = 0u;
+#pragma unroll
+  for (int j = 0; j < kTopkKpt; ++j) {
+    const int p = p_lo + j * kTopkThreads + tid;
+    key[j] = p < p_hi ? ord_enc(__ldcg(u + p)) : 0u;
+  }
+#pragma unroll
+  for (int j = 0; j < kTopkKpt; ++j) {
+    if (p_lo + j * kTopkThreads + tid < p_hi) {
+      lo_k = min(lo_k, key[j]);
+      hi_k = max(hi_k, key[j]);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    lo_k = min(lo_k, __shfl_xor_sync(0xffffffffu, lo_k, o));
+    hi_k = max(hi_k, __shfl_xor_sync(0xffffffffu, hi_k, o));
+  }
+  if (lane == 0) warp_mm[warp] = make_uint2(lo_k, hi_k);
+  __syncthreads();
+  // every block of the cluster is running before the first push
+  asm volatile("barrier.cluster.wait.aligned;\n" ::: "memory");
+  if (warp == 0) {
+    uint2 m = warp_mm[lane];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      m.x = min(m.x, __shfl_xor_sync(0xffffffffu, m.x, o));
+      m.y = max(m.y, __shfl_xor_sync(0xffffffffu, m.y, o));
+    }
+    if (lane < kTopkCluster) cluster.map_shared_rank(&all_mm[0], lane)[rank] = m;
+  }
+  cluster.sync();
+  uint32_t kmin = 0xffffffffu, kmax = 0u;
+#pragma unroll
+  for (int r = 0; r < kTopkCluster; ++r) {
+    kmin = min(kmin, all_mm[r].x);
+    kmax = max(kmax, all_mm[r].y);
+  }
+  // Radix select of the k-th largest key, 8 bits a pass, below the leading
+  // bits that every key shares.
+  const int rb = (kmin ^ kmax) ? 32 - __clz((int)(kmin ^ kmax)) : 0;
+  uint32_t mask = rb >= 32 ? 0u : (0xffffffffu << rb);
+  uint32_t prefix = kmin & mask;
+  int remaining = k, eq_count = n, eq_before = min(p_lo, n);  // (all keys equal: every page ties)
+  int par = 0;
+  for (int sh = rb - 8; rb > 0; sh -= 8, par ^= 1) {
+    const int shift = sh > 0 ? sh : 0;  // the last digit may overlap the decided bits
+    if (tid < 256) hist[tid] = 0;
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < kTopkKpt; ++j)
+      if (p_lo + j * kTopkThreads + tid < p_hi && (key[j] & mask) == prefix)
+        atomicAdd(&hist[(key[j] >> shift) & 255u], 1);
+    __syncthreads();
+    // A half is rewritten two digits later, and no block gets there before
+    // every block has passed the next barrier, i.e. finished reading it.
+    for (int i = tid; i < 256 * kTopkCluster; i += kTopkThreads)
+      cluster.map_shared_rank(&all_hist[par][rank][0], i >> 8)[i & 255] = hist[i & 255];
+    cluster.sync();
+    if (warp == 0) {
+      // lane l owns digits 255−8l … 248−8l (descending); the lane where the
+      // count from the top reaches `remaining` walks its digits again
+      int tot = 0;
+#pragma unroll 2
+      for (int j = 0; j < 8; ++j)
+#pragma unroll
+        for (int r = 0; r < kTopkCluster; ++r) tot += all_hist[par][r][255 - 8 * lane - j];
+      int incl = tot;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const int excl = incl - tot;
+      if (excl < remaining && incl >= remaining) {
+        int run = excl;
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t digit = 255u - 8u * lane - j;
+          int c = 0, before = 0;
+          for (int r = 0; r < kTopkCluster; ++r) {
+            const int v = all_hist[par][r][digit];
+            c += v;
+            if (r < rank) before += v;
+          }
+          if (run + c >= remaining) {
+            sh_prefix = prefix | (digit << shift);
+            sh_mask = mask | (255u << shift);
+            sh_remaining = remaining - run;
+            sh_eq_count = c;
+            sh_eq_before = before;
+            break;
+          }
+          run += c;
+        }
+      }
+    }
+    __syncthreads();
+    prefix = sh_prefix;
+    mask = sh_mask;
+    remaining = sh_remaining;
+    eq_count = sh_eq_count;
+    eq_before = sh_eq_before;
+    if (shift == 0) break;
+  }
+  // T = prefix is the k-th largest key: keep every key > T and the
+  // `remaining` lowest-index pages with key == T (eq_before of them lie in
+  // the blocks below this one).
+  const uint32_t T = prefix;
+  const bool split_ties = eq_count > remaining;
+  int taken = eq_before;
+#pragma unroll
+  for (int j = 0; j < kTopkKpt; ++j) {
+    const int p0 = p_lo + j * kTopkThreads;
+    if (p0 >= p_hi) continue;  // block-uniform
+    const int p = p0 + tid;
+    const bool valid = p < p_hi;
+    bool sel = valid && key[j] > T;
+    const bool eq = valid && key[j] == T;
+    if (!split_ties) {
+      sel = sel || eq;
+    } else {
+      int tot;
+      const int before = block_exclusive_scan(eq ? 1 : 0, sh_scan, tot);
+      sel = sel || (eq && taken + before < remaining);
+      taken += tot;
+    }
+    const uint32_t bits = __ballot_sync(0xffffffffu, sel);
+    if (lane == 0 && p0 + warp * 32 < p_hi) bm[p >> 5] = bits;
+  }
+}
+
 cudaError_t launch_tauhat(const DecodeArgs& a, cudaStream_t st) {
   dim3 grid(kTauhatCluster, a.Hq, a.S);
   if (a.fit.orders) launch_k(false, tauhat_kernel<2>, dim3(grid), dim3(kThreads), 0, st, a);
@@ -559,6 +740,10 @@ cudaError_t launch_tauhat(const DecodeArgs& a, cudaStream_t st) {
 }
 
 cudaError_t launch_topk(const DecodeArgs& a, int mode, cudaStream_t st) {
+  if (mode == 0 && a.maxp <= kTopkClusterKeys) {
+    launch_k(false, topk_cluster_kernel, dim3(kTopkCluster, a.Hkv, a.S), dim3(kTopkThreads), 0, st, a);
+    return cudaGetLastError();
+  }
   dim3 grid(a.Hkv, a.S);
   const int smem = 4 * (a.maxp < kTopkKeys ? a.maxp : kTopkKeys);
   const cudaError_t e = ensure_smem((const void*)topk_kernel, smem);

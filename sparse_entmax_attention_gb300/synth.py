@@ -48,7 +48,7 @@ def _gen(device, *parts) -> torch.Generator:
     return g
 
 
-_Q, _KV, _STEPQ, _APPEND, _TABLE, _LENS = 1, 2, 3, 4, 5, 6
+_Q, _KV, _STEPQ, _APPEND, _TABLE, _LENS, _REPEAT = 1, 2, 3, 4, 5, 6, 7
 
 
 @dataclass
@@ -187,6 +187,21 @@ class HeadDraws:
 
     def needle_keys(self) -> torch.Tensor:
         return self.k[self.needle_pos].float()
+
+
+def repeated_pages(n_pages: int, page_size: int, head_dim: int, n_distinct: int,
+                   dtype=torch.bfloat16, seed: int = 0, device="cpu"):
+    """Keys and values of one KV head made of ``n_distinct`` random pages
+    (entries ~ N(0, I)), each logical page a copy of one of them picked at
+    random: pages with equal contents give exact ties in every per-page
+    bound and statistic. Returns (k, v), [n_pages·page_size, d] each."""
+    g = _gen(device, seed, _REPEAT, n_pages, n_distinct)
+    base_k = torch.randn(n_distinct, page_size, head_dim, generator=g, device=device)
+    base_v = torch.randn(n_distinct, page_size, head_dim, generator=g, device=device)
+    pick = torch.randint(0, n_distinct, (n_pages,), generator=g, device=device)
+    k = base_k[pick].reshape(n_pages * page_size, head_dim)
+    v = base_v[pick].reshape(n_pages * page_size, head_dim)
+    return k.to(dtype), v.to(dtype)
 
 
 def append_token(spec: Spec, b: int, j: int, pos: int, step: int, centroids,

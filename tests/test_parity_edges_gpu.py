@@ -153,3 +153,44 @@ def test_scorer_wait_timeout_is_flagged_and_the_context_stays_usable(meta_bf16):
     assert torch.all(torch.isnan(o.tau))
     check_decode(built, "gaussian", 1.5, 0, 0.5)
     assert c.read_status() == 0
+
+
+@pytest.mark.parametrize("n_pages,n_distinct,max_pages", [
+    (300, 3, None), (5000, 4, None), (2000, 1, None), (700, 3, 70000)])
+def test_topk_exact_ties_go_to_the_lower_page(n_pages, n_distinct, max_pages):
+    """Pages with equal contents have equal bounds, so the top-k boundary can
+    cut through a class of exact ties; the kept pages of that class must be
+    its lowest page indices, bit for bit (summary §2B.1, ties to the lower
+    index). 300 pages fall in 5 blocks of the cluster select and 5000 in all
+    8, so the tie offset crosses blocks; 2000 copies of one page make every
+    key equal (no radix digit at all); a table of 70000 pages per sequence
+    takes the one-block select."""
+    P, d, g = 16, 128, 4
+    spec = synth.custom(g, 1, d, P, [n_pages * P], torch.bfloat16, 1.5, shuffled_table=True)
+    bt, total, _ = synth.block_tables(spec)
+    maxp = max_pages or bt.shape[1]
+    cache = B.PagedCache(1, g, d, P, 1, maxp, total, torch.bfloat16, "cuda")
+    cache.block_table[:, : bt.shape[1]].copy_(bt.cuda())
+    k, v = synth.repeated_pages(n_pages, P, d, n_distinct)
+    B.append(cache, k[None, None].cuda().contiguous(), v[None, None].cuda().contiguous())
+    q = synth.queries(spec, 0).cuda()[None].contiguous()
+    K, V, Q = k.double().numpy(), v.double().numpy(), q[0].double().cpu().numpy()
+    meta = opg.page_metadata(K, P)
+    uhat = np.stack([opg.bbox_bound(Q[h], meta["kmin"], meta["kmax"]) for h in range(g)]).max(axis=0)
+    classes = np.unique(uhat)[::-1]
+    if classes.size == 1:
+        kp = n_pages // 3
+    else:  # through the middle of the second-largest class
+        kp = int((uhat > classes[1]).sum() + (uhat == classes[1]).sum() // 2)
+    assert 0 < kp < n_pages
+    o = B.decode(cache, q, 1.5, "topk", kp * P)
+    torch.cuda.synchronize()
+    # (equal pages give equal page maxima, which can fill the exact-τ
+    # candidate lists and send the solve down its full-scan path)
+    assert cache.device_status() & ~B.DEV_CAND_OVERFLOW == 0, hex(cache.device_status())
+    r = odec.decode_group(K, V, Q, 1.5, "topk", P, kp * P)
+    ids = o.page_ids[0, 0, : int(o.n_sel[0, 0])].cpu().tolist()
+    assert ids == list(r["page_ids"]) == list(opg.select_topk(uhat, kp))
+    for h in range(g):
+        assert rel_l2(o.out[0, h].cpu().numpy(), r["out"][h]) <= 2e-3
+        assert abs(float(o.tau[0, h]) - r["tau"][h]) <= 1e-4
