@@ -570,8 +570,9 @@ __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThre
     topk_cluster_kernel(DecodeArgs a) {
   pdl_enter();
   cg::cluster_group cluster = cg::this_cluster();
-  __shared__ int hist[256];
+  __shared__ int hist[2][256];                     // this block's histogram, one per digit parity
   __shared__ int all_hist[2][kTopkCluster][256];  // pushed by every block, one half per digit parity
+  __shared__ int tot_sh[256], bef_sh[256];         // per digit: cluster total, total in lower blocks
   __shared__ uint2 all_mm[kTopkCluster];           // every block's (smallest, largest) key
   __shared__ uint2 warp_mm[kTopkThreads / 32];
   __shared__ int sh_scan[32];
@@ -580,14 +581,25 @@ __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThre
   const int kvh = blockIdx.y, s = blockIdx.z;
   const int rank = (int)cluster.block_rank();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // The blocks split the table's row (max_pages_per_seq), so each block's key
+  // loads go out before the sequence length is known; keys past the length
+  // are masked afterwards.
+  const int chunk = (((a.maxp + 31) / 32 + kTopkCluster - 1) / kTopkCluster) * 32;
+  const int p_lo = rank * chunk;
+  const float* u = a.bbox_uhat + ((size_t)s * a.Hkv + kvh) * a.maxp;
+  uint32_t key[kTopkKpt];
+#pragma unroll
+  for (int j = 0; j < kTopkKpt; ++j) {
+    const int p = p_lo + j * kTopkThreads + tid;
+    key[j] = p < a.maxp ? ord_enc(__ldcg(u + p)) : 0u;
+  }
+  if (tid < 256) hist[0][tid] = hist[1][tid] = 0;
   // Every block of the cluster takes the same exits, so no cluster barrier
   // is left waiting.
   const int seq = seq_row(a.seq_ids, s, a.max_seqs, (rank == 0 && tid == 0) ? a.status : nullptr);
   const int L = seq_len_clamped(a.seq_lens, seq, a.maxp, a.P, (rank == 0 && tid == 0) ? a.status : nullptr);
   const int n = (L + a.P - 1) / a.P;
-  const int words = (n + 31) / 32;
-  const int chunk = ((words + kTopkCluster - 1) / kTopkCluster) * 32;
-  const int p_lo = rank * chunk, p_hi = min(n, p_lo + chunk);
+  const int p_hi = min(n, p_lo + chunk);
   uint32_t* bm = a.bitmap + ((size_t)s * a.Hkv + kvh) * a.words;
   const int k = min(a.kpages, n);
   if (k == n) {  // keep every page (also n = 0)
@@ -598,14 +610,7 @@ __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThre
     return;
   }
   asm volatile("barrier.cluster.arrive.relaxed.aligned;\n" ::: "memory");
-  const float* u = a.bbox_uhat + ((size_t)s * a.Hkv + kvh) * a.maxp;
-  uint32_t key[kTopkKpt];
   uint32_t lo_k = 0xffffffffu, hi_k = 0u;
-#pragma unroll
-  for (int j = 0; j < kTopkKpt; ++j) {
-    const int p = p_lo + j * kTopkThreads + tid;
-    key[j] = p < p_hi ? ord_enc(__ldcg(u + p)) : 0u;
-  }
 #pragma unroll
   for (int j = 0; j < kTopkKpt; ++j) {
     if (p_lo + j * kTopkThreads + tid < p_hi) {
@@ -647,26 +652,39 @@ __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThre
   int par = 0;
   for (int sh = rb - 8; rb > 0; sh -= 8, par ^= 1) {
     const int shift = sh > 0 ? sh : 0;  // the last digit may overlap the decided bits
-    if (tid < 256) hist[tid] = 0;
-    __syncthreads();
 #pragma unroll
     for (int j = 0; j < kTopkKpt; ++j)
       if (p_lo + j * kTopkThreads + tid < p_hi && (key[j] & mask) == prefix)
-        atomicAdd(&hist[(key[j] >> shift) & 255u], 1);
+        atomicAdd(&hist[par][(key[j] >> shift) & 255u], 1);
     __syncthreads();
-    // A half is rewritten two digits later, and no block gets there before
-    // every block has passed the next barrier, i.e. finished reading it.
+    // A half of all_hist is rewritten two digits later, and no block gets
+    // there before every block has passed the next barrier, i.e. finished
+    // reading it. The other local half was pushed before the last barrier,
+    // so it is cleared for the next digit now.
     for (int i = tid; i < 256 * kTopkCluster; i += kTopkThreads)
-      cluster.map_shared_rank(&all_hist[par][rank][0], i >> 8)[i & 255] = hist[i & 255];
+      cluster.map_shared_rank(&all_hist[par][rank][0], i >> 8)[i & 255] = hist[par][i & 255];
+    if (tid < 256) hist[par ^ 1][tid] = 0;
     cluster.sync();
-    if (warp == 0) {
-      // lane l owns digits 255−8l … 248−8l (descending); the lane where the
-      // count from the top reaches `remaining` walks its digits again
-      int tot = 0;
-#pragma unroll 2
-      for (int j = 0; j < 8; ++j)
+    if (tid < 256) {  // per digit: the cluster's count, and the count in the blocks below this one
+      int t = 0, b = 0;
 #pragma unroll
-        for (int r = 0; r < kTopkCluster; ++r) tot += all_hist[par][r][255 - 8 * lane - j];
+      for (int r = 0; r < kTopkCluster; ++r) {
+        const int v = all_hist[par][r][tid];
+        t += v;
+        b += r < rank ? v : 0;
+      }
+      tot_sh[tid] = t;
+      bef_sh[tid] = b;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // lane l owns digits 255−8l … 248−8l (descending)
+      int cnt[8], tot = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        cnt[j] = tot_sh[255 - 8 * lane - j];
+        tot += cnt[j];
+      }
       int incl = tot;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -675,25 +693,23 @@ __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThre
       }
       const int excl = incl - tot;
       if (excl < remaining && incl >= remaining) {
-        int run = excl;
-        for (int j = 0; j < 8; ++j) {
-          const uint32_t digit = 255u - 8u * lane - j;
-          int c = 0, before = 0;
-          for (int r = 0; r < kTopkCluster; ++r) {
-            const int v = all_hist[par][r][digit];
-            c += v;
-            if (r < rank) before += v;
+        int run = excl, jj = 7;
+#pragma unroll
+        for (int j = 7; j >= 0; --j) {  // the first digit (from the top) where the count reaches it
+          int before = excl;
+#pragma unroll
+          for (int i = 0; i < j; ++i) before += cnt[i];
+          if (before + cnt[j] >= remaining) {
+            jj = j;
+            run = before;
           }
-          if (run + c >= remaining) {
-            sh_prefix = prefix | (digit << shift);
-            sh_mask = mask | (255u << shift);
-            sh_remaining = remaining - run;
-            sh_eq_count = c;
-            sh_eq_before = before;
-            break;
-          }
-          run += c;
         }
+        const uint32_t digit = 255u - 8u * lane - jj;
+        sh_prefix = prefix | (digit << shift);
+        sh_mask = mask | (255u << shift);
+        sh_remaining = remaining - run;
+        sh_eq_count = tot_sh[digit];
+        sh_eq_before = bef_sh[digit];
       }
     }
     __syncthreads();
