@@ -18,7 +18,8 @@ constexpr int kThreads = 256;       // decode / scoring blocks: 8 warps
 constexpr int kWarps = kThreads / 32;
 constexpr int kSolveCap = 8192;     // candidate scores the τ solver keeps in shared memory
 constexpr int kListCap = 1024;      // selected pages one decode block handles
-constexpr int kTauhatCluster = 8;   // blocks per τ̂ cluster (one cluster per query head)
+constexpr int kTauhatCluster = 8;   // most blocks per τ̂ cluster (one cluster per query head)
+constexpr int kTauhatBlockPages = 4096;  // pages one τ̂ block keeps in registers (16 a thread)
 constexpr int kTopkCluster = 8;     // blocks per top-k cluster (one cluster per (sequence, KV head))
 
 // Chebyshev fits of J_ν(t) = E[(t + Z)_+^ν], Z ~ N(0, 1), for the Gaussian

@@ -705,7 +705,12 @@ int gauss_grid_x(int maxp, int Hkv, int S, int sms) {
   const int rows = ((Hkv + 7) / 8) * S;
   int gx = (groups + 7) / 8;
   if (sms > 0) {
-    const int cap = (2 * sms + rows - 1) / rows;
+    // One sequence: one wave of 2 blocks per SM. Several sequences, whose
+    // lengths differ: four waves' worth of blocks, each sequence's split
+    // evenly, so that the many blocks of the long ones spread over the SMs
+    // that the short ones leave early.
+    const int waves = S > 1 ? 8 : 2;
+    const int cap = (waves * sms + rows - 1) / rows;
     if (gx > cap) gx = cap;
   }
   return gx < 1 ? 1 : gx;

@@ -116,20 +116,20 @@ __device__ __forceinline__ void moments_x2(u64 mb, u64 sr, u64 ir, u64 nr, u64 n
 // a.fit, one page at a time; Newton steps when β ≤ 1, where F has no second
 // derivative).
 template <int MODE>
-__global__ void __cluster_dims__(kTauhatCluster, 1, 1) __launch_bounds__(kThreads, 2)
-    tauhat_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(kThreads, 2) tauhat_kernel(DecodeArgs a, int cls) {
   constexpr bool B2 = MODE == 1;
   pdl_enter();
   constexpr int kParts = kTauhatCluster * kWarps / 32;  // partials per lane after the exchange
   static_assert(kTauhatCluster * kWarps % 32 == 0, "whole partials per lane");
   cg::cluster_group cluster = cg::this_cluster();
   // Every warp of the cluster pushes its partial (F, D1, D2) into this slot
-  // of every block, so after the cluster barrier all reads are local.
+  // of every block, so after the cluster barrier all reads are local. The
+  // slots of ranks the cluster does not have stay zero.
   __shared__ float4 slot[2][kTauhatCluster * kWarps];
   __shared__ float wmax_sh[kWarps];
   const int h = blockIdx.y, s = blockIdx.z;
   const int kvh = h / a.G;
-  const int rank = (int)cluster.block_rank();
+  const int rank = (int)cluster.block_rank(), C = (int)cluster.num_blocks();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // Every block of a cluster takes the same early exits, so no cluster
   // barrier is ever left waiting.
@@ -137,17 +137,22 @@ __global__ void __cluster_dims__(kTauhatCluster, 1, 1) __launch_bounds__(kThread
   const int L = seq_len_clamped(a.seq_lens, seq, a.maxp, a.P, nullptr);
   const int n_pages = (L + a.P - 1) / a.P;
   if (n_pages == 0) return;
+  if ((cls == 1 && n_pages > kTauhatBlockPages) || (cls == 2 && n_pages <= kTauhatBlockPages)) return;
+  for (int i = tid; i < 2 * kTauhatCluster * kWarps; i += kThreads) {
+    const int e = i % (kTauhatCluster * kWarps);
+    if (e >= C * kWarps) slot[i / (kTauhatCluster * kWarps)][e] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  }
   const float2* ms = a.gauss_ms + ((size_t)s * a.Hq + h) * a.maxp;
   const int words = (n_pages + 31) / 32;
-  const int chunk = ((words + kTauhatCluster - 1) / kTauhatCluster) * 32;
+  const int chunk = ((words + C - 1) / C) * 32;
   const int p_lo = rank * chunk, p_hi = min(n_pages, p_lo + chunk);
 
   // This thread's pages stay in registers for every iteration (kRegPages
-  // each, which covers 8·256·kRegPages pages per query head), as pairs for
-  // the packed arithmetic; pages beyond that are re-read from memory. Their
-  // loads are issued before the maximum is known. An empty slot holds a
-  // finite page of zero weight far below every threshold.
-  constexpr int kRegPages = 16, kPairs = kRegPages / 2;
+  // each, which covers C·kTauhatBlockPages pages per query head), as pairs
+  // for the packed arithmetic; pages beyond that are re-read from memory.
+  // Their loads are issued before the maximum is known. An empty slot holds
+  // a finite page of zero weight far below every threshold.
+  constexpr int kRegPages = kTauhatBlockPages / kThreads, kPairs = kRegPages / 2;
   float mb[kRegPages], sr[kRegPages], nr[kRegPages];
 #pragma unroll
   for (int k = 0; k < kRegPages; ++k) {
@@ -254,7 +259,7 @@ __global__ void __cluster_dims__(kTauhatCluster, 1, 1) __launch_bounds__(kThread
     // iterations later, and no block gets there before every block has passed
     // the next barrier, i.e. finished reading it.
     if (it == 0) asm volatile("barrier.cluster.wait.aligned;\n" ::: "memory");
-    if (lane < kTauhatCluster)
+    if (lane < C)
       cluster.map_shared_rank(&slot[it & 1][0], lane)[rank * kWarps + warp] = make_float4(f, df, d2f, 0.0f);
     cluster.sync();
     float F = 0.0f, D1 = 0.0f, D2 = 0.0f;  // F, −dF/dτ, d²F/dτ²
@@ -747,12 +752,42 @@ __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThre
   }
 }
 
+// One launch of the τ̂ kernel with clusters of C blocks; cls selects the
+// sequences it solves (0 all, 1 those of at most kTauhatBlockPages pages,
+// 2 the longer ones).
+static cudaError_t launch_tauhat_c(const DecodeArgs& a, int C, int cls, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(C, a.Hq, a.S);
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (a.fit.orders) return cudaLaunchKernelEx(&cfg, tauhat_kernel<2>, a, cls);
+  if (a.beta == 2.0f) return cudaLaunchKernelEx(&cfg, tauhat_kernel<1>, a, cls);
+  return cudaLaunchKernelEx(&cfg, tauhat_kernel<0>, a, cls);
+}
+
+// A cluster holds the longest row's pages in its blocks' registers (up to
+// kTauhatCluster blocks). With several sequences and rows longer than one
+// block, the sequences that fit one block are solved by single-block
+// clusters in a launch of their own: a short sequence then takes one block
+// and no cluster barrier, instead of C blocks mostly without pages.
 cudaError_t launch_tauhat(const DecodeArgs& a, cudaStream_t st) {
-  dim3 grid(kTauhatCluster, a.Hq, a.S);
-  if (a.fit.orders) launch_k(false, tauhat_kernel<2>, dim3(grid), dim3(kThreads), 0, st, a);
-  else if (a.beta == 2.0f) launch_k(false, tauhat_kernel<1>, dim3(grid), dim3(kThreads), 0, st, a);
-  else launch_k(false, tauhat_kernel<0>, dim3(grid), dim3(kThreads), 0, st, a);
-  return cudaGetLastError();
+  int C = (a.maxp + kTauhatBlockPages - 1) / kTauhatBlockPages;
+  C = C < 1 ? 1 : (C > kTauhatCluster ? kTauhatCluster : C);
+  cudaError_t e;
+  if (a.S > 1 && C > 1) {
+    e = launch_tauhat_c(a, 1, 1, st);
+    if (e == cudaSuccess) e = launch_tauhat_c(a, C, 2, st);
+  } else {
+    e = launch_tauhat_c(a, C, 0, st);
+  }
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_topk(const DecodeArgs& a, int mode, cudaStream_t st) {
