@@ -402,6 +402,10 @@ static int32_t decode_impl(const entmaxkv_config* cfg, const entmaxkv_cache* cac
   a.delta_out = delta;
   bind_workspace(a, workspace, L);
   a.splits = launch_splits(L, n_seqs, cfg->num_kv_heads, policy, sms);
+  // The dry runs of pass A's tail only pay when the grid is one wave: with
+  // more, the tail's code is already in L2 by the time a last block runs it,
+  // and a dry run keeps a block from the next wave.
+  a.dry_tail = (long long)a.splits * cfg->num_kv_heads * n_seqs <= 2LL * sms;
   a.mslots = gauss_grid_x(cfg->max_pages_per_seq, cfg->num_kv_heads, n_seqs, sms);
 
   cudaStream_t s = (cudaStream_t)stream;
@@ -451,6 +455,7 @@ static int32_t decode_impl(const entmaxkv_config* cfg, const entmaxkv_cache* cac
     f.delta_out = nullptr;
     bind_workspace(f, ws2, LF);
     f.splits = launch_splits(LF, n_seqs, cfg->num_kv_heads, f.policy, sms);
+    f.dry_tail = (long long)f.splits * cfg->num_kv_heads * n_seqs <= 2LL * sms;
     f.mslots = 0;
     e = cudaMemsetAsync(ws2, 0, LF.ctrl_end, s);
     if (e == cudaSuccess) e = soft ? launch_softmax(f, dt, s) : launch_pass_a(f, dt, s);

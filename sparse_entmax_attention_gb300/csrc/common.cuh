@@ -47,6 +47,7 @@ struct DecodeArgs {
   // geometry
   int Hkv, G, Hq, D, P, maxp, nphys, max_seqs, S, words;
   int policy, splits, cap_pages, kpages, gcap;
+  int dry_tail;        // pass A's blocks that are not last warm the tail's code (one-wave grids)
   uint32_t flags;
   float alpha, a1, beta, zscale, inv_sqrt_d, margin_z;
   // cache

@@ -437,9 +437,9 @@ __global__ void __launch_bounds__(kThreads, 2) pass_a_kernel(DecodeArgs a) {
   // nothing to global memory. The tail runs once per decode, after the
   // scorer's stream has left none of its code in L2; the dry runs bring that
   // code into L2 (and into their SMs' instruction caches) before the last
-  // block needs it.
+  // block needs it. Grids of more than one wave skip them (a.dry_tail).
   const bool dry = !last_sh;
-  if (dry && a.cap_pages <= 0) return;
+  if (dry && (a.cap_pages <= 0 || !a.dry_tail)) return;
   __threadfence();
   // Exact τ of the G query heads, block-parallel:
   //  A  keep the listed candidate pages whose max clears T0 = z_max − 1
