@@ -5,6 +5,8 @@
 
 #include <atomic>
 
+#include <cudaTypedefs.h>
+
 #include "common.cuh"
 
 namespace ekv {
@@ -27,6 +29,36 @@ static int device_sms() {
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) return 0;
   g_sms[dev].store(n, std::memory_order_relaxed);
   return n;
+}
+
+// The driver's tensor-map encoder, looked up once through the runtime.
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static std::atomic<void*> fn{nullptr};
+  void* f = fn.load(std::memory_order_acquire);
+  if (f) return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !f)
+    return nullptr;
+  fn.store(f, std::memory_order_release);
+  return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+}
+
+// The bf16 V pool [nphys][Hkv][P][D] as a 3-D tensor (dim, KV head · token,
+// page) read in boxes of 64 dims × P tokens × 1 page with 128-byte swizzle:
+// one box per 64 dims of a (page, KV head) slab. The pool is 16-byte aligned
+// (checked with the cache).
+cudaError_t make_v_map(CUtensorMap* map, const void* v_pool, int nphys, int Hkv, int P, int D) {
+  const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hkv * P, (cuuint64_t)nphys};
+  const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)Hkv * P * D * 2};
+  const cuuint32_t box[3] = {64, (cuuint32_t)P, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(v_pool), dims, strides, box,
+                         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 struct Layout {

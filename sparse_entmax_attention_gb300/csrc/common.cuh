@@ -2,6 +2,7 @@
 // libentmaxkv kernels (sm_103a). Internal: not part of the C ABI.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -451,6 +452,43 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t si
       : "memory");
 }
 
+// Tiled tensor copies (TMA). A 3-D map over the V pool [page][KV head ·
+// token][dim] of bf16 moves one page's slab of a KV head as boxes of
+// P rows × 64 dims (128-byte rows, 128-byte swizzle: the 16-byte chunk c of
+// row t lands at chunk c ^ (t & 7)), so an ldmatrix over 8 rows of one chunk
+// column touches 8 different bank groups. The destination is 1024-byte
+// aligned; the box's x coordinate (0 or 64 dims) is 128-byte aligned.
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];\n" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+// Byte offset of 16-byte chunk c (0..7) of row t in a 128-byte-swizzled box.
+__device__ __forceinline__ uint32_t swz128(int t, int c) { return (uint32_t)(t * 128 + ((c ^ (t & 7)) << 4)); }
+// Four transposed 8×8 b16 tiles: lanes 8j..8j+7 give the row addresses of
+// tile j, and register j returns it, as mma's A or B fragments want it.
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3,
+                                              uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+// bf16 pair (lo in the low half) from two floats, rounded to nearest.
+__device__ __forceinline__ uint32_t bf2_rn(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+// x = hi + lo with hi = bf16(x) and lo = bf16(x − hi): 16 significant bits
+// of x, so a bf16 × bf16 product accumulated in fp32 sees x to about 2^-16.
+__device__ __forceinline__ void bf16_split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = bf2_rn(x0 - __low2float(h), x1 - __high2float(h));
+}
+
 // Packed fp32 pairs (two lanes of a 64-bit register) and the sm_100-family
 // paired FMA: d = a·b + c on both halves.
 __device__ __forceinline__ unsigned long long f2_pack(float lo, float hi) {
@@ -624,6 +662,8 @@ cudaError_t launch_gauss(const DecodeArgs& a, int kv_dtype, int sms, cudaStream_
 int gauss_grid_x(int maxp, int Hkv, int S, int sms);
 cudaError_t launch_tauhat(const DecodeArgs& a, cudaStream_t st);
 cudaError_t launch_topk(const DecodeArgs& a, int mode, cudaStream_t st);
+// The V pool's tensor map for pass B and the softmax kernel (bf16 pools).
+cudaError_t make_v_map(CUtensorMap* map, const void* v_pool, int nphys, int Hkv, int P, int D);
 cudaError_t launch_exact_delta(const DecodeArgs& m, const DecodeArgs& f, cudaStream_t st);
 cudaError_t launch_pass_a(const DecodeArgs& a, int kv_dtype, cudaStream_t st);
 cudaError_t launch_pass_b(const DecodeArgs& a, int kv_dtype, cudaStream_t st);

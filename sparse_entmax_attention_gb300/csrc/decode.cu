@@ -750,8 +750,10 @@ struct VTraits<__nv_bfloat16> {
 // all its V loads at once (lane: 16 bytes of a row, tokens tg, tg+TG, ...),
 // and accumulates p·v in fp32 registers.
 template <typename T, int D, int GP>
-__global__ void __launch_bounds__(kThreads, GP <= 4 ? 2 : 1) pass_b_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(kThreads, GP <= 4 ? 2 : 1)
+    pass_b_kernel(DecodeArgs a, const __grid_constant__ CUtensorMap vmap) {
   pdl_enter();
+  constexpr bool MMA = sizeof(T) == 2;           // bf16 pages: p·v on the tensor cores
   constexpr int VEC = VTraits<T>::VEC, LPR = D / VEC, TG = 32 / LPR;
   constexpr int MAXT = 32 / TG;                  // rows per lane in a 32-token page
   __shared__ double tau_sh[GP];
@@ -760,7 +762,9 @@ __global__ void __launch_bounds__(kThreads, GP <= 4 ? 2 : 1) pass_b_kernel(Decod
   __shared__ float dsum[kWarps][GP];
   __shared__ int list_sh[kListCap];
   __shared__ uint64_t vbar[kWarps];
-  extern __shared__ __align__(128) unsigned char vstage[];  // [kWarps][P][D] of T
+  // fp32: [kWarps][P][D]; bf16: [kWarps][D/64][P][128 B] swizzled boxes, from a
+  // 1024-byte boundary
+  extern __shared__ __align__(128) unsigned char vstage[];
   __shared__ int scan_sh[32];
   __shared__ int last_sh;
   const int split = blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
@@ -794,11 +798,16 @@ __global__ void __launch_bounds__(kThreads, GP <= 4 ? 2 : 1) pass_b_kernel(Decod
     taud[h] = tau_sh[h];
     tau[h] = (float)taud[h];
   }
-  unsigned long long accp[GP][VEC / 2];  // fp32 pairs of columns, for the paired FMA
+  unsigned long long accp[GP][VEC / 2];  // fp32: pairs of columns, for the paired FMA
 #pragma unroll
   for (int h = 0; h < GP; ++h)
 #pragma unroll
     for (int i = 0; i < VEC / 2; ++i) accp[h][i] = 0ull;
+  // bf16: out^T = V^T·p per m16n8k16 tile (16 dims × 8 heads, 16 tokens deep);
+  // lane l holds dims 16m + l/4 (+8) of heads 2(l%4), 2(l%4) + 1
+  float cacc[MMA ? D / 16 : 1][4];
+#pragma unroll
+  for (int m = 0; m < (MMA ? D / 16 : 1); ++m) cacc[m][0] = cacc[m][1] = cacc[m][2] = cacc[m][3] = 0.0f;
   float* zw = zs[warp];
 
   // One page: its V slab (P rows × D) arrives in this warp's shared buffer
@@ -806,7 +815,9 @@ __global__ void __launch_bounds__(kThreads, GP <= 4 ? 2 : 1) pass_b_kernel(Decod
   // to it, and a compact row loop accumulates p·v in fp32 (lane: VEC columns
   // of rows tg, tg+TG, ...). The loop is kept small on purpose: it runs once
   // per page, usually with cold instruction caches.
-  T* vbuf = reinterpret_cast<T*>(vstage) + (size_t)warp * P * D;
+  const uint32_t vs_base = (smem_u32(vstage) + 1023u) & ~1023u;
+  unsigned char* vbase = vstage + (vs_base - smem_u32(vstage));
+  T* vbuf = reinterpret_cast<T*>(MMA ? vbase : vstage) + (size_t)warp * P * D;
   if (lane == 0) {
     mbar_init(&vbar[warp], 1);
     mbar_fence_init();
@@ -820,7 +831,14 @@ __global__ void __launch_bounds__(kThreads, GP <= 4 ? 2 : 1) pass_b_kernel(Decod
     const uint32_t bytes = (uint32_t)(P * D * sizeof(T));
     if (lane == 0) {
       mbar_expect_tx(&vbar[warp], bytes);
-      bulk_g2s(vbuf, (const T*)a.v_pool + ((size_t)ph * a.Hkv + kvh) * P * D, bytes, &vbar[warp]);
+      if constexpr (MMA) {
+#pragma unroll
+        for (int hf = 0; hf < D / 64; ++hf)
+          tma_load_3d(reinterpret_cast<unsigned char*>(vbuf) + hf * P * 128, &vmap, 64 * hf, kvh * P, ph,
+                      &vbar[warp]);
+      } else {
+        bulk_g2s(vbuf, (const T*)a.v_pool + ((size_t)ph * a.Hkv + kvh) * P * D, bytes, &vbar[warp]);
+      }
     }
     const float* zb = a.z + (skv * a.cap_pages + rank) * (size_t)P * G;
 #pragma unroll
@@ -851,6 +869,41 @@ __global__ void __launch_bounds__(kThreads, GP <= 4 ? 2 : 1) pass_b_kernel(Decod
       return;
     }
     vphase ^= 1u;
+    if constexpr (MMA) {
+      unsigned char* vb = reinterpret_cast<unsigned char*>(vbuf);
+      if (nv < P) {  // token slots past the sequence's end: zero, so p = 0 meets no NaN
+        for (int e = lane; e < (D / 64) * (P - nv) * 8; e += 32) {
+          const int hf = e / ((P - nv) * 8), rem = e - hf * (P - nv) * 8;
+          *reinterpret_cast<uint4*>(vb + hf * P * 128 + (nv + rem / 8) * 128 + (rem % 8) * 16) =
+              make_uint4(0u, 0u, 0u, 0u);
+        }
+        __syncwarp();
+      }
+      const int c = lane & 3, r = lane >> 2;
+      const uint32_t vb_s = smem_u32(vb);
+#pragma unroll
+      for (int ks = 0; ks < P / 16; ++ks) {
+        // B = p (tokens × heads): tokens 16ks + 2c (+1) and +8, head r
+        const int t0 = 16 * ks + 2 * c;
+        const bool hv = r < G;
+        uint32_t bh0, bl0, bh1, bl1;
+        bf16_split2(hv ? zw[t0 * G + r] : 0.0f, hv ? zw[(t0 + 1) * G + r] : 0.0f, bh0, bl0);
+        bf16_split2(hv ? zw[(t0 + 8) * G + r] : 0.0f, hv ? zw[(t0 + 9) * G + r] : 0.0f, bh1, bl1);
+        // A = V^T (dims × tokens): lane i addresses token 16ks + i%8 (+8 for
+        // tiles 2, 3) in the 16-byte chunk of dims 16m (+8 for tiles 1, 3)
+        const int tr = 16 * ks + (lane & 7) + ((lane >> 4) << 3);
+#pragma unroll
+        for (int m = 0; m < D / 16; ++m) {
+          const int ch = 2 * m + ((lane >> 3) & 1);
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4_trans(a0, a1, a2, a3, vb_s + (ch >> 3) * P * 128 + swz128(tr, ch & 7));
+          mma_bf16(cacc[m], a0, a1, a2, a3, bh0, bh1);
+          mma_bf16(cacc[m], a0, a1, a2, a3, bl0, bl1);
+        }
+      }
+      __syncwarp();  // the buffer and zw are refilled for the next page
+      return;
+    }
     const T* vrow = vbuf + dc * VEC;
 #pragma unroll 2
     for (int u = 0; u < MAXT; ++u) {
@@ -989,17 +1042,32 @@ __global__ void __launch_bounds__(kThreads, GP <= 4 ? 2 : 1) pass_b_kernel(Decod
     }
     __syncwarp();
   }
+  if constexpr (MMA) {
+    const int c = lane & 3, r = lane >> 2;
 #pragma unroll
-  for (int o = LPR; o < 32; o <<= 1)
+    for (int m = 0; m < D / 16; ++m) {
+      if (2 * c < GP) {
+        red[warp][2 * c][16 * m + r] = cacc[m][0];
+        red[warp][2 * c][16 * m + r + 8] = cacc[m][2];
+      }
+      if (2 * c + 1 < GP) {
+        red[warp][2 * c + 1][16 * m + r] = cacc[m][1];
+        red[warp][2 * c + 1][16 * m + r + 8] = cacc[m][3];
+      }
+    }
+  } else {
 #pragma unroll
-    for (int h = 0; h < GP; ++h)
+    for (int o = LPR; o < 32; o <<= 1)
 #pragma unroll
-      for (int j = 0; j < VEC; ++j) acc[h][j] += __shfl_xor_sync(0xffffffffu, acc[h][j], o);
-  if (tg == 0) {
+      for (int h = 0; h < GP; ++h)
 #pragma unroll
-    for (int h = 0; h < GP; ++h)
+        for (int j = 0; j < VEC; ++j) acc[h][j] += __shfl_xor_sync(0xffffffffu, acc[h][j], o);
+    if (tg == 0) {
 #pragma unroll
-      for (int j = 0; j < VEC; ++j) red[warp][h][dc * VEC + j] = acc[h][j];
+      for (int h = 0; h < GP; ++h)
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) red[warp][h][dc * VEC + j] = acc[h][j];
+    }
   }
   // top-k: this block's share of the certified dropped mass
   if (a.policy == ENTMAXKV_POLICY_TOPK) {
@@ -1150,29 +1218,38 @@ cudaError_t launch_pass_a(const DecodeArgs& a, int kv_dtype, cudaStream_t st) {
 }
 
 template <typename T, int D, int GP>
-static cudaError_t pass_b_launch(const DecodeArgs& a, dim3 grid, cudaStream_t st) {
-  const int smem = kWarps * a.P * D * (int)sizeof(T);  // one V slab per warp
-  const cudaError_t e = ensure_smem((const void*)pass_b_kernel<T, D, GP>, kWarps * 32 * D * (int)sizeof(T));
+static cudaError_t pass_b_launch(const DecodeArgs& a, const CUtensorMap& vmap, dim3 grid, cudaStream_t st) {
+  // one V slab per warp (bf16: plus the slack that aligns the boxes to 1024 bytes)
+  constexpr int slack = sizeof(T) == 2 ? 1024 : 0;
+  const int smem = kWarps * a.P * D * (int)sizeof(T) + slack;
+  const cudaError_t e =
+      ensure_smem((const void*)pass_b_kernel<T, D, GP>, kWarps * 32 * D * (int)sizeof(T) + slack);
   if (e != cudaSuccess) return e;
-  launch_k(false, pass_b_kernel<T, D, GP>, dim3(grid), dim3(kThreads), smem, st, a);
+  launch_k(false, pass_b_kernel<T, D, GP>, dim3(grid), dim3(kThreads), smem, st, a, vmap);
   return cudaGetLastError();
 }
 
 template <typename T, int D>
-static cudaError_t pass_b_g(const DecodeArgs& a, dim3 grid, cudaStream_t st) {
+static cudaError_t pass_b_g(const DecodeArgs& a, const CUtensorMap& vmap, dim3 grid, cudaStream_t st) {
   switch (pick_gp(a.G)) {
-    case 1: return pass_b_launch<T, D, 1>(a, grid, st);
-    case 2: return pass_b_launch<T, D, 2>(a, grid, st);
-    case 4: return pass_b_launch<T, D, 4>(a, grid, st);
-    default: return pass_b_launch<T, D, 8>(a, grid, st);
+    case 1: return pass_b_launch<T, D, 1>(a, vmap, grid, st);
+    case 2: return pass_b_launch<T, D, 2>(a, vmap, grid, st);
+    case 4: return pass_b_launch<T, D, 4>(a, vmap, grid, st);
+    default: return pass_b_launch<T, D, 8>(a, vmap, grid, st);
   }
 }
 
 cudaError_t launch_pass_b(const DecodeArgs& a, int kv_dtype, cudaStream_t st) {
   dim3 grid(a.splits, a.Hkv, a.S);
-  if (kv_dtype == ENTMAXKV_BF16)
-    return a.D == 128 ? pass_b_g<__nv_bfloat16, 128>(a, grid, st) : pass_b_g<__nv_bfloat16, 64>(a, grid, st);
-  return a.D == 128 ? pass_b_g<float, 128>(a, grid, st) : pass_b_g<float, 64>(a, grid, st);
+  CUtensorMap vmap;
+  memset(&vmap, 0, sizeof(vmap));
+  if (kv_dtype == ENTMAXKV_BF16) {
+    const cudaError_t e = make_v_map(&vmap, a.v_pool, a.nphys, a.Hkv, a.P, a.D);
+    if (e != cudaSuccess) return e;
+    return a.D == 128 ? pass_b_g<__nv_bfloat16, 128>(a, vmap, grid, st)
+                      : pass_b_g<__nv_bfloat16, 64>(a, vmap, grid, st);
+  }
+  return a.D == 128 ? pass_b_g<float, 128>(a, vmap, grid, st) : pass_b_g<float, 64>(a, vmap, grid, st);
 }
 
 }  // namespace ekv
