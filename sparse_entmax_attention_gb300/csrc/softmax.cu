@@ -22,8 +22,10 @@
 namespace ekv {
 
 template <typename T, int D, int GP>
-__global__ void __launch_bounds__(kThreads, 2) softmax_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(kThreads, 2)
+    softmax_kernel(DecodeArgs a, const __grid_constant__ CUtensorMap vmap) {
   pdl_enter();
+  constexpr bool MMA = sizeof(T) == 2;  // bf16 pages: p·v on the tensor cores
   constexpr int VEC = 16 / sizeof(T), LPR = D / VEC, TG = 32 / LPR;
   constexpr int MAXT = 32 / TG;                  // tokens per lane in a 32-token page
   constexpr int CH = MAXT < 8 ? MAXT : 8;        // V rows in flight per lane
@@ -44,7 +46,9 @@ __global__ void __launch_bounds__(kThreads, 2) softmax_kernel(DecodeArgs a) {
   __shared__ int sh_scan[32];
   __shared__ int last_sh;
   __shared__ uint64_t vbar[kWarps];
-  extern __shared__ __align__(128) unsigned char vstage_sm[];  // bf16: [kWarps][P][D], a V slab per warp
+  // bf16: a V slab per warp, [kWarps][D/64][P][128 B] swizzled boxes from a
+  // 1024-byte boundary
+  extern __shared__ __align__(128) unsigned char vstage_sm[];
   const int split = blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = a.G, P = a.P;
@@ -69,19 +73,30 @@ __global__ void __launch_bounds__(kThreads, 2) softmax_kernel(DecodeArgs a) {
     for (int i = tid; i < G * D; i += kThreads) qs[i / D][i % D] = ((const float*)a.q)[hq0 * D + i];
     __syncthreads();
   }
-  float m[GP], l[GP], acc[GP][VEC];
+  float m[GP], l[GP], acc[MMA ? 1 : GP][VEC];
 #pragma unroll
   for (int h = 0; h < GP; ++h) {
     m[h] = -CUDART_INF_F;
     l[h] = 0.0f;
+  }
+#pragma unroll
+  for (int h = 0; h < (MMA ? 1 : GP); ++h)
 #pragma unroll
     for (int j = 0; j < VEC; ++j) acc[h][j] = 0.0f;
-  }
+  // bf16: out^T = V^T·p per m16n8k16 tile (16 dims × 8 heads, 16 tokens deep);
+  // lane l holds dims 16m + l/4 (+8) of heads 2(l%4), 2(l%4) + 1, and the
+  // running sum of p for head l/4 over its tokens
+  float cacc[MMA ? D / 16 : 1][4];
+#pragma unroll
+  for (int mt = 0; mt < (MMA ? D / 16 : 1); ++mt) cacc[mt][0] = cacc[mt][1] = cacc[mt][2] = cacc[mt][3] = 0.0f;
+  float lpart = 0.0f;
+  const int cq = lane & 3, rq = lane >> 2;
   // bf16 pages: the V slab is requested by one bulk copy into the warp's
   // buffer before the page's scores are computed, so its transfer overlaps
   // the K loads and the scores, and the weighted sum reads it from shared
   // memory (no V registers in flight)
-  T* vbuf = reinterpret_cast<T*>(vstage_sm) + (size_t)warp * P * D;
+  const uint32_t vs_base = (smem_u32(vstage_sm) + 1023u) & ~1023u;
+  T* vbuf = reinterpret_cast<T*>(vstage_sm + (vs_base - smem_u32(vstage_sm))) + (size_t)warp * P * D;
   uint32_t vphase = 0u;
   bool stuck = false;
   if constexpr (sizeof(T) == 2) {
@@ -101,7 +116,10 @@ __global__ void __launch_bounds__(kThreads, 2) softmax_kernel(DecodeArgs a) {
       if (lane == 0) {
         const uint32_t bytes = (uint32_t)(P * D * sizeof(T));
         mbar_expect_tx(&vbar[warp], bytes);
-        bulk_g2s(vbuf, (const T*)a.v_pool + slab_off, bytes, &vbar[warp]);
+#pragma unroll
+        for (int hf = 0; hf < D / 64; ++hf)
+          tma_load_3d(reinterpret_cast<unsigned char*>(vbuf) + hf * P * 128, &vmap, 64 * hf, kvh * P, ph,
+                      &vbar[warp]);
       }
     }
     if constexpr (sizeof(T) == 2) {
@@ -156,79 +174,121 @@ __global__ void __launch_bounds__(kThreads, 2) softmax_kernel(DecodeArgs a) {
       }
     }
     __syncwarp();
+    if constexpr (MMA) {
+      // rescale: the lane's p sum is of head rq, its accumulators of heads 2cq, 2cq + 1
+      float s_r = 1.0f, s_0 = 1.0f, s_1 = 1.0f;
 #pragma unroll
-    for (int h = 0; h < GP; ++h) {
-      const float mn = fmaxf(m[h], h < G ? pmx[warp][h] : -CUDART_INF_F);
-      if (mn > m[h]) {
-        const float sc = exp2f(m[h] - mn);  // 0 when m was −inf
-        l[h] *= sc;
-#pragma unroll
-        for (int j = 0; j < VEC; ++j) acc[h][j] *= sc;
-        m[h] = mn;
+      for (int h = 0; h < GP; ++h) {
+        const float mn = fmaxf(m[h], h < G ? pmx[warp][h] : -CUDART_INF_F);
+        if (mn > m[h]) {
+          const float sc = exp2f(m[h] - mn);  // 0 when m was −inf
+          if (h == rq) s_r = sc;
+          if (h == 2 * cq) s_0 = sc;
+          if (h == 2 * cq + 1) s_1 = sc;
+          m[h] = mn;
+        }
       }
-    }
-    if constexpr (sizeof(T) == 2) {
+      lpart *= s_r;
+#pragma unroll
+      for (int mt = 0; mt < D / 16; ++mt) {
+        cacc[mt][0] *= s_0;
+        cacc[mt][2] *= s_0;
+        cacc[mt][1] *= s_1;
+        cacc[mt][3] *= s_1;
+      }
+      float m_r = -CUDART_INF_F;
+#pragma unroll
+      for (int h = 0; h < GP; ++h)
+        if (h == rq) m_r = m[h];
       if (!__all_sync(0xffffffffu, mbar_wait_bounded(&vbar[warp], vphase))) {
         stuck = true;
         break;
       }
       vphase ^= 1u;
-      const T* vrow = vbuf + dc * VEC;
-#pragma unroll 4
-      for (int u = 0; u < MAXT; ++u) {
-        const int t = tg + TG * u;
-        if (t < nv) {
-          const uint4 raw = *reinterpret_cast<const uint4*>(vrow + (size_t)t * D);
-          float v[VEC];
-          v[0] = bf_lo(raw.x); v[1] = bf_hi(raw.x); v[2] = bf_lo(raw.y); v[3] = bf_hi(raw.y);
-          v[4] = bf_lo(raw.z); v[5] = bf_hi(raw.z); v[6] = bf_lo(raw.w); v[7] = bf_hi(raw.w);
+      unsigned char* vb = reinterpret_cast<unsigned char*>(vbuf);
+      if (nv < P) {  // token slots past the sequence's end: zero, so p = 0 meets no NaN
+        for (int e = lane; e < (D / 64) * (P - nv) * 8; e += 32) {
+          const int hf = e / ((P - nv) * 8), rem = e - hf * (P - nv) * 8;
+          *reinterpret_cast<uint4*>(vb + hf * P * 128 + (nv + rem / 8) * 128 + (rem % 8) * 16) =
+              make_uint4(0u, 0u, 0u, 0u);
+        }
+        __syncwarp();
+      }
+      // p = 2^(s − m) of tokens 16ks + 2cq (+1) and +8 for head rq (0 for
+      // padding heads, heads without a finite max and invalid tokens)
+      const bool hv = rq < G && m_r > -CUDART_INF_F;
+      const uint32_t vb_s = smem_u32(vb);
 #pragma unroll
-          for (int h = 0; h < GP; ++h) {
-            if (h < G && m[h] > -CUDART_INF_F) {
-              const float p = exp2f(sbuf[warp][t][h] - m[h]);
-              l[h] += p;
+      for (int ks = 0; ks < P / 16; ++ks) {
+        const int t0 = 16 * ks + 2 * cq;
+        const int hs = rq < GP ? rq : 0;
+        const float p0 = hv ? exp2f(sbuf[warp][t0][hs] - m_r) : 0.0f;
+        const float p1 = hv ? exp2f(sbuf[warp][t0 + 1][hs] - m_r) : 0.0f;
+        const float p2 = hv ? exp2f(sbuf[warp][t0 + 8][hs] - m_r) : 0.0f;
+        const float p3 = hv ? exp2f(sbuf[warp][t0 + 9][hs] - m_r) : 0.0f;
+        lpart += (p0 + p1) + (p2 + p3);
+        uint32_t bh0, bl0, bh1, bl1;
+        bf16_split2(p0, p1, bh0, bl0);
+        bf16_split2(p2, p3, bh1, bl1);
+        const int tr = 16 * ks + (lane & 7) + ((lane >> 4) << 3);
 #pragma unroll
-              for (int j = 0; j < VEC; ++j) acc[h][j] = fmaf(p, v[j], acc[h][j]);
-            }
-          }
+        for (int mt = 0; mt < D / 16; ++mt) {
+          const int ch = 2 * mt + ((lane >> 3) & 1);
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4_trans(a0, a1, a2, a3, vb_s + (ch >> 3) * P * 128 + swz128(tr, ch & 7));
+          mma_bf16(cacc[mt], a0, a1, a2, a3, bh0, bh1);
+          mma_bf16(cacc[mt], a0, a1, a2, a3, bl0, bl1);
         }
       }
       __syncwarp();  // the buffer is refilled for the next page
       continue;
     }
-    const T* vs = (const T*)a.v_pool + slab_off + dc * VEC;
-    for (int c0 = 0; c0 < MAXT; c0 += CH) {
-      uint4 raw[CH];
-#pragma unroll
-      for (int u = 0; u < CH; ++u) {
-        const int t = tg + TG * (c0 + u);
-        raw[u] = t < nv ? ld_stream(vs + (size_t)t * D) : make_uint4(0u, 0u, 0u, 0u);
+    if constexpr (!MMA) {  // fp32 pages: p·v in fp32 on the CUDA cores
+  #pragma unroll
+      for (int h = 0; h < GP; ++h) {
+        const float mn = fmaxf(m[h], h < G ? pmx[warp][h] : -CUDART_INF_F);
+        if (mn > m[h]) {
+          const float sc = exp2f(m[h] - mn);  // 0 when m was −inf
+          l[h] *= sc;
+  #pragma unroll
+          for (int j = 0; j < VEC; ++j) acc[h][j] *= sc;
+          m[h] = mn;
+        }
       }
-#pragma unroll
-      for (int u = 0; u < CH; ++u) {
-        const int t = tg + TG * (c0 + u);
-        if (t < nv) {
-          float v[VEC];
-          if constexpr (sizeof(T) == 2) {
-            v[0] = bf_lo(raw[u].x); v[1] = bf_hi(raw[u].x); v[2] = bf_lo(raw[u].y); v[3] = bf_hi(raw[u].y);
-            v[4] = bf_lo(raw[u].z); v[5] = bf_hi(raw[u].z); v[6] = bf_lo(raw[u].w); v[7] = bf_hi(raw[u].w);
-          } else {
-            v[0] = __uint_as_float(raw[u].x); v[1] = __uint_as_float(raw[u].y);
-            v[2] = __uint_as_float(raw[u].z); v[3] = __uint_as_float(raw[u].w);
-          }
-#pragma unroll
-          for (int h = 0; h < GP; ++h) {
-            if (h < G && m[h] > -CUDART_INF_F) {
-              const float p = exp2f(sbuf[warp][t][h] - m[h]);
-              l[h] += p;
-#pragma unroll
-              for (int j = 0; j < VEC; ++j) acc[h][j] = fmaf(p, v[j], acc[h][j]);
+      const T* vs = (const T*)a.v_pool + slab_off + dc * VEC;
+      for (int c0 = 0; c0 < MAXT; c0 += CH) {
+        uint4 raw[CH];
+  #pragma unroll
+        for (int u = 0; u < CH; ++u) {
+          const int t = tg + TG * (c0 + u);
+          raw[u] = t < nv ? ld_stream(vs + (size_t)t * D) : make_uint4(0u, 0u, 0u, 0u);
+        }
+  #pragma unroll
+        for (int u = 0; u < CH; ++u) {
+          const int t = tg + TG * (c0 + u);
+          if (t < nv) {
+            float v[VEC];
+            if constexpr (sizeof(T) == 2) {
+              v[0] = bf_lo(raw[u].x); v[1] = bf_hi(raw[u].x); v[2] = bf_lo(raw[u].y); v[3] = bf_hi(raw[u].y);
+              v[4] = bf_lo(raw[u].z); v[5] = bf_hi(raw[u].z); v[6] = bf_lo(raw[u].w); v[7] = bf_hi(raw[u].w);
+            } else {
+              v[0] = __uint_as_float(raw[u].x); v[1] = __uint_as_float(raw[u].y);
+              v[2] = __uint_as_float(raw[u].z); v[3] = __uint_as_float(raw[u].w);
+            }
+  #pragma unroll
+            for (int h = 0; h < GP; ++h) {
+              if (h < G && m[h] > -CUDART_INF_F) {
+                const float p = exp2f(sbuf[warp][t][h] - m[h]);
+                l[h] += p;
+  #pragma unroll
+                for (int j = 0; j < VEC; ++j) acc[h][j] = fmaf(p, v[j], acc[h][j]);
+              }
             }
           }
         }
       }
+      __syncwarp();
     }
-    __syncwarp();
   }
   if (stuck) {  // a copy did not arrive within the bound: flag it, let it land, stop
     if (lane == 0) {
@@ -237,26 +297,49 @@ __global__ void __launch_bounds__(kThreads, 2) softmax_kernel(DecodeArgs a) {
     }
     __syncwarp();
   }
+  if constexpr (MMA) {
+    // head rq's p sum: over the four lanes of its tokens
+    lpart += __shfl_xor_sync(0xffffffffu, lpart, 1);
+    lpart += __shfl_xor_sync(0xffffffffu, lpart, 2);
+    __syncthreads();  // every warp is done with qs and sbuf
 #pragma unroll
-  for (int o = LPR; o < 32; o <<= 1)
-#pragma unroll
-    for (int h = 0; h < GP; ++h) {
-      l[h] += __shfl_xor_sync(0xffffffffu, l[h], o);
-#pragma unroll
-      for (int j = 0; j < VEC; ++j) acc[h][j] += __shfl_xor_sync(0xffffffffu, acc[h][j], o);
+    for (int mt = 0; mt < D / 16; ++mt) {
+      if (2 * cq < GP) {
+        red[warp][2 * cq][16 * mt + rq] = cacc[mt][0];
+        red[warp][2 * cq][16 * mt + rq + 8] = cacc[mt][2];
+      }
+      if (2 * cq + 1 < GP) {
+        red[warp][2 * cq + 1][16 * mt + rq] = cacc[mt][1];
+        red[warp][2 * cq + 1][16 * mt + rq + 8] = cacc[mt][3];
+      }
     }
-  __syncthreads();  // every warp is done with qs and sbuf
-  if (tg == 0) {
+    if (cq == 0 && rq < GP) wl_sh[warp][rq] = lpart;
+    if (lane == 0) {
 #pragma unroll
-    for (int h = 0; h < GP; ++h)
+      for (int h = 0; h < GP; ++h) wm_sh[warp][h] = m[h];
+    }
+  } else {
 #pragma unroll
-      for (int j = 0; j < VEC; ++j) red[warp][h][dc * VEC + j] = acc[h][j];
-  }
-  if (lane == 0) {
+    for (int o = LPR; o < 32; o <<= 1)
 #pragma unroll
-    for (int h = 0; h < GP; ++h) {
-      wm_sh[warp][h] = m[h];
-      wl_sh[warp][h] = l[h];
+      for (int h = 0; h < GP; ++h) {
+        l[h] += __shfl_xor_sync(0xffffffffu, l[h], o);
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) acc[h][j] += __shfl_xor_sync(0xffffffffu, acc[h][j], o);
+      }
+    __syncthreads();  // every warp is done with qs and sbuf
+    if (tg == 0) {
+#pragma unroll
+      for (int h = 0; h < GP; ++h)
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) red[warp][h][dc * VEC + j] = acc[h][j];
+    }
+    if (lane == 0) {
+#pragma unroll
+      for (int h = 0; h < GP; ++h) {
+        wm_sh[warp][h] = m[h];
+        wl_sh[warp][h] = l[h];
+      }
     }
   }
   if (bitmap) {  // this block's share of all pages: the dropped ones' Σ n_p·e^{U_p}, online
@@ -404,32 +487,38 @@ __global__ void __launch_bounds__(kThreads, 2) softmax_kernel(DecodeArgs a) {
 }
 
 template <typename T, int D, int GP>
-static void softmax_l(const DecodeArgs& a, dim3 grid, cudaStream_t st) {
-  // bf16: a V slab per warp in dynamic shared memory
-  const int smem = sizeof(T) == 2 ? kWarps * a.P * D * (int)sizeof(T) : 0;
-  if (smem && ensure_smem((const void*)softmax_kernel<T, D, GP>, smem) != cudaSuccess)
-    return;
-  launch_k(false, softmax_kernel<T, D, GP>, dim3(grid), dim3(kThreads), (size_t)smem, st, a);
+static cudaError_t softmax_l(const DecodeArgs& a, const CUtensorMap& vmap, dim3 grid, cudaStream_t st) {
+  // bf16: a V slab per warp in dynamic shared memory, plus the slack that
+  // aligns the boxes to 1024 bytes
+  const int smem = sizeof(T) == 2 ? kWarps * a.P * D * (int)sizeof(T) + 1024 : 0;
+  if (smem) {
+    const cudaError_t e = ensure_smem((const void*)softmax_kernel<T, D, GP>, smem);
+    if (e != cudaSuccess) return e;
+  }
+  return launch_k(false, softmax_kernel<T, D, GP>, dim3(grid), dim3(kThreads), (size_t)smem, st, a, vmap);
 }
 
 template <typename T, int D>
-static void softmax_g(const DecodeArgs& a, dim3 grid, cudaStream_t st) {
-  if (a.G <= 1) softmax_l<T, D, 1>(a, grid, st);
-  else if (a.G <= 2) softmax_l<T, D, 2>(a, grid, st);
-  else if (a.G <= 4) softmax_l<T, D, 4>(a, grid, st);
-  else softmax_l<T, D, 8>(a, grid, st);
+static cudaError_t softmax_g(const DecodeArgs& a, const CUtensorMap& vmap, dim3 grid, cudaStream_t st) {
+  if (a.G <= 1) return softmax_l<T, D, 1>(a, vmap, grid, st);
+  if (a.G <= 2) return softmax_l<T, D, 2>(a, vmap, grid, st);
+  if (a.G <= 4) return softmax_l<T, D, 4>(a, vmap, grid, st);
+  return softmax_l<T, D, 8>(a, vmap, grid, st);
 }
 
 cudaError_t launch_softmax(const DecodeArgs& a, int kv_dtype, cudaStream_t st) {
   dim3 grid(a.splits, a.Hkv, a.S);
+  CUtensorMap vmap;
+  memset(&vmap, 0, sizeof(vmap));
+  cudaError_t e;
   if (kv_dtype == ENTMAXKV_BF16) {
-    if (a.D == 128) softmax_g<__nv_bfloat16, 128>(a, grid, st);
-    else softmax_g<__nv_bfloat16, 64>(a, grid, st);
+    e = make_v_map(&vmap, a.v_pool, a.nphys, a.Hkv, a.P, a.D);
+    if (e != cudaSuccess) return e;
+    e = a.D == 128 ? softmax_g<__nv_bfloat16, 128>(a, vmap, grid, st) : softmax_g<__nv_bfloat16, 64>(a, vmap, grid, st);
   } else {
-    if (a.D == 128) softmax_g<float, 128>(a, grid, st);
-    else softmax_g<float, 64>(a, grid, st);
+    e = a.D == 128 ? softmax_g<float, 128>(a, vmap, grid, st) : softmax_g<float, 64>(a, vmap, grid, st);
   }
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace ekv
