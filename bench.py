@@ -36,7 +36,7 @@ L2_FLUSH_BYTES = 512 << 20   # > 129 MB L2: read between timed steps
 # DRAM bytes (read + write) of one launch of the dominant kernel on this
 # workload, from an ncu capture of the bench command itself (no scaling);
 # reset to None whenever that kernel changes.
-NCU_TRAFFIC_PER_LAUNCH = 134624512 + 6006272
+NCU_TRAFFIC_PER_LAUNCH = 134591744 + 5172992
 
 
 def measured_peaks():
