@@ -352,18 +352,32 @@ __global__ void __launch_bounds__(kThreads, 2)
     const uint32_t* bm = a.bitmap + skv * a.words;
     const int plo = (int)(((long long)n_pages * split) / a.splits);
     const int phi = (int)(((long long)n_pages * (split + 1)) / a.splits);
-    for (int p = plo + tid; p < phi; p += kThreads) {
-      if ((bm[p >> 5] >> (p & 31)) & 1u) continue;
-      const float np = (float)min(P, L - p * P);
+    // four pages a thread per round, their bitmap words and bounds loaded together
+    for (int p0 = plo + tid; p0 < phi; p0 += 4 * kThreads) {
+      uint32_t w[4];
+      float uu[4][GP];
 #pragma unroll
-      for (int h = 0; h < GP; ++h) {
-        if (h < G) {
-          const float u = a.bbox_u[(hq0 + h) * a.maxp + p];
-          if (u > um[h]) {
-            us[h] = us[h] * expf(um[h] - u) + np;
-            um[h] = u;
-          } else {
-            us[h] += np * expf(u - um[h]);
+      for (int j = 0; j < 4; ++j) {
+        const int p = p0 + j * kThreads;
+        w[j] = p < phi ? bm[p >> 5] : 0xffffffffu;
+#pragma unroll
+        for (int h = 0; h < GP; ++h) uu[j][h] = (p < phi && h < G) ? a.bbox_u[(hq0 + h) * a.maxp + p] : 0.0f;
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int p = p0 + j * kThreads;
+        if (p >= phi || ((w[j] >> (p & 31)) & 1u)) continue;  // kept pages drop nothing
+        const float np = (float)min(P, L - p * P);
+#pragma unroll
+        for (int h = 0; h < GP; ++h) {
+          if (h < G) {
+            const float u = uu[j][h];
+            if (u > um[h]) {
+              us[h] = us[h] * expf(um[h] - u) + np;
+              um[h] = u;
+            } else {
+              us[h] += np * expf(u - um[h]);
+            }
           }
         }
       }
