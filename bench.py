@@ -166,7 +166,7 @@ def run_ours(args, rank, world):
     dev = torch.device("cuda", local)
     K, W = args.steps, args.warmup
     spec = synth.workload(WORKLOAD)
-    n_append = 2 * (K + W) + 4
+    n_append = 4 * (K + W) + 8  # the timed steps, then the eager and the captured e2e steps
     wl = runner.Workload(spec, seed=0, device=dev, extra_steps=n_append, meta_bf16=True)
     cache = wl.cache
     peaks, peak_kind = measured_peaks()
@@ -441,20 +441,21 @@ def roofline(wl, B, flush, qbuf, K, peaks, peak_kind):
 
 def e2e(wl, B, toks, qs, n_app, K, W):
     """Same step through the public API from pinned host buffers: H2D of the
-    new token and the queries, append + decode, D2H of out/τ/δ/n_sel."""
+    new token and the queries, append + decode, D2H of out/τ/δ/n_sel. The
+    value is the library's captured serving step (`B.DecodeStep`: the
+    launches replayed from a CUDA graph); `eager` is the same step by one
+    API call per operation."""
     import torch
     cache, spec = wl.cache, wl.spec
-    hk = [toks[n_app[0] + i][0].cpu().pin_memory() for i in range(K + W)]
-    hv = [toks[n_app[0] + i][1].cpu().pin_memory() for i in range(K + W)]
-    hq = [qs[i % len(qs)].cpu().pin_memory() for i in range(K + W)]
+    hk = [toks[n_app[0] + i][0].cpu().pin_memory() for i in range(2 * (K + W))]
+    hv = [toks[n_app[0] + i][1].cpu().pin_memory() for i in range(2 * (K + W))]
+    hq = [qs[i % len(qs)].cpu().pin_memory() for i in range(2 * (K + W))]
     dk, dv, dq = hk[0].cuda(), hv[0].cuda(), hq[0].cuda()
     ws = B.alloc_workspace(cache, spec.batch, "gaussian", 0)
     o = B.alloc_outputs(cache, spec.batch, "gaussian", 0)
     ho = [torch.empty_like(t, device="cpu").pin_memory() for t in (o.out, o.tau, o.delta, o.n_sel)]
-    us = []
-    for i in range(K + W):
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
+
+    def eager(i):
         dk.copy_(hk[i], non_blocking=True)
         dv.copy_(hv[i], non_blocking=True)
         dq.copy_(hq[i], non_blocking=True)
@@ -462,15 +463,33 @@ def e2e(wl, B, toks, qs, n_app, K, W):
         B.decode(cache, dq, ALPHA, "gaussian", 0, MARGIN, workspace=ws, outputs=o)
         for h, d in zip(ho, (o.out, o.tau, o.delta, o.n_sel)):
             h.copy_(d, non_blocking=True)
-        b.record()
-        b.synchronize()
-        if i >= W:
-            us.append(a.elapsed_time(b) * 1e3)
+
+    step = B.DecodeStep(cache, spec.batch, ALPHA, "gaussian", 0, MARGIN)
+
+    def captured(i):
+        step.run(hk[i], hv[i], hq[i], host_outputs=ho)
+
+    def timed(fn, i0):
+        us = []
+        for i in range(K + W):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn(i0 + i)
+            b.record()
+            b.synchronize()
+            if i >= W:
+                us.append(a.elapsed_time(b) * 1e3)
+        return statistics.mean(us)
+
+    v_eager = timed(eager, 0)
+    v_graph = timed(captured, K + W)
     h2d = sum(t.numel() * t.element_size() for t in (hk[0], hv[0], hq[0]))
     d2h = sum(t.numel() * t.element_size() for t in ho)
-    return {"value": round(statistics.mean(us), 2), "unit": "us/step",
+    return {"value": round(v_graph, 2), "unit": "us/step",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "how": "per-step CUDA events around H2D + append + decode + D2H (eager API calls)"}
+            "eager": round(v_eager, 2),
+            "how": "per-step CUDA events around H2D + append + decode + D2H; value: the captured "
+                   "serving step (DecodeStep.run), eager: one API call per operation"}
 
 
 # --------------------------------------------------------------------------
@@ -809,7 +828,7 @@ def reference_inputs(K, W):
     from oracle import pages as opg
     from sparse_entmax_attention_gb300 import synth
     spec = synth.workload(WORKLOAD)
-    n_append = 2 * (K + W) + 4
+    n_append = 4 * (K + W) + 8  # the timed steps, then the eager and the captured e2e steps
     spec = synth.Spec(**{**spec.__dict__, "steps": n_append, "append_per_step": True})
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     q = synth.queries(spec, 0, 0, dev)

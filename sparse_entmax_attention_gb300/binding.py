@@ -283,6 +283,46 @@ def decode(cache: PagedCache, q, alpha=1.5, policy="gaussian", budget_tokens=0, 
     return o
 
 
+class DecodeStep:
+    """One serving step, append one token per sequence and decode, captured
+    once as a CUDA graph of the library's launches over fixed device
+    buffers. `run` copies the step's new keys, values and queries in (from
+    pinned host memory or device tensors), replays the graph and returns the
+    outputs; `host_outputs` optionally receives them by asynchronous copies.
+    The capture launches nothing: the cache changes only when `run` replays.
+    Arguments as for `append` and `decode`; k and v are [n_seqs, Hkv, 1, d]."""
+
+    def __init__(self, cache: PagedCache, n_seqs, alpha=1.5, policy="gaussian", budget_tokens=0,
+                 margin=0.0, flags=0, seq_ids=None):
+        dev, d = cache.device, cache.cfg.head_dim
+        self.cache = cache
+        self.k = torch.zeros(n_seqs, cache.cfg.num_kv_heads, 1, d, dtype=cache.dtype, device=dev)
+        self.v = torch.zeros_like(self.k)
+        self.q = torch.zeros(n_seqs, cache.num_q_heads, d, dtype=cache.dtype, device=dev)
+        self.workspace = alloc_workspace(cache, n_seqs, policy, budget_tokens, flags)
+        self.outputs = alloc_outputs(cache, n_seqs, policy, budget_tokens)
+        args = (alpha, policy, budget_tokens, margin, flags)
+        # one decode outside the capture: first-launch set-up (shared-memory
+        # attributes, moment fits) happens here, and no token is appended
+        decode(cache, self.q, *args, seq_ids=seq_ids, workspace=self.workspace, outputs=self.outputs)
+        torch.cuda.synchronize(dev)
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            append(cache, self.k, self.v, seq_ids=seq_ids)
+            decode(cache, self.q, *args, seq_ids=seq_ids, workspace=self.workspace, outputs=self.outputs)
+
+    def run(self, k, v, q, host_outputs=None) -> DecodeOutputs:
+        self.k.copy_(k, non_blocking=True)
+        self.v.copy_(v, non_blocking=True)
+        self.q.copy_(q, non_blocking=True)
+        self.graph.replay()
+        if host_outputs is not None:
+            o = self.outputs
+            for h, t in zip(host_outputs, (o.out, o.tau, o.delta, o.n_sel)):
+                h.copy_(t, non_blocking=True)
+        return self.outputs
+
+
 def stage_events():
     """STAGE_EVENTS timing events with their CUDA handles already created."""
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(STAGE_EVENTS)]

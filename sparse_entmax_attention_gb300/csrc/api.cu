@@ -122,6 +122,10 @@ static int compute_layout(const entmaxkv_config* c, int S, int policy, int budge
   L.cap_pages = cap;
   const long long units = (long long)S * Hkv;
   long long splits = (cap + 7) / 8;
+  // entmax top-k's pass B also sums the certified dropped-mass bound over
+  // every page of the row: at least 512 pages of that per block (not for
+  // softmax top-k, whose last block merges one partial per split)
+  if (policy == ENTMAXKV_POLICY_TOPK && splits < (maxp + 511) / 512) splits = (maxp + 511) / 512;
   long long tgt = (kLayoutBlocks + units - 1) / units;
   if (splits > tgt) splits = tgt;
   const bool bitmap = topk || policy == ENTMAXKV_POLICY_GAUSSIAN;
@@ -231,6 +235,8 @@ static size_t total_bytes(const entmaxkv_config* c, int S, int policy, int budge
 static int launch_splits(const Layout& L, int S, int Hkv, int policy, int sms) {
   const long long units = (long long)S * Hkv;
   long long splits = (L.cap_pages + 7) / 8;
+  const long long row = 32LL * L.words;  // the table's row, rounded up to a bitmap word
+  if (policy == ENTMAXKV_POLICY_TOPK && splits < (row + 511) / 512) splits = (row + 511) / 512;  // (as in the layout)
   const long long tgt = (2LL * sms + units - 1) / units;
   if (splits > tgt) splits = tgt;
   const bool bitmap = policy == ENTMAXKV_POLICY_TOPK || policy == ENTMAXKV_POLICY_SOFTMAX_TOPK ||

@@ -254,3 +254,27 @@ def test_exact_tau_general_alpha(small_bf16, small_f32, alpha, policy, budget):
     so the solve keeps a bracket)."""
     check_decode(small_bf16, policy, alpha, budget)
     check_decode(small_f32, policy, alpha, budget)
+
+
+# The tensor-core weighted sums (TMA-staged V, p·v as out^T = V^T·p) at the
+# shapes they specialise on: d = 64 (one swizzled box per slab), groups of 1
+# and 2 query heads (padding heads in the MMA tile), pages of 16 and 32.
+@pytest.fixture(scope="module")
+def small_bf16_d64_g2():
+    spec = synth.custom(4, 2, 64, 32, [2345, 700], torch.bfloat16, 1.5, n_needles=4, n_outliers=2,
+                        shuffled_table=True)
+    return Built(spec)
+
+
+@pytest.fixture(scope="module")
+def small_bf16_g1_p16():
+    spec = synth.custom(2, 2, 128, 16, [1500], torch.bfloat16, 1.5, n_needles=3)
+    return Built(spec)
+
+
+@pytest.mark.parametrize("policy,budget,margin,flags", [
+    ("full", 0, 0.0, 0), ("full", 0, 0.0, B.FLAG_DENSE_V), ("softmax", 0, 0.0, 0),
+    ("topk", 256, 0.0, 0), ("softmax_topk", 256, 0.0, 0), ("gaussian", 0, 0.5, 0)])
+def test_decode_bf16_tensor_core_shapes(small_bf16_d64_g2, small_bf16_g1_p16, policy, budget, margin, flags):
+    for built in (small_bf16_d64_g2, small_bf16_g1_p16):
+        check_decode(built, policy, 1.5, budget, margin, flags=flags)
