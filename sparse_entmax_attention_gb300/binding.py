@@ -285,42 +285,96 @@ def decode(cache: PagedCache, q, alpha=1.5, policy="gaussian", budget_tokens=0, 
 
 class DecodeStep:
     """One serving step, append one token per sequence and decode, captured
-    once as a CUDA graph of the library's launches over fixed device
-    buffers. `run` copies the step's new keys, values and queries in (from
-    pinned host memory or device tensors), replays the graph and returns the
-    outputs; `host_outputs` optionally receives them by asynchronous copies.
-    The capture launches nothing: the cache changes only when `run` replays.
-    Arguments as for `append` and `decode`; k and v are [n_seqs, Hkv, 1, d]."""
+    once as CUDA graphs of the library's launches over fixed buffers.
+
+    `run(k, v, q)` takes device tensors: it copies them into the step's
+    buffers and replays the launches. `run_host(k, v, q)` takes host tensors:
+    they are copied into one pinned staging buffer, and a second graph moves
+    them to the device in one copy, runs the launches and returns out, τ, δ
+    and n_sel to pinned host memory in one copy; it returns those host views
+    once the step is done. Capturing launches nothing: the cache changes only
+    on replay. Arguments as for `append` and `decode`; k and v are
+    [n_seqs, Hkv, 1, d], q is [n_seqs, Hq, d]."""
 
     def __init__(self, cache: PagedCache, n_seqs, alpha=1.5, policy="gaussian", budget_tokens=0,
                  margin=0.0, flags=0, seq_ids=None):
         dev, d = cache.device, cache.cfg.head_dim
         self.cache = cache
-        self.k = torch.zeros(n_seqs, cache.cfg.num_kv_heads, 1, d, dtype=cache.dtype, device=dev)
-        self.v = torch.zeros_like(self.k)
-        self.q = torch.zeros(n_seqs, cache.num_q_heads, d, dtype=cache.dtype, device=dev)
+        Hkv, Hq = cache.cfg.num_kv_heads, cache.num_q_heads
+        el = torch.tensor([], dtype=cache.dtype).element_size()
+        shapes_in = [(n_seqs, Hkv, 1, d), (n_seqs, Hkv, 1, d), (n_seqs, Hq, d)]
+        n_in = [int(torch.Size(sh).numel()) * el for sh in shapes_in]
+        self.dev_in = torch.zeros(sum(n_in), dtype=torch.uint8, device=dev)
+        self.host_in = torch.zeros(sum(n_in), dtype=torch.uint8).pin_memory()
+
+        def views(buf):
+            out, off = [], 0
+            for sh, n in zip(shapes_in, n_in):
+                out.append(buf[off:off + n].view(cache.dtype).view(sh))
+                off += n
+            return out
+
+        self.k, self.v, self.q = views(self.dev_in)
+        self._hk, self._hv, self._hq = views(self.host_in)
+        # outputs: out, τ, δ, n_sel packed in one buffer (one copy back); page ids apart
+        cap = page_capacity(cache, policy, budget_tokens)
+        shapes_out = [((n_seqs, Hq, d), torch.float32), ((n_seqs, Hq), torch.float32),
+                      ((n_seqs, Hq), torch.float32), ((n_seqs, Hkv), torch.int32)]
+        n_out = [int(torch.Size(sh).numel()) * 4 for sh, _ in shapes_out]
+        self.dev_out = torch.zeros(sum(n_out), dtype=torch.uint8, device=dev)
+        self.host_out = torch.zeros(sum(n_out), dtype=torch.uint8).pin_memory()
+
+        def out_views(buf):
+            res, off = [], 0
+            for (sh, dt), n in zip(shapes_out, n_out):
+                res.append(buf[off:off + n].view(dt).view(sh))
+                off += n
+            return res
+
+        out, tau, delta, n_sel = out_views(self.dev_out)
+        self.outputs = DecodeOutputs(out=out, tau=tau, delta=delta, n_sel=n_sel,
+                                     page_ids=torch.full((n_seqs, Hkv, cap), -1, dtype=torch.int32, device=dev))
+        self.host_outputs = out_views(self.host_out)
         self.workspace = alloc_workspace(cache, n_seqs, policy, budget_tokens, flags)
-        self.outputs = alloc_outputs(cache, n_seqs, policy, budget_tokens)
         args = (alpha, policy, budget_tokens, margin, flags)
-        # one decode outside the capture: first-launch set-up (shared-memory
+
+        def launches():
+            append(cache, self.k, self.v, seq_ids=seq_ids)
+            decode(cache, self.q, *args, seq_ids=seq_ids, workspace=self.workspace, outputs=self.outputs)
+
+        # one decode outside the captures: first-launch set-up (shared-memory
         # attributes, moment fits) happens here, and no token is appended
         decode(cache, self.q, *args, seq_ids=seq_ids, workspace=self.workspace, outputs=self.outputs)
         torch.cuda.synchronize(dev)
         self.graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(self.graph):
-            append(cache, self.k, self.v, seq_ids=seq_ids)
-            decode(cache, self.q, *args, seq_ids=seq_ids, workspace=self.workspace, outputs=self.outputs)
+            launches()
+        self.graph_io = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph_io):
+            self.dev_in.copy_(self.host_in, non_blocking=True)
+            launches()
+            self.host_out.copy_(self.dev_out, non_blocking=True)
 
-    def run(self, k, v, q, host_outputs=None) -> DecodeOutputs:
+    def run(self, k, v, q) -> DecodeOutputs:
+        """Device tensors in; the outputs stay on the device."""
         self.k.copy_(k, non_blocking=True)
         self.v.copy_(v, non_blocking=True)
         self.q.copy_(q, non_blocking=True)
         self.graph.replay()
-        if host_outputs is not None:
-            o = self.outputs
-            for h, t in zip(host_outputs, (o.out, o.tau, o.delta, o.n_sel)):
-                h.copy_(t, non_blocking=True)
         return self.outputs
+
+    def run_host(self, k, v, q, wait=True):
+        """Host tensors in; returns (out, τ, δ, n_sel) as pinned host tensors.
+        With wait=True the call returns once the step has finished; with
+        wait=False the caller synchronises the current stream before reading
+        them (and before the next call reuses the staging buffer)."""
+        self._hk.copy_(k)
+        self._hv.copy_(v)
+        self._hq.copy_(q)
+        self.graph_io.replay()
+        if wait:
+            torch.cuda.current_stream(self.cache.device).synchronize()
+        return self.host_outputs
 
 
 def stage_events():

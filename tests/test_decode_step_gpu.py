@@ -38,3 +38,27 @@ def test_captured_step_matches_eager_calls(policy, budget, margin):
         torch.testing.assert_close(eb.tau, ea.tau, rtol=1e-5, atol=1e-6)
     assert a.cache.device_status() & ~B.DEV_CAND_OVERFLOW == 0
     assert b.cache.device_status() & ~B.DEV_CAND_OVERFLOW == 0
+
+
+def test_captured_step_with_host_io_matches_eager_calls():
+    """run_host: host tensors in, one H2D and one D2H inside the step's graph."""
+    spec = synth.custom(8, 2, 128, 32, [3000, 1217], torch.bfloat16, 1.5, n_needles=3, steps=4,
+                        append_per_step=True)
+    a = runner.Workload(spec, device="cuda", meta_bf16=True)
+    b = runner.Workload(spec, device="cuda", meta_bf16=True)
+    step = B.DecodeStep(b.cache, spec.batch, 1.5, "gaussian", 0, 0.5)
+    ws = B.alloc_workspace(a.cache, spec.batch, "gaussian")
+    o = B.alloc_outputs(a.cache, spec.batch, "gaussian")
+    for i in range(3):
+        k, v = a.step_tokens(i)
+        q = a.step_queries(i)
+        B.append(a.cache, k, v)
+        ea = B.decode(a.cache, q, 1.5, "gaussian", 0, 0.5, workspace=ws, outputs=o)
+        out, tau, delta, n_sel = step.run_host(k.cpu(), v.cpu(), q.cpu())
+        torch.cuda.synchronize()
+        assert torch.equal(a.cache.seq_lens, b.cache.seq_lens)
+        assert torch.equal(n_sel, ea.n_sel.cpu())
+        torch.testing.assert_close(out, ea.out.cpu(), rtol=1e-5, atol=1e-6)
+        torch.testing.assert_close(tau, ea.tau.cpu(), rtol=1e-5, atol=1e-6)
+        torch.testing.assert_close(delta, ea.delta.cpu(), rtol=1e-5, atol=1e-6)
+    assert b.cache.device_status() & ~B.DEV_CAND_OVERFLOW == 0
