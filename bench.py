@@ -352,12 +352,19 @@ def dropped_mass(wl, B, qbuf):
     import torch
     cache, spec = wl.cache, wl.spec
     res = {"budget_tokens": TOPK_BUDGET}
+    kinds = {B.DELTA_CERTIFIED: "certified bound", B.DELTA_MODEL: "model estimate", B.DELTA_EXACT: "exact"}
     for name, pol, budget in (("entmax_topk", "topk", TOPK_BUDGET),
                               ("softmax_topk", "softmax_topk", TOPK_BUDGET), ("gaussian", "gaussian", 0)):
         o = B.decode(cache, qbuf, ALPHA, pol, budget, MARGIN, B.FLAG_EXACT_DELTA)
         torch.cuda.synchronize()
         dl = o.delta.float().cpu()
+        # the δ a decode returns without the flag, beside the exact one
+        r = B.decode(cache, qbuf, ALPHA, pol, budget, MARGIN)
+        torch.cuda.synchronize()
+        dr = r.delta.float().cpu()
         res[name] = {"mean": round(float(dl.mean()), 5), "max": round(float(dl.max()), 5),
+                     "reported_kind": kinds.get(B.delta_kind(pol), "?"),
+                     "reported_mean": round(float(dr.mean()), 5), "reported_max": round(float(dr.max()), 5),
                      "pages_per_kv_head": round(float(o.n_sel.float().mean()), 1)}
     return res
 
