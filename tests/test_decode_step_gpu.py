@@ -11,6 +11,12 @@ from sparse_entmax_attention_gb300 import runner, synth
 pytestmark = pytest.mark.gpu
 
 
+def _close_per_head(got, want, tol=1e-5):
+    g, w = got.double().cpu(), want.double().cpu()
+    err = (g - w).norm(dim=-1) / w.norm(dim=-1).clamp_min(1e-30)
+    assert float(err.max()) <= tol, float(err.max())
+
+
 @pytest.mark.parametrize("policy,budget,margin", [("gaussian", 0, 0.5), ("topk", 256, 0.0)])
 def test_captured_step_matches_eager_calls(policy, budget, margin):
     spec = synth.custom(8, 2, 128, 32, [3000, 1217], torch.bfloat16, 1.5, n_needles=3, steps=4,
@@ -33,8 +39,10 @@ def test_captured_step_matches_eager_calls(policy, budget, margin):
             for j in range(spec.num_kv_heads):
                 n = int(ea.n_sel[s, j])
                 assert torch.equal(ea.page_ids[s, j, :n], eb.page_ids[s, j, :n])
-        # the output and τ are summed with float atomics, in the order blocks finish
-        torch.testing.assert_close(eb.out, ea.out, rtol=1e-5, atol=1e-6)
+        # the output is summed with float atomics in the order blocks finish:
+        # each head's output vector agrees in relative L2 (single entries
+        # near zero can differ by a few ulps of the larger terms)
+        _close_per_head(eb.out, ea.out)
         torch.testing.assert_close(eb.tau, ea.tau, rtol=1e-5, atol=1e-6)
     assert a.cache.device_status() & ~B.DEV_CAND_OVERFLOW == 0
     assert b.cache.device_status() & ~B.DEV_CAND_OVERFLOW == 0
@@ -58,7 +66,7 @@ def test_captured_step_with_host_io_matches_eager_calls():
         torch.cuda.synchronize()
         assert torch.equal(a.cache.seq_lens, b.cache.seq_lens)
         assert torch.equal(n_sel, ea.n_sel.cpu())
-        torch.testing.assert_close(out, ea.out.cpu(), rtol=1e-5, atol=1e-6)
+        _close_per_head(out, ea.out.cpu())
         torch.testing.assert_close(tau, ea.tau.cpu(), rtol=1e-5, atol=1e-6)
         torch.testing.assert_close(delta, ea.delta.cpu(), rtol=1e-5, atol=1e-6)
     assert b.cache.device_status() & ~B.DEV_CAND_OVERFLOW == 0
