@@ -237,12 +237,14 @@ static int launch_splits(const Layout& L, int S, int Hkv, int policy, int sms) {
   long long splits = (L.cap_pages + 7) / 8;
   const long long row = 32LL * L.words;  // the table's row, rounded up to a bitmap word
   if (policy == ENTMAXKV_POLICY_TOPK && splits < (row + 511) / 512) splits = (row + 511) / 512;  // (as in the layout)
-  const long long tgt = (2LL * sms + units - 1) / units;
+  // one wave of 2 blocks per SM; two waves' worth when several sequences
+  // (of unequal lengths) share the launch
+  const long long tgt = ((S > 1 ? 4LL : 2LL) * sms + units - 1) / units;
   if (splits > tgt) splits = tgt;
-  const bool bitmap = policy == ENTMAXKV_POLICY_TOPK || policy == ENTMAXKV_POLICY_SOFTMAX_TOPK ||
-                      policy == ENTMAXKV_POLICY_GAUSSIAN;
+  // The softmax kernel's page list must hold a block's whole share of the
+  // top-k selection; pass A's continues in the global selection list.
   const long long need = (L.cap_pages + kListCap - 1) / kListCap;
-  if (bitmap && splits < need) splits = need;
+  if (policy == ENTMAXKV_POLICY_SOFTMAX_TOPK && splits < need) splits = need;
   if (splits > L.splits) splits = L.splits;
   return splits < 1 ? 1 : (int)splits;
 }

@@ -615,9 +615,12 @@ __device__ __forceinline__ bool uses_bitmap(int policy) {
 }
 
 // This block's share [lo, hi) of the n_sel selected pages; for bitmap
-// policies the page ids of that share go to list[0 .. hi−lo).
+// policies the page ids of that share go to list[0 .. hi−lo), the ranks
+// past kListCap of a longer share to spill[rank] (none without spill: the
+// caller's split count keeps its shares within kListCap).
 __device__ __forceinline__ void block_page_range(const DecodeArgs& a, int s, int kvh, int n_pages, int split,
-                                 int* list, int* sh_scan, int& n_sel, int& lo, int& hi) {
+                                 int* list, int* sh_scan, int& n_sel, int& lo, int& hi,
+                                 int* spill = nullptr) {
   if (!uses_bitmap(a.policy)) {
     n_sel = n_pages;
     lo = (int)(((long long)n_sel * split) / a.splits);
@@ -644,7 +647,10 @@ __device__ __forceinline__ void block_page_range(const DecodeArgs& a, int s, int
     uint32_t bits = bm[w0 + j];
     while (bits) {
       const int b = __ffs(bits) - 1;
-      if (r >= lo && r < hi) list[r - lo] = (w0 + j) * 32 + b;
+      if (r >= lo && r < hi) {
+        if (r - lo < kListCap) list[r - lo] = (w0 + j) * 32 + b;
+        else if (spill) spill[r] = (w0 + j) * 32 + b;
+      }
       ++r;
       bits &= bits - 1u;
     }

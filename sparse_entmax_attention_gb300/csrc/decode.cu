@@ -235,8 +235,12 @@ __global__ void __launch_bounds__(kThreads, 2) pass_a_kernel(DecodeArgs a) {
     for (int i = tid; i < G * D; i += kThreads) qs[i / D][i % D] = ((const float*)a.q)[hq0 * D + i];
   }
   int n_sel, lo, hi;
-  block_page_range(a, s, kvh, n_pages, split, list, sh_scan, n_sel, lo, hi);
+  // a share longer than the list continues in the selection's global list
+  int* spill = uses_bitmap(a.policy) ? a.sel_list + (size_t)s * a.Hkv * a.cap_pages + (size_t)kvh * a.cap_pages
+                                     : nullptr;
+  block_page_range(a, s, kvh, n_pages, split, list, sh_scan, n_sel, lo, hi, spill);
   const bool bitmap = uses_bitmap(a.policy);
+  auto page_of = [&](int i) { return i < kListCap ? list[i] : spill[lo + i]; };
   const bool beta2 = a.beta == 2.0f;
   const bool gauss = a.policy == ENTMAXKV_POLICY_GAUSSIAN;
   if (split == 0 && a.out)  // pass B adds its blocks' sums into these rows
@@ -260,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 2) pass_a_kernel(DecodeArgs a) {
   const int GI = gauss ? G : 1;
   for (int e = tid; e < (hi - lo) * GI; e += kThreads) {
     const int i = e / GI, h = e - i * GI;
-    const int page = bitmap ? list[i] : lo + i;
+    const int page = bitmap ? page_of(i) : lo + i;
     float2 v = make_float2(0.0f, 0.0f);
     float th = 0.0f;
     if (gauss) {  // summary §2B.2: 1 − kept model mass estimates the dropped mass δ
@@ -290,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 2) pass_a_kernel(DecodeArgs a) {
   for (int h = 0; h < 8; ++h) wm[h] = -CUDART_INF_F;
   for (int i = warp; i < hi - lo; i += kWarps) {
     const int rank = lo + i;
-    const int page = bitmap ? list[i] : rank;
+    const int page = bitmap ? page_of(i) : rank;
     const int ph = staged ? phys_sh[i] : phys_page(a.block_table, seq, page, a.maxp, a.nphys, lane == 0 ? a.status : nullptr);
     if (staged && lane == 0 && i + kAhead * kWarps < hi - lo) {
       const int ph_next = phys_sh[i + kAhead * kWarps];

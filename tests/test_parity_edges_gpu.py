@@ -194,3 +194,17 @@ def test_topk_exact_ties_go_to_the_lower_page(n_pages, n_distinct, max_pages):
     for h in range(g):
         assert rel_l2(o.out[0, h].cpu().numpy(), r["out"][h]) <= 2e-3
         assert abs(float(o.tau[0, h]) - r["tau"][h]) <= 1e-4
+
+
+def test_pass_a_share_longer_than_its_page_list():
+    """256 (sequence, KV head) units of 3100 pages each, top-k keeping all but
+    one page: a multi-sequence launch gives each unit 3 blocks on a 152-SM
+    GPU, so a block's share (1033 pages) runs past its 1024-entry page list
+    and continues in the global selection list. Ids, output and τ against the
+    oracle on sampled units."""
+    P, n_pages = 16, 3100
+    spec = synth.custom(32, 32, 64, P, [n_pages * P] * 8, torch.bfloat16, 1.5, n_needles=2)
+    built = Built(spec)
+    budget = (n_pages - 1) * P
+    check_decode(built, "topk", 1.5, budget, 0.0, units=[(0, 0), (3, 17), (7, 31)])
+    check_decode(built, "gaussian", 1.5, 0, 2.0, units=[(5, 9)])
