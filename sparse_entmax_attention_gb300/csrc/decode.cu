@@ -14,11 +14,13 @@
 //           as candidates. The last block to finish solves the exact τ of each
 //           query head from the candidates (one warp per head).
 //   pass B  gathers V only for pages with some z above τ (all pages for the
-//           dense baseline), accumulates Σ p_i v_i with p_i = [z_i − τ]_+^β in
-//           fp32, and adds each block's sums into the output rows (zeroed
-//           by pass A) with vector float atomics; the order of those
-//           additions, and so the last bits of the output, vary from run to
-//           run.
+//           dense baseline), accumulates Σ p_i v_i with p_i = [z_i − τ]_+^β
+//           (bf16: V by TMA tensor copies into swizzled shared memory and
+//           out^T = V^T·p on the tensor cores, p split into bf16 hi + lo;
+//           fp32: CUDA-core FMA), and adds each block's sums into the output
+//           rows (zeroed by pass A) with vector float atomics; the order of
+//           those additions, and so the last bits of the output, vary from
+//           run to run.
 // Exact τ: τ solves Σ_i [z_i − τ]_+^β = 1. Starting from τ = z_max − 1
 // (where the sum is ≥ 1) Newton steps on this convex decreasing function stay
 // below the root; after each step the closed-form root on the current support
@@ -750,9 +752,11 @@ struct VTraits<__nv_bfloat16> {
 };
 
 // Pass B: for each kept page with some z above τ (every page with
-// ENTMAXKV_FLAG_DENSE_V) the warp stages the page's z in shared memory, issues
-// all its V loads at once (lane: 16 bytes of a row, tokens tg, tg+TG, ...),
-// and accumulates p·v in fp32 registers.
+// ENTMAXKV_FLAG_DENSE_V) the warp requests the page's V slab into its shared
+// buffer (bf16: two TMA tensor boxes with 128-byte swizzle; fp32: one bulk
+// copy), stages the page's z beside it, forms p once per (token, head), and
+// accumulates p·v: bf16 on the tensor cores (V^T by ldmatrix.trans, p as
+// bf16 hi + lo), fp32 with paired FMA in registers.
 template <typename T, int D, int GP>
 __global__ void __launch_bounds__(kThreads, GP <= 4 ? 2 : 1)
     pass_b_kernel(DecodeArgs a, const __grid_constant__ CUtensorMap vmap) {

@@ -7,6 +7,11 @@
 // Σ 2^{s−m} v) per query head in the base-2 domain, the block merges its warps
 // and writes (m, l, acc) as a partial, and the last block to finish merges the
 // partials in split order. The "τ" output carries log Σ_i exp(s_i).
+// bf16 pages: the scores are m16n8k16 MMAs on K loaded straight into the
+// fragments; the page's V arrives by two TMA tensor boxes (128-byte swizzle)
+// while they run, and Σ 2^{s−m} v is out^T = V^T·p on the tensor cores (V^T by
+// ldmatrix.trans, p split into bf16 hi + lo), the fragments rescaled per head
+// when a head's running max grows.
 //
 // With ENTMAXKV_POLICY_SOFTMAX_TOPK the same kernel runs over the top-k
 // selected pages only (the softmax side of the summary's comparison at equal
