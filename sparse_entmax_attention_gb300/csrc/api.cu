@@ -164,7 +164,9 @@ static int compute_layout(const entmaxkv_config* c, int S, int policy, int budge
   L.partial = entmax ? none : take(nk * (size_t)L.splits * L.pstride * 4);
   L.diag = take(nq * 4);
   L.mslots = gauss_grid_x(maxp, Hkv, S, 0);
-  L.mslot = policy == ENTMAXKV_POLICY_GAUSSIAN ? take(nq * (size_t)L.mslots * 4) : none;
+  L.mslot = policy == ENTMAXKV_POLICY_GAUSSIAN ? take(nq * (size_t)L.mslots * 4)
+            : topk                               ? take(nk * (size_t)L.mslots * 4)
+                                                 : none;
   L.total = off;
   return ENTMAXKV_OK;
 }
@@ -447,6 +449,8 @@ static int32_t decode_impl(const entmaxkv_config* cfg, const entmaxkv_cache* cac
   // and a dry run keeps a block from the next wave.
   a.dry_tail = (long long)a.splits * cfg->num_kv_heads * n_seqs <= 2LL * sms;
   a.mslots = gauss_grid_x(cfg->max_pages_per_seq, cfg->num_kv_heads, n_seqs, sms);
+  // the bf16 bounding box also leaves each scoring block's largest bound
+  a.bbox_slots = topk && cfg->kv_dtype == ENTMAXKV_BF16 ? a.mslots : 0;
 
   cudaStream_t s = (cudaStream_t)stream;
   auto mark = [&](int i) -> cudaError_t {

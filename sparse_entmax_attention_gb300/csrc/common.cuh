@@ -99,8 +99,10 @@ struct DecodeArgs {
   float* partial;      // [S][Hkv][splits][pstride]: acc [G][D], then (m, l) per head
   int pstride;         // floats per split partial: G·D + 2G rounded up to 4
   int32_t* diag;       // [S][Hq] τ̂ iterations (Gaussian)
-  uint32_t* mslot;     // [S][Hq][mslots] ordered-encoded max m of each scoring block
+  uint32_t* mslot;     // [S][Hq][mslots] ordered-encoded max m of each scoring block (Gaussian);
+                       // [S][Hkv][mslots] its largest bound Û (top-k, bf16 bounding box)
   int mslots;          // scoring blocks per (sequence, 8 KV heads) row
+  int bbox_slots;      // top-k: block maxima of Û in mslot (mslots), 0 when none were written
   uint4* ctrl;         // the workspace words zeroed before each decode's counters are used
   int ctrl_vec;        // their count in 16-byte units
   MomentFit fit;       // Gaussian selector at a general α (orders == 0 otherwise)

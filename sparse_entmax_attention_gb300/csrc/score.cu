@@ -420,6 +420,11 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_mma_kernel(DecodeArgs 
   if (MODE == 0)
     for (int i = threadIdx.x; i < KH * a.G; i += blockDim.x)
       a.mslot[((size_t)s * a.Hq + (size_t)kv0 * a.G + i) * a.mslots + blockIdx.x] = 0u;
+  // MODE 1: this block's largest bound Û per KV head (the top-k select's lower
+  // bound), "no page" until the block has scored its pages; lane 0 of the
+  // head's warp writes both, in order
+  uint32_t* bslot = MODE == 1 && active ? a.mslot + ((size_t)s * a.Hkv + kvh) * a.mslots + blockIdx.x : nullptr;
+  if (bslot && lane == 0) *bslot = ord_enc(-CUDART_INF_F);
   const int seq = seq_row(a.seq_ids, s, a.max_seqs, threadIdx.x == 0 ? a.status : nullptr);
   if (seq < 0) return;
   const int L = seq_len_clamped(a.seq_lens, seq, a.maxp, a.P, threadIdx.x == 0 ? a.status : nullptr);
@@ -600,6 +605,7 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_mma_kernel(DecodeArgs 
         if (p < n_pages && active) {
           if (hv) a.bbox_u[((size_t)s * a.Hq + (size_t)kvh * a.G + r) * a.maxp + p] = uv;
           if (r == 0) a.bbox_uhat[((size_t)s * a.Hkv + kvh) * a.maxp + p] = mx;
+          runmax = fmaxf(runmax, mx);
         }
       }
       continue;
@@ -630,7 +636,11 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_mma_kernel(DecodeArgs 
         if (f > 0) mbar_wait_bounded(&full[st], (uint32_t)((f - 1) & 1));
       }
   }
-  if (MODE == 1) return;
+  if (MODE == 1) {
+    runmax = warp_max(runmax);
+    if (bslot && lane == 0 && !stuck && runmax > -CUDART_INF_F) *bslot = ord_enc(runmax);
+    return;
+  }
   runmax = fmaxf(runmax, __shfl_xor_sync(0xffffffffu, runmax, 1));
   runmax = fmaxf(runmax, __shfl_xor_sync(0xffffffffu, runmax, 2));
   if (hv && (lane & 3) == 0 && runmax > -CUDART_INF_F) smax[warp][r] = ord_enc(runmax);
@@ -663,7 +673,7 @@ cudaError_t launch_bbox(const DecodeArgs& a, int kv_dtype, int sms, cudaStream_t
   const int other = a.Hkv * a.S;
   if (kv_dtype == ENTMAXKV_BF16) {
     // the streamed tensor-core kernel, rows of up to 8 KV heads
-    dim3 grid(gauss_grid_x(a.maxp, a.Hkv, a.S, sms), (a.Hkv + 7) / 8, a.S);
+    dim3 grid(a.mslots, (a.Hkv + 7) / 8, a.S);  // a.mslots = gauss_grid_x(maxp, Hkv, S, sms)
     const cudaError_t e = a.D == 128 ? gauss_mma_launch<128, 1>(a, grid, st) : gauss_mma_launch<64, 1>(a, grid, st);
     if (e != cudaSuccess) return e;
   } else {

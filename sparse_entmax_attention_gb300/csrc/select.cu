@@ -568,7 +568,7 @@ __global__ void __launch_bounds__(1024) topk_kernel(DecodeArgs a, int mode) {
 // so every block ends with the same k-th largest key T. Keys equal to T are
 // kept lowest page first: the last digit's histograms already hold each
 // block's count of them, which gives this block's offset among the ties.
-constexpr int kTopkThreads = 1024, kTopkKpt = 8;
+constexpr int kTopkThreads = 1024, kTopkKpt = 8, kTopkCand = 256;
 constexpr int kTopkClusterKeys = kTopkCluster * kTopkThreads * kTopkKpt;
 
 __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThreads)
@@ -583,6 +583,11 @@ __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThre
   __shared__ int sh_scan[32];
   __shared__ uint32_t sh_prefix, sh_mask;
   __shared__ int sh_remaining, sh_eq_count, sh_eq_before;
+  __shared__ __align__(16) uint32_t bm_sh[kTopkThreads];  // the scoring blocks' largest bounds
+  __shared__ uint32_t sh_tlo;
+  __shared__ int cand_n, all_cnt[kTopkCluster];
+  __shared__ uint2 cand_loc[kTopkCand];              // this block's (key, page) at or above T_lo
+  __shared__ __align__(16) uint2 all_cand[kTopkCluster][kTopkCand];  // every block's, pushed
   const int kvh = blockIdx.y, s = blockIdx.z;
   const int rank = (int)cluster.block_rank();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -599,6 +604,10 @@ __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThre
     key[j] = p < a.maxp ? ord_enc(__ldcg(u + p)) : 0u;
   }
   if (tid < 256) hist[0][tid] = hist[1][tid] = 0;
+  // the scoring blocks' largest bounds (fast path below), loaded with the keys
+  const int nbm = a.bbox_slots;
+  uint32_t bmv = 0u;  // 0: below every encoded key
+  if (tid < nbm && nbm <= kTopkThreads) bmv = __ldcg(a.mslot + ((size_t)s * a.Hkv + kvh) * a.mslots + tid);
   // Every block of the cluster takes the same exits, so no cluster barrier
   // is left waiting.
   const int seq = seq_row(a.seq_ids, s, a.max_seqs, (rank == 0 && tid == 0) ? a.status : nullptr);
@@ -615,6 +624,168 @@ __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThre
     return;
   }
   asm volatile("barrier.cluster.arrive.relaxed.aligned;\n" ::: "memory");
+  // Fast path. When the bounding-box kernel left each scoring block's largest
+  // bound and there are at least k of them, the k-th largest of those maxima,
+  // T_lo, is a lower bound of the k-th largest key: k distinct pages reach
+  // it. Only keys ≥ T_lo can be kept; each block pushes those (key, page)
+  // pairs to every block, and every block ranks the union by (key
+  // descending, page ascending), which is exactly the top-k order with ties
+  // to the lower page. A block with more than kTopkCand of them sends the
+  // whole cluster (all blocks see the same counts) down the radix path.
+  bool fast = nbm > 0 && nbm <= kTopkThreads && k <= nbm;  // uniform over the cluster
+  bool waited = false;
+  if (fast) {
+    // T_lo: the lower edge of the 8-bit bin (below the leading bits all the
+    // maxima share) that holds the k-th largest maximum, so at least k
+    // maxima, and with them k pages, reach it
+    uint32_t mlo = tid < nbm ? bmv : 0xffffffffu, mhi = bmv;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      mlo = min(mlo, __shfl_xor_sync(0xffffffffu, mlo, o));
+      mhi = max(mhi, __shfl_xor_sync(0xffffffffu, mhi, o));
+    }
+    if (lane == 0) warp_mm[warp] = make_uint2(mlo, mhi);
+    if (tid == 0) {
+      sh_tlo = 0u;
+      cand_n = 0;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      uint2 m = warp_mm[lane];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        m.x = min(m.x, __shfl_xor_sync(0xffffffffu, m.x, o));
+        m.y = max(m.y, __shfl_xor_sync(0xffffffffu, m.y, o));
+      }
+      if (lane == 0) {
+        sh_prefix = m.x;
+        sh_mask = m.y;
+      }
+    }
+    __syncthreads();
+    const uint32_t bmin = sh_prefix, bmax = sh_mask;
+    const int brb = (bmin ^ bmax) ? 32 - __clz((int)(bmin ^ bmax)) : 0;  // bits below the shared prefix
+    const int bsh = brb > 8 ? brb - 8 : 0;
+    if (tid < nbm) atomicAdd(&hist[0][(bmv >> bsh) & 255u], 1);
+    __syncthreads();
+    if (warp == 0) {
+      int cnt[8], tot = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        cnt[j] = hist[0][255 - 8 * lane - j];
+        tot += cnt[j];
+      }
+      int incl = tot;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const int excl = incl - tot;
+      if (excl < k && incl >= k) {
+        int jj = 7;
+#pragma unroll
+        for (int j = 7; j >= 0; --j) {
+          int before = excl;
+#pragma unroll
+          for (int i = 0; i < j; ++i) before += cnt[i];
+          if (before + cnt[j] >= k) jj = j;
+        }
+        const uint32_t digit = 255u - 8u * lane - jj;
+        const uint32_t keep = brb >= 32 ? 0u : (0xffffffffu << brb);  // the shared prefix
+        sh_tlo = (bmin & keep) | (digit << bsh);
+      }
+    }
+    __syncthreads();
+    if (tid < 256) hist[0][tid] = 0;  // (the radix path below starts from a clear histogram)
+    const uint32_t tlo = sh_tlo;
+    fast = tlo > ord_enc(-CUDART_INF_F);  // (k scoring blocks saw a readable page)
+    if (fast) {
+#pragma unroll
+      for (int j = 0; j < kTopkKpt; ++j) {
+        const int p = p_lo + j * kTopkThreads + tid;
+        if (p < p_hi && key[j] >= tlo) {
+          const int i = atomicAdd(&cand_n, 1);
+          if (i < kTopkCand) cand_loc[i] = make_uint2(key[j], (uint32_t)p);
+        }
+      }
+      __syncthreads();
+      const int nc = cand_n;
+      // every block of the cluster is running before the first push
+      asm volatile("barrier.cluster.wait.aligned;\n" ::: "memory");
+      waited = true;
+      const int nsend = min(nc, kTopkCand);
+      if (tid < kTopkCluster) cluster.map_shared_rank(&all_cnt[0], tid)[rank] = nc;
+      for (int i = tid; i < kTopkCluster * nsend; i += kTopkThreads) {
+        const int r = i / nsend, q = i - r * nsend;
+        cluster.map_shared_rank(&all_cand[0][0], r)[rank * kTopkCand + q] = cand_loc[q];
+      }
+      cluster.sync();
+      int C = 0;
+      bool over = false;
+#pragma unroll
+      for (int r = 0; r < kTopkCluster; ++r) {
+        over = over || all_cnt[r] > kTopkCand;
+        C += all_cnt[r];
+      }
+      over = over || C < k;  // (cannot happen: k pages reach T_lo)
+      if (!over) {
+        // the candidates packed at the front of all_cand (read into
+        // registers, then written: 2 a thread at most), padded to an even
+        // count with a pair that ranks below every other
+        uint2* flat = &all_cand[0][0];
+        uint2 mine[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int i = tid + u * kTopkThreads;
+          if (i < C) {
+            int r = 0, q = i;
+            while (q >= all_cnt[r]) q -= all_cnt[r++];
+            mine[u] = all_cand[r][q];
+          }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int i = tid + u * kTopkThreads;
+          if (i < C) flat[i] = mine[u];
+        }
+        if (tid == 0 && (C & 1)) flat[C] = make_uint2(0u, 0xffffffffu);
+        __syncthreads();
+        // T = the candidate of rank k − 1 (every rank is unique: pages are)
+        const uint4* c4 = reinterpret_cast<const uint4*>(flat);
+        const int C2 = (C + 1) / 2;
+        for (int i = tid; i < C; i += kTopkThreads) {
+          const uint2 ci = flat[i];
+          int rk = 0;
+#pragma unroll 4
+          for (int j2 = 0; j2 < C2; ++j2) {
+            const uint4 w = c4[j2];  // two candidates
+            rk += (w.x > ci.x || (w.x == ci.x && w.y < ci.y)) ? 1 : 0;
+            rk += (w.z > ci.x || (w.z == ci.x && w.w < ci.y)) ? 1 : 0;
+          }
+          if (rk == k - 1) {
+            sh_prefix = ci.x;
+            sh_eq_before = (int)ci.y;
+          }
+        }
+        __syncthreads();
+        const uint32_t T = sh_prefix;
+        const int Tp = sh_eq_before;
+#pragma unroll
+        for (int j = 0; j < kTopkKpt; ++j) {
+          const int p0 = p_lo + j * kTopkThreads;
+          if (p0 >= p_hi) continue;  // block-uniform
+          const int p = p0 + tid;
+          const bool sel = p < p_hi && (key[j] > T || (key[j] == T && p <= Tp));
+          const uint32_t bits = __ballot_sync(0xffffffffu, sel);
+          if (lane == 0 && p0 + warp * 32 < p_hi) bm[p >> 5] = bits;
+        }
+        return;  // no block touches another's shared memory after the barrier
+      }
+      fast = false;
+    }
+  }
   uint32_t lo_k = 0xffffffffu, hi_k = 0u;
 #pragma unroll
   for (int j = 0; j < kTopkKpt; ++j) {
@@ -631,7 +802,7 @@ __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThre
   if (lane == 0) warp_mm[warp] = make_uint2(lo_k, hi_k);
   __syncthreads();
   // every block of the cluster is running before the first push
-  asm volatile("barrier.cluster.wait.aligned;\n" ::: "memory");
+  if (!waited) asm volatile("barrier.cluster.wait.aligned;\n" ::: "memory");
   if (warp == 0) {
     uint2 m = warp_mm[lane];
 #pragma unroll

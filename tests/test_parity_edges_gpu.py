@@ -155,16 +155,19 @@ def test_scorer_wait_timeout_is_flagged_and_the_context_stays_usable(meta_bf16):
     assert c.read_status() == 0
 
 
-@pytest.mark.parametrize("n_pages,n_distinct,max_pages", [
-    (300, 3, None), (5000, 4, None), (2000, 1, None), (700, 3, 70000)])
-def test_topk_exact_ties_go_to_the_lower_page(n_pages, n_distinct, max_pages):
+@pytest.mark.parametrize("n_pages,n_distinct,max_pages,k_top", [
+    (300, 3, None, 0), (5000, 4, None, 0), (2000, 1, None, 0), (700, 3, 70000, 0), (5000, 3, None, 40)])
+def test_topk_exact_ties_go_to_the_lower_page(n_pages, n_distinct, max_pages, k_top):
     """Pages with equal contents have equal bounds, so the top-k boundary can
     cut through a class of exact ties; the kept pages of that class must be
     its lowest page indices, bit for bit (summary §2B.1, ties to the lower
     index). 300 pages fall in 5 blocks of the cluster select and 5000 in all
     8, so the tie offset crosses blocks; 2000 copies of one page make every
     key equal (no radix digit at all); a table of 70000 pages per sequence
-    takes the one-block select."""
+    takes the one-block select. k_top > 0 keeps that many pages of the
+    largest class: k is then below the count of scoring blocks, so the
+    cluster select's candidate path (keys at or above the k-th largest
+    block maximum) decides, with every candidate tied."""
     P, d, g = 16, 128, 4
     spec = synth.custom(g, 1, d, P, [n_pages * P], torch.bfloat16, 1.5, shuffled_table=True)
     bt, total, _ = synth.block_tables(spec)
@@ -178,7 +181,10 @@ def test_topk_exact_ties_go_to_the_lower_page(n_pages, n_distinct, max_pages):
     meta = opg.page_metadata(K, P)
     uhat = np.stack([opg.bbox_bound(Q[h], meta["kmin"], meta["kmax"]) for h in range(g)]).max(axis=0)
     classes = np.unique(uhat)[::-1]
-    if classes.size == 1:
+    if k_top:
+        kp = k_top
+        assert (uhat == classes[0]).sum() > kp
+    elif classes.size == 1:
         kp = n_pages // 3
     else:  # through the middle of the second-largest class
         kp = int((uhat > classes[1]).sum() + (uhat == classes[1]).sum() // 2)
