@@ -631,8 +631,10 @@ __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThre
   // pairs to every block, and every block ranks the union by (key
   // descending, page ascending), which is exactly the top-k order with ties
   // to the lower page. A block with more than kTopkCand of them sends the
-  // whole cluster (all blocks see the same counts) down the radix path.
-  bool fast = nbm > 0 && nbm <= kTopkThreads && k <= nbm;  // uniform over the cluster
+  // whole cluster (all blocks see the same counts) down the radix path, and
+  // so does a union of more than kTopkThreads candidates.
+  // (k well below the count of maxima keeps T_lo tight and the candidates few)
+  bool fast = nbm > 0 && nbm <= kTopkThreads && 4 * k <= nbm;  // uniform over the cluster
   bool waited = false;
   if (fast) {
     // T_lo: the lower edge of the 8-bit bin (below the leading bits all the
@@ -728,7 +730,7 @@ __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThre
         over = over || all_cnt[r] > kTopkCand;
         C += all_cnt[r];
       }
-      over = over || C < k;  // (cannot happen: k pages reach T_lo)
+      over = over || C < k || C > kTopkThreads;  // (C < k cannot happen: k pages reach T_lo)
       if (!over) {
         // the candidates packed at the front of all_cand (read into
         // registers, then written: 2 a thread at most), padded to an even

@@ -156,7 +156,7 @@ def test_scorer_wait_timeout_is_flagged_and_the_context_stays_usable(meta_bf16):
 
 
 @pytest.mark.parametrize("n_pages,n_distinct,max_pages,k_top", [
-    (300, 3, None, 0), (5000, 4, None, 0), (2000, 1, None, 0), (700, 3, 70000, 0), (5000, 3, None, 40)])
+    (300, 3, None, 0), (5000, 4, None, 0), (2000, 1, None, 0), (700, 3, 70000, 0), (5000, 12, None, 30)])
 def test_topk_exact_ties_go_to_the_lower_page(n_pages, n_distinct, max_pages, k_top):
     """Pages with equal contents have equal bounds, so the top-k boundary can
     cut through a class of exact ties; the kept pages of that class must be
