@@ -53,17 +53,19 @@ __device__ __forceinline__ void append_page(const AppendArgs& a, int b, int seq,
     mx[e] = -CUDART_INF_F;
     sum[e] = 0.0f;
   }
-  // four rows at a time: eight loads in flight a lane before the first store
+  // U rows at a time, their K and V loads in flight together before the
+  // first store (about 256 bytes a lane: 16 rows of bf16, 8 of fp32 at d = 128)
+  constexpr int U = sizeof(V) >= 16 ? 8 : 16;
   int t = 0;
-  for (; t + 4 <= n_new; t += 4) {
-    V kv[4], vv[4];
+  for (; t + U <= n_new; t += U) {
+    V kv[U], vv[U];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < U; ++u) {
       kv[u] = *reinterpret_cast<const V*>(ks + (size_t)(t + u) * D);
       vv[u] = *reinterpret_cast<const V*>(vs + (size_t)(t + u) * D);
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < U; ++u) {
       *reinterpret_cast<V*>(kd + (size_t)(t + u) * D) = kv[u];
       *reinterpret_cast<V*>(vd + (size_t)(t + u) * D) = vv[u];
 #pragma unroll
