@@ -4,7 +4,8 @@ Some embedders cannot call cudaMalloc at decode time (code running inside an
 allocator's own callbacks, graph-building code that must not allocate, or a
 runtime that owns all device memory), so the library offers one decode whose
 scratch is a fixed array compiled into it. This checks, through the C ABI,
-that two calls in a row match the ordinary softmax decode. Kept in its own
+that two calls in a row match the ordinary softmax decode and the float64
+oracle's full-cache softmax. Kept in its own
 file, named so that pytest collects it last.
 """
 
@@ -13,6 +14,7 @@ import ctypes
 import pytest
 import torch
 
+from oracle import decode as odec
 from sparse_entmax_attention_gb300 import binding as B
 from sparse_entmax_attention_gb300 import synth
 
@@ -47,6 +49,15 @@ def test_noalloc_softmax_matches_decode_twice():
             for h in range(spec.num_q_heads):
                 assert rel_l2(out[b, h].cpu().numpy(), ref.out[b, h].cpu().numpy()) <= 2e-3
         torch.testing.assert_close(lse, ref.tau, rtol=0, atol=1e-4)
+    # and against the float64 oracle's full-cache softmax on the stored bits
+    g = spec.group
+    for b in range(q.shape[0]):
+        for j in range(spec.num_kv_heads):
+            K, V = built.host_kv(b, j)
+            r = odec.decode_group(K, V, built.host_q(b, j), 1.5, "softmax", spec.page_size, diagnostics=False)
+            for h in range(g):
+                assert rel_l2(out[b, j * g + h].cpu().numpy(), r["out"][h]) <= 2e-3, (b, j, h)
+                assert abs(float(lse[b, j * g + h]) - r["tau"][h]) <= 1e-4, (b, j, h)
 
 
 def test_noalloc_rejects_oversized_shape():
