@@ -389,6 +389,12 @@ __device__ __forceinline__ void ldsm_x2(uint32_t& r0, uint32_t& r1, const void* 
                : "r"(smem_u32(p)));
 }
 
+__device__ __forceinline__ void ldsm_x4(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3, const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(smem_u32(p)));
+}
+
 __device__ __forceinline__ uint32_t bf2_pack(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&v);
@@ -396,7 +402,16 @@ __device__ __forceinline__ uint32_t bf2_pack(float lo, float hi) {
 
 // MODE 0: the Gaussian statistics (μ, σ) from the bf16 mean and m2 copies;
 // MODE 1: the bounding box U = (q⁺·kmax + q⁻·kmin)/√d from the bf16 kmax and
-// kmin (exact term by term), per query head and as the group's maximum.
+// kmin (exact term by term), per query head and as the group's maximum;
+// MODE 2: MODE 0 for groups of at most 4 query heads with the operands
+// swapped. The stage is A: rows 0-7 the 8 pages' mean, rows 8-15 their m2.
+// The queries are B, held in registers for the whole kernel: columns 0-3
+// are q and 4-7 q² hi, and a second B has zero and q² lo. Then
+// C[mean row][q column] = μ and C[m2 row][q² column] = σ² (hi + lo from the
+// two accumulators), and the rest of C is unused. A stage's A fragments fit
+// in registers at once, so, as in MODE 1, a warp releases the stage before
+// its MMAs and the refill does not wait on them. MODE 0 holds three query
+// fragments per 16 dims instead and has no room for that.
 template <int D, int MODE>
 __global__ void __launch_bounds__(kGaussWarps * 32) gauss_mma_kernel(DecodeArgs a) {
   pdl_enter();
@@ -417,7 +432,8 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_mma_kernel(DecodeArgs 
   __shared__ int phys_pre[kGaussMmaPre];
   static_assert(NST * PPS <= 32, "warp 0 looks up the first stages' pages at once");
   clear_ctrl_slice(a.ctrl, a.ctrl_vec);
-  if (MODE == 0)
+  constexpr bool GAUSS = MODE != 1;
+  if (GAUSS)
     for (int i = threadIdx.x; i < KH * a.G; i += blockDim.x)
       a.mslot[((size_t)s * a.Hq + (size_t)kv0 * a.G + i) * a.mslots + blockIdx.x] = 0u;
   // MODE 1: this block's largest bound Û per KV head (the top-k select's lower
@@ -450,7 +466,7 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_mma_kernel(DecodeArgs 
     if (lane == 0) mbar_expect_tx(&full[st], (uint32_t)__popc(valid) * (uint32_t)run);
     __syncwarp();
     if (ph >= 0) {
-      const __nv_bfloat16* arr = MODE == 0 ? ((lane & 1) ? a.m2_lo : a.mean_lo)
+      const __nv_bfloat16* arr = GAUSS ? ((lane & 1) ? a.m2_lo : a.mean_lo)
                                            : (const __nv_bfloat16*)((lane & 1) ? a.kmin : a.kmax);
       const __nv_bfloat16* src = arr + ((size_t)ph * a.Hkv + kv0) * D;
       bulk_g2s(dyn + st * sstride + (lane >> 1) * pstride + (lane & 1) * run, src, (uint32_t)run, &full[st]);
@@ -486,21 +502,31 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_mma_kernel(DecodeArgs 
     n_issued = nfill;
   }
 
-  // A fragments: row lane/4 (a query head of the group), dims 2(lane%4)+{0,1}
-  // and +8 of each 16-dim step; rows 8..15 are zero. MODE 0: q, q² hi,
-  // q² lo; MODE 1: q⁺ and q⁻ (in aq and ah; al unused).
+  // Query fragments, dims 2(lane%4)+{0,1} and +8 of each 16-dim step.
+  // MODE 0 and 1 (A): row lane/4 is a query head of the group, rows 8..15
+  // are zero; MODE 0 holds q, q² hi, q² lo, MODE 1 q⁺ and q⁻ (in aq and ah;
+  // al unused). MODE 2 (B): column lane/4 is head (lane/4)%4; lanes 0-15
+  // hold q in aq and zero in ah, lanes 16-31 q² hi in aq and q² lo in ah.
   const int r = lane >> 2, cpair = 2 * (lane & 3);
+  const int qrow = MODE == 2 ? (r & 3) : r;
   const bool hv = active && r < a.G;
-  const __nv_bfloat16* qh = (const __nv_bfloat16*)a.q + ((size_t)s * a.Hq + (size_t)(hv ? kvh : 0) * a.G + (hv ? r : 0)) * D;
+  const bool qv = active && qrow < a.G;
+  const __nv_bfloat16* qh = (const __nv_bfloat16*)a.q + ((size_t)s * a.Hq + (size_t)(qv ? kvh : 0) * a.G + (qv ? qrow : 0)) * D;
   uint32_t aq[KS][2], ah[KS][2], al[KS][2];
 #pragma unroll
   for (int k = 0; k < KS; ++k)
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
       const int d0 = 16 * k + 8 * u + cpair;
-      const uint32_t w = hv ? *reinterpret_cast<const uint32_t*>(qh + d0) : 0u;
+      const uint32_t w = qv ? *reinterpret_cast<const uint32_t*>(qh + d0) : 0u;
       if (MODE == 1) {
         split_sign(w, aq[k][u], ah[k][u]);
+        al[k][u] = 0u;
+        continue;
+      }
+      if (MODE == 2 && lane < 16) {
+        aq[k][u] = w;
+        ah[k][u] = 0u;
         al[k][u] = 0u;
         continue;
       }
@@ -508,6 +534,12 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_mma_kernel(DecodeArgs 
       const float x0 = bf_lo(w), x1 = bf_hi(w);
       const float s0 = x0 * x0, s1 = x1 * x1;  // exact: at most 16 significant bits
       const float h0 = __bfloat162float(__float2bfloat16_rn(s0)), h1 = __bfloat162float(__float2bfloat16_rn(s1));
+      if (MODE == 2) {
+        aq[k][u] = bf2_pack(h0, h1);
+        ah[k][u] = bf2_pack(s0 - h0, s1 - h1);
+        al[k][u] = 0u;
+        continue;
+      }
       ah[k][u] = bf2_pack(h0, h1);
       al[k][u] = bf2_pack(s0 - h0, s1 - h1);  // the exact remainders, representable in bf16
     }
@@ -562,6 +594,33 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_mma_kernel(DecodeArgs 
 #pragma unroll
         for (int i = 0; i < 4; ++i) mu[i] += sg[i];
       }
+    } else if constexpr (MODE == 2) {
+      // lanes 8j..8j+7 address tile j: pages lane%8, mean (j even) or m2
+      // (j odd), dims 0-7 (j < 2) or 8-15 of the step
+      uint32_t fa[KS][4];
+      if (active) {
+        const unsigned char* rowa = dyn + st * sstride + lrow * pstride + ((lane >> 3) & 1) * run + warp * D * 2 +
+                                    (lane >> 4) * 16;
+#pragma unroll
+        for (int k = 0; k < KS; ++k) ldsm_x4(fa[k][0], fa[k][1], fa[k][2], fa[k][3], rowa + 32 * k);
+        ph0 = phys_sm[st * PPS + r];
+      }
+      __syncwarp();
+      if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(&empty[st])) : "memory");
+      if (warp == 0 && j + NST < n_mine) {
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&empty[st], par))) {
+          stuck = 1;
+          break;
+        }
+        issue(g + NST, st);
+      }
+      if (active) {
+#pragma unroll
+        for (int k = 0; k < KS; ++k) {
+          mma_bf16(mu, fa[k][0], fa[k][1], fa[k][2], fa[k][3], aq[k][0], aq[k][1]);  // μ; σ² hi
+          mma_bf16(sg, fa[k][0], fa[k][1], fa[k][2], fa[k][3], ah[k][0], ah[k][1]);  // σ² lo
+        }
+      }
     } else if (active) {
       const unsigned char* rowm = dyn + st * sstride + lrow * pstride + warp * D * 2 + lk;
       const unsigned char* rowv = rowm + run;
@@ -610,6 +669,31 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_mma_kernel(DecodeArgs 
       }
       continue;
     }
+    if (MODE == 2) {
+      // lane l holds page l/4. With c = l%4: c < 2 has μ of heads 2c, 2c+1
+      // (mu[0..1]); c ≥ 2 has σ² hi + lo of heads 2c−4, 2c−3 (mu[2..3] +
+      // sg[2..3]). One exchange with lane l^2 leaves each lane (μ, σ²) of
+      // one head: c = 0, 1, 2, 3 → head 0, 2, 1, 3.
+      const int c = lane & 3;
+      const bool lowc = c < 2;
+      const float sq0 = mu[2] + sg[2], sq1 = mu[3] + sg[3];
+      const float got = __shfl_xor_sync(0xffffffffu, lowc ? mu[1] : sq0, 2);
+      const int hh = lowc ? 2 * c : 2 * c - 3;
+      const float muv = lowc ? mu[0] : got, sgv = lowc ? got : sq1;
+      const int p = g * PPS + r;
+      if (!active || hh >= a.G || p >= n_pages) continue;
+      float2* dst = a.gauss_ms + ((size_t)s * a.Hq + (size_t)kvh * a.G + hh) * a.maxp;
+      if (ph0 < 0) {  // unreadable page: no mass, never selected
+        dst[p] = make_float2(-CUDART_INF_F, 0.0f);
+        continue;
+      }
+      const int nv = min(a.P, L - p * a.P);
+      const float inv_n = nv == a.P ? inv_full : 1.0f / ((float)nv * (float)D);
+      const float m = a.a1 * muv * a.inv_sqrt_d;
+      dst[p] = make_float2(m, a.a1 * sqrtf(fmaxf(sgv, 0.0f) * inv_n));
+      runmax = fmaxf(runmax, m);
+      continue;
+    }
     if (!hv) continue;
     float2* dst = a.gauss_ms + ((size_t)s * a.Hq + (size_t)kvh * a.G + r) * a.maxp;
 #pragma unroll
@@ -641,9 +725,18 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_mma_kernel(DecodeArgs 
     if (bslot && lane == 0 && !stuck && runmax > -CUDART_INF_F) *bslot = ord_enc(runmax);
     return;
   }
-  runmax = fmaxf(runmax, __shfl_xor_sync(0xffffffffu, runmax, 1));
-  runmax = fmaxf(runmax, __shfl_xor_sync(0xffffffffu, runmax, 2));
-  if (hv && (lane & 3) == 0 && runmax > -CUDART_INF_F) smax[warp][r] = ord_enc(runmax);
+  if (MODE == 2) {
+    // the lanes of one head differ in bits 2..4 (the page)
+    runmax = fmaxf(runmax, __shfl_xor_sync(0xffffffffu, runmax, 4));
+    runmax = fmaxf(runmax, __shfl_xor_sync(0xffffffffu, runmax, 8));
+    runmax = fmaxf(runmax, __shfl_xor_sync(0xffffffffu, runmax, 16));
+    const int hh = (lane & 3) < 2 ? 2 * (lane & 3) : 2 * (lane & 3) - 3;
+    if (active && lane < 4 && hh < a.G && runmax > -CUDART_INF_F) smax[warp][hh] = ord_enc(runmax);
+  } else {
+    runmax = fmaxf(runmax, __shfl_xor_sync(0xffffffffu, runmax, 1));
+    runmax = fmaxf(runmax, __shfl_xor_sync(0xffffffffu, runmax, 2));
+    if (hv && (lane & 3) == 0 && runmax > -CUDART_INF_F) smax[warp][r] = ord_enc(runmax);
+  }
   __syncthreads();
   if (threadIdx.x < 64) {
     const int w = threadIdx.x >> 3, h = threadIdx.x & 7;
@@ -730,7 +823,8 @@ cudaError_t launch_gauss(const DecodeArgs& a, int kv_dtype, int sms, cudaStream_
   dim3 grid(a.mslots, (a.Hkv + 7) / 8, a.S);
   cudaError_t e;
   if (kv_dtype == ENTMAXKV_BF16 && a.mean_lo)  // bf16 q and metadata: tensor cores
-    e = a.D == 128 ? gauss_mma_launch<128, 0>(a, grid, st) : gauss_mma_launch<64, 0>(a, grid, st);
+    e = a.G <= 4 ? (a.D == 128 ? gauss_mma_launch<128, 2>(a, grid, st) : gauss_mma_launch<64, 2>(a, grid, st))
+                 : (a.D == 128 ? gauss_mma_launch<128, 0>(a, grid, st) : gauss_mma_launch<64, 0>(a, grid, st));
   else if (kv_dtype == ENTMAXKV_BF16)
     e = a.D == 128 ? gauss_dispatch_g<__nv_bfloat16, 128>(a, grid, st)
                    : gauss_dispatch_g<__nv_bfloat16, 64>(a, grid, st);
