@@ -411,7 +411,11 @@ __device__ __forceinline__ uint32_t bf2_pack(float lo, float hi) {
 // two accumulators), and the rest of C is unused. A stage's A fragments fit
 // in registers at once, so, as in MODE 1, a warp releases the stage before
 // its MMAs and the refill does not wait on them. MODE 0 holds three query
-// fragments per 16 dims instead and has no room for that.
+// fragments per 16 dims instead and has no room for that;
+// MODE 3: MODE 1 with the same swap. A: rows 0-7 the 8 pages' kmax, rows
+// 8-15 their kmin; B: columns 0-3 q⁺ and 4-7 q⁻, so one MMA per 16 dims
+// gives q⁺·kmax in C[kmax row][q⁺ column] and q⁻·kmin in C[kmin row][q⁻
+// column].
 template <int D, int MODE>
 __global__ void __launch_bounds__(kGaussWarps * 32) gauss_mma_kernel(DecodeArgs a) {
   pdl_enter();
@@ -432,14 +436,16 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_mma_kernel(DecodeArgs 
   __shared__ int phys_pre[kGaussMmaPre];
   static_assert(NST * PPS <= 32, "warp 0 looks up the first stages' pages at once");
   clear_ctrl_slice(a.ctrl, a.ctrl_vec);
-  constexpr bool GAUSS = MODE != 1;
+  constexpr bool GAUSS = MODE == 0 || MODE == 2;
+  constexpr bool BOX = !GAUSS;
+  constexpr bool SWAP = MODE >= 2;  // metadata rows in A, queries in B
   if (GAUSS)
     for (int i = threadIdx.x; i < KH * a.G; i += blockDim.x)
       a.mslot[((size_t)s * a.Hq + (size_t)kv0 * a.G + i) * a.mslots + blockIdx.x] = 0u;
   // MODE 1: this block's largest bound Û per KV head (the top-k select's lower
   // bound), "no page" until the block has scored its pages; lane 0 of the
   // head's warp writes both, in order
-  uint32_t* bslot = MODE == 1 && active ? a.mslot + ((size_t)s * a.Hkv + kvh) * a.mslots + blockIdx.x : nullptr;
+  uint32_t* bslot = BOX && active ? a.mslot + ((size_t)s * a.Hkv + kvh) * a.mslots + blockIdx.x : nullptr;
   if (bslot && lane == 0) *bslot = ord_enc(-CUDART_INF_F);
   const int seq = seq_row(a.seq_ids, s, a.max_seqs, threadIdx.x == 0 ? a.status : nullptr);
   if (seq < 0) return;
@@ -507,8 +513,9 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_mma_kernel(DecodeArgs 
   // are zero; MODE 0 holds q, q² hi, q² lo, MODE 1 q⁺ and q⁻ (in aq and ah;
   // al unused). MODE 2 (B): column lane/4 is head (lane/4)%4; lanes 0-15
   // hold q in aq and zero in ah, lanes 16-31 q² hi in aq and q² lo in ah.
+  // MODE 3 (B): lanes 0-15 hold q⁺ in aq, lanes 16-31 q⁻.
   const int r = lane >> 2, cpair = 2 * (lane & 3);
-  const int qrow = MODE == 2 ? (r & 3) : r;
+  const int qrow = SWAP ? (r & 3) : r;
   const bool hv = active && r < a.G;
   const bool qv = active && qrow < a.G;
   const __nv_bfloat16* qh = (const __nv_bfloat16*)a.q + ((size_t)s * a.Hq + (size_t)(qv ? kvh : 0) * a.G + (qv ? qrow : 0)) * D;
@@ -521,6 +528,14 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_mma_kernel(DecodeArgs 
       const uint32_t w = qv ? *reinterpret_cast<const uint32_t*>(qh + d0) : 0u;
       if (MODE == 1) {
         split_sign(w, aq[k][u], ah[k][u]);
+        al[k][u] = 0u;
+        continue;
+      }
+      if (MODE == 3) {
+        uint32_t pos, neg;
+        split_sign(w, pos, neg);
+        aq[k][u] = lane < 16 ? pos : neg;
+        ah[k][u] = 0u;
         al[k][u] = 0u;
         continue;
       }
@@ -594,7 +609,7 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_mma_kernel(DecodeArgs 
 #pragma unroll
         for (int i = 0; i < 4; ++i) mu[i] += sg[i];
       }
-    } else if constexpr (MODE == 2) {
+    } else if constexpr (SWAP) {
       // lanes 8j..8j+7 address tile j: pages lane%8, mean (j even) or m2
       // (j odd), dims 0-7 (j < 2) or 8-15 of the step
       uint32_t fa[KS][4];
@@ -617,9 +632,16 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_mma_kernel(DecodeArgs 
       if (active) {
 #pragma unroll
         for (int k = 0; k < KS; ++k) {
-          mma_bf16(mu, fa[k][0], fa[k][1], fa[k][2], fa[k][3], aq[k][0], aq[k][1]);  // μ; σ² hi
-          mma_bf16(sg, fa[k][0], fa[k][1], fa[k][2], fa[k][3], ah[k][0], ah[k][1]);  // σ² lo
+          if (MODE == 2) {
+            mma_bf16(mu, fa[k][0], fa[k][1], fa[k][2], fa[k][3], aq[k][0], aq[k][1]);  // μ; σ² hi
+            mma_bf16(sg, fa[k][0], fa[k][1], fa[k][2], fa[k][3], ah[k][0], ah[k][1]);  // σ² lo
+          } else {  // q⁺·kmax; q⁻·kmin, even and odd steps in two chains
+            mma_bf16(k & 1 ? sg : mu, fa[k][0], fa[k][1], fa[k][2], fa[k][3], aq[k][0], aq[k][1]);
+          }
         }
+        if (MODE == 3)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) mu[i] += sg[i];
       }
     } else if (active) {
       const unsigned char* rowm = dyn + st * sstride + lrow * pstride + warp * D * 2 + lk;
@@ -666,6 +688,29 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_mma_kernel(DecodeArgs 
           if (r == 0) a.bbox_uhat[((size_t)s * a.Hkv + kvh) * a.maxp + p] = mx;
           runmax = fmaxf(runmax, mx);
         }
+      }
+      continue;
+    }
+    if (MODE == 3) {
+      // lane l holds page l/4. With c = l%4: c < 2 has q⁺·kmax of heads 2c,
+      // 2c+1 (mu[0..1]), c ≥ 2 q⁻·kmin of heads 2c−4, 2c−3 (mu[2..3]); one
+      // exchange with lane l^2 gives U of one head: c = 0, 1, 2, 3 → head 0,
+      // 2, 1, 3. The group's maximum per page is over the lanes of one page
+      // (bits 0..1).
+      const int c = lane & 3;
+      const bool lowc = c < 2;
+      const float got = __shfl_xor_sync(0xffffffffu, lowc ? mu[1] : mu[2], 2);
+      const int hh = lowc ? 2 * c : 2 * c - 3;
+      const int p = g * PPS + r;
+      const bool hok = active && hh < a.G;
+      const float uv = (hok && ph0 >= 0) ? ((lowc ? mu[0] : mu[3]) + got) * a.inv_sqrt_d : -CUDART_INF_F;
+      float mx = uv;
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      if (p < n_pages && active) {
+        if (hok) a.bbox_u[((size_t)s * a.Hq + (size_t)kvh * a.G + hh) * a.maxp + p] = uv;
+        if (c == 0) a.bbox_uhat[((size_t)s * a.Hkv + kvh) * a.maxp + p] = mx;
+        runmax = fmaxf(runmax, mx);
       }
       continue;
     }
@@ -720,7 +765,7 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_mma_kernel(DecodeArgs 
         if (f > 0) mbar_wait_bounded(&full[st], (uint32_t)((f - 1) & 1));
       }
   }
-  if (MODE == 1) {
+  if (BOX) {
     runmax = warp_max(runmax);
     if (bslot && lane == 0 && !stuck && runmax > -CUDART_INF_F) *bslot = ord_enc(runmax);
     return;
@@ -767,7 +812,9 @@ cudaError_t launch_bbox(const DecodeArgs& a, int kv_dtype, int sms, cudaStream_t
   if (kv_dtype == ENTMAXKV_BF16) {
     // the streamed tensor-core kernel, rows of up to 8 KV heads
     dim3 grid(a.mslots, (a.Hkv + 7) / 8, a.S);  // a.mslots = gauss_grid_x(maxp, Hkv, S, sms)
-    const cudaError_t e = a.D == 128 ? gauss_mma_launch<128, 1>(a, grid, st) : gauss_mma_launch<64, 1>(a, grid, st);
+    const cudaError_t e =
+        a.G <= 4 ? (a.D == 128 ? gauss_mma_launch<128, 3>(a, grid, st) : gauss_mma_launch<64, 3>(a, grid, st))
+                 : (a.D == 128 ? gauss_mma_launch<128, 1>(a, grid, st) : gauss_mma_launch<64, 1>(a, grid, st));
     if (e != cudaSuccess) return e;
   } else {
     dim3 grid(grid_x_for(a.maxp, kThreads, sms, other), a.Hkv, a.S);

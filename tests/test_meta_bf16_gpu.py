@@ -44,11 +44,11 @@ def test_gaussian_decode_on_bf16_metadata(built_meta16, alpha, margin):
     check_decode(built_meta16, "gaussian", alpha, 0, margin)
 
 
-# The tensor-core scorer's two operand layouts: groups of up to 4 query
-# heads put the metadata in the tile's rows and the queries in its columns,
-# larger groups the other way round. Shapes: d = 64 and 128, a padded head
-# (group 3), and KV-head counts that leave warps of a block idle (3 and 9 of
-# a block's 8).
+# The tensor-core scorers' two operand layouts (Gaussian statistics and the
+# top-k bounding box): groups of up to 4 query heads put the metadata in the
+# tile's rows and the queries in its columns, larger groups the other way
+# round. Shapes: d = 64 and 128, a padded head (group 3), and KV-head counts
+# that leave warps of a block idle (3 and 9 of a block's 8).
 @pytest.mark.parametrize("hq,hkv,d,p", [(24, 3, 64, 32), (6, 2, 64, 16), (10, 2, 128, 32), (9, 9, 128, 16)])
 def test_gaussian_scorer_group_shapes(hq, hkv, d, p):
     spec = synth.custom(hq, hkv, d, p, [1900, 333], torch.bfloat16, 1.5, n_needles=3, n_outliers=1,
@@ -57,6 +57,7 @@ def test_gaussian_scorer_group_shapes(hq, hkv, d, p):
     _copies_match(built.cache)
     for alpha, margin in ((1.5, 0.5), (2.0, 0.0)):
         check_decode(built, "gaussian", alpha, 0, margin)
+    check_decode(built, "topk", 1.5, 256, 0.0)
 
 
 def test_bf16_metadata_appended_token_by_token():
