@@ -458,12 +458,16 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_mma_kernel(DecodeArgs 
   if (n_mine <= 0) return;
   if (threadIdx.x < 64) smax[threadIdx.x >> 3][threadIdx.x & 7] = 0u;
   // the block's later pages (after the first NST stages) are looked up now,
-  // all at once, so that a refill issues its copies without a dependent load
+  // all at once, so that a refill issues its copies without a dependent load.
+  // Warps 1..7 do it: warp 0 goes straight to the first stages' lookups and
+  // copies, which would otherwise wait behind these loads (one round trip
+  // more before the block's first byte arrives).
   const int n_pre = min(kGaussMmaPre, n_mine * PPS);
-  for (int i = NST * PPS + (int)threadIdx.x; i < n_pre; i += blockDim.x) {
-    const int p = g_lo * PPS + i;
-    phys_pre[i] = p < n_pages ? phys_page(a.block_table, seq, p, a.maxp, a.nphys, a.status) : -1;
-  }
+  if (warp > 0)
+    for (int i = NST * PPS + (int)threadIdx.x - 32; i < n_pre; i += (int)blockDim.x - 32) {
+      const int p = g_lo * PPS + i;
+      phys_pre[i] = p < n_pages ? phys_page(a.block_table, seq, p, a.maxp, a.nphys, a.status) : -1;
+    }
 
   // producer (warp 0): lanes 0..2·PPS−1 copy one run each (page lane/2, array lane%2)
   auto issue_copies = [&](int st) {
