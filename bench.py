@@ -35,10 +35,10 @@ NOMINAL_HBM_GBS = 8000.0
 L2_FLUSH_BYTES = 512 << 20   # > 129 MB L2: read between timed steps
 # DRAM bytes (read + write) of one launch of the dominant kernel on this
 # workload: an ncu capture of the same kernel on a 512k-token cache of the
-# same shape (67,213,312 B read, 359,424 B written; reads 1.001 x that
+# same shape (67,208,704 B read, 497,152 B written; reads 1.001 x that
 # launch's metadata bytes) scaled by the page count to 1M; reset to None
 # whenever that kernel changes.
-NCU_TRAFFIC_PER_LAUNCH = 2 * (67213312 + 359424)
+NCU_TRAFFIC_PER_LAUNCH = 2 * (67208704 + 497152)
 
 
 def measured_peaks():
