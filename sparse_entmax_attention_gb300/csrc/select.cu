@@ -583,7 +583,6 @@ __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThre
   __shared__ int sh_scan[32];
   __shared__ uint32_t sh_prefix, sh_mask;
   __shared__ int sh_remaining, sh_eq_count, sh_eq_before;
-  __shared__ __align__(16) uint32_t bm_sh[kTopkThreads];  // the scoring blocks' largest bounds
   __shared__ uint32_t sh_tlo;
   __shared__ int cand_n, all_cnt[kTopkCluster];
   __shared__ uint2 cand_loc[kTopkCand];              // this block's (key, page) at or above T_lo

@@ -56,8 +56,11 @@ def test_gqa128k_rotated_steps(gqa128k, alpha, margin):
 @pytest.fixture(scope="module")
 def gqa1m():
     # the benchmark's cache: fp32 statistics plus the bf16 copies the
-    # Gaussian scorer streams
-    return Built(synth.workload("gqa32x8-d128-1m-p32-bf16"), meta_bf16=True)
+    # Gaussian scorer streams, with room in the table for one appended token
+    # (the last test of this module appends it)
+    spec = synth.workload("gqa32x8-d128-1m-p32-bf16")
+    spec = synth.Spec(**{**spec.__dict__, "steps": 1, "append_per_step": True})
+    return Built(spec, meta_bf16=True)
 
 
 @pytest.mark.parametrize("policy,budget,margin", [
@@ -134,3 +137,30 @@ def test_gqa1m_bulk_prefill_metadata(gqa1m):
                                        atol=1e-5, rtol=1e-4)
             assert torch.equal(c.mean_bf16[ph, j], c.mean[ph, j].to(torch.bfloat16))
             assert torch.equal(c.m2_bf16[ph, j], c.m2[ph, j].to(torch.bfloat16))
+
+
+def test_gqa1m_one_token_past_eight_tauhat_blocks(gqa1m):
+    """One appended token takes the 1M row to 32769 pages, as in the
+    benchmark's timed steps. That is one page past the 8 × 4096 that the τ̂
+    cluster holds in registers, so 7 of its 8 blocks carry pages past their
+    registers. The Gaussian decode (tensor-core scorer, τ̂, passes A and B)
+    and top-k against the oracle after the append. Runs last in the module:
+    it grows the shared cache."""
+    spec, c = gqa1m.spec, gqa1m.cache
+    b = 0
+    pos = int(c.seq_lens[b].item())
+    kk, vv = [], []
+    for j in range(spec.num_kv_heads):
+        d = gqa1m.draws[b][j]
+        k, v = synth.append_token(spec, b, j, pos, 0, d.centroids, d.out_ch, d.out_off, device="cuda")
+        kk.append(k)
+        vv.append(v)
+    K = torch.stack(kk).unsqueeze(0).unsqueeze(2).contiguous()  # [1, Hkv, 1, d]
+    V = torch.stack(vv).unsqueeze(0).unsqueeze(2).contiguous()
+    B.append(c, K, V)
+    gqa1m.K[b] = torch.cat([gqa1m.K[b], K[0]], dim=1)
+    gqa1m.V[b] = torch.cat([gqa1m.V[b], V[0]], dim=1)
+    L = int(c.seq_lens[b].item())
+    assert L == (1 << 20) + 1 and -(-L // spec.page_size) == 8 * 4096 + 1
+    check_decode(gqa1m, "gaussian", 1.5, 0, 0.5, units=[(0, 0), (0, 7)])
+    check_decode(gqa1m, "topk", 1.5, 2048, 0.0, units=[(0, 0), (0, 7)])
