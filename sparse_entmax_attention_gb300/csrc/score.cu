@@ -8,10 +8,10 @@
 //    with μ_p = q·mean_p/√d and σ_p² = Σ_d q_d²·var_{p,d}/d (diagonal model),
 //    reported on the z scale: m_p = (α−1)μ_p, ς_p = (α−1)σ_p.
 //
-// bf16 metadata (both kinds): the group's query heads against 8 pages form an
-// m16n8k16 tile (products of bf16 values are exact in the fp32 accumulator),
-// with the pages' rows streamed through a ring of shared-memory stages by
-// bulk copies (gauss_mma_kernel).
+// bf16 metadata (both kinds): 8 pages' metadata rows against the group's
+// query heads form m16n8k16 tiles (products of bf16 values are exact in the
+// fp32 accumulator), with the pages' rows streamed through a ring of
+// shared-memory stages by bulk copies (gauss_mma_kernel).
 #include "common.cuh"
 
 namespace ekv {
@@ -364,15 +364,15 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_kernel(DecodeArgs a) {
 
 // Gaussian page scores on the tensor cores, for bf16 queries with the bf16
 // metadata copies: μ = q·mean and σ² = Σ_d q_d²·m2_d are a dense contraction
-// (pages × dims × heads). One m16n8k16 tile puts the group's query heads in
-// its rows (padded to 16) and 8 pages in its columns. The products are exact
+// (pages × dims × heads) on m16n8k16 tiles of 8 pages. The products are exact
 // in fp32: q·mean is bf16 × bf16, and q² (at most 16 significant bits) is
-// split exactly into bf16 hi + lo, two MMAs into one accumulator. The
-// accumulator hands lane l the totals of head l/4 for pages 2(l%4) and
-// 2(l%4)+1, so no cross-lane reduction is left. The streaming is the one of
-// gauss_kernel: stages of 8 pages (for up to 8 KV heads) filled by bulk
-// copies on full/empty mbarriers. Page runs sit 16 bytes apart modulo 128, so
-// the 8 page rows an ldmatrix reads fall in different banks.
+// split exactly into bf16 hi + lo, two MMAs whose sums are added. The tile's
+// orientation depends on the group (the MODE comment below): up to 4 heads,
+// the pages' rows are A and the queries B; larger groups the other way
+// round. The streaming is the one of gauss_kernel: stages of 8 pages (for up
+// to 8 KV heads) filled by bulk copies on full/empty mbarriers. Page runs sit
+// 16 bytes apart modulo 128, so the 8 page rows an ldmatrix reads fall in
+// different banks.
 constexpr int kGaussMmaPPS = 8, kGaussMmaNST = 3;
 constexpr int kGaussMmaPre = 512;  // physical ids of a block's pages looked up at the start
 
