@@ -442,9 +442,9 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_mma_kernel(DecodeArgs 
   if (GAUSS)
     for (int i = threadIdx.x; i < KH * a.G; i += blockDim.x)
       a.mslot[((size_t)s * a.Hq + (size_t)kv0 * a.G + i) * a.mslots + blockIdx.x] = 0u;
-  // MODE 1: this block's largest bound Û per KV head (the top-k select's lower
-  // bound), "no page" until the block has scored its pages; lane 0 of the
-  // head's warp writes both, in order
+  // MODE 1 and 3: this block's largest bound Û per KV head (the top-k
+  // select's lower bound), "no page" until the block has scored its pages;
+  // lane 0 of the head's warp writes both, in order
   uint32_t* bslot = BOX && active ? a.mslot + ((size_t)s * a.Hkv + kvh) * a.mslots + blockIdx.x : nullptr;
   if (bslot && lane == 0) *bslot = ord_enc(-CUDART_INF_F);
   const int seq = seq_row(a.seq_ids, s, a.max_seqs, threadIdx.x == 0 ? a.status : nullptr);
@@ -577,8 +577,9 @@ __global__ void __launch_bounds__(kGaussWarps * 32) gauss_mma_kernel(DecodeArgs 
       stuck = 1;
       break;
     }
-    // three independent accumulator chains (μ, σ² hi, σ² lo; MODE 1: q⁺·kmax,
-    // q⁻·kmin), added at the end: each chain waits on its own MMAs only
+    // independent accumulator chains, added at the end, so each chain waits
+    // on its own MMAs only: MODE 0 three (μ, σ² hi, σ² lo), MODE 1 two
+    // (q⁺·kmax, q⁻·kmin); MODE 2 and 3 deal their steps as their branch says
     float mu[4] = {0.f, 0.f, 0.f, 0.f}, sg[4] = {0.f, 0.f, 0.f, 0.f}, sl[4] = {0.f, 0.f, 0.f, 0.f};
     int ph0 = -1, ph1 = -1;
     if constexpr (MODE == 1) {
