@@ -18,11 +18,11 @@ Modules:
   decode  -- one decode step per (sequence, KV head): selection, sparse
              entmax attention, τ, dropped mass δ, support recall.
 
-Parity status: the pages print no worked example and no numeric value for
-τ, τ̂, δ, recall or outputs on any input, so no function here is pinned to a
-printed number ("parity unpinned" at the paper level). Each function is
-instead pinned by closed forms, textbook special cases, brute force and the
-invariants the pages state; ``tests/test_oracle_*.py`` hold those pins.
+Pins: the pages print no worked example and no numeric value for τ, τ̂, δ,
+recall or outputs on any input, so no function here is checked against a
+printed number. Every function is pinned instead by closed forms, textbook
+special cases, brute force on small inputs and the invariants the pages
+state; ``tests/test_oracle_*.py`` hold those pins.
 """
 
 from . import entmax, pages, decode  # noqa: F401
